@@ -1,0 +1,365 @@
+"""CPU oracle of the pre-norm transformer encoder block forward (f64).
+
+TEST INFRASTRUCTURE.  Only the tests, the smoke check and the bench's CPU
+baseline leg may import this module.  It shares no code with the CUDA
+library and imports nothing from it: it is the plain definition of what the
+library computes, written out with numpy in float64 so that a reader can check
+it against the pages by eye.
+
+Sources (the three pages the method is described on):
+
+* "cortiq-engine 0.8.39 src/gpu_metal/egemma2.rs" - the EmbeddingGemma 2
+  text and vision encoders on Metal: the program builder (``Prog::rms``,
+  ``Prog::add_norm``, ``Prog::gelu``, ``Prog::qkv``, ``Prog::attention``),
+  ``att_plan`` (sliding-window key span) and ``TextGpu::forward`` (the layer
+  loop, final norm and mean-pool).
+* "cortiq-engine 0.7.6 src/gpu_metal/zimage.rs" - the Z-Image DiT on Metal:
+  the module doc (q8_row weights, "Measured"), ``Enc::block`` / ``Enc::rowop``
+  (post-norm residual + next pre-norm, q/k norm + RoPE, SwiGLU) and
+  ``bench_gemm`` / ``bench_flash`` (their f64 host checks).
+* "cera 0.2.4 src/model/vision_encoder_gpu.rs" - the LFM2-VL ViT encoder:
+  ``trait VitGpuOps`` (layernorm, gelu, attention, bias_add, add) and the block
+  loop of ``encode_image_gpu``.
+
+Storage precision (the CUDA path stores these, so the oracle rounds at the
+same points): the residual stream and the outputs of the O and down
+projections that feed a norm are f32; normed activations, the q|k|v panel,
+the attention output, the gate|up output and the FFN hidden are bf16
+(round-to-nearest-even).  Everything between two storage points is f64 here.
+
+Readings where the pages are silent (each is listed in the design doc):
+RMSNorm multiplies by the stored weight (not 1 + w) with eps inside the root;
+LayerNorm uses the biased variance; a key j is visible to query i iff both
+lie in the same sequence and (window == 0 or |i - j| <= window); q/k norm is
+applied before RoPE; RoPE is rotate-half within sections of ``sec`` channels;
+the first half of the gate|up panel is the gate; pooling divides by the
+sequence length after the final norm.
+
+Parity pins: every function here is pinned in tests/test_oracle.py against
+something other than itself (brute-force loops, closed forms, invariants or
+a library routine).  The whole block has no worked example on the pages;
+its parity rests on the pinned parts plus block-level invariants.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# storage rounding
+
+
+def round_bf16(a):
+    """Round to the nearest bfloat16 value, ties to even; returned as f64.
+
+    bfloat16 keeps 8 significant bits and float32's exponent range, so the
+    quantum of a value with binary exponent e (a = m*2^e, 0.5 <= |m| < 1) is
+    2^(e-8); below the smallest normal (2^-126) the quantum stays 2^-133.
+    A result that reaches 2^128 is past the largest finite value: infinity.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)
+    e = np.maximum(e, -125)
+    quantum = np.ldexp(1.0, e - 8)
+    out = np.rint(a / quantum) * quantum
+    return np.where(np.abs(out) >= 2.0 ** 128, np.copysign(np.inf, a), out)
+
+
+def round_f32(a):
+    """Round to the nearest float32 (ties to even); returned as f64."""
+    return np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def widen_int8(q):
+    """int8 -> real value; every int8 is exact in bf16, f32 and f64
+    (zimage.rs module doc: the int8 tile is staged as half "exact")."""
+    return np.asarray(q, dtype=np.int8).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# q8_row linear
+
+
+def q8_linear(x, q, s, b=None, residual=None):
+    """y[t, o] = s[o] * sum_k x[t, k] * q[o, k]  (+ b[o])  (+ residual[t, o]).
+
+    q8_row weights: int8 [n, k] row-major and one scale per output row,
+    dequantised as W[o, k] = s[o] * q[o, k] (zimage.rs module doc; the f64
+    form of ``bench_gemm``'s host check).  The bias follows the ViT's biased
+    linears (``bias_add`` of ``VitGpuOps``), the residual the plain pre-norm
+    block's ``x += proj`` (``encode_image_gpu``).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    y = (x @ widen_int8(q).T) * np.asarray(s, dtype=np.float64)[None, :]
+    if b is not None:
+        y = y + np.asarray(b, dtype=np.float64)[None, :]
+    if residual is not None:
+        y = y + np.asarray(residual, dtype=np.float64)
+    return y
+
+
+# ---------------------------------------------------------------------------
+# norms
+
+
+def rms_norm(x, w, eps, pre=1.0):
+    """y = rms(pre*x) * w with rms(v) = v / sqrt(mean(v^2) + eps)
+    (egemma2.rs ``Prog::rms``; the weight multiplies as stored)."""
+    v = pre * np.asarray(x, dtype=np.float64)
+    inv = 1.0 / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + eps)
+    return v * inv * np.asarray(w, dtype=np.float64)
+
+
+def layer_norm(x, w, b, eps):
+    """(x - mean) * inv_std * w + b per row, biased variance
+    (vision_encoder_gpu.rs ``VitGpuOps::layernorm``)."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = np.mean(x, axis=-1, keepdims=True)
+    var = np.mean((x - mu) ** 2, axis=-1, keepdims=True)
+    y = (x - mu) / np.sqrt(var + eps) * np.asarray(w, dtype=np.float64)
+    if b is not None:
+        y = y + np.asarray(b, dtype=np.float64)
+    return y
+
+
+def norm(kind, x, w, b, eps):
+    if kind == "rms":
+        return rms_norm(x, w, eps)
+    if kind == "ln":
+        return layer_norm(x, w, b, eps)
+    raise ValueError(kind)
+
+
+def add_norm_sandwich(h, t, w_post, post, eps):
+    """H = (H + rms(T) * w_post) * post  (egemma2.rs ``Prog::add_norm``;
+    zimage.rs ``Enc::rowop`` post-norm mode)."""
+    return (np.asarray(h, dtype=np.float64) + rms_norm(t, w_post, eps)) * post
+
+
+# ---------------------------------------------------------------------------
+# q/k norm + RoPE
+
+
+def rope(x, cos, sin, sec):
+    """Rotate-half RoPE within each section of ``sec`` channels.
+
+    x: [rows, hd]; cos/sin: [rows, hd/2] (each row's angles).  For section s
+    and i < sec/2 the pair (x[s*sec+i], x[s*sec+i+sec/2]) rotates by the angle
+    at table column s*sec/2 + i (egemma2.rs ``EgQkv.sec``: 1-D uses sec = hd,
+    the vision tower's 2-D form sec = hd/2, "the column half, then the row
+    half").
+    """
+    x = np.asarray(x, dtype=np.float64)
+    cos = np.asarray(cos, dtype=np.float64)
+    sin = np.asarray(sin, dtype=np.float64)
+    hd = x.shape[-1]
+    half = sec // 2
+    out = np.empty_like(x)
+    for sct in range(hd // sec):
+        x1 = x[:, sct * sec: sct * sec + half]
+        x2 = x[:, sct * sec + half: (sct + 1) * sec]
+        c = cos[:, sct * half: (sct + 1) * half]
+        s = sin[:, sct * half: (sct + 1) * half]
+        out[:, sct * sec: sct * sec + half] = x1 * c - x2 * s
+        out[:, sct * sec + half: (sct + 1) * sec] = x2 * c + x1 * s
+    return out
+
+
+def qk_prep(qkv, nq, nkv, hd, q_off, k_off, qn, kn, eps, cos, sin, pos, sec, q_mul):
+    """q/k RMSNorm per head with [hd] weights, then RoPE, then q * q_mul;
+    the panel is returned rounded to bf16 (egemma2.rs ``Prog::qkv``;
+    zimage.rs ``Enc::block`` "qk-norm + RoPE in place", q pre-multiplied).
+
+    ``pos`` selects each row's table row (None = the row index).
+    """
+    out = np.array(qkv, dtype=np.float64, copy=True)
+    rows = out.shape[0]
+    if sec:
+        idx = np.arange(rows) if pos is None else np.asarray(pos, dtype=np.int64)
+        c_rows = np.asarray(cos, dtype=np.float64)[idx]
+        s_rows = np.asarray(sin, dtype=np.float64)[idx]
+    for off, nh, w, mul in ((q_off, nq, qn, q_mul), (k_off, nkv, kn, 1.0)):
+        for h in range(nh):
+            sl = slice(off + h * hd, off + (h + 1) * hd)
+            v = out[:, sl]
+            if w is not None:
+                v = rms_norm(v, w, eps)
+            if sec:
+                v = rope(v, c_rows, s_rows, sec)
+            out[:, sl] = v * mul
+    return round_bf16(out)
+
+
+# ---------------------------------------------------------------------------
+# attention
+
+
+def visible_mask(n, window):
+    """Key j visible to query i of one sequence iff window == 0 or
+    |i - j| <= window (egemma2.rs ``att_plan``: keys of a query block span
+    [q0 - W, q_last + W], W = 0 meaning the whole sequence)."""
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    if window == 0:
+        return np.ones((n, n), dtype=bool)
+    return np.abs(i - j) <= window
+
+
+def softmax_probs(q, k, scale, visible):
+    """p[i, j] = exp(scale*q_i.k_j - max_j) / sum_j, invisible keys exactly 0."""
+    s = scale * (np.asarray(q, dtype=np.float64) @ np.asarray(k, dtype=np.float64).T)
+    s = np.where(visible, s, -np.inf)
+    s = s - np.max(s, axis=1, keepdims=True)
+    p = np.where(visible, np.exp(s), 0.0)
+    return p / np.sum(p, axis=1, keepdims=True)
+
+
+def attention_varlen(qkv, cu, nq, nkv, hd, q_off, k_off, v_off, window, scale,
+                     rows=None):
+    """Bidirectional multi-head attention over a packed batch.
+
+    o[i, h] = sum_j softmax_j(scale * q[i,h] . k[j,kvh]) v[j,kvh] over the
+    visible keys j of i's own sequence, kvh = h // (nq/nkv) (egemma2.rs
+    ``Prog::attention`` / ``att_plan``; vision_encoder_gpu.rs
+    ``VitGpuOps::attention``).  Returns f64 [T, nq*hd]; with ``rows`` only
+    those query rows are computed (the others stay NaN).
+    """
+    qkv = np.asarray(qkv, dtype=np.float64)
+    cu = np.asarray(cu, dtype=np.int64)
+    T = qkv.shape[0]
+    out = np.full((T, nq * hd), np.nan)
+    group = nq // nkv
+    want = None if rows is None else np.zeros(T, dtype=bool)
+    if want is not None:
+        want[np.asarray(rows)] = True
+    for sidx in range(len(cu) - 1):
+        r0, r1 = int(cu[sidx]), int(cu[sidx + 1])
+        n = r1 - r0
+        if n == 0:
+            continue
+        vis = visible_mask(n, window)
+        qi = np.arange(n) if want is None else np.nonzero(want[r0:r1])[0]
+        if len(qi) == 0:
+            continue
+        for h in range(nq):
+            kvh = h // group
+            Q = qkv[r0 + qi, q_off + h * hd: q_off + (h + 1) * hd]
+            K = qkv[r0:r1, k_off + kvh * hd: k_off + (kvh + 1) * hd]
+            V = qkv[r0:r1, v_off + kvh * hd: v_off + (kvh + 1) * hd]
+            P = softmax_probs(Q, K, scale, vis[qi])
+            out[r0 + qi, h * hd:(h + 1) * hd] = P @ V
+    return out
+
+
+# ---------------------------------------------------------------------------
+# gating
+
+
+def gelu_tanh(g):
+    """0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) (egemma2.rs
+    ``Prog::gelu``; vision_encoder_gpu.rs ``VitGpuOps::gelu``)."""
+    g = np.asarray(g, dtype=np.float64)
+    return 0.5 * g * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (g + 0.044715 * g ** 3)))
+
+
+def silu(g):
+    """g / (1 + e^-g) (zimage.rs SwiGLU: h = silu(w1 x) * (w3 x))."""
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g))
+
+
+def gate_act(gu, f, gated, act):
+    """m = act(g) * u with g = gu[:, :f], u = gu[:, f:2f]; ungated m = act(gu)."""
+    gu = np.asarray(gu, dtype=np.float64)
+    fn = gelu_tanh if act == "gelu_tanh" else silu
+    if gated:
+        return fn(gu[:, :f]) * gu[:, f:2 * f]
+    return fn(gu[:, :f])
+
+
+# ---------------------------------------------------------------------------
+# pooling
+
+
+def pool_mean(x, cu, w, eps):
+    """out[s] = (1/len_s) sum_{r in s} rms(x_r) * w  (egemma2.rs
+    ``TextGpu::forward``: ``row_inv`` then ``pool``; None = no final norm)."""
+    x = np.asarray(x, dtype=np.float64)
+    cu = np.asarray(cu, dtype=np.int64)
+    out = np.zeros((len(cu) - 1, x.shape[1]))
+    for sidx in range(len(cu) - 1):
+        seg = x[cu[sidx]:cu[sidx + 1]]
+        if w is not None:
+            seg = rms_norm(seg, w, eps)
+        out[sidx] = seg.mean(axis=0)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the block
+
+
+def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None):
+    """One encoder block, step by step; returns every stored intermediate.
+
+    cfg: a BlockConfig-like object (d, heads, kv_heads, hd, ffn, gated, act,
+    norm, form, qk_norm, eps, post, scale, window_of(layer)); p: the layer's
+    weights; x: f32 residual stream [T, d]; a: this block's normed input
+    (bf16 values); tables: RoPE inputs; next_norm: (w, b) of the next block's
+    pre-norm or None.
+
+    Plain form (vision_encoder_gpu.rs ``encode_image_gpu``):
+        x += o Wo^T (+b);  a = Norm2(x);  x += act-FFN(a);  a = Norm1'(x)
+    Sandwich form (egemma2.rs ``TextGpu::forward``; zimage.rs ``Enc::block``):
+        x = (x + rms(o Wo^T) w_pa) post;  a = rms(x) w_2;
+        x = (x + rms(FFN(a)) w_pf) post;  a = rms(x) w_next
+    ``rows`` restricts attention to sampled query rows (the output rows that
+    depend on them are then only valid on those rows).
+    """
+    hd, H, KV, d, F = cfg.hd, cfg.heads, cfg.kv_heads, cfg.d, cfg.ffn
+    eps = cfg.eps
+    r = {}
+    x = round_f32(x)
+    a = round_bf16(a)
+    qw, kw = H * hd, KV * hd
+    qkv = np.concatenate([
+        q8_linear(a, p["wq"]["q"], p["wq"]["s"], p["wq"]["b"]),
+        q8_linear(a, p["wk"]["q"], p["wk"]["s"], p["wk"]["b"]),
+        q8_linear(a, p["wv"]["q"], p["wv"]["s"], p["wv"]["b"]),
+    ], axis=1)
+    r["qkv_raw"] = qkv = round_bf16(qkv)
+    if cfg.qk_norm or tables["sec"]:
+        qkv = qk_prep(qkv, H, KV, hd, 0, qw,
+                      p["q_norm"] if cfg.qk_norm else None,
+                      p["k_norm"] if cfg.qk_norm else None,
+                      eps, tables["cos"], tables["sin"], tables["pos"], tables["sec"], 1.0)
+    r["qkv"] = qkv
+    o = attention_varlen(qkv, cu, H, KV, hd, 0, qw, qw + kw, cfg.window_of(layer),
+                         cfg.scale, rows=rows)
+    r["o"] = o = round_bf16(o)
+    if cfg.form == "plain":
+        x = round_f32(q8_linear(o, p["wo"]["q"], p["wo"]["s"], p["wo"]["b"], residual=x))
+    else:
+        t = round_f32(q8_linear(o, p["wo"]["q"], p["wo"]["s"], p["wo"]["b"]))
+        r["t"] = t
+        x = round_f32(add_norm_sandwich(x, t, p["post_attn_w"], cfg.post, eps))
+    r["x_mid"] = x
+    r["a_mid"] = a2 = round_bf16(norm(cfg.norm, x, p["norm2_w"], p["norm2_b"], eps))
+    parts = [q8_linear(a2, p["wg"]["q"], p["wg"]["s"], p["wg"]["b"])]
+    if cfg.gated:
+        parts.append(q8_linear(a2, p["wu"]["q"], p["wu"]["s"], p["wu"]["b"]))
+    r["gu"] = gu = round_bf16(np.concatenate(parts, axis=1))
+    r["m"] = m = round_bf16(gate_act(gu, F, cfg.gated, cfg.act))
+    if cfg.form == "plain":
+        x = round_f32(q8_linear(m, p["wd"]["q"], p["wd"]["s"], p["wd"]["b"], residual=x))
+    else:
+        f = round_f32(q8_linear(m, p["wd"]["q"], p["wd"]["s"], p["wd"]["b"]))
+        r["f"] = f
+        x = round_f32(add_norm_sandwich(x, f, p["post_ffn_w"], cfg.post, eps))
+    r["x_out"] = x
+    if next_norm is not None:
+        r["a_out"] = round_bf16(norm(cfg.norm, x, next_norm[0], next_norm[1], eps))
+    else:
+        r["a_out"] = None
+    return r

@@ -1,0 +1,501 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks one oracle function against brute force on tiny inputs, a
+closed form, an invariant the pages' definitions imply, or a library routine
+that computes the same textbook quantity, chosen so that a plausible slip in
+the oracle (a dropped term, a wrong sign or index, a transposed operand)
+fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import encoder as O
+from transformer_encoder_forward_gb300 import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------- rounding
+
+def test_round_bf16_matches_torch_rne_on_f32_inputs():
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(3.0),
+        (rng.standard_normal(2000) * 1e-38).astype(np.float32),       # subnormal range
+        np.array([0.0, -0.0, 1.0, -1.0, 1.00390625, 1.01171875, 3.4e38, 1e-45],
+                 dtype=np.float32),
+    ])
+    # exact ties: f32 values halfway between two bf16 values
+    ties = (np.arange(1, 200, dtype=np.uint32) << 16 | 0x8000).view(np.float32) \
+        .astype(np.float32)
+    ties = np.concatenate([ties, (np.arange(0x3F80, 0x3FA0, dtype=np.uint32) << 16 | 0x8000)
+                           .view(np.float32)])
+    vals = np.concatenate([vals, ties])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_bf16(vals.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_round_f32_is_float32_cast():
+    v = np.array([1.0 + 2.0 ** -30, math.pi, -1e-40])
+    np.testing.assert_array_equal(O.round_f32(v), v.astype(np.float32).astype(np.float64))
+
+
+def test_int8_widening_is_exact_for_all_values():
+    q = np.arange(-128, 128, dtype=np.int8)
+    w = O.widen_int8(q)
+    np.testing.assert_array_equal(w, np.arange(-128, 128, dtype=np.float64))
+    # every int8 is a bf16 value: rounding changes nothing
+    np.testing.assert_array_equal(O.round_bf16(w), w)
+    ref = torch.from_numpy(q).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(w, ref)
+
+
+# ---------------------------------------------------------------- q8 linear
+
+def _q8_brute(x, q, s, b, r):
+    t, k = x.shape
+    n = q.shape[0]
+    y = [[0.0] * n for _ in range(t)]
+    for i in range(t):
+        for o in range(n):
+            acc = 0.0
+            for kk in range(k):
+                acc += float(x[i, kk]) * int(q[o, kk])
+            v = float(s[o]) * acc
+            if b is not None:
+                v += float(b[o])
+            if r is not None:
+                v += float(r[i, o])
+            y[i][o] = v
+    return np.array(y)
+
+
+def test_q8_linear_brute_force_tiny():
+    rng = np.random.default_rng(2)
+    x = O.round_bf16(rng.standard_normal((5, 24)))
+    q = rng.integers(-127, 128, (7, 24), dtype=np.int8)
+    s = rng.uniform(0.01, 0.02, 7).astype(np.float32)
+    b = rng.standard_normal(7).astype(np.float32)
+    r = rng.standard_normal((5, 7)).astype(np.float32)
+    for bb, rr in ((None, None), (b, None), (b, r), (None, r)):
+        np.testing.assert_allclose(O.q8_linear(x, q, s, bb, rr), _q8_brute(x, q, s, bb, rr),
+                                   rtol=1e-13, atol=1e-13)
+
+
+def test_q8_linear_exact_integer_case():
+    # integer activations |x| <= 16, unit scale, K <= 1024: every partial sum
+    # is an integer below 2^24, so the result is exact in f32 as well.
+    rng = np.random.default_rng(3)
+    k = 1024
+    x = rng.integers(-16, 17, (9, k)).astype(np.float64)
+    q = rng.integers(-127, 128, (11, k), dtype=np.int8)
+    y = O.q8_linear(x, q, np.ones(11, np.float32))
+    exact = x.astype(np.int64) @ q.astype(np.int64).T
+    np.testing.assert_array_equal(y, exact.astype(np.float64))
+    assert np.all(np.abs(exact) < 2 ** 24)
+
+
+def test_q8_linear_row_scale_is_per_output_row():
+    # a transposed scale (per input column) would break this
+    q = np.eye(4, dtype=np.int8)
+    s = np.array([1.0, 2.0, 3.0, 4.0], dtype=np.float32)
+    x = np.array([[1.0, 1.0, 1.0, 1.0]])
+    np.testing.assert_array_equal(O.q8_linear(x, q, s), [[1.0, 2.0, 3.0, 4.0]])
+    x = np.array([[1.0, 0.0, 0.0, 0.0]])
+    q2 = np.array([[0, 0, 0, 0], [5, 0, 0, 0], [0, 0, 0, 0], [0, 0, 0, 0]], dtype=np.int8)
+    np.testing.assert_array_equal(O.q8_linear(x, q2, s), [[0.0, 10.0, 0.0, 0.0]])
+
+
+# ---------------------------------------------------------------- norms
+
+def test_rms_norm_constant_row_closed_form():
+    for c in (0.5, -3.0, 1e-4):
+        w = np.linspace(0.5, 1.5, 16)
+        y = O.rms_norm(np.full((1, 16), c), w, 1e-6)
+        np.testing.assert_allclose(y[0], c / math.sqrt(c * c + 1e-6) * w, rtol=1e-14)
+
+
+def test_rms_norm_unit_rms_without_eps_and_pre_scale():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((6, 40)) * 5
+    y = O.rms_norm(x, np.ones(40), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, rtol=1e-13)
+    # scale invariance: rms(c x) = rms(x) when eps = 0, and pre multiplies before
+    np.testing.assert_allclose(O.rms_norm(3 * x, np.ones(40), 0.0), y, rtol=1e-13)
+    np.testing.assert_allclose(O.rms_norm(x, np.ones(40), 1e-3, pre=2.0),
+                               O.rms_norm(2 * x, np.ones(40), 1e-3), rtol=1e-14)
+    # eps enters under the root: rms of a zero row is zero, not NaN
+    assert np.all(O.rms_norm(np.zeros((1, 8)), np.ones(8), 1e-6) == 0)
+
+
+def test_layer_norm_against_torch_and_constant_row():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((7, 48)) * 2 + 1
+    w = rng.standard_normal(48)
+    b = rng.standard_normal(48)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (48,), torch.from_numpy(w),
+                                         torch.from_numpy(b), 1e-5).numpy()
+    np.testing.assert_allclose(O.layer_norm(x, w, b, 1e-5), ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(O.layer_norm(np.full((1, 48), 7.0), w, b, 1e-5)[0], b,
+                               atol=1e-12)
+    y = O.layer_norm(x, np.ones(48), None, 0.0)
+    np.testing.assert_allclose(y.mean(axis=1), 0, atol=1e-13)
+    np.testing.assert_allclose(y.var(axis=1), 1, rtol=1e-12)
+
+
+def test_add_norm_sandwich_closed_form():
+    h = np.array([[1.0, 2.0, 3.0, 4.0]])
+    t = np.full((1, 4), 2.0)
+    w = np.array([1.0, 0.5, 2.0, 1.0])
+    out = O.add_norm_sandwich(h, t, w, 0.5, 0.0)
+    np.testing.assert_allclose(out, (h + w) * 0.5, rtol=1e-15)
+
+
+# ---------------------------------------------------------------- RoPE / qk prep
+
+def _rope_complex(x, ang, sec):
+    # independent formulation: pair (x1, x2) as x1 + i x2 times e^{i angle}
+    hd = x.shape[1]
+    half = sec // 2
+    out = np.empty_like(x)
+    for s in range(hd // sec):
+        z = x[:, s * sec: s * sec + half] + 1j * x[:, s * sec + half:(s + 1) * sec]
+        z = z * np.exp(1j * ang[:, s * half:(s + 1) * half])
+        out[:, s * sec: s * sec + half] = z.real
+        out[:, s * sec + half:(s + 1) * sec] = z.imag
+    return out
+
+
+@pytest.mark.parametrize("sec", [16, 8])
+def test_rope_matches_complex_rotation_and_preserves_pair_norms(sec):
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((9, 16))
+    ang = rng.uniform(-4, 4, (9, 8))
+    y = O.rope(x, np.cos(ang), np.sin(ang), sec)
+    np.testing.assert_allclose(y, _rope_complex(x, ang, sec), rtol=1e-13, atol=1e-13)
+    half = sec // 2
+    for s in range(16 // sec):
+        a, b = slice(s * sec, s * sec + half), slice(s * sec + half, (s + 1) * sec)
+        np.testing.assert_allclose(x[:, a] ** 2 + x[:, b] ** 2, y[:, a] ** 2 + y[:, b] ** 2,
+                                   rtol=1e-12)
+    # angle 0 is the identity
+    np.testing.assert_allclose(O.rope(x, np.ones((9, 8)), np.zeros((9, 8)), sec), x)
+
+
+def test_rope_1d_tables_give_relative_positions():
+    cfg = synth.small_config("c2", hd=16)
+    lens = [40]
+    tb = synth.rope_tables(cfg, lens)
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal(16)
+    k = rng.standard_normal(16)
+    def at(v, p):
+        return O.rope(v[None, :], tb["cos"][p:p + 1], tb["sin"][p:p + 1], 16)[0]
+    d1 = at(q, 10) @ at(k, 3)
+    d2 = at(q, 27) @ at(k, 20)
+    assert abs(d1 - d2) < 1e-5 * (abs(d1) + 1)
+
+
+def test_qk_prep_heads_and_q_mul():
+    rng = np.random.default_rng(8)
+    hd, nq, nkv = 8, 2, 1
+    qkv = O.round_bf16(rng.standard_normal((3, (nq + 2 * nkv) * hd)))
+    # no norm, no RoPE, q_mul = 1: the identity on bf16 values
+    same = O.qk_prep(qkv, nq, nkv, hd, 0, nq * hd, None, None, 1e-6, None, None, None, 0, 1.0)
+    np.testing.assert_array_equal(same, qkv)
+    # q_mul touches q only (v, at the tail, never changes)
+    two = O.qk_prep(qkv, nq, nkv, hd, 0, nq * hd, None, None, 1e-6, None, None, None, 0, 2.0)
+    np.testing.assert_array_equal(two[:, :nq * hd], 2 * qkv[:, :nq * hd])
+    np.testing.assert_array_equal(two[:, nq * hd:], qkv[:, nq * hd:])
+    # norm acts per head: each q head, rescaled alone, has unit RMS
+    qn = np.ones(hd)
+    nrm = O.qk_prep(qkv, nq, nkv, hd, 0, nq * hd, qn, qn, 0.0, None, None, None, 0, 1.0)
+    for h in range(nq + nkv):
+        blk = nrm[:, h * hd:(h + 1) * hd]
+        np.testing.assert_allclose(np.sqrt(np.mean(blk ** 2, axis=1)), 1.0, rtol=1e-2)
+
+
+# ---------------------------------------------------------------- attention
+
+def _attn_brute(q, k, v, scale, vis):
+    n, hd = q.shape
+    out = np.zeros_like(q)
+    for i in range(n):
+        sc = [scale * sum(q[i, c] * k[j, c] for c in range(hd)) if vis[i, j] else None
+              for j in range(k.shape[0])]
+        mx = max(s for s in sc if s is not None)
+        w = [math.exp(s - mx) if s is not None else 0.0 for s in sc]
+        tot = sum(w)
+        for c in range(hd):
+            out[i, c] = sum(w[j] * v[j, c] for j in range(k.shape[0])) / tot
+    return out
+
+
+def _panel(rng, T, nq, nkv, hd):
+    return O.round_bf16(rng.standard_normal((T, (nq + 2 * nkv) * hd)))
+
+
+def test_attention_brute_force_with_window_and_two_sequences():
+    rng = np.random.default_rng(9)
+    hd, nq = 4, 2
+    cu = np.array([0, 7, 12])
+    qkv = _panel(rng, 12, nq, nq, hd)
+    for window in (0, 2):
+        o = O.attention_varlen(qkv, cu, nq, nq, hd, 0, nq * hd, 2 * nq * hd, window, 0.7)
+        for s in range(2):
+            r0, r1 = cu[s], cu[s + 1]
+            n = r1 - r0
+            vis = np.array([[window == 0 or abs(i - j) <= window for j in range(n)]
+                            for i in range(n)])
+            for h in range(nq):
+                ref = _attn_brute(qkv[r0:r1, h * hd:(h + 1) * hd],
+                                  qkv[r0:r1, nq * hd + h * hd: nq * hd + (h + 1) * hd],
+                                  qkv[r0:r1, 2 * nq * hd + h * hd: 2 * nq * hd + (h + 1) * hd],
+                                  0.7, vis)
+                np.testing.assert_allclose(o[r0:r1, h * hd:(h + 1) * hd], ref, rtol=1e-12,
+                                           atol=1e-12)
+
+
+def test_attention_matches_torch_sdpa_with_mask():
+    rng = np.random.default_rng(10)
+    n, hd = 33, 16
+    q, k, v = (rng.standard_normal((n, hd)) for _ in range(3))
+    vis = O.visible_mask(n, 5)
+    p = O.softmax_probs(q, k, 0.25, vis)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(k)[None], torch.from_numpy(v)[None],
+        attn_mask=torch.from_numpy(vis)[None], scale=0.25)[0].numpy()
+    np.testing.assert_allclose(p @ v, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_softmax_rows_sum_to_one_and_masked_weights_are_zero():
+    rng = np.random.default_rng(11)
+    q, k = rng.standard_normal((20, 8)) * 4, rng.standard_normal((20, 8)) * 4
+    vis = O.visible_mask(20, 3)
+    p = O.softmax_probs(q, k, 1.0, vis)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=1e-14)
+    assert np.all(p[~vis] == 0.0)
+    assert np.all(p[vis] > 0.0)
+
+
+def test_identical_keys_give_mean_of_visible_values():
+    rng = np.random.default_rng(12)
+    hd, n, W = 8, 17, 4
+    qkv = np.zeros((n, 3 * hd))
+    qkv[:, :hd] = rng.standard_normal((n, hd))
+    qkv[:, hd:2 * hd] = rng.standard_normal(hd)          # every key identical
+    qkv[:, 2 * hd:] = rng.standard_normal((n, hd))
+    o = O.attention_varlen(qkv, [0, n], 1, 1, hd, 0, hd, 2 * hd, W, 1.0)
+    for i in range(n):
+        lo, hi = max(0, i - W), min(n, i + W + 1)
+        np.testing.assert_allclose(o[i], qkv[lo:hi, 2 * hd:].mean(axis=0), rtol=1e-12)
+
+
+def test_length_one_sequence_returns_v_and_sequences_are_independent():
+    rng = np.random.default_rng(13)
+    hd = 8
+    qkv = rng.standard_normal((10, 3 * hd))
+    cu = [0, 1, 6, 10]
+    o = O.attention_varlen(qkv, cu, 1, 1, hd, 0, hd, 2 * hd, 0, 1.0)
+    np.testing.assert_allclose(o[0], qkv[0, 2 * hd:])
+    qkv2 = qkv.copy()
+    qkv2[6:] = rng.standard_normal((4, 3 * hd))          # change the last sequence
+    o2 = O.attention_varlen(qkv2, cu, 1, 1, hd, 0, hd, 2 * hd, 0, 1.0)
+    np.testing.assert_array_equal(o[:6], o2[:6])
+
+
+def test_out_of_window_keys_have_no_effect_and_wide_window_is_full():
+    rng = np.random.default_rng(14)
+    hd, n, W = 8, 30, 5
+    qkv = rng.standard_normal((n, 3 * hd))
+    o = O.attention_varlen(qkv, [0, n], 1, 1, hd, 0, hd, 2 * hd, W, 0.5)
+    # perturb every key/value farther than W from row 0: row 0 is unchanged
+    qkv2 = qkv.copy()
+    qkv2[W + 1:, hd:] = rng.standard_normal((n - W - 1, 2 * hd)) * 100
+    o2 = O.attention_varlen(qkv2, [0, n], 1, 1, hd, 0, hd, 2 * hd, W, 0.5)
+    np.testing.assert_array_equal(o[0], o2[0])
+    full = O.attention_varlen(qkv, [0, n], 1, 1, hd, 0, hd, 2 * hd, 0, 0.5)
+    wide = O.attention_varlen(qkv, [0, n], 1, 1, hd, 0, hd, 2 * hd, n - 1, 0.5)
+    np.testing.assert_array_equal(full, wide)
+
+
+def test_gqa_head_grouping():
+    rng = np.random.default_rng(15)
+    hd, nq, nkv, n = 4, 4, 2, 6
+    qkv = rng.standard_normal((n, (nq + 2 * nkv) * hd))
+    o = O.attention_varlen(qkv, [0, n], nq, nkv, hd, 0, nq * hd, (nq + nkv) * hd, 0, 1.0)
+    # q head 3 uses kv head 1
+    q = qkv[:, 3 * hd:4 * hd]
+    k = qkv[:, nq * hd + hd: nq * hd + 2 * hd]
+    v = qkv[:, (nq + nkv) * hd + hd:(nq + nkv) * hd + 2 * hd]
+    ref = _attn_brute(q, k, v, 1.0, np.ones((n, n), bool))
+    np.testing.assert_allclose(o[:, 3 * hd:], ref, rtol=1e-12)
+
+
+# ---------------------------------------------------------------- gating
+
+def test_gelu_tanh_and_silu_against_torch_and_symmetries():
+    x = np.linspace(-8, 8, 1001)
+    tx = torch.from_numpy(x)
+    np.testing.assert_allclose(O.gelu_tanh(x),
+                               torch.nn.functional.gelu(tx, approximate="tanh").numpy(),
+                               rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(O.silu(x), torch.nn.functional.silu(tx).numpy(),
+                               rtol=1e-14, atol=1e-15)
+    assert O.gelu_tanh(0.0) == 0.0 and O.silu(0.0) == 0.0
+    np.testing.assert_allclose(O.gelu_tanh(x) - O.gelu_tanh(-x), x, atol=1e-14)
+    np.testing.assert_allclose(O.silu(x) - O.silu(-x), x, atol=1e-14)
+    # closed form at 1: 0.5 (1 + tanh(sqrt(2/pi) * 1.044715))
+    assert abs(O.gelu_tanh(1.0) - 0.5 * (1 + math.tanh(math.sqrt(2 / math.pi) * 1.044715))) < 1e-16
+
+
+def test_gate_act_takes_gate_first():
+    gu = np.array([[1.0, -2.0, 3.0, 4.0]])      # f = 2: g = [1, -2], u = [3, 4]
+    m = O.gate_act(gu, 2, True, "silu")
+    np.testing.assert_allclose(m, [[O.silu(1.0) * 3.0, O.silu(-2.0) * 4.0]])
+    np.testing.assert_allclose(O.gate_act(gu, 2, False, "gelu_tanh"),
+                               [[O.gelu_tanh(1.0), O.gelu_tanh(-2.0)]])
+
+
+# ---------------------------------------------------------------- pooling
+
+def test_pool_mean_identical_rows_and_plain_mean():
+    rng = np.random.default_rng(16)
+    row = rng.standard_normal(12)
+    x = np.vstack([np.tile(row, (5, 1)), rng.standard_normal((3, 12))])
+    w = rng.uniform(0.5, 1.5, 12)
+    out = O.pool_mean(x, [0, 5, 8], w, 1e-6)
+    np.testing.assert_allclose(out[0], O.rms_norm(row[None], w, 1e-6)[0], rtol=1e-13)
+    plain = O.pool_mean(x, [0, 5, 8], None, 1e-6)
+    np.testing.assert_allclose(plain[1], x[5:8].sum(axis=0) / 3, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- the block
+
+def _tiny(form, norm, gated, act, rope, qk_norm, window=0, bias=False):
+    return synth.BlockConfig("tiny", 1, 32, 2, 2, 16, 48, gated, act, norm, form, qk_norm,
+                             rope, window, "all", bias, False, (9, 14))
+
+
+def _torch_block(cfg, p, x, cu, tables, next_norm):
+    """The same block written with torch's own library ops (linear, layer_norm,
+    scaled_dot_product_attention, gelu/silu, complex rotation for RoPE)."""
+    t = lambda a: torch.as_tensor(np.asarray(a, np.float64))
+    bf = lambda v: v.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    f32 = lambda v: v.to(torch.float32).to(torch.float64)
+    F = torch.nn.functional
+
+    def lin(v, w):
+        out = F.linear(v, t(w["q"].astype(np.float64)) * t(w["s"])[:, None])
+        return out + t(w["b"]) if w["b"] is not None else out
+
+    def nrm(v, w, b):
+        if cfg.norm == "ln":
+            return F.layer_norm(v, (v.shape[-1],), t(w), None if b is None else t(b), cfg.eps)
+        return F.rms_norm(v, (v.shape[-1],), t(w), cfg.eps)
+
+    x = f32(t(x))
+    a = bf(nrm(x, p["norm1_w"], p["norm1_b"]))
+    H, hd = cfg.heads, cfg.hd
+    qkv = bf(torch.cat([lin(a, p["wq"]), lin(a, p["wk"]), lin(a, p["wv"])], 1))
+    q, k, v = qkv[:, :H * hd], qkv[:, H * hd:2 * H * hd], qkv[:, 2 * H * hd:]
+    def prep(u, w):
+        u = u.reshape(-1, H, hd)
+        if cfg.qk_norm:
+            u = F.rms_norm(u, (hd,), t(w), cfg.eps)
+        if tables["sec"]:
+            ang = torch.atan2(t(tables["sin"]), t(tables["cos"]))[t(tables["pos"]).long()]
+            sec = tables["sec"]
+            half = sec // 2
+            parts = []
+            for s in range(hd // sec):
+                z = torch.complex(u[..., s * sec:s * sec + half], u[..., s * sec + half:(s + 1) * sec])
+                z = z * torch.polar(torch.ones_like(ang[:, None, s * half:(s + 1) * half]),
+                                    ang[:, None, s * half:(s + 1) * half])
+                parts.append((z.real, z.imag))
+            u = torch.cat([c for pr in parts for c in pr], -1)
+        return u.reshape(-1, H * hd)
+    if cfg.qk_norm or tables["sec"]:
+        q, k = bf(prep(q, p.get("q_norm"))), bf(prep(k, p.get("k_norm")))
+    o = torch.zeros_like(q)
+    for s in range(len(cu) - 1):
+        r0, r1 = int(cu[s]), int(cu[s + 1])
+        n = r1 - r0
+        ii = torch.arange(n)
+        mask = torch.ones(n, n, dtype=torch.bool) if cfg.window == 0 else \
+            (ii[:, None] - ii[None, :]).abs() <= cfg.window
+        qs = q[r0:r1].reshape(n, H, hd).transpose(0, 1)
+        ks = k[r0:r1].reshape(n, H, hd).transpose(0, 1)
+        vs = v[r0:r1].reshape(n, H, hd).transpose(0, 1)
+        os_ = F.scaled_dot_product_attention(qs, ks, vs, attn_mask=mask, scale=cfg.scale)
+        o[r0:r1] = os_.transpose(0, 1).reshape(n, H * hd)
+    o = bf(o)
+    if cfg.form == "plain":
+        x = f32(x + lin(o, p["wo"]))
+    else:
+        x = f32(x + F.rms_norm(f32(lin(o, p["wo"])), (cfg.d,), t(p["post_attn_w"]), cfg.eps))
+    a2 = bf(nrm(x, p["norm2_w"], p["norm2_b"]))
+    g = lin(a2, p["wg"])
+    actf = (lambda u: F.gelu(u, approximate="tanh")) if cfg.act == "gelu_tanh" else F.silu
+    m = bf(actf(bf(g)) * bf(lin(a2, p["wu"]))) if cfg.gated else bf(actf(bf(g)))
+    if cfg.form == "plain":
+        x = f32(x + lin(m, p["wd"]))
+    else:
+        x = f32(x + F.rms_norm(f32(lin(m, p["wd"])), (cfg.d,), t(p["post_ffn_w"]), cfg.eps))
+    a_out = bf(nrm(x, *next_norm)) if next_norm is not None else None
+    return x.numpy(), (a_out.numpy() if a_out is not None else None), a.numpy()
+
+
+@pytest.mark.parametrize("form,norm,gated,act,rope,qk,window,bias", [
+    ("plain", "rms", True, "gelu_tanh", None, False, 0, False),     # c1 form
+    ("plain", "ln", False, "gelu_tanh", None, False, 0, True),      # c3 form
+    ("sandwich", "rms", True, "gelu_tanh", "1d", True, 4, False),   # c2 form
+    ("sandwich", "rms", True, "silu", "2d", True, 0, False),        # c4/c5 form
+])
+def test_block_matches_torch_library_composition(form, norm, gated, act, rope, qk, window, bias):
+    cfg = _tiny(form, norm, gated, act, rope, qk, window, bias)
+    lens = cfg.lens
+    cu = synth.cu_seqlens(lens)
+    T = int(cu[-1])
+    p = synth.draw_layer(cfg, 0, 99)
+    x = synth.draw_x(T, cfg.d, 5)
+    tables = synth.rope_tables(cfg, lens)
+    nxt = synth.draw_norm(np.random.default_rng(3), cfg.d, cfg.norm == "ln")
+    x_ref, a_ref, a_in = _torch_block(cfg, p, x, cu, tables, nxt)
+    r = O.block_forward(cfg, p, x, a_in, cu, 0, tables, next_norm=nxt)
+    np.testing.assert_allclose(r["x_out"], x_ref, rtol=2e-5, atol=2e-5)
+    np.testing.assert_allclose(r["a_out"], a_ref, rtol=2e-2, atol=2e-2)
+    rel = np.linalg.norm(r["a_out"] - a_ref) / np.linalg.norm(a_ref)
+    assert rel < 1e-4
+
+
+def test_block_with_zero_weights_is_identity_on_residual():
+    for form in ("plain", "sandwich"):
+        cfg = _tiny(form, "rms", True, "silu", None, False)
+        p = synth.draw_layer(cfg, 0, 1)
+        for key in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+            p[key]["s"] = np.zeros_like(p[key]["s"])
+        cu = synth.cu_seqlens(cfg.lens)
+        x = synth.draw_x(int(cu[-1]), cfg.d, 2)
+        a = O.round_bf16(O.rms_norm(x, p["norm1_w"], cfg.eps))
+        r = O.block_forward(cfg, p, x, a, cu, 0, synth.rope_tables(cfg, cfg.lens))
+        np.testing.assert_array_equal(r["x_out"], x.astype(np.float64))
+
+
+def test_block_is_equivariant_to_sequence_order():
+    cfg = _tiny("sandwich", "rms", True, "gelu_tanh", "1d", True, 3)
+    p = synth.draw_layer(cfg, 0, 4)
+    lens = (9, 14)
+    cu = synth.cu_seqlens(lens)
+    x = synth.draw_x(23, cfg.d, 6)
+    a = O.round_bf16(O.rms_norm(x, p["norm1_w"], cfg.eps))
+    r = O.block_forward(cfg, p, x, a, cu, 0, synth.rope_tables(cfg, lens))
+    perm = np.r_[9:23, 0:9]
+    lens2 = (14, 9)
+    r2 = O.block_forward(cfg, p, x[perm], a[perm], synth.cu_seqlens(lens2), 0,
+                         synth.rope_tables(cfg, lens2))
+    np.testing.assert_allclose(r2["x_out"], r["x_out"][perm], rtol=1e-12, atol=1e-12)

@@ -1,0 +1,204 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the smoke check.
+
+This module draws random numbers and lays out buffers; it holds none of the
+encoder's arithmetic.  Both the CUDA path and the CPU oracle receive the
+arrays it returns, so they see identical bytes.
+
+Workloads (sizes and value recipes follow the pages' own workloads; the pages
+name no public dataset, so these seeded arrays stand in for real inputs):
+
+* ``c1`` - one pre-norm block, d=256, 4 heads x 64, gated GELU-tanh FFN 1024,
+  RMSNorm, packed lengths 37+64.
+* ``c2`` - text encoder stack: 24 sandwich-norm blocks, d=512, 8 heads x 64,
+  gated GELU-tanh FFN 2048, q/k RMSNorm + 1-D RoPE, a 512-token sliding
+  window on odd layers, 32 sequences with lengths uniform in [16, 1024],
+  final norm + mean-pool (EmbeddingGemma 2 text tower, cortiq-engine
+  ``egemma2.rs``, ``TextGpu::forward``).
+* ``c3`` - ViT stack: 16 plain pre-norm blocks, d=768, 12 heads x 64,
+  LayerNorm with bias, biased linears, GELU-tanh MLP 3072, 4 x 1024 tokens
+  (cera ``vision_encoder_gpu.rs``, ``encode_image_gpu``).
+* ``c4`` - one DiT block, d=3840, 30 heads x 128, q/k RMSNorm + 2-D RoPE,
+  SwiGLU FFN 10240, sandwich ("post-norm") residual, 2 x 1056 tokens
+  (cortiq-engine ``zimage.rs``, ``Enc::block``).
+* ``c5`` - the same block shape stacked 30 deep at 2 x 4224 tokens.
+
+Random recipe: ``x ~ N(0,1)`` f32; int8 weights uniform on [-127, 127]; row
+scale ``1/(127*sqrt(K))`` (optionally jittered by a factor in [0.75, 1.25] so
+that a wrong row index is visible); RMS/LN weights ``1 + N(0, 0.1)``, LN
+biases ``N(0, 0.1)``, linear biases ``N(0, 0.02)``.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+BASE_SEED = 20261202
+
+
+@dataclasses.dataclass(frozen=True)
+class BlockConfig:
+    """Shape and form of one encoder stack."""
+
+    name: str
+    layers: int
+    d: int
+    heads: int
+    kv_heads: int
+    hd: int
+    ffn: int
+    gated: bool          # gate|up pair (z=2) vs a single up projection
+    act: str             # "gelu_tanh" | "silu"
+    norm: str            # "rms" | "ln"
+    form: str            # "plain" (x += proj) | "sandwich" (x = x + RMS(proj)*w)
+    qk_norm: bool
+    rope: Optional[str]  # None | "1d" | "2d"
+    window: int          # sliding window on the layers it applies to (0 = full)
+    window_layers: str   # "all" | "odd"
+    bias: bool
+    pool: bool
+    lens: tuple          # fixed lengths, or () when drawn
+    n_seqs: int = 0      # number of drawn lengths when ``lens`` is empty
+    len_lo: int = 0
+    len_hi: int = 0
+    eps: float = 1e-6
+    post: float = 1.0
+
+    def window_of(self, layer: int) -> int:
+        if self.window == 0:
+            return 0
+        if self.window_layers == "all" or layer % 2 == 1:
+            return self.window
+        return 0
+
+    @property
+    def qkv_width(self) -> int:
+        return (self.heads + 2 * self.kv_heads) * self.hd
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.hd)
+
+
+CONFIGS = {
+    "c1": BlockConfig("c1_block_d256", 1, 256, 4, 4, 64, 1024, True, "gelu_tanh",
+                      "rms", "plain", False, None, 0, "all", False, False, (37, 64)),
+    "c2": BlockConfig("c2_text_stack24_d512", 24, 512, 8, 8, 64, 2048, True, "gelu_tanh",
+                      "rms", "sandwich", True, "1d", 512, "odd", False, True, (),
+                      n_seqs=32, len_lo=16, len_hi=1024),
+    "c3": BlockConfig("c3_vit_stack16_d768", 16, 768, 12, 12, 64, 3072, False, "gelu_tanh",
+                      "ln", "plain", False, None, 0, "all", True, False, (1024,) * 4,
+                      eps=1e-5),
+    "c4": BlockConfig("c4_dit_block_d3840", 1, 3840, 30, 30, 128, 10240, True, "silu",
+                      "rms", "sandwich", True, "2d", 0, "all", False, False, (1056, 1056)),
+    "c5": BlockConfig("c5_dit_stack30_d3840", 30, 3840, 30, 30, 128, 10240, True, "silu",
+                      "rms", "sandwich", True, "2d", 0, "all", False, False, (4224, 4224)),
+}
+
+
+def config_seed(key: str) -> int:
+    return BASE_SEED + int(key[1:]) if key[:1] == "c" and key[1:].isdigit() else BASE_SEED
+
+
+def draw_lens(cfg: BlockConfig, seed: int = BASE_SEED) -> np.ndarray:
+    """Sequence lengths of the packed batch (int32).  The text workload's 32
+    lengths drawn with the base seed sum to 16238 rows (longest 955)."""
+    if cfg.lens:
+        return np.asarray(cfg.lens, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    return rng.integers(cfg.len_lo, cfg.len_hi + 1, cfg.n_seqs).astype(np.int32)
+
+
+def cu_seqlens(lens) -> np.ndarray:
+    """Prefix offsets [0, l0, l0+l1, ...] (int32, length nseq+1)."""
+    lens = np.asarray(lens, dtype=np.int64)
+    cu = np.zeros(len(lens) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(lens)
+    return cu.astype(np.int32)
+
+
+def draw_x(t: int, d: int, seed: int) -> np.ndarray:
+    return np.random.default_rng(seed).standard_normal((t, d)).astype(np.float32)
+
+
+def draw_q8(rng: np.random.Generator, n: int, k: int, jitter: bool, bias: bool):
+    """One q8_row weight: int8 [n, k] row-major, f32 scale [n], optional f32 bias [n]."""
+    q = rng.integers(-127, 128, size=(n, k), dtype=np.int8)
+    s = np.full(n, 1.0 / (127.0 * math.sqrt(k)), dtype=np.float64)
+    if jitter:
+        s = s * rng.uniform(0.75, 1.25, n)
+    b = (rng.standard_normal(n) * 0.02).astype(np.float32) if bias else None
+    return {"q": q, "s": s.astype(np.float32), "b": b}
+
+
+def draw_norm(rng: np.random.Generator, d: int, with_bias: bool):
+    w = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    b = (0.1 * rng.standard_normal(d)).astype(np.float32) if with_bias else None
+    return w, b
+
+
+def draw_layer(cfg: BlockConfig, layer: int, seed: int, jitter: bool = True) -> dict:
+    """All weights of one layer (host numpy arrays)."""
+    rng = np.random.default_rng([seed, 7919, layer])
+    d, hd, F = cfg.d, cfg.hd, cfg.ffn
+    p = {}
+    p["wq"] = draw_q8(rng, cfg.heads * hd, d, jitter, cfg.bias)
+    p["wk"] = draw_q8(rng, cfg.kv_heads * hd, d, jitter, cfg.bias)
+    p["wv"] = draw_q8(rng, cfg.kv_heads * hd, d, jitter, cfg.bias)
+    p["wo"] = draw_q8(rng, d, cfg.heads * hd, jitter, cfg.bias)
+    p["wg"] = draw_q8(rng, F, d, jitter, cfg.bias)
+    p["wu"] = draw_q8(rng, F, d, jitter, cfg.bias) if cfg.gated else None
+    p["wd"] = draw_q8(rng, d, F, jitter, cfg.bias)
+    ln = cfg.norm == "ln"
+    p["norm1_w"], p["norm1_b"] = draw_norm(rng, d, ln)          # attention pre-norm
+    p["norm2_w"], p["norm2_b"] = draw_norm(rng, d, ln)          # FFN pre-norm
+    if cfg.form == "sandwich":
+        p["post_attn_w"], _ = draw_norm(rng, d, False)
+        p["post_ffn_w"], _ = draw_norm(rng, d, False)
+    if cfg.qk_norm:
+        p["q_norm"], _ = draw_norm(rng, hd, False)
+        p["k_norm"], _ = draw_norm(rng, hd, False)
+    return p
+
+
+def draw_final_norm(cfg: BlockConfig, seed: int) -> np.ndarray:
+    rng = np.random.default_rng([seed, 104729])
+    return (1.0 + 0.1 * rng.standard_normal(cfg.d)).astype(np.float32)
+
+
+def rope_tables(cfg: BlockConfig, lens) -> dict:
+    """RoPE inputs for the boundary: cos/sin tables [P, hd/2] (f32), a per-row
+    table index ``pos`` (int32 [T]) and the section width ``sec``.
+
+    1-D (text): angle(p, i) = p * 10000^(-2i/hd); positions restart at 0 in
+    every sequence, table rows indexed by position.  2-D (DiT/vision): one
+    table row per packed row; (r, c) = divmod(index in sequence, 32); the
+    first hd/4 entries rotate by the column c, the next hd/4 by the row r,
+    each with 10000^(-2i/(hd/2)); ``sec = hd/2``.
+    """
+    if cfg.rope is None:
+        return {"cos": None, "sin": None, "pos": None, "sec": 0}
+    lens = np.asarray(lens, dtype=np.int64)
+    hd = cfg.hd
+    local = np.concatenate([np.arange(n) for n in lens]).astype(np.int64)
+    if cfg.rope == "1d":
+        P = int(lens.max())
+        i = np.arange(hd // 2, dtype=np.float64)
+        inv = 10000.0 ** (-2.0 * i / hd)
+        ang = np.arange(P, dtype=np.float64)[:, None] * inv[None, :]
+        return {"cos": np.cos(ang).astype(np.float32), "sin": np.sin(ang).astype(np.float32),
+                "pos": local.astype(np.int32), "sec": hd}
+    quarter = hd // 4
+    i = np.arange(quarter, dtype=np.float64)
+    inv = 10000.0 ** (-2.0 * i / (hd // 2))
+    r, c = np.divmod(local, 32)
+    ang = np.concatenate([c[:, None] * inv[None, :], r[:, None] * inv[None, :]], axis=1)
+    return {"cos": np.cos(ang).astype(np.float32), "sin": np.sin(ang).astype(np.float32),
+            "pos": np.arange(len(local), dtype=np.int32), "sec": hd // 2}
+
+
+def small_config(key: str, **over) -> BlockConfig:
+    """A shrunken copy of a workload for the oracle-sized parity tests."""
+    return dataclasses.replace(CONFIGS[key], **over)
