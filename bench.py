@@ -1,0 +1,498 @@
+"""Throughput of the encoder forward on GB300 (one JSON line on stdout).
+
+A step is one forward pass of the whole encoder stack (every block, the
+input norm and, for the text workload, the final-norm mean-pool) over one
+packed batch of seeded synthetic input already resident in HBM.  The forward
+is captured once in a CUDA graph and replayed; L2 is flushed (a 512 MiB
+write) before every timed step and each step is timed with CUDA events on the
+launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2|c3|c4|c5|c1]
+                  [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain f64 numpy restatement of
+the method, test infrastructure) on a bounded sample of the same workload on
+this machine's host cores; it is the slow baseline, not a target.
+
+Multi-GPU: sequences are independent and the forward has no exchange step,
+so N ranks run N independent replicas (weak scaling, no data-path
+collective); value = the work of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from transformer_encoder_forward_gb300 import synth  # noqa: E402
+
+METRIC = "encoder-block TFLOP/s and tokens/s at 1 GB300; % of dense bf16 tensor peak"
+
+
+# ------------------------------------------------------------ work counting
+
+def visible_pairs(lens, window):
+    """(query, key) pairs the attention computes: same sequence and, with a
+    window, |i - j| <= window."""
+    tot = 0
+    for n in lens:
+        n = int(n)
+        if window == 0 or window >= n - 1:
+            tot += n * n
+        else:
+            i = np.arange(n)
+            tot += int(np.sum(np.minimum(n - 1, i + window) - np.maximum(0, i - window) + 1))
+    return tot
+
+
+def layer_flops(cfg, lens, layer):
+    T = int(np.sum(lens))
+    d, hd, H, KV, F = cfg.d, cfg.hd, cfg.heads, cfg.kv_heads, cfg.ffn
+    gemm = 2 * T * (d * (H + 2 * KV) * hd + H * hd * d + d * F * (2 if cfg.gated else 1) + F * d)
+    attn = 4 * hd * H * visible_pairs(lens, cfg.window_of(layer))
+    return gemm, attn
+
+
+def forward_flops(cfg, lens, layers=None):
+    n = cfg.layers if layers is None else layers
+    g = a = 0
+    for i in range(n):
+        gi, ai = layer_flops(cfg, lens, i)
+        g += gi
+        a += ai
+    return g, a
+
+
+def launches_per_forward(cfg):
+    """Kernels of this library one forward launches (what the graph replays)."""
+    n = 1                                                     # input pre-norm
+    for i in range(cfg.layers):
+        n += 4                                                # q8 GEMMs: qkv, o, gate|up, down
+        n += 1 if (cfg.qk_norm or cfg.rope) else 0            # q/k norm + RoPE
+        n += 3                                                # attention, FFN pre-norm, gate
+        n += 1 if (cfg.form == "sandwich" or i + 1 < cfg.layers) else 0   # closing norm
+    return n + (1 if cfg.pool else 0)                         # final norm + pool
+
+
+# ------------------------------------------------------------------ helpers
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def build_stack(key, device):
+    from transformer_encoder_forward_gb300.model import EncoderStack
+    cfg = synth.CONFIGS[key]
+    lens = synth.draw_lens(cfg)
+    seed = synth.config_seed(key)
+    layers = [synth.draw_layer(cfg, i, seed, jitter=False) for i in range(cfg.layers)]
+    tables = synth.rope_tables(cfg, lens)
+    fin = synth.draw_final_norm(cfg, seed) if cfg.pool else None
+    st = EncoderStack(cfg, layers, lens, tables, fin, device=device)
+    x0 = synth.draw_x(st.T, cfg.d, seed)
+    return cfg, lens, st, x0, layers, tables
+
+
+# --------------------------------------------------------------- GPU timing
+
+def time_kernels(cfg, st, torch, reps=20):
+    """Per-launch device time of each op of one block, launched alone with the
+    workload's shapes (CUDA events on the launching stream, after warm-up).
+    Returns {name: (ms per launch, flops, bytes, launches per forward)}."""
+    import transformer_encoder_forward_gb300 as te
+    T, d, hd, H, KV, F = st.T, cfg.d, cfg.hd, cfg.heads, cfg.kv_heads, cfg.ffn
+    qw, kw = H * hd, KV * hd
+    ldq = qw + 2 * kw
+    dev = st.device
+    L0 = st.layers[0]
+    a = torch.randn(T, d, device=dev).to(torch.bfloat16)
+    qkv = torch.randn(T, ldq, device=dev).to(torch.bfloat16)
+    o = torch.randn(T, qw, device=dev).to(torch.bfloat16)
+    tmp = torch.empty(T, d, device=dev)
+    gu = torch.randn(T, 2 * F, device=dev).to(torch.bfloat16)
+    m = torch.randn(T, F, device=dev).to(torch.bfloat16)
+    x = torch.randn(T, d, device=dev)
+    w = lambda k: te.q8w(*L0.t[k])
+    nl = cfg.layers
+    ops = {}
+
+    def gemm_items(keys, y, ldy, offs):
+        return [{"w": w(k), "y": y[:, off:] if off else y, "ldy": ldy} for k, off in zip(keys, offs)]
+
+    ug = 2 if cfg.gated else 1
+    g_keys = ["wg", "wu"] if cfg.gated else ["wg"]
+    ops["q8_gemm qkv (z=3)"] = (lambda: te.q8_linear(a, gemm_items(["wq", "wk", "wv"], qkv, ldq, [0, qw, qw + kw])),
+                                2 * T * d * ldq, T * d * 2 + ldq * d + T * ldq * 2, nl)
+    ops["q8_gemm o"] = (lambda: te.q8_linear(o, [{"w": w("wo"), "y": tmp, "ldy": d}]),
+                        2 * T * qw * d, T * qw * 2 + qw * d + T * d * 4, nl)
+    ops["q8_gemm gate|up (z=2)"] = (lambda: te.q8_linear(a, gemm_items(g_keys, gu, ug * F, [0, F][:ug])),
+                                    2 * T * d * F * ug, T * d * 2 + ug * F * d + T * ug * F * 2, nl)
+    ops["q8_gemm down"] = (lambda: te.q8_linear(m, [{"w": w("wd"), "y": tmp, "ldy": d}]),
+                           2 * T * F * d, T * F * 2 + F * d + T * d * 4, nl)
+    for li in sorted({cfg.window_of(i) for i in range(nl)}):
+        cnt = sum(1 for i in range(nl) if cfg.window_of(i) == li)
+        pairs = visible_pairs(st.lens, li)
+        ops[f"attn (window {li})"] = (
+            lambda li=li: te.attn_varlen_fwd(qkv, ldq, 0, qw, qw + kw, st.cu_host, st.cu_dev, H, KV, hd,
+                                             li, cfg.scale, o, qw),
+            4 * hd * H * pairs, T * ldq * 2 + T * qw * 2, cnt)
+    if cfg.qk_norm or cfg.rope:
+        ops["qk_prep_rope"] = (lambda: te.qk_prep_rope(
+            qkv, ldq, 0, qw, H, KV, hd, L0.t["q_norm"], L0.t["k_norm"], cfg.eps, st.rope_cos, st.rope_sin,
+            st.rope_pos, st.rope_sec, 1.0, T), 0, 2 * T * (qw + kw) * 2, nl)
+    ops["gate_act"] = (lambda: te.gate_act(gu, ug * F, F if cfg.gated else -1,
+                                           te.TE_ACT_SILU if cfg.act == "silu" else te.TE_ACT_GELU_TANH,
+                                           m, F, T, F), 0, T * F * 2 * (ug + 1), nl)
+    ops["add_norm"] = (lambda: te.add_norm(x, tmp, L0.t["post_attn_w"] if cfg.form == "sandwich" else None,
+                                           1.0, L0.t["norm2_w"], L0.t["norm2_b"],
+                                           te.TE_NORM_LN if cfg.norm == "ln" else te.TE_NORM_RMS, cfg.eps, a),
+                       0, T * d * (4 * 3 + 2), 2 * nl)
+    res = {}
+    stream = torch.cuda.current_stream()
+    for name, (fn, flops, nbytes, count) in ops.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for s, e in ev:
+            s.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(s.elapsed_time(e) for s, e in ev)
+        res[name] = (ms, flops, nbytes, count)
+    te.check()
+    return res
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import transformer_encoder_forward_gb300 as te
+    te.lib()
+    cfg, lens, st, x0_np, _, _ = build_stack(args.config, dev)
+    T = st.T
+    gflops, aflops = forward_flops(cfg, lens)
+    total_flops = gflops + aflops
+    x0 = torch.from_numpy(x0_np).to(dev)
+    x, a, out = st.buffers()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # capture one forward in a CUDA graph (warm the launch path first)
+    with torch.cuda.stream(stream):
+        x.copy_(x0)
+        st.forward_device(x, a, out, stream=stream)
+    torch.cuda.synchronize()
+    te.check(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        st.forward_device(x, a, out, stream=stream)
+    torch.cuda.synchronize()
+
+    def step():
+        x.copy_(x0)
+        flush.fill_(1)
+        graph.replay()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    te.check(stream)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for s, e in evs:
+                x.copy_(x0)
+                flush.fill_(1)
+                s.record(stream)
+                graph.replay()
+                e.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    te.check(stream)
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    clk = clocks.summary()
+
+    # end to end through the public API from pinned host memory (eager calls)
+    x_host = torch.from_numpy(x0_np).pin_memory()
+    res_host = torch.empty((len(lens) if cfg.pool else T, cfg.d), dtype=torch.float32).pin_memory()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            st.forward_host(x_host, res_host, x, a, out, stream=stream)
+    torch.cuda.synchronize()
+    e2e = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            flush.fill_(1)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            st.forward_host(x_host, res_host, x, a, out, stream=stream)
+            e.record(stream)
+            e2e.append((s, e))
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(s.elapsed_time(e) for s, e in e2e)
+    te.check(stream)
+
+    # per-kernel device times with the workload's shapes -> roofline
+    kern = time_kernels(cfg, st, torch)
+    peaks = read_peaks()
+    per_fwd = {k: v[0] * v[3] for k, v in kern.items()}
+    gemm_ms = sum(v[0] * v[3] for k, v in kern.items() if k.startswith("q8_gemm"))
+    gemm_flops = sum(v[1] * v[3] for k, v in kern.items() if k.startswith("q8_gemm"))
+    attn_ms = sum(v[0] * v[3] for k, v in kern.items() if k.startswith("attn"))
+    attn_fl = sum(v[1] * v[3] for k, v in kern.items() if k.startswith("attn"))
+    gemm_tf = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    peak_tf = peaks["bf16_tflops_sustained"]
+    roofline = {"kernel": "q8_gemm_kernel (all four projections of a block)", "bound": "tensor",
+                "achieved": round(gemm_tf, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(gemm_tf / peak_tf, 4), "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 sustained (cuBLAS)"}
+    kernels = {k: {"ms_per_launch": round(v[0], 4), "launches_per_forward": v[3],
+                   "ms_per_forward": round(v[0] * v[3], 3),
+                   **({"tflops": round(v[1] / (v[0] * 1e-3) / 1e12, 1)} if v[1] else {}),
+                   "gbs": round(v[2] / (v[0] * 1e-3) / 1e9, 1)} for k, v in kern.items()}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(cfg, args.config, budget_s=args.cpu_seconds)
+
+    tflops = total_flops / (ms * 1e-3) / 1e12 * world
+    line = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init q8_row weights of the named shape)",
+        "config": {"workload": cfg.name, "layers": cfg.layers, "tokens": T, "seqs": len(lens),
+                   "d": cfg.d, "heads": cfg.heads, "head_dim": cfg.hd, "ffn": cfg.ffn,
+                   "l2": "flushed before every step (512 MiB write)", "graph": "one CUDA graph per forward",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": round(T * world / (ms * 1e-3), 1),
+        "pct_bf16_peak": round(100 * tflops / world / peaks["bf16_tflops"], 2),
+        "flops_per_step": {"gemm": gflops, "attention": aflops},
+        "e2e": {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": x_host.numel() * 4,
+                "d2h_bytes_per_step": res_host.numel() * 4,
+                "path": "EncoderStack.forward_host: pinned H2D, eager C-ABI calls, D2H of the result"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "attention_tflops": round(attn_fl / (attn_ms * 1e-3) / 1e12, 1) if attn_ms else None,
+        "gpu_launches": launches_per_forward(cfg) * args.steps,
+        "clocks": clk,
+        "wall_s_timed": round(wall, 3),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def cpu_sample(key):
+    """A bounded sample of the workload for the oracle: one layer of the stack
+    over the first sequences (about a second of numpy f64 work)."""
+    cfg = synth.CONFIGS[key]
+    lens = synth.draw_lens(cfg)
+    seed = synth.config_seed(key)
+    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1}[key]
+    sl = lens[:take]
+    if key in ("c4", "c5"):
+        sl = np.asarray([min(int(sl[0]), 1056)], dtype=np.int32)
+    return cfg, sl, seed
+
+
+def oracle_layer(cfg, lens, layer, p, x, tables):
+    from oracle import encoder as O
+    cu = synth.cu_seqlens(lens)
+    a = O.round_bf16(O.norm(cfg.norm, x, p["norm1_w"], p["norm1_b"], cfg.eps))
+    return O.block_forward(cfg, p, x, a, cu, layer, tables, None)
+
+
+def cpu_baseline(cfg_full, key, budget_s=15.0):
+    cfg, sl, seed = cpu_sample(key)
+    tables = synth.rope_tables(cfg, sl)
+    T = int(np.sum(sl))
+    x = synth.draw_x(T, cfg.d, seed).astype(np.float64)
+    ps = {}
+    done, flops, t_used = 0, 0.0, 0.0
+    layer = 0
+    while t_used < budget_s and done < 2 * max(1, cfg.layers):
+        li = layer % cfg.layers
+        if li not in ps:
+            ps[li] = synth.draw_layer(cfg, li, seed, jitter=False)
+        t0 = time.perf_counter()
+        oracle_layer(cfg, sl, li, ps[li], x, tables)
+        t_used += time.perf_counter() - t0
+        g, a = layer_flops(cfg, sl, li)
+        flops += g + a
+        done += 1
+        layer += 1
+        if done >= 2:
+            break
+    return {"value": round(flops / t_used / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{done} layer(s) of {cfg.name} over the first {len(sl)} sequence(s) "
+                      f"({T} tokens), numpy f64, {t_used:.1f} s",
+            "tokens_per_s": round(T * done / t_used / cfg.layers, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg, sl, seed = cpu_sample(args.config)
+    tables = synth.rope_tables(cfg, sl)
+    T = int(np.sum(sl))
+    x = synth.draw_x(T, cfg.d, seed).astype(np.float64)
+    ps = [synth.draw_layer(cfg, i, seed, jitter=False) for i in range(min(2, cfg.layers))]
+    for i in range(args.warmup):
+        oracle_layer(cfg, sl, i % len(ps), ps[i % len(ps)], x, tables)
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        li = i % len(ps)
+        t0 = time.perf_counter()
+        oracle_layer(cfg, sl, li, ps[li], x, tables)
+        times.append(time.perf_counter() - t0)
+        g, a = layer_flops(cfg, sl, li)
+        flops += g + a
+    tot = sum(times)
+    val = flops / tot / 1e12
+    full_cfg = synth.CONFIGS[args.config]
+    sample = (f"each step: one layer of {cfg.name} over the first {len(sl)} sequence(s) "
+              f"({T} tokens), numpy f64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot / len(times), 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": full_cfg.name, "sample": sample},
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="c2", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

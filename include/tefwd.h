@@ -1,0 +1,228 @@
+/*
+ * tefwd - forward pass of a pre-norm transformer encoder block over a packed
+ * batch of variable-length sequences, with int8 row-scaled (q8_row) weights,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (the pages this library restates; each entry point cites its
+ * section):
+ *   [EG2]  "cortiq-engine 0.8.39 src/gpu_metal/egemma2.rs"  (EmbeddingGemma 2
+ *          text/vision encoders on Metal: Prog::rms, Prog::add_norm,
+ *          Prog::gelu, Prog::qkv, Prog::attention, att_plan,
+ *          TextGpu::forward, VisionGpu::forward)
+ *   [ZI]   "cortiq-engine 0.7.6 src/gpu_metal/zimage.rs"  (Z-Image DiT on
+ *          Metal: module doc "The chain" / "Measured", Enc::gemm, Enc::rowop,
+ *          Enc::block, bench_gemm, bench_flash)
+ *   [VIT]  "cera 0.2.4 src/model/vision_encoder_gpu.rs"  (LFM2-VL ViT:
+ *          trait VitGpuOps, encode_image_gpu)
+ *
+ * Conventions shared by every entry point
+ *   - Memory is owned by the caller.  The library never allocates, frees or
+ *     synchronises (te_check excepted); scratch is passed in as a workspace.
+ *   - Device pointers are CUDA device addresses on the current device; host
+ *     pointers (the *_host arguments and descriptors) are read during the
+ *     call only.  Every device pointer must be 16-byte aligned and every
+ *     leading dimension a multiple of 16 bytes.
+ *   - Matrices are row-major.  "bf16" is IEEE bfloat16 stored as uint16,
+ *     written with round-to-nearest-even.
+ *   - All arguments are validated on the host before anything is launched;
+ *     on any error no output is touched and a non-TE_OK status is returned,
+ *     with a message in te_last_error() (thread-local).  Errors from earlier
+ *     asynchronous work surface as TE_ECUDA from te_check().
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream); the
+ *     calls return before it completes.  Every call is capturable in a CUDA
+ *     graph (no host synchronisation, no allocation).
+ */
+#ifndef TEFWD_H
+#define TEFWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *te_stream; /* the same handle as cudaStream_t */
+
+typedef enum {
+    TE_OK = 0,
+    TE_EINVAL = 1,      /* a NULL pointer, a bad enum, or a bad cu_seqlens   */
+    TE_ESHAPE = 2,      /* a size outside what the kernels support           */
+    TE_EALIGN = 3,      /* a pointer or leading dimension not 16-byte aligned */
+    TE_EWORKSPACE = 4,  /* workspace too small                              */
+    TE_ECUDA = 5,       /* a CUDA runtime/driver call failed                 */
+    TE_EDEVICE = 6      /* a kernel gave up a bounded wait (see te_check)    */
+} te_status;
+
+typedef enum { TE_F32 = 0, TE_BF16 = 1 } te_dtype;
+typedef enum { TE_NORM_RMS = 0, TE_NORM_LN = 1 } te_norm_kind;
+typedef enum { TE_ACT_GELU_TANH = 0, TE_ACT_SILU = 1 } te_act_kind;
+typedef enum { TE_RESID_PLAIN = 0, TE_RESID_SANDWICH = 1 } te_resid_form;
+
+/* One q8_row weight ([ZI] module doc "The chain": the file's q8_row bytes,
+ * int8 tile staged exactly, row scale applied in the f32 epilogue).
+ *   q     int8 [n, k] row-major (device)        W[o, j] = scale[o] * q[o, j]
+ *   scale f32 [n] (device)
+ *   bias  f32 [n] (device) or NULL              ([VIT] bias_add of the linears)
+ * Requirements: k % 64 == 0, n % 32 == 0, n >= 32. */
+typedef struct {
+    const int8_t *q;
+    const float *scale;
+    const float *bias;
+    int32_t n;
+    int32_t k;
+} te_q8w;
+
+/* One item of a grouped q8 GEMM ([EG2] Prog::mm item table, one item per
+ * grid z; [ZI] Enc::gemm, z <= 3).  All items share the activation x.
+ *   y        [m, ldy] of y_dtype (TE_F32 or TE_BF16), device
+ *   residual f32 [m, ldr] or NULL; y may alias residual (same pointer and
+ *            leading dimension) for the in-place x += proj of the plain
+ *            pre-norm block ([VIT] encode_image_gpu "add"). */
+typedef struct {
+    te_q8w w;
+    void *y;
+    int64_t ldy;
+    int32_t y_dtype;
+    int32_t reserved;
+    const float *residual;
+    int64_t ldr;
+} te_q8_item;
+
+/* q8_linear: for each item i < z,
+ *     y_i[t, o] = scale_i[o] * sum_j x[t, j] * q_i[o, j]  (+ bias_i[o])  (+ residual_i[t, o])
+ * x: bf16 [m, k] with leading dimension ldx (elements), device.
+ * f32 accumulation on the tensor cores; int8 widened to bf16 exactly.
+ * Sizes: 1 <= m, k % 64 == 0 and every item's w.k == k, 1 <= z <= 4.
+ * Cites [ZI] module doc ("Each GEMM stages the int8 tile as half (exact) and
+ * applies the row scale in its f32 epilogue"), [EG2] Prog::mm. */
+te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t k,
+                       const te_q8_item *items, int32_t z, te_stream stream);
+
+/* attn_varlen_fwd: bidirectional multi-head attention over packed rows.
+ * qkv: bf16 [T, ld] (device) holding q heads at columns q_off + h*hd, k and
+ * v heads at k_off / v_off + g*hd, g = h / (nq_heads / nkv_heads).
+ * Sequence s owns rows [cu[s], cu[s+1]); T = cu[nseq].  For a query row i
+ * of sequence s the visible keys are the rows j of s with window == 0 or
+ * |i - j| <= window.
+ *     out[i, h*hd + c] = sum_j softmax_j(scale * q_i . k_j) v_j[c]   (bf16)
+ * cu_host / cu_dev: the same int32 [nseq+1] offsets on the host (validated,
+ * used to size the launch) and on the device (read by the kernel); cu[0] = 0,
+ * strictly increasing.  hd in {64, 128}; nq_heads % nkv_heads == 0;
+ * window >= 0; out bf16 [T, ldo], must not overlap qkv.
+ * Cites [EG2] Prog::attention and att_plan (window span, "zeros outside the
+ * window"), [ZI] module doc (flash attention, online softmax), [VIT]
+ * VitGpuOps::attention. */
+te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off,
+                             int32_t v_off, const int32_t *cu_host, const int32_t *cu_dev,
+                             int32_t nseq, int32_t nq_heads, int32_t nkv_heads, int32_t hd,
+                             int32_t window, float scale, void *out, int64_t ldo,
+                             te_stream stream);
+
+/* rownorm: y = Norm(pre * x) per row.
+ *   RMS: v / sqrt(mean(v^2) + eps) * w            ([EG2] Prog::rms)
+ *   LN : (v - mean) / sqrt(var + eps) * w + b      ([VIT] VitGpuOps::layernorm;
+ *        biased variance, b may be NULL)
+ * x [t, ldx] of xdt (f32/bf16), y [t, ldy] of ydt; may not overlap unless
+ * identical with equal dtypes.  d % 8 == 0, 8 <= d <= 8192. */
+te_status te_rownorm(const void *x, int32_t xdt, int64_t ldx, const float *w, const float *b,
+                     int32_t kind, float eps, float pre, void *y, int32_t ydt, int64_t ldy,
+                     int32_t t, int32_t d, te_stream stream);
+
+/* add_norm: the residual add fused with the next pre-norm.
+ *   h (f32 [rows, d], in place):
+ *     w_post != NULL:  h = (h + RMS(t) * w_post) * post     ([EG2] Prog::add_norm,
+ *                                                            [ZI] Enc::rowop post mode)
+ *     w_post == NULL:  h = h + t      (t may be NULL: no add)
+ *   then, when w_next != NULL:  a = Norm(h) * w_next (+ b_next), kind RMS/LN,
+ *   stored as adt in a [rows, d].  d % 8 == 0, 8 <= d <= 8192. */
+te_status te_add_norm(float *h, const float *t, const float *w_post, float post,
+                      const float *w_next, const float *b_next, int32_t kind, float eps,
+                      void *a, int32_t adt, int32_t rows, int32_t d, te_stream stream);
+
+/* qk_prep_rope: in place on the bf16 q|k panel of qkv [rows, ld].
+ * Per row and head: if qn/kn != NULL, x = x / sqrt(mean(x^2) + eps) * w
+ * (w: f32 [hd], shared by all heads); then if sec > 0, rotate-half RoPE within
+ * each section of sec channels: for section s and i < sec/2 the pair
+ * (x[s*sec+i], x[s*sec+i+sec/2]) rotates by the angle whose cos/sin sit at
+ * table column s*sec/2 + i of table row pos[row] (pos == NULL: the row index);
+ * then q heads are multiplied by q_mul.  cos/sin: f32 [table_rows, hd/2].
+ * sec in {0, hd, hd/2}; hd in {64, 128}.
+ * Cites [EG2] Prog::qkv and EgQkv.sec (1-D sec = hd; vision 2-D sec = hd/2,
+ * "the column half, then the row half"), [ZI] Enc::block (qk-norm + RoPE in
+ * place, q pre-multiplied). */
+te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t nq,
+                          int32_t nkv, int32_t hd, const float *qn, const float *kn, float eps,
+                          const float *cos, const float *sin, const int32_t *pos,
+                          int32_t table_rows, int32_t sec, float q_mul, int32_t rows,
+                          te_stream stream);
+
+/* gate_act: m = act(g) * u with g = gu[:, 0:f], u = gu[:, u_off:u_off+f];
+ * u_off < 0: ungated, m = act(g).  act: GELU-tanh
+ * 0.5 g (1 + tanh(sqrt(2/pi)(g + 0.044715 g^3))) or SiLU g / (1 + e^-g).
+ * gu bf16 [rows, ld], m bf16 [rows, ldm].  f % 8 == 0.
+ * Cites [EG2] Prog::gelu, [ZI] Enc::block SwiGLU, [VIT] VitGpuOps::gelu. */
+te_status te_gate_act(const void *gu, int64_t ld, int32_t u_off, int32_t act, void *m,
+                      int64_t ldm, int32_t rows, int32_t f, te_stream stream);
+
+/* pool_mean: out[s] = (1/len_s) sum_{r in s} RMS(x_r) * w_final
+ * (w_final == NULL: the plain mean).  x f32 [T, d], out f32 [nseq, d].
+ * Cites [EG2] TextGpu::forward (row_inv then pool: final-normed hidden
+ * state mean-pooled per sequence).  d % 8 == 0, d <= 8192. */
+te_status te_pool_mean(const float *x, int32_t d, const int32_t *cu_host,
+                       const int32_t *cu_dev, int32_t nseq, const float *w_final, float eps,
+                       float *out, te_stream stream);
+
+/* One encoder block ([EG2] TextGpu::forward layer loop; [ZI] Enc::block;
+ * [VIT] encode_image_gpu block loop). */
+typedef struct {
+    int32_t d, n_heads, n_kv_heads, head_dim, ffn;
+    int32_t norm_kind;   /* te_norm_kind: the FFN pre-norm and the next norm      */
+    int32_t resid_form;  /* te_resid_form                                          */
+    int32_t act;         /* te_act_kind                                            */
+    int32_t gated;       /* 1: gate|up pair (wg, wu), 0: single up (wg)            */
+    int32_t window;      /* sliding window (0 = full attention)                    */
+    float eps, attn_scale, post, q_mul;
+    te_q8w wq, wk, wv, wo, wg, wu, wd;
+    const float *ffn_norm_w, *ffn_norm_b;   /* FFN pre-norm (b: LN only, or NULL) */
+    const float *post_attn_w, *post_ffn_w;  /* sandwich form only                 */
+    const float *next_norm_w, *next_norm_b; /* next block's pre-norm, NULL = none */
+    const float *q_norm, *k_norm;           /* [head_dim] or NULL                 */
+    const float *rope_cos, *rope_sin;       /* [rope_rows, head_dim/2] or NULL    */
+    const int32_t *rope_pos;                /* [T] table row per packed row, NULL = row index */
+    int32_t rope_sec, rope_rows;
+} te_block_desc;
+
+/* Workspace bytes te_encoder_block_fwd needs for t packed rows. */
+size_t te_encoder_block_workspace(const te_block_desc *desc, int32_t t);
+
+/* encoder_block_fwd: one block, in place.
+ *   x: f32 [t, d] residual stream (in/out).
+ *   a: bf16 [t, d]; in: this block's normed input; out: Norm_next(x_out) when
+ *      next_norm_w != NULL (otherwise left as the FFN's input).
+ * Plain form ([VIT]):    x += Wo attn(qkv(a)) (+b); a = Norm2(x);
+ *                        x += Wd act(Wg a, Wu a) (+b); a = Norm_next(x)
+ * Sandwich form ([EG2], [ZI]): x = (x + RMS(Wo attn) w_pa) post; a = RMS(x) w_2;
+ *                        x = (x + RMS(Wd act) w_pf) post; a = RMS(x) w_next
+ * t = cu_host[nseq]; workspace of te_encoder_block_workspace(desc, t) bytes,
+ * 256-byte aligned. */
+te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, void *a,
+                               const int32_t *cu_host, const int32_t *cu_dev, int32_t nseq,
+                               void *workspace, size_t ws_bytes, te_stream stream);
+
+/* Synchronises `stream`; returns TE_ECUDA for a pending asynchronous CUDA
+ * error, TE_EDEVICE if a kernel gave up a bounded wait since the last check
+ * (the device-side word is then cleared), TE_OK otherwise. */
+te_status te_check(te_stream stream);
+
+/* Message of this thread's last non-OK status ("" if none). */
+const char *te_last_error(void);
+
+/* Library version string. */
+const char *te_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TEFWD_H */

@@ -314,8 +314,10 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None):
     Sandwich form (egemma2.rs ``TextGpu::forward``; zimage.rs ``Enc::block``):
         x = (x + rms(o Wo^T) w_pa) post;  a = rms(x) w_2;
         x = (x + rms(FFN(a)) w_pf) post;  a = rms(x) w_next
-    ``rows`` restricts attention to sampled query rows (the output rows that
-    depend on them are then only valid on those rows).
+    ``rows`` restricts the block to sampled query rows: q|k|v is computed for
+    every row (all keys are needed), everything after attention only for the
+    sampled rows (it is row-local), and the returned post-attention
+    intermediates hold those rows only, in the order given.
     """
     hd, H, KV, d, F = cfg.hd, cfg.heads, cfg.kv_heads, cfg.d, cfg.ffn
     eps = cfg.eps
@@ -337,6 +339,9 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None):
     r["qkv"] = qkv
     o = attention_varlen(qkv, cu, H, KV, hd, 0, qw, qw + kw, cfg.window_of(layer),
                          cfg.scale, rows=rows)
+    if rows is not None:
+        rows = np.asarray(rows)
+        o, x = o[rows], x[rows]
     r["o"] = o = round_bf16(o)
     if cfg.form == "plain":
         x = round_f32(q8_linear(o, p["wo"]["q"], p["wo"]["s"], p["wo"]["b"], residual=x))

@@ -1,0 +1,158 @@
+"""The C-ABI library builds, loads, exports what include/tefwd.h declares, and
+rejects bad arguments on the host before launching anything (no GPU needed:
+every call here must fail validation)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import transformer_encoder_forward_gb300 as te
+from transformer_encoder_forward_gb300 import build as tebuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(te.LIB_PATH):
+        tebuild.build()
+    return te.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tefwd.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(te_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(te.EXPORTS), "binding and header disagree"
+
+
+def test_version_and_empty_error(L):
+    assert "sm_103a" in te.version()
+
+
+FAKE = 0x10000   # never dereferenced: every call below fails validation first
+
+
+def _call(L, name, *args):
+    st = getattr(L, name)(*args)
+    return st, L.te_last_error().decode()
+
+
+def test_q8_linear_rejects_bad_arguments(L):
+    item = te.te_q8_item(te.te_q8w(FAKE, FAKE, None, 64, 128), FAKE, 64, te.TE_F32, 0, None, 0)
+    arr = (te.te_q8_item * 1)(item)
+    st, msg = _call(L, "te_q8_linear", FAKE, 128, 16, 128, arr, 0, None)
+    assert st == te.TE_ESHAPE and "z=" in msg
+    st, msg = _call(L, "te_q8_linear", FAKE, 128, 16, 100, arr, 1, None)
+    assert st == te.TE_ESHAPE and "k=100" in msg
+    st, msg = _call(L, "te_q8_linear", FAKE + 2, 128, 16, 128, arr, 1, None)
+    assert st == te.TE_EALIGN
+    bad_k = (te.te_q8_item * 1)(te.te_q8_item(te.te_q8w(FAKE, FAKE, None, 64, 64), FAKE, 64,
+                                              te.TE_F32, 0, None, 0))
+    st, msg = _call(L, "te_q8_linear", FAKE, 128, 16, 128, bad_k, 1, None)
+    assert st == te.TE_ESHAPE and "item 0" in msg
+    bad_n = (te.te_q8_item * 1)(te.te_q8_item(te.te_q8w(FAKE, FAKE, None, 40, 128), FAKE, 64,
+                                              te.TE_F32, 0, None, 0))
+    assert _call(L, "te_q8_linear", FAKE, 128, 16, 128, bad_n, 1, None)[0] == te.TE_ESHAPE
+    inplace_bf16 = (te.te_q8_item * 1)(te.te_q8_item(te.te_q8w(FAKE, FAKE, None, 64, 128), FAKE,
+                                                     64, te.TE_BF16, 0, FAKE, 64))
+    assert _call(L, "te_q8_linear", FAKE, 128, 16, 128, inplace_bf16, 1, None)[0] == te.TE_EINVAL
+    null_y = (te.te_q8_item * 1)(te.te_q8_item(te.te_q8w(FAKE, FAKE, None, 64, 128), None, 64,
+                                               te.TE_F32, 0, None, 0))
+    assert _call(L, "te_q8_linear", FAKE, 128, 16, 128, null_y, 1, None)[0] == te.TE_EINVAL
+
+
+def _cu(vals):
+    a = np.asarray(vals, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def test_attention_rejects_bad_cu_seqlens_and_shapes(L):
+    a, p = _cu([0, 5, 5, 9])            # an empty sequence
+    st, msg = _call(L, "te_attn_varlen_fwd", FAKE, 192, 0, 64, 128, p, FAKE, 3, 1, 1, 64, 0,
+                    1.0, FAKE * 4, 64, None)
+    assert st == te.TE_EINVAL and "length 0" in msg
+    a, p = _cu([1, 5])                   # does not start at 0
+    assert _call(L, "te_attn_varlen_fwd", FAKE, 192, 0, 64, 128, p, FAKE, 1, 1, 1, 64, 0, 1.0,
+                 FAKE * 4, 64, None)[0] == te.TE_EINVAL
+    a, p = _cu([0, 9, 5])                # decreasing
+    assert _call(L, "te_attn_varlen_fwd", FAKE, 192, 0, 64, 128, p, FAKE, 2, 1, 1, 64, 0, 1.0,
+                 FAKE * 4, 64, None)[0] == te.TE_EINVAL
+    a, p = _cu([0, 9])
+    assert _call(L, "te_attn_varlen_fwd", FAKE, 288, 0, 96, 192, p, FAKE, 1, 1, 1, 96, 0, 1.0,
+                 FAKE * 4, 96, None)[0] == te.TE_ESHAPE                       # hd = 96
+    assert _call(L, "te_attn_varlen_fwd", FAKE, 192, 0, 64, 128, p, FAKE, 1, 3, 2, 64, 0, 1.0,
+                 FAKE * 4, 192, None)[0] == te.TE_ESHAPE                      # 3 % 2 heads
+    assert _call(L, "te_attn_varlen_fwd", FAKE, 192, 0, 64, 128, p, FAKE, 1, 1, 1, 64, -1, 1.0,
+                 FAKE * 4, 64, None)[0] == te.TE_EINVAL                       # window < 0
+    assert _call(L, "te_attn_varlen_fwd", FAKE, 192, 0, 64, 128, p, FAKE, 1, 1, 1, 64, 0, 1.0,
+                 FAKE + 64, 64, None)[0] == te.TE_EINVAL                      # out overlaps qkv
+    assert _call(L, "te_attn_varlen_fwd", FAKE, 100, 0, 64, 128, p, FAKE, 1, 1, 1, 64, 0, 1.0,
+                 FAKE * 4, 64, None)[0] == te.TE_ESHAPE                       # ld too small
+
+
+def test_row_ops_reject_bad_arguments(L):
+    assert _call(L, "te_rownorm", FAKE, te.TE_F32, 100, FAKE, None, te.TE_NORM_RMS, 1e-6, 1.0,
+                 FAKE, te.TE_BF16, 100, 4, 100, None)[0] == te.TE_ESHAPE      # d % 8
+    assert _call(L, "te_rownorm", FAKE, te.TE_F32, 64, FAKE, None, 7, 1e-6, 1.0, FAKE, te.TE_BF16,
+                 64, 4, 64, None)[0] == te.TE_EINVAL                          # bad kind
+    assert _call(L, "te_rownorm", FAKE + 4, te.TE_F32, 64, FAKE, None, te.TE_NORM_RMS, 1e-6, 1.0,
+                 FAKE, te.TE_BF16, 64, 4, 64, None)[0] == te.TE_EALIGN
+    assert _call(L, "te_add_norm", FAKE, None, FAKE, 1.0, None, None, te.TE_NORM_RMS, 1e-6, None,
+                 te.TE_BF16, 4, 64, None)[0] == te.TE_EINVAL                  # w_post without t
+    assert _call(L, "te_qk_prep_rope", FAKE, 384, 0, 128, 2, 2, 64, None, None, 1e-6, FAKE, FAKE,
+                 None, 4, 48, 1.0, 8, None)[0] == te.TE_ESHAPE                # sec = 48
+    assert _call(L, "te_qk_prep_rope", FAKE, 384, 0, 128, 2, 2, 64, None, None, 1e-6, FAKE, FAKE,
+                 None, 4, 64, 1.0, 8, None)[0] == te.TE_ESHAPE                # table too short
+    assert _call(L, "te_gate_act", FAKE, 64, 60, te.TE_ACT_SILU, FAKE, 32, 4, 32, None)[0] \
+        == te.TE_ESHAPE                                                      # u runs past ld
+    assert _call(L, "te_gate_act", FAKE, 64, 32, 5, FAKE, 32, 4, 32, None)[0] == te.TE_EINVAL
+    a, p = _cu([0, 3, 3])
+    assert _call(L, "te_pool_mean", FAKE, 64, p, FAKE, 2, None, 1e-6, FAKE, None)[0] == te.TE_EINVAL
+
+
+def _desc(**over):
+    d = te.te_block_desc()
+    d.d, d.n_heads, d.n_kv_heads, d.head_dim, d.ffn = 256, 4, 4, 64, 1024
+    d.gated, d.eps, d.attn_scale, d.post = 1, 1e-6, 0.125, 1.0
+    for key, (n, k) in dict(wq=(256, 256), wk=(256, 256), wv=(256, 256), wo=(256, 256),
+                            wg=(1024, 256), wu=(1024, 256), wd=(256, 1024)).items():
+        setattr(d, key, te.te_q8w(FAKE, FAKE, None, n, k))
+    d.ffn_norm_w = FAKE
+    for k, v in over.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_block_validation_and_workspace(L):
+    a, p = _cu([0, 37, 101])
+    d = _desc()
+    ws = L.te_encoder_block_workspace(ctypes.byref(d), 101)
+    expect = sum(((101 * w + 255) // 256) * 256 for w in (768 * 2, 256 * 2, 256 * 4, 2048 * 2,
+                                                          1024 * 2))
+    assert ws == expect
+    st, msg = _call(L, "te_encoder_block_fwd", ctypes.byref(d), FAKE, FAKE, p, FAKE, 2, FAKE * 256,
+                    ws - 1, None)
+    assert st == te.TE_EWORKSPACE
+    bad = _desc(wo=te.te_q8w(FAKE, FAKE, None, 256, 512))
+    st, msg = _call(L, "te_encoder_block_fwd", ctypes.byref(bad), FAKE, FAKE, p, FAKE, 2,
+                    FAKE * 256, ws, None)
+    assert st == te.TE_ESHAPE and "wo" in msg
+    sand = _desc(resid_form=te.TE_RESID_SANDWICH)
+    assert _call(L, "te_encoder_block_fwd", ctypes.byref(sand), FAKE, FAKE, p, FAKE, 2,
+                 FAKE * 256, ws, None)[0] == te.TE_EINVAL
+    qn_only = _desc(q_norm=FAKE)
+    assert _call(L, "te_encoder_block_fwd", ctypes.byref(qn_only), FAKE, FAKE, p, FAKE, 2,
+                 FAKE * 256, ws, None)[0] == te.TE_EINVAL
+    unal = _desc()
+    assert _call(L, "te_encoder_block_fwd", ctypes.byref(unal), FAKE, FAKE, p, FAKE, 2,
+                 FAKE * 256 + 16, ws, None)[0] == te.TE_EALIGN

@@ -1,0 +1,154 @@
+"""Whole-block and stack parity of the CUDA path (te_encoder_block_fwd through
+the C-ABI) against the CPU oracle.
+
+Gate: relative Frobenius error <= 5e-3 on the block output x (also checked on
+the residual-free delta x_out - x_in, the stricter diagnostic) and on the next
+block's normed input a.  Stacks are compared teacher-forced: the oracle takes
+the GPU's input to each checked layer.  At the largest workload the oracle
+runs on sampled query rows (all keys).
+"""
+import numpy as np
+import pytest
+
+import transformer_encoder_forward_gb300 as te
+from oracle import encoder as O
+from transformer_encoder_forward_gb300 import synth
+from transformer_encoder_forward_gb300.model import EncoderStack
+from tests.gpu_util import rel_frob, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-3
+
+
+def _stack(cfg, lens, layers, seed=11, jitter=True):
+    ps = [synth.draw_layer(cfg, i, seed, jitter) for i in range(layers)]
+    tables = synth.rope_tables(cfg, lens)
+    fin = synth.draw_final_norm(cfg, seed) if cfg.pool else None
+    return EncoderStack(cfg, ps, lens, tables, fin), ps, tables
+
+
+def _next_norm(ps, i):
+    return (ps[i + 1]["norm1_w"], ps[i + 1]["norm1_b"]) if i + 1 < len(ps) else None
+
+
+def _check_layer(cfg, st, ps, tables, i, x, a, rows=None):
+    """Runs GPU layer i in place on (x, a) and compares against the oracle on
+    the same inputs."""
+    import torch
+    x_in, a_in = to_np(x), to_np(a)
+    te.encoder_block_fwd(st.descs[i], x, a, st.cu_host, st.cu_dev, st.workspace)
+    te.check()
+    r = O.block_forward(cfg, ps[i], x_in, a_in, st.cu_host, i, tables, _next_norm(ps, i),
+                        rows=rows)
+    sel = slice(None) if rows is None else np.asarray(rows)
+    got_x = to_np(x)[sel]
+    xin = x_in[sel]
+    assert np.all(np.isfinite(got_x))
+    e_x = rel_frob(got_x, r["x_out"])
+    e_d = rel_frob(got_x - xin, r["x_out"] - xin)
+    assert e_x < TOL, (i, e_x)
+    assert e_d < 2 * TOL, (i, e_d)
+    if r["a_out"] is not None:
+        e_a = rel_frob(to_np(a)[sel], r["a_out"])
+        assert e_a < TOL, (i, e_a)
+    return e_x, e_d
+
+
+FORMS = {
+    "c1_full": ("c1", {}, (37, 64)),
+    "c2_small": ("c2", dict(layers=2, window=40), (100, 1, 300, 37)),
+    "c3_small": ("c3", dict(layers=2), (200, 129)),
+    "c4_small": ("c4", dict(d=512, heads=4, kv_heads=4, ffn=1024), (150, 133)),
+    "gqa_small": ("c2", dict(layers=2, kv_heads=2, window=0), (64, 65)),
+}
+
+
+@pytest.mark.parametrize("name", list(FORMS))
+def test_block_forms_match_oracle(name):
+    key, over, lens = FORMS[name]
+    cfg = synth.small_config(key, lens=lens, **over)
+    st, ps, tables = _stack(cfg, lens, cfg.layers)
+    x = to_dev(synth.draw_x(st.T, cfg.d, 3))
+    import torch
+    a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    st.input_norm(x, a)
+    a0 = O.round_bf16(O.norm(cfg.norm, to_np(x), ps[0]["norm1_w"], ps[0]["norm1_b"], cfg.eps))
+    assert rel_frob(to_np(a), a0) < 2e-3
+    for i in range(cfg.layers):
+        _check_layer(cfg, st, ps, tables, i, x, a)
+
+
+def test_text_stack_24_layers_teacher_forced_and_pooled():
+    import torch
+    cfg = synth.CONFIGS["c2"]
+    lens = synth.draw_lens(cfg)
+    st, ps, tables = _stack(cfg, lens, cfg.layers)
+    x = to_dev(synth.draw_x(st.T, cfg.d, 4))
+    a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    st.input_norm(x, a)
+    check = {0, 1, 12, 23}
+    for i in range(cfg.layers):
+        if i in check:
+            _check_layer(cfg, st, ps, tables, i, x, a)
+        else:
+            te.encoder_block_fwd(st.descs[i], x, a, st.cu_host, st.cu_dev, st.workspace)
+    out = torch.empty(len(lens), cfg.d, dtype=torch.float32, device="cuda")
+    te.pool_mean(x, st.cu_host, st.cu_dev, st.final_norm, cfg.eps, out)
+    te.check()
+    ref = O.pool_mean(to_np(x), st.cu_host, synth.draw_final_norm(cfg, 11), cfg.eps)
+    assert rel_frob(to_np(out), ref) < 1e-5
+
+
+def test_vit_stack_16_layers_teacher_forced():
+    import torch
+    cfg = synth.CONFIGS["c3"]
+    lens = synth.draw_lens(cfg)
+    st, ps, tables = _stack(cfg, lens, cfg.layers)
+    x = to_dev(synth.draw_x(st.T, cfg.d, 5))
+    a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    st.input_norm(x, a)
+    for i in range(cfg.layers):
+        if i in (0, 8, 15):
+            _check_layer(cfg, st, ps, tables, i, x, a)
+        else:
+            te.encoder_block_fwd(st.descs[i], x, a, st.cu_host, st.cu_dev, st.workspace)
+
+
+def test_dit_block_full_size():
+    import torch
+    cfg = synth.CONFIGS["c4"]
+    lens = synth.draw_lens(cfg)
+    st, ps, tables = _stack(cfg, lens, 1, jitter=False)
+    x = to_dev(synth.draw_x(st.T, cfg.d, 6))
+    a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    st.input_norm(x, a)
+    _check_layer(cfg, st, ps, tables, 0, x, a)
+
+
+def test_dit_stack_layer_at_4224_tokens_sampled_rows():
+    import torch
+    cfg = synth.small_config("c5", layers=2)
+    lens = synth.draw_lens(cfg)
+    st, ps, tables = _stack(cfg, lens, 2, jitter=False)
+    x = to_dev(synth.draw_x(st.T, cfg.d, 7))
+    a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    st.input_norm(x, a)
+    rng = np.random.default_rng(8)
+    rows = np.sort(np.r_[rng.choice(st.T, 60, replace=False), [0, 4223, 4224, 8447]])
+    _check_layer(cfg, st, ps, tables, 0, x, a, rows=rows)
+
+
+def test_stack_forward_is_deterministic():
+    import torch
+    cfg = synth.small_config("c2", layers=2, window=40, lens=(100, 300, 37))
+    st, _, _ = _stack(cfg, cfg.lens, 2)
+    x0 = to_dev(synth.draw_x(st.T, cfg.d, 9))
+    outs = []
+    for _ in range(2):
+        x, a, out = st.buffers()
+        x.copy_(x0)
+        st.forward_device(x, a, out)
+        outs.append((x.clone(), out.clone()))
+    te.check()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])

@@ -1,0 +1,290 @@
+"""Per-op parity of the CUDA kernels (called through the C-ABI) against the
+CPU oracle on the same seeded inputs.
+
+Tolerances (relative Frobenius): 1e-3 per GEMM, 3e-3 for attention (bf16 P),
+2e-3 for row ops with bf16 outputs (the oracle rounds at the same storage
+points, so only rare rounding flips differ).  Integer work (int8 widening,
+index/mask computation) is compared bit for bit.
+"""
+import numpy as np
+import pytest
+
+import transformer_encoder_forward_gb300 as te
+from oracle import encoder as O
+from transformer_encoder_forward_gb300 import synth
+from tests.gpu_util import bf16_input, q8_dev, rel_frob, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    torch.cuda.init()
+    te.lib()
+    yield
+    te.check()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+# ------------------------------------------------------------------ q8 GEMM
+
+GEMM_CASES = [
+    # m, k, item widths, bias, residual, out dtype
+    (1, 64, [32], False, False, "f32"),
+    (37, 256, [256, 256, 256], False, False, "bf16"),
+    (101, 256, [1024, 1024], False, False, "bf16"),
+    (101, 1024, [256], False, True, "f32"),
+    (300, 512, [96, 160], True, False, "f32"),
+    (777, 768, [768, 768, 768], True, False, "bf16"),
+    (1000, 192, [64, 128, 192, 288], True, True, "f32"),
+    (2112, 3840, [384], False, False, "f32"),
+    (4100, 320, [640], False, False, "bf16"),
+]
+
+
+@pytest.mark.parametrize("m,k,ns,bias,resid,ydt", GEMM_CASES)
+def test_q8_linear_matches_oracle(m, k, ns, bias, resid, ydt):
+    torch = _torch()
+    rng = np.random.default_rng([m, k, len(ns)])
+    x, x64 = bf16_input(rng, (m, k))
+    ws = [synth.draw_q8(rng, n, k, True, bias) for n in ns]
+    dt = torch.float32 if ydt == "f32" else torch.bfloat16
+    items, outs, refs = [], [], []
+    for w in ws:
+        q, s, b = q8_dev(w)
+        n = w["q"].shape[0]
+        r_np = rng.standard_normal((m, n)).astype(np.float32) if resid else None
+        y = to_dev(r_np) if resid else torch.full((m, n), float("nan"), dtype=dt, device="cuda")
+        it = {"w": te.q8w(q, s, b), "y": y, "ldy": n}
+        if resid:
+            it.update(residual=y, ldr=n)       # in place: y = y + s*acc + b
+        items.append(it)
+        outs.append((y, (q, s, b)))
+        ref = O.q8_linear(x64, w["q"], w["s"], w["b"], r_np)
+        refs.append(O.round_bf16(ref) if ydt == "bf16" else ref)
+    te.q8_linear(x, items)
+    te.check()
+    for (y, _), ref in zip(outs, refs):
+        got = to_np(y)
+        assert np.all(np.isfinite(got))
+        assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
+
+
+def test_q8_linear_exact_integer_case_is_bit_exact():
+    # integer x with |x| <= 16, unit scale, K = 1024: every partial sum is an
+    # integer below 2^24, so f32 accumulation is exact and so is the result
+    torch = _torch()
+    rng = np.random.default_rng(5)
+    m, k = 333, 1024
+    xi = rng.integers(-16, 17, (m, k)).astype(np.float32)
+    x = torch.from_numpy(xi).to(torch.bfloat16).cuda()
+    q_np = rng.integers(-127, 128, (256, k), dtype=np.int8)
+    q = to_dev(q_np)
+    s = torch.ones(256, dtype=torch.float32, device="cuda")
+    y = torch.empty(m, 256, dtype=torch.float32, device="cuda")
+    te.q8_linear(x, [{"w": te.q8w(q, s), "y": y, "ldy": 256}])
+    exact = xi.astype(np.int64) @ q_np.astype(np.int64).T
+    np.testing.assert_array_equal(to_np(y), exact.astype(np.float64))
+
+
+def test_int8_widening_and_indexing_are_bit_exact():
+    # one-hot activation rows pick single weight columns: y[t, o] = q[o, j_t]
+    # exactly, for every int8 value (including -128) and every row/column
+    torch = _torch()
+    k, n = 256, 256
+    q_np = (np.arange(n * k, dtype=np.int64).reshape(n, k) * 37 % 256 - 128).astype(np.int8)
+    m = 2 * k + 3
+    cols = np.r_[np.arange(k), np.arange(k)[::-1], [0, 17, 255]]
+    xi = np.zeros((m, k), np.float32)
+    xi[np.arange(m), cols] = 1.0
+    x = torch.from_numpy(xi).to(torch.bfloat16).cuda()
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    te.q8_linear(x, [{"w": te.q8w(to_dev(q_np), torch.ones(n, device="cuda")), "y": y, "ldy": n}])
+    np.testing.assert_array_equal(to_np(y), q_np[:, cols].T.astype(np.float64))
+    assert set(np.unique(q_np)) == set(range(-128, 128))
+
+
+# ---------------------------------------------------------------- attention
+
+ATTN_CASES = [
+    # lens, nq, nkv, hd, window
+    ([1], 2, 2, 64, 0),
+    ([37, 64], 4, 4, 64, 0),
+    ([5, 130, 64, 1, 200], 3, 3, 64, 0),
+    ([5, 130, 64, 1, 200], 2, 2, 128, 17),
+    ([300, 77], 4, 2, 64, 64),
+    ([700, 129], 2, 1, 128, 512),
+    ([1056, 1056], 2, 2, 128, 0),
+    ([955, 16, 400], 2, 2, 64, 512),
+]
+
+
+def _attn_run(qkv_t, cu, nq, nkv, hd, window, scale):
+    torch = _torch()
+    T = qkv_t.shape[0]
+    out = torch.full((T, nq * hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    te.attn_varlen_fwd(qkv_t, qkv_t.shape[1], 0, nq * hd, (nq + nkv) * hd, cu, to_dev(cu), nq,
+                       nkv, hd, window, scale, out, nq * hd)
+    return out
+
+
+@pytest.mark.parametrize("lens,nq,nkv,hd,window", ATTN_CASES)
+def test_attention_matches_oracle(lens, nq, nkv, hd, window):
+    rng = np.random.default_rng([len(lens), nq, hd, window])
+    cu = synth.cu_seqlens(lens)
+    T = int(cu[-1])
+    W = (nq + 2 * nkv) * hd
+    qkv_t, qkv = bf16_input(rng, (T, W), 1.5)
+    scale = 1.0 / np.sqrt(hd)
+    out = _attn_run(qkv_t, cu, nq, nkv, hd, window, scale)
+    te.check()
+    ref = O.attention_varlen(qkv, cu, nq, nkv, hd, 0, nq * hd, (nq + nkv) * hd, window, scale)
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    assert rel_frob(got, O.round_bf16(ref)) < 3e-3, rel_frob(got, ref)
+
+
+def test_attention_scale_one_and_length_one_sequences():
+    rng = np.random.default_rng(21)
+    lens = [1, 1, 3, 1]
+    cu = synth.cu_seqlens(lens)
+    qkv_t, qkv = bf16_input(rng, (6, 3 * 64))
+    out = to_np(_attn_run(qkv_t, cu, 1, 1, 64, 0, 1.0))
+    for r in (0, 1, 5):                      # a length-1 sequence returns its own v exactly
+        np.testing.assert_array_equal(out[r], qkv[r, 128:])
+    ref = O.attention_varlen(qkv, cu, 1, 1, 64, 0, 64, 128, 0, 1.0)
+    assert rel_frob(out, O.round_bf16(ref)) < 3e-3
+
+
+def test_attention_masked_keys_and_other_sequences_have_no_effect():
+    torch = _torch()
+    rng = np.random.default_rng(22)
+    lens = [200, 150]
+    cu = synth.cu_seqlens(lens)
+    nq, hd, W = 2, 64, 20
+    qkv_t, _ = bf16_input(rng, (350, 3 * nq * hd))
+    base = _attn_run(qkv_t, cu, nq, nq, hd, W, 0.125).clone()
+    pert = qkv_t.clone()
+    # keys/values of rows 100.. of sequence 0 and all of sequence 1 change
+    pert[100:200, nq * hd:] = torch.randn(100, 2 * nq * hd, device="cuda").to(torch.bfloat16) * 50
+    pert[200:, :] = torch.randn(150, 3 * nq * hd, device="cuda").to(torch.bfloat16)
+    out = _attn_run(pert, cu, nq, nq, hd, W, 0.125)
+    # rows 0 .. 100-W-1 of sequence 0 see none of the changed keys: bit-identical
+    assert torch.equal(out[:100 - W], base[:100 - W])
+    assert not torch.equal(out[100 - W:200], base[100 - W:200])
+
+
+def test_attention_wide_window_equals_full():
+    torch = _torch()
+    rng = np.random.default_rng(23)
+    lens = [130, 61]
+    cu = synth.cu_seqlens(lens)
+    qkv_t, _ = bf16_input(rng, (191, 3 * 128))
+    full = _attn_run(qkv_t, cu, 1, 1, 128, 0, 0.1)
+    wide = _attn_run(qkv_t, cu, 1, 1, 128, 129, 0.1)
+    assert torch.equal(full, wide)
+
+
+# ----------------------------------------------------------------- row ops
+
+@pytest.mark.parametrize("d,kind,xdt", [(256, "rms", "f32"), (768, "ln", "f32"),
+                                        (3840, "rms", "f32"), (512, "ln", "bf16"),
+                                        (4096, "rms", "bf16")])
+def test_rownorm_matches_oracle(d, kind, xdt):
+    torch = _torch()
+    rng = np.random.default_rng([d, len(kind)])
+    t = 203
+    if xdt == "f32":
+        x64 = rng.standard_normal((t, d)).astype(np.float32) * 2 + 0.3
+        x = to_dev(x64)
+    else:
+        x, x64 = bf16_input(rng, (t, d), 2.0)
+    w, b = synth.draw_norm(rng, d, kind == "ln")
+    y = torch.empty(t, d, dtype=torch.bfloat16, device="cuda")
+    te.rownorm(x, to_dev(w), to_dev(b) if b is not None else None,
+               te.TE_NORM_LN if kind == "ln" else te.TE_NORM_RMS, 1e-5, y, pre=0.5)
+    ref = O.round_bf16(O.norm(kind, 0.5 * np.asarray(x64, np.float64), w, b, 1e-5))
+    assert rel_frob(to_np(y), ref) < 2e-3
+
+
+@pytest.mark.parametrize("d,sandwich,nxt,kind", [(512, True, True, "rms"), (3840, True, False, "rms"),
+                                                 (768, False, True, "ln"), (256, False, False, "rms")])
+def test_add_norm_matches_oracle(d, sandwich, nxt, kind):
+    torch = _torch()
+    rng = np.random.default_rng([d, int(sandwich), int(nxt)])
+    rows = 157
+    h = rng.standard_normal((rows, d)).astype(np.float32)
+    t = rng.standard_normal((rows, d)).astype(np.float32) * 3
+    wp, _ = synth.draw_norm(rng, d, False)
+    wn, bn = synth.draw_norm(rng, d, kind == "ln")
+    h_t, t_t = to_dev(h), to_dev(t)
+    a = torch.zeros(rows, d, dtype=torch.bfloat16, device="cuda")
+    te.add_norm(h_t, t_t, to_dev(wp) if sandwich else None, 0.75,
+                to_dev(wn) if nxt else None, to_dev(bn) if (nxt and bn is not None) else None,
+                te.TE_NORM_LN if kind == "ln" else te.TE_NORM_RMS, 1e-6, a)
+    h_ref = O.add_norm_sandwich(h, t, wp, 0.75, 1e-6) if sandwich else h.astype(np.float64) + t
+    assert rel_frob(to_np(h_t), h_ref) < 1e-6
+    if nxt:
+        a_ref = O.round_bf16(O.norm(kind, O.round_f32(h_ref), wn, bn, 1e-6))
+        assert rel_frob(to_np(a), a_ref) < 2e-3
+    else:
+        assert torch.count_nonzero(a) == 0
+
+
+@pytest.mark.parametrize("hd,nq,nkv,rope,qk", [(64, 8, 8, "1d", True), (128, 4, 4, "2d", True),
+                                               (64, 4, 2, "2d", False), (128, 2, 1, None, True)])
+def test_qk_prep_rope_matches_oracle(hd, nq, nkv, rope, qk):
+    torch = _torch()
+    rng = np.random.default_rng([hd, nq, nkv])
+    lens = [37, 64, 100]
+    cfg = synth.small_config("c2", hd=hd, rope=rope)
+    tb = synth.rope_tables(cfg, lens)
+    T = sum(lens)
+    W = (nq + 2 * nkv) * hd
+    qkv_t, qkv = bf16_input(rng, (T, W), 2.0)
+    qn, _ = synth.draw_norm(rng, hd, False)
+    kn, _ = synth.draw_norm(rng, hd, False)
+    cos = to_dev(tb["cos"]) if rope else None
+    sin = to_dev(tb["sin"]) if rope else None
+    pos = to_dev(tb["pos"]) if rope else None
+    te.qk_prep_rope(qkv_t, W, 0, nq * hd, nq, nkv, hd, to_dev(qn) if qk else None,
+                    to_dev(kn) if qk else None, 1e-6, cos, sin, pos, tb["sec"], 1.25, T)
+    ref = O.qk_prep(qkv, nq, nkv, hd, 0, nq * hd, qn if qk else None, kn if qk else None, 1e-6,
+                    tb["cos"], tb["sin"], tb["pos"], tb["sec"], 1.25)
+    got = to_np(qkv_t)
+    assert rel_frob(got, ref) < 2e-3
+    np.testing.assert_array_equal(got[:, (nq + nkv) * hd:], qkv[:, (nq + nkv) * hd:])  # v untouched
+
+
+@pytest.mark.parametrize("act,gated,f", [("gelu_tanh", True, 1024), ("silu", True, 10240),
+                                         ("gelu_tanh", False, 3072), ("silu", False, 64)])
+def test_gate_act_matches_oracle(act, gated, f):
+    torch = _torch()
+    rng = np.random.default_rng([f, int(gated)])
+    rows = 211
+    ld = 2 * f if gated else f
+    gu_t, gu = bf16_input(rng, (rows, ld), 2.0)
+    m = torch.empty(rows, f, dtype=torch.bfloat16, device="cuda")
+    te.gate_act(gu_t, ld, f if gated else -1, te.TE_ACT_SILU if act == "silu" else te.TE_ACT_GELU_TANH,
+                m, f, rows, f)
+    ref = O.round_bf16(O.gate_act(gu, f, gated, act))
+    assert rel_frob(to_np(m), ref) < 2e-3
+
+
+@pytest.mark.parametrize("d,norm", [(512, True), (256, False), (3840, True)])
+def test_pool_mean_matches_oracle(d, norm):
+    torch = _torch()
+    rng = np.random.default_rng([d, int(norm)])
+    lens = synth.draw_lens(synth.CONFIGS["c2"])[:7]
+    cu = synth.cu_seqlens(lens)
+    x = rng.standard_normal((int(cu[-1]), d)).astype(np.float32)
+    w = (1 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    out = torch.empty(len(lens), d, dtype=torch.float32, device="cuda")
+    te.pool_mean(to_dev(x), cu, to_dev(cu), to_dev(w) if norm else None, 1e-6, out)
+    ref = O.pool_mean(x, cu, w if norm else None, 1e-6)
+    assert rel_frob(to_np(out), ref) < 1e-5

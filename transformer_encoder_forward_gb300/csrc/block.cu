@@ -1,0 +1,174 @@
+// One pre-norm transformer encoder block as a fixed sequence of launches on
+// one stream (no host synchronisation, no allocation).
+//
+// Sources: "cortiq-engine 0.8.39 src/gpu_metal/egemma2.rs" TextGpu::forward
+// (per layer: q|k|v GEMM z=3 -> q/k norm + RoPE -> attention -> O GEMM ->
+// add_norm -> gate|up GEMM z=2 -> GELU-tanh gate -> down GEMM -> add_norm with
+// the next layer's input norm); "cortiq-engine 0.7.6 src/gpu_metal/zimage.rs"
+// Enc::block (the same chain with SwiGLU and the post-norm residual row op);
+// "cera 0.2.4 src/model/vision_encoder_gpu.rs" encode_image_gpu (plain
+// pre-norm block: LayerNorm, biased linears, x += proj, GELU MLP).
+//
+// Workspace layout (each region 256-byte aligned):
+//   qkv bf16 [t, (nq + 2 nkv) hd] | o bf16 [t, nq hd] | tmp f32 [t, d]
+//   | gu bf16 [t, (gated ? 2 : 1) F] | m bf16 [t, F]
+#include "common.cuh"
+
+namespace tefwd {
+namespace {
+
+inline size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct WsLayout {
+    size_t qkv, o, tmp, gu, m, total;
+};
+
+WsLayout ws_layout(const te_block_desc &d, int32_t t) {
+    WsLayout L;
+    const size_t T = (size_t)t;
+    const size_t qkvw = (size_t)(d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+    const size_t ow = (size_t)d.n_heads * d.head_dim;
+    size_t off = 0;
+    L.qkv = off; off = up256(off + T * qkvw * 2);
+    L.o = off;   off = up256(off + T * ow * 2);
+    L.tmp = off; off = up256(off + T * d.d * 4);
+    L.gu = off;  off = up256(off + T * (size_t)(d.gated ? 2 : 1) * d.ffn * 2);
+    L.m = off;   off = up256(off + T * (size_t)d.ffn * 2);
+    L.total = off;
+    return L;
+}
+
+te_status check_w(const te_q8w &w, int n, int k, const char *name) {
+    if (!w.q || !w.scale) return fail(TE_EINVAL, "block: weight %s has a NULL q or scale", name);
+    if (w.n != n || w.k != k)
+        return fail(TE_ESHAPE, "block: weight %s is [%d, %d], need [%d, %d]", name, w.n, w.k, n, k);
+    if (!aligned16(w.q) || (reinterpret_cast<uintptr_t>(w.scale) & 3) ||
+        (w.bias && (reinterpret_cast<uintptr_t>(w.bias) & 3)))
+        return fail(TE_EALIGN, "block: weight %s: q must be 16-byte, scale/bias 4-byte aligned", name);
+    return TE_OK;
+}
+
+te_status check_desc(const te_block_desc *d) {
+    if (!d) return fail(TE_EINVAL, "block: NULL descriptor");
+    if (d->head_dim != 64 && d->head_dim != 128) return fail(TE_ESHAPE, "block: head_dim=%d", d->head_dim);
+    if (d->n_heads < 1 || d->n_kv_heads < 1 || d->n_heads % d->n_kv_heads)
+        return fail(TE_ESHAPE, "block: heads %d / kv heads %d", d->n_heads, d->n_kv_heads);
+    if (d->d < 64 || d->d % 64 || d->d > 4096) return fail(TE_ESHAPE, "block: d=%d (multiple of 64, <= 4096)", d->d);
+    if (d->ffn < 64 || d->ffn % 64) return fail(TE_ESHAPE, "block: ffn=%d (multiple of 64)", d->ffn);
+    if (d->norm_kind != TE_NORM_RMS && d->norm_kind != TE_NORM_LN) return fail(TE_EINVAL, "block: norm_kind");
+    if (d->resid_form != TE_RESID_PLAIN && d->resid_form != TE_RESID_SANDWICH)
+        return fail(TE_EINVAL, "block: resid_form");
+    if (d->act != TE_ACT_GELU_TANH && d->act != TE_ACT_SILU) return fail(TE_EINVAL, "block: act");
+    if (d->window < 0) return fail(TE_EINVAL, "block: window < 0");
+    if (!d->ffn_norm_w) return fail(TE_EINVAL, "block: NULL ffn_norm_w");
+    if (d->resid_form == TE_RESID_SANDWICH && (!d->post_attn_w || !d->post_ffn_w))
+        return fail(TE_EINVAL, "block: sandwich form needs post_attn_w and post_ffn_w");
+    if ((d->q_norm == nullptr) != (d->k_norm == nullptr))
+        return fail(TE_EINVAL, "block: give both q_norm and k_norm or neither");
+    if (d->rope_sec && (!d->rope_cos || !d->rope_sin))
+        return fail(TE_EINVAL, "block: rope_sec set without tables");
+    const float *vecs[] = {d->ffn_norm_w, d->ffn_norm_b, d->post_attn_w, d->post_ffn_w,
+                           d->next_norm_w, d->next_norm_b, d->q_norm, d->k_norm};
+    for (const float *v : vecs)
+        if (v && !aligned16(v)) return fail(TE_EALIGN, "block: norm weights must be 16-byte aligned");
+    const int hd = d->head_dim, qw = d->n_heads * hd, kw = d->n_kv_heads * hd;
+    te_status st;
+    if ((st = check_w(d->wq, qw, d->d, "wq")) || (st = check_w(d->wk, kw, d->d, "wk")) ||
+        (st = check_w(d->wv, kw, d->d, "wv")) || (st = check_w(d->wo, d->d, qw, "wo")) ||
+        (st = check_w(d->wg, d->ffn, d->d, "wg")) || (st = check_w(d->wd, d->d, d->ffn, "wd")))
+        return st;
+    if (d->gated && (st = check_w(d->wu, d->ffn, d->d, "wu"))) return st;
+    return TE_OK;
+}
+
+}  // namespace
+}  // namespace tefwd
+
+using namespace tefwd;
+
+extern "C" size_t te_encoder_block_workspace(const te_block_desc *desc, int32_t t) {
+    if (!desc || t < 0) return 0;
+    return ws_layout(*desc, t).total;
+}
+
+extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, void *a,
+                                          const int32_t *cu_host, const int32_t *cu_dev,
+                                          int32_t nseq, void *workspace, size_t ws_bytes,
+                                          te_stream stream) {
+    te_status st = check_desc(desc);
+    if (st != TE_OK) return st;
+    const te_block_desc &d = *desc;
+    if (!x || !a || !workspace) return fail(TE_EINVAL, "block: NULL x, a or workspace");
+    int32_t t = 0, max_len = 0;
+    if ((st = check_cu(cu_host, cu_dev, nseq, &t, &max_len)) != TE_OK) return st;
+    if (d.rope_sec && !d.rope_pos && d.rope_rows < t)
+        return fail(TE_ESHAPE, "block: RoPE table has %d rows for %d packed rows", d.rope_rows, t);
+    const WsLayout L = ws_layout(d, t);
+    if (ws_bytes < L.total)
+        return fail(TE_EWORKSPACE, "block: workspace %zu bytes, need %zu", ws_bytes, L.total);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(TE_EALIGN, "block: workspace must be 256-byte aligned");
+    if (!aligned16(x) || !aligned16(a)) return fail(TE_EALIGN, "block: x and a must be 16-byte aligned");
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int hd = d.head_dim, H = d.n_heads, KV = d.n_kv_heads, D = d.d, F = d.ffn;
+    const int qw = H * hd, kw = KV * hd, ldqkv = qw + 2 * kw;
+    __nv_bfloat16 *qkv = reinterpret_cast<__nv_bfloat16 *>(ws + L.qkv);
+    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(ws + L.o);
+    float *tmp = reinterpret_cast<float *>(ws + L.tmp);
+    __nv_bfloat16 *gu = reinterpret_cast<__nv_bfloat16 *>(ws + L.gu);
+    __nv_bfloat16 *m = reinterpret_cast<__nv_bfloat16 *>(ws + L.m);
+    const int ldgu = (d.gated ? 2 : 1) * F;
+    const bool plain = d.resid_form == TE_RESID_PLAIN;
+
+    // 1. q|k|v projections, one grouped launch (z = 3)
+    te_q8_item it[3] = {};
+    it[0] = {d.wq, qkv, ldqkv, TE_BF16, 0, nullptr, 0};
+    it[1] = {d.wk, qkv + qw, ldqkv, TE_BF16, 0, nullptr, 0};
+    it[2] = {d.wv, qkv + qw + kw, ldqkv, TE_BF16, 0, nullptr, 0};
+    if ((st = te_q8_linear(a, D, t, D, it, 3, stream)) != TE_OK) return st;
+    // 2. q/k norm + RoPE in place
+    if (d.q_norm || d.rope_sec || d.q_mul != 1.f) {
+        if ((st = te_qk_prep_rope(qkv, ldqkv, 0, qw, H, KV, hd, d.q_norm, d.k_norm, d.eps, d.rope_cos,
+                                  d.rope_sin, d.rope_pos, d.rope_rows,
+                                  d.rope_sec, d.q_mul, t, stream)) != TE_OK)
+            return st;
+    }
+    // 3. attention
+    if ((st = te_attn_varlen_fwd(qkv, ldqkv, 0, qw, qw + kw, cu_host, cu_dev, nseq, H, KV, hd,
+                                 d.window, d.attn_scale, o, qw, stream)) != TE_OK)
+        return st;
+    // 4. O projection: plain form adds into x in the epilogue
+    te_q8_item io = plain ? te_q8_item{d.wo, x, D, TE_F32, 0, x, D}
+                          : te_q8_item{d.wo, tmp, D, TE_F32, 0, nullptr, 0};
+    if ((st = te_q8_linear(o, qw, t, qw, &io, 1, stream)) != TE_OK) return st;
+    // 5. residual + FFN pre-norm
+    if (plain)
+        st = te_rownorm(x, TE_F32, D, d.ffn_norm_w, d.ffn_norm_b, d.norm_kind, d.eps, 1.f, a, TE_BF16,
+                        D, t, D, stream);
+    else
+        st = te_add_norm(x, tmp, d.post_attn_w, d.post, d.ffn_norm_w, d.ffn_norm_b, d.norm_kind,
+                         d.eps, a, TE_BF16, t, D, stream);
+    if (st != TE_OK) return st;
+    // 6. gate|up (z = 2) or up
+    te_q8_item ig[2] = {};
+    ig[0] = {d.wg, gu, ldgu, TE_BF16, 0, nullptr, 0};
+    ig[1] = {d.wu, gu + F, ldgu, TE_BF16, 0, nullptr, 0};
+    if ((st = te_q8_linear(a, D, t, D, ig, d.gated ? 2 : 1, stream)) != TE_OK) return st;
+    // 7. gate activation
+    if ((st = te_gate_act(gu, ldgu, d.gated ? F : -1, d.act, m, F, t, F, stream)) != TE_OK) return st;
+    // 8. down projection
+    te_q8_item id = plain ? te_q8_item{d.wd, x, D, TE_F32, 0, x, D}
+                          : te_q8_item{d.wd, tmp, D, TE_F32, 0, nullptr, 0};
+    if ((st = te_q8_linear(m, F, t, F, &id, 1, stream)) != TE_OK) return st;
+    // 9. residual + the next block's pre-norm
+    if (plain) {
+        if (d.next_norm_w)
+            st = te_rownorm(x, TE_F32, D, d.next_norm_w, d.next_norm_b, d.norm_kind, d.eps, 1.f, a,
+                            TE_BF16, D, t, D, stream);
+    } else {
+        st = te_add_norm(x, tmp, d.post_ffn_w, d.post, d.next_norm_w, d.next_norm_b, d.norm_kind,
+                         d.eps, d.next_norm_w ? a : nullptr, TE_BF16, t, D, stream);
+    }
+    return st;
+}

@@ -1,0 +1,569 @@
+// Row operations of the encoder block: RMSNorm / LayerNorm, the residual add
+// fused with the next norm, q/k norm + RoPE, the gate activation and the
+// final-norm mean-pool.  Each is bound by HBM bandwidth: one warp owns a row
+// (or a (row, head) pair), reads it once with 16-byte vector loads, keeps it
+// in registers across the reductions and writes it once.
+//
+// Sources: "cortiq-engine 0.8.39 src/gpu_metal/egemma2.rs" (Prog::rms,
+// Prog::add_norm, Prog::gelu, Prog::qkv, TextGpu::forward final norm + pool),
+// "cortiq-engine 0.7.6 src/gpu_metal/zimage.rs" (Enc::rowop, Enc::block
+// qk-norm + RoPE and SwiGLU), "cera 0.2.4 src/model/vision_encoder_gpu.rs"
+// (VitGpuOps::layernorm / gelu / add).
+#include <stdarg.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace tefwd {
+
+// ------------------------------------------------------------ error reporting
+
+static thread_local char g_msg[512] = "";
+
+te_status fail(te_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+te_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(TE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+te_status check_cu(const int32_t *cu_host, const int32_t *cu_dev, int32_t nseq, int32_t *total,
+                   int32_t *max_len) {
+    if (!cu_host || !cu_dev) return fail(TE_EINVAL, "cu_seqlens: NULL host or device array");
+    if (nseq < 1) return fail(TE_EINVAL, "cu_seqlens: nseq = %d, need >= 1", nseq);
+    if ((reinterpret_cast<uintptr_t>(cu_dev) & 3u) != 0)
+        return fail(TE_EALIGN, "cu_seqlens: device array not 4-byte aligned");
+    if (cu_host[0] != 0) return fail(TE_EINVAL, "cu_seqlens: cu[0] = %d, need 0", cu_host[0]);
+    int32_t mx = 0;
+    for (int32_t s = 0; s < nseq; ++s) {
+        const int64_t len = (int64_t)cu_host[s + 1] - cu_host[s];
+        if (len < 1)
+            return fail(TE_EINVAL, "cu_seqlens: sequence %d has length %lld (need >= 1)", s,
+                        (long long)len);
+        if (len > mx) mx = (int32_t)len;
+    }
+    *total = cu_host[nseq];
+    *max_len = mx;
+    return TE_OK;
+}
+
+__device__ int g_rowop_err;
+
+// --------------------------------------------------------------- vector I/O
+
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0];
+    const float4 b = reinterpret_cast<const float4 *>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+    v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
+    uint4 u;
+    u.x = pack_bf16x2(v[0], v[1]); u.y = pack_bf16x2(v[2], v[3]);
+    u.z = pack_bf16x2(v[4], v[5]); u.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4 *>(p) = u;
+}
+
+// Normalises the warp's row held in v (NV chunks of 8 per lane, chunk i of
+// lane l covers columns (i*32 + l)*8 ...) and writes w*v (+b) to y.
+template <typename Tout, int NV>
+__device__ __forceinline__ void norm_store(float (&v)[NV][8], int lane, int d, int kind, float eps,
+                                           const float *w, const float *b, Tout *y) {
+    float inv, mean = 0.f;
+    if (kind == TE_NORM_LN) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if ((i * 32 + lane) * 8 < d)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s += v[i][e];
+        mean = warp_sum(s) / (float)d;
+        float q = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if ((i * 32 + lane) * 8 < d)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q += (v[i][e] - mean) * (v[i][e] - mean);
+        inv = rsqrtf(warp_sum(q) / (float)d + eps);
+    } else {
+        float q = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if ((i * 32 + lane) * 8 < d)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q += v[i][e] * v[i][e];
+        inv = rsqrtf(warp_sum(q) / (float)d + eps);
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = (i * 32 + lane) * 8;
+        if (c < d) {
+            float wv[8], o[8];
+            load8(w + c, wv);
+            if (b) {
+                float bv[8];
+                load8(b + c, bv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = (v[i][e] - mean) * inv * wv[e] + bv[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = (v[i][e] - mean) * inv * wv[e];
+            }
+            store8(y + c, o);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ rownorm
+
+template <typename Tin, typename Tout, int NV>
+__global__ void __launch_bounds__(256) rownorm_kernel(const Tin *__restrict__ x, long long ldx,
+                                                      const float *__restrict__ w,
+                                                      const float *__restrict__ b, int kind,
+                                                      float eps, float pre, Tout *y, long long ldy,
+                                                      int t, int d) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= t) return;
+    float v[NV][8];
+    const Tin *xr = x + (long long)row * ldx;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = (i * 32 + lane) * 8;
+        if (c < d) {
+            load8(xr + c, v[i]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[i][e] *= pre;
+        }
+    }
+    norm_store<Tout, NV>(v, lane, d, kind, eps, w, kind == TE_NORM_LN ? b : nullptr,
+                         y + (long long)row * ldy);
+}
+
+// ----------------------------------------------------------------- add_norm
+
+template <typename Tout, int NV>
+__global__ void __launch_bounds__(256) add_norm_kernel(float *h, const float *__restrict__ t,
+                                                       const float *__restrict__ w_post,
+                                                       float post, const float *__restrict__ w_next,
+                                                       const float *__restrict__ b_next, int kind,
+                                                       float eps, Tout *a, int rows, int d) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float v[NV][8];
+    float *hr = h + (long long)row * d;
+    const float *tr = t ? t + (long long)row * d : nullptr;
+    if (tr) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = (i * 32 + lane) * 8;
+            if (c < d) load8(tr + c, v[i]);
+        }
+    }
+    float inv_t = 1.f;
+    if (tr && w_post) {
+        float q = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if ((i * 32 + lane) * 8 < d)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q += v[i][e] * v[i][e];
+        inv_t = rsqrtf(warp_sum(q) / (float)d + eps);
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = (i * 32 + lane) * 8;
+        if (c < d) {
+            float hv[8];
+            load8(hr + c, hv);
+            if (tr && w_post) {
+                float wv[8];
+                load8(w_post + c, wv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] = (hv[e] + v[i][e] * inv_t * wv[e]) * post;
+            } else if (tr) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] = hv[e] + v[i][e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] = hv[e];
+            }
+            if (tr) store8(hr + c, v[i]);
+        }
+    }
+    if (w_next)
+        norm_store<Tout, NV>(v, lane, d, kind, eps, w_next, kind == TE_NORM_LN ? b_next : nullptr,
+                             a + (long long)row * d);
+}
+
+// ------------------------------------------------------------- qk prep + RoPE
+
+template <int HD>
+__global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long long ld, int q_off,
+                                                      int k_off, int nq, int nkv,
+                                                      const float *__restrict__ qn,
+                                                      const float *__restrict__ kn, float eps,
+                                                      const float *__restrict__ cosb,
+                                                      const float *__restrict__ sinb,
+                                                      const int *__restrict__ pos, int table_rows,
+                                                      int sec, float q_mul, int rows) {
+    constexpr int EPL = HD / 32;   // elements per lane: 2 or 4
+    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int nh = nq + nkv;
+    const long long row = gw / nh;
+    const int hh = (int)(gw % nh);
+    if (row >= rows) return;
+    const bool isq = hh < nq;
+    __nv_bfloat16 *p = qkv + row * ld + (isq ? q_off + hh * HD : k_off + (hh - nq) * HD) + lane * EPL;
+    float v[EPL];
+    if constexpr (EPL == 2) {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        v[0] = bf16_lo(u); v[1] = bf16_hi(u);
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
+        v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+    }
+    const float *nw = isq ? qn : kn;
+    if (nw) {
+        float q = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) q += v[e] * v[e];
+        const float inv = rsqrtf(warp_sum(q) / (float)HD + eps);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) v[e] = v[e] * inv * nw[lane * EPL + e];
+    }
+    if (sec) {
+        long long prow = pos ? pos[row] : row;
+        if (prow < 0 || prow >= table_rows) {
+            atomicExch(&g_rowop_err, 2);
+            prow = 0;
+        }
+        const int half = sec >> 1;
+        const int xr = half / EPL;   // lane distance to the partner element
+        const float *cr = cosb + prow * (HD / 2);
+        const float *sr = sinb + prow * (HD / 2);
+        float o[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const float partner = __shfl_xor_sync(0xFFFFFFFFu, v[e], xr);
+            const int idx = lane * EPL + e;
+            const int sct = idx / sec;
+            const int i = idx - sct * sec;
+            const bool first = i < half;
+            const int tc = sct * half + (first ? i : i - half);
+            const float c = cr[tc], s = sr[tc];
+            o[e] = first ? v[e] * c - partner * s : v[e] * c + partner * s;
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) v[e] = o[e];
+    }
+    if (isq) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) v[e] *= q_mul;
+    }
+    if constexpr (EPL == 2) {
+        *reinterpret_cast<uint32_t *>(p) = pack_bf16x2(v[0], v[1]);
+    } else {
+        uint2 u;
+        u.x = pack_bf16x2(v[0], v[1]);
+        u.y = pack_bf16x2(v[2], v[3]);
+        *reinterpret_cast<uint2 *>(p) = u;
+    }
+}
+
+// ---------------------------------------------------------------- gate_act
+
+__device__ __forceinline__ float act_fn(float g, int act) {
+    if (act == TE_ACT_GELU_TANH)
+        return 0.5f * g * (1.f + tanhf(0.7978845608028654f * (g + 0.044715f * g * g * g)));
+    return g / (1.f + expf(-g));
+}
+
+__global__ void __launch_bounds__(256) gate_act_kernel(const __nv_bfloat16 *__restrict__ gu,
+                                                       long long ld, int u_off, int act,
+                                                       __nv_bfloat16 *__restrict__ m,
+                                                       long long ldm, int rows, int f) {
+    const int per_row = f >> 3;
+    const long long total = (long long)rows * per_row;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long row = idx / per_row;
+        const int c = (int)(idx - row * per_row) * 8;
+        float g[8], o[8];
+        load8(gu + row * ld + c, g);
+        if (u_off >= 0) {
+            float u[8];
+            load8(gu + row * ld + u_off + c, u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = act_fn(g[e], act) * u[e];
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = act_fn(g[e], act);
+        }
+        store8(m + row * ldm + c, o);
+    }
+}
+
+// --------------------------------------------------------------- pool_mean
+
+// One CTA per sequence; 8 warps take rows round-robin, each keeps column
+// partial sums in registers; the partials are combined in a fixed order, so
+// the result does not depend on scheduling.
+template <int NV>
+__global__ void __launch_bounds__(256) pool_kernel(const float *__restrict__ x, int d,
+                                                   const int *__restrict__ cu,
+                                                   const float *__restrict__ w, float eps,
+                                                   float *__restrict__ out) {
+    extern __shared__ float part[];   // [d]
+    const int s = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = cu[s], r1 = cu[s + 1];
+    float acc[NV][8];
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+    for (int r = r0 + warp; r < r1; r += 8) {
+        const float *xr = x + (long long)r * d;
+        float inv = 1.f;
+        if (w) {   // first pass: the row's RMS (the second pass re-reads it from L1)
+            float q = 0.f;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int c = (i * 32 + lane) * 8;
+                if (c < d) {
+                    float v[8];
+                    load8(xr + c, v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q += v[e] * v[e];
+                }
+            }
+            inv = rsqrtf(warp_sum(q) / (float)d + eps);
+        }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = (i * 32 + lane) * 8;
+            if (c < d) {
+                float v[8];
+                load8(xr + c, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[i][e] += v[e] * inv;
+            }
+        }
+    }
+    for (int ww = 0; ww < 8; ++ww) {
+        if (warp == ww) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int c = (i * 32 + lane) * 8;
+                if (c < d)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) part[c + e] = (ww ? part[c + e] : 0.f) + acc[i][e];
+            }
+        }
+        __syncthreads();
+    }
+    const float scale = 1.f / (float)(r1 - r0);
+    for (int c = threadIdx.x; c < d; c += blockDim.x)
+        out[(long long)s * d + c] = part[c] * scale * (w ? w[c] : 1.f);
+}
+
+// --------------------------------------------------------------- dispatch
+
+static int nv_for(int d) {
+    const int chunks = (d + 255) / 256;   // per-lane chunks of 8
+    if (chunks <= 1) return 1;
+    if (chunks <= 2) return 2;
+    if (chunks <= 4) return 4;
+    if (chunks <= 8) return 8;
+    return 16;
+}
+
+#define TE_NV_SWITCH(nv, ...)                       \
+    switch (nv) {                                   \
+    case 1: { constexpr int NV = 1; __VA_ARGS__; } break;   \
+    case 2: { constexpr int NV = 2; __VA_ARGS__; } break;   \
+    case 4: { constexpr int NV = 4; __VA_ARGS__; } break;   \
+    case 8: { constexpr int NV = 8; __VA_ARGS__; } break;   \
+    default: { constexpr int NV = 16; __VA_ARGS__; } break; \
+    }
+
+static te_status launched(const char *what) {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TE_OK : cuda_fail(e, what);
+}
+
+static bool dtype_ok(int32_t dt) { return dt == TE_F32 || dt == TE_BF16; }
+
+}  // namespace tefwd
+
+using namespace tefwd;
+
+extern "C" {
+
+te_status te_rownorm(const void *x, int32_t xdt, int64_t ldx, const float *w, const float *b,
+                     int32_t kind, float eps, float pre, void *y, int32_t ydt, int64_t ldy,
+                     int32_t t, int32_t d, te_stream stream) {
+    if (!x || !w || !y) return fail(TE_EINVAL, "rownorm: NULL x, w or y");
+    if (!dtype_ok(xdt) || !dtype_ok(ydt)) return fail(TE_EINVAL, "rownorm: bad dtype");
+    if (kind != TE_NORM_RMS && kind != TE_NORM_LN) return fail(TE_EINVAL, "rownorm: bad kind");
+    if (t < 0 || d < 8 || d > 4096 || d % 8) return fail(TE_ESHAPE, "rownorm: t=%d d=%d (d %% 8 == 0, 8..4096)", t, d);
+    if (ldx < d || ldy < d) return fail(TE_ESHAPE, "rownorm: leading dimension below d");
+    if (!aligned16(x) || !aligned16(y) || !aligned16(w) || (b && !aligned16(b)) ||
+        (ldx * (xdt == TE_F32 ? 4 : 2)) % 16 || (ldy * (ydt == TE_F32 ? 4 : 2)) % 16)
+        return fail(TE_EALIGN, "rownorm: pointers and rows must be 16-byte aligned");
+    if (x == y && (xdt != ydt || ldx != ldy))
+        return fail(TE_EINVAL, "rownorm: in place needs equal dtype and leading dimension");
+    if (t == 0) return TE_OK;
+    const dim3 grid((t + 7) / 8);
+    TE_NV_SWITCH(nv_for(d), {
+        if (xdt == TE_F32 && ydt == TE_BF16)
+            rownorm_kernel<float, __nv_bfloat16, NV><<<grid, 256, 0, stream>>>(
+                (const float *)x, ldx, w, b, kind, eps, pre, (__nv_bfloat16 *)y, ldy, t, d);
+        else if (xdt == TE_F32 && ydt == TE_F32)
+            rownorm_kernel<float, float, NV><<<grid, 256, 0, stream>>>(
+                (const float *)x, ldx, w, b, kind, eps, pre, (float *)y, ldy, t, d);
+        else if (xdt == TE_BF16 && ydt == TE_BF16)
+            rownorm_kernel<__nv_bfloat16, __nv_bfloat16, NV><<<grid, 256, 0, stream>>>(
+                (const __nv_bfloat16 *)x, ldx, w, b, kind, eps, pre, (__nv_bfloat16 *)y, ldy, t, d);
+        else
+            rownorm_kernel<__nv_bfloat16, float, NV><<<grid, 256, 0, stream>>>(
+                (const __nv_bfloat16 *)x, ldx, w, b, kind, eps, pre, (float *)y, ldy, t, d);
+    })
+    return launched("rownorm launch");
+}
+
+te_status te_add_norm(float *h, const float *t, const float *w_post, float post,
+                      const float *w_next, const float *b_next, int32_t kind, float eps, void *a,
+                      int32_t adt, int32_t rows, int32_t d, te_stream stream) {
+    if (!h) return fail(TE_EINVAL, "add_norm: NULL h");
+    if (w_post && !t) return fail(TE_EINVAL, "add_norm: w_post given without t");
+    if (w_next && !a) return fail(TE_EINVAL, "add_norm: w_next given without a");
+    if (w_next && !dtype_ok(adt)) return fail(TE_EINVAL, "add_norm: bad dtype");
+    if (kind != TE_NORM_RMS && kind != TE_NORM_LN) return fail(TE_EINVAL, "add_norm: bad kind");
+    if (rows < 0 || d < 8 || d > 4096 || d % 8) return fail(TE_ESHAPE, "add_norm: rows=%d d=%d (d %% 8 == 0, 8..4096)", rows, d);
+    if (!aligned16(h) || (t && !aligned16(t)) || (w_post && !aligned16(w_post)) ||
+        (w_next && !aligned16(w_next)) || (b_next && !aligned16(b_next)) || (a && !aligned16(a)))
+        return fail(TE_EALIGN, "add_norm: pointers must be 16-byte aligned");
+    if (rows == 0) return TE_OK;
+    const dim3 grid((rows + 7) / 8);
+    TE_NV_SWITCH(nv_for(d), {
+        if (adt == TE_F32)
+            add_norm_kernel<float, NV><<<grid, 256, 0, stream>>>(h, t, w_post, post, w_next, b_next,
+                                                                 kind, eps, (float *)a, rows, d);
+        else
+            add_norm_kernel<__nv_bfloat16, NV><<<grid, 256, 0, stream>>>(
+                h, t, w_post, post, w_next, b_next, kind, eps, (__nv_bfloat16 *)a, rows, d);
+    })
+    return launched("add_norm launch");
+}
+
+te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t nq,
+                          int32_t nkv, int32_t hd, const float *qn, const float *kn, float eps,
+                          const float *cos, const float *sin, const int32_t *pos,
+                          int32_t table_rows, int32_t sec, float q_mul, int32_t rows,
+                          te_stream stream) {
+    if (!qkv) return fail(TE_EINVAL, "qk_prep_rope: NULL qkv");
+    if (hd != 64 && hd != 128) return fail(TE_ESHAPE, "qk_prep_rope: hd=%d (64 or 128)", hd);
+    if (nq < 0 || nkv < 0 || rows < 0 || q_off < 0 || k_off < 0)
+        return fail(TE_ESHAPE, "qk_prep_rope: negative size or offset");
+    if ((int64_t)q_off + (int64_t)nq * hd > ld || (int64_t)k_off + (int64_t)nkv * hd > ld)
+        return fail(TE_ESHAPE, "qk_prep_rope: heads run past the row (ld=%lld)", (long long)ld);
+    if (sec != 0 && sec != hd && sec != hd / 2)
+        return fail(TE_ESHAPE, "qk_prep_rope: sec=%d (0, hd or hd/2)", sec);
+    if (sec && (!cos || !sin || table_rows < 1))
+        return fail(TE_EINVAL, "qk_prep_rope: RoPE needs cos, sin and table_rows >= 1");
+    if (sec && !pos && table_rows < rows)
+        return fail(TE_ESHAPE, "qk_prep_rope: table has %d rows, need %d (pos == NULL)", table_rows, rows);
+    if (!aligned16(qkv) || (ld * 2) % 16 || (q_off * 2) % 8 || (k_off * 2) % 8)
+        return fail(TE_EALIGN, "qk_prep_rope: qkv rows must be 16-byte aligned, offsets 8-byte");
+    const long long warps = (long long)rows * (nq + nkv);
+    if (warps == 0) return TE_OK;
+    const dim3 grid((unsigned)((warps + 7) / 8));
+    if (hd == 64)
+        qk_prep_kernel<64><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, nq,
+                                                     nkv, qn, kn, eps, cos, sin, pos, table_rows,
+                                                     sec, q_mul, rows);
+    else
+        qk_prep_kernel<128><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, nq,
+                                                      nkv, qn, kn, eps, cos, sin, pos, table_rows,
+                                                      sec, q_mul, rows);
+    return launched("qk_prep_rope launch");
+}
+
+te_status te_gate_act(const void *gu, int64_t ld, int32_t u_off, int32_t act, void *m,
+                      int64_t ldm, int32_t rows, int32_t f, te_stream stream) {
+    if (!gu || !m) return fail(TE_EINVAL, "gate_act: NULL gu or m");
+    if (act != TE_ACT_GELU_TANH && act != TE_ACT_SILU) return fail(TE_EINVAL, "gate_act: bad act");
+    if (rows < 0 || f < 8 || f % 8) return fail(TE_ESHAPE, "gate_act: rows=%d f=%d (f %% 8 == 0)", rows, f);
+    if (ld < f || (u_off >= 0 && (int64_t)u_off + f > ld) || ldm < f)
+        return fail(TE_ESHAPE, "gate_act: columns run past the row");
+    if (!aligned16(gu) || !aligned16(m) || (ld * 2) % 16 || (ldm * 2) % 16 ||
+        (u_off >= 0 && (u_off * 2) % 16))
+        return fail(TE_EALIGN, "gate_act: rows and u_off must be 16-byte aligned");
+    if (rows == 0) return TE_OK;
+    const long long total = (long long)rows * (f / 8);
+    const long long want = (total + 255) / 256;
+    const unsigned blocks = (unsigned)(want < 152 * 16 ? want : 152 * 16);
+    gate_act_kernel<<<blocks, 256, 0, stream>>>((const __nv_bfloat16 *)gu, ld, u_off, act,
+                                                (__nv_bfloat16 *)m, ldm, rows, f);
+    return launched("gate_act launch");
+}
+
+te_status te_pool_mean(const float *x, int32_t d, const int32_t *cu_host, const int32_t *cu_dev,
+                       int32_t nseq, const float *w_final, float eps, float *out,
+                       te_stream stream) {
+    if (!x || !out) return fail(TE_EINVAL, "pool_mean: NULL x or out");
+    if (d < 8 || d > 4096 || d % 8) return fail(TE_ESHAPE, "pool_mean: d=%d (d %% 8 == 0, 8..4096)", d);
+    int32_t total = 0, mx = 0;
+    te_status st = check_cu(cu_host, cu_dev, nseq, &total, &mx);
+    if (st != TE_OK) return st;
+    if (!aligned16(x) || !aligned16(out) || (w_final && !aligned16(w_final)))
+        return fail(TE_EALIGN, "pool_mean: pointers must be 16-byte aligned");
+    TE_NV_SWITCH(nv_for(d), {
+        pool_kernel<NV><<<nseq, 256, d * sizeof(float), stream>>>(x, d, cu_dev, w_final, eps, out);
+    })
+    return launched("pool_mean launch");
+}
+
+te_status te_check(te_stream stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "te_check: stream");
+    int rowop = 0;
+    e = cudaMemcpyFromSymbol(&rowop, g_rowop_err, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "te_check: read error word");
+    if (rowop) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_rowop_err, &zero, sizeof(int));
+    }
+    const int gemm = read_clear_gemm_error();
+    const int attn = read_clear_attn_error();
+    if (gemm < 0 || attn < 0) return fail(TE_ECUDA, "te_check: could not read device error words");
+    if (rowop || gemm || attn)
+        return fail(TE_EDEVICE, "device error words: rowops=%d gemm=%d attn=%d "
+                    "(2 = RoPE table index out of range, 1 = bounded wait gave up)", rowop, gemm, attn);
+    return TE_OK;
+}
+
+const char *te_last_error(void) { return g_msg; }
+
+const char *te_version(void) { return "tefwd 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

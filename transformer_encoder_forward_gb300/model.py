@@ -1,0 +1,137 @@
+"""An encoder stack driven through the C-ABI: device copies of the weights,
+one te_block_desc per layer, and the forward loop.
+
+Marshalling only: the initial pre-norm, every block and the final pool are
+calls into libtefwd.  The stack follows "cortiq-engine 0.8.39
+src/gpu_metal/egemma2.rs" TextGpu::forward (an input norm, then the layers,
+each ending with the next layer's input norm, then the final norm and
+mean-pool) and "cera 0.2.4 src/model/vision_encoder_gpu.rs"
+encode_image_gpu (plain pre-norm blocks).
+"""
+from __future__ import annotations
+
+from typing import List, Optional
+
+import numpy as np
+
+from . import (TE_ACT_GELU_TANH, TE_ACT_SILU, TE_NORM_LN, TE_NORM_RMS, TE_RESID_PLAIN,
+               TE_RESID_SANDWICH, block_workspace, encoder_block_fwd, pool_mean, q8w, rownorm,
+               te_block_desc)
+
+
+def _dev(a, device, dtype=None):
+    import torch
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+class LayerWeights:
+    """Device tensors of one layer (q8 weights, scales, biases, norm vectors)."""
+
+    def __init__(self, cfg, p: dict, device):
+        import torch
+        self.t = {}
+        for key in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+            w = p.get(key)
+            if w is None:
+                self.t[key] = None
+                continue
+            self.t[key] = (_dev(w["q"], device), _dev(w["s"], device), _dev(w["b"], device))
+        for key in ("norm1_w", "norm1_b", "norm2_w", "norm2_b", "post_attn_w", "post_ffn_w",
+                    "q_norm", "k_norm"):
+            self.t[key] = _dev(p.get(key), device, torch.float32)
+
+
+class EncoderStack:
+    """A stack of encoder blocks over a packed batch with fixed lengths."""
+
+    def __init__(self, cfg, layers: List[dict], lens, tables: dict,
+                 final_norm: Optional[np.ndarray] = None, device="cuda"):
+        import torch
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.lens = np.asarray(lens, dtype=np.int32)
+        cu = np.zeros(len(lens) + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(self.lens)
+        self.cu_host = cu
+        self.cu_dev = torch.from_numpy(cu).to(self.device)
+        self.T = int(cu[-1])
+        self.layers = [LayerWeights(cfg, p, self.device) for p in layers]
+        self.final_norm = _dev(final_norm, self.device, torch.float32)
+        self.rope_cos = _dev(tables.get("cos"), self.device, torch.float32)
+        self.rope_sin = _dev(tables.get("sin"), self.device, torch.float32)
+        self.rope_pos = _dev(tables.get("pos"), self.device, torch.int32)
+        self.rope_sec = int(tables.get("sec") or 0)
+        self.descs = [self._desc(i) for i in range(len(self.layers))]
+        ws = max(block_workspace(d, self.T) for d in self.descs)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
+
+    def _desc(self, i: int) -> te_block_desc:
+        cfg, L = self.cfg, self.layers[i]
+        nxt = self.layers[i + 1] if i + 1 < len(self.layers) else None
+        ptr = lambda t: t.data_ptr() if t is not None else None
+        d = te_block_desc()
+        d.d, d.n_heads, d.n_kv_heads, d.head_dim, d.ffn = cfg.d, cfg.heads, cfg.kv_heads, cfg.hd, cfg.ffn
+        d.norm_kind = TE_NORM_LN if cfg.norm == "ln" else TE_NORM_RMS
+        d.resid_form = TE_RESID_SANDWICH if cfg.form == "sandwich" else TE_RESID_PLAIN
+        d.act = TE_ACT_SILU if cfg.act == "silu" else TE_ACT_GELU_TANH
+        d.gated = 1 if cfg.gated else 0
+        d.window = cfg.window_of(i)
+        d.eps, d.attn_scale, d.post, d.q_mul = cfg.eps, cfg.scale, cfg.post, 1.0
+        for key in ("wq", "wk", "wv", "wo", "wg", "wd"):
+            setattr(d, key, q8w(*L.t[key]))
+        if L.t["wu"] is not None:
+            d.wu = q8w(*L.t["wu"])
+        d.ffn_norm_w, d.ffn_norm_b = ptr(L.t["norm2_w"]), ptr(L.t["norm2_b"])
+        d.post_attn_w, d.post_ffn_w = ptr(L.t["post_attn_w"]), ptr(L.t["post_ffn_w"])
+        if nxt is not None:
+            d.next_norm_w, d.next_norm_b = ptr(nxt.t["norm1_w"]), ptr(nxt.t["norm1_b"])
+        if cfg.qk_norm:
+            d.q_norm, d.k_norm = ptr(L.t["q_norm"]), ptr(L.t["k_norm"])
+        if self.rope_sec:
+            d.rope_cos, d.rope_sin = ptr(self.rope_cos), ptr(self.rope_sin)
+            d.rope_pos, d.rope_sec = ptr(self.rope_pos), self.rope_sec
+            d.rope_rows = self.rope_cos.shape[0]
+        return d
+
+    # ------------------------------------------------------------ forward
+
+    def buffers(self):
+        import torch
+        x = torch.empty(self.T, self.cfg.d, dtype=torch.float32, device=self.device)
+        a = torch.empty(self.T, self.cfg.d, dtype=torch.bfloat16, device=self.device)
+        out = torch.empty(len(self.lens), self.cfg.d, dtype=torch.float32, device=self.device)
+        return x, a, out
+
+    def input_norm(self, x, a, stream=None):
+        L0 = self.layers[0]
+        kind = TE_NORM_LN if self.cfg.norm == "ln" else TE_NORM_RMS
+        rownorm(x, L0.t["norm1_w"], L0.t["norm1_b"], kind, self.cfg.eps, a, stream=stream)
+
+    def forward_device(self, x, a, out=None, layers=None, stream=None):
+        """In place on the device: x (f32 [T, d]) goes through every layer;
+        a ends as the last block's FFN input; out (f32 [nseq, d]) receives
+        the final-normed mean-pool when the stack pools."""
+        self.input_norm(x, a, stream)
+        n = len(self.layers) if layers is None else layers
+        for i in range(n):
+            encoder_block_fwd(self.descs[i], x, a, self.cu_host, self.cu_dev, self.workspace,
+                              stream=stream)
+        if out is not None and self.cfg.pool:
+            pool_mean(x, self.cu_host, self.cu_dev, self.final_norm, self.cfg.eps, out,
+                      stream=stream)
+
+    def forward_host(self, x_host, result_host, x=None, a=None, out=None, stream=None):
+        """End to end from pinned host memory: copies the input rows in, runs
+        the stack and copies the result (the pooled rows, else x) back."""
+        if x is None:
+            x, a, out = self.buffers()
+        x.copy_(x_host, non_blocking=True)
+        self.forward_device(x, a, out, stream=stream)
+        src = out if self.cfg.pool else x
+        result_host.copy_(src, non_blocking=True)
+        return result_host
