@@ -18,6 +18,8 @@
  * Conventions shared by every entry point
  *   - Memory is owned by the caller.  The library never allocates, frees or
  *     synchronises (te_check excepted); scratch is passed in as a workspace.
+ *     The one exception is te_encoder_block_fwd_static, which uses a fixed
+ *     array of the library's own (see its comment).
  *   - Device pointers are CUDA device addresses on the current device; host
  *     pointers (the *_host arguments and descriptors) are read during the
  *     call only.  Every device pointer must be 16-byte aligned and every
@@ -29,8 +31,9 @@
  *     with a message in te_last_error() (thread-local).  Errors from earlier
  *     asynchronous work surface as TE_ECUDA from te_check().
  *   - Work is enqueued on `stream` (NULL = the legacy default stream); the
- *     calls return before it completes.  Every call is capturable in a CUDA
- *     graph (no host synchronisation, no allocation).
+ *     calls return before it completes.  te_q8_linear, te_attn_varlen_fwd,
+ *     the row ops and te_encoder_block_fwd are capturable in a CUDA graph
+ *     (no host synchronisation, no allocation).
  */
 #ifndef TEFWD_H
 #define TEFWD_H
@@ -124,7 +127,7 @@ te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t
  *   LN : (v - mean) / sqrt(var + eps) * w + b      ([VIT] VitGpuOps::layernorm;
  *        biased variance, b may be NULL)
  * x [t, ldx] of xdt (f32/bf16), y [t, ldy] of ydt; may not overlap unless
- * identical with equal dtypes.  d % 8 == 0, 8 <= d <= 8192. */
+ * identical with equal dtypes.  d % 8 == 0, 8 <= d <= 4096. */
 te_status te_rownorm(const void *x, int32_t xdt, int64_t ldx, const float *w, const float *b,
                      int32_t kind, float eps, float pre, void *y, int32_t ydt, int64_t ldy,
                      int32_t t, int32_t d, te_stream stream);
@@ -135,7 +138,7 @@ te_status te_rownorm(const void *x, int32_t xdt, int64_t ldx, const float *w, co
  *                                                            [ZI] Enc::rowop post mode)
  *     w_post == NULL:  h = h + t      (t may be NULL: no add)
  *   then, when w_next != NULL:  a = Norm(h) * w_next (+ b_next), kind RMS/LN,
- *   stored as adt in a [rows, d].  d % 8 == 0, 8 <= d <= 8192. */
+ *   stored as adt in a [rows, d].  d % 8 == 0, 8 <= d <= 4096. */
 te_status te_add_norm(float *h, const float *t, const float *w_post, float post,
                       const float *w_next, const float *b_next, int32_t kind, float eps,
                       void *a, int32_t adt, int32_t rows, int32_t d, te_stream stream);
@@ -168,7 +171,7 @@ te_status te_gate_act(const void *gu, int64_t ld, int32_t u_off, int32_t act, vo
 /* pool_mean: out[s] = (1/len_s) sum_{r in s} RMS(x_r) * w_final
  * (w_final == NULL: the plain mean).  x f32 [T, d], out f32 [nseq, d].
  * Cites [EG2] TextGpu::forward (row_inv then pool: final-normed hidden
- * state mean-pooled per sequence).  d % 8 == 0, d <= 8192. */
+ * state mean-pooled per sequence).  d % 8 == 0, d <= 4096. */
 te_status te_pool_mean(const float *x, int32_t d, const int32_t *cu_host,
                        const int32_t *cu_dev, int32_t nseq, const float *w_final, float eps,
                        float *out, te_stream stream);
@@ -209,6 +212,31 @@ size_t te_encoder_block_workspace(const te_block_desc *desc, int32_t t);
 te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, void *a,
                                const int32_t *cu_host, const int32_t *cu_dev, int32_t nseq,
                                void *workspace, size_t ws_bytes, te_stream stream);
+
+/* te_encoder_block_fwd_static: the same block as te_encoder_block_fwd, with
+ * the same arguments and results, for callers that cannot allocate device
+ * memory - e.g. an application whose device memory is all handed to its own
+ * allocator and which forbids libraries from calling cudaMalloc, or a
+ * latency-critical loop where no allocation may happen.  Such a caller has
+ * no workspace to pass, so this entry point takes none: its scratch is one
+ * fixed array in device memory owned by the library (32 MiB, 256-byte
+ * aligned), which every GPU that loads the library holds until the process
+ * exits.  Nothing is allocated or freed by a call.
+ *   - Limit: te_encoder_block_workspace(desc, t) must be <= 32 MiB (about
+ *     1,800 packed rows for a d=512, F=2048 block); larger t returns
+ *     TE_EWORKSPACE before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     with that device current; make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array, which keeps the last call's contents.
+ *     No part of it needs to start at zero (each scratch region is written
+ *     before it is read).  Calls that overlap on the GPU - on different
+ *     streams or from different host threads - race on the array: issue them
+ *     on one stream.
+ * The pages have no counterpart of this entry point. */
+te_status te_encoder_block_fwd_static(const te_block_desc *desc, float *x, void *a,
+                                      const int32_t *cu_host, const int32_t *cu_dev,
+                                      int32_t nseq, te_stream stream);
 
 /* Synchronises `stream`; returns TE_ECUDA for a pending asynchronous CUDA
  * error, TE_EDEVICE if a kernel gave up a bounded wait since the last check

@@ -72,6 +72,8 @@ EXPORTS = {
     "te_encoder_block_workspace": (ctypes.c_size_t, [ctypes.POINTER(te_block_desc), c_i32]),
     "te_encoder_block_fwd": (ctypes.c_int, [ctypes.POINTER(te_block_desc), c_p, c_p, c_p, c_p, c_i32,
                                             c_p, ctypes.c_size_t, c_p]),
+    "te_encoder_block_fwd_static": (ctypes.c_int, [ctypes.POINTER(te_block_desc), c_p, c_p, c_p,
+                                                   c_p, c_i32, c_p]),
     "te_check": (ctypes.c_int, [c_p]),
     "te_last_error": (ctypes.c_char_p, []),
     "te_version": (ctypes.c_char_p, []),
@@ -199,6 +201,14 @@ def encoder_block_fwd(desc: te_block_desc, x, a, cu_host, cu_dev, workspace, str
     _ok(lib().te_encoder_block_fwd(ctypes.byref(desc), x.data_ptr(), a.data_ptr(), hp,
                                    cu_dev.data_ptr(), len(arr) - 1, workspace.data_ptr(),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def encoder_block_fwd_static(desc: te_block_desc, x, a, cu_host, cu_dev, stream=None):
+    """The block with the library's fixed scratch array instead of a
+    workspace (for callers that cannot allocate device memory)."""
+    arr, hp = _host_i32(cu_host)
+    _ok(lib().te_encoder_block_fwd_static(ctypes.byref(desc), x.data_ptr(), a.data_ptr(), hp,
+                                          cu_dev.data_ptr(), len(arr) - 1, _stream(stream)))
 
 
 def check(stream=None):
