@@ -171,75 +171,165 @@ def build_stack(key, device):
 
 # --------------------------------------------------------------- GPU timing
 
-def time_kernels(cfg, st, torch, reps=20):
-    """Per-launch device time of each op of one block, launched alone with the
-    workload's shapes (CUDA events on the launching stream, after warm-up).
-    Returns {name: (ms per launch, flops, bytes, launches per forward)}."""
+OP_SOURCE = {"gemm": "q8_linear.cu", "attn": "attn.cu", "qk_prep": "rowops.cu",
+             "gate_act": "rowops.cu", "add_norm": "rowops.cu"}
+
+
+def workload_ops(cfg, st, torch):
+    """Each op of one block with the workload's shapes, launched alone.
+    Returns {name: (fn(stream), algorithmic flops, algorithmic bytes,
+    launches per forward, bound)}."""
     import transformer_encoder_forward_gb300 as te
     T, d, hd, H, KV, F = st.T, cfg.d, cfg.hd, cfg.heads, cfg.kv_heads, cfg.ffn
     qw, kw = H * hd, KV * hd
     ldq = qw + 2 * kw
     dev = st.device
     L0 = st.layers[0]
-    a = torch.randn(T, d, device=dev).to(torch.bfloat16)
-    qkv = torch.randn(T, ldq, device=dev).to(torch.bfloat16)
-    o = torch.randn(T, qw, device=dev).to(torch.bfloat16)
-    tmp = torch.empty(T, d, device=dev)
-    gu = torch.randn(T, 2 * F, device=dev).to(torch.bfloat16)
-    m = torch.randn(T, F, device=dev).to(torch.bfloat16)
-    x = torch.randn(T, d, device=dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = torch.randn(T, d, device=dev, generator=g).to(torch.bfloat16)
+    qkv = torch.randn(T, ldq, device=dev, generator=g).to(torch.bfloat16)
+    o = torch.randn(T, qw, device=dev, generator=g).to(torch.bfloat16)
+    tmp = torch.randn(T, d, device=dev, generator=g)
+    gu = torch.randn(T, 2 * F, device=dev, generator=g).to(torch.bfloat16)
+    m = torch.randn(T, F, device=dev, generator=g).to(torch.bfloat16)
+    x = torch.randn(T, d, device=dev, generator=g)
     w = lambda k: te.q8w(*L0.t[k])
     nl = cfg.layers
-    ops = {}
-
-    def gemm_items(keys, y, ldy, offs):
-        return [{"w": w(k), "y": y[:, off:] if off else y, "ldy": ldy} for k, off in zip(keys, offs)]
-
     ug = 2 if cfg.gated else 1
     g_keys = ["wg", "wu"] if cfg.gated else ["wg"]
-    ops["q8_gemm qkv (z=3)"] = (lambda: te.q8_linear(a, gemm_items(["wq", "wk", "wv"], qkv, ldq, [0, qw, qw + kw])),
-                                2 * T * d * ldq, T * d * 2 + ldq * d + T * ldq * 2, nl)
-    ops["q8_gemm o"] = (lambda: te.q8_linear(o, [{"w": w("wo"), "y": tmp, "ldy": d}]),
-                        2 * T * qw * d, T * qw * 2 + qw * d + T * d * 4, nl)
-    ops["q8_gemm gate|up (z=2)"] = (lambda: te.q8_linear(a, gemm_items(g_keys, gu, ug * F, [0, F][:ug])),
-                                    2 * T * d * F * ug, T * d * 2 + ug * F * d + T * ug * F * 2, nl)
-    ops["q8_gemm down"] = (lambda: te.q8_linear(m, [{"w": w("wd"), "y": tmp, "ldy": d}]),
-                           2 * T * F * d, T * F * 2 + F * d + T * d * 4, nl)
-    for li in sorted({cfg.window_of(i) for i in range(nl)}):
-        cnt = sum(1 for i in range(nl) if cfg.window_of(i) == li)
-        pairs = visible_pairs(st.lens, li)
-        ops[f"attn (window {li})"] = (
-            lambda li=li: te.attn_varlen_fwd(qkv, ldq, 0, qw, qw + kw, st.cu_host, st.cu_dev, H, KV, hd,
-                                             li, cfg.scale, o, qw),
-            4 * hd * H * pairs, T * ldq * 2 + T * qw * 2, cnt)
+
+    def items(keys, y, ldy, offs):
+        return [{"w": w(k), "y": y[:, off:] if off else y, "ldy": ldy} for k, off in zip(keys, offs)]
+
+    it_qkv = items(["wq", "wk", "wv"], qkv, ldq, [0, qw, qw + kw])
+    it_gu = items(g_keys, gu, ug * F, [0, F][:ug])
+    ops = {
+        "gemm_qkv": (lambda s: te.q8_linear(a, it_qkv, stream=s), 2 * T * d * ldq,
+                     T * d * 2 + ldq * d + T * ldq * 2, nl, "tensor"),
+        "gemm_o": (lambda s: te.q8_linear(o, [{"w": w("wo"), "y": tmp, "ldy": d}], stream=s),
+                   2 * T * qw * d, T * qw * 2 + qw * d + T * d * 4, nl, "tensor"),
+        "gemm_gu": (lambda s: te.q8_linear(a, it_gu, stream=s), 2 * T * d * F * ug,
+                    T * d * 2 + ug * F * d + T * ug * F * 2, nl, "tensor"),
+        "gemm_down": (lambda s: te.q8_linear(m, [{"w": w("wd"), "y": tmp, "ldy": d}], stream=s),
+                      2 * T * F * d, T * F * 2 + F * d + T * d * 4, nl, "tensor"),
+    }
+    for win in sorted({cfg.window_of(i) for i in range(nl)}):
+        cnt = sum(1 for i in range(nl) if cfg.window_of(i) == win)
+        pairs = visible_pairs(st.lens, win)
+        ops[f"attn_w{win}"] = (
+            lambda s, win=win: te.attn_varlen_fwd(qkv, ldq, 0, qw, qw + kw, st.cu_host, st.cu_dev, H,
+                                                  KV, hd, win, cfg.scale, o, qw, stream=s),
+            4 * hd * H * pairs, T * ldq * 2 + T * qw * 2, cnt, "tensor")
     if cfg.qk_norm or cfg.rope:
-        ops["qk_prep_rope"] = (lambda: te.qk_prep_rope(
-            qkv, ldq, 0, qw, H, KV, hd, L0.t["q_norm"], L0.t["k_norm"], cfg.eps, st.rope_cos, st.rope_sin,
-            st.rope_pos, st.rope_sec, 1.0, T), 0, 2 * T * (qw + kw) * 2, nl)
-    ops["gate_act"] = (lambda: te.gate_act(gu, ug * F, F if cfg.gated else -1,
-                                           te.TE_ACT_SILU if cfg.act == "silu" else te.TE_ACT_GELU_TANH,
-                                           m, F, T, F), 0, T * F * 2 * (ug + 1), nl)
-    ops["add_norm"] = (lambda: te.add_norm(x, tmp, L0.t["post_attn_w"] if cfg.form == "sandwich" else None,
-                                           1.0, L0.t["norm2_w"], L0.t["norm2_b"],
-                                           te.TE_NORM_LN if cfg.norm == "ln" else te.TE_NORM_RMS, cfg.eps, a),
-                       0, T * d * (4 * 3 + 2), 2 * nl)
-    res = {}
-    stream = torch.cuda.current_stream()
-    for name, (fn, flops, nbytes, count) in ops.items():
+        ops["qk_prep"] = (lambda s: te.qk_prep_rope(
+            qkv, ldq, 0, qw, H, KV, hd, L0.t["q_norm"], L0.t["k_norm"], cfg.eps, st.rope_cos,
+            st.rope_sin, st.rope_pos, st.rope_sec, 1.0, T, stream=s), 0, 2 * T * (qw + kw) * 2, nl,
+            "hbm")
+    ops["gate_act"] = (lambda s: te.gate_act(gu, ug * F, F if cfg.gated else -1,
+                                             te.TE_ACT_SILU if cfg.act == "silu" else te.TE_ACT_GELU_TANH,
+                                             m, F, T, F, stream=s), 0, T * F * 2 * (ug + 1), nl, "hbm")
+    ops["add_norm"] = (lambda s: te.add_norm(x, tmp, L0.t["post_attn_w"] if cfg.form == "sandwich" else None,
+                                             1.0, L0.t["norm2_w"], L0.t["norm2_b"],
+                                             te.TE_NORM_LN if cfg.norm == "ln" else te.TE_NORM_RMS, cfg.eps,
+                                             a, stream=s), 0, T * d * (4 * 3 + 2), 2 * nl, "hbm")
+    return ops
+
+
+def time_op(fn, torch, dev, reps=20):
+    """Device time per launch: `reps` launches captured in one CUDA graph and
+    replayed (no host gaps), timed with CUDA events on the replay stream."""
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
         for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(reps)]
-        for s, e in ev:
-            s.record(stream)
-            fn()
-            e.record(stream)
-        torch.cuda.synchronize()
-        ms = statistics.median(s.elapsed_time(e) for s, e in ev)
-        res[name] = (ms, flops, nbytes, count)
+            fn(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(reps):
+            fn(stream)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        graph.replay()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / reps
+
+
+def time_kernels(cfg, st, torch):
+    import transformer_encoder_forward_gb300 as te
+    res = {}
+    for name, (fn, flops, nbytes, count, bound) in workload_ops(cfg, st, torch).items():
+        res[name] = (time_op(fn, torch, st.device), flops, nbytes, count, bound)
     te.check()
     return res
+
+
+def source_sha(op):
+    import hashlib
+    key = next(k for k in OP_SOURCE if op.startswith(k))
+    path = os.path.join(ROOT, "transformer_encoder_forward_gb300", "csrc", OP_SOURCE[key])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def measured_traffic(config_key, op):
+    """DRAM bytes per launch of `op` from the committed ncu summary, or None
+    when there is none or the kernel source changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    rec = j.get(f"{op}@{config_key}")
+    if not rec or rec.get("source_sha256") != source_sha(op):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def roofline_for(kern, config_key, peaks):
+    """The op with the largest share of the forward, against its roof."""
+    name = max(kern, key=lambda k: kern[k][0] * kern[k][3])
+    ms, flops, nbytes, count, bound = kern[name]
+    if bound == "tensor":
+        ach = flops / (ms * 1e-3) / 1e12
+        peak, unit, src = peaks["bf16_tflops"], "TFLOP/s", "bf16 burst (cuBLAS), timed alone"
+    else:
+        ach = nbytes / (ms * 1e-3) / 1e9
+        peak, unit, src = peaks["hbm_gbs"], "GB/s", "HBM copy"
+    return {"kernel": name, "bound": bound, "achieved": round(ach, 1), "peak": peak, "unit": unit,
+            "frac": round(ach / peak, 4), "traffic": measured_traffic(config_key, name),
+            "algorithmic_per_launch": flops if bound == "tensor" else nbytes,
+            "ms_per_launch": round(ms, 4), "peak_source": f"{peaks['source']} {src}"}
+
+
+def run_op(args):
+    """One op of the workload alone (for profiling): W warm-up launches, then
+    K launches; prints one JSON line with its per-launch device time."""
+    import torch
+    import transformer_encoder_forward_gb300 as te
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    te.lib()
+    cfg, lens, st, _, _, _ = build_stack(args.config, dev)
+    ops = workload_ops(cfg, st, torch)
+    fn, flops, nbytes, count, bound = ops[args.op]
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        fn(stream)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        fn(stream)
+    torch.cuda.synchronize()
+    te.check()
+    ms = time_op(fn, torch, dev)
+    out = {"op": args.op, "config": cfg.name, "ms_per_launch": round(ms, 4),
+           "launches_per_forward": count, "bound": bound}
+    if flops:
+        out["tflops"] = round(flops / (ms * 1e-3) / 1e12, 1)
+    out["gbs_algorithmic"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+    print(json.dumps(out), flush=True)
 
 
 def run_ours(args):
@@ -337,17 +427,11 @@ def run_ours(args):
     # per-kernel device times with the workload's shapes -> roofline
     kern = time_kernels(cfg, st, torch)
     peaks = read_peaks()
-    per_fwd = {k: v[0] * v[3] for k, v in kern.items()}
-    gemm_ms = sum(v[0] * v[3] for k, v in kern.items() if k.startswith("q8_gemm"))
-    gemm_flops = sum(v[1] * v[3] for k, v in kern.items() if k.startswith("q8_gemm"))
+    roofline = roofline_for(kern, args.config, peaks)
     attn_ms = sum(v[0] * v[3] for k, v in kern.items() if k.startswith("attn"))
     attn_fl = sum(v[1] * v[3] for k, v in kern.items() if k.startswith("attn"))
-    gemm_tf = gemm_flops / (gemm_ms * 1e-3) / 1e12
-    peak_tf = peaks["bf16_tflops_sustained"]
-    roofline = {"kernel": "q8_gemm_kernel (all four projections of a block)", "bound": "tensor",
-                "achieved": round(gemm_tf, 1), "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": round(gemm_tf / peak_tf, 4), "traffic": None,
-                "peak_source": f"{peaks['source']} bf16 sustained (cuBLAS)"}
+    gemm_ms = sum(v[0] * v[3] for k, v in kern.items() if k.startswith("gemm"))
+    gemm_fl = sum(v[1] * v[3] for k, v in kern.items() if k.startswith("gemm"))
     kernels = {k: {"ms_per_launch": round(v[0], 4), "launches_per_forward": v[3],
                    "ms_per_forward": round(v[0] * v[3], 3),
                    **({"tflops": round(v[1] / (v[0] * 1e-3) / 1e12, 1)} if v[1] else {}),
@@ -377,6 +461,7 @@ def run_ours(args):
         "roofline": roofline,
         "kernels": kernels,
         "attention_tflops": round(attn_fl / (attn_ms * 1e-3) / 1e12, 1) if attn_ms else None,
+        "gemm_tflops": round(gemm_fl / (gemm_ms * 1e-3) / 1e12, 1) if gemm_ms else None,
         "gpu_launches": launches_per_forward(cfg) * args.steps,
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
@@ -485,11 +570,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--op", default=None,
+                    help="time one op of the workload alone (gemm_qkv, gemm_o, gemm_gu, gemm_down, "
+                         "attn_w<window>, qk_prep, gate_act, add_norm) instead of the forward")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.op:
+        run_op(args)
     else:
         run_ours(args)
 

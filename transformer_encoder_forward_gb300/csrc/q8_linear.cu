@@ -8,24 +8,29 @@
 // and "cortiq-engine 0.8.39 src/gpu_metal/egemma2.rs" (Prog::mm: one dispatch
 // over an item table, one item per grid z).
 //
-// GB300 design (not the pages' 64x64x32 simdgroup tiling).  The tile computes
-// the TRANSPOSED product Y^T[o, t] = W[o, :] . X[t, :] so that the 128 weight
-// rows of a tile sit on the 128 TMEM lanes:
+// GB300 design (not the pages' 64x64x32 simdgroup tiling).  A tile computes
+// the TRANSPOSED product Y^T[o, t] = W[o, :] . X[t, :] so that its 128 weight
+// rows sit on the 128 TMEM lanes.  One persistent CTA per SM walks a static
+// list of (128 features x BN tokens) tiles with warp-specialised roles:
 //   * warp 0 (one lane) streams K-slices of 64 with TMA: the bf16 activation
 //     tile [BN tokens x 64] into 128-byte-swizzled shared memory (the MMA's B
 //     operand) and the int8 weight tile [128 x 64] (64-byte swizzle);
-//   * warps 2-5 widen the int8 tile to bf16 in registers (exact: |q| <= 127
-//     fits bf16's 8-bit significand) and write it straight into TMEM with
-//     tcgen05.st, where it is the MMA's A operand - the widened tile never
-//     touches shared memory, leaving shared-memory bandwidth to the B reads;
-//   * warp 1 (one lane) issues tcgen05.mma kind::f16 M=128 N=BN K=16 into an
-//     f32 TMEM accumulator and releases each stage with tcgen05.commit;
-//   * warps 2-5 then read the accumulator with tcgen05.ld: lane = output
-//     feature o, so the row scale and bias are per-thread constants and each
-//     store instruction writes 32 consecutive features of one token (one
-//     128-byte line in f32).
-// Every mbarrier wait is bounded (about 200 ms); a timeout sets an error word
-// that te_check() reports, and the kernel still frees its TMEM.
+//   * warps 2-9 widen the int8 tile to bf16 in registers - exact, |q| <= 127
+//     fits bf16's 8-bit significand - with a byte-permute / f32-add magic
+//     number sequence that stays off the slow conversion pipe, and write it
+//     straight into TMEM with tcgen05.st, where it is the MMA's A operand
+//     (two warps per TMEM lane quadrant, each half of the 64 K columns); the
+//     widened tile never touches shared memory, which keeps shared-memory
+//     bandwidth for the B reads;
+//   * warp 1 (one lane) issues tcgen05.mma kind::f16 M=128 N=BN K=16 into one
+//     of two f32 TMEM accumulators and releases stages with tcgen05.commit;
+//   * warps 10-13 drain the other accumulator meanwhile (tcgen05.ld): lane =
+//     output feature, so the row scale and bias are per-thread constants and
+//     every store instruction writes 32 consecutive features of one token.
+// TMEM: 2 accumulators of BN columns + 4 A stages of 32 columns (= 512 for
+// BN = 192).  Every mbarrier wait is bounded (about 200 ms); a timeout sets
+// an error word that te_check() reports, the role stops, and the kernel still
+// waits for its own copies and MMAs and frees its TMEM.
 #include <cuda.h>
 
 #include <mutex>
@@ -37,9 +42,10 @@ namespace {
 
 constexpr int BM = 128;       // weight rows (output features) per tile = TMEM lanes
 constexpr int BK = 64;        // K per pipeline stage
-constexpr int NST = 4;        // pipeline stages
+constexpr int NA = 4;         // TMEM stages of the widened A operand
 constexpr int MAXZ = 4;
-constexpr int NTHREADS = 192;
+constexpr int NWARPS = 14;    // producer, MMA, 8 converters, 4 epilogue
+constexpr int NTHREADS = NWARPS * 32;
 
 struct Item {
     const float *scale;
@@ -47,181 +53,355 @@ struct Item {
     void *y;
     const float *resid;
     long long ldy, ldr;
-    int n, ydt, tile0, pad;
+    int n, ydt, tile0, ntiles;
 };
 
 struct Params {
     CUtensorMap tx;           // x: bf16 [m, k]
     CUtensorMap tw[MAXZ];     // q_i: int8 [n_i, k]
     Item it[MAXZ];
-    int z, m, k;
+    int z, m, k, ttiles, nunits;
 };
 
 __device__ int g_gemm_err;
 
 template <int BN>
 struct Layout {
+    static constexpr int NST = BN >= 192 ? 6 : 8;       // shared-memory load stages
     static constexpr int XBYTES = BN * BK * 2;          // activation stage
     static constexpr int WBYTES = BM * BK;              // int8 weight stage
     static constexpr int X_OFF = 0;
     static constexpr int W_OFF = NST * XBYTES;
-    static constexpr int BAR_OFF = W_OFF + NST * WBYTES;
-    // at most two CTAs per SM may hold TMEM at once (2 x 256 columns): the
-    // smallest tile pads its shared memory so that a third cannot start
-    static constexpr int USED = BAR_OFF + 8 * (3 * NST + 1) + 16;
-    static constexpr int BYTES = (BN <= 64 && USED < 80 * 1024) ? 80 * 1024 : USED;
-    static constexpr int TMEM_COLS = (BN + NST * 32 <= 256) ? 256 : 512;
-    static_assert(BN + NST * 32 <= TMEM_COLS, "TMEM budget");
+    // epilogue staging: one padded 32 x 33 f32 block per epilogue warp
+    static constexpr int STG_OFF = W_OFF + NST * WBYTES;
+    static constexpr int STG_BYTES = 4 * 32 * 33 * 4;
+    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+    // barriers: full, empty [NST]; afull, aempty [NA]; accfull, accempty [2]; done
+    static constexpr int NBAR = 2 * NST + 2 * NA + 4 + 1;
+    static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
+    static constexpr int A_COL = 2 * BN;                // first TMEM column of the A stages
+    static constexpr int TMEM_COLS = (2 * BN + NA * 32 <= 256) ? 256 : 512;
+    static_assert(2 * BN + NA * 32 <= TMEM_COLS, "TMEM budget");
+    static_assert(XBYTES % 1024 == 0, "swizzled stages stay 1024-byte aligned");
 };
 
-__device__ __forceinline__ int32_t sx8(uint32_t w, int byte) {
-    return (int32_t)(w << (24 - 8 * byte)) >> 24;
+// int8 x4 -> two bf16x2 words, exactly.  (b ^ 0x80) is q + 128; placed as the
+// low byte of the f32 pattern 0x4B0000xx it reads 2^23 + q + 128, and one f32
+// subtraction leaves q.  |q| <= 128 needs at most 8 significant bits, so the
+// upper 16 bits of that f32 are its exact bf16.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float magic = 8388736.0f;   // 2^23 + 128
+    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - magic;
+    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - magic;
+    const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - magic;
+    const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - magic;
+    lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+    hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+struct TileCoord {
+    int zi, o0, t0;
+};
+
+// Work units are (pair of 128-row feature tiles, BN-token tile).  The two CTAs
+// of a cluster take the two feature tiles of one unit: they share the token
+// tile, so each loads half of it and multicasts that half to both.  Feature
+// tile major, token tiles fastest: clusters running together share weight
+// tiles, and the activation (re-read once per feature pair) stays in L2.  A
+// feature tile past the last one (odd count) is a phantom: its weights read
+// as zeros and its epilogue stores nothing.
+__device__ __forceinline__ TileCoord tile_coord(const Params &p, int unit, int rank) {
+    const int fp = unit / p.ttiles;
+    const int tt = unit - fp * p.ttiles;
+    const int ft = 2 * fp + rank;
+    int zi = 0;
+    while (zi + 1 < p.z && ft >= p.it[zi + 1].tile0) ++zi;
+    return {zi, (ft - p.it[zi].tile0) * BM, tt};
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// TMA 2-D load multicast to the CTAs in `mask`: the box lands at the same
+// shared-memory offset in each, and each one's mbarrier at `bar`'s offset
+// receives the completed bytes.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *map, uint32_t bar, int32_t c0,
+                                               int32_t c1, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+        : "memory");
+}
+
+// Arrives on the mbarrier at `bar`'s offset in every CTA of `mask` once the
+// MMAs issued so far by this thread are done.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
+        : "memory");
 }
 
 template <int BN>
-__global__ void __launch_bounds__(NTHREADS, 1) q8_gemm_kernel(const __grid_constant__ Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+    q8_gemm_kernel(const __grid_constant__ Params p) {
     using L = Layout<BN>;
+    constexpr int NST = L::NST;
+    constexpr int HALF = BN / 2;                       // token rows each CTA of the pair loads
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
     const uint32_t bar_full = sb + L::BAR_OFF;
-    const uint32_t bar_afull = bar_full + 8 * NST;
-    const uint32_t bar_empty = bar_afull + 8 * NST;
-    const uint32_t bar_acc = bar_empty + 8 * NST;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * (3 * NST + 1));
+    const uint32_t bar_empty = bar_full + 8 * NST;
+    const uint32_t bar_afull = bar_empty + 8 * NST;
+    const uint32_t bar_aempty = bar_afull + 8 * NA;
+    const uint32_t bar_accfull = bar_aempty + 8 * NA;
+    const uint32_t bar_accempty = bar_accfull + 16;
+    const uint32_t bar_done = bar_accempty + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBAR);
 
-    // once any CTA has given up a wait, the rest skip their work (the call
-    // has failed; te_check reports it) instead of timing out one by one
-    if (*reinterpret_cast<volatile int *>(&g_gemm_err) != 0) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ftile = blockIdx.y;
-    int zi = 0;
-    while (zi + 1 < p.z && ftile >= p.it[zi + 1].tile0) ++zi;
-    const Item &it = p.it[zi];
-    const int o0 = (ftile - it.tile0) * BM;
-    const int t0 = blockIdx.x * BN;
     const int nkb = p.k / BK;
+    const int rank = (int)cluster_rank();
+    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    // once any CTA has given up a wait, the rest skip their work (the call
+    // has failed; te_check reports it) instead of timing out one by one; the
+    // flag is read once, before the cluster's first handshake, and both CTAs
+    // of a pair decide together
+    __shared__ int s_skip;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_afull + 8 * s, 128);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 2);   // both CTAs' MMAs must be done with the stage
         }
-        mbar_init(bar_acc, 1);
+        for (int a = 0; a < NA; ++a) {
+            mbar_init(bar_afull + 8 * a, 8);   // one arrival per converter warp
+            mbar_init(bar_aempty + 8 * a, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_accfull + 8 * b, 1);
+            mbar_init(bar_accempty + 8 * b, 4);   // one arrival per epilogue warp
+        }
+        mbar_init(bar_done, 1);
         fence_mbar_init();
+        s_skip = *reinterpret_cast<volatile int *>(&g_gemm_err) != 0;
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();            // the peer's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    bool ok = true;
+    bool ok = s_skip == 0;
+    const int nunits = ok ? p.nunits : 0;
 
     if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&p.tx);
-            tma_prefetch_desc(&p.tw[zi]);
-            int issued = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % NST;
-                const uint32_t ph = (kb / NST) & 1;
-                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar_full + 8 * s, L::XBYTES + L::WBYTES);
-                tma_load_2d(sb + L::X_OFF + s * L::XBYTES, &p.tx, bar_full + 8 * s, kb * BK, t0);
-                tma_load_2d(sb + L::W_OFF + s * L::WBYTES, &p.tw[zi], bar_full + 8 * s, kb * BK, o0);
-                issued = kb + 1;
+            int kbg = 0;
+            for (int u = cid; u < nunits && ok; u += ncl) {
+                const TileCoord tc = tile_coord(p, u, rank);
+                const void *wmap = &p.tw[tc.zi];
+                for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+                    const int s = kbg % NST;
+                    if (!mbar_wait(bar_empty + 8 * s, ((kbg / NST) & 1) ^ 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bar_full + 8 * s, L::XBYTES + L::WBYTES);
+                    tma_load_2d_mc(sb + L::X_OFF + s * L::XBYTES + rank * HALF * 128, &p.tx,
+                                   bar_full + 8 * s, kb * BK, tc.t0 * BN + rank * HALF, 0x3);
+                    tma_load_2d(sb + L::W_OFF + s * L::WBYTES, wmap, bar_full + 8 * s, kb * BK, tc.o0);
+                }
             }
             // make sure no copy of ours is still landing when the CTA exits
-            for (int kb = issued - NST < 0 ? 0 : issued - NST; kb < issued; ++kb)
-                mbar_wait(bar_full + 8 * (kb % NST), (kb / NST) & 1, 20000000ull);
+            for (int j = kbg - NST < 0 ? 0 : kbg - NST; j < kbg; ++j)
+                mbar_wait(bar_full + 8 * (j % NST), (j / NST) & 1, 20000000ull);
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % NST;
-                const uint32_t ph = (kb / NST) & 1;
-                if (!mbar_wait(bar_full + 8 * s, ph) || !mbar_wait(bar_afull + 8 * s, ph)) {
-                    ok = false;
-                    break;
-                }
+            int kbg = 0, lt = 0;
+            for (int u = cid; u < nunits && ok; u += ncl, ++lt) {
+                const int b = lt & 1;
+                if (!mbar_wait(bar_accempty + 8 * b, ((lt >> 1) & 1) ^ 1)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t xs = sb + L::X_OFF + s * L::XBYTES;
+                const uint32_t dcol = tbase + b * BN;
+                for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+                    const int s = kbg % NST, a = kbg % NA;
+                    if (!mbar_wait(bar_full + 8 * s, (kbg / NST) & 1) ||
+                        !mbar_wait(bar_afull + 8 * a, (kbg / NA) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xs = sb + L::X_OFF + s * L::XBYTES;
 #pragma unroll
-                for (int j = 0; j < BK / 16; ++j)
-                    mma_ts_bf16(tbase, tbase + BN + 32 * s + 8 * j, smem_desc_sw128(xs + 32 * j),
-                                idesc, (kb | j) != 0);
-                mma_commit(bar_empty + 8 * s);
+                    for (int j = 0; j < BK / 16; ++j)
+                        mma_ts_bf16(dcol, tbase + L::A_COL + 32 * a + 8 * j,
+                                    smem_desc_sw128(xs + 32 * j), idesc, (kb | j) != 0);
+                    mma_commit_mc(bar_empty + 8 * s, 0x3);
+                    mma_commit(bar_aempty + 8 * a);
+                }
+                if (ok) mma_commit(bar_accfull + 8 * b);
             }
-            mma_commit(bar_acc);   // fires once every MMA issued above has completed
+            // every MMA issued above has completed once this fires
+            mma_commit(bar_done);
+            mbar_wait(bar_done, 0, 20000000ull);
+        }
+    } else if (warp < 10) {
+        // -------------------------------- widen int8 -> bf16 into TMEM (A)
+        const int q = warp & 3;                        // TMEM lane quadrant
+        const int h = (warp - 2) >> 2;                 // which 32 of the 64 K columns
+        const int row = 32 * q + lane;                 // weight row within the tile
+        const uint32_t tl = (uint32_t)(32 * q) << 16;
+        int kbg = 0;
+        for (int u = cid; u < nunits && ok; u += ncl) {
+            for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+                const int s = kbg % NST, a = kbg % NA;
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8 * s, (kbg / NST) & 1) &&
+                                                 mbar_wait(bar_aempty + 8 * a, ((kbg / NA) & 1) ^ 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + row * 64;
+                const int sw = (row >> 1) & 3;
+                const uint4 v0 = *reinterpret_cast<const uint4 *>(wrow + (((2 * h) ^ sw) << 4));
+                const uint4 v1 = *reinterpret_cast<const uint4 *>(wrow + (((2 * h + 1) ^ sw) << 4));
+                uint32_t r[16];
+                widen4(v0.x, r[0], r[1]);
+                widen4(v0.y, r[2], r[3]);
+                widen4(v0.z, r[4], r[5]);
+                widen4(v0.w, r[6], r[7]);
+                widen4(v1.x, r[8], r[9]);
+                widen4(v1.y, r[10], r[11]);
+                widen4(v1.z, r[12], r[13]);
+                widen4(v1.w, r[14], r[15]);
+                tmem_st16(tbase + tl + L::A_COL + 32 * a + 16 * h, r);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_afull + 8 * a);
+            }
         }
     } else {
-        // ---- widen int8 -> bf16 into TMEM (A operand), then the epilogue
-        const int q = warp & 3;                       // TMEM lane quadrant of this warp
-        const int row = 32 * q + lane;                // weight row within the tile
+        // ----------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
         const uint32_t tl = (uint32_t)(32 * q) << 16;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % NST;
-            const uint32_t ph = (kb / NST) & 1;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8 * s, ph));
+        int lt = 0;
+        for (int u = cid; u < nunits && ok; u += ncl, ++lt) {
+            const int b = lt & 1;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_accfull + 8 * b, (lt >> 1) & 1));
             if (!ok) break;
             tc_fence_after();
-            const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + row * 64;
-            uint32_t a[32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(wrow + ((c ^ ((row >> 1) & 3)) << 4));
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    a[c * 8 + e * 2 + 0] = pack_bf16x2((float)sx8(w4[e], 0), (float)sx8(w4[e], 1));
-                    a[c * 8 + e * 2 + 1] = pack_bf16x2((float)sx8(w4[e], 2), (float)sx8(w4[e], 3));
-                }
-            }
-            tmem_st32(tbase + tl + BN + 32 * s, a);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar_afull + 8 * s);
-        }
-        ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait(bar_acc, 0));
-        if (ok) {
-            tc_fence_after();
-            const int o = o0 + row;
-            const bool ov = o < it.n;
-            const float sc = ov ? it.scale[o] : 0.f;
-            const float bi = (ov && it.bias) ? it.bias[o] : 0.f;
+            const TileCoord tc = tile_coord(p, u, rank);
+            // the item's fields in registers: the stores below cannot alias them
+            const int o = tc.o0 + row;
+            const bool ov = o < p.it[tc.zi].n;
+            const float sc = ov ? p.it[tc.zi].scale[o] : 0.f;
+            const float *bias = p.it[tc.zi].bias;
+            const float bi = (ov && bias) ? bias[o] : 0.f;
+            const int t0 = tc.t0 * BN;
+            const long long ldy = p.it[tc.zi].ldy, ldr = p.it[tc.zi].ldr;
+            const bool f32out = p.it[tc.zi].ydt == TE_F32;
+            char *__restrict__ ybase = reinterpret_cast<char *>(p.it[tc.zi].y);
+            const float *__restrict__ rbase = p.it[tc.zi].resid;
+            // Each 32 (features) x 32 (tokens) block goes through a padded
+            // shared-memory transpose, so that every lane then writes 16
+            // contiguous bytes along the feature axis: a warp store covers
+            // 4 (f32) or 8 (bf16) token rows instead of one.
+            float *stg = reinterpret_cast<float *>(smem + L::STG_OFF) + (warp - 10) * 32 * 33;
+            const int fo = tc.o0 + 32 * q;                  // first feature of this warp's block
             for (int c = 0; c < BN / 32; ++c) {
-                if (t0 + 32 * c >= p.m) break;        // warp-uniform
+                if (t0 + 32 * c >= p.m) break;          // warp-uniform
                 uint32_t v[32];
-                tmem_ld32(tbase + tl + 32 * c, v);
+                tmem_ld32(tbase + tl + b * BN + 32 * c, v);
                 tmem_wait_ld();
-                if (ov) {
-#pragma unroll 8
-                    for (int j = 0; j < 32; ++j) {
-                        const int t = t0 + 32 * c + j;
-                        if (t >= p.m) break;
-                        float y = __uint_as_float(v[j]) * sc + bi;
-                        if (it.resid) y += it.resid[(long long)t * it.ldr + o];
-                        if (it.ydt == TE_F32)
-                            reinterpret_cast<float *>(it.y)[(long long)t * it.ldy + o] = y;
-                        else
-                            reinterpret_cast<__nv_bfloat16 *>(it.y)[(long long)t * it.ldy + o] =
-                                __float2bfloat16_rn(y);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) stg[j * 33 + lane] = __uint_as_float(v[j]) * sc + bi;
+                __syncwarp();
+                const long long tb = t0 + 32 * c;
+                if (fo < p.it[tc.zi].n) {
+                    if (f32out) {
+                        const int fl = 4 * (lane & 7);     // 4 features of one token row
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int j = (lane >> 3) + 4 * i;
+                            if (tb + j < p.m) {
+                                float4 y = make_float4(stg[j * 33 + fl], stg[j * 33 + fl + 1],
+                                                       stg[j * 33 + fl + 2], stg[j * 33 + fl + 3]);
+                                if (rbase) {
+                                    const float4 r = *reinterpret_cast<const float4 *>(
+                                        rbase + (tb + j) * ldr + fo + fl);
+                                    y.x += r.x; y.y += r.y; y.z += r.z; y.w += r.w;
+                                }
+                                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(ybase) +
+                                                            (tb + j) * ldy + fo + fl) = y;
+                            }
+                        }
+                    } else {
+                        const int fl = 8 * (lane & 3);     // 8 features of one token row
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int j = (lane >> 2) + 8 * i;
+                            if (tb + j < p.m) {
+                                float y[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) y[e] = stg[j * 33 + fl + e];
+                                if (rbase) {
+                                    const float *rr = rbase + (tb + j) * ldr + fo + fl;
+                                    const float4 r0 = *reinterpret_cast<const float4 *>(rr);
+                                    const float4 r1 = *reinterpret_cast<const float4 *>(rr + 4);
+                                    y[0] += r0.x; y[1] += r0.y; y[2] += r0.z; y[3] += r0.w;
+                                    y[4] += r1.x; y[5] += r1.y; y[6] += r1.z; y[7] += r1.w;
+                                }
+                                uint4 u;
+                                u.x = pack_bf16x2(y[0], y[1]); u.y = pack_bf16x2(y[2], y[3]);
+                                u.z = pack_bf16x2(y[4], y[5]); u.w = pack_bf16x2(y[6], y[7]);
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(ybase) +
+                                                           (tb + j) * ldy + fo + fl) = u;
+                            }
+                        }
                     }
                 }
                 __syncwarp();
             }
+            // this accumulator may take the next tile's MMAs
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
         }
     }
-    if (!ok) atomicExch(&g_gemm_err, 1);
+    if (!ok && s_skip == 0) atomicExch(&g_gemm_err, 1);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, L::TMEM_COLS);
     }
+    // the peer may still multicast into our shared memory or arrive on our
+    // barriers until it is done too
+    cluster_sync();
 }
 
 // ------------------------------------------------------------------ host side
@@ -261,19 +441,53 @@ te_status make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base
     return TE_OK;
 }
 
-template <int BN>
-te_status launch(const Params &p, int ftiles, cudaStream_t stream) {
-    const int smem = Layout<BN>::BYTES + 1024;
-    static bool attr_done = false;   // per instantiation; benign race: same value
-    if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(q8_gemm_kernel<BN>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(e, "q8_linear: set shared memory size");
-        attr_done = true;
+int sm_count() {
+    static int count[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!count[dev]) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1)
+            c = 148;
+        count[dev] = c;
     }
-    const dim3 grid((p.m + BN - 1) / BN, ftiles);
-    q8_gemm_kernel<BN><<<grid, NTHREADS, smem, stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    return count[dev];
+}
+
+template <int BN>
+te_status launch(Params &p, int ftiles, cudaStream_t stream) {
+    const int smem = Layout<BN>::BYTES + 1024;
+    // per instantiation and device: dynamic shared memory size, and how many
+    // 2-CTA clusters can be resident at once (the persistent grid's size)
+    static int max_clusters[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "q8_linear: cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(TE_EINVAL, "q8_linear: device %d out of range", dev);
+    if (!max_clusters[dev]) {
+        e = cudaFuncSetAttribute(q8_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_fail(e, "q8_linear: set shared memory size");
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * sm_count(), 1, 1);
+        cfg.blockDim = dim3(NTHREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, q8_gemm_kernel<BN>, &cfg);
+        if (e != cudaSuccess || n < 1) n = sm_count() / 2;
+        max_clusters[dev] = n;
+    }
+    p.ttiles = (p.m + BN - 1) / BN;
+    p.nunits = p.ttiles * ((ftiles + 1) / 2);
+    const int clusters = p.nunits < max_clusters[dev] ? p.nunits : max_clusters[dev];
+    q8_gemm_kernel<BN><<<2 * clusters, NTHREADS, smem, stream>>>(p);
+    e = cudaGetLastError();
     return e == cudaSuccess ? TE_OK : cuda_fail(e, "q8_linear launch");
 }
 
@@ -316,13 +530,15 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         if (src.y_dtype != TE_F32 && src.y_dtype != TE_BF16)
             return fail(TE_EINVAL, "q8_linear: item %d bad y dtype", i);
         if (src.ldy < src.w.n) return fail(TE_ESHAPE, "q8_linear: item %d ldy < n", i);
+        if ((src.ldy * (src.y_dtype == TE_F32 ? 4 : 2)) % 16)
+            return fail(TE_EALIGN, "q8_linear: item %d: rows of y must be 16-byte aligned", i);
         if (!aligned16(src.w.q) || !aligned16(src.y) || (reinterpret_cast<uintptr_t>(src.w.scale) & 3) ||
             (src.w.bias && (reinterpret_cast<uintptr_t>(src.w.bias) & 3)))
             return fail(TE_EALIGN, "q8_linear: item %d: q and y must be 16-byte aligned", i);
         if (src.residual) {
             if (src.ldr < src.w.n) return fail(TE_ESHAPE, "q8_linear: item %d ldr < n", i);
-            if ((reinterpret_cast<uintptr_t>(src.residual) & 3))
-                return fail(TE_EALIGN, "q8_linear: item %d residual not 4-byte aligned", i);
+            if (!aligned16(src.residual) || src.ldr % 4)
+                return fail(TE_EALIGN, "q8_linear: item %d: residual rows must be 16-byte aligned", i);
             if (src.residual == src.y && (src.ldr != src.ldy || src.y_dtype != TE_F32))
                 return fail(TE_EINVAL, "q8_linear: item %d: in-place residual needs f32 y and ldr == ldy", i);
         }
@@ -336,12 +552,14 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         d.n = src.w.n;
         d.ydt = src.y_dtype;
         d.tile0 = ftiles;
-        ftiles += (src.w.n + BM - 1) / BM;
+        d.ntiles = (src.w.n + BM - 1) / BM;
+        ftiles += d.ntiles;
     }
     if (m == 0) return TE_OK;
-    const int bn = m >= 512 ? 256 : (m > 64 ? 128 : 64);
+    const int bn = m >= 1024 ? 192 : (m > 64 ? 128 : 64);
+    // each CTA of a cluster pair loads half of the token tile (and multicasts it)
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
-                               (uint64_t)ldx * 2, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+                               (uint64_t)ldx * 2, BK, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_OK) return st;
     for (int i = 0; i < z; ++i) {
         st = make_map_2d(&p.tw[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, items[i].w.q, (uint64_t)k,
@@ -349,7 +567,7 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         if (st != TE_OK) return st;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (bn == 256) return launch<256>(p, ftiles, s);
+    if (bn == 192) return launch<192>(p, ftiles, s);
     if (bn == 128) return launch<128>(p, ftiles, s);
     return launch<64>(p, ftiles, s);
 }

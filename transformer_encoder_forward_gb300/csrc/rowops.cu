@@ -213,6 +213,10 @@ __global__ void __launch_bounds__(256) add_norm_kernel(float *h, const float *__
 
 // ------------------------------------------------------------- qk prep + RoPE
 
+// One warp per packed row.  Each lane owns 8 consecutive channels (one
+// 16-byte load); a head of HD channels spans HD/8 lanes, so the per-head RMS
+// is a reduction over an aligned lane group and the RoPE partner (channel
+// +-sec/2 in the same section) sits in lane (l ^ sec/16) at the same offset.
 template <int HD>
 __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long long ld, int q_off,
                                                       int k_off, int nq, int nkv,
@@ -222,69 +226,85 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
                                                       const float *__restrict__ sinb,
                                                       const int *__restrict__ pos, int table_rows,
                                                       int sec, float q_mul, int rows) {
-    constexpr int EPL = HD / 32;   // elements per lane: 2 or 4
-    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    constexpr int LPH = HD / 8;                 // lanes per head
+    constexpr int HPI = 32 / LPH;               // heads per warp iteration
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const int nh = nq + nkv;
-    const long long row = gw / nh;
-    const int hh = (int)(gw % nh);
     if (row >= rows) return;
-    const bool isq = hh < nq;
-    __nv_bfloat16 *p = qkv + row * ld + (isq ? q_off + hh * HD : k_off + (hh - nq) * HD) + lane * EPL;
-    float v[EPL];
-    if constexpr (EPL == 2) {
-        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
-        v[0] = bf16_lo(u); v[1] = bf16_hi(u);
-    } else {
-        const uint2 u = *reinterpret_cast<const uint2 *>(p);
-        v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
-        v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-    }
-    const float *nw = isq ? qn : kn;
-    if (nw) {
-        float q = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) q += v[e] * v[e];
-        const float inv = rsqrtf(warp_sum(q) / (float)HD + eps);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) v[e] = v[e] * inv * nw[lane * EPL + e];
-    }
+    const int hl = lane / LPH;                  // head slot of this lane in an iteration
+    const int c0 = (lane % LPH) * 8;            // first channel of this lane within its head
+    const float *cr = nullptr, *sr = nullptr;
+    float cv[8], sv[8];
+    const int half = sec >> 1;
     if (sec) {
         long long prow = pos ? pos[row] : row;
         if (prow < 0 || prow >= table_rows) {
             atomicExch(&g_rowop_err, 2);
             prow = 0;
         }
-        const int half = sec >> 1;
-        const int xr = half / EPL;   // lane distance to the partner element
-        const float *cr = cosb + prow * (HD / 2);
-        const float *sr = sinb + prow * (HD / 2);
-        float o[EPL];
+        cr = cosb + prow * (HD / 2);
+        sr = sinb + prow * (HD / 2);
+        const int sct = c0 / sec;
+        const int i = c0 - sct * sec;
+        const int tc = sct * half + (i < half ? i : i - half);   // 8 consecutive table entries
+        const float4 a0 = *reinterpret_cast<const float4 *>(cr + tc);
+        const float4 a1 = *reinterpret_cast<const float4 *>(cr + tc + 4);
+        const float4 b0 = *reinterpret_cast<const float4 *>(sr + tc);
+        const float4 b1 = *reinterpret_cast<const float4 *>(sr + tc + 4);
+        cv[0] = a0.x; cv[1] = a0.y; cv[2] = a0.z; cv[3] = a0.w;
+        cv[4] = a1.x; cv[5] = a1.y; cv[6] = a1.z; cv[7] = a1.w;
+        sv[0] = b0.x; sv[1] = b0.y; sv[2] = b0.z; sv[3] = b0.w;
+        sv[4] = b1.x; sv[5] = b1.y; sv[6] = b1.z; sv[7] = b1.w;
+    }
+    const bool first_half = sec ? ((c0 % sec) < half) : true;
+    const int xr = sec ? half / 8 : 0;          // lane distance to the RoPE partner
+    const int nh = nq + nkv;
+    for (int h0 = 0; h0 < nh; h0 += HPI) {
+        const int hh = h0 + hl;
+        const bool active = hh < nh;            // lane groups past the last head idle
+        const bool isq = hh < nq;
+        __nv_bfloat16 *p = qkv + row * ld + (isq ? q_off + hh * HD : k_off + (hh - nq) * HD) + c0;
+        float v[8];
+        if (active) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(p);
+            v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+            v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+        } else {
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const float partner = __shfl_xor_sync(0xFFFFFFFFu, v[e], xr);
-            const int idx = lane * EPL + e;
-            const int sct = idx / sec;
-            const int i = idx - sct * sec;
-            const bool first = i < half;
-            const int tc = sct * half + (first ? i : i - half);
-            const float c = cr[tc], s = sr[tc];
-            o[e] = first ? v[e] * c - partner * s : v[e] * c + partner * s;
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
         }
+        const float *nw = isq ? qn : kn;
+        if (nw) {                               // qn and kn are both given or both NULL
+            float q = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) v[e] = o[e];
-    }
-    if (isq) {
+            for (int e = 0; e < 8; ++e) q += v[e] * v[e];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) v[e] *= q_mul;
-    }
-    if constexpr (EPL == 2) {
-        *reinterpret_cast<uint32_t *>(p) = pack_bf16x2(v[0], v[1]);
-    } else {
-        uint2 u;
-        u.x = pack_bf16x2(v[0], v[1]);
-        u.y = pack_bf16x2(v[2], v[3]);
-        *reinterpret_cast<uint2 *>(p) = u;
+            for (int o = 1; o < LPH; o <<= 1) q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
+            const float inv = rsqrtf(q / (float)HD + eps);
+            if (active) {
+                const float4 w0 = *reinterpret_cast<const float4 *>(nw + c0);
+                const float4 w1 = *reinterpret_cast<const float4 *>(nw + c0 + 4);
+                v[0] *= inv * w0.x; v[1] *= inv * w0.y; v[2] *= inv * w0.z; v[3] *= inv * w0.w;
+                v[4] *= inv * w1.x; v[5] *= inv * w1.y; v[6] *= inv * w1.z; v[7] *= inv * w1.w;
+            }
+        }
+        if (sec) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float partner = __shfl_xor_sync(0xFFFFFFFFu, v[e], xr);
+                o[e] = first_half ? v[e] * cv[e] - partner * sv[e] : v[e] * cv[e] + partner * sv[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = o[e];
+        }
+        if (active) {
+            const float mul = isq ? q_mul : 1.f;
+            uint4 u;
+            u.x = pack_bf16x2(v[0] * mul, v[1] * mul); u.y = pack_bf16x2(v[2] * mul, v[3] * mul);
+            u.z = pack_bf16x2(v[4] * mul, v[5] * mul); u.w = pack_bf16x2(v[6] * mul, v[7] * mul);
+            *reinterpret_cast<uint4 *>(p) = u;
+        }
     }
 }
 
@@ -492,11 +512,14 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
         return fail(TE_EINVAL, "qk_prep_rope: RoPE needs cos, sin and table_rows >= 1");
     if (sec && !pos && table_rows < rows)
         return fail(TE_ESHAPE, "qk_prep_rope: table has %d rows, need %d (pos == NULL)", table_rows, rows);
-    if (!aligned16(qkv) || (ld * 2) % 16 || (q_off * 2) % 8 || (k_off * 2) % 8)
-        return fail(TE_EALIGN, "qk_prep_rope: qkv rows must be 16-byte aligned, offsets 8-byte");
-    const long long warps = (long long)rows * (nq + nkv);
-    if (warps == 0) return TE_OK;
-    const dim3 grid((unsigned)((warps + 7) / 8));
+    if (!aligned16(qkv) || (ld * 2) % 16 || (q_off * 2) % 16 || (k_off * 2) % 16 ||
+        (qn && !aligned16(qn)) || (kn && !aligned16(kn)) || (cos && !aligned16(cos)) ||
+        (sin && !aligned16(sin)))
+        return fail(TE_EALIGN, "qk_prep_rope: qkv rows, head offsets and tables must be 16-byte aligned");
+    if ((qn == nullptr) != (kn == nullptr))
+        return fail(TE_EINVAL, "qk_prep_rope: give both qn and kn or neither");
+    if (rows == 0 || nq + nkv == 0) return TE_OK;
+    const dim3 grid((unsigned)(((long long)rows + 7) / 8));
     if (hd == 64)
         qk_prep_kernel<64><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, nq,
                                                      nkv, qn, kn, eps, cos, sin, pos, table_rows,
