@@ -1,4 +1,5 @@
-// Varlen bidirectional multi-head attention over packed rows (flash form).
+// Varlen bidirectional multi-head attention over packed rows (flash form) on
+// the 5th-generation tensor cores (sm_103a).
 //
 //     o[i, h] = sum_j softmax_j(scale * q[i, h] . k[j, g]) v[j, g],  g = h / (nq / nkv)
 //
@@ -8,260 +9,349 @@
 // "Attention", Prog::attention, att_plan: the key span of a query block is
 // [q0 - W, q_last + W] clipped to the sequence, zeros outside the window and
 // the padding); "cortiq-engine 0.7.6 src/gpu_metal/zimage.rs" (module doc,
-// flash zi_flash_q64pf: 64 queries a group, 32-key blocks staged, running
-// max and sum); "cera 0.2.4 src/model/vision_encoder_gpu.rs"
-// (VitGpuOps::attention).
+// flash zi_flash_q64pf: a query tile resident, key blocks staged, running
+// max and sum, q pre-scaled so that the softmax is 2^(s - max)); "cera 0.2.4
+// src/model/vision_encoder_gpu.rs" (VitGpuOps::attention).
 //
-// This kernel: one CTA per (64-query tile, head, sequence); 4 warps x 16
-// query rows; 64-key K/V tiles double-buffered in swizzled shared memory by
-// cp.async; S = Q K^T and O += P V on mma.sync m16n8k16 (bf16 in, f32
-// accumulate); online softmax in registers with exp2 and the scale folded
-// with log2(e); P rounded to bf16 for the P V product and the row sum taken
-// over the same rounded values.  Key tiles wholly outside the window or the
-// sequence are never visited; boundary tiles are masked per element, and a
-// masked key contributes exactly 0.
+// GB300 design.  One CTA per (128-query tile, head, sequence):
+//   * warp 4 (one lane) loads the Q tile once and streams 128-key K and V
+//     tiles with TMA (128-byte swizzle, double-buffered);
+//   * warp 5 (one lane) issues S = Q K^T (tcgen05.mma kind::f16, M=128 N=128,
+//     both operands K-major in shared memory) into a TMEM S buffer, and
+//     O += P V (A = P from TMEM, B = V as an MN-major shared-memory operand)
+//     into the TMEM O accumulator; for hd = 128, S is double-buffered so the
+//     tensor core computes S(j+1) while the softmax works on S(j);
+//   * warps 0-3 own one query row per thread (TMEM lane = query): they read
+//     the S row with tcgen05.ld, mask it (sequence end, window), take the row
+//     max, write P = 2^(s*scale*log2e - m) as bf16 back into TMEM and sum the
+//     same rounded values.  The running max is only moved (and O rescaled
+//     through TMEM) when it grows by more than 2^8, which keeps P in range and
+//     leaves the result unchanged: O and the row sum always share one max.
+//   * at the end the same threads divide O by the sum and store their row.
+// Key tiles wholly outside the window or the sequence are never loaded; a
+// masked key contributes exactly 0.  Every mbarrier wait is bounded (about
+// 200 ms): a timeout sets an error word that te_check() reports.
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace tefwd {
 namespace {
 
-constexpr int BQ = 64;
-constexpr int BKV = 64;
+constexpr int BQ = 128;     // queries per CTA (= TMEM lanes)
+constexpr int BKV = 128;    // keys per tile
+constexpr int NTHREADS = 192;
 
 __device__ int g_attn_err;
 
 struct AttnParams {
-    const __nv_bfloat16 *qkv;
+    CUtensorMap map;           // the bf16 q|k|v panel [T, ld], box 64 x 128
     __nv_bfloat16 *out;
     const int *cu;
-    long long ld, ldo;
+    long long ldo;
     int q_off, k_off, v_off, group, window;
     float scale_log2;
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+template <int HD, int NS>
+struct ALayout {
+    static constexpr int NB = HD / 64;              // 64-column boxes per tile row
+    static constexpr int TILE = 128 * HD * 2;       // one 128-row tile
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = TILE;              // K[2]
+    static constexpr int V_OFF = 3 * TILE;          // V[2]
+    static constexpr int BAR_OFF = 5 * TILE;
+    // q_full, k_full[2], v_full[2], kv_empty[2], s_full[NS], s_empty[NS], p_full, pv_done, fin
+    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 * NS + 3;
+    static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
+    static constexpr int S_COL = 0;                 // NS x 128 f32 columns
+    static constexpr int O_COL = NS * 128;          // HD f32 columns
+    static constexpr int P_COL = O_COL + HD;        // 64 columns of bf16 pairs
+    static constexpr int COLS = P_COL + 64 <= 256 ? 256 : 512;
+    static_assert(P_COL + 64 <= COLS, "TMEM budget");
+};
+
+// Shared-memory descriptor of an MN-major operand stored as 64-element-wide
+// boxes with the 128-byte swizzle: rows (along K) 128 bytes apart, 8-row
+// groups 1024 bytes apart (stride byte offset), 64-element groups along MN
+// `lbo` bytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Byte offset of (row, 16-byte chunk) in a [rows x HD] bf16 tile whose
-// chunks are XOR-swizzled by the row (conflict-free ldmatrix).
-template <int HD>
-__device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
-    return (uint32_t)(row * HD * 2 + ((chunk ^ (row & 7)) << 4));
-}
-
-// Loads rows [r0, r0 + 64) x columns [col, col + HD) of the panel; rows at or
-// past `rend` are zero-filled.
-template <int HD>
-__device__ __forceinline__ void load_tile(uint32_t dst, const __nv_bfloat16 *base, long long ld,
-                                          int r0, int rend, int col) {
-    constexpr int CPR = HD / 8;   // 16-byte chunks per row
-#pragma unroll
-    for (int i = threadIdx.x; i < 64 * CPR; i += 128) {
-        const int r = i / CPR, c = i % CPR;
-        const bool valid = r0 + r < rend;
-        const __nv_bfloat16 *src = valid ? base + (long long)(r0 + r) * ld + col + c * 8 : base;
-        cp_async16(dst + tile_off<HD>(r, c), src, valid);
-    }
-}
-
-template <int HD>
-__global__ void __launch_bounds__(128) attn_fwd_kernel(const AttnParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+template <int HD, int NS>
+__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
+    using L = ALayout<HD, NS>;
+    extern __shared__ uint8_t smem_raw[];
     const int seq = blockIdx.z;
     const int r0 = p.cu[seq];
     const int len = p.cu[seq + 1] - r0;
     const int q0 = blockIdx.x * BQ;
     if (q0 >= len) return;
+    if (*reinterpret_cast<volatile int *>(&g_attn_err) != 0) return;
     const int h = blockIdx.y;
     const int g = h / p.group;
     const int W = p.window;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    constexpr int TILE = 64 * HD * 2;
-    const uint32_t sQ = smem_u32(smem);
-    const uint32_t sK = sQ + TILE;            // 2 buffers
-    const uint32_t sV = sK + 2 * TILE;        // 2 buffers
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar_q = sb + L::BAR_OFF;
+    const uint32_t bar_kf = bar_q + 8;             // [2]
+    const uint32_t bar_vf = bar_kf + 16;           // [2]
+    const uint32_t bar_kve = bar_vf + 16;          // [2]
+    const uint32_t bar_sf = bar_kve + 16;          // [NS]
+    const uint32_t bar_se = bar_sf + 8 * NS;       // [NS]
+    const uint32_t bar_pf = bar_se + 8 * NS;
+    const uint32_t bar_pv = bar_pf + 8;
+    const uint32_t bar_fin = bar_pv + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBAR);
 
-    const __nv_bfloat16 *seqbase = p.qkv + (long long)r0 * p.ld;
+    // key tiles this query tile needs: the window's span, clipped
     int klo = 0, khi = len;
+    const int qhi = (q0 + BQ < len ? q0 + BQ : len) - 1;
     if (W > 0) {
         klo = q0 - W > 0 ? q0 - W : 0;
-        const int qlast = (q0 + BQ < len ? q0 + BQ : len) - 1;
-        khi = qlast + W + 1 < len ? qlast + W + 1 : len;
+        khi = qhi + W + 1 < len ? qhi + W + 1 : len;
     }
     const int kt0 = klo / BKV;
-    const int kt1 = (khi + BKV - 1) / BKV;
+    const int n = (khi + BKV - 1) / BKV - kt0;
 
-    load_tile<HD>(sQ, seqbase, p.ld, q0, len, p.q_off + h * HD);
-    load_tile<HD>(sK, seqbase, p.ld, kt0 * BKV, len, p.k_off + g * HD);
-    load_tile<HD>(sV, seqbase, p.ld, kt0 * BKV, len, p.v_off + g * HD);
-    cp_async_commit();
-
-    float o[HD / 8][4];
-#pragma unroll
-    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-    const int qa = q0 + warp * 16 + (lane >> 2);   // this thread's two query rows
-    const int qb = qa + 8;
-    const int qhi = (q0 + BQ < len ? q0 + BQ : len) - 1;
-
-    for (int kt = kt0; kt < kt1; ++kt) {
-        const int buf = (kt - kt0) & 1;
-        if (kt + 1 < kt1) {
-            load_tile<HD>(sK + (buf ^ 1) * TILE, seqbase, p.ld, (kt + 1) * BKV, len, p.k_off + g * HD);
-            load_tile<HD>(sV + (buf ^ 1) * TILE, seqbase, p.ld, (kt + 1) * BKV, len, p.v_off + g * HD);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_kf + 8 * i, 1);
+            mbar_init(bar_vf + 8 * i, 1);
+            mbar_init(bar_kve + 8 * i, 1);
         }
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-
-        const uint32_t kbuf = sK + buf * TILE, vbuf = sV + buf * TILE;
-        // ---- S = Q K^T  (16 x 64 per warp)
-        float s[8][4];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            {
-                const int r = warp * 16 + (lane & 15);
-                ldsm_x4(sQ + tile_off<HD>(r, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
-            }
-#pragma unroll
-            for (int nb = 0; nb < 4; ++nb) {
-                uint32_t b0, b1, b2, b3;
-                const int key = nb * 16 + (lane & 7) + ((lane >> 4) << 3);
-                ldsm_x4(kbuf + tile_off<HD>(key, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
-                mma16816(s[2 * nb], a0, a1, a2, a3, b0, b1);
-                mma16816(s[2 * nb + 1], a0, a1, a2, a3, b2, b3);
-            }
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(bar_sf + 8 * i, 1);
+            mbar_init(bar_se + 8 * i, 4);
         }
-        // ---- mask, scale, online softmax
-        const int kv0 = kt * BKV;
-        const bool full = kv0 + BKV <= len &&
-                          (W == 0 || (qhi - kv0 <= W && kv0 + BKV - 1 - q0 <= W));
-        float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v = s[j][e] * p.scale_log2;
-                if (!full) {
-                    const int kj = kv0 + j * 8 + 2 * (lane & 3) + (e & 1);
-                    const int qi = e < 2 ? qa : qb;
-                    const int dq = qi - kj;
-                    const bool vis = kj < len && (W == 0 || (dq <= W && -dq <= W));
-                    if (!vis) v = -INFINITY;
-                }
-                s[j][e] = v;
-            }
-            mx_a = fmaxf(mx_a, fmaxf(s[j][0], s[j][1]));
-            mx_b = fmaxf(mx_b, fmaxf(s[j][2], s[j][3]));
-        }
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xFFFFFFFFu, mx_a, 1));
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xFFFFFFFFu, mx_a, 2));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xFFFFFFFFu, mx_b, 1));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xFFFFFFFFu, mx_b, 2));
-        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-        const float mu_a = mn_a == -INFINITY ? 0.f : mn_a;
-        const float mu_b = mn_b == -INFINITY ? 0.f : mn_b;
-        const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
-        m_a = mn_a;
-        m_b = mn_b;
-        uint32_t pa[8][2];
-        float rs_a = 0.f, rs_b = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            pa[j][0] = pack_bf16x2(exp2f(s[j][0] - mu_a), exp2f(s[j][1] - mu_a));
-            pa[j][1] = pack_bf16x2(exp2f(s[j][2] - mu_b), exp2f(s[j][3] - mu_b));
-            rs_a += bf16_lo(pa[j][0]) + bf16_hi(pa[j][0]);
-            rs_b += bf16_lo(pa[j][1]) + bf16_hi(pa[j][1]);
-        }
-        l_a = l_a * al_a + rs_a;
-        l_b = l_b * al_b + rs_b;
-#pragma unroll
-        for (int i = 0; i < HD / 8; ++i) {
-            o[i][0] *= al_a; o[i][1] *= al_a;
-            o[i][2] *= al_b; o[i][3] *= al_b;
-        }
-        // ---- O += P V
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {   // 16 keys per step
-            const uint32_t a0 = pa[2 * kk][0], a1 = pa[2 * kk][1];
-            const uint32_t a2 = pa[2 * kk + 1][0], a3 = pa[2 * kk + 1][1];
-#pragma unroll
-            for (int nb = 0; nb < HD / 16; ++nb) {
-                uint32_t b0, b1, b2, b3;
-                const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                ldsm_x4_t(vbuf + tile_off<HD>(key, nb * 2 + (lane >> 4)), b0, b1, b2, b3);
-                mma16816(o[2 * nb], a0, a1, a2, a3, b0, b1);
-                mma16816(o[2 * nb + 1], a0, a1, a2, a3, b2, b3);
-            }
-        }
-        __syncthreads();
+        mbar_init(bar_pf, 4);
+        mbar_init(bar_pv, 1);
+        mbar_init(bar_fin, 1);
+        fence_mbar_init();
     }
-    cp_async_wait<0>();
+    if (warp == 5) tmem_alloc(smem_u32(tmem_slot), L::COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    bool ok = true;
 
-    l_a += __shfl_xor_sync(0xFFFFFFFFu, l_a, 1);
-    l_a += __shfl_xor_sync(0xFFFFFFFFu, l_a, 2);
-    l_b += __shfl_xor_sync(0xFFFFFFFFu, l_b, 1);
-    l_b += __shfl_xor_sync(0xFFFFFFFFu, l_b, 2);
-    const float ia = l_a > 0.f ? 1.f / l_a : 0.f;
-    const float ib = l_b > 0.f ? 1.f / l_b : 0.f;
-    __nv_bfloat16 *obase = p.out + (long long)r0 * p.ldo + h * HD + 2 * (lane & 3);
+    if (warp == 4) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.map);
+            mbar_arrive_expect_tx(bar_q, L::TILE);
+            for (int c = 0; c < L::NB; ++c)
+                tma_load_2d(sb + L::Q_OFF + c * 16384, &p.map, bar_q, p.q_off + h * HD + 64 * c, r0 + q0);
+            int j = 0;
+            for (; j < n; ++j) {
+                const int st = j & 1;
+                if (!mbar_wait(bar_kve + 8 * st, ((j >> 1) & 1) ^ 1)) { ok = false; break; }
+                const int row = r0 + (kt0 + j) * BKV;
+                mbar_arrive_expect_tx(bar_kf + 8 * st, L::TILE);
+                for (int c = 0; c < L::NB; ++c)
+                    tma_load_2d(sb + L::K_OFF + st * L::TILE + c * 16384, &p.map, bar_kf + 8 * st,
+                                p.k_off + g * HD + 64 * c, row);
+                mbar_arrive_expect_tx(bar_vf + 8 * st, L::TILE);
+                for (int c = 0; c < L::NB; ++c)
+                    tma_load_2d(sb + L::V_OFF + st * L::TILE + c * 16384, &p.map, bar_vf + 8 * st,
+                                p.v_off + g * HD + 64 * c, row);
+            }
+            // no copy of ours may still be landing when the CTA exits
+            mbar_wait(bar_q, 0, 20000000ull);
+            for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) {
+                mbar_wait(bar_kf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
+                mbar_wait(bar_vf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, BKV);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD) | (1u << 16);   // B MN-major
+            auto issue_s = [&](int j) -> bool {
+                const int st = j & 1, sbuf = j % NS;
+                if (!mbar_wait(bar_kf + 8 * st, (j >> 1) & 1)) return false;
+                if (!mbar_wait(bar_se + 8 * sbuf, ((j / NS) & 1) ^ 1)) return false;
+                tc_fence_after();
+                const uint32_t kb = sb + L::K_OFF + st * L::TILE;
 #pragma unroll
-    for (int i = 0; i < HD / 8; ++i) {
-        if (qa < len)
-            *reinterpret_cast<uint32_t *>(obase + (long long)qa * p.ldo + i * 8) =
-                pack_bf16x2(o[i][0] * ia, o[i][1] * ia);
-        if (qb < len)
-            *reinterpret_cast<uint32_t *>(obase + (long long)qb * p.ldo + i * 8) =
-                pack_bf16x2(o[i][2] * ib, o[i][3] * ib);
+                for (int k = 0; k < HD / 16; ++k) {
+                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_ss_bf16(tbase + L::S_COL + sbuf * 128, smem_desc_sw128(sb + L::Q_OFF + off),
+                                smem_desc_sw128(kb + off), idesc_s, k > 0);
+                }
+                mma_commit(bar_sf + 8 * sbuf);
+                return true;
+            };
+            ok = mbar_wait(bar_q, 0) && issue_s(0);
+            for (int j = 0; j < n && ok; ++j) {
+                if (j + 1 < n && !issue_s(j + 1)) { ok = false; break; }
+                // O += P(j) V(j)
+                if (!mbar_wait(bar_pf, j & 1) || !mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t vb = sb + L::V_OFF + (j & 1) * L::TILE;
+#pragma unroll
+                for (int s = 0; s < BKV / 16; ++s)
+                    mma_ts_bf16(tbase + L::O_COL, tbase + L::P_COL + 8 * s,
+                                smem_desc_mn_sw128(vb + s * 2048, 16384), idesc_pv, (j | s) != 0);
+                mma_commit(bar_kve + 8 * (j & 1));
+                mma_commit(bar_pv);
+            }
+            mma_commit(bar_fin);
+            mbar_wait(bar_fin, 0, 20000000ull);
+        }
+    } else {
+        // ---------------------------------------- softmax, one query per thread
+        const int row = 32 * warp + lane;
+        const int qi = q0 + row;
+        const uint32_t tl = (uint32_t)(32 * warp) << 16;
+        float m_used = -INFINITY, l = 0.f;
+        for (int j = 0; j < n; ++j) {
+            const int sbuf = j % NS;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_sf + 8 * sbuf, (j / NS) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            float x[BKV];
+#pragma unroll
+            for (int c = 0; c < BKV / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tbase + tl + L::S_COL + sbuf * 128 + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]) * p.scale_log2;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_se + 8 * sbuf);
+            // mask: keys past the sequence end or outside the window
+            const int kv0 = (kt0 + j) * BKV;
+            const bool full = kv0 + BKV <= len &&
+                              (W == 0 || (qhi - kv0 <= W && kv0 + BKV - 1 - q0 <= W));
+            if (!full) {
+#pragma unroll
+                for (int e = 0; e < BKV; ++e) {
+                    const int dq = qi - (kv0 + e);
+                    if (kv0 + e >= len || (W > 0 && (dq > W || -dq > W))) x[e] = -INFINITY;
+                }
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int e = 1; e < BKV; ++e) mx = fmaxf(mx, x[e]);
+            const bool resc = mx > m_used + 8.f;
+            bool pv_waited = false;
+            if (__any_sync(0xFFFFFFFFu, resc)) {
+                const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
+                if (resc) m_used = mx;
+                l *= alpha;
+                if (j > 0) {
+                    // O holds the products of the earlier tiles: wait for the
+                    // last one, then rescale it in place
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv, (j - 1) & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(tbase + tl + L::O_COL + 32 * c, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st32(tbase + tl + L::O_COL + 32 * c, v);
+                    }
+                    tmem_wait_st();
+                    pv_waited = true;
+                }
+            }
+            const float mu = m_used == -INFINITY ? 0.f : m_used;
+            uint32_t pk[BKV / 2];
+            float rs = 0.f;
+#pragma unroll
+            for (int e = 0; e < BKV / 2; ++e) {
+                pk[e] = pack_bf16x2(fast_exp2(x[2 * e] - mu), fast_exp2(x[2 * e + 1] - mu));
+                rs += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+            }
+            l += rs;
+            if (j > 0 && !pv_waited) {
+                // the P buffer is free once the previous P V product is done
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv, (j - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            tmem_st32(tbase + tl + L::P_COL, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+            tmem_st32(tbase + tl + L::P_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_pf);
+        }
+        // ---- epilogue: O / l, one row per thread
+        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv, (n - 1) & 1));
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow = p.out + (long long)(r0 + qi) * p.ldo + h * HD;
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tbase + tl + L::O_COL + 32 * c, v);
+                tmem_wait_ld();
+                if (qi < len) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 u;
+                        u.x = pack_bf16x2(__uint_as_float(v[8 * e + 0]) * inv, __uint_as_float(v[8 * e + 1]) * inv);
+                        u.y = pack_bf16x2(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv);
+                        u.z = pack_bf16x2(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv);
+                        u.w = pack_bf16x2(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * e) = u;
+                    }
+                }
+            }
+        }
+    }
+    if (!ok) atomicExch(&g_attn_err, 1);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tbase, L::COLS);
     }
 }
 
-template <int HD>
+template <int HD, int NS>
 te_status launch(const AttnParams &p, int max_len, int nq, int nseq, cudaStream_t stream) {
-    const int smem = 5 * 64 * HD * 2;
+    using L = ALayout<HD, NS>;
+    const int smem = L::BYTES + 1024;
     static bool attr_done = false;
     if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>,
+        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, NS>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_fail(e, "attn: set shared memory size");
         attr_done = true;
     }
     const dim3 grid((max_len + BQ - 1) / BQ, nq, nseq);
-    attn_fwd_kernel<HD><<<grid, 128, smem, stream>>>(p);
+    attn_tc_kernel<HD, NS><<<grid, NTHREADS, smem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TE_OK : cuda_fail(e, "attn launch");
 }
@@ -311,10 +401,12 @@ extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_o
         if (a0 < b1 && b0 < a1) return fail(TE_EINVAL, "attn: out overlaps qkv");
     }
     AttnParams p;
-    p.qkv = reinterpret_cast<const __nv_bfloat16 *>(qkv);
+    memset(&p, 0, sizeof(p));
+    st = make_map_2d(&p.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)ld, (uint64_t)total,
+                     (uint64_t)ld * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != TE_OK) return st;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.cu = cu_dev;
-    p.ld = ld;
     p.ldo = ldo;
     p.q_off = q_off;
     p.k_off = k_off;
@@ -323,6 +415,6 @@ extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_o
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return hd == 64 ? launch<64>(p, max_len, nq_heads, nseq, s)
-                    : launch<128>(p, max_len, nq_heads, nseq, s);
+    return hd == 64 ? launch<64, 1>(p, max_len, nq_heads, nseq, s)
+                    : launch<128, 2>(p, max_len, nq_heads, nseq, s);
 }

@@ -1,6 +1,7 @@
 // Shared host and device helpers of the tefwd library (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -23,6 +24,12 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // total row count and the longest sequence.
 te_status check_cu(const int32_t *cu_host, const int32_t *cu_dev, int32_t nseq,
                    int32_t *total, int32_t *max_len);
+
+// Encodes a 2-D tiled TMA descriptor (row-major, `inner` elements per row,
+// `outer` rows, `row_bytes` apart) for a box of box_inner x box_outer.
+te_status make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                      uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle sw);
 
 // Bounded-wait error words: each translation unit with bounded waits owns one
 // and exposes a reader that returns and clears it (0 = nothing happened).
