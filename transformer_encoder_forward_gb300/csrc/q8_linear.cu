@@ -9,26 +9,35 @@
 // over an item table, one item per grid z).
 //
 // GB300 design (not the pages' 64x64x32 simdgroup tiling).  A tile computes
-// the TRANSPOSED product Y^T[o, t] = W[o, :] . X[t, :] so that its 128 weight
-// rows sit on the 128 TMEM lanes.  One persistent CTA per SM walks a static
-// list of (128 features x BN tokens) tiles with warp-specialised roles:
-//   * warp 0 (one lane) streams K-slices of 64 with TMA: the bf16 activation
-//     tile [BN tokens x 64] into 128-byte-swizzled shared memory (the MMA's B
-//     operand) and the int8 weight tile [128 x 64] (64-byte swizzle);
+// the TRANSPOSED product Y^T[o, t] = W[o, :] . X[t, :] so that its weight
+// rows sit on the TMEM lanes.  Persistent 2-CTA clusters (one CTA per SM)
+// walk a static list of (256 features x BN tokens) tiles: each CTA owns 128
+// feature rows and half of the BN tokens, and the leader CTA issues 2-SM
+// MMAs (cta_group::2, M=256) that read both CTAs' operands, so each SM only
+// ingests its own weight rows and half of the activation tile.  Roles:
+//   * warp 0 (one lane) streams K-slices of 128 with TMA, each as two
+//     64-wide boxes: this CTA's half of the bf16 activation tile [BN/2 tokens
+//     x 128] into 128-byte-swizzled shared memory (its part of the MMA's B
+//     operand) and its int8 weight tile [128 x 128] (64-byte swizzle);
 //   * warps 2-9 widen the int8 tile to bf16 in registers - exact, |q| <= 127
 //     fits bf16's 8-bit significand - with a byte-permute / f32-add magic
 //     number sequence that stays off the slow conversion pipe, and write it
 //     straight into TMEM with tcgen05.st, where it is the MMA's A operand
-//     (two warps per TMEM lane quadrant, each half of the 64 K columns); the
+//     (two warps per TMEM lane quadrant, each one 64-column box); the
 //     widened tile never touches shared memory, which keeps shared-memory
 //     bandwidth for the B reads;
-//   * warp 1 (one lane) issues tcgen05.mma kind::f16 M=128 N=BN K=16 into one
-//     of two f32 TMEM accumulators and releases stages with tcgen05.commit;
+//   * warp 1 (one lane of the leader) issues tcgen05.mma.cta_group::2
+//     kind::f16 M=256 N=BN K=16 into one of two f32 TMEM accumulators (each
+//     CTA holds its 128 rows) and releases both CTAs' stages with multicast
+//     tcgen05.commit; the converters and epilogue warps of both CTAs report to
+//     the leader's barriers through their cluster addresses;
 //   * warps 10-13 drain the other accumulator meanwhile (tcgen05.ld): lane =
 //     output feature, so the row scale and bias are per-thread constants and
 //     every store instruction writes 32 consecutive features of one token.
-// TMEM: 2 accumulators of BN columns + 4 A stages of 32 columns (= 512 for
-// BN = 192).  Every mbarrier wait is bounded (about 200 ms); a timeout sets
+// TMEM: 2 accumulators of BN columns + 2 A stages of 64 columns (= 512 for
+// BN = 192).  A stage is 8 MMAs deep, so the barrier round trip between
+// stages (about 0.1-0.2 us for the issuing thread) is amortised over 768
+// tensor-core cycles.  Every mbarrier wait is bounded (about 200 ms); a timeout sets
 // an error word that te_check() reports, the role stops, and the kernel still
 // waits for its own copies and MMAs and frees its TMEM.
 #include <cuda.h>
@@ -41,8 +50,9 @@ namespace tefwd {
 namespace {
 
 constexpr int BM = 128;       // weight rows (output features) per tile = TMEM lanes
-constexpr int BK = 64;        // K per pipeline stage
-constexpr int NA = 4;         // TMEM stages of the widened A operand
+constexpr int BK = 128;       // K per pipeline stage (two 64-wide TMA boxes)
+constexpr int BOX = 64;       // K width of one TMA box
+constexpr int NA = 2;         // TMEM stages of the widened A operand (64 columns each)
 constexpr int MAXZ = 4;
 constexpr int NWARPS = 14;    // producer, MMA, 8 converters, 4 epilogue
 constexpr int NTHREADS = NWARPS * 32;
@@ -67,9 +77,12 @@ __device__ int g_gemm_err;
 
 template <int BN>
 struct Layout {
-    static constexpr int NST = BN >= 192 ? 6 : 8;       // shared-memory load stages
-    static constexpr int XBYTES = BN * BK * 2;          // activation stage
-    static constexpr int WBYTES = BM * BK;              // int8 weight stage
+    static constexpr int HALF = BN / 2;                 // token rows each CTA of the pair holds
+    static constexpr int NST = BN >= 192 ? 5 : 6;       // shared-memory load stages
+    static constexpr int XBOX = HALF * BOX * 2;         // one 64-wide box of this CTA's activation half
+    static constexpr int XBYTES = 2 * XBOX;             // this CTA's half of the activation stage
+    static constexpr int WBOX = BM * BOX;               // one 64-wide box of the int8 weight tile
+    static constexpr int WBYTES = 2 * WBOX;             // int8 weight stage (own 128 rows)
     static constexpr int X_OFF = 0;
     static constexpr int W_OFF = NST * XBYTES;
     // epilogue staging: one padded 32 x 33 f32 block per epilogue warp
@@ -80,9 +93,9 @@ struct Layout {
     static constexpr int NBAR = 2 * NST + 2 * NA + 4 + 1;
     static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
     static constexpr int A_COL = 2 * BN;                // first TMEM column of the A stages
-    static constexpr int TMEM_COLS = (2 * BN + NA * 32 <= 256) ? 256 : 512;
-    static_assert(2 * BN + NA * 32 <= TMEM_COLS, "TMEM budget");
-    static_assert(XBYTES % 1024 == 0, "swizzled stages stay 1024-byte aligned");
+    static constexpr int TMEM_COLS = (2 * BN + NA * 64 <= 256) ? 256 : 512;
+    static_assert(2 * BN + NA * 64 <= TMEM_COLS, "TMEM budget");
+    static_assert(XBOX % 1024 == 0, "swizzled boxes stay 1024-byte aligned");
 };
 
 // int8 x4 -> two bf16x2 words, exactly.  (b ^ 0x80) is q + 128; placed as the
@@ -98,16 +111,6 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
     const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - magic;
     lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
     hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15])
-        : "memory");
 }
 
 struct TileCoord {
@@ -141,25 +144,36 @@ __device__ __forceinline__ void cluster_sync() {
                      : "memory");
 }
 
-// TMA 2-D load multicast to the CTAs in `mask`: the box lands at the same
-// shared-memory offset in each, and each one's mbarrier at `bar`'s offset
-// receives the completed bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *map, uint32_t bar, int32_t c0,
-                                               int32_t c1, uint16_t mask) {
+// Arrives on the mbarrier at `bar`'s offset in every CTA of `mask` once the
+// 2-SM MMAs issued so far by this thread are done.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
         : "memory");
 }
 
-// Arrives on the mbarrier at `bar`'s offset in every CTA of `mask` once the
-// MMAs issued so far by this thread are done.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+// D(tmem, both CTAs) (+)= A(tmem, both CTAs) * B(smem desc, N split across the pair).
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar), "h"(mask)
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
 }
 
 template <int BN>
@@ -167,7 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     q8_gemm_kernel(const __grid_constant__ Params p) {
     using L = Layout<BN>;
     constexpr int NST = L::NST;
-    constexpr int HALF = BN / 2;                       // token rows each CTA of the pair loads
+    constexpr int HALF = L::HALF;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -182,39 +196,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBAR);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nkb = p.k / BK;
+    const int nkb = (p.k + BK - 1) / BK;   // a trailing half stage reads zeros past k
     const int rank = (int)cluster_rank();
+    const bool leader = rank == 0;
     const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
     // once any CTA has given up a wait, the rest skip their work (the call
-    // has failed; te_check reports it) instead of timing out one by one; the
-    // flag is read once, before the cluster's first handshake, and both CTAs
-    // of a pair decide together
+    // has failed; te_check reports it) instead of timing out one by one
     __shared__ int s_skip;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 2);   // both CTAs' MMAs must be done with the stage
+            mbar_init(bar_empty + 8 * s, 1);      // the leader's MMA commit, multicast
         }
         for (int a = 0; a < NA; ++a) {
-            mbar_init(bar_afull + 8 * a, 8);   // one arrival per converter warp
+            mbar_init(bar_afull + 8 * a, 16);     // every converter warp of both CTAs (leader's copy)
             mbar_init(bar_aempty + 8 * a, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_accfull + 8 * b, 1);
-            mbar_init(bar_accempty + 8 * b, 4);   // one arrival per epilogue warp
+            mbar_init(bar_accempty + 8 * b, 8);   // every epilogue warp of both CTAs (leader's copy)
         }
         mbar_init(bar_done, 1);
         fence_mbar_init();
         s_skip = *reinterpret_cast<volatile int *>(&g_gemm_err) != 0;
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+    if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), L::TMEM_COLS);
     tc_fence_before();
-    cluster_sync();            // the peer's barriers exist before any multicast reaches them
+    cluster_sync();            // both CTAs' barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
     bool ok = s_skip == 0;
     const int nunits = ok ? p.nunits : 0;
+    // the leader's copies of the pair-wide barriers, as cluster addresses
+    const uint32_t afull_ldr = mapa_shared(bar_afull, 0);
+    const uint32_t accempty_ldr = mapa_shared(bar_accempty, 0);
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -228,9 +244,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const int s = kbg % NST;
                     if (!mbar_wait(bar_empty + 8 * s, ((kbg / NST) & 1) ^ 1)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar_full + 8 * s, L::XBYTES + L::WBYTES);
-                    tma_load_2d_mc(sb + L::X_OFF + s * L::XBYTES + rank * HALF * 128, &p.tx,
-                                   bar_full + 8 * s, kb * BK, tc.t0 * BN + rank * HALF, 0x3);
-                    tma_load_2d(sb + L::W_OFF + s * L::WBYTES, wmap, bar_full + 8 * s, kb * BK, tc.o0);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tma_load_2d(sb + L::X_OFF + s * L::XBYTES + c * L::XBOX, &p.tx, bar_full + 8 * s,
+                                    kb * BK + c * BOX, tc.t0 * BN + rank * HALF);
+                        tma_load_2d(sb + L::W_OFF + s * L::WBYTES + c * L::WBOX, wmap, bar_full + 8 * s,
+                                    kb * BK + c * BOX, tc.o0);
+                    }
                 }
             }
             // make sure no copy of ours is still landing when the CTA exits
@@ -238,41 +258,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 mbar_wait(bar_full + 8 * (j % NST), (j / NST) & 1, 20000000ull);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        // -------------------------------------- MMA issuer (leader CTA only)
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
             int kbg = 0, lt = 0;
             for (int u = cid; u < nunits && ok; u += ncl, ++lt) {
                 const int b = lt & 1;
-                if (!mbar_wait(bar_accempty + 8 * b, ((lt >> 1) & 1) ^ 1)) { ok = false; break; }
+                if (!mbar_wait_cluster(bar_accempty + 8 * b, ((lt >> 1) & 1) ^ 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t dcol = tbase + b * BN;
                 for (int kb = 0; kb < nkb; ++kb, ++kbg) {
                     const int s = kbg % NST, a = kbg % NA;
-                    if (!mbar_wait(bar_full + 8 * s, (kbg / NST) & 1) ||
-                        !mbar_wait(bar_afull + 8 * a, (kbg / NA) & 1)) {
-                        ok = false;
-                        break;
-                    }
+                    // both CTAs' converters have widened stage a, which they
+                    // only do once their own TMA stage s has landed
+                    if (!mbar_wait_cluster(bar_afull + 8 * a, (kbg / NA) & 1)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t xs = sb + L::X_OFF + s * L::XBYTES;
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)
-                        mma_ts_bf16(dcol, tbase + L::A_COL + 32 * a + 8 * j,
-                                    smem_desc_sw128(xs + 32 * j), idesc, (kb | j) != 0);
-                    mma_commit_mc(bar_empty + 8 * s, 0x3);
-                    mma_commit(bar_aempty + 8 * a);
+                        mma_ts_pair(dcol, tbase + L::A_COL + 64 * a + 8 * j,
+                                    smem_desc_sw128(xs + (j >> 2) * L::XBOX + (j & 3) * 32), idesc,
+                                    (kb | j) != 0);
+                    mma_commit_pair(bar_empty + 8 * s, 0x3);
+                    mma_commit_pair(bar_aempty + 8 * a, 0x3);
                 }
-                if (ok) mma_commit(bar_accfull + 8 * b);
+                if (ok) mma_commit_pair(bar_accfull + 8 * b, 0x3);
             }
             // every MMA issued above has completed once this fires
-            mma_commit(bar_done);
+            mma_commit_pair(bar_done, 0x1);
             mbar_wait(bar_done, 0, 20000000ull);
         }
     } else if (warp < 10) {
         // -------------------------------- widen int8 -> bf16 into TMEM (A)
         const int q = warp & 3;                        // TMEM lane quadrant
-        const int h = (warp - 2) >> 2;                 // which 32 of the 64 K columns
+        const int h = (warp - 2) >> 2;                 // which 64 of the 128 K columns (TMA box)
         const int row = 32 * q + lane;                 // weight row within the tile
         const uint32_t tl = (uint32_t)(32 * q) << 16;
         int kbg = 0;
@@ -283,24 +302,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                                  mbar_wait(bar_aempty + 8 * a, ((kbg / NA) & 1) ^ 1));
                 if (!ok) break;
                 tc_fence_after();
-                const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + row * 64;
+                const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + h * L::WBOX + row * 64;
                 const int sw = (row >> 1) & 3;
-                const uint4 v0 = *reinterpret_cast<const uint4 *>(wrow + (((2 * h) ^ sw) << 4));
-                const uint4 v1 = *reinterpret_cast<const uint4 *>(wrow + (((2 * h + 1) ^ sw) << 4));
-                uint32_t r[16];
-                widen4(v0.x, r[0], r[1]);
-                widen4(v0.y, r[2], r[3]);
-                widen4(v0.z, r[4], r[5]);
-                widen4(v0.w, r[6], r[7]);
-                widen4(v1.x, r[8], r[9]);
-                widen4(v1.y, r[10], r[11]);
-                widen4(v1.z, r[12], r[13]);
-                widen4(v1.w, r[14], r[15]);
-                tmem_st16(tbase + tl + L::A_COL + 32 * a + 16 * h, r);
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw) << 4));
+                    widen4(v.x, r[8 * c + 0], r[8 * c + 1]);
+                    widen4(v.y, r[8 * c + 2], r[8 * c + 3]);
+                    widen4(v.z, r[8 * c + 4], r[8 * c + 5]);
+                    widen4(v.w, r[8 * c + 6], r[8 * c + 7]);
+                }
+                tmem_st32(tbase + tl + L::A_COL + 64 * a + 32 * h, r);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_afull + 8 * a);
+                if (lane == 0) mbar_arrive_cluster_relaxed(afull_ldr + 8 * a);
             }
         }
     } else {
@@ -389,18 +406,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // this accumulator may take the next tile's MMAs
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
+            if (lane == 0) mbar_arrive_cluster_relaxed(accempty_ldr + 8 * b);
         }
     }
     if (!ok && s_skip == 0) atomicExch(&g_gemm_err, 1);
     tc_fence_before();
     __syncthreads();
+    // the leader's MMAs write both CTAs' TMEM: both wait for them before freeing it
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tbase, L::TMEM_COLS);
+        tmem_dealloc_pair(tbase, L::TMEM_COLS);
     }
-    // the peer may still multicast into our shared memory or arrive on our
-    // barriers until it is done too
+    // the peer may still arrive on our barriers until it is done too
     cluster_sync();
 }
 
@@ -559,11 +577,11 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
     const int bn = m >= 1024 ? 192 : (m > 64 ? 128 : 64);
     // each CTA of a cluster pair loads half of the token tile (and multicasts it)
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
-                               (uint64_t)ldx * 2, BK, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+                               (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_OK) return st;
     for (int i = 0; i < z; ++i) {
         st = make_map_2d(&p.tw[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, items[i].w.q, (uint64_t)k,
-                         (uint64_t)items[i].w.n, (uint64_t)k, BK, BM, CU_TENSOR_MAP_SWIZZLE_64B);
+                         (uint64_t)items[i].w.n, (uint64_t)k, BOX, BM, CU_TENSOR_MAP_SWIZZLE_64B);
         if (st != TE_OK) return st;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
