@@ -13,24 +13,28 @@
 // max and sum, q pre-scaled so that the softmax is 2^(s - max)); "cera 0.2.4
 // src/model/vision_encoder_gpu.rs" (VitGpuOps::attention).
 //
-// GB300 design.  One CTA per (128-query tile, head, sequence):
-//   * warp 4 (one lane) loads the Q tile once and streams 128-key K and V
-//     tiles with TMA (128-byte swizzle, double-buffered);
-//   * warp 5 (one lane) issues S = Q K^T (tcgen05.mma kind::f16, M=128 N=128,
-//     both operands K-major in shared memory) into a TMEM S buffer, and
-//     O += P V (A = P from TMEM, B = V as an MN-major shared-memory operand)
-//     into the TMEM O accumulator; for hd = 128, S is double-buffered so the
-//     tensor core computes S(j+1) while the softmax works on S(j);
-//   * warps 0-3 own one query row per thread (TMEM lane = query): they read
-//     the S row with tcgen05.ld, mask it (sequence end, window), take the row
-//     max, write P = 2^(s*scale*log2e - m) as bf16 back into TMEM and sum the
-//     same rounded values.  The running max is only moved (and O rescaled
-//     through TMEM) when it grows by more than 2^8, which keeps P in range and
-//     leaves the result unchanged: O and the row sum always share one max.
+// GB300 design.  One CTA per (256 queries, head, sequence), as two 128-query
+// tiles A and B that share one stream of 128-key K/V tiles:
+//   * warp 9 (one lane) loads both Q tiles once and streams K and V tiles
+//     with TMA (128-byte swizzle, double-buffered);
+//   * warp 8 (one lane) issues the MMAs: S_w = Q_w K^T (tcgen05.mma kind::f16,
+//     M=128 N=128, both operands K-major in shared memory) into tile w's TMEM
+//     S buffer, and O_w += P_w V (A = P_w from TMEM, B = V as an MN-major
+//     shared-memory operand) into its TMEM O accumulator, in the order
+//     PV_A(j), PV_B(j), S_A(j+1), S_B(j+1): while one warpgroup runs its
+//     softmax, the tensor core works on the other tile;
+//   * warps 0-3 (tile A) and 4-7 (tile B) own one query row per thread (TMEM
+//     lane = query): they read the S row with tcgen05.ld, mask it (sequence
+//     end, window), take the row max, and write P = 2^(s*scale*log2e - m) as
+//     bf16 into the first half of their own S buffer (S_w(j+1) is only issued
+//     once PV_w(j) has consumed it).  The running max is only moved (and O
+//     rescaled through TMEM) when it grows by more than 2^8, which keeps P in
+//     range and leaves the result unchanged: O and the row sum always share
+//     one max;
 //   * at the end the same threads divide O by the sum and store their row.
-// Key tiles wholly outside the window or the sequence are never loaded; a
-// masked key contributes exactly 0.  Every mbarrier wait is bounded (about
-// 200 ms): a timeout sets an error word that te_check() reports.
+// Key tiles wholly outside both tiles' windows or the sequence are never
+// loaded; a masked key contributes exactly 0.  Every mbarrier wait is bounded
+// (about 200 ms): a timeout sets an error word that te_check() reports.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -38,9 +42,9 @@
 namespace tefwd {
 namespace {
 
-constexpr int BQ = 128;     // queries per CTA (= TMEM lanes)
+constexpr int BQ = 128;     // queries per tile (= TMEM lanes); two tiles per CTA
 constexpr int BKV = 128;    // keys per tile
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;
 
 __device__ int g_attn_err;
 
@@ -53,22 +57,21 @@ struct AttnParams {
     float scale_log2;
 };
 
-template <int HD, int NS>
+template <int HD>
 struct ALayout {
     static constexpr int NB = HD / 64;              // 64-column boxes per tile row
     static constexpr int TILE = 128 * HD * 2;       // one 128-row tile
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = TILE;              // K[2]
-    static constexpr int V_OFF = 3 * TILE;          // V[2]
-    static constexpr int BAR_OFF = 5 * TILE;
-    // q_full, k_full[2], v_full[2], kv_empty[2], s_full[NS], s_empty[NS], p_full, pv_done, fin
-    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 * NS + 3;
+    static constexpr int Q_OFF = 0;                 // Q[2] (tiles A, B)
+    static constexpr int K_OFF = 2 * TILE;          // K[2]
+    static constexpr int V_OFF = 4 * TILE;          // V[2]
+    static constexpr int BAR_OFF = 6 * TILE;
+    // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], fin
+    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1;
     static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
-    static constexpr int S_COL = 0;                 // NS x 128 f32 columns
-    static constexpr int O_COL = NS * 128;          // HD f32 columns
-    static constexpr int P_COL = O_COL + HD;        // 64 columns of bf16 pairs
-    static constexpr int COLS = P_COL + 64 <= 256 ? 256 : 512;
-    static_assert(P_COL + 64 <= COLS, "TMEM budget");
+    static constexpr int S_COL = 0;                 // S_A, S_B: 2 x 128 f32 columns (P aliased)
+    static constexpr int O_COL = 256;               // O_A, O_B: 2 x HD f32 columns
+    static constexpr int COLS = 512;
+    static_assert(O_COL + 2 * HD <= COLS, "TMEM budget");
 };
 
 // Shared-memory descriptor of an MN-major operand stored as 64-element-wide
@@ -91,19 +94,81 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-template <int HD, int NS>
+// Row max of one 128-key S row held in TMEM (columns scol..scol+127), with
+// keys outside the sequence or the window ignored when MASK.  Eight
+// independent partial maxima keep the dependency chains short.
+template <bool MASK>
+__device__ __forceinline__ float row_max(uint32_t scol, int qi, int kv0, int len, int W) {
+    float m8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < BKV / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(scol + 32 * cc, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float x = __uint_as_float(v[e]);
+            if (MASK) {
+                const int k = kv0 + 32 * cc + e, dq = qi - k;
+                if (k < len && (W == 0 || (dq <= W && -dq <= W))) m8[e & 7] = fmaxf(m8[e & 7], x);
+            } else {
+                m8[e & 7] = fmaxf(m8[e & 7], x);
+            }
+        }
+    }
+    return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+}
+
+// P = 2^(s*c + nm) over the row as bf16 pairs, written over S columns the row
+// has already consumed (chunk cc of P lands in columns [16cc, 16cc+16), which
+// held keys read by earlier chunks).  Returns the row sum of P.
+template <bool MASK>
+__device__ __forceinline__ float row_exp(uint32_t scol, float c, float nm, int qi, int kv0, int len,
+                                         int W) {
+    float r8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r8[i] = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < BKV / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(scol + 32 * cc, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), c, nm));
+            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c, nm));
+            if (MASK) {
+                const int k = kv0 + 32 * cc + 2 * e, d0 = qi - k, d1 = d0 - 1;
+                if (!(k < len && (W == 0 || (d0 <= W && -d0 <= W)))) p0 = 0.f;
+                if (!(k + 1 < len && (W == 0 || (d1 <= W && -d1 <= W)))) p1 = 0.f;
+            }
+            r8[(2 * e) & 7] += p0;
+            r8[(2 * e + 1) & 7] += p1;
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(scol + 16 * cc, pk);
+    }
+    return ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+}
+
+template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
-    using L = ALayout<HD, NS>;
+    using L = ALayout<HD>;
     extern __shared__ uint8_t smem_raw[];
     const int seq = blockIdx.z;
     const int r0 = p.cu[seq];
     const int len = p.cu[seq + 1] - r0;
-    const int q0 = blockIdx.x * BQ;
+    const int q0 = blockIdx.x * 2 * BQ;
     if (q0 >= len) return;
     if (*reinterpret_cast<volatile int *>(&g_attn_err) != 0) return;
     const int h = blockIdx.y;
     const int g = h / p.group;
     const int W = p.window;
+    const int ntile = q0 + BQ < len ? 2 : 1;        // tile B exists
 
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -112,16 +177,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const uint32_t bar_kf = bar_q + 8;             // [2]
     const uint32_t bar_vf = bar_kf + 16;           // [2]
     const uint32_t bar_kve = bar_vf + 16;          // [2]
-    const uint32_t bar_sf = bar_kve + 16;          // [NS]
-    const uint32_t bar_se = bar_sf + 8 * NS;       // [NS]
-    const uint32_t bar_pf = bar_se + 8 * NS;
-    const uint32_t bar_pv = bar_pf + 8;
-    const uint32_t bar_fin = bar_pv + 8;
+    const uint32_t bar_sf = bar_kve + 16;          // [2] per query tile
+    const uint32_t bar_pf = bar_sf + 16;           // [2] per query tile
+    const uint32_t bar_pv = bar_pf + 16;           // [2] per query tile
+    const uint32_t bar_fin = bar_pv + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBAR);
 
-    // key tiles this query tile needs: the window's span, clipped
+    // key tiles the two query tiles need: the union of their windows, clipped
     int klo = 0, khi = len;
-    const int qhi = (q0 + BQ < len ? q0 + BQ : len) - 1;
+    const int qhi = (q0 + 2 * BQ < len ? q0 + 2 * BQ : len) - 1;
     if (W > 0) {
         klo = q0 - W > 0 ? q0 - W : 0;
         khi = qhi + W + 1 < len ? qhi + W + 1 : len;
@@ -136,30 +200,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             mbar_init(bar_kf + 8 * i, 1);
             mbar_init(bar_vf + 8 * i, 1);
             mbar_init(bar_kve + 8 * i, 1);
-        }
-        for (int i = 0; i < NS; ++i) {
             mbar_init(bar_sf + 8 * i, 1);
-            mbar_init(bar_se + 8 * i, 4);
+            mbar_init(bar_pf + 8 * i, 4);
+            mbar_init(bar_pv + 8 * i, 1);
         }
-        mbar_init(bar_pf, 4);
-        mbar_init(bar_pv, 1);
         mbar_init(bar_fin, 1);
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(smem_u32(tmem_slot), L::COLS);
+    if (warp == 8) tmem_alloc(smem_u32(tmem_slot), L::COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
     bool ok = true;
 
-    if (warp == 4) {
+    if (warp == 9) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&p.map);
-            mbar_arrive_expect_tx(bar_q, L::TILE);
-            for (int c = 0; c < L::NB; ++c)
-                tma_load_2d(sb + L::Q_OFF + c * 16384, &p.map, bar_q, p.q_off + h * HD + 64 * c, r0 + q0);
+            mbar_arrive_expect_tx(bar_q, ntile * L::TILE);
+            for (int w = 0; w < ntile; ++w)
+                for (int c = 0; c < L::NB; ++c)
+                    tma_load_2d(sb + L::Q_OFF + w * L::TILE + c * 16384, &p.map, bar_q,
+                                p.q_off + h * HD + 64 * c, r0 + q0 + w * BQ);
             int j = 0;
             for (; j < n; ++j) {
                 const int st = j & 1;
@@ -181,140 +244,114 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 mbar_wait(bar_vf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 8) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, BKV);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD) | (1u << 16);   // B MN-major
-            auto issue_s = [&](int j) -> bool {
-                const int st = j & 1, sbuf = j % NS;
-                if (!mbar_wait(bar_kf + 8 * st, (j >> 1) & 1)) return false;
-                if (!mbar_wait(bar_se + 8 * sbuf, ((j / NS) & 1) ^ 1)) return false;
+            auto issue_s = [&](int w, int j) -> bool {
+                if (!mbar_wait(bar_kf + 8 * (j & 1), (j >> 1) & 1)) return false;
                 tc_fence_after();
-                const uint32_t kb = sb + L::K_OFF + st * L::TILE;
+                const uint32_t kb = sb + L::K_OFF + (j & 1) * L::TILE;
+                const uint32_t qb = sb + L::Q_OFF + w * L::TILE;
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
                     const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_ss_bf16(tbase + L::S_COL + sbuf * 128, smem_desc_sw128(sb + L::Q_OFF + off),
+                    mma_ss_bf16(tbase + L::S_COL + w * 128, smem_desc_sw128(qb + off),
                                 smem_desc_sw128(kb + off), idesc_s, k > 0);
                 }
-                mma_commit(bar_sf + 8 * sbuf);
+                mma_commit(bar_sf + 8 * w);
                 return true;
             };
-            ok = mbar_wait(bar_q, 0) && issue_s(0);
+            ok = mbar_wait(bar_q, 0);
+            for (int w = 0; w < ntile && ok; ++w) ok = issue_s(w, 0);
             for (int j = 0; j < n && ok; ++j) {
-                if (j + 1 < n && !issue_s(j + 1)) { ok = false; break; }
-                // O += P(j) V(j)
-                if (!mbar_wait(bar_pf, j & 1) || !mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t vb = sb + L::V_OFF + (j & 1) * L::TILE;
+                // O_w += P_w(j) V(j)
+                if (!mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1)) { ok = false; break; }
+                for (int w = 0; w < ntile && ok; ++w) {
+                    if (!mbar_wait(bar_pf + 8 * w, j & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t vb = sb + L::V_OFF + (j & 1) * L::TILE;
 #pragma unroll
-                for (int s = 0; s < BKV / 16; ++s)
-                    mma_ts_bf16(tbase + L::O_COL, tbase + L::P_COL + 8 * s,
-                                smem_desc_mn_sw128(vb + s * 2048, 16384), idesc_pv, (j | s) != 0);
-                mma_commit(bar_kve + 8 * (j & 1));
-                mma_commit(bar_pv);
+                    for (int s2 = 0; s2 < BKV / 16; ++s2)
+                        mma_ts_bf16(tbase + L::O_COL + w * HD, tbase + L::S_COL + w * 128 + 8 * s2,
+                                    smem_desc_mn_sw128(vb + s2 * 2048, 16384), idesc_pv, (j | s2) != 0);
+                    mma_commit(bar_pv + 8 * w);
+                }
+                if (!ok) break;
+                mma_commit(bar_kve + 8 * (j & 1));   // K(j), V(j) are free once both PVs are done
+                if (j + 1 < n) {
+                    // S_w(j+1) overwrites the P_w(j) that PV_w(j) reads: wait for it first
+                    for (int w = 0; w < ntile && ok; ++w)
+                        ok = mbar_wait(bar_pv + 8 * w, j & 1) && issue_s(w, j + 1);
+                }
             }
             mma_commit(bar_fin);
             mbar_wait(bar_fin, 0, 20000000ull);
         }
-    } else {
+    } else if (warp < 4 * ntile) {
         // ---------------------------------------- softmax, one query per thread
-        const int row = 32 * warp + lane;
-        const int qi = q0 + row;
-        const uint32_t tl = (uint32_t)(32 * warp) << 16;
+        const int w = warp >> 2;                         // query tile of this warpgroup
+        const int wq = warp & 3;                         // TMEM lane quadrant
+        const int row = 32 * wq + lane;
+        const int tq0 = q0 + w * BQ;                     // first query of the tile
+        const int qi = tq0 + row;
+        const int tqhi = (tq0 + BQ < len ? tq0 + BQ : len) - 1;
+        const uint32_t tl = (uint32_t)(32 * wq) << 16;
+        const uint32_t scol = tbase + tl + L::S_COL + w * 128;
+        const uint32_t ocol = tbase + tl + L::O_COL + w * HD;
+        const float c = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         for (int j = 0; j < n; ++j) {
-            const int sbuf = j % NS;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_sf + 8 * sbuf, (j / NS) & 1));
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_sf + 8 * w, j & 1));
             if (!ok) break;
+            // S_w(j) landed, so PV_w(j-1) is done: P_w and O_w may be touched
             tc_fence_after();
-            float x[BKV];
-#pragma unroll
-            for (int c = 0; c < BKV / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tbase + tl + L::S_COL + sbuf * 128 + 32 * c, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]) * p.scale_log2;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_se + 8 * sbuf);
             // mask: keys past the sequence end or outside the window
             const int kv0 = (kt0 + j) * BKV;
             const bool full = kv0 + BKV <= len &&
-                              (W == 0 || (qhi - kv0 <= W && kv0 + BKV - 1 - q0 <= W));
-            if (!full) {
-#pragma unroll
-                for (int e = 0; e < BKV; ++e) {
-                    const int dq = qi - (kv0 + e);
-                    if (kv0 + e >= len || (W > 0 && (dq > W || -dq > W))) x[e] = -INFINITY;
-                }
-            }
-            float mx = x[0];
-#pragma unroll
-            for (int e = 1; e < BKV; ++e) mx = fmaxf(mx, x[e]);
+                              (W == 0 || (tqhi - kv0 <= W && kv0 + BKV - 1 - tq0 <= W));
+            // pass 1: the row max of the raw scores
+            float mx = full ? row_max<false>(scol, qi, kv0, len, W) : row_max<true>(scol, qi, kv0, len, W);
+            mx *= c;                                     // c > 0: the max of the scaled row
             const bool resc = mx > m_used + 8.f;
-            bool pv_waited = false;
             if (__any_sync(0xFFFFFFFFu, resc)) {
                 const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
                 if (resc) m_used = mx;
                 l *= alpha;
                 if (j > 0) {
-                    // O holds the products of the earlier tiles: wait for the
-                    // last one, then rescale it in place
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv, (j - 1) & 1));
-                    if (!ok) break;
-                    tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < HD / 32; ++c) {
+                    for (int cc = 0; cc < HD / 32; ++cc) {
                         uint32_t v[32];
-                        tmem_ld32(tbase + tl + L::O_COL + 32 * c, v);
+                        tmem_ld32(ocol + 32 * cc, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        tmem_st32(tbase + tl + L::O_COL + 32 * c, v);
+                        tmem_st32(ocol + 32 * cc, v);
                     }
                     tmem_wait_st();
-                    pv_waited = true;
                 }
             }
-            const float mu = m_used == -INFINITY ? 0.f : m_used;
-            uint32_t pk[BKV / 2];
-            float rs = 0.f;
-#pragma unroll
-            for (int e = 0; e < BKV / 2; ++e) {
-                pk[e] = pack_bf16x2(fast_exp2(x[2 * e] - mu), fast_exp2(x[2 * e + 1] - mu));
-                rs += bf16_lo(pk[e]) + bf16_hi(pk[e]);
-            }
+            // pass 2: P as bf16 into the consumed S columns, and its row sum
+            const float nm = m_used == -INFINITY ? 0.f : -m_used;
+            const float rs = full ? row_exp<false>(scol, c, nm, qi, kv0, len, W)
+                                  : row_exp<true>(scol, c, nm, qi, kv0, len, W);
             l += rs;
-            if (j > 0 && !pv_waited) {
-                // the P buffer is free once the previous P V product is done
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv, (j - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
-            }
-            tmem_st32(tbase + tl + L::P_COL, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-            tmem_st32(tbase + tl + L::P_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_pf);
+            if (lane == 0) mbar_arrive(bar_pf + 8 * w);
         }
         // ---- epilogue: O / l, one row per thread
-        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv, (n - 1) & 1));
+        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv + 8 * w, (n - 1) & 1));
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *orow = p.out + (long long)(r0 + qi) * p.ldo + h * HD;
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int cc = 0; cc < HD / 32; ++cc) {
                 uint32_t v[32];
-                tmem_ld32(tbase + tl + L::O_COL + 32 * c, v);
+                tmem_ld32(ocol + 32 * cc, v);
                 tmem_wait_ld();
                 if (qi < len) {
 #pragma unroll
@@ -324,7 +361,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                         u.y = pack_bf16x2(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv);
                         u.z = pack_bf16x2(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv);
                         u.w = pack_bf16x2(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * e) = u;
+                        *reinterpret_cast<uint4 *>(orow + 32 * cc + 8 * e) = u;
                     }
                 }
             }
@@ -333,25 +370,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     if (!ok) atomicExch(&g_attn_err, 1);
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tbase, L::COLS);
     }
 }
 
-template <int HD, int NS>
+template <int HD>
 te_status launch(const AttnParams &p, int max_len, int nq, int nseq, cudaStream_t stream) {
-    using L = ALayout<HD, NS>;
+    using L = ALayout<HD>;
     const int smem = L::BYTES + 1024;
     static bool attr_done = false;
     if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, NS>,
+        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_fail(e, "attn: set shared memory size");
         attr_done = true;
     }
-    const dim3 grid((max_len + BQ - 1) / BQ, nq, nseq);
-    attn_tc_kernel<HD, NS><<<grid, NTHREADS, smem, stream>>>(p);
+    const dim3 grid((max_len + 2 * BQ - 1) / (2 * BQ), nq, nseq);
+    attn_tc_kernel<HD><<<grid, NTHREADS, smem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TE_OK : cuda_fail(e, "attn launch");
 }
@@ -415,6 +452,6 @@ extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_o
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return hd == 64 ? launch<64, 1>(p, max_len, nq_heads, nseq, s)
-                    : launch<128, 2>(p, max_len, nq_heads, nseq, s);
+    return hd == 64 ? launch<64>(p, max_len, nq_heads, nseq, s)
+                    : launch<128>(p, max_len, nq_heads, nseq, s);
 }
