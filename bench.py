@@ -77,9 +77,9 @@ def launches_per_forward(cfg):
     """Kernels of this library one forward launches (what the graph replays)."""
     n = 1                                                     # input pre-norm
     for i in range(cfg.layers):
-        n += 4                                                # q8 GEMMs: qkv, o, gate|up, down
+        n += 4                                                # q8 GEMMs: qkv, o, gate|up (+gate), down
         n += 1 if (cfg.qk_norm or cfg.rope) else 0            # q/k norm + RoPE
-        n += 3                                                # attention, FFN pre-norm, gate
+        n += 2                                                # attention, FFN pre-norm
         n += 1 if (cfg.form == "sandwich" or i + 1 < cfg.layers) else 0   # closing norm
     return n + (1 if cfg.pool else 0)                         # final norm + pool
 
@@ -172,7 +172,7 @@ def build_stack(key, device):
 # --------------------------------------------------------------- GPU timing
 
 OP_SOURCE = {"gemm": "q8_linear.cu", "attn": "attn.cu", "qk_prep": "rowops.cu",
-             "gate_act": "rowops.cu", "add_norm": "rowops.cu"}
+             "add_norm": "rowops.cu"}
 
 
 def workload_ops(cfg, st, torch):
@@ -190,7 +190,6 @@ def workload_ops(cfg, st, torch):
     qkv = torch.randn(T, ldq, device=dev, generator=g).to(torch.bfloat16)
     o = torch.randn(T, qw, device=dev, generator=g).to(torch.bfloat16)
     tmp = torch.randn(T, d, device=dev, generator=g)
-    gu = torch.randn(T, 2 * F, device=dev, generator=g).to(torch.bfloat16)
     m = torch.randn(T, F, device=dev, generator=g).to(torch.bfloat16)
     x = torch.randn(T, d, device=dev, generator=g)
     w = lambda k: te.q8w(*L0.t[k])
@@ -202,14 +201,21 @@ def workload_ops(cfg, st, torch):
         return [{"w": w(k), "y": y[:, off:] if off else y, "ldy": ldy} for k, off in zip(keys, offs)]
 
     it_qkv = items(["wq", "wk", "wv"], qkv, ldq, [0, qw, qw + kw])
-    it_gu = items(g_keys, gu, ug * F, [0, F][:ug])
+    act_code = te.TE_ACT_SILU if cfg.act == "silu" else te.TE_ACT_GELU_TANH
+
+    def gate_up(s):
+        # the block's FFN producer: gate|up with the gate in the epilogue
+        # (ungated: up with the activation in the epilogue); writes m
+        if cfg.gated:
+            te.q8_gated_linear(a, w("wg"), w("wu"), act_code, m, stream=s)
+        else:
+            te.q8_linear(a, [{"w": w("wg"), "y": m, "ldy": F, "epilogue": act_code + 1}], stream=s)
     ops = {
         "gemm_qkv": (lambda s: te.q8_linear(a, it_qkv, stream=s), 2 * T * d * ldq,
                      T * d * 2 + ldq * d + T * ldq * 2, nl, "tensor"),
         "gemm_o": (lambda s: te.q8_linear(o, [{"w": w("wo"), "y": tmp, "ldy": d}], stream=s),
                    2 * T * qw * d, T * qw * 2 + qw * d + T * d * 4, nl, "tensor"),
-        "gemm_gu": (lambda s: te.q8_linear(a, it_gu, stream=s), 2 * T * d * F * ug,
-                    T * d * 2 + ug * F * d + T * ug * F * 2, nl, "tensor"),
+        "gemm_gu": (gate_up, 2 * T * d * F * ug, T * d * 2 + ug * F * d + T * F * 2, nl, "tensor"),
         "gemm_down": (lambda s: te.q8_linear(m, [{"w": w("wd"), "y": tmp, "ldy": d}], stream=s),
                       2 * T * F * d, T * F * 2 + F * d + T * d * 4, nl, "tensor"),
     }
@@ -225,9 +231,6 @@ def workload_ops(cfg, st, torch):
             qkv, ldq, 0, qw, H, KV, hd, L0.t["q_norm"], L0.t["k_norm"], cfg.eps, st.rope_cos,
             st.rope_sin, st.rope_pos, st.rope_sec, 1.0, T, stream=s), 0, 2 * T * (qw + kw) * 2, nl,
             "hbm")
-    ops["gate_act"] = (lambda s: te.gate_act(gu, ug * F, F if cfg.gated else -1,
-                                             te.TE_ACT_SILU if cfg.act == "silu" else te.TE_ACT_GELU_TANH,
-                                             m, F, T, F, stream=s), 0, T * F * 2 * (ug + 1), nl, "hbm")
     ops["add_norm"] = (lambda s: te.add_norm(x, tmp, L0.t["post_attn_w"] if cfg.form == "sandwich" else None,
                                              1.0, L0.t["norm2_w"], L0.t["norm2_b"],
                                              te.TE_NORM_LN if cfg.norm == "ln" else te.TE_NORM_RMS, cfg.eps,
@@ -571,8 +574,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--op", default=None,
-                    help="time one op of the workload alone (gemm_qkv, gemm_o, gemm_gu, gemm_down, "
-                         "attn_w<window>, qk_prep, gate_act, add_norm) instead of the forward")
+                    help="time one op of the workload alone (gemm_qkv, gemm_o, gemm_gu (gate fused), "
+                         "gemm_down, attn_w<window>, qk_prep, add_norm) instead of the forward")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -31,7 +31,8 @@
  *     with a message in te_last_error() (thread-local).  Errors from earlier
  *     asynchronous work surface as TE_ECUDA from te_check().
  *   - Work is enqueued on `stream` (NULL = the legacy default stream); the
- *     calls return before it completes.  te_q8_linear, te_attn_varlen_fwd,
+ *     calls return before it completes.  te_q8_linear, te_q8_gated_linear,
+ *     te_attn_varlen_fwd,
  *     the row ops and te_encoder_block_fwd are capturable in a CUDA graph
  *     (no host synchronisation, no allocation).
  */
@@ -76,9 +77,15 @@ typedef struct {
     int32_t k;
 } te_q8w;
 
+/* Activation applied in a GEMM epilogue (TE_EPI_NONE: none). */
+typedef enum { TE_EPI_NONE = 0, TE_EPI_GELU_TANH = 1, TE_EPI_SILU = 2 } te_epilogue;
+
 /* One item of a grouped q8 GEMM ([EG2] Prog::mm item table, one item per
  * grid z; [ZI] Enc::gemm, z <= 3).  All items share the activation x.
  *   y        [m, ldy] of y_dtype (TE_F32 or TE_BF16), device
+ *   epilogue te_epilogue: y = act(bf16(s*acc + b)), the ungated MLP's
+ *            activation folded into its producer ([VIT] encode_image_gpu
+ *            "gelu" after the up projection); needs residual == NULL
  *   residual f32 [m, ldr] or NULL; y may alias residual (same pointer and
  *            leading dimension) for the in-place x += proj of the plain
  *            pre-norm block ([VIT] encode_image_gpu "add"). */
@@ -87,7 +94,7 @@ typedef struct {
     void *y;
     int64_t ldy;
     int32_t y_dtype;
-    int32_t reserved;
+    int32_t epilogue;
     const float *residual;
     int64_t ldr;
 } te_q8_item;
@@ -101,6 +108,21 @@ typedef struct {
  * applies the row scale in its f32 epilogue"), [EG2] Prog::mm. */
 te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t k,
                        const te_q8_item *items, int32_t z, te_stream stream);
+
+/* q8_gated_linear: the gate|up projections and the gate in one pass,
+ *     m[t, f] = act(bf16(g[t, f])) * bf16(u[t, f])   (stored bf16)
+ *     g = s_g * (x . q_g^T) + b_g,   u = s_u * (x . q_u^T) + b_u
+ * with act GELU-tanh or SiLU (te_act_kind).  The two products are rounded to
+ * bf16 before the gate, exactly as storing g|u and then applying te_gate_act
+ * would; the g|u panel itself is never written.
+ * x: bf16 [m, k] (ldx); wg, wu: q8_row weights of equal shape [f, k]
+ * (f % 32 == 0, k % 64 == 0); out: bf16 [m, ldm].
+ * Cites [EG2] Prog::gelu (O = gelu_tanh(G) U over the gate|up GEMM's
+ * output), [ZI] Enc::block SwiGLU (h = silu(w1 x) (w3 x)) and the module
+ * doc's rule of folding a column-wise factor into the producer's epilogue. */
+te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, int32_t k, const te_q8w *wg,
+                             const te_q8w *wu, int32_t act, void *out, int64_t ldm,
+                             te_stream stream);
 
 /* attn_varlen_fwd: bidirectional multi-head attention over packed rows.
  * qkv: bf16 [T, ld] (device) holding q heads at columns q_off + h*hd, k and

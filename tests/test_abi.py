@@ -71,6 +71,25 @@ def test_q8_linear_rejects_bad_arguments(L):
     assert _call(L, "te_q8_linear", FAKE, 128, 16, 128, null_y, 1, None)[0] == te.TE_EINVAL
 
 
+def test_gated_linear_and_epilogue_reject_bad_arguments(L):
+    wg = te.te_q8w(FAKE, FAKE, None, 256, 128)
+    wu = te.te_q8w(FAKE, FAKE, None, 256, 128)
+    assert _call(L, "te_q8_gated_linear", FAKE, 128, 16, 128, ctypes.byref(wg), ctypes.byref(wu), 7,
+                 FAKE, 256, None)[0] == te.TE_EINVAL                           # bad act
+    wu_bad = te.te_q8w(FAKE, FAKE, None, 192, 128)
+    st, msg = _call(L, "te_q8_gated_linear", FAKE, 128, 16, 128, ctypes.byref(wg), ctypes.byref(wu_bad),
+                    te.TE_ACT_SILU, FAKE, 256, None)
+    assert st == te.TE_ESHAPE and "wu" in msg
+    assert _call(L, "te_q8_gated_linear", FAKE, 128, 16, 128, ctypes.byref(wg), ctypes.byref(wu),
+                 te.TE_ACT_SILU, FAKE + 8, 256, None)[0] == te.TE_EALIGN
+    act_res = (te.te_q8_item * 1)(te.te_q8_item(te.te_q8w(FAKE, FAKE, None, 64, 128), FAKE, 64,
+                                                te.TE_BF16, te.TE_EPI_SILU, FAKE, 64))
+    assert _call(L, "te_q8_linear", FAKE, 128, 16, 128, act_res, 1, None)[0] == te.TE_EINVAL
+    bad_epi = (te.te_q8_item * 1)(te.te_q8_item(te.te_q8w(FAKE, FAKE, None, 64, 128), FAKE, 64,
+                                                te.TE_BF16, 9, None, 0))
+    assert _call(L, "te_q8_linear", FAKE, 128, 16, 128, bad_epi, 1, None)[0] == te.TE_EINVAL
+
+
 def _cu(vals):
     a = np.asarray(vals, dtype=np.int32)
     return a, a.ctypes.data_as(ctypes.c_void_p)
@@ -137,8 +156,7 @@ def test_block_validation_and_workspace(L):
     a, p = _cu([0, 37, 101])
     d = _desc()
     ws = L.te_encoder_block_workspace(ctypes.byref(d), 101)
-    expect = sum(((101 * w + 255) // 256) * 256 for w in (768 * 2, 256 * 2, 256 * 4, 2048 * 2,
-                                                          1024 * 2))
+    expect = sum(((101 * w + 255) // 256) * 256 for w in (768 * 2, 256 * 2, 256 * 4, 1024 * 2))
     assert ws == expect
     st, msg = _call(L, "te_encoder_block_fwd", ctypes.byref(d), FAKE, FAKE, p, FAKE, 2, FAKE * 256,
                     ws - 1, None)

@@ -109,6 +109,48 @@ def test_int8_widening_and_indexing_are_bit_exact():
     assert set(np.unique(q_np)) == set(range(-128, 128))
 
 
+@pytest.mark.parametrize("m,k,f,act,bias", [(37, 256, 1024, "gelu_tanh", False),
+                                            (1000, 512, 2048, "gelu_tanh", True),
+                                            (2112, 3840, 10240, "silu", False),
+                                            (101, 256, 96, "silu", True),
+                                            (300, 192, 32, "gelu_tanh", False)])
+def test_gated_linear_matches_oracle(m, k, f, act, bias):
+    # m = act(bf16(g)) * bf16(u): the same storage points as the g|u panel
+    # followed by the gate, without the panel
+    torch = _torch()
+    rng = np.random.default_rng([m, k, f])
+    x, x64 = bf16_input(rng, (m, k))
+    wg = synth.draw_q8(rng, f, k, True, bias)
+    wu = synth.draw_q8(rng, f, k, True, bias)
+    dg, du = q8_dev(wg), q8_dev(wu)
+    out = torch.full((m, f), float("nan"), dtype=torch.bfloat16, device="cuda")
+    te.q8_gated_linear(x, te.q8w(*dg), te.q8w(*du),
+                       te.TE_ACT_SILU if act == "silu" else te.TE_ACT_GELU_TANH, out)
+    te.check()
+    g = O.round_bf16(O.q8_linear(x64, wg["q"], wg["s"], wg["b"]))
+    u = O.round_bf16(O.q8_linear(x64, wu["q"], wu["s"], wu["b"]))
+    ref = O.round_bf16(O.gate_act(np.concatenate([g, u], axis=1), f, True, act))
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    assert rel_frob(got, ref) < 2e-3, rel_frob(got, ref)
+
+
+@pytest.mark.parametrize("m,k,n,act", [(4096, 768, 3072, "gelu_tanh"), (77, 256, 96, "silu")])
+def test_q8_linear_epilogue_activation_matches_oracle(m, k, n, act):
+    torch = _torch()
+    rng = np.random.default_rng([m, n])
+    x, x64 = bf16_input(rng, (m, k))
+    w = synth.draw_q8(rng, n, k, True, True)
+    dw = q8_dev(w)
+    y = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    te.q8_linear(x, [{"w": te.q8w(*dw), "y": y, "ldy": n,
+                      "epilogue": te.TE_EPI_SILU if act == "silu" else te.TE_EPI_GELU_TANH}])
+    te.check()
+    pre = O.round_bf16(O.q8_linear(x64, w["q"], w["s"], w["b"]))
+    ref = O.round_bf16(O.gate_act(pre, n, False, act))
+    assert rel_frob(to_np(y), ref) < 2e-3
+
+
 # ---------------------------------------------------------------- attention
 
 ATTN_CASES = [

@@ -19,6 +19,7 @@ TE_F32, TE_BF16 = 0, 1
 TE_NORM_RMS, TE_NORM_LN = 0, 1
 TE_ACT_GELU_TANH, TE_ACT_SILU = 0, 1
 TE_RESID_PLAIN, TE_RESID_SANDWICH = 0, 1
+TE_EPI_NONE, TE_EPI_GELU_TANH, TE_EPI_SILU = 0, 1, 2
 
 _STATUS = {0: "TE_OK", 1: "TE_EINVAL", 2: "TE_ESHAPE", 3: "TE_EALIGN", 4: "TE_EWORKSPACE",
            5: "TE_ECUDA", 6: "TE_EDEVICE"}
@@ -39,7 +40,7 @@ class te_q8w(ctypes.Structure):
 
 class te_q8_item(ctypes.Structure):
     _fields_ = [("w", te_q8w), ("y", c_p), ("ldy", c_i64), ("y_dtype", c_i32),
-                ("reserved", c_i32), ("residual", c_p), ("ldr", c_i64)]
+                ("epilogue", c_i32), ("residual", c_p), ("ldr", c_i64)]
 
 
 class te_block_desc(ctypes.Structure):
@@ -59,6 +60,8 @@ _lib = None
 
 EXPORTS = {
     "te_q8_linear": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, ctypes.POINTER(te_q8_item), c_i32, c_p]),
+    "te_q8_gated_linear": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, ctypes.POINTER(te_q8w),
+                                          ctypes.POINTER(te_q8w), c_i32, c_p, c_i64, c_p]),
     "te_attn_varlen_fwd": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_i32, c_p, c_p, c_i32, c_i32,
                                           c_i32, c_i32, c_i32, c_f32, c_p, c_i64, c_p]),
     "te_rownorm": (ctypes.c_int, [c_p, c_i32, c_i64, c_p, c_p, c_i32, c_f32, c_f32, c_p, c_i32,
@@ -138,10 +141,17 @@ def q8_linear(x, items: Sequence[dict], stream=None):
         y = it["y"]
         r = it.get("residual")
         arr[i] = te_q8_item(it["w"], y.data_ptr(), it["ldy"],
-                            TE_F32 if y.dtype == torch.float32 else TE_BF16, 0,
-                            _ptr(r), it.get("ldr", 0))
+                            TE_F32 if y.dtype == torch.float32 else TE_BF16,
+                            it.get("epilogue", TE_EPI_NONE), _ptr(r), it.get("ldr", 0))
     _ok(lib().te_q8_linear(x.data_ptr(), it_ld(x), x.shape[0], x.shape[1], arr, len(items),
                            _stream(stream)))
+
+
+def q8_gated_linear(x, wg: te_q8w, wu: te_q8w, act, out, stream=None):
+    """m = act(bf16(x Wg^T)) * bf16(x Wu^T) in one GEMM (bf16 out)."""
+    _ok(lib().te_q8_gated_linear(x.data_ptr(), x.stride(0), x.shape[0], x.shape[1],
+                                 ctypes.byref(wg), ctypes.byref(wu), act, out.data_ptr(),
+                                 out.stride(0), _stream(stream)))
 
 
 def it_ld(t) -> int:

@@ -9,9 +9,12 @@
 // "cera 0.2.4 src/model/vision_encoder_gpu.rs" encode_image_gpu (plain
 // pre-norm block: LayerNorm, biased linears, x += proj, GELU MLP).
 //
+// The FFN gate runs in the gate|up GEMM's epilogue (te_q8_gated_linear; the
+// ungated MLP's activation in its up projection's epilogue), so the g|u
+// panel is never stored.
+//
 // Workspace layout (each region 256-byte aligned):
-//   qkv bf16 [t, (nq + 2 nkv) hd] | o bf16 [t, nq hd] | tmp f32 [t, d]
-//   | gu bf16 [t, (gated ? 2 : 1) F] | m bf16 [t, F]
+//   qkv bf16 [t, (nq + 2 nkv) hd] | o bf16 [t, nq hd] | tmp f32 [t, d] | m bf16 [t, F]
 #include "common.cuh"
 
 namespace tefwd {
@@ -20,7 +23,7 @@ namespace {
 inline size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t qkv, o, tmp, gu, m, total;
+    size_t qkv, o, tmp, m, total;
 };
 
 WsLayout ws_layout(const te_block_desc &d, int32_t t) {
@@ -32,7 +35,6 @@ WsLayout ws_layout(const te_block_desc &d, int32_t t) {
     L.qkv = off; off = up256(off + T * qkvw * 2);
     L.o = off;   off = up256(off + T * ow * 2);
     L.tmp = off; off = up256(off + T * d.d * 4);
-    L.gu = off;  off = up256(off + T * (size_t)(d.gated ? 2 : 1) * d.ffn * 2);
     L.m = off;   off = up256(off + T * (size_t)d.ffn * 2);
     L.total = off;
     return L;
@@ -116,14 +118,12 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
     __nv_bfloat16 *qkv = reinterpret_cast<__nv_bfloat16 *>(ws + L.qkv);
     __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(ws + L.o);
     float *tmp = reinterpret_cast<float *>(ws + L.tmp);
-    __nv_bfloat16 *gu = reinterpret_cast<__nv_bfloat16 *>(ws + L.gu);
     __nv_bfloat16 *m = reinterpret_cast<__nv_bfloat16 *>(ws + L.m);
-    const int ldgu = (d.gated ? 2 : 1) * F;
     const bool plain = d.resid_form == TE_RESID_PLAIN;
 
     // 1. q|k|v projections, one grouped launch (z = 3)
     te_q8_item it[3] = {};
-    it[0] = {d.wq, qkv, ldqkv, TE_BF16, 0, nullptr, 0};
+    it[0] = {d.wq, qkv, ldqkv, TE_BF16, TE_EPI_NONE, nullptr, 0};
     it[1] = {d.wk, qkv + qw, ldqkv, TE_BF16, 0, nullptr, 0};
     it[2] = {d.wv, qkv + qw + kw, ldqkv, TE_BF16, 0, nullptr, 0};
     if ((st = te_q8_linear(a, D, t, D, it, 3, stream)) != TE_OK) return st;
@@ -150,13 +150,15 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
         st = te_add_norm(x, tmp, d.post_attn_w, d.post, d.ffn_norm_w, d.ffn_norm_b, d.norm_kind,
                          d.eps, a, TE_BF16, t, D, stream);
     if (st != TE_OK) return st;
-    // 6. gate|up (z = 2) or up
-    te_q8_item ig[2] = {};
-    ig[0] = {d.wg, gu, ldgu, TE_BF16, 0, nullptr, 0};
-    ig[1] = {d.wu, gu + F, ldgu, TE_BF16, 0, nullptr, 0};
-    if ((st = te_q8_linear(a, D, t, D, ig, d.gated ? 2 : 1, stream)) != TE_OK) return st;
-    // 7. gate activation
-    if ((st = te_gate_act(gu, ldgu, d.gated ? F : -1, d.act, m, F, t, F, stream)) != TE_OK) return st;
+    // 6-7. gate|up with the gate in the epilogue, or up with the activation
+    if (d.gated) {
+        st = te_q8_gated_linear(a, D, t, D, &d.wg, &d.wu, d.act, m, F, stream);
+    } else {
+        te_q8_item iu = {d.wg, m, F, TE_BF16, d.act == TE_ACT_SILU ? TE_EPI_SILU : TE_EPI_GELU_TANH,
+                         nullptr, 0};
+        st = te_q8_linear(a, D, t, D, &iu, 1, stream);
+    }
+    if (st != TE_OK) return st;
     // 8. down projection
     te_q8_item id = plain ? te_q8_item{d.wd, x, D, TE_F32, 0, x, D}
                           : te_q8_item{d.wd, tmp, D, TE_F32, 0, nullptr, 0};

@@ -56,6 +56,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// The FFN gate activations: GELU with the tanh approximation,
+// 0.5 g (1 + tanh(z)), z = sqrt(2/pi) (g + 0.044715 g^3), and SiLU,
+// g / (1 + e^-g).  Both are written through the logistic function, using
+// 0.5 (1 + tanh z) = 1 / (1 + e^-2z): g * sigma(2z) and g * sigma(g), with
+// e^y = 2^(y log2 e) on the hardware exp2 and reciprocal (relative error
+// ~1e-7, far below the bf16 rounding that follows).
+__device__ __forceinline__ float hw_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float hw_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float apply_act(float g, int act) {
+    // -2 z log2(e) for GELU-tanh; -g log2(e) for SiLU
+    const float t = act == TE_ACT_GELU_TANH
+                        ? g * fmaf(-0.10294324f, g * g, -2.3022082f)   // -2*log2e*sqrt(2/pi)*(1 + 0.044715 g^2)
+                        : -1.4426950408889634f * g;
+    // exp2 of a large t is +inf: g * rcp(inf) = g * 0 = 0, the right limit
+    return g * hw_rcp(1.f + hw_exp2(t));
+}
+
+// Rounds to the nearest bfloat16 (ties to even) and back: the value a bf16
+// store would keep.
+__device__ __forceinline__ float round_bf16(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

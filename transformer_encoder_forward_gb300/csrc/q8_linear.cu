@@ -60,10 +60,12 @@ constexpr int NTHREADS = NWARPS * 32;
 struct Item {
     const float *scale;
     const float *bias;
+    const float *scale2;      // gated mode: the up projection's scale and bias
+    const float *bias2;
     void *y;
     const float *resid;
     long long ldy, ldr;
-    int n, ydt, tile0, ntiles;
+    int n, ydt, tile0, ntiles, act;
 };
 
 struct Params {
@@ -124,13 +126,15 @@ struct TileCoord {
 // tiles, and the activation (re-read once per feature pair) stays in L2.  A
 // feature tile past the last one (odd count) is a phantom: its weights read
 // as zeros and its epilogue stores nothing.
+template <bool GATED>
 __device__ __forceinline__ TileCoord tile_coord(const Params &p, int unit, int rank) {
     const int fp = unit / p.ttiles;
     const int tt = unit - fp * p.ttiles;
     const int ft = 2 * fp + rank;
     int zi = 0;
     while (zi + 1 < p.z && ft >= p.it[zi + 1].tile0) ++zi;
-    return {zi, (ft - p.it[zi].tile0) * BM, tt};
+    // gated: a tile holds 64 gate rows and the 64 matching up rows
+    return {zi, (ft - p.it[zi].tile0) * (GATED ? BM / 2 : BM), tt};
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -176,7 +180,13 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
-template <int BN>
+// Named barrier between the two epilogue warps that hold the gate and the up
+// values of the same features (barrier ids 1 and 2; id 0 is __syncthreads).
+__device__ __forceinline__ void pair_sync(int pair) {
+    asm volatile("bar.sync %0, 64;" ::"r"(pair + 1) : "memory");
+}
+
+template <int BN, bool GATED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     q8_gemm_kernel(const __grid_constant__ Params p) {
     using L = Layout<BN>;
@@ -238,7 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             tma_prefetch_desc(&p.tx);
             int kbg = 0;
             for (int u = cid; u < nunits && ok; u += ncl) {
-                const TileCoord tc = tile_coord(p, u, rank);
+                const TileCoord tc = tile_coord<GATED>(p, u, rank);
                 const void *wmap = &p.tw[tc.zi];
                 for (int kb = 0; kb < nkb; ++kb, ++kbg) {
                     const int s = kbg % NST;
@@ -246,10 +256,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     mbar_arrive_expect_tx(bar_full + 8 * s, L::XBYTES + L::WBYTES);
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
+                        const uint32_t wdst = sb + L::W_OFF + s * L::WBYTES + c * L::WBOX;
                         tma_load_2d(sb + L::X_OFF + s * L::XBYTES + c * L::XBOX, &p.tx, bar_full + 8 * s,
                                     kb * BK + c * BOX, tc.t0 * BN + rank * HALF);
-                        tma_load_2d(sb + L::W_OFF + s * L::WBYTES + c * L::WBOX, wmap, bar_full + 8 * s,
-                                    kb * BK + c * BOX, tc.o0);
+                        if (GATED) {   // rows 0-63: gate, rows 64-127: up, same features
+                            tma_load_2d(wdst, &p.tw[0], bar_full + 8 * s, kb * BK + c * BOX, tc.o0);
+                            tma_load_2d(wdst + (BM / 2) * BOX, &p.tw[1], bar_full + 8 * s,
+                                        kb * BK + c * BOX, tc.o0);
+                        } else {
+                            tma_load_2d(wdst, wmap, bar_full + 8 * s, kb * BK + c * BOX, tc.o0);
+                        }
                     }
                 }
             }
@@ -326,18 +342,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const int row = 32 * q + lane;
         const uint32_t tl = (uint32_t)(32 * q) << 16;
         int lt = 0;
+        __shared__ int s_pair_ok[2][4];
         for (int u = cid; u < nunits && ok; u += ncl, ++lt) {
             const int b = lt & 1;
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_accfull + 8 * b, (lt >> 1) & 1));
+            if (GATED) {
+                // the gate and up warps of a pair meet at named barriers below:
+                // they continue or stop together
+                if (lane == 0) s_pair_ok[lt & 1][q] = ok;
+                pair_sync(q & 1);
+                ok = ok && s_pair_ok[lt & 1][q ^ 2];
+            }
             if (!ok) break;
             tc_fence_after();
-            const TileCoord tc = tile_coord(p, u, rank);
+            const TileCoord tc = tile_coord<GATED>(p, u, rank);
             // the item's fields in registers: the stores below cannot alias them
-            const int o = tc.o0 + row;
+            // (gated: lanes 0-63 hold gate rows, 64-127 the up rows of the same features)
+            const bool upper = GATED && row >= BM / 2;
+            const int o = tc.o0 + (GATED ? (row & (BM / 2 - 1)) : row);
             const bool ov = o < p.it[tc.zi].n;
-            const float sc = ov ? p.it[tc.zi].scale[o] : 0.f;
-            const float *bias = p.it[tc.zi].bias;
+            const float *scale = upper ? p.it[tc.zi].scale2 : p.it[tc.zi].scale;
+            const float *bias = upper ? p.it[tc.zi].bias2 : p.it[tc.zi].bias;
+            const float sc = ov ? scale[o] : 0.f;
             const float bi = (ov && bias) ? bias[o] : 0.f;
+            const int act = p.it[tc.zi].act;
             const int t0 = tc.t0 * BN;
             const long long ldy = p.it[tc.zi].ldy, ldr = p.it[tc.zi].ldr;
             const bool f32out = p.it[tc.zi].ydt == TE_F32;
@@ -348,14 +376,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // contiguous bytes along the feature axis: a warp store covers
             // 4 (f32) or 8 (bf16) token rows instead of one.
             float *stg = reinterpret_cast<float *>(smem + L::STG_OFF) + (warp - 10) * 32 * 33;
+            if (GATED) {
+                // warps q and q+2 hold the gate and the up values of the same
+                // 32 features: both stage their (bf16-rounded) block, then
+                // each writes m = act(g) * u for 16 of the 32 tokens
+                // (warp 10 + i holds quadrant (2 + i) & 3: the gate warps are 12, 13)
+                float *stg_u = reinterpret_cast<float *>(smem + L::STG_OFF) + (q & 1) * 32 * 33;
+                float *stg_g = stg_u + 2 * 32 * 33;
+                const int fo = tc.o0 + 32 * (q & 1);
+                const int jbase = q < 2 ? 0 : 16;
+                for (int c = 0; c < BN / 32; ++c) {
+                    if (t0 + 32 * c >= p.m) break;      // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld32(tbase + tl + b * BN + 32 * c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) stg[j * 33 + lane] = round_bf16(__uint_as_float(v[j]) * sc + bi);
+                    pair_sync(q & 1);
+                    const long long tb = t0 + 32 * c;
+                    if (fo < p.it[tc.zi].n) {
+                        const int fl = 8 * (lane & 3);
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int j = jbase + (lane >> 2) + 8 * i;
+                            if (tb + j < p.m) {
+                                float y[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    y[e] = apply_act(stg_g[j * 33 + fl + e], act) * stg_u[j * 33 + fl + e];
+                                uint4 pk;
+                                pk.x = pack_bf16x2(y[0], y[1]); pk.y = pack_bf16x2(y[2], y[3]);
+                                pk.z = pack_bf16x2(y[4], y[5]); pk.w = pack_bf16x2(y[6], y[7]);
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(ybase) +
+                                                           (tb + j) * ldy + fo + fl) = pk;
+                            }
+                        }
+                    }
+                    pair_sync(q & 1);
+                }
+            } else {
             const int fo = tc.o0 + 32 * q;                  // first feature of this warp's block
             for (int c = 0; c < BN / 32; ++c) {
                 if (t0 + 32 * c >= p.m) break;          // warp-uniform
                 uint32_t v[32];
                 tmem_ld32(tbase + tl + b * BN + 32 * c, v);
                 tmem_wait_ld();
+                if (act) {   // the ungated MLP: act(bf16(s*acc + b)), no residual
 #pragma unroll
-                for (int j = 0; j < 32; ++j) stg[j * 33 + lane] = __uint_as_float(v[j]) * sc + bi;
+                    for (int j = 0; j < 32; ++j)
+                        stg[j * 33 + lane] = apply_act(round_bf16(__uint_as_float(v[j]) * sc + bi), act - 1);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) stg[j * 33 + lane] = __uint_as_float(v[j]) * sc + bi;
+                }
                 __syncwarp();
                 const long long tb = t0 + 32 * c;
                 if (fo < p.it[tc.zi].n) {
@@ -392,16 +465,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                     y[0] += r0.x; y[1] += r0.y; y[2] += r0.z; y[3] += r0.w;
                                     y[4] += r1.x; y[5] += r1.y; y[6] += r1.z; y[7] += r1.w;
                                 }
-                                uint4 u;
-                                u.x = pack_bf16x2(y[0], y[1]); u.y = pack_bf16x2(y[2], y[3]);
-                                u.z = pack_bf16x2(y[4], y[5]); u.w = pack_bf16x2(y[6], y[7]);
+                                uint4 pk;
+                                pk.x = pack_bf16x2(y[0], y[1]); pk.y = pack_bf16x2(y[2], y[3]);
+                                pk.z = pack_bf16x2(y[4], y[5]); pk.w = pack_bf16x2(y[6], y[7]);
                                 *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(ybase) +
-                                                           (tb + j) * ldy + fo + fl) = u;
+                                                           (tb + j) * ldy + fo + fl) = pk;
                             }
                         }
                     }
                 }
                 __syncwarp();
+            }
             }
             // this accumulator may take the next tile's MMAs
             tc_fence_before();
@@ -437,7 +511,7 @@ int sm_count() {
     return count[dev];
 }
 
-template <int BN>
+template <int BN, bool GATED>
 te_status launch(Params &p, int ftiles, cudaStream_t stream) {
     const int smem = Layout<BN>::BYTES + 1024;
     // per instantiation and device: dynamic shared memory size, and how many
@@ -448,7 +522,7 @@ te_status launch(Params &p, int ftiles, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "q8_linear: cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(TE_EINVAL, "q8_linear: device %d out of range", dev);
     if (!max_clusters[dev]) {
-        e = cudaFuncSetAttribute(q8_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(q8_gemm_kernel<BN, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_fail(e, "q8_linear: set shared memory size");
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * sm_count(), 1, 1);
@@ -462,14 +536,14 @@ te_status launch(Params &p, int ftiles, cudaStream_t stream) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, q8_gemm_kernel<BN>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, q8_gemm_kernel<BN, GATED>, &cfg);
         if (e != cudaSuccess || n < 1) n = sm_count() / 2;
         max_clusters[dev] = n;
     }
     p.ttiles = (p.m + BN - 1) / BN;
     p.nunits = p.ttiles * ((ftiles + 1) / 2);
     const int clusters = p.nunits < max_clusters[dev] ? p.nunits : max_clusters[dev];
-    q8_gemm_kernel<BN><<<2 * clusters, NTHREADS, smem, stream>>>(p);
+    q8_gemm_kernel<BN, GATED><<<2 * clusters, NTHREADS, smem, stream>>>(p);
     e = cudaGetLastError();
     return e == cudaSuccess ? TE_OK : cuda_fail(e, "q8_linear launch");
 }
@@ -553,6 +627,10 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         if (!aligned16(src.w.q) || !aligned16(src.y) || (reinterpret_cast<uintptr_t>(src.w.scale) & 3) ||
             (src.w.bias && (reinterpret_cast<uintptr_t>(src.w.bias) & 3)))
             return fail(TE_EALIGN, "q8_linear: item %d: q and y must be 16-byte aligned", i);
+        if (src.epilogue < TE_EPI_NONE || src.epilogue > TE_EPI_SILU)
+            return fail(TE_EINVAL, "q8_linear: item %d bad epilogue %d", i, src.epilogue);
+        if (src.epilogue != TE_EPI_NONE && src.residual)
+            return fail(TE_EINVAL, "q8_linear: item %d: an epilogue activation takes no residual", i);
         if (src.residual) {
             if (src.ldr < src.w.n) return fail(TE_ESHAPE, "q8_linear: item %d ldr < n", i);
             if (!aligned16(src.residual) || src.ldr % 4)
@@ -569,6 +647,7 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         d.ldr = src.ldr;
         d.n = src.w.n;
         d.ydt = src.y_dtype;
+        d.act = src.epilogue;
         d.tile0 = ftiles;
         d.ntiles = (src.w.n + BM - 1) / BM;
         ftiles += d.ntiles;
@@ -585,7 +664,61 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         if (st != TE_OK) return st;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (bn == 192) return launch<192>(p, ftiles, s);
-    if (bn == 128) return launch<128>(p, ftiles, s);
-    return launch<64>(p, ftiles, s);
+    if (bn == 192) return launch<192, false>(p, ftiles, s);
+    if (bn == 128) return launch<128, false>(p, ftiles, s);
+    return launch<64, false>(p, ftiles, s);
+}
+
+extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, int32_t k,
+                                        const te_q8w *wg, const te_q8w *wu, int32_t act, void *out,
+                                        int64_t ldm, te_stream stream) {
+    if (!x || !wg || !wu || !out) return fail(TE_EINVAL, "q8_gated_linear: NULL x, wg, wu or out");
+    if (act != TE_ACT_GELU_TANH && act != TE_ACT_SILU) return fail(TE_EINVAL, "q8_gated_linear: bad act");
+    if (m < 0 || k < 64 || k % 64) return fail(TE_ESHAPE, "q8_gated_linear: m=%d k=%d (k %% 64 == 0)", m, k);
+    if (ldx < k || ldx % 8) return fail(TE_ESHAPE, "q8_gated_linear: ldx=%lld (>= k, multiple of 8)", (long long)ldx);
+    if (!wg->q || !wg->scale || !wu->q || !wu->scale)
+        return fail(TE_EINVAL, "q8_gated_linear: NULL q or scale");
+    if (wg->k != k || wu->k != k || wg->n != wu->n)
+        return fail(TE_ESHAPE, "q8_gated_linear: wg [%d, %d] and wu [%d, %d] must both be [f, %d]", wg->n,
+                    wg->k, wu->n, wu->k, k);
+    const int f = wg->n;
+    if (f < 32 || f % 32) return fail(TE_ESHAPE, "q8_gated_linear: f=%d (multiple of 32)", f);
+    if (ldm < f || ldm % 8) return fail(TE_ESHAPE, "q8_gated_linear: ldm=%lld (>= f, multiple of 8)", (long long)ldm);
+    if (!aligned16(x) || !aligned16(out) || !aligned16(wg->q) || !aligned16(wu->q) ||
+        (reinterpret_cast<uintptr_t>(wg->scale) & 3) || (reinterpret_cast<uintptr_t>(wu->scale) & 3) ||
+        (wg->bias && (reinterpret_cast<uintptr_t>(wg->bias) & 3)) ||
+        (wu->bias && (reinterpret_cast<uintptr_t>(wu->bias) & 3)))
+        return fail(TE_EALIGN, "q8_gated_linear: x, out and q must be 16-byte aligned");
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.z = 1;
+    p.m = m;
+    p.k = k;
+    Item &d = p.it[0];
+    d.scale = wg->scale;
+    d.bias = wg->bias;
+    d.scale2 = wu->scale;
+    d.bias2 = wu->bias;
+    d.y = out;
+    d.ldy = ldm;
+    d.n = f;
+    d.ydt = TE_BF16;
+    d.act = act;
+    d.tile0 = 0;
+    d.ntiles = (f + BM / 2 - 1) / (BM / 2);
+    if (m == 0) return TE_OK;
+    const int bn = m >= 1024 ? 192 : (m > 64 ? 128 : 64);
+    te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
+                               (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != TE_OK) return st;
+    if ((st = make_map_2d(&p.tw[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, wg->q, (uint64_t)k, (uint64_t)f,
+                          (uint64_t)k, BOX, BM / 2, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_OK)
+        return st;
+    if ((st = make_map_2d(&p.tw[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, wu->q, (uint64_t)k, (uint64_t)f,
+                          (uint64_t)k, BOX, BM / 2, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bn == 192) return launch<192, true>(p, d.ntiles, s);
+    if (bn == 128) return launch<128, true>(p, d.ntiles, s);
+    return launch<64, true>(p, d.ntiles, s);
 }

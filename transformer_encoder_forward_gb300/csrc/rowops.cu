@@ -310,12 +310,6 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
 
 // ---------------------------------------------------------------- gate_act
 
-__device__ __forceinline__ float act_fn(float g, int act) {
-    if (act == TE_ACT_GELU_TANH)
-        return 0.5f * g * (1.f + tanhf(0.7978845608028654f * (g + 0.044715f * g * g * g)));
-    return g / (1.f + expf(-g));
-}
-
 __global__ void __launch_bounds__(256) gate_act_kernel(const __nv_bfloat16 *__restrict__ gu,
                                                        long long ld, int u_off, int act,
                                                        __nv_bfloat16 *__restrict__ m,
@@ -332,10 +326,10 @@ __global__ void __launch_bounds__(256) gate_act_kernel(const __nv_bfloat16 *__re
             float u[8];
             load8(gu + row * ld + u_off + c, u);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = act_fn(g[e], act) * u[e];
+            for (int e = 0; e < 8; ++e) o[e] = apply_act(g[e], act) * u[e];
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = act_fn(g[e], act);
+            for (int e = 0; e < 8; ++e) o[e] = apply_act(g[e], act);
         }
         store8(m + row * ldm + c, o);
     }
