@@ -255,7 +255,9 @@ def test_rownorm_matches_oracle(d, kind, xdt):
 
 
 @pytest.mark.parametrize("d,sandwich,nxt,kind", [(512, True, True, "rms"), (3840, True, False, "rms"),
-                                                 (768, False, True, "ln"), (256, False, False, "rms")])
+                                                 (768, False, True, "ln"), (256, False, False, "rms"),
+                                                 (3840, True, True, "rms"), (2048, False, True, "ln"),
+                                                 (4096, True, True, "ln"), (1032, True, True, "rms")])
 def test_add_norm_matches_oracle(d, sandwich, nxt, kind):
     torch = _torch()
     rng = np.random.default_rng([d, int(sandwich), int(nxt)])

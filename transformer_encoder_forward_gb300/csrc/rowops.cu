@@ -211,6 +211,113 @@ __global__ void __launch_bounds__(256) add_norm_kernel(float *h, const float *__
                              a + (long long)row * d);
 }
 
+// Wide rows (d > 1024): four warps per row, two rows per 256-thread CTA.
+// Each thread holds at most NV 8-column chunks of t and of h, all loaded up
+// front (more bytes in flight per SM than one warp per row allows); the row
+// reductions go through shared memory.
+template <int NV>
+__device__ __forceinline__ float row4_sum(float x, float (*red)[4], int slot, int wr, int lane) {
+    x = warp_sum(x);
+    if (lane == 0) red[slot][wr] = x;
+    __syncthreads();
+    const float s = (red[slot][0] + red[slot][1]) + (red[slot][2] + red[slot][3]);
+    __syncthreads();
+    return s;
+}
+
+template <typename Tout, int NV>
+__global__ void __launch_bounds__(256) add_norm_wide_kernel(float *h, const float *__restrict__ t,
+                                                            const float *__restrict__ w_post,
+                                                            float post,
+                                                            const float *__restrict__ w_next,
+                                                            const float *__restrict__ b_next, int kind,
+                                                            float eps, Tout *a, int rows, int d) {
+    __shared__ float red[2][4];
+    const int slot = threadIdx.x >> 7, tid = threadIdx.x & 127;
+    const int wr = tid >> 5, lane = tid & 31;
+    const int row = blockIdx.x * 2 + slot;
+    const bool active = row < rows;            // inactive threads still join the barriers
+    float *hr = h + (long long)(active ? row : 0) * d;
+    const float *tr = t ? t + (long long)(active ? row : 0) * d : nullptr;
+    float tv[NV][8], hv[NV][8];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = (i * 128 + tid) * 8;
+        if (active && c < d) {
+            if (tr) load8(tr + c, tv[i]);
+            load8(hr + c, hv[i]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tv[i][e] = hv[i][e] = 0.f;
+        }
+    }
+    if (tr) {
+        float inv_t = 1.f;
+        if (w_post) {
+            float q = 0.f;
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q += tv[i][e] * tv[i][e];
+            inv_t = rsqrtf(row4_sum<NV>(q, red, slot, wr, lane) / (float)d + eps);
+        }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = (i * 128 + tid) * 8;
+            if (active && c < d) {
+                if (w_post) {
+                    float wv[8];
+                    load8(w_post + c, wv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) hv[i][e] = (hv[i][e] + tv[i][e] * inv_t * wv[e]) * post;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) hv[i][e] += tv[i][e];
+                }
+                store8(hr + c, hv[i]);
+            }
+        }
+    }
+    if (!w_next) return;                       // uniform across the CTA
+    float mean = 0.f;
+    if (kind == TE_NORM_LN) {
+        float s1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s1 += hv[i][e];
+        mean = row4_sum<NV>(s1, red, slot, wr, lane) / (float)d;
+    }
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = (i * 128 + tid) * 8;
+        if (c < d)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q += (hv[i][e] - mean) * (hv[i][e] - mean);
+    }
+    const float inv = rsqrtf(row4_sum<NV>(q, red, slot, wr, lane) / (float)d + eps);
+    const float *bn = kind == TE_NORM_LN ? b_next : nullptr;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = (i * 128 + tid) * 8;
+        if (active && c < d) {
+            float wv[8], o[8];
+            load8(w_next + c, wv);
+            if (bn) {
+                float bv[8];
+                load8(bn + c, bv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = (hv[i][e] - mean) * inv * wv[e] + bv[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = (hv[i][e] - mean) * inv * wv[e];
+            }
+            store8(a + (long long)row * d + c, o);
+        }
+    }
+}
+
 // ------------------------------------------------------------- qk prep + RoPE
 
 // One warp per packed row.  Each lane owns 8 consecutive channels (one
@@ -477,6 +584,17 @@ te_status te_add_norm(float *h, const float *t, const float *w_post, float post,
         (w_next && !aligned16(w_next)) || (b_next && !aligned16(b_next)) || (a && !aligned16(a)))
         return fail(TE_EALIGN, "add_norm: pointers must be 16-byte aligned");
     if (rows == 0) return TE_OK;
+    if (d > 1024) {
+        // four warps per row (d <= 4096: at most 4 chunks of 8 per thread)
+        const dim3 grid2((rows + 1) / 2);
+        if (adt == TE_F32)
+            add_norm_wide_kernel<float, 4><<<grid2, 256, 0, stream>>>(h, t, w_post, post, w_next, b_next,
+                                                                      kind, eps, (float *)a, rows, d);
+        else
+            add_norm_wide_kernel<__nv_bfloat16, 4><<<grid2, 256, 0, stream>>>(
+                h, t, w_post, post, w_next, b_next, kind, eps, (__nv_bfloat16 *)a, rows, d);
+        return launched("add_norm launch");
+    }
     const dim3 grid((rows + 7) / 8);
     TE_NV_SWITCH(nv_for(d), {
         if (adt == TE_F32)
