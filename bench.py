@@ -14,9 +14,11 @@ launching stream.
 the method, test infrastructure) on a bounded sample of the same workload on
 this machine's host cores; it is the slow baseline, not a target.
 
-Multi-GPU: sequences are independent and the forward has no exchange step,
-so N ranks run N independent replicas (weak scaling, no data-path
-collective); value = the work of all ranks / the slowest rank's time.
+Multi-GPU: sequences are independent and the forward has no exchange step.
+With N ranks the packed batch is N draws of the one-GPU batch, split along
+sequence boundaries into N shares of near-equal work (shard.partition), one
+per rank (weak scaling, no data-path collective); value = the work of all
+ranks / the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -156,17 +158,28 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def build_stack(key, device):
+def build_stack(key, device, lens=None, x_seed_offset=0):
     from transformer_encoder_forward_gb300.model import EncoderStack
     cfg = synth.CONFIGS[key]
-    lens = synth.draw_lens(cfg)
+    lens = synth.draw_lens(cfg) if lens is None else np.asarray(lens, dtype=np.int32)
     seed = synth.config_seed(key)
     layers = [synth.draw_layer(cfg, i, seed, jitter=False) for i in range(cfg.layers)]
     tables = synth.rope_tables(cfg, lens)
     fin = synth.draw_final_norm(cfg, seed) if cfg.pool else None
     st = EncoderStack(cfg, layers, lens, tables, fin, device=device)
-    x0 = synth.draw_x(st.T, cfg.d, seed)
+    x0 = synth.draw_x(st.T, cfg.d, seed + x_seed_offset)
     return cfg, lens, st, x0, layers, tables
+
+
+def rank_lens(key, world, rank):
+    """This rank's share of the packed batch of a `world`-GPU run."""
+    from transformer_encoder_forward_gb300 import shard
+    cfg = synth.CONFIGS[key]
+    if world == 1:
+        return synth.draw_lens(cfg)
+    allv = shard.global_lens(cfg, world, lambda c, r: synth.draw_lens(c, synth.BASE_SEED + r))
+    part = shard.partition(shard.sequence_costs(cfg, allv), world)
+    return allv[part[rank]]
 
 
 # --------------------------------------------------------------- GPU timing
@@ -348,11 +361,15 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     import transformer_encoder_forward_gb300 as te
+    from transformer_encoder_forward_gb300 import shard
     te.lib()
-    cfg, lens, st, x0_np, _, _ = build_stack(args.config, dev)
+    cfg, lens, st, x0_np, _, _ = build_stack(args.config, dev, rank_lens(args.config, world, rank),
+                                             x_seed_offset=rank)
     T = st.T
     gflops, aflops = forward_flops(cfg, lens)
     total_flops = gflops + aflops
+    all_flops = shard.sum_over_ranks(total_flops, dist)
+    all_tokens = shard.sum_over_ranks(T, dist)
     x0 = torch.from_numpy(x0_np).to(dev)
     x, a, out = st.buffers()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -400,11 +417,7 @@ def run_ours(args):
         dist.barrier()
     te.check(stream)
     step_ms = [s.elapsed_time(e) for s, e in evs]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = shard.max_over_ranks(sum(step_ms) / len(step_ms), dist)
     clk = clocks.summary()
 
     # end to end through the public API from pinned host memory (eager calls)
@@ -424,7 +437,7 @@ def run_ours(args):
             e.record(stream)
             e2e.append((s, e))
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(s.elapsed_time(e) for s, e in e2e)
+    e2e_ms = shard.max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in e2e), dist)
     te.check(stream)
 
     # per-kernel device times with the workload's shapes -> roofline
@@ -444,7 +457,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(cfg, args.config, budget_s=args.cpu_seconds)
 
-    tflops = total_flops / (ms * 1e-3) / 1e12 * world
+    tflops = all_flops / (ms * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -453,11 +466,12 @@ def run_ours(args):
         "config": {"workload": cfg.name, "layers": cfg.layers, "tokens": T, "seqs": len(lens),
                    "d": cfg.d, "heads": cfg.heads, "head_dim": cfg.hd, "ffn": cfg.ffn,
                    "l2": "flushed before every step (512 MiB write)", "graph": "one CUDA graph per forward",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "tokens_per_s": round(T * world / (ms * 1e-3), 1),
+                   "parallelism": (f"data-parallel x{world}: sequences split by work, "
+                                   f"{int(all_tokens)} tokens in all") if world > 1 else "single GPU"},
+        "tokens_per_s": round(all_tokens / (ms * 1e-3), 1),
         "pct_bf16_peak": round(100 * tflops / world / peaks["bf16_tflops"], 2),
         "flops_per_step": {"gemm": gflops, "attention": aflops},
-        "e2e": {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(all_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": x_host.numel() * 4,
                 "d2h_bytes_per_step": res_host.numel() * 4,
                 "path": "EncoderStack.forward_host: pinned H2D, eager C-ABI calls, D2H of the result"},
