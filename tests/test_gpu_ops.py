@@ -44,6 +44,12 @@ GEMM_CASES = [
     (1000, 192, [64, 128, 192, 288], True, True, "f32"),
     (2112, 3840, [384], False, False, "f32"),
     (4100, 320, [640], False, False, "bf16"),
+    # two 192-token tiles per weight stage (many feature tiles, ragged last pair)
+    (3000, 256, [3840, 3840], True, False, "bf16"),
+    (3000, 256, [3840, 3840], False, True, "f32"),
+    # a residual other than y (f32 and bf16 y), rows wider than n
+    (300, 512, [96, 160], True, "sep", "f32"),
+    (777, 256, [256, 512], False, "sep", "bf16"),
 ]
 
 
@@ -59,20 +65,32 @@ def test_q8_linear_matches_oracle(m, k, ns, bias, resid, ydt):
         q, s, b = q8_dev(w)
         n = w["q"].shape[0]
         r_np = rng.standard_normal((m, n)).astype(np.float32) if resid else None
-        y = to_dev(r_np) if resid else torch.full((m, n), float("nan"), dtype=dt, device="cuda")
-        it = {"w": te.q8w(q, s, b), "y": y, "ldy": n}
-        if resid:
-            it.update(residual=y, ldr=n)       # in place: y = y + s*acc + b
+        if resid == "sep":
+            # separate residual and output, both with padded rows
+            r_dev = torch.zeros(m, n + 8, dtype=torch.float32, device="cuda")
+            r_dev[:, :n] = to_dev(r_np)
+            y_full = torch.full((m, n + 16), float("nan"), dtype=dt, device="cuda")
+            y = y_full[:, :n]
+            it = {"w": te.q8w(q, s, b), "y": y, "ldy": n + 16, "residual": r_dev, "ldr": n + 8}
+            outs_keep = (r_dev, y_full)
+        else:
+            y = to_dev(r_np) if resid else torch.full((m, n), float("nan"), dtype=dt, device="cuda")
+            it = {"w": te.q8w(q, s, b), "y": y, "ldy": n}
+            outs_keep = None
+            if resid:
+                it.update(residual=y, ldr=n)       # in place: y = y + s*acc + b
         items.append(it)
-        outs.append((y, (q, s, b)))
+        outs.append((y, (q, s, b, outs_keep)))
         ref = O.q8_linear(x64, w["q"], w["s"], w["b"], r_np)
         refs.append(O.round_bf16(ref) if ydt == "bf16" else ref)
     te.q8_linear(x, items)
     te.check()
-    for (y, _), ref in zip(outs, refs):
+    for (y, (_, _, _, keep)), ref in zip(outs, refs):
         got = to_np(y)
         assert np.all(np.isfinite(got))
         assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
+        if keep is not None:                   # the row padding of y is untouched
+            assert bool(torch.isnan(keep[1][:, y.shape[1]:]).all())
 
 
 def test_q8_linear_exact_integer_case_is_bit_exact():

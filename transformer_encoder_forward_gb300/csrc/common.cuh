@@ -197,6 +197,42 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint3
         : "memory");
 }
 
+// Tensor store of a box from shared memory (plain layout, no swizzle) to
+// global memory at element coordinates (c0 inner, c1 outer); rows past the
+// tensor's extent are not written.  c0 * element size must be a multiple of
+// 16 bytes and neither coordinate may be negative.
+__device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// As tma_store_2d, but adds the box into global memory (f32: one rounding).
+__device__ __forceinline__ void tma_reduce_add_2d(const void *map, uint32_t src, int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until the bulk stores committed so far have finished reading shared
+// memory (the source buffer may be overwritten).
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until the bulk stores committed so far are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's shared-memory writes before later bulk (async proxy) reads.
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -32,10 +32,14 @@
 //     tcgen05.commit; the converters and epilogue warps of both CTAs report to
 //     the leader's barriers through their cluster addresses;
 //   * warps 10-13 drain the other accumulator meanwhile (tcgen05.ld): lane =
-//     output feature, so the row scale and bias are per-thread constants and
-//     every store instruction writes 32 consecutive features of one token.
-// TMEM: 2 accumulators of BN columns + 2 A stages of 64 columns (= 512 for
-// BN = 192).  A stage is 8 MMAs deep, so the barrier round trip between
+//     output feature, so the row scale and bias are per-thread constants;
+//     each 32 x 32 block is written into a staging tile in the output's own
+//     layout and leaves with one TMA tensor store (a TMA reduce-add when the
+//     residual is y itself, the in-place x += proj of the plain block).
+// With long K a unit can hold two token tiles: each widened weight stage then
+// feeds both tiles' MMAs (see tokens_per_stage).
+// TMEM: 2 accumulators of BN columns + as many A stages of 64 columns as fit
+// in the 512 (2 for BN = 192, 3 for 160, 4 for 128 and 64).  A stage is 8 MMAs deep, so the barrier round trip between
 // stages (about 0.1-0.2 us for the issuing thread) is amortised over 768
 // tensor-core cycles.  Every mbarrier wait is bounded (about 200 ms); a timeout sets
 // an error word that te_check() reports, the role stops, and the kernel still
@@ -52,7 +56,6 @@ namespace {
 constexpr int BM = 128;       // weight rows (output features) per tile = TMEM lanes
 constexpr int BK = 128;       // K per pipeline stage (two 64-wide TMA boxes)
 constexpr int BOX = 64;       // K width of one TMA box
-constexpr int NA = 2;         // TMEM stages of the widened A operand (64 columns each)
 constexpr int MAXZ = 4;
 constexpr int NWARPS = 14;    // producer, MMA, 8 converters, 4 epilogue
 constexpr int NTHREADS = NWARPS * 32;
@@ -71,33 +74,44 @@ struct Item {
 struct Params {
     CUtensorMap tx;           // x: bf16 [m, k]
     CUtensorMap tw[MAXZ];     // q_i: int8 [n_i, k]
+    CUtensorMap ty[MAXZ];     // y_i: [m, n_i] (f32 or bf16), 32-feature boxes
     Item it[MAXZ];
     int z, m, k, ttiles, nunits;
 };
 
 __device__ int g_gemm_err;
 
-template <int BN>
+template <int BN, int TPA>
 struct Layout {
     static constexpr int HALF = BN / 2;                 // token rows each CTA of the pair holds
-    static constexpr int NST = BN >= 192 ? 5 : 6;       // shared-memory load stages
+    // shared-memory load stages (a stage holds TPA token tiles)
+    static constexpr int NST = TPA == 2 ? 3 : (BN >= 160 ? 5 : 6);
+    // TMEM stages of the widened A operand (64 columns each): what the two
+    // BN-column accumulators leave of the 512 columns, at most 4
+    static constexpr int NA = (512 - 2 * BN) / 64 < 4 ? (512 - 2 * BN) / 64 : 4;
     static constexpr int XBOX = HALF * BOX * 2;         // one 64-wide box of this CTA's activation half
-    static constexpr int XBYTES = 2 * XBOX;             // this CTA's half of the activation stage
+    static constexpr int XTILE = 2 * XBOX;              // this CTA's half of one token tile's stage
+    static constexpr int XBYTES = TPA * XTILE;          // ... of all TPA token tiles
     static constexpr int WBOX = BM * BOX;               // one 64-wide box of the int8 weight tile
     static constexpr int WBYTES = 2 * WBOX;             // int8 weight stage (own 128 rows)
     static constexpr int X_OFF = 0;
     static constexpr int W_OFF = NST * XBYTES;
-    // epilogue staging: one padded 32 x 33 f32 block per epilogue warp
+    // epilogue staging: ungated, one 32 x 32 output tile (f32 or bf16) per
+    // epilogue warp; gated, one padded 32 x 33 f32 exchange block per warp and
+    // a 16 x 32 bf16 output tile per warp.  128-byte aligned (TMA sources).
     static constexpr int STG_OFF = W_OFF + NST * WBYTES;
-    static constexpr int STG_BYTES = 4 * 32 * 33 * 4;
+    static constexpr int XCHG_BYTES = 4 * 32 * 33 * 4;
+    static constexpr int STG_BYTES = XCHG_BYTES + 4 * 1024;
+    static_assert(4 * 4096 <= STG_BYTES && XCHG_BYTES % 128 == 0, "staging");
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
     // barriers: full, empty [NST]; afull, aempty [NA]; accfull, accempty [2]; done
     static constexpr int NBAR = 2 * NST + 2 * NA + 4 + 1;
     static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
     static constexpr int A_COL = 2 * BN;                // first TMEM column of the A stages
-    static constexpr int TMEM_COLS = (2 * BN + NA * 64 <= 256) ? 256 : 512;
-    static_assert(2 * BN + NA * 64 <= TMEM_COLS, "TMEM budget");
+    static constexpr int TMEM_COLS = 512;
+    static_assert(NA >= 2 && 2 * BN + NA * 64 <= TMEM_COLS, "TMEM budget");
     static_assert(XBOX % 1024 == 0, "swizzled boxes stay 1024-byte aligned");
+    static_assert(BYTES + 1024 <= 227 * 1024, "shared memory per CTA");
 };
 
 // int8 x4 -> two bf16x2 words, exactly.  (b ^ 0x80) is q + 128; placed as the
@@ -186,11 +200,12 @@ __device__ __forceinline__ void pair_sync(int pair) {
     asm volatile("bar.sync %0, 64;" ::"r"(pair + 1) : "memory");
 }
 
-template <int BN, bool GATED>
+template <int BN, bool GATED, int TPA>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     q8_gemm_kernel(const __grid_constant__ Params p) {
-    using L = Layout<BN>;
+    using L = Layout<BN, TPA>;
     constexpr int NST = L::NST;
+    constexpr int NA = L::NA;
     constexpr int HALF = L::HALF;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -257,8 +272,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const uint32_t wdst = sb + L::W_OFF + s * L::WBYTES + c * L::WBOX;
-                        tma_load_2d(sb + L::X_OFF + s * L::XBYTES + c * L::XBOX, &p.tx, bar_full + 8 * s,
-                                    kb * BK + c * BOX, tc.t0 * BN + rank * HALF);
+#pragma unroll
+                        for (int tt = 0; tt < TPA; ++tt)
+                            tma_load_2d(sb + L::X_OFF + s * L::XBYTES + tt * L::XTILE + c * L::XBOX, &p.tx,
+                                        bar_full + 8 * s, kb * BK + c * BOX, (tc.t0 * TPA + tt) * BN + rank * HALF);
                         if (GATED) {   // rows 0-63: gate, rows 64-127: up, same features
                             tma_load_2d(wdst, &p.tw[0], bar_full + 8 * s, kb * BK + c * BOX, tc.o0);
                             tma_load_2d(wdst + (BM / 2) * BOX, &p.tw[1], bar_full + 8 * s,
@@ -279,10 +296,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
             int kbg = 0, lt = 0;
             for (int u = cid; u < nunits && ok; u += ncl, ++lt) {
-                const int b = lt & 1;
-                if (!mbar_wait_cluster(bar_accempty + 8 * b, ((lt >> 1) & 1) ^ 1)) { ok = false; break; }
+                // TPA == 1: units alternate between the two accumulators;
+                // TPA == 2: a unit's two token tiles use both
+                const int b = TPA == 2 ? 0 : (lt & 1);
+                const uint32_t ph = TPA == 2 ? (lt & 1) : ((lt >> 1) & 1);
+                if (!mbar_wait_cluster(bar_accempty + 8 * b, ph ^ 1)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t dcol = tbase + b * BN;
                 for (int kb = 0; kb < nkb; ++kb, ++kbg) {
                     const int s = kbg % NST, a = kbg % NA;
                     // both CTAs' converters have widened stage a, which they
@@ -292,9 +311,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const uint32_t xs = sb + L::X_OFF + s * L::XBYTES;
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)
-                        mma_ts_pair(dcol, tbase + L::A_COL + 64 * a + 8 * j,
-                                    smem_desc_sw128(xs + (j >> 2) * L::XBOX + (j & 3) * 32), idesc,
-                                    (kb | j) != 0);
+#pragma unroll
+                        for (int tt = 0; tt < TPA; ++tt)
+                            mma_ts_pair(tbase + (TPA == 2 ? tt : b) * BN, tbase + L::A_COL + 64 * a + 8 * j,
+                                        smem_desc_sw128(xs + tt * L::XTILE + (j >> 2) * L::XBOX + (j & 3) * 32),
+                                        idesc, (kb | j) != 0);
                     mma_commit_pair(bar_empty + 8 * s, 0x3);
                     mma_commit_pair(bar_aempty + 8 * a, 0x3);
                 }
@@ -338,14 +359,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
     } else {
         // ----------------------------------------------------------- epilogue
+        // Lane = output feature: each 32 (features) x 32 (tokens) block is
+        // scaled in registers, written to a staging tile in the output's own
+        // layout (token rows, features contiguous) and sent out with one TMA
+        // tensor store - or a TMA reduce-add when the residual is y itself.
         const int q = warp & 3;
         const int row = 32 * q + lane;
         const uint32_t tl = (uint32_t)(32 * q) << 16;
         int lt = 0;
         __shared__ int s_pair_ok[2][4];
+        // gated: the exchange blocks of the gate/up warp pairs, then one
+        // 16-token output tile per warp; ungated: one 32-token tile per warp
+        float *xchg = reinterpret_cast<float *>(smem + L::STG_OFF);
+        const uint32_t ostg_off = L::STG_OFF + (GATED ? L::XCHG_BYTES + (warp - 10) * 1024 : (warp - 10) * 4096);
+        const uint32_t ostg = sb + ostg_off;                 // the TMA source (shared address)
+        float *ostg_f = reinterpret_cast<float *>(smem + ostg_off);
+        __nv_bfloat16 *ostg_h = reinterpret_cast<__nv_bfloat16 *>(smem + ostg_off);
         for (int u = cid; u < nunits && ok; u += ncl, ++lt) {
-            const int b = lt & 1;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_accfull + 8 * b, (lt >> 1) & 1));
+            const int b = TPA == 2 ? 0 : (lt & 1);
+            const uint32_t ph = TPA == 2 ? (lt & 1) : ((lt >> 1) & 1);
+            // this tile's row scale and bias before the wait: their load
+            // latency overlaps the mainloop
+            const TileCoord tc = tile_coord<GATED>(p, u, rank);
+            const bool upper = GATED && row >= BM / 2;
+            const int o = tc.o0 + (GATED ? (row & (BM / 2 - 1)) : row);
+            const bool ov = o < p.it[tc.zi].n;
+            const float *scale = upper ? p.it[tc.zi].scale2 : p.it[tc.zi].scale;
+            const float *bias = upper ? p.it[tc.zi].bias2 : p.it[tc.zi].bias;
+            const float sc = ov ? scale[o] : 0.f;
+            const float bi = (ov && bias) ? bias[o] : 0.f;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_accfull + 8 * b, ph));
             if (GATED) {
                 // the gate and up warps of a pair meet at named barriers below:
                 // they continue or stop together
@@ -355,126 +398,109 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
             if (!ok) break;
             tc_fence_after();
-            const TileCoord tc = tile_coord<GATED>(p, u, rank);
-            // the item's fields in registers: the stores below cannot alias them
-            // (gated: lanes 0-63 hold gate rows, 64-127 the up rows of the same features)
-            const bool upper = GATED && row >= BM / 2;
-            const int o = tc.o0 + (GATED ? (row & (BM / 2 - 1)) : row);
-            const bool ov = o < p.it[tc.zi].n;
-            const float *scale = upper ? p.it[tc.zi].scale2 : p.it[tc.zi].scale;
-            const float *bias = upper ? p.it[tc.zi].bias2 : p.it[tc.zi].bias;
-            const float sc = ov ? scale[o] : 0.f;
-            const float bi = (ov && bias) ? bias[o] : 0.f;
             const int act = p.it[tc.zi].act;
-            const int t0 = tc.t0 * BN;
-            const long long ldy = p.it[tc.zi].ldy, ldr = p.it[tc.zi].ldr;
+            const int n = p.it[tc.zi].n;
+            const void *ymap = &p.ty[tc.zi];
+            const long long ldr = p.it[tc.zi].ldr;
             const bool f32out = p.it[tc.zi].ydt == TE_F32;
-            char *__restrict__ ybase = reinterpret_cast<char *>(p.it[tc.zi].y);
             const float *__restrict__ rbase = p.it[tc.zi].resid;
-            // Each 32 (features) x 32 (tokens) block goes through a padded
-            // shared-memory transpose, so that every lane then writes 16
-            // contiguous bytes along the feature axis: a warp store covers
-            // 4 (f32) or 8 (bf16) token rows instead of one.
-            float *stg = reinterpret_cast<float *>(smem + L::STG_OFF) + (warp - 10) * 32 * 33;
+            const bool inplace = rbase != nullptr && rbase == p.it[tc.zi].y;
+            for (int tt = 0; tt < TPA; ++tt) {
+            const int acol = (TPA == 2 ? tt : b) * BN;     // this token tile's accumulator
+            const int t0 = (tc.t0 * TPA + tt) * BN;
             if (GATED) {
-                // warps q and q+2 hold the gate and the up values of the same
-                // 32 features: both stage their (bf16-rounded) block, then
+                // warps q and q+2 hold the up and the gate values of the same
+                // 32 features (warp 10 + i holds quadrant (2 + i) & 3: the gate
+                // warps are 12, 13); both stage their bf16-rounded block, then
                 // each writes m = act(g) * u for 16 of the 32 tokens
-                // (warp 10 + i holds quadrant (2 + i) & 3: the gate warps are 12, 13)
-                float *stg_u = reinterpret_cast<float *>(smem + L::STG_OFF) + (q & 1) * 32 * 33;
-                float *stg_g = stg_u + 2 * 32 * 33;
+                float *stg = xchg + (warp - 10) * 32 * 33;
+                const float *stg_u = xchg + (q & 1) * 32 * 33;
+                const float *stg_g = stg_u + 2 * 32 * 33;
                 const int fo = tc.o0 + 32 * (q & 1);
                 const int jbase = q < 2 ? 0 : 16;
                 for (int c = 0; c < BN / 32; ++c) {
-                    if (t0 + 32 * c >= p.m) break;      // warp-uniform
+                    if (t0 + 32 * c >= p.m) break;      // uniform over the pair
                     uint32_t v[32];
-                    tmem_ld32(tbase + tl + b * BN + 32 * c, v);
+                    tmem_ld32(tbase + tl + acol + 32 * c, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) stg[j * 33 + lane] = round_bf16(__uint_as_float(v[j]) * sc + bi);
                     pair_sync(q & 1);
-                    const long long tb = t0 + 32 * c;
-                    if (fo < p.it[tc.zi].n) {
-                        const int fl = 8 * (lane & 3);
+                    const int tb = t0 + 32 * c + jbase;
+                    if (lane == 0) bulk_wait_read();       // the previous tile has left ostg
+                    __syncwarp();
+                    float yv[16];
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            const int j = jbase + (lane >> 2) + 8 * i;
-                            if (tb + j < p.m) {
-                                float y[8];
+                    for (int j = 0; j < 16; ++j)
+                        yv[j] = apply_act(stg_g[(jbase + j) * 33 + lane], act) * stg_u[(jbase + j) * 33 + lane];
 #pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    y[e] = apply_act(stg_g[j * 33 + fl + e], act) * stg_u[j * 33 + fl + e];
-                                uint4 pk;
-                                pk.x = pack_bf16x2(y[0], y[1]); pk.y = pack_bf16x2(y[2], y[3]);
-                                pk.z = pack_bf16x2(y[4], y[5]); pk.w = pack_bf16x2(y[6], y[7]);
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(ybase) +
-                                                           (tb + j) * ldy + fo + fl) = pk;
-                            }
-                        }
+                    for (int j = 0; j < 16; ++j) ostg_h[j * 32 + lane] = __float2bfloat16_rn(yv[j]);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && fo < n && tb < p.m) {
+                        tma_store_2d(ymap, ostg, fo, tb);
+                        bulk_commit();
                     }
                     pair_sync(q & 1);
                 }
             } else {
-            const int fo = tc.o0 + 32 * q;                  // first feature of this warp's block
-            for (int c = 0; c < BN / 32; ++c) {
-                if (t0 + 32 * c >= p.m) break;          // warp-uniform
-                uint32_t v[32];
-                tmem_ld32(tbase + tl + b * BN + 32 * c, v);
-                tmem_wait_ld();
-                if (act) {   // the ungated MLP: act(bf16(s*acc + b)), no residual
+                const int fo = tc.o0 + 32 * q;              // first feature of this warp's block
+                for (int c = 0; c < BN / 32; ++c) {
+                    if (t0 + 32 * c >= p.m) break;      // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld32(tbase + tl + acol + 32 * c, v);
+                    tmem_wait_ld();
+                    const int tb = t0 + 32 * c;
+                    // v[] becomes the output values in place (f32 bits)
+                    if (act) {   // the ungated MLP: act(bf16(s*acc + b)), no residual
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        stg[j * 33 + lane] = apply_act(round_bf16(__uint_as_float(v[j]) * sc + bi), act - 1);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) stg[j * 33 + lane] = __uint_as_float(v[j]) * sc + bi;
-                }
-                __syncwarp();
-                const long long tb = t0 + 32 * c;
-                if (fo < p.it[tc.zi].n) {
-                    if (f32out) {
-                        const int fl = 4 * (lane & 7);     // 4 features of one token row
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int j = (lane >> 3) + 4 * i;
-                            if (tb + j < p.m) {
-                                float4 y = make_float4(stg[j * 33 + fl], stg[j * 33 + fl + 1],
-                                                       stg[j * 33 + fl + 2], stg[j * 33 + fl + 3]);
-                                if (rbase) {
-                                    const float4 r = *reinterpret_cast<const float4 *>(
-                                        rbase + (tb + j) * ldr + fo + fl);
-                                    y.x += r.x; y.y += r.y; y.z += r.z; y.w += r.w;
-                                }
-                                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(ybase) +
-                                                            (tb + j) * ldy + fo + fl) = y;
-                            }
-                        }
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = __float_as_uint(apply_act(round_bf16(__uint_as_float(v[j]) * sc + bi), act - 1));
                     } else {
-                        const int fl = 8 * (lane & 3);     // 8 features of one token row
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int j = (lane >> 2) + 8 * i;
-                            if (tb + j < p.m) {
-                                float y[8];
+                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sc + bi);
+                    }
+                    if (lane == 0) bulk_wait_read();       // the previous tile has left ostg
+                    __syncwarp();
+                    if (rbase && !inplace) {
+                        // a residual other than y (not used by the block): stage
+                        // f32, add the residual rows from global memory, then
+                        // narrow in place if y is bf16.  Row j's bf16 bytes only
+                        // cover f32 rows <= j, which were read before.
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) y[e] = stg[j * 33 + fl + e];
-                                if (rbase) {
-                                    const float *rr = rbase + (tb + j) * ldr + fo + fl;
-                                    const float4 r0 = *reinterpret_cast<const float4 *>(rr);
-                                    const float4 r1 = *reinterpret_cast<const float4 *>(rr + 4);
-                                    y[0] += r0.x; y[1] += r0.y; y[2] += r0.z; y[3] += r0.w;
-                                    y[4] += r1.x; y[5] += r1.y; y[6] += r1.z; y[7] += r1.w;
-                                }
-                                uint4 pk;
-                                pk.x = pack_bf16x2(y[0], y[1]); pk.y = pack_bf16x2(y[2], y[3]);
-                                pk.z = pack_bf16x2(y[4], y[5]); pk.w = pack_bf16x2(y[6], y[7]);
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(ybase) +
-                                                           (tb + j) * ldy + fo + fl) = pk;
+                        for (int j = 0; j < 32; ++j) ostg_f[j * 32 + lane] = __uint_as_float(v[j]);
+                        __syncwarp();
+                        const float *rr = rbase + (long long)tb * ldr + o;
+                        const int jn = p.m - tb < 32 ? p.m - tb : 32;
+#pragma unroll 1
+                        for (int j = 0; j < jn; ++j)
+                            if (ov) ostg_f[j * 32 + lane] += rr[(long long)j * ldr];
+                        if (!f32out) {
+#pragma unroll 1
+                            for (int j = 0; j < 32; ++j) {
+                                __syncwarp();
+                                const float y = ostg_f[j * 32 + lane];
+                                __syncwarp();
+                                ostg_h[j * 32 + lane] = __float2bfloat16_rn(y);
                             }
                         }
+                    } else if (f32out) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) ostg_f[j * 32 + lane] = __uint_as_float(v[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) ostg_h[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && fo < n) {
+                        if (inplace)
+                            tma_reduce_add_2d(ymap, ostg, fo, tb);
+                        else
+                            tma_store_2d(ymap, ostg, fo, tb);
+                        bulk_commit();
                     }
                 }
-                __syncwarp();
             }
             }
             // this accumulator may take the next tile's MMAs
@@ -482,6 +508,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(accempty_ldr + 8 * b);
         }
+        // the stores must be complete before the CTA's shared memory goes away
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     if (!ok && s_skip == 0) atomicExch(&g_gemm_err, 1);
     tc_fence_before();
@@ -511,9 +540,27 @@ int sm_count() {
     return count[dev];
 }
 
-template <int BN, bool GATED>
+// Token tiles of 192 per unit (1 or 2).  With 2, each widened weight stage
+// feeds the MMAs of two token tiles, which halves the TMEM stores of the
+// widened operand per flop (those stores contend with the MMAs for TMEM), at
+// the price of an accumulator drain that the next unit's MMAs wait for: it
+// pays off only with long K (measured: 1.10-1.16x at K = 3840 and 10240 with
+// 8448 tokens, 0.8x at K = 512 and 2048).  Among those shapes the choice
+// follows the estimated time of the busiest cluster.
+int tokens_per_stage(int m, int k, int ftiles) {
+    if (k < 3072) return 1;
+    const int clusters = sm_count() / 2;
+    const long long fpairs = (ftiles + 1) / 2;
+    const long long u1 = fpairs * ((m + 191) / 192), u2 = fpairs * ((m + 383) / 384);
+    const long long w1 = (u1 + clusters - 1) / clusters, w2 = (u2 + clusters - 1) / clusters;
+    // a two-tile unit takes about 1.5-1.7x as long as a one-tile unit
+    // (measured at K = 3840 and 10240)
+    return (double)w2 * 1.65 < (double)w1 ? 2 : 1;
+}
+
+template <int BN, bool GATED, int TPA>
 te_status launch(Params &p, int ftiles, cudaStream_t stream) {
-    const int smem = Layout<BN>::BYTES + 1024;
+    const int smem = Layout<BN, TPA>::BYTES + 1024;
     // per instantiation and device: dynamic shared memory size, and how many
     // 2-CTA clusters can be resident at once (the persistent grid's size)
     static int max_clusters[64] = {};
@@ -522,7 +569,7 @@ te_status launch(Params &p, int ftiles, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "q8_linear: cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(TE_EINVAL, "q8_linear: device %d out of range", dev);
     if (!max_clusters[dev]) {
-        e = cudaFuncSetAttribute(q8_gemm_kernel<BN, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(q8_gemm_kernel<BN, GATED, TPA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_fail(e, "q8_linear: set shared memory size");
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * sm_count(), 1, 1);
@@ -536,14 +583,14 @@ te_status launch(Params &p, int ftiles, cudaStream_t stream) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, q8_gemm_kernel<BN, GATED>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, q8_gemm_kernel<BN, GATED, TPA>, &cfg);
         if (e != cudaSuccess || n < 1) n = sm_count() / 2;
         max_clusters[dev] = n;
     }
-    p.ttiles = (p.m + BN - 1) / BN;
+    p.ttiles = (p.m + TPA * BN - 1) / (TPA * BN);
     p.nunits = p.ttiles * ((ftiles + 1) / 2);
     const int clusters = p.nunits < max_clusters[dev] ? p.nunits : max_clusters[dev];
-    q8_gemm_kernel<BN, GATED><<<2 * clusters, NTHREADS, smem, stream>>>(p);
+    q8_gemm_kernel<BN, GATED, TPA><<<2 * clusters, NTHREADS, smem, stream>>>(p);
     e = cudaGetLastError();
     return e == cudaSuccess ? TE_OK : cuda_fail(e, "q8_linear launch");
 }
@@ -654,6 +701,7 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
     }
     if (m == 0) return TE_OK;
     const int bn = m >= 1024 ? 192 : (m > 64 ? 128 : 64);
+    const int tpa = bn == 192 ? tokens_per_stage(m, k, ftiles) : 1;
     // each CTA of a cluster pair loads half of the token tile (and multicasts it)
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
                                (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -662,11 +710,16 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         st = make_map_2d(&p.tw[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, items[i].w.q, (uint64_t)k,
                          (uint64_t)items[i].w.n, (uint64_t)k, BOX, BM, CU_TENSOR_MAP_SWIZZLE_64B);
         if (st != TE_OK) return st;
+        const bool f32 = items[i].y_dtype == TE_F32;
+        st = make_map_2d(&p.ty[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         items[i].y, (uint64_t)items[i].w.n, (uint64_t)m,
+                         (uint64_t)items[i].ldy * (f32 ? 4 : 2), 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != TE_OK) return st;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (bn == 192) return launch<192, false>(p, ftiles, s);
-    if (bn == 128) return launch<128, false>(p, ftiles, s);
-    return launch<64, false>(p, ftiles, s);
+    if (bn == 192) return tpa == 2 ? launch<192, false, 2>(p, ftiles, s) : launch<192, false, 1>(p, ftiles, s);
+    if (bn == 128) return launch<128, false, 1>(p, ftiles, s);
+    return launch<64, false, 1>(p, ftiles, s);
 }
 
 extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, int32_t k,
@@ -708,6 +761,7 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     d.ntiles = (f + BM / 2 - 1) / (BM / 2);
     if (m == 0) return TE_OK;
     const int bn = m >= 1024 ? 192 : (m > 64 ? 128 : 64);
+    const int tpa = bn == 192 ? tokens_per_stage(m, k, d.ntiles) : 1;
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
                                (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_OK) return st;
@@ -717,8 +771,12 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     if ((st = make_map_2d(&p.tw[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, wu->q, (uint64_t)k, (uint64_t)f,
                           (uint64_t)k, BOX, BM / 2, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_OK)
         return st;
+    // each epilogue warp of a gate/up pair stores 16 of the 32 tokens of a block
+    if ((st = make_map_2d(&p.ty[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, (uint64_t)f, (uint64_t)m,
+                          (uint64_t)ldm * 2, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_OK)
+        return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (bn == 192) return launch<192, true>(p, d.ntiles, s);
-    if (bn == 128) return launch<128, true>(p, d.ntiles, s);
-    return launch<64, true>(p, d.ntiles, s);
+    if (bn == 192) return tpa == 2 ? launch<192, true, 2>(p, d.ntiles, s) : launch<192, true, 1>(p, d.ntiles, s);
+    if (bn == 128) return launch<128, true, 1>(p, d.ntiles, s);
+    return launch<64, true, 1>(p, d.ntiles, s);
 }

@@ -320,10 +320,16 @@ __global__ void __launch_bounds__(256) add_norm_wide_kernel(float *h, const floa
 
 // ------------------------------------------------------------- qk prep + RoPE
 
-// One warp per packed row.  Each lane owns 8 consecutive channels (one
-// 16-byte load); a head of HD channels spans HD/8 lanes, so the per-head RMS
-// is a reduction over an aligned lane group and the RoPE partner (channel
-// +-sec/2 in the same section) sits in lane (l ^ sec/16) at the same offset.
+// One warp per (packed row, group of QK_U * 32 / (HD / 8) heads).  Each lane
+// owns 8 consecutive channels (one 16-byte load); a head of HD channels spans
+// HD/8 lanes, so the per-head RMS is a reduction over an aligned lane group and
+// the RoPE partner (channel +-sec/2 in the same section) sits in lane
+// (l ^ sec/16) at the same offset.  The warp issues all QK_U loads of its
+// group before any arithmetic, so QK_U 16-byte loads per lane are in flight
+// (a loop of load -> norm -> store per head pair waited a full memory latency
+// per iteration).
+constexpr int QK_U = 4;
+
 template <int HD>
 __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long long ld, int q_off,
                                                       int k_off, int nq, int nkv,
@@ -334,13 +340,14 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
                                                       const int *__restrict__ pos, int table_rows,
                                                       int sec, float q_mul, int rows) {
     constexpr int LPH = HD / 8;                 // lanes per head
-    constexpr int HPI = 32 / LPH;               // heads per warp iteration
+    constexpr int HPI = 32 / LPH;               // heads per load slot
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const int hl = lane / LPH;                  // head slot of this lane in an iteration
+    const int hl = lane / LPH;                  // head slot of this lane in a load slot
     const int c0 = (lane % LPH) * 8;            // first channel of this lane within its head
-    const float *cr = nullptr, *sr = nullptr;
+    const int nh = nq + nkv;
+    const int hbase = blockIdx.y * (HPI * QK_U);
     float cv[8], sv[8];
     const int half = sec >> 1;
     if (sec) {
@@ -349,8 +356,8 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
             atomicExch(&g_rowop_err, 2);
             prow = 0;
         }
-        cr = cosb + prow * (HD / 2);
-        sr = sinb + prow * (HD / 2);
+        const float *cr = cosb + prow * (HD / 2);
+        const float *sr = sinb + prow * (HD / 2);
         const int sct = c0 / sec;
         const int i = c0 - sct * sec;
         const int tc = sct * half + (i < half ? i : i - half);   // 8 consecutive table entries
@@ -362,26 +369,34 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
         cv[4] = a1.x; cv[5] = a1.y; cv[6] = a1.z; cv[7] = a1.w;
         sv[0] = b0.x; sv[1] = b0.y; sv[2] = b0.z; sv[3] = b0.w;
         sv[4] = b1.x; sv[5] = b1.y; sv[6] = b1.z; sv[7] = b1.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cv[e] = sv[e] = 0.f;
     }
     const bool first_half = sec ? ((c0 % sec) < half) : true;
     const int xr = sec ? half / 8 : 0;          // lane distance to the RoPE partner
-    const int nh = nq + nkv;
-    for (int h0 = 0; h0 < nh; h0 += HPI) {
-        const int hh = h0 + hl;
+    uint4 raw[QK_U];
+#pragma unroll
+    for (int u = 0; u < QK_U; ++u) {           // every load of the group first
+        const int hh = hbase + u * HPI + hl;
+        if (hh < nh) {
+            const __nv_bfloat16 *p =
+                qkv + row * ld + (hh < nq ? q_off + hh * HD : k_off + (hh - nq) * HD) + c0;
+            raw[u] = *reinterpret_cast<const uint4 *>(p);
+        } else {
+            raw[u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < QK_U; ++u) {
+        const int hh = hbase + u * HPI + hl;
         const bool active = hh < nh;            // lane groups past the last head idle
         const bool isq = hh < nq;
-        __nv_bfloat16 *p = qkv + row * ld + (isq ? q_off + hh * HD : k_off + (hh - nq) * HD) + c0;
         float v[8];
-        if (active) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(p);
-            v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-            v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = 0.f;
-        }
+        v[0] = bf16_lo(raw[u].x); v[1] = bf16_hi(raw[u].x); v[2] = bf16_lo(raw[u].y); v[3] = bf16_hi(raw[u].y);
+        v[4] = bf16_lo(raw[u].z); v[5] = bf16_hi(raw[u].z); v[6] = bf16_lo(raw[u].w); v[7] = bf16_hi(raw[u].w);
         const float *nw = isq ? qn : kn;
-        if (nw) {                               // qn and kn are both given or both NULL
+        if (qn) {                               // qn and kn are both given or both NULL
             float q = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) q += v[e] * v[e];
@@ -407,10 +422,12 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
         }
         if (active) {
             const float mul = isq ? q_mul : 1.f;
-            uint4 u;
-            u.x = pack_bf16x2(v[0] * mul, v[1] * mul); u.y = pack_bf16x2(v[2] * mul, v[3] * mul);
-            u.z = pack_bf16x2(v[4] * mul, v[5] * mul); u.w = pack_bf16x2(v[6] * mul, v[7] * mul);
-            *reinterpret_cast<uint4 *>(p) = u;
+            uint4 w;
+            w.x = pack_bf16x2(v[0] * mul, v[1] * mul); w.y = pack_bf16x2(v[2] * mul, v[3] * mul);
+            w.z = pack_bf16x2(v[4] * mul, v[5] * mul); w.w = pack_bf16x2(v[6] * mul, v[7] * mul);
+            __nv_bfloat16 *p =
+                qkv + row * ld + (isq ? q_off + hh * HD : k_off + (hh - nq) * HD) + c0;
+            *reinterpret_cast<uint4 *>(p) = w;
         }
     }
 }
@@ -631,7 +648,9 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
     if ((qn == nullptr) != (kn == nullptr))
         return fail(TE_EINVAL, "qk_prep_rope: give both qn and kn or neither");
     if (rows == 0 || nq + nkv == 0) return TE_OK;
-    const dim3 grid((unsigned)(((long long)rows + 7) / 8));
+    const int heads_per_warp = (32 / (hd / 8)) * QK_U;
+    const dim3 grid((unsigned)(((long long)rows + 7) / 8),
+                    (unsigned)((nq + nkv + heads_per_warp - 1) / heads_per_warp));
     if (hd == 64)
         qk_prep_kernel<64><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, nq,
                                                      nkv, qn, kn, eps, cos, sin, pos, table_rows,
