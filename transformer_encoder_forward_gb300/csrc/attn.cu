@@ -21,8 +21,7 @@
 //     M=128 N=128, both operands K-major in shared memory) into tile w's TMEM
 //     S buffer, and O_w += P_w V (A = P_w from TMEM, B = V as an MN-major
 //     shared-memory operand) into its TMEM O accumulator, in the order
-//     PV_A(j), PV_B(j), S_A(j+1), S_B(j+1): while one warpgroup runs its
-//     softmax, the tensor core works on the other tile;
+//     PV_A(j), S_A(j+1), PV_B(j), S_B(j+1);
 //   * warps 0-3 (tile A) and 4-7 (tile B) own one query row per thread (TMEM
 //     lane = query): they read the S row with tcgen05.ld, mask it (sequence
 //     end, window), take the row max, and write P = 2^(s*scale*log2e - m) as
@@ -31,6 +30,10 @@
 //     rescaled through TMEM) when it grows by more than 2^8, which keeps P in
 //     range and leaves the result unchanged: O and the row sum always share
 //     one max;
+//     The exp passes of the two tiles take turns (A(0), B(0), A(1), ...,
+//     handed over through an mbarrier pair): the exp units of an SM cannot
+//     keep up with the tensor core for both tiles at once, so each tile's exp
+//     pass runs alone while the tensor core works on the other tile;
 //   * at the end the same threads divide O by the sum and store their row.
 // Key tiles wholly outside both tiles' windows or the sequence are never
 // loaded; a masked key contributes exactly 0.  Every mbarrier wait is bounded
@@ -65,8 +68,8 @@ struct ALayout {
     static constexpr int K_OFF = 2 * TILE;          // K[2]
     static constexpr int V_OFF = 4 * TILE;          // V[2]
     static constexpr int BAR_OFF = 6 * TILE;
-    // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], fin
-    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+    // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], fin, turn[2]
+    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 2;
     static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
     static constexpr int S_COL = 0;                 // S_A, S_B: 2 x 128 f32 columns (P aliased)
     static constexpr int O_COL = 256;               // O_A, O_B: 2 x HD f32 columns
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const uint32_t bar_pf = bar_sf + 16;           // [2] per query tile
     const uint32_t bar_pv = bar_pf + 16;           // [2] per query tile
     const uint32_t bar_fin = bar_pv + 16;
+    const uint32_t bar_turn = bar_fin + 8;         // [2] per query tile: its turn at the exp pass
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBAR);
 
     // key tiles the two query tiles need: the union of their windows, clipped
@@ -202,6 +206,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             mbar_init(bar_sf + 8 * i, 1);
             mbar_init(bar_pf + 8 * i, 4);
             mbar_init(bar_pv + 8 * i, 1);
+            mbar_init(bar_turn + 8 * i, 4);
         }
         mbar_init(bar_fin, 1);
         fence_mbar_init();
@@ -262,27 +267,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 mma_commit(bar_sf + 8 * w);
                 return true;
             };
+            auto issue_pv = [&](int w, int j) {
+                const uint32_t vb = sb + L::V_OFF + (j & 1) * L::TILE;
+#pragma unroll
+                for (int s2 = 0; s2 < BKV / 16; ++s2)
+                    mma_ts_bf16(tbase + L::O_COL + w * HD, tbase + L::S_COL + w * 128 + 8 * s2,
+                                smem_desc_mn_sw128(vb + s2 * 2048, 16384), idesc_pv, (j | s2) != 0);
+                mma_commit(bar_pv + 8 * w);
+            };
             ok = mbar_wait(bar_q, 0);
             for (int w = 0; w < ntile && ok; ++w) ok = issue_s(w, 0);
+            // Issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the order in
+            // which the alternating exp passes release them.  S_w(j+1)
+            // overwrites the P_w(j) that PV_w(j) reads (a different
+            // accumulator, so not ordered by the tensor pipe): it waits for
+            // PV_w(j) to complete.
             for (int j = 0; j < n && ok; ++j) {
-                // O_w += P_w(j) V(j)
                 if (!mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1)) { ok = false; break; }
                 for (int w = 0; w < ntile && ok; ++w) {
                     if (!mbar_wait(bar_pf + 8 * w, j & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t vb = sb + L::V_OFF + (j & 1) * L::TILE;
-#pragma unroll
-                    for (int s2 = 0; s2 < BKV / 16; ++s2)
-                        mma_ts_bf16(tbase + L::O_COL + w * HD, tbase + L::S_COL + w * 128 + 8 * s2,
-                                    smem_desc_mn_sw128(vb + s2 * 2048, 16384), idesc_pv, (j | s2) != 0);
-                    mma_commit(bar_pv + 8 * w);
-                }
-                if (!ok) break;
-                mma_commit(bar_kve + 8 * (j & 1));   // K(j), V(j) are free once both PVs are done
-                if (j + 1 < n) {
-                    // S_w(j+1) overwrites the P_w(j) that PV_w(j) reads: wait for it first
-                    for (int w = 0; w < ntile && ok; ++w)
-                        ok = mbar_wait(bar_pv + 8 * w, j & 1) && issue_s(w, j + 1);
+                    issue_pv(w, j);
+                    // K(j), V(j) are free once both tiles' PV(j) are done
+                    if (w == ntile - 1) mma_commit(bar_kve + 8 * (j & 1));
+                    if (j + 1 < n) ok = mbar_wait(bar_pv + 8 * w, j & 1) && issue_s(w, j + 1);
                 }
             }
             mma_commit(bar_fin);
@@ -313,6 +321,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             // pass 1: the row max of the raw scores
             float mx = full ? row_max<false>(scol, qi, kv0, len, W) : row_max<true>(scol, qi, kv0, len, W);
             mx *= c;                                     // c > 0: the max of the scaled row
+            // The exp pass of the two tiles alternates (A(0), B(0), A(1), ...):
+            // each tile then has the SM's exp units to itself while the tensor
+            // core runs the other tile's MMAs.
+            if (ntile == 2 && (w == 1 || j > 0)) {
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_turn + 8 * w, (w == 0 ? j - 1 : j) & 1));
+                if (!ok) break;
+            }
             const bool resc = mx > m_used + 8.f;
             if (__any_sync(0xFFFFFFFFu, resc)) {
                 const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
@@ -339,7 +354,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_pf + 8 * w);
+            if (lane == 0) {
+                mbar_arrive(bar_pf + 8 * w);
+                if (ntile == 2) mbar_arrive(bar_turn + 8 * (w ^ 1));   // the other tile's turn
+            }
         }
         // ---- epilogue: O / l, one row per thread
         if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv + 8 * w, (n - 1) & 1));
