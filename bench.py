@@ -244,10 +244,16 @@ def workload_ops(cfg, st, torch):
             qkv, ldq, 0, qw, H, KV, hd, L0.t["q_norm"], L0.t["k_norm"], cfg.eps, st.rope_cos,
             st.rope_sin, st.rope_pos, st.rope_sec, 1.0, T, stream=s), 0, 2 * T * (qw + kw) * 2, nl,
             "hbm")
-    ops["add_norm"] = (lambda s: te.add_norm(x, tmp, L0.t["post_attn_w"] if cfg.form == "sandwich" else None,
-                                             1.0, L0.t["norm2_w"], L0.t["norm2_b"],
-                                             te.TE_NORM_LN if cfg.norm == "ln" else te.TE_NORM_RMS, cfg.eps,
-                                             a, stream=s), 0, T * d * (4 * 3 + 2), 2 * nl, "hbm")
+    if cfg.adaln:   # with the gate on the branch and the scale on the next norm
+        md = L0.t["mod"]
+        ops["add_norm"] = (lambda s: te.add_norm_mod(x, tmp, L0.t["post_attn_w"], md[1], 1.0, L0.t["norm2_w"],
+                                                     None, md[2], te.TE_NORM_RMS, cfg.eps, a, stream=s),
+                           0, T * d * (4 * 3 + 2), 2 * nl, "hbm")
+    else:
+        ops["add_norm"] = (lambda s: te.add_norm(x, tmp, L0.t["post_attn_w"] if cfg.form == "sandwich" else None,
+                                                 1.0, L0.t["norm2_w"], L0.t["norm2_b"],
+                                                 te.TE_NORM_LN if cfg.norm == "ln" else te.TE_NORM_RMS, cfg.eps,
+                                                 a, stream=s), 0, T * d * (4 * 3 + 2), 2 * nl, "hbm")
     return ops
 
 
@@ -498,9 +504,9 @@ def cpu_sample(key):
     cfg = synth.CONFIGS[key]
     lens = synth.draw_lens(cfg)
     seed = synth.config_seed(key)
-    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1}[key]
+    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1}[key]
     sl = lens[:take]
-    if key in ("c4", "c5"):
+    if key in ("c4", "c5", "c4m", "c5m"):
         sl = np.asarray([min(int(sl[0]), 1056)], dtype=np.int32)
     return cfg, sl, seed
 
@@ -508,8 +514,10 @@ def cpu_sample(key):
 def oracle_layer(cfg, lens, layer, p, x, tables):
     from oracle import encoder as O
     cu = synth.cu_seqlens(lens)
-    a = O.round_bf16(O.norm(cfg.norm, x, p["norm1_w"], p["norm1_b"], cfg.eps))
-    return O.block_forward(cfg, p, x, a, cu, layer, tables, None)
+    mod = p.get("mod")
+    a = O.round_bf16(O.norm(cfg.norm, x, p["norm1_w"], p["norm1_b"], cfg.eps,
+                            mod_scale=None if mod is None else mod[0]))
+    return O.block_forward(cfg, p, x, a, cu, layer, tables, None, mod=mod)
 
 
 def cpu_baseline(cfg_full, key, budget_s=15.0):

@@ -165,6 +165,24 @@ te_status te_add_norm(float *h, const float *t, const float *w_post, float post,
                       const float *w_next, const float *b_next, int32_t kind, float eps,
                       void *a, int32_t adt, int32_t rows, int32_t d, te_stream stream);
 
+/* adaLN-modulated row ops of the DiT block ([ZI] Enc::block: per block the
+ * vectors [s_msa | g_msa | s_mlp | g_mlp], a scale on each pre-norm and a gate
+ * on each post-norm residual, Enc::rowop has_s / has_g; refine_caption: the
+ * unmodulated block is s = 0, gate = 1).  The pages do not print the row
+ * op's arithmetic; the reading taken is
+ *   pre-norm:  a = (Norm(x) * w (+ b)) * (1 + s)          s: f32 [d]
+ *   residual:  h = (h + g * RMS(t) * w_post) * post       g: f32 [d]
+ * (w_post == NULL: h = h + g * t).  NULL s or g: unmodulated.  Otherwise as
+ * te_rownorm / te_add_norm. */
+te_status te_rownorm_mod(const void *x, int32_t xdt, int64_t ldx, const float *w, const float *b,
+                         const float *mod_scale, int32_t kind, float eps, float pre, void *y,
+                         int32_t ydt, int64_t ldy, int32_t t, int32_t d, te_stream stream);
+
+te_status te_add_norm_mod(float *h, const float *t, const float *w_post, const float *gate,
+                          float post, const float *w_next, const float *b_next,
+                          const float *mod_scale, int32_t kind, float eps, void *a, int32_t adt,
+                          int32_t rows, int32_t d, te_stream stream);
+
 /* qk_prep_rope: in place on the bf16 q|k panel of qkv [rows, ld].
  * Per row and head: if qn/kn != NULL, x = x / sqrt(mean(x^2) + eps) * w
  * (w: f32 [hd], shared by all heads); then if sec > 0, rotate-half RoPE within
@@ -216,6 +234,11 @@ typedef struct {
     const float *rope_cos, *rope_sin;       /* [rope_rows, head_dim/2] or NULL    */
     const int32_t *rope_pos;                /* [T] table row per packed row, NULL = row index */
     int32_t rope_sec, rope_rows;
+    /* adaLN modulation (sandwich form only; see te_add_norm_mod), or NULL:
+     * mod = this block's f32 [4, d] = s_msa | g_msa | s_mlp | g_mlp (s_msa
+     * scales this block's input a, which the caller's previous norm made);
+     * next_mod_scale = the next block's s_msa, f32 [d], applied to a_out. */
+    const float *mod, *next_mod_scale;
 } te_block_desc;
 
 /* Workspace bytes te_encoder_block_fwd needs for t packed rows. */
@@ -229,6 +252,9 @@ size_t te_encoder_block_workspace(const te_block_desc *desc, int32_t t);
  *                        x += Wd act(Wg a, Wu a) (+b); a = Norm_next(x)
  * Sandwich form ([EG2], [ZI]): x = (x + RMS(Wo attn) w_pa) post; a = RMS(x) w_2;
  *                        x = (x + RMS(Wd act) w_pf) post; a = RMS(x) w_next
+ * With adaLN modulation (mod != NULL, [ZI] Enc::block):
+ *                        x = (x + g_msa RMS(Wo attn) w_pa) post; a = RMS(x) w_2 (1 + s_mlp);
+ *                        x = (x + g_mlp RMS(Wd act) w_pf) post; a = RMS(x) w_next (1 + s_next)
  * t = cu_host[nseq]; workspace of te_encoder_block_workspace(desc, t) bytes,
  * 256-byte aligned. */
 te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, void *a,

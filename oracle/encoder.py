@@ -33,7 +33,10 @@ LayerNorm uses the biased variance; a key j is visible to query i iff both
 lie in the same sequence and (window == 0 or |i - j| <= window); q/k norm is
 applied before RoPE; RoPE is rotate-half within sections of ``sec`` channels;
 the first half of the gate|up panel is the gate; pooling divides by the
-sequence length after the final norm.
+sequence length after the final norm; the DiT's adaLN scale s multiplies a
+normed row by (1 + s) and its gate g multiplies the post-normed branch before
+the residual add (the pages print only the vectors' layout and that the
+unmodulated block is s = 0, gate = 1).
 
 Parity pins: every function here is pinned in tests/test_oracle.py against
 something other than itself (brute-force loops, closed forms, invariants or
@@ -123,18 +126,29 @@ def layer_norm(x, w, b, eps):
     return y
 
 
-def norm(kind, x, w, b, eps):
+def norm(kind, x, w, b, eps, mod_scale=None):
+    """The block's pre-norm; with the DiT's adaLN scale s the normed row is
+    then multiplied by (1 + s) (zimage.rs ``Enc::rowop`` pre mode with
+    ``has_s``; ``refine_caption``: unmodulated is s = 0)."""
     if kind == "rms":
-        return rms_norm(x, w, eps)
-    if kind == "ln":
-        return layer_norm(x, w, b, eps)
-    raise ValueError(kind)
+        y = rms_norm(x, w, eps)
+    elif kind == "ln":
+        y = layer_norm(x, w, b, eps)
+    else:
+        raise ValueError(kind)
+    if mod_scale is not None:
+        y = y * (1.0 + np.asarray(mod_scale, dtype=np.float64))
+    return y
 
 
-def add_norm_sandwich(h, t, w_post, post, eps):
-    """H = (H + rms(T) * w_post) * post  (egemma2.rs ``Prog::add_norm``;
-    zimage.rs ``Enc::rowop`` post-norm mode)."""
-    return (np.asarray(h, dtype=np.float64) + rms_norm(t, w_post, eps)) * post
+def add_norm_sandwich(h, t, w_post, post, eps, gate=None):
+    """H = (H + g * rms(T) * w_post) * post  (egemma2.rs ``Prog::add_norm``;
+    zimage.rs ``Enc::rowop`` post-norm mode, the adaLN gate g with ``has_g``;
+    unmodulated g = 1)."""
+    branch = rms_norm(t, w_post, eps)
+    if gate is not None:
+        branch = branch * np.asarray(gate, dtype=np.float64)
+    return (np.asarray(h, dtype=np.float64) + branch) * post
 
 
 # ---------------------------------------------------------------------------
@@ -300,7 +314,8 @@ def pool_mean(x, cu, w, eps):
 # the block
 
 
-def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None):
+def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mod=None,
+                  next_mod_scale=None):
     """One encoder block, step by step; returns every stored intermediate.
 
     cfg: a BlockConfig-like object (d, heads, kv_heads, hd, ffn, gated, act,
@@ -314,6 +329,11 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None):
     Sandwich form (egemma2.rs ``TextGpu::forward``; zimage.rs ``Enc::block``):
         x = (x + rms(o Wo^T) w_pa) post;  a = rms(x) w_2;
         x = (x + rms(FFN(a)) w_pf) post;  a = rms(x) w_next
+    adaLN-modulated DiT block (zimage.rs ``Enc::block``: ``mods`` =
+    [s_msa | g_msa | s_mlp | g_mlp], sandwich form only): ``mod`` [4, d] gates
+    the two residual branches with g_msa, g_mlp and scales the FFN input by
+    (1 + s_mlp); s_msa scales this block's input ``a`` (made by the caller)
+    and ``next_mod_scale`` (the next block's s_msa) the returned ``a_out``.
     ``rows`` restricts the block to sampled query rows: q|k|v is computed for
     every row (all keys are needed), everything after attention only for the
     sampled rows (it is row-local), and the returned post-attention
@@ -321,6 +341,12 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None):
     """
     hd, H, KV, d, F = cfg.hd, cfg.heads, cfg.kv_heads, cfg.d, cfg.ffn
     eps = cfg.eps
+    if (mod is not None or next_mod_scale is not None) and cfg.form != "sandwich":
+        raise ValueError("adaLN modulation applies to the sandwich (post-norm) form")
+    g_msa = s_mlp = g_mlp = None
+    if mod is not None:
+        mod = np.asarray(mod, dtype=np.float64).reshape(4, d)
+        g_msa, s_mlp, g_mlp = mod[1], mod[2], mod[3]
     r = {}
     x = round_f32(x)
     a = round_bf16(a)
@@ -348,9 +374,9 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None):
     else:
         t = round_f32(q8_linear(o, p["wo"]["q"], p["wo"]["s"], p["wo"]["b"]))
         r["t"] = t
-        x = round_f32(add_norm_sandwich(x, t, p["post_attn_w"], cfg.post, eps))
+        x = round_f32(add_norm_sandwich(x, t, p["post_attn_w"], cfg.post, eps, gate=g_msa))
     r["x_mid"] = x
-    r["a_mid"] = a2 = round_bf16(norm(cfg.norm, x, p["norm2_w"], p["norm2_b"], eps))
+    r["a_mid"] = a2 = round_bf16(norm(cfg.norm, x, p["norm2_w"], p["norm2_b"], eps, mod_scale=s_mlp))
     parts = [q8_linear(a2, p["wg"]["q"], p["wg"]["s"], p["wg"]["b"])]
     if cfg.gated:
         parts.append(q8_linear(a2, p["wu"]["q"], p["wu"]["s"], p["wu"]["b"]))
@@ -361,10 +387,11 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None):
     else:
         f = round_f32(q8_linear(m, p["wd"]["q"], p["wd"]["s"], p["wd"]["b"]))
         r["f"] = f
-        x = round_f32(add_norm_sandwich(x, f, p["post_ffn_w"], cfg.post, eps))
+        x = round_f32(add_norm_sandwich(x, f, p["post_ffn_w"], cfg.post, eps, gate=g_mlp))
     r["x_out"] = x
     if next_norm is not None:
-        r["a_out"] = round_bf16(norm(cfg.norm, x, next_norm[0], next_norm[1], eps))
+        r["a_out"] = round_bf16(norm(cfg.norm, x, next_norm[0], next_norm[1], eps,
+                                     mod_scale=next_mod_scale))
     else:
         r["a_out"] = None
     return r

@@ -139,6 +139,20 @@ def test_row_ops_reject_bad_arguments(L):
     assert _call(L, "te_pool_mean", FAKE, 64, p, FAKE, 2, None, 1e-6, FAKE, None)[0] == te.TE_EINVAL
 
 
+def test_adaln_row_ops_reject_bad_arguments(L):
+    # scale without a next norm, gate without a branch, misaligned vectors
+    assert _call(L, "te_add_norm_mod", FAKE, FAKE, FAKE, None, 1.0, None, None, FAKE, te.TE_NORM_RMS,
+                 1e-6, None, te.TE_BF16, 4, 64, None)[0] == te.TE_EINVAL
+    assert _call(L, "te_add_norm_mod", FAKE, None, None, FAKE, 1.0, None, None, None, te.TE_NORM_RMS,
+                 1e-6, None, te.TE_BF16, 4, 64, None)[0] == te.TE_EINVAL
+    assert _call(L, "te_add_norm_mod", FAKE, FAKE, FAKE, FAKE + 4, 1.0, FAKE, None, None,
+                 te.TE_NORM_RMS, 1e-6, FAKE, te.TE_BF16, 4, 64, None)[0] == te.TE_EALIGN
+    assert _call(L, "te_rownorm_mod", FAKE, te.TE_F32, 64, FAKE, None, FAKE + 8, te.TE_NORM_RMS,
+                 1e-6, 1.0, FAKE, te.TE_BF16, 64, 4, 64, None)[0] == te.TE_EALIGN
+    assert _call(L, "te_rownorm_mod", FAKE, te.TE_F32, 100, FAKE, None, FAKE, te.TE_NORM_RMS,
+                 1e-6, 1.0, FAKE, te.TE_BF16, 100, 4, 100, None)[0] == te.TE_ESHAPE
+
+
 def _desc(**over):
     d = te.te_block_desc()
     d.d, d.n_heads, d.n_kv_heads, d.head_dim, d.ffn = 256, 4, 4, 64, 1024
@@ -174,3 +188,14 @@ def test_block_validation_and_workspace(L):
     unal = _desc()
     assert _call(L, "te_encoder_block_fwd", ctypes.byref(unal), FAKE, FAKE, p, FAKE, 2,
                  FAKE * 256 + 16, ws, None)[0] == te.TE_EALIGN
+    # adaLN modulation: sandwich form only, aligned, next scale needs a next norm
+    plain_mod = _desc(mod=FAKE)
+    assert _call(L, "te_encoder_block_fwd", ctypes.byref(plain_mod), FAKE, FAKE, p, FAKE, 2,
+                 FAKE * 256, ws, None)[0] == te.TE_EINVAL
+    sand_ok = dict(resid_form=te.TE_RESID_SANDWICH, post_attn_w=FAKE, post_ffn_w=FAKE)
+    mod_unal = _desc(mod=FAKE + 4, **sand_ok)
+    assert _call(L, "te_encoder_block_fwd", ctypes.byref(mod_unal), FAKE, FAKE, p, FAKE, 2,
+                 FAKE * 256, ws, None)[0] == te.TE_EALIGN
+    next_s_only = _desc(mod=FAKE, next_mod_scale=FAKE, **sand_ok)
+    assert _call(L, "te_encoder_block_fwd", ctypes.byref(next_s_only), FAKE, FAKE, p, FAKE, 2,
+                 FAKE * 256, ws, None)[0] == te.TE_EINVAL

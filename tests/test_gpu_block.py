@@ -32,6 +32,13 @@ def _next_norm(ps, i):
     return (ps[i + 1]["norm1_w"], ps[i + 1]["norm1_b"]) if i + 1 < len(ps) else None
 
 
+def _mods(ps, i):
+    """(this block's adaLN vectors, the next block's s_msa), or Nones."""
+    mod = ps[i].get("mod")
+    nxt = ps[i + 1]["mod"][0] if mod is not None and i + 1 < len(ps) else None
+    return mod, nxt
+
+
 def _check_layer(cfg, st, ps, tables, i, x, a, rows=None):
     """Runs GPU layer i in place on (x, a) and compares against the oracle on
     the same inputs."""
@@ -39,8 +46,9 @@ def _check_layer(cfg, st, ps, tables, i, x, a, rows=None):
     x_in, a_in = to_np(x), to_np(a)
     te.encoder_block_fwd(st.descs[i], x, a, st.cu_host, st.cu_dev, st.workspace)
     te.check()
+    mod, next_s = _mods(ps, i)
     r = O.block_forward(cfg, ps[i], x_in, a_in, st.cu_host, i, tables, _next_norm(ps, i),
-                        rows=rows)
+                        rows=rows, mod=mod, next_mod_scale=next_s)
     sel = slice(None) if rows is None else np.asarray(rows)
     got_x = to_np(x)[sel]
     xin = x_in[sel]
@@ -61,6 +69,9 @@ FORMS = {
     "c3_small": ("c3", dict(layers=2), (200, 129)),
     "c4_small": ("c4", dict(d=512, heads=4, kv_heads=4, ffn=1024), (150, 133)),
     "gqa_small": ("c2", dict(layers=2, kv_heads=2, window=0), (64, 65)),
+    # the DiT block with adaLN modulation (gates on both branches, scales on
+    # every pre-norm including the next block's input)
+    "c4m_small": ("c4m", dict(layers=3, d=512, heads=4, kv_heads=4, ffn=1024), (150, 133)),
 }
 
 
@@ -73,7 +84,9 @@ def test_block_forms_match_oracle(name):
     import torch
     a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
     st.input_norm(x, a)
-    a0 = O.round_bf16(O.norm(cfg.norm, to_np(x), ps[0]["norm1_w"], ps[0]["norm1_b"], cfg.eps))
+    s0 = ps[0]["mod"][0] if cfg.adaln else None
+    a0 = O.round_bf16(O.norm(cfg.norm, to_np(x), ps[0]["norm1_w"], ps[0]["norm1_b"], cfg.eps,
+                             mod_scale=s0))
     assert rel_frob(to_np(a), a0) < 2e-3
     for i in range(cfg.layers):
         _check_layer(cfg, st, ps, tables, i, x, a)
@@ -120,6 +133,17 @@ def test_dit_block_full_size():
     cfg = synth.CONFIGS["c4"]
     lens = synth.draw_lens(cfg)
     st, ps, tables = _stack(cfg, lens, 1, jitter=False)
+    x = to_dev(synth.draw_x(st.T, cfg.d, 6))
+    a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    st.input_norm(x, a)
+    _check_layer(cfg, st, ps, tables, 0, x, a)
+
+
+def test_dit_block_with_adaln_full_size():
+    import torch
+    cfg = synth.small_config("c4m", layers=2)
+    lens = synth.draw_lens(cfg)
+    st, ps, tables = _stack(cfg, lens, 2, jitter=False)
     x = to_dev(synth.draw_x(st.T, cfg.d, 6))
     a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
     st.input_norm(x, a)

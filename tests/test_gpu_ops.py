@@ -298,6 +298,57 @@ def test_add_norm_matches_oracle(d, sandwich, nxt, kind):
         assert torch.count_nonzero(a) == 0
 
 
+@pytest.mark.parametrize("d,sandwich,kind", [(512, True, "rms"), (3840, True, "rms"),
+                                            (768, False, "ln"), (2048, False, "rms")])
+def test_add_norm_with_adaln_gate_and_scale_matches_oracle(d, sandwich, kind):
+    torch = _torch()
+    rng = np.random.default_rng([d, 77, int(sandwich)])
+    rows = 141
+    h = rng.standard_normal((rows, d)).astype(np.float32)
+    t = rng.standard_normal((rows, d)).astype(np.float32) * 3
+    wp, _ = synth.draw_norm(rng, d, False)
+    wn, bn = synth.draw_norm(rng, d, kind == "ln")
+    mod = synth.draw_mods(rng, d)
+    g, s = mod[1], mod[2]
+    h_t, t_t = to_dev(h), to_dev(t)
+    a = torch.zeros(rows, d, dtype=torch.bfloat16, device="cuda")
+    te.add_norm_mod(h_t, t_t, to_dev(wp) if sandwich else None, to_dev(g), 0.75, to_dev(wn),
+                    to_dev(bn) if bn is not None else None, to_dev(s),
+                    te.TE_NORM_LN if kind == "ln" else te.TE_NORM_RMS, 1e-6, a)
+    if sandwich:
+        h_ref = O.add_norm_sandwich(h, t, wp, 0.75, 1e-6, gate=g)
+    else:
+        h_ref = h.astype(np.float64) + g.astype(np.float64) * t
+    assert rel_frob(to_np(h_t), h_ref) < 1e-6
+    a_ref = O.round_bf16(O.norm(kind, O.round_f32(h_ref), wn, bn, 1e-6, mod_scale=s))
+    assert rel_frob(to_np(a), a_ref) < 2e-3
+    # rownorm with the scale alone
+    y = torch.empty(rows, d, dtype=torch.bfloat16, device="cuda")
+    te.rownorm_mod(h_t, to_dev(wn), to_dev(bn) if bn is not None else None, to_dev(s),
+                   te.TE_NORM_LN if kind == "ln" else te.TE_NORM_RMS, 1e-6, y)
+    y_ref = O.round_bf16(O.norm(kind, to_np(h_t), wn, bn, 1e-6, mod_scale=s))
+    assert rel_frob(to_np(y), y_ref) < 2e-3
+
+
+def test_adaln_identity_vectors_are_bit_exact_no_ops():
+    # s = 0 and g = 1 must give exactly the unmodulated row ops
+    torch = _torch()
+    rng = np.random.default_rng(91)
+    rows, d = 99, 3840
+    h = to_dev(rng.standard_normal((rows, d)).astype(np.float32))
+    t = to_dev(rng.standard_normal((rows, d)).astype(np.float32))
+    wp, _ = synth.draw_norm(rng, d, False)
+    wn, _ = synth.draw_norm(rng, d, False)
+    zeros, ones = torch.zeros(d, device="cuda"), torch.ones(d, device="cuda")
+    h1, h2 = h.clone(), h.clone()
+    a1 = torch.empty(rows, d, dtype=torch.bfloat16, device="cuda")
+    a2 = torch.empty_like(a1)
+    te.add_norm(h1, t, to_dev(wp), 1.0, to_dev(wn), None, te.TE_NORM_RMS, 1e-6, a1)
+    te.add_norm_mod(h2, t, to_dev(wp), ones, 1.0, to_dev(wn), None, zeros, te.TE_NORM_RMS, 1e-6, a2)
+    te.check()
+    assert torch.equal(h1, h2) and torch.equal(a1, a2)
+
+
 @pytest.mark.parametrize("hd,nq,nkv,rope,qk", [(64, 8, 8, "1d", True), (128, 4, 4, "2d", True),
                                                (64, 4, 2, "2d", False), (128, 2, 1, None, True)])
 def test_qk_prep_rope_matches_oracle(hd, nq, nkv, rope, qk):

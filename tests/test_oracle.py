@@ -499,3 +499,91 @@ def test_block_is_equivariant_to_sequence_order():
     r2 = O.block_forward(cfg, p, x[perm], a[perm], synth.cu_seqlens(lens2), 0,
                          synth.rope_tables(cfg, lens2))
     np.testing.assert_allclose(r2["x_out"], r["x_out"][perm], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- adaLN (DiT)
+# The pages fix two things about the modulation (zimage.rs Enc::block /
+# refine_caption): the per-block layout [s_msa | g_msa | s_mlp | g_mlp] and that
+# the unmodulated block is s = 0, gate = 1.  The pins below check the oracle's
+# modulated block against those facts and against the block's structure: which
+# vector acts on which branch, that s scales through (1 + s), that g multiplies
+# the whole post-normed branch.
+
+def _dit_case(seed=7):
+    cfg = _tiny("sandwich", "rms", True, "silu", "2d", True, 0)
+    p = synth.draw_layer(cfg, 0, seed)
+    cu = synth.cu_seqlens(cfg.lens)
+    x = synth.draw_x(int(cu[-1]), cfg.d, seed + 1)
+    tables = synth.rope_tables(cfg, cfg.lens)
+    return cfg, p, cu, x, tables
+
+
+def test_adaln_identity_modulation_is_the_unmodulated_block():
+    cfg, p, cu, x, tables = _dit_case()
+    d = cfg.d
+    nxt = synth.draw_norm(np.random.default_rng(3), d, False)
+    a = O.round_bf16(O.norm("rms", x, p["norm1_w"], None, cfg.eps, mod_scale=np.zeros(d)))
+    ident = np.stack([np.zeros(d), np.ones(d), np.zeros(d), np.ones(d)])
+    r0 = O.block_forward(cfg, p, x, a, cu, 0, tables, next_norm=nxt)
+    r1 = O.block_forward(cfg, p, x, a, cu, 0, tables, next_norm=nxt, mod=ident,
+                         next_mod_scale=np.zeros(d))
+    for key in ("x_mid", "a_mid", "x_out", "a_out"):
+        np.testing.assert_array_equal(r1[key], r0[key])
+
+
+def test_adaln_zero_gates_leave_the_residual_stream_unchanged():
+    cfg, p, cu, x, tables = _dit_case(11)
+    d = cfg.d
+    rng = np.random.default_rng(2)
+    mod = np.stack([rng.normal(0, .3, d), np.zeros(d), rng.normal(0, .3, d), np.zeros(d)])
+    a = O.round_bf16(O.norm("rms", x, p["norm1_w"], None, cfg.eps, mod_scale=mod[0]))
+    r = O.block_forward(cfg, p, x, a, cu, 0, tables, mod=mod)
+    np.testing.assert_array_equal(r["x_mid"], x.astype(np.float64))
+    np.testing.assert_array_equal(r["x_out"], x.astype(np.float64))
+
+
+def test_adaln_gate_scales_only_its_own_branch():
+    # g_msa acts on the attention branch: x_mid - x = g_msa * rms(t) w_pa,
+    # so dividing the delta by g_msa gives the unmodulated delta; g_mlp does
+    # not touch x_mid
+    cfg, p, cu, x, tables = _dit_case(13)
+    d = cfg.d
+    rng = np.random.default_rng(4)
+    a = O.round_bf16(O.norm("rms", x, p["norm1_w"], None, cfg.eps))
+    base = O.block_forward(cfg, p, x, a, cu, 0, tables)
+    g = rng.uniform(0.5, 1.5, d) * rng.choice([-1, 1], d)
+    mod = np.stack([np.zeros(d), g, np.zeros(d), rng.uniform(0.5, 1.5, d)])
+    r = O.block_forward(cfg, p, x, a, cu, 0, tables, mod=mod)
+    x64 = x.astype(np.float64)
+    delta_mod = (r["x_mid"] - x64) / g
+    delta_ref = base["x_mid"] - x64
+    np.testing.assert_allclose(delta_mod, delta_ref, rtol=1e-5, atol=1e-6)
+    np.testing.assert_array_equal(r["t"], base["t"])      # same attention branch input
+
+
+def test_adaln_scale_multiplies_the_normed_ffn_input_by_one_plus_s():
+    cfg, p, cu, x, tables = _dit_case(17)
+    d = cfg.d
+    rng = np.random.default_rng(5)
+    a = O.round_bf16(O.norm("rms", x, p["norm1_w"], None, cfg.eps))
+    s = rng.normal(0, .5, d)
+    mod = np.stack([np.zeros(d), np.ones(d), s, np.ones(d)])
+    r = O.block_forward(cfg, p, x, a, cu, 0, tables, mod=mod)
+    # a_mid is stored bf16: compare with the unrounded reference within bf16
+    ref = O.rms_norm(r["x_mid"], p["norm2_w"], cfg.eps) * (1.0 + s)
+    np.testing.assert_allclose(r["a_mid"], ref, rtol=2 ** -8, atol=1e-30)
+    # s = -1 on every channel zeroes the FFN input, hence the FFN branch
+    mod2 = np.stack([np.zeros(d), np.ones(d), -np.ones(d), np.ones(d)])
+    r2 = O.block_forward(cfg, p, x, a, cu, 0, tables, mod=mod2)
+    assert not np.any(r2["a_mid"])
+    np.testing.assert_array_equal(r2["f"], np.zeros_like(r2["f"]))
+
+
+def test_adaln_rejects_the_plain_form():
+    cfg = _tiny("plain", "rms", True, "silu", None, False)
+    p = synth.draw_layer(cfg, 0, 1)
+    cu = synth.cu_seqlens(cfg.lens)
+    x = synth.draw_x(int(cu[-1]), cfg.d, 2)
+    with pytest.raises(ValueError):
+        O.block_forward(cfg, p, x, x, cu, 0, synth.rope_tables(cfg, cfg.lens),
+                        mod=np.zeros((4, cfg.d)))

@@ -53,7 +53,8 @@ class te_block_desc(ctypes.Structure):
                 ("ffn_norm_w", c_p), ("ffn_norm_b", c_p), ("post_attn_w", c_p),
                 ("post_ffn_w", c_p), ("next_norm_w", c_p), ("next_norm_b", c_p),
                 ("q_norm", c_p), ("k_norm", c_p), ("rope_cos", c_p), ("rope_sin", c_p),
-                ("rope_pos", c_p), ("rope_sec", c_i32), ("rope_rows", c_i32)]
+                ("rope_pos", c_p), ("rope_sec", c_i32), ("rope_rows", c_i32),
+                ("mod", c_p), ("next_mod_scale", c_p)]
 
 
 _lib = None
@@ -68,6 +69,10 @@ EXPORTS = {
                                   c_i64, c_i32, c_i32, c_p]),
     "te_add_norm": (ctypes.c_int, [c_p, c_p, c_p, c_f32, c_p, c_p, c_i32, c_f32, c_p, c_i32, c_i32,
                                    c_i32, c_p]),
+    "te_rownorm_mod": (ctypes.c_int, [c_p, c_i32, c_i64, c_p, c_p, c_p, c_i32, c_f32, c_f32, c_p,
+                                      c_i32, c_i64, c_i32, c_i32, c_p]),
+    "te_add_norm_mod": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_f32, c_p, c_p, c_p, c_i32, c_f32, c_p,
+                                       c_i32, c_i32, c_i32, c_p]),
     "te_qk_prep_rope": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32, c_p, c_p,
                                        c_f32, c_p, c_p, c_p, c_i32, c_i32, c_f32, c_i32, c_p]),
     "te_gate_act": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_i64, c_i32, c_i32, c_p]),
@@ -181,6 +186,21 @@ def add_norm(h, t, w_post, post, w_next, b_next, kind, eps, a, stream=None):
     _ok(lib().te_add_norm(h.data_ptr(), _ptr(t), _ptr(w_post), post, _ptr(w_next), _ptr(b_next),
                           kind, eps, _ptr(a), _dt(a) if a is not None else TE_BF16, h.shape[0],
                           h.shape[1], _stream(stream)))
+
+
+def rownorm_mod(x, w, b, mod_scale, kind, eps, y, pre=1.0, stream=None):
+    """rownorm with the adaLN scale: y = (Norm(x) w (+b)) (1 + mod_scale)."""
+    _ok(lib().te_rownorm_mod(x.data_ptr(), _dt(x), x.stride(0), _ptr(w), _ptr(b), _ptr(mod_scale),
+                             kind, eps, pre, y.data_ptr(), _dt(y), y.stride(0), x.shape[0],
+                             x.shape[1], _stream(stream)))
+
+
+def add_norm_mod(h, t, w_post, gate, post, w_next, b_next, mod_scale, kind, eps, a, stream=None):
+    """add_norm with the adaLN gate on the branch and scale on the next norm."""
+    _ok(lib().te_add_norm_mod(h.data_ptr(), _ptr(t), _ptr(w_post), _ptr(gate), post, _ptr(w_next),
+                              _ptr(b_next), _ptr(mod_scale), kind, eps, _ptr(a),
+                              _dt(a) if a is not None else TE_BF16, h.shape[0], h.shape[1],
+                              _stream(stream)))
 
 
 def qk_prep_rope(qkv, ld, q_off, k_off, nq, nkv, hd, qn, kn, eps, cos, sin, pos, sec, q_mul,

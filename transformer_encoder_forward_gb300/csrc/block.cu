@@ -69,8 +69,13 @@ te_status check_desc(const te_block_desc *d) {
         return fail(TE_EINVAL, "block: give both q_norm and k_norm or neither");
     if (d->rope_sec && (!d->rope_cos || !d->rope_sin))
         return fail(TE_EINVAL, "block: rope_sec set without tables");
+    if ((d->mod || d->next_mod_scale) && d->resid_form != TE_RESID_SANDWICH)
+        return fail(TE_EINVAL, "block: adaLN modulation needs the sandwich form");
+    if (d->next_mod_scale && !d->next_norm_w)
+        return fail(TE_EINVAL, "block: next_mod_scale given without next_norm_w");
     const float *vecs[] = {d->ffn_norm_w, d->ffn_norm_b, d->post_attn_w, d->post_ffn_w,
-                           d->next_norm_w, d->next_norm_b, d->q_norm, d->k_norm};
+                           d->next_norm_w, d->next_norm_b, d->q_norm, d->k_norm,
+                           d->mod, d->next_mod_scale};
     for (const float *v : vecs)
         if (v && !aligned16(v)) return fail(TE_EALIGN, "block: norm weights must be 16-byte aligned");
     const int hd = d->head_dim, qw = d->n_heads * hd, kw = d->n_kv_heads * hd;
@@ -146,9 +151,10 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
     if (plain)
         st = te_rownorm(x, TE_F32, D, d.ffn_norm_w, d.ffn_norm_b, d.norm_kind, d.eps, 1.f, a, TE_BF16,
                         D, t, D, stream);
-    else
-        st = te_add_norm(x, tmp, d.post_attn_w, d.post, d.ffn_norm_w, d.ffn_norm_b, d.norm_kind,
-                         d.eps, a, TE_BF16, t, D, stream);
+    else   // adaLN: gate g_msa on the attention branch, scale s_mlp on the FFN input
+        st = te_add_norm_mod(x, tmp, d.post_attn_w, d.mod ? d.mod + D : nullptr, d.post, d.ffn_norm_w,
+                             d.ffn_norm_b, d.mod ? d.mod + 2 * D : nullptr, d.norm_kind, d.eps, a,
+                             TE_BF16, t, D, stream);
     if (st != TE_OK) return st;
     // 6-7. gate|up with the gate in the epilogue, or up with the activation
     if (d.gated) {
@@ -169,8 +175,10 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
             st = te_rownorm(x, TE_F32, D, d.next_norm_w, d.next_norm_b, d.norm_kind, d.eps, 1.f, a,
                             TE_BF16, D, t, D, stream);
     } else {
-        st = te_add_norm(x, tmp, d.post_ffn_w, d.post, d.next_norm_w, d.next_norm_b, d.norm_kind,
-                         d.eps, d.next_norm_w ? a : nullptr, TE_BF16, t, D, stream);
+        // adaLN: gate g_mlp on the FFN branch, the next block's s_msa on its input
+        st = te_add_norm_mod(x, tmp, d.post_ffn_w, d.mod ? d.mod + 3 * D : nullptr, d.post, d.next_norm_w,
+                             d.next_norm_b, d.next_mod_scale, d.norm_kind, d.eps,
+                             d.next_norm_w ? a : nullptr, TE_BF16, t, D, stream);
     }
     return st;
 }

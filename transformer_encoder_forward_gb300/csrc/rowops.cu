@@ -79,10 +79,11 @@ __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
 }
 
 // Normalises the warp's row held in v (NV chunks of 8 per lane, chunk i of
-// lane l covers columns (i*32 + l)*8 ...) and writes w*v (+b) to y.
+// lane l covers columns (i*32 + l)*8 ...) and writes w*v (+b) to y, times
+// (1 + ms) when the adaLN scale ms is given.
 template <typename Tout, int NV>
 __device__ __forceinline__ void norm_store(float (&v)[NV][8], int lane, int d, int kind, float eps,
-                                           const float *w, const float *b, Tout *y) {
+                                           const float *w, const float *b, const float *ms, Tout *y) {
     float inv, mean = 0.f;
     if (kind == TE_NORM_LN) {
         float s = 0.f;
@@ -123,6 +124,12 @@ __device__ __forceinline__ void norm_store(float (&v)[NV][8], int lane, int d, i
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = (v[i][e] - mean) * inv * wv[e];
             }
+            if (ms) {
+                float sv[8];
+                load8(ms + c, sv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] *= 1.f + sv[e];
+            }
             store8(y + c, o);
         }
     }
@@ -133,7 +140,8 @@ __device__ __forceinline__ void norm_store(float (&v)[NV][8], int lane, int d, i
 template <typename Tin, typename Tout, int NV>
 __global__ void __launch_bounds__(256) rownorm_kernel(const Tin *__restrict__ x, long long ldx,
                                                       const float *__restrict__ w,
-                                                      const float *__restrict__ b, int kind,
+                                                      const float *__restrict__ b,
+                                                      const float *__restrict__ ms, int kind,
                                                       float eps, float pre, Tout *y, long long ldy,
                                                       int t, int d) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -150,17 +158,19 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const Tin *__restrict__ x,
             for (int e = 0; e < 8; ++e) v[i][e] *= pre;
         }
     }
-    norm_store<Tout, NV>(v, lane, d, kind, eps, w, kind == TE_NORM_LN ? b : nullptr,
+    norm_store<Tout, NV>(v, lane, d, kind, eps, w, kind == TE_NORM_LN ? b : nullptr, ms,
                          y + (long long)row * ldy);
 }
 
 // ----------------------------------------------------------------- add_norm
 
-template <typename Tout, int NV>
+template <typename Tout, int NV, bool MOD>
 __global__ void __launch_bounds__(256) add_norm_kernel(float *h, const float *__restrict__ t,
                                                        const float *__restrict__ w_post,
+                                                       const float *__restrict__ gate,
                                                        float post, const float *__restrict__ w_next,
-                                                       const float *__restrict__ b_next, int kind,
+                                                       const float *__restrict__ b_next,
+                                                       const float *__restrict__ ms, int kind,
                                                        float eps, Tout *a, int rows, int d) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -191,6 +201,12 @@ __global__ void __launch_bounds__(256) add_norm_kernel(float *h, const float *__
         if (c < d) {
             float hv[8];
             load8(hr + c, hv);
+            if (MOD && tr && gate) {            // adaLN gate on the branch
+                float gv[8];
+                load8(gate + c, gv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] *= gv[e];
+            }
             if (tr && w_post) {
                 float wv[8];
                 load8(w_post + c, wv);
@@ -208,7 +224,7 @@ __global__ void __launch_bounds__(256) add_norm_kernel(float *h, const float *__
     }
     if (w_next)
         norm_store<Tout, NV>(v, lane, d, kind, eps, w_next, kind == TE_NORM_LN ? b_next : nullptr,
-                             a + (long long)row * d);
+                             MOD ? ms : nullptr, a + (long long)row * d);
 }
 
 // Wide rows (d > 1024): four warps per row, two rows per 256-thread CTA.
@@ -225,12 +241,14 @@ __device__ __forceinline__ float row4_sum(float x, float (*red)[4], int slot, in
     return s;
 }
 
-template <typename Tout, int NV>
+template <typename Tout, int NV, bool MOD>
 __global__ void __launch_bounds__(256) add_norm_wide_kernel(float *h, const float *__restrict__ t,
                                                             const float *__restrict__ w_post,
+                                                            const float *__restrict__ gate,
                                                             float post,
                                                             const float *__restrict__ w_next,
-                                                            const float *__restrict__ b_next, int kind,
+                                                            const float *__restrict__ b_next,
+                                                            const float *__restrict__ ms, int kind,
                                                             float eps, Tout *a, int rows, int d) {
     __shared__ float red[2][4];
     const int slot = threadIdx.x >> 7, tid = threadIdx.x & 127;
@@ -265,6 +283,12 @@ __global__ void __launch_bounds__(256) add_norm_wide_kernel(float *h, const floa
         for (int i = 0; i < NV; ++i) {
             const int c = (i * 128 + tid) * 8;
             if (active && c < d) {
+                if (MOD && gate) {              // adaLN gate on the branch
+                    float gv[8];
+                    load8(gate + c, gv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) tv[i][e] *= gv[e];
+                }
                 if (w_post) {
                     float wv[8];
                     load8(w_post + c, wv);
@@ -312,6 +336,12 @@ __global__ void __launch_bounds__(256) add_norm_wide_kernel(float *h, const floa
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = (hv[i][e] - mean) * inv * wv[e];
+            }
+            if (MOD && ms) {
+                float sv[8];
+                load8(ms + c, sv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] *= 1.f + sv[e];
             }
             store8(a + (long long)row * d + c, o);
         }
@@ -556,15 +586,15 @@ using namespace tefwd;
 
 extern "C" {
 
-te_status te_rownorm(const void *x, int32_t xdt, int64_t ldx, const float *w, const float *b,
-                     int32_t kind, float eps, float pre, void *y, int32_t ydt, int64_t ldy,
-                     int32_t t, int32_t d, te_stream stream) {
+te_status te_rownorm_mod(const void *x, int32_t xdt, int64_t ldx, const float *w, const float *b,
+                         const float *ms, int32_t kind, float eps, float pre, void *y, int32_t ydt,
+                         int64_t ldy, int32_t t, int32_t d, te_stream stream) {
     if (!x || !w || !y) return fail(TE_EINVAL, "rownorm: NULL x, w or y");
     if (!dtype_ok(xdt) || !dtype_ok(ydt)) return fail(TE_EINVAL, "rownorm: bad dtype");
     if (kind != TE_NORM_RMS && kind != TE_NORM_LN) return fail(TE_EINVAL, "rownorm: bad kind");
     if (t < 0 || d < 8 || d > 4096 || d % 8) return fail(TE_ESHAPE, "rownorm: t=%d d=%d (d %% 8 == 0, 8..4096)", t, d);
     if (ldx < d || ldy < d) return fail(TE_ESHAPE, "rownorm: leading dimension below d");
-    if (!aligned16(x) || !aligned16(y) || !aligned16(w) || (b && !aligned16(b)) ||
+    if (!aligned16(x) || !aligned16(y) || !aligned16(w) || (b && !aligned16(b)) || (ms && !aligned16(ms)) ||
         (ldx * (xdt == TE_F32 ? 4 : 2)) % 16 || (ldy * (ydt == TE_F32 ? 4 : 2)) % 16)
         return fail(TE_EALIGN, "rownorm: pointers and rows must be 16-byte aligned");
     if (x == y && (xdt != ydt || ldx != ldy))
@@ -574,54 +604,91 @@ te_status te_rownorm(const void *x, int32_t xdt, int64_t ldx, const float *w, co
     TE_NV_SWITCH(nv_for(d), {
         if (xdt == TE_F32 && ydt == TE_BF16)
             rownorm_kernel<float, __nv_bfloat16, NV><<<grid, 256, 0, stream>>>(
-                (const float *)x, ldx, w, b, kind, eps, pre, (__nv_bfloat16 *)y, ldy, t, d);
+                (const float *)x, ldx, w, b, ms, kind, eps, pre, (__nv_bfloat16 *)y, ldy, t, d);
         else if (xdt == TE_F32 && ydt == TE_F32)
             rownorm_kernel<float, float, NV><<<grid, 256, 0, stream>>>(
-                (const float *)x, ldx, w, b, kind, eps, pre, (float *)y, ldy, t, d);
+                (const float *)x, ldx, w, b, ms, kind, eps, pre, (float *)y, ldy, t, d);
         else if (xdt == TE_BF16 && ydt == TE_BF16)
             rownorm_kernel<__nv_bfloat16, __nv_bfloat16, NV><<<grid, 256, 0, stream>>>(
-                (const __nv_bfloat16 *)x, ldx, w, b, kind, eps, pre, (__nv_bfloat16 *)y, ldy, t, d);
+                (const __nv_bfloat16 *)x, ldx, w, b, ms, kind, eps, pre, (__nv_bfloat16 *)y, ldy, t, d);
         else
             rownorm_kernel<__nv_bfloat16, float, NV><<<grid, 256, 0, stream>>>(
-                (const __nv_bfloat16 *)x, ldx, w, b, kind, eps, pre, (float *)y, ldy, t, d);
+                (const __nv_bfloat16 *)x, ldx, w, b, ms, kind, eps, pre, (float *)y, ldy, t, d);
     })
     return launched("rownorm launch");
+}
+
+te_status te_rownorm(const void *x, int32_t xdt, int64_t ldx, const float *w, const float *b,
+                     int32_t kind, float eps, float pre, void *y, int32_t ydt, int64_t ldy,
+                     int32_t t, int32_t d, te_stream stream) {
+    return te_rownorm_mod(x, xdt, ldx, w, b, nullptr, kind, eps, pre, y, ydt, ldy, t, d, stream);
+}
+
+te_status te_add_norm_mod(float *h, const float *t, const float *w_post, const float *gate, float post,
+                          const float *w_next, const float *b_next, const float *ms, int32_t kind,
+                          float eps, void *a, int32_t adt, int32_t rows, int32_t d, te_stream stream) {
+    if (!h) return fail(TE_EINVAL, "add_norm: NULL h");
+    if (w_post && !t) return fail(TE_EINVAL, "add_norm: w_post given without t");
+    if (gate && !t) return fail(TE_EINVAL, "add_norm: gate given without t");
+    if (w_next && !a) return fail(TE_EINVAL, "add_norm: w_next given without a");
+    if (ms && !w_next) return fail(TE_EINVAL, "add_norm: scale given without w_next");
+    if (w_next && !dtype_ok(adt)) return fail(TE_EINVAL, "add_norm: bad dtype");
+    if (kind != TE_NORM_RMS && kind != TE_NORM_LN) return fail(TE_EINVAL, "add_norm: bad kind");
+    if (rows < 0 || d < 8 || d > 4096 || d % 8) return fail(TE_ESHAPE, "add_norm: rows=%d d=%d (d %% 8 == 0, 8..4096)", rows, d);
+    if (!aligned16(h) || (t && !aligned16(t)) || (w_post && !aligned16(w_post)) ||
+        (w_next && !aligned16(w_next)) || (b_next && !aligned16(b_next)) || (a && !aligned16(a)) ||
+        (gate && !aligned16(gate)) || (ms && !aligned16(ms)))
+        return fail(TE_EALIGN, "add_norm: pointers must be 16-byte aligned");
+    if (rows == 0) return TE_OK;
+    // the adaLN loads only in their own instantiation: the unmodulated kernel
+    // keeps its registers (and occupancy)
+    const bool mod = gate || ms;
+    if (d > 1024) {
+        // four warps per row (d <= 4096: at most 4 chunks of 8 per thread)
+        const dim3 grid2((rows + 1) / 2);
+        if (adt == TE_F32) {
+            if (mod)
+                add_norm_wide_kernel<float, 4, true><<<grid2, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (float *)a, rows, d);
+            else
+                add_norm_wide_kernel<float, 4, false><<<grid2, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (float *)a, rows, d);
+        } else {
+            if (mod)
+                add_norm_wide_kernel<__nv_bfloat16, 4, true><<<grid2, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (__nv_bfloat16 *)a, rows, d);
+            else
+                add_norm_wide_kernel<__nv_bfloat16, 4, false><<<grid2, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (__nv_bfloat16 *)a, rows, d);
+        }
+        return launched("add_norm launch");
+    }
+    const dim3 grid((rows + 7) / 8);
+    TE_NV_SWITCH(nv_for(d), {
+        if (adt == TE_F32) {
+            if (mod)
+                add_norm_kernel<float, NV, true><<<grid, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (float *)a, rows, d);
+            else
+                add_norm_kernel<float, NV, false><<<grid, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (float *)a, rows, d);
+        } else {
+            if (mod)
+                add_norm_kernel<__nv_bfloat16, NV, true><<<grid, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (__nv_bfloat16 *)a, rows, d);
+            else
+                add_norm_kernel<__nv_bfloat16, NV, false><<<grid, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (__nv_bfloat16 *)a, rows, d);
+        }
+    })
+    return launched("add_norm launch");
 }
 
 te_status te_add_norm(float *h, const float *t, const float *w_post, float post,
                       const float *w_next, const float *b_next, int32_t kind, float eps, void *a,
                       int32_t adt, int32_t rows, int32_t d, te_stream stream) {
-    if (!h) return fail(TE_EINVAL, "add_norm: NULL h");
-    if (w_post && !t) return fail(TE_EINVAL, "add_norm: w_post given without t");
-    if (w_next && !a) return fail(TE_EINVAL, "add_norm: w_next given without a");
-    if (w_next && !dtype_ok(adt)) return fail(TE_EINVAL, "add_norm: bad dtype");
-    if (kind != TE_NORM_RMS && kind != TE_NORM_LN) return fail(TE_EINVAL, "add_norm: bad kind");
-    if (rows < 0 || d < 8 || d > 4096 || d % 8) return fail(TE_ESHAPE, "add_norm: rows=%d d=%d (d %% 8 == 0, 8..4096)", rows, d);
-    if (!aligned16(h) || (t && !aligned16(t)) || (w_post && !aligned16(w_post)) ||
-        (w_next && !aligned16(w_next)) || (b_next && !aligned16(b_next)) || (a && !aligned16(a)))
-        return fail(TE_EALIGN, "add_norm: pointers must be 16-byte aligned");
-    if (rows == 0) return TE_OK;
-    if (d > 1024) {
-        // four warps per row (d <= 4096: at most 4 chunks of 8 per thread)
-        const dim3 grid2((rows + 1) / 2);
-        if (adt == TE_F32)
-            add_norm_wide_kernel<float, 4><<<grid2, 256, 0, stream>>>(h, t, w_post, post, w_next, b_next,
-                                                                      kind, eps, (float *)a, rows, d);
-        else
-            add_norm_wide_kernel<__nv_bfloat16, 4><<<grid2, 256, 0, stream>>>(
-                h, t, w_post, post, w_next, b_next, kind, eps, (__nv_bfloat16 *)a, rows, d);
-        return launched("add_norm launch");
-    }
-    const dim3 grid((rows + 7) / 8);
-    TE_NV_SWITCH(nv_for(d), {
-        if (adt == TE_F32)
-            add_norm_kernel<float, NV><<<grid, 256, 0, stream>>>(h, t, w_post, post, w_next, b_next,
-                                                                 kind, eps, (float *)a, rows, d);
-        else
-            add_norm_kernel<__nv_bfloat16, NV><<<grid, 256, 0, stream>>>(
-                h, t, w_post, post, w_next, b_next, kind, eps, (__nv_bfloat16 *)a, rows, d);
-    })
-    return launched("add_norm launch");
+    return te_add_norm_mod(h, t, w_post, nullptr, post, w_next, b_next, nullptr, kind, eps, a, adt, rows, d,
+                           stream);
 }
 
 te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t nq,

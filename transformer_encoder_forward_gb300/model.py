@@ -16,7 +16,7 @@ import numpy as np
 
 from . import (TE_ACT_GELU_TANH, TE_ACT_SILU, TE_NORM_LN, TE_NORM_RMS, TE_RESID_PLAIN,
                TE_RESID_SANDWICH, block_workspace, encoder_block_fwd, pool_mean, q8w, rownorm,
-               te_block_desc)
+               rownorm_mod, te_block_desc)
 
 
 def _dev(a, device, dtype=None):
@@ -42,8 +42,10 @@ class LayerWeights:
                 continue
             self.t[key] = (_dev(w["q"], device), _dev(w["s"], device), _dev(w["b"], device))
         for key in ("norm1_w", "norm1_b", "norm2_w", "norm2_b", "post_attn_w", "post_ffn_w",
-                    "q_norm", "k_norm"):
+                    "q_norm", "k_norm", "mod"):
             self.t[key] = _dev(p.get(key), device, torch.float32)
+        # adaLN: s_msa (row 0 of mod) scales this layer's input norm
+        self.s_msa = self.t["mod"][0] if self.t["mod"] is not None else None
 
 
 class EncoderStack:
@@ -90,6 +92,8 @@ class EncoderStack:
         d.post_attn_w, d.post_ffn_w = ptr(L.t["post_attn_w"]), ptr(L.t["post_ffn_w"])
         if nxt is not None:
             d.next_norm_w, d.next_norm_b = ptr(nxt.t["norm1_w"]), ptr(nxt.t["norm1_b"])
+            d.next_mod_scale = ptr(nxt.s_msa)
+        d.mod = ptr(L.t["mod"])
         if cfg.qk_norm:
             d.q_norm, d.k_norm = ptr(L.t["q_norm"]), ptr(L.t["k_norm"])
         if self.rope_sec:
@@ -110,7 +114,11 @@ class EncoderStack:
     def input_norm(self, x, a, stream=None):
         L0 = self.layers[0]
         kind = TE_NORM_LN if self.cfg.norm == "ln" else TE_NORM_RMS
-        rownorm(x, L0.t["norm1_w"], L0.t["norm1_b"], kind, self.cfg.eps, a, stream=stream)
+        if L0.s_msa is not None:
+            rownorm_mod(x, L0.t["norm1_w"], L0.t["norm1_b"], L0.s_msa, kind, self.cfg.eps, a,
+                        stream=stream)
+        else:
+            rownorm(x, L0.t["norm1_w"], L0.t["norm1_b"], kind, self.cfg.eps, a, stream=stream)
 
     def forward_device(self, x, a, out=None, layers=None, stream=None):
         """In place on the device: x (f32 [T, d]) goes through every layer;

@@ -65,6 +65,7 @@ class BlockConfig:
     len_hi: int = 0
     eps: float = 1e-6
     post: float = 1.0
+    adaln: bool = False  # DiT adaLN modulation: per block [s_msa | g_msa | s_mlp | g_mlp]
 
     def window_of(self, layer: int) -> int:
         if self.window == 0:
@@ -96,6 +97,11 @@ CONFIGS = {
     "c5": BlockConfig("c5_dit_stack30_d3840", 30, 3840, 30, 30, 128, 10240, True, "silu",
                       "rms", "sandwich", True, "2d", 0, "all", False, False, (4224, 4224)),
 }
+# The DiT shapes with adaLN modulation (zimage.rs Enc::block ``mods``): the
+# per-block vectors are synthetic (the timestep MLP that makes them lies
+# outside the block).
+CONFIGS["c4m"] = dataclasses.replace(CONFIGS["c4"], name="c4m_dit_block_adaln_d3840", adaln=True)
+CONFIGS["c5m"] = dataclasses.replace(CONFIGS["c5"], name="c5m_dit_stack30_adaln_d3840", adaln=True)
 
 
 def config_seed(key: str) -> int:
@@ -160,7 +166,17 @@ def draw_layer(cfg: BlockConfig, layer: int, seed: int, jitter: bool = True) -> 
     if cfg.qk_norm:
         p["q_norm"], _ = draw_norm(rng, hd, False)
         p["k_norm"], _ = draw_norm(rng, hd, False)
+    if cfg.adaln:
+        p["mod"] = draw_mods(rng, d)
     return p
+
+
+def draw_mods(rng: np.random.Generator, d: int) -> np.ndarray:
+    """adaLN vectors of one block, f32 [4, d] = s_msa | g_msa | s_mlp | g_mlp:
+    scales s ~ 0.1 N(0, 1), gates g = tanh(N(0, 1))."""
+    s = 0.1 * rng.standard_normal((2, d))
+    g = np.tanh(rng.standard_normal((2, d)))
+    return np.stack([s[0], g[0], s[1], g[1]]).astype(np.float32)
 
 
 def draw_final_norm(cfg: BlockConfig, seed: int) -> np.ndarray:
