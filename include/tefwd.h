@@ -63,22 +63,43 @@ typedef enum { TE_NORM_RMS = 0, TE_NORM_LN = 1 } te_norm_kind;
 typedef enum { TE_ACT_GELU_TANH = 0, TE_ACT_SILU = 1 } te_act_kind;
 typedef enum { TE_RESID_PLAIN = 0, TE_RESID_SANDWICH = 1 } te_resid_form;
 
-/* One q8_row weight ([ZI] module doc "The chain": the file's q8_row bytes,
- * int8 tile staged exactly, row scale applied in the f32 epilogue).
+/* One quantised weight.
+ * q8_row ([ZI] module doc "The chain": the file's q8_row bytes, int8 tile
+ * staged exactly, row scale applied in the f32 epilogue):
  *   q     int8 [n, k] row-major (device)        W[o, j] = scale[o] * q[o, j]
  *   scale f32 [n] (device)
  *   bias  f32 [n] (device) or NULL              ([VIT] bias_add of the linears)
- * Requirements: k % 64 == 0, n % 32 == 0, n >= 32. */
+ *   block_scale NULL
+ * 32-element block formats (Q8_0, Q4_0 of [VIT]; unpacked by te_q8_0_unpack /
+ * te_q4_0_unpack into q and block_scale):
+ *   block_scale f16 bits [n, k/32] (device)    W[o, j] = scale[o] * bf16(q[o, j] * d[o, j/32])
+ *   scale may be NULL (1).  The product q * d is exact in f32 and is rounded
+ *   once, to the bf16 tensor-core operand.
+ * Requirements: k % 64 == 0, n % 32 == 0, n >= 32; block_scale 4-byte aligned. */
 typedef struct {
     const int8_t *q;
     const float *scale;
     const float *bias;
     int32_t n;
     int32_t k;
+    const uint16_t *block_scale;
 } te_q8w;
 
 /* Activation applied in a GEMM epilogue (TE_EPI_NONE: none). */
 typedef enum { TE_EPI_NONE = 0, TE_EPI_GELU_TANH = 1, TE_EPI_SILU = 2 } te_epilogue;
+
+/* Unpack the 32-element block formats of [VIT] (the test quantisers of
+ * vision_encoder_gpu.rs; packed row-major, k/32 blocks per row):
+ *   Q8_0: 34 bytes a block = f16 scale d (little-endian) + 32 int8 q
+ *   Q4_0: 18 bytes a block = f16 scale d + 16 bytes; byte i holds element i
+ *         in its low nibble and element i + 16 in its high nibble, each
+ *         stored as q + 8 (q in [-8, 7])
+ * into q int8 [n, k] and block_scale f16 bits [n, k/32] (bit-exact integer
+ * work).  k % 32 == 0; q 16-byte aligned, block_scale 4-byte aligned. */
+te_status te_q8_0_unpack(const void *packed, int32_t n, int32_t k, int8_t *q, uint16_t *block_scale,
+                         te_stream stream);
+te_status te_q4_0_unpack(const void *packed, int32_t n, int32_t k, int8_t *q, uint16_t *block_scale,
+                         te_stream stream);
 
 /* One item of a grouped q8 GEMM ([EG2] Prog::mm item table, one item per
  * grid z; [ZI] Enc::gemm, z <= 3).  All items share the activation x.

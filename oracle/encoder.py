@@ -106,6 +106,54 @@ def q8_linear(x, q, s, b=None, residual=None):
 # norms
 
 
+def decode_q8_0(packed, n, k):
+    """Q8_0 bytes -> (q int8 [n, k], d f64 [n, k/32]) (vision_encoder_gpu.rs
+    ``q8_0_weight``: 34 bytes a block, the f16 scale first, then 32 int8)."""
+    raw = np.frombuffer(bytes(packed), dtype=np.uint8).reshape(n, k // 32, 34)
+    d = raw[:, :, 0:2].copy().view("<f2")[:, :, 0].astype(np.float64)
+    q = raw[:, :, 2:].copy().view(np.int8).reshape(n, k)
+    return q, d
+
+
+def decode_q4_0(packed, n, k):
+    """Q4_0 bytes -> (q int8 [n, k] in [-8, 7], d f64 [n, k/32])
+    (``q4_0_weight``: 18 bytes a block, the f16 scale, then 16 bytes whose
+    low nibble is element i and high nibble element i + 16, stored + 8)."""
+    raw = np.frombuffer(bytes(packed), dtype=np.uint8).reshape(n, k // 32, 18)
+    d = raw[:, :, 0:2].copy().view("<f2")[:, :, 0].astype(np.float64)
+    by = raw[:, :, 2:].astype(np.int16)
+    q = np.concatenate([(by & 15) - 8, (by >> 4) - 8], axis=2).astype(np.int8).reshape(n, k)
+    return q, d
+
+
+def q8_block_linear(x, q, d, s=None, b=None):
+    """The GEMM with 32-element block scales: y[t, o] = s[o] * sum_k x[t, k] *
+    bf16(q[o, k] * d[o, k // 32]) (+ b[o]).  The library feeds the tensor
+    cores bf16 operands, so the dequantised weight is rounded once to bf16
+    (q * d itself is exact); s = None is 1."""
+    q = widen_int8(q)
+    n, k = q.shape
+    wdq = round_bf16(q * np.repeat(np.asarray(d, dtype=np.float64), 32, axis=1)[:, :k])
+    y = np.asarray(x, dtype=np.float64) @ wdq.T
+    if s is not None:
+        y = y * np.asarray(s, dtype=np.float64)[None, :]
+    if b is not None:
+        y = y + np.asarray(b, dtype=np.float64)[None, :]
+    return y
+
+
+def linear(x, w, residual=None):
+    """One projection of the block in its weight's format: q8_row
+    (``q8_linear``) or the packed 32-element block formats (decoded, then
+    ``q8_block_linear``)."""
+    if "packed" in w:
+        dec = decode_q8_0 if w["fmt"] == "q8_0" else decode_q4_0
+        q, d = dec(w["packed"], w["n"], w["k"])
+        y = q8_block_linear(x, q, d, w.get("s"), w.get("b"))
+        return y if residual is None else y + np.asarray(residual, dtype=np.float64)
+    return q8_linear(x, w["q"], w["s"], w["b"], residual=residual)
+
+
 def rms_norm(x, w, eps, pre=1.0):
     """y = rms(pre*x) * w with rms(v) = v / sqrt(mean(v^2) + eps)
     (egemma2.rs ``Prog::rms``; the weight multiplies as stored)."""
@@ -352,9 +400,9 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mo
     a = round_bf16(a)
     qw, kw = H * hd, KV * hd
     qkv = np.concatenate([
-        q8_linear(a, p["wq"]["q"], p["wq"]["s"], p["wq"]["b"]),
-        q8_linear(a, p["wk"]["q"], p["wk"]["s"], p["wk"]["b"]),
-        q8_linear(a, p["wv"]["q"], p["wv"]["s"], p["wv"]["b"]),
+        linear(a, p["wq"]),
+        linear(a, p["wk"]),
+        linear(a, p["wv"]),
     ], axis=1)
     r["qkv_raw"] = qkv = round_bf16(qkv)
     if cfg.qk_norm or tables["sec"]:
@@ -370,22 +418,22 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mo
         o, x = o[rows], x[rows]
     r["o"] = o = round_bf16(o)
     if cfg.form == "plain":
-        x = round_f32(q8_linear(o, p["wo"]["q"], p["wo"]["s"], p["wo"]["b"], residual=x))
+        x = round_f32(linear(o, p["wo"], residual=x))
     else:
-        t = round_f32(q8_linear(o, p["wo"]["q"], p["wo"]["s"], p["wo"]["b"]))
+        t = round_f32(linear(o, p["wo"]))
         r["t"] = t
         x = round_f32(add_norm_sandwich(x, t, p["post_attn_w"], cfg.post, eps, gate=g_msa))
     r["x_mid"] = x
     r["a_mid"] = a2 = round_bf16(norm(cfg.norm, x, p["norm2_w"], p["norm2_b"], eps, mod_scale=s_mlp))
-    parts = [q8_linear(a2, p["wg"]["q"], p["wg"]["s"], p["wg"]["b"])]
+    parts = [linear(a2, p["wg"])]
     if cfg.gated:
-        parts.append(q8_linear(a2, p["wu"]["q"], p["wu"]["s"], p["wu"]["b"]))
+        parts.append(linear(a2, p["wu"]))
     r["gu"] = gu = round_bf16(np.concatenate(parts, axis=1))
     r["m"] = m = round_bf16(gate_act(gu, F, cfg.gated, cfg.act))
     if cfg.form == "plain":
-        x = round_f32(q8_linear(m, p["wd"]["q"], p["wd"]["s"], p["wd"]["b"], residual=x))
+        x = round_f32(linear(m, p["wd"], residual=x))
     else:
-        f = round_f32(q8_linear(m, p["wd"]["q"], p["wd"]["s"], p["wd"]["b"]))
+        f = round_f32(linear(m, p["wd"]))
         r["f"] = f
         x = round_f32(add_norm_sandwich(x, f, p["post_ffn_w"], cfg.post, eps, gate=g_mlp))
     r["x_out"] = x

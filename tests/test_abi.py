@@ -139,6 +139,18 @@ def test_row_ops_reject_bad_arguments(L):
     assert _call(L, "te_pool_mean", FAKE, 64, p, FAKE, 2, None, 1e-6, FAKE, None)[0] == te.TE_EINVAL
 
 
+def test_block_formats_reject_bad_arguments(L):
+    no_scale = (te.te_q8_item * 1)()
+    no_scale[0] = te.te_q8_item(te.te_q8w(FAKE, None, None, 128, 128, None), FAKE, 128, te.TE_F32, 0, None, 0)
+    assert _call(L, "te_q8_linear", FAKE, 128, 16, 128, no_scale, 1, None)[0] == te.TE_EINVAL
+    bad_bs = (te.te_q8_item * 1)()
+    bad_bs[0] = te.te_q8_item(te.te_q8w(FAKE, None, None, 128, 128, FAKE + 2), FAKE, 128, te.TE_F32, 0, None, 0)
+    assert _call(L, "te_q8_linear", FAKE, 128, 16, 128, bad_bs, 1, None)[0] == te.TE_EALIGN
+    assert _call(L, "te_q8_0_unpack", FAKE, 4, 48, FAKE, FAKE, None)[0] == te.TE_ESHAPE      # k % 32
+    assert _call(L, "te_q4_0_unpack", FAKE + 1, 4, 64, FAKE, FAKE, None)[0] == te.TE_EALIGN
+    assert _call(L, "te_q8_0_unpack", None, 4, 64, FAKE, FAKE, None)[0] == te.TE_EINVAL
+
+
 def test_adaln_row_ops_reject_bad_arguments(L):
     # scale without a next norm, gate without a branch, misaligned vectors
     assert _call(L, "te_add_norm_mod", FAKE, FAKE, FAKE, None, 1.0, None, None, FAKE, te.TE_NORM_RMS,

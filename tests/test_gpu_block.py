@@ -72,6 +72,9 @@ FORMS = {
     # the DiT block with adaLN modulation (gates on both branches, scales on
     # every pre-norm including the next block's input)
     "c4m_small": ("c4m", dict(layers=3, d=512, heads=4, kv_heads=4, ffn=1024), (150, 133)),
+    # the ViT block with the 32-element block weight formats
+    "c3q8_small": ("c3q8", dict(layers=2), (200, 129)),
+    "c3q4_small": ("c3q4", dict(layers=2), (200, 129)),
 }
 
 

@@ -401,3 +401,95 @@ def test_pool_mean_matches_oracle(d, norm):
     te.pool_mean(to_dev(x), cu, to_dev(cu), to_dev(w) if norm else None, 1e-6, out)
     ref = O.pool_mean(x, cu, w if norm else None, 1e-6)
     assert rel_frob(to_np(out), ref) < 1e-5
+
+
+# ------------------------------------------------- 32-element block formats
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+def test_block_unpack_is_bit_exact(fmt):
+    torch = _torch()
+    rng = np.random.default_rng([len(fmt), 3])
+    n, k = 77, 640
+    w = synth.draw_block_packed(rng, n, k, fmt)
+    packed = torch.from_numpy(w["packed"]).cuda()
+    q = torch.empty(n, k, dtype=torch.int8, device="cuda")
+    bs = torch.empty(n, k // 32, dtype=torch.int16, device="cuda")
+    (te.q8_0_unpack if fmt == "q8_0" else te.q4_0_unpack)(packed, n, k, q, bs)
+    te.check()
+    q_ref, d_ref = (O.decode_q8_0 if fmt == "q8_0" else O.decode_q4_0)(w["packed"], n, k)
+    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+    d_got = bs.cpu().numpy().view(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(d_got, d_ref)
+
+
+def _block_weight(rng, n, k, fmt, with_scale, bias):
+    """Device operands of one block-format weight (unpacked on the GPU) and
+    the oracle's decode of the same bytes."""
+    torch = _torch()
+    w = synth.draw_block_packed(rng, n, k, fmt)
+    q = torch.empty(n, k, dtype=torch.int8, device="cuda")
+    bs = torch.empty(n, k // 32, dtype=torch.int16, device="cuda")
+    (te.q8_0_unpack if fmt == "q8_0" else te.q4_0_unpack)(torch.from_numpy(w["packed"]).cuda(), n, k, q, bs)
+    q_np, d_np = (O.decode_q8_0 if fmt == "q8_0" else O.decode_q4_0)(w["packed"], n, k)
+    s = rng.uniform(0.5, 2.0, n).astype(np.float32) if with_scale else None
+    b = (rng.standard_normal(n) * 0.02).astype(np.float32) if bias else None
+    dev = (q, to_dev(s) if s is not None else None, to_dev(b) if b is not None else None, bs)
+    return dev, (q_np, d_np, s, b)
+
+
+@pytest.mark.parametrize("m,k,specs,ydt", [
+    (37, 256, [("q8_0", True, False, 384)], "f32"),
+    (300, 512, [("q4_0", False, True, 384), ("q8_0", True, False, 256)], "bf16"),
+    (1000, 3840, [("q8_0", False, False, 384)], "bf16"),
+    # enough feature tiles for two 192-token tiles per weight stage, ragged tail
+    (2200, 3840, [("q4_0", True, False, 3840), ("q8_0", False, False, 3840)], "bf16"),
+])
+def test_block_format_gemm_matches_oracle(m, k, specs, ydt):
+    torch = _torch()
+    rng = np.random.default_rng([m, k, len(specs)])
+    x, x64 = bf16_input(rng, (m, k))
+    dt = torch.float32 if ydt == "f32" else torch.bfloat16
+    items, checks = [], []
+    for fmt, with_scale, bias, n in specs:
+        dev, ref = _block_weight(rng, n, k, fmt, with_scale, bias)
+        y = torch.full((m, n), float("nan"), dtype=dt, device="cuda")
+        items.append({"w": te.q8w(dev[0], dev[1], dev[2], dev[3]), "y": y, "ldy": n})
+        r = O.q8_block_linear(x64, ref[0], ref[1], ref[2], ref[3])
+        checks.append((y, O.round_bf16(r) if ydt == "bf16" else r, dev))
+    te.q8_linear(x, items)
+    te.check()
+    for y, ref, _ in checks:
+        got = to_np(y)
+        assert np.all(np.isfinite(got))
+        assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
+
+
+def test_block_format_gated_linear_matches_oracle():
+    torch = _torch()
+    rng = np.random.default_rng(71)
+    m, k, f = 777, 768, 512
+    x, x64 = bf16_input(rng, (m, k))
+    dg, rg = _block_weight(rng, f, k, "q8_0", False, False)
+    du, ru = _block_weight(rng, f, k, "q4_0", True, False)
+    out = torch.empty(m, f, dtype=torch.bfloat16, device="cuda")
+    te.q8_gated_linear(x, te.q8w(*dg), te.q8w(*du), te.TE_ACT_SILU, out)
+    te.check()
+    g = O.round_bf16(O.q8_block_linear(x64, *rg))
+    u = O.round_bf16(O.q8_block_linear(x64, *ru))
+    ref = O.round_bf16(O.gate_act(np.concatenate([g, u], axis=1), f, True, "silu"))
+    assert rel_frob(to_np(out), ref) < 1e-3
+
+
+def test_block_format_gemm_unit_scales_is_bit_exact():
+    # d = 1 (f16 0x3C00) and integer x: every product and partial sum is an
+    # integer below 2^24, so the result is exact
+    torch = _torch()
+    rng = np.random.default_rng(72)
+    m, k, n = 129, 512, 256
+    xi = rng.integers(-16, 17, (m, k)).astype(np.float32)
+    x = torch.from_numpy(xi).to(torch.bfloat16).cuda()
+    q_np = rng.integers(-127, 128, (n, k), dtype=np.int8)
+    bs = torch.full((n, k // 32), 0x3C00, dtype=torch.int16, device="cuda")
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    te.q8_linear(x, [{"w": te.q8w(to_dev(q_np), None, None, bs), "y": y, "ldy": n}])
+    np.testing.assert_array_equal(to_np(y), (xi.astype(np.int64) @ q_np.astype(np.int64).T).astype(np.float64))

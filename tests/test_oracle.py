@@ -587,3 +587,85 @@ def test_adaln_rejects_the_plain_form():
     with pytest.raises(ValueError):
         O.block_forward(cfg, p, x, x, cu, 0, synth.rope_tables(cfg, cfg.lens),
                         mod=np.zeros((4, cfg.d)))
+
+
+# ------------------------------------------------- 32-element block formats
+# vision_encoder_gpu.rs' test quantisers fix the byte layouts: Q8_0 = f16 scale
+# + 32 int8; Q4_0 = f16 scale + 16 bytes (low nibble element i, high nibble
+# element i + 16, each + 8).  The pins build blocks by hand, round-trip the
+# pages' quantiser rule, and check the block GEMM by brute force.
+
+def test_decode_q8_0_hand_built_block():
+    payload = np.arange(-16, 16, dtype=np.int8)
+    blk = np.concatenate([np.array([0x00, 0x38], np.uint8), payload.view(np.uint8)])   # f16 0.5
+    q, d = O.decode_q8_0(blk.tobytes(), 1, 32)
+    np.testing.assert_array_equal(q[0], payload)
+    assert d.shape == (1, 1) and d[0, 0] == 0.5
+
+
+def test_decode_q4_0_nibble_layout():
+    lo = np.arange(16, dtype=np.uint8)             # element i   -> i - 8
+    hi = (15 - np.arange(16)).astype(np.uint8)     # element 16+i -> 7 - i
+    blk = np.concatenate([np.array([0x00, 0x3C], np.uint8), lo | (hi << 4)])           # f16 1.0
+    q, d = O.decode_q4_0(blk.tobytes(), 1, 32)
+    np.testing.assert_array_equal(q[0, :16], np.arange(16) - 8)
+    np.testing.assert_array_equal(q[0, 16:], 7 - np.arange(16))
+    assert d[0, 0] == 1.0
+
+
+def _quantize_like_the_pages(w, fmt):
+    """Per 32-element block: d = amax / qmax, q = round(w / d) clamped
+    (Q8_0: +-127; Q4_0: stored q + 8 in [0, 15]), d stored as f16."""
+    n, k = w.shape
+    out = bytearray()
+    for row in w:
+        for blk in row.reshape(-1, 32):
+            amax = np.abs(blk).max()
+            d = amax / (127.0 if fmt == "q8_0" else 7.0)
+            inv = 1.0 / d if d else 0.0
+            out += np.float16(d).tobytes()
+            if fmt == "q8_0":
+                out += np.clip(np.round(blk * inv), -127, 127).astype(np.int8).tobytes()
+            else:
+                u = np.clip(np.round(blk * inv) + 8, 0, 15).astype(np.uint8)
+                out += (u[:16] | (u[16:] << 4)).astype(np.uint8).tobytes()
+    return bytes(out)
+
+
+@pytest.mark.parametrize("fmt,qmax", [("q8_0", 127), ("q4_0", 7)])
+def test_block_decode_round_trips_the_quantiser_within_half_a_step(fmt, qmax):
+    rng = np.random.default_rng(12)
+    w = rng.standard_normal((6, 128))
+    dec = O.decode_q8_0 if fmt == "q8_0" else O.decode_q4_0
+    q, d = dec(_quantize_like_the_pages(w, fmt), 6, 128)
+    wd = q.astype(np.float64) * np.repeat(d, 32, axis=1)
+    step = np.repeat(np.abs(w).reshape(6, 4, 32).max(axis=2) / qmax, 32, axis=1)
+    # half a quantisation step, plus the f16 rounding of the scale
+    assert np.all(np.abs(w - wd) <= 0.5 * step + qmax * step * 2.0 ** -11 + 1e-12)
+
+
+def test_block_linear_matches_brute_force_with_bf16_weights():
+    rng = np.random.default_rng(13)
+    m, n, k = 3, 5, 64
+    x = rng.standard_normal((m, k))
+    q = rng.integers(-127, 128, (n, k)).astype(np.int8)
+    d = rng.uniform(0.001, 0.01, (n, k // 32)).astype(np.float16).astype(np.float64)
+    s = rng.uniform(0.5, 2.0, n)
+    b = rng.standard_normal(n)
+    y = O.q8_block_linear(x, q, d, s, b)
+    for t in range(m):
+        for o in range(n):
+            acc = 0.0
+            for j in range(k):
+                acc += x[t, j] * float(O.round_bf16(np.float64(q[o, j]) * d[o, j // 32]))
+            assert abs(y[t, o] - (s[o] * acc + b[o])) <= 1e-12 * (1 + abs(y[t, o]))
+
+
+def test_block_linear_exact_cases():
+    rng = np.random.default_rng(14)
+    x = rng.integers(-16, 17, (7, 96)).astype(np.float64)
+    q = rng.integers(-127, 128, (8, 96)).astype(np.int8)
+    exact = x @ q.astype(np.float64).T
+    # unit scales: the integer product; a power-of-two scale: the same, scaled
+    np.testing.assert_array_equal(O.q8_block_linear(x, q, np.ones((8, 3))), exact)
+    np.testing.assert_array_equal(O.q8_block_linear(x, q, np.full((8, 3), 2.0 ** -7)), exact * 2.0 ** -7)

@@ -35,7 +35,8 @@ c_i32, c_i64, c_f32, c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctype
 
 
 class te_q8w(ctypes.Structure):
-    _fields_ = [("q", c_p), ("scale", c_p), ("bias", c_p), ("n", c_i32), ("k", c_i32)]
+    _fields_ = [("q", c_p), ("scale", c_p), ("bias", c_p), ("n", c_i32), ("k", c_i32),
+                ("block_scale", c_p)]
 
 
 class te_q8_item(ctypes.Structure):
@@ -69,6 +70,8 @@ EXPORTS = {
                                   c_i64, c_i32, c_i32, c_p]),
     "te_add_norm": (ctypes.c_int, [c_p, c_p, c_p, c_f32, c_p, c_p, c_i32, c_f32, c_p, c_i32, c_i32,
                                    c_i32, c_p]),
+    "te_q8_0_unpack": (ctypes.c_int, [c_p, c_i32, c_i32, c_p, c_p, c_p]),
+    "te_q4_0_unpack": (ctypes.c_int, [c_p, c_i32, c_i32, c_p, c_p, c_p]),
     "te_rownorm_mod": (ctypes.c_int, [c_p, c_i32, c_i64, c_p, c_p, c_p, c_i32, c_f32, c_f32, c_p,
                                       c_i32, c_i64, c_i32, c_i32, c_p]),
     "te_add_norm_mod": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_f32, c_p, c_p, c_p, c_i32, c_f32, c_p,
@@ -130,10 +133,23 @@ def _host_i32(a):
 
 # --------------------------------------------------------------------- ops
 
-def q8w(q, s, b=None) -> te_q8w:
-    """Descriptor of one q8_row weight held in device tensors (q int8 [n, k],
-    s f32 [n], optional b f32 [n])."""
-    return te_q8w(_ptr(q), _ptr(s), _ptr(b), q.shape[0], q.shape[1])
+def q8w(q, s, b=None, block_scale=None) -> te_q8w:
+    """Descriptor of one quantised weight held in device tensors (q int8
+    [n, k], s f32 [n] or None, optional b f32 [n]; block_scale: f16 bits
+    [n, k/32] for the 32-element block formats, else None for q8_row)."""
+    return te_q8w(_ptr(q), _ptr(s), _ptr(b), q.shape[0], q.shape[1], _ptr(block_scale))
+
+
+def q8_0_unpack(packed, n, k, q, block_scale, stream=None):
+    """Packed Q8_0 bytes (uint8 device tensor) -> q int8 [n, k], block_scale [n, k/32]."""
+    _ok(lib().te_q8_0_unpack(packed.data_ptr(), n, k, q.data_ptr(), block_scale.data_ptr(),
+                             _stream(stream)))
+
+
+def q4_0_unpack(packed, n, k, q, block_scale, stream=None):
+    """Packed Q4_0 bytes (uint8 device tensor) -> q int8 [n, k], block_scale [n, k/32]."""
+    _ok(lib().te_q4_0_unpack(packed.data_ptr(), n, k, q.data_ptr(), block_scale.data_ptr(),
+                             _stream(stream)))
 
 
 def q8_linear(x, items: Sequence[dict], stream=None):

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtefwd.so")
-SOURCES = ["rowops.cu", "q8_linear.cu", "attn.cu", "block.cu", "block_static.cu"]
+SOURCES = ["rowops.cu", "q8_linear.cu", "attn.cu", "block.cu", "block_static.cu", "codecs.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

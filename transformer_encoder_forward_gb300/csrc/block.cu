@@ -41,7 +41,10 @@ WsLayout ws_layout(const te_block_desc &d, int32_t t) {
 }
 
 te_status check_w(const te_q8w &w, int n, int k, const char *name) {
-    if (!w.q || !w.scale) return fail(TE_EINVAL, "block: weight %s has a NULL q or scale", name);
+    if (!w.q || (!w.scale && !w.block_scale))
+        return fail(TE_EINVAL, "block: weight %s has a NULL q or scale (NULL scale needs block scales)", name);
+    if (reinterpret_cast<uintptr_t>(w.block_scale) & 3)
+        return fail(TE_EALIGN, "block: weight %s: block scales must be 4-byte aligned", name);
     if (w.n != n || w.k != k)
         return fail(TE_ESHAPE, "block: weight %s is [%d, %d], need [%d, %d]", name, w.n, w.k, n, k);
     if (!aligned16(w.q) || (reinterpret_cast<uintptr_t>(w.scale) & 3) ||

@@ -61,10 +61,12 @@ constexpr int NWARPS = 14;    // producer, MMA, 8 converters, 4 epilogue
 constexpr int NTHREADS = NWARPS * 32;
 
 struct Item {
-    const float *scale;
+    const float *scale;       // NULL: 1 (block-scaled weights)
     const float *bias;
     const float *scale2;      // gated mode: the up projection's scale and bias
     const float *bias2;
+    const uint16_t *bsc;      // f16 block scales [n, k/32] of the 32-element formats, or NULL
+    const uint16_t *bsc2;     // gated mode: the up projection's
     void *y;
     const float *resid;
     long long ldy, ldr;
@@ -77,6 +79,7 @@ struct Params {
     CUtensorMap ty[MAXZ];     // y_i: [m, n_i] (f32 or bf16), 32-feature boxes
     Item it[MAXZ];
     int z, m, k, ttiles, nunits;
+    int kb32;                 // k / 32: the row stride of the block scales
 };
 
 __device__ int g_gemm_err;
@@ -127,6 +130,19 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
     const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - magic;
     lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
     hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+}
+
+// As widen4, each value then multiplied by the block scale d (exact in f32:
+// 8 x 11 significant bits) and rounded once to bf16.
+__device__ __forceinline__ void widen4_scaled(uint32_t w, float d, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float magic = 8388736.0f;   // 2^23 + 128
+    const float f0 = (__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - magic) * d;
+    const float f1 = (__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - magic) * d;
+    const float f2 = (__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - magic) * d;
+    const float f3 = (__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - magic) * d;
+    lo = pack_bf16x2(f0, f1);
+    hi = pack_bf16x2(f2, f3);
 }
 
 struct TileCoord {
@@ -333,8 +349,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const uint32_t tl = (uint32_t)(32 * q) << 16;
         int kbg = 0;
         for (int u = cid; u < nunits && ok; u += ncl) {
+            // the 32-element block formats: this row's f16 block scales (the
+            // item is uniform over the warp: a warp's 32 rows share it)
+            const uint16_t *bsr = nullptr;
+            bool blk = false;
+            {
+                const TileCoord tc = tile_coord<GATED>(p, u, rank);
+                const bool upper = GATED && row >= BM / 2;
+                const int o = tc.o0 + (GATED ? (row & (BM / 2 - 1)) : row);
+                const uint16_t *b = upper ? p.it[tc.zi].bsc2 : p.it[tc.zi].bsc;
+                blk = b != nullptr;
+                if (blk && o < p.it[tc.zi].n) bsr = b + (long long)o * p.kb32;
+            }
             for (int kb = 0; kb < nkb; ++kb, ++kbg) {
                 const int s = kbg % NST, a = kbg % NA;
+                // blocks 4 kb + 2 h and the next one (issued before the waits)
+                uint32_t dd = 0;
+                const int j0 = kb * 4 + h * 2;
+                if (bsr && j0 < p.kb32) dd = *reinterpret_cast<const uint32_t *>(bsr + j0);
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8 * s, (kbg / NST) & 1) &&
                                                  mbar_wait(bar_aempty + 8 * a, ((kbg / NA) & 1) ^ 1));
                 if (!ok) break;
@@ -342,13 +374,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + h * L::WBOX + row * 64;
                 const int sw = (row >> 1) & 3;
                 uint32_t r[32];
+                if (blk) {
+                    const float d2[2] = {__half2float(__ushort_as_half((unsigned short)(dd & 0xFFFFu))),
+                                         __half2float(__ushort_as_half((unsigned short)(dd >> 16)))};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw) << 4));
-                    widen4(v.x, r[8 * c + 0], r[8 * c + 1]);
-                    widen4(v.y, r[8 * c + 2], r[8 * c + 3]);
-                    widen4(v.z, r[8 * c + 4], r[8 * c + 5]);
-                    widen4(v.w, r[8 * c + 6], r[8 * c + 7]);
+                    for (int c = 0; c < 4; ++c) {       // chunks 0-1: block j0, 2-3: block j0 + 1
+                        const uint4 v = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw) << 4));
+                        const float d = d2[c >> 1];
+                        widen4_scaled(v.x, d, r[8 * c + 0], r[8 * c + 1]);
+                        widen4_scaled(v.y, d, r[8 * c + 2], r[8 * c + 3]);
+                        widen4_scaled(v.z, d, r[8 * c + 4], r[8 * c + 5]);
+                        widen4_scaled(v.w, d, r[8 * c + 6], r[8 * c + 7]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw) << 4));
+                        widen4(v.x, r[8 * c + 0], r[8 * c + 1]);
+                        widen4(v.y, r[8 * c + 2], r[8 * c + 3]);
+                        widen4(v.z, r[8 * c + 4], r[8 * c + 5]);
+                        widen4(v.w, r[8 * c + 6], r[8 * c + 7]);
+                    }
                 }
                 tmem_st32(tbase + tl + L::A_COL + 64 * a + 32 * h, r);
                 tmem_wait_st();
@@ -386,7 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const bool ov = o < p.it[tc.zi].n;
             const float *scale = upper ? p.it[tc.zi].scale2 : p.it[tc.zi].scale;
             const float *bias = upper ? p.it[tc.zi].bias2 : p.it[tc.zi].bias;
-            const float sc = ov ? scale[o] : 0.f;
+            const float sc = ov ? (scale ? scale[o] : 1.f) : 0.f;
             const float bi = (ov && bias) ? bias[o] : 0.f;
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_accfull + 8 * b, ph));
             if (GATED) {
@@ -658,11 +704,14 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
     p.z = z;
     p.m = m;
     p.k = k;
+    p.kb32 = k / 32;
     int ftiles = 0;
     for (int i = 0; i < z; ++i) {
         const te_q8_item &src = items[i];
-        if (!src.w.q || !src.w.scale || !src.y)
-            return fail(TE_EINVAL, "q8_linear: item %d has a NULL q, scale or y", i);
+        if (!src.w.q || !src.y || (!src.w.scale && !src.w.block_scale))
+            return fail(TE_EINVAL, "q8_linear: item %d has a NULL q, y or scale (NULL scale needs block scales)", i);
+        if (src.w.block_scale && (reinterpret_cast<uintptr_t>(src.w.block_scale) & 3))
+            return fail(TE_EALIGN, "q8_linear: item %d: block scales must be 4-byte aligned", i);
         if (src.w.k != k) return fail(TE_ESHAPE, "q8_linear: item %d has k=%d, x has %d", i, src.w.k, k);
         if (src.w.n < 32 || src.w.n % 32)
             return fail(TE_ESHAPE, "q8_linear: item %d n=%d (multiple of 32)", i, src.w.n);
@@ -688,6 +737,7 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         Item &d = p.it[i];
         d.scale = src.w.scale;
         d.bias = src.w.bias;
+        d.bsc = src.w.block_scale;
         d.y = src.y;
         d.resid = src.residual;
         d.ldy = src.ldy;
@@ -729,8 +779,10 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     if (act != TE_ACT_GELU_TANH && act != TE_ACT_SILU) return fail(TE_EINVAL, "q8_gated_linear: bad act");
     if (m < 0 || k < 64 || k % 64) return fail(TE_ESHAPE, "q8_gated_linear: m=%d k=%d (k %% 64 == 0)", m, k);
     if (ldx < k || ldx % 8) return fail(TE_ESHAPE, "q8_gated_linear: ldx=%lld (>= k, multiple of 8)", (long long)ldx);
-    if (!wg->q || !wg->scale || !wu->q || !wu->scale)
-        return fail(TE_EINVAL, "q8_gated_linear: NULL q or scale");
+    if (!wg->q || !wu->q || (!wg->scale && !wg->block_scale) || (!wu->scale && !wu->block_scale))
+        return fail(TE_EINVAL, "q8_gated_linear: NULL q or scale (NULL scale needs block scales)");
+    if ((reinterpret_cast<uintptr_t>(wg->block_scale) & 3) || (reinterpret_cast<uintptr_t>(wu->block_scale) & 3))
+        return fail(TE_EALIGN, "q8_gated_linear: block scales must be 4-byte aligned");
     if (wg->k != k || wu->k != k || wg->n != wu->n)
         return fail(TE_ESHAPE, "q8_gated_linear: wg [%d, %d] and wu [%d, %d] must both be [f, %d]", wg->n,
                     wg->k, wu->n, wu->k, k);
@@ -747,11 +799,14 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     p.z = 1;
     p.m = m;
     p.k = k;
+    p.kb32 = k / 32;
     Item &d = p.it[0];
     d.scale = wg->scale;
     d.bias = wg->bias;
     d.scale2 = wu->scale;
     d.bias2 = wu->bias;
+    d.bsc = wg->block_scale;
+    d.bsc2 = wu->block_scale;
     d.y = out;
     d.ldy = ldm;
     d.n = f;

@@ -15,8 +15,8 @@ from typing import List, Optional
 import numpy as np
 
 from . import (TE_ACT_GELU_TANH, TE_ACT_SILU, TE_NORM_LN, TE_NORM_RMS, TE_RESID_PLAIN,
-               TE_RESID_SANDWICH, block_workspace, encoder_block_fwd, pool_mean, q8w, rownorm,
-               rownorm_mod, te_block_desc)
+               TE_RESID_SANDWICH, block_workspace, encoder_block_fwd, pool_mean, q4_0_unpack,
+               q8_0_unpack, q8w, rownorm, rownorm_mod, te_block_desc)
 
 
 def _dev(a, device, dtype=None):
@@ -40,7 +40,17 @@ class LayerWeights:
             if w is None:
                 self.t[key] = None
                 continue
-            self.t[key] = (_dev(w["q"], device), _dev(w["s"], device), _dev(w["b"], device))
+            if "packed" in w:
+                # a 32-element block format: upload the packed bytes and
+                # unpack them on the device once (int8 q + f16 block scales)
+                n, k = w["n"], w["k"]
+                q = torch.empty(n, k, dtype=torch.int8, device=device)
+                bs = torch.empty(n, k // 32, dtype=torch.int16, device=device)
+                unpack = q8_0_unpack if w["fmt"] == "q8_0" else q4_0_unpack
+                unpack(_dev(w["packed"], device), n, k, q, bs)
+                self.t[key] = (q, _dev(w.get("s"), device), _dev(w["b"], device), bs)
+            else:
+                self.t[key] = (_dev(w["q"], device), _dev(w["s"], device), _dev(w["b"], device), None)
         for key in ("norm1_w", "norm1_b", "norm2_w", "norm2_b", "post_attn_w", "post_ffn_w",
                     "q_norm", "k_norm", "mod"):
             self.t[key] = _dev(p.get(key), device, torch.float32)

@@ -66,6 +66,7 @@ class BlockConfig:
     eps: float = 1e-6
     post: float = 1.0
     adaln: bool = False  # DiT adaLN modulation: per block [s_msa | g_msa | s_mlp | g_mlp]
+    codec: str = "q8_row"  # weight format: "q8_row" | "q8_0" | "q4_0"
 
     def window_of(self, layer: int) -> int:
         if self.window == 0:
@@ -102,6 +103,10 @@ CONFIGS = {
 # outside the block).
 CONFIGS["c4m"] = dataclasses.replace(CONFIGS["c4"], name="c4m_dit_block_adaln_d3840", adaln=True)
 CONFIGS["c5m"] = dataclasses.replace(CONFIGS["c5"], name="c5m_dit_stack30_adaln_d3840", adaln=True)
+# The ViT stack with the 32-element block weight formats of
+# vision_encoder_gpu.rs (Q8_0, Q4_0) in place of q8_row.
+CONFIGS["c3q8"] = dataclasses.replace(CONFIGS["c3"], name="c3q8_vit_stack16_q8_0_d768", codec="q8_0")
+CONFIGS["c3q4"] = dataclasses.replace(CONFIGS["c3"], name="c3q4_vit_stack16_q4_0_d768", codec="q4_0")
 
 
 def config_seed(key: str) -> int:
@@ -139,6 +144,28 @@ def draw_q8(rng: np.random.Generator, n: int, k: int, jitter: bool, bias: bool):
     return {"q": q, "s": s.astype(np.float32), "b": b}
 
 
+def draw_block_packed(rng: np.random.Generator, n: int, k: int, fmt: str) -> dict:
+    """Packed bytes of a [n, k] weight in a 32-element block format (the
+    layout of vision_encoder_gpu.rs' test quantisers): per block an f16 scale
+    then the payload.  q uniform on the format's range; scales U[0.5, 1.5]
+    times the value that gives the weights the spread of the q8_row draws
+    (standard deviation about 0.58 / sqrt(k))."""
+    nb = k // 32
+    if fmt == "q8_0":
+        q = rng.integers(-127, 128, (n, nb, 32)).astype(np.int8)
+        d = (rng.uniform(0.5, 1.5, (n, nb)) / (127 * np.sqrt(k))).astype(np.float16)
+        payload = q.view(np.uint8)
+    elif fmt == "q4_0":
+        q = rng.integers(-8, 8, (n, nb, 32)).astype(np.int8)
+        d = (rng.uniform(0.5, 1.5, (n, nb)) / (8 * np.sqrt(k))).astype(np.float16)
+        u = (q.astype(np.int16) + 8).astype(np.uint8)
+        payload = (u[:, :, :16] | (u[:, :, 16:] << 4)).astype(np.uint8)
+    else:
+        raise ValueError(fmt)
+    blocks = np.concatenate([d.view(np.uint8).reshape(n, nb, 2), payload], axis=2)
+    return {"packed": blocks.reshape(-1).copy(), "n": n, "k": k, "fmt": fmt}
+
+
 def draw_norm(rng: np.random.Generator, d: int, with_bias: bool):
     w = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
     b = (0.1 * rng.standard_normal(d)).astype(np.float32) if with_bias else None
@@ -149,14 +176,23 @@ def draw_layer(cfg: BlockConfig, layer: int, seed: int, jitter: bool = True) -> 
     """All weights of one layer (host numpy arrays)."""
     rng = np.random.default_rng([seed, 7919, layer])
     d, hd, F = cfg.d, cfg.hd, cfg.ffn
+
+    def w(n, k):
+        if cfg.codec == "q8_row":
+            return draw_q8(rng, n, k, jitter, cfg.bias)
+        out = draw_block_packed(rng, n, k, cfg.codec)
+        out["s"] = None
+        out["b"] = (rng.standard_normal(n) * 0.02).astype(np.float32) if cfg.bias else None
+        return out
+
     p = {}
-    p["wq"] = draw_q8(rng, cfg.heads * hd, d, jitter, cfg.bias)
-    p["wk"] = draw_q8(rng, cfg.kv_heads * hd, d, jitter, cfg.bias)
-    p["wv"] = draw_q8(rng, cfg.kv_heads * hd, d, jitter, cfg.bias)
-    p["wo"] = draw_q8(rng, d, cfg.heads * hd, jitter, cfg.bias)
-    p["wg"] = draw_q8(rng, F, d, jitter, cfg.bias)
-    p["wu"] = draw_q8(rng, F, d, jitter, cfg.bias) if cfg.gated else None
-    p["wd"] = draw_q8(rng, d, F, jitter, cfg.bias)
+    p["wq"] = w(cfg.heads * hd, d)
+    p["wk"] = w(cfg.kv_heads * hd, d)
+    p["wv"] = w(cfg.kv_heads * hd, d)
+    p["wo"] = w(d, cfg.heads * hd)
+    p["wg"] = w(F, d)
+    p["wu"] = w(F, d) if cfg.gated else None
+    p["wd"] = w(d, F)
     ln = cfg.norm == "ln"
     p["norm1_w"], p["norm1_b"] = draw_norm(rng, d, ln)          # attention pre-norm
     p["norm2_w"], p["norm2_b"] = draw_norm(rng, d, ln)          # FFN pre-norm
