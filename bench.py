@@ -504,9 +504,9 @@ def cpu_sample(key):
     cfg = synth.CONFIGS[key]
     lens = synth.draw_lens(cfg)
     seed = synth.config_seed(key)
-    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1, "c3q8": 1, "c3q4": 1}[key]
+    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1, "c3q8": 1, "c3q4": 1, "c4f": 1}[key]
     sl = lens[:take]
-    if key in ("c4", "c5", "c4m", "c5m"):
+    if key in ("c4", "c5", "c4m", "c5m", "c4f"):
         sl = np.asarray([min(int(sl[0]), 1056)], dtype=np.int32)
     return cfg, sl, seed
 

@@ -75,7 +75,13 @@ typedef enum { TE_RESID_PLAIN = 0, TE_RESID_SANDWICH = 1 } te_resid_form;
  *   block_scale f16 bits [n, k/32] (device)    W[o, j] = scale[o] * bf16(q[o, j] * d[o, j/32])
  *   scale may be NULL (1).  The product q * d is exact in f32 and is rounded
  *   once, to the bf16 tensor-core operand.
- * Requirements: k % 64 == 0, n % 32 == 0, n >= 32; block_scale 4-byte aligned. */
+ * q8_2f ([ZI] ensure_dev: q8_row plus a per-column f16 field):
+ *   col f32 [k] (device) or NULL               W[o, j] = scale[o] * bf16(q[o, j] * col[j])
+ *   ([ZI] folds the field into the activation's producer; here it is folded
+ *   into the widened weight, rounded once to the bf16 operand.)  col and
+ *   block_scale may not both be given.
+ * Requirements: k % 64 == 0, n % 32 == 0, n >= 32; block_scale 4-byte and
+ * col 16-byte aligned. */
 typedef struct {
     const int8_t *q;
     const float *scale;
@@ -83,6 +89,7 @@ typedef struct {
     int32_t n;
     int32_t k;
     const uint16_t *block_scale;
+    const float *col;
 } te_q8w;
 
 /* Activation applied in a GEMM epilogue (TE_EPI_NONE: none). */

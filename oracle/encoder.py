@@ -142,6 +142,22 @@ def q8_block_linear(x, q, d, s=None, b=None):
     return y
 
 
+def q8_2f_linear(x, q, col, s, b=None, residual=None):
+    """The q8_2f GEMM: y[t, o] = s[o] * sum_k x[t, k] * bf16(q[o, k] * col[k])
+    (+ b[o]) (+ residual).  zimage.rs ``ensure_dev`` (q8_2f = q8_row bytes +
+    f16 row scales + an f16 field per column); the library folds the column
+    field into the widened weight and rounds that product once to the bf16
+    tensor-core operand."""
+    wq = round_bf16(widen_int8(q) * np.asarray(col, dtype=np.float64)[None, :])
+    y = np.asarray(x, dtype=np.float64) @ wq.T
+    y = y * np.asarray(s, dtype=np.float64)[None, :]
+    if b is not None:
+        y = y + np.asarray(b, dtype=np.float64)[None, :]
+    if residual is not None:
+        y = y + np.asarray(residual, dtype=np.float64)
+    return y
+
+
 def linear(x, w, residual=None):
     """One projection of the block in its weight's format: q8_row
     (``q8_linear``) or the packed 32-element block formats (decoded, then
@@ -151,6 +167,8 @@ def linear(x, w, residual=None):
         q, d = dec(w["packed"], w["n"], w["k"])
         y = q8_block_linear(x, q, d, w.get("s"), w.get("b"))
         return y if residual is None else y + np.asarray(residual, dtype=np.float64)
+    if w.get("col") is not None:
+        return q8_2f_linear(x, w["q"], w["col"], w["s"], w["b"], residual=residual)
     return q8_linear(x, w["q"], w["s"], w["b"], residual=residual)
 
 

@@ -493,3 +493,30 @@ def test_block_format_gemm_unit_scales_is_bit_exact():
     y = torch.empty(m, n, dtype=torch.float32, device="cuda")
     te.q8_linear(x, [{"w": te.q8w(to_dev(q_np), None, None, bs), "y": y, "ldy": n}])
     np.testing.assert_array_equal(to_np(y), (xi.astype(np.int64) @ q_np.astype(np.int64).T).astype(np.float64))
+
+
+# ------------------------------------------------------------------- q8_2f
+
+@pytest.mark.parametrize("m,k,ns,ydt", [(101, 256, [256], "f32"), (777, 768, [768, 512], "bf16"),
+                                        (2200, 3840, [3840, 3840], "bf16"), (300, 320, [96], "f32")])
+def test_q8_2f_gemm_matches_oracle(m, k, ns, ydt):
+    torch = _torch()
+    rng = np.random.default_rng([m, k, 2])
+    x, x64 = bf16_input(rng, (m, k))
+    dt = torch.float32 if ydt == "f32" else torch.bfloat16
+    items, checks, keep = [], [], []
+    for n in ns:
+        w = synth.draw_q8(rng, n, k, True, True)
+        col = rng.uniform(0.5, 1.5, k).astype(np.float16).astype(np.float32)
+        dev = (to_dev(w["q"]), to_dev(w["s"]), to_dev(w["b"]), None, to_dev(col))
+        keep.append(dev)
+        y = torch.full((m, n), float("nan"), dtype=dt, device="cuda")
+        items.append({"w": te.q8w(*dev), "y": y, "ldy": n})
+        r = O.q8_2f_linear(x64, w["q"], col, w["s"], w["b"])
+        checks.append((y, O.round_bf16(r) if ydt == "bf16" else r))
+    te.q8_linear(x, items)
+    te.check()
+    for y, ref in checks:
+        got = to_np(y)
+        assert np.all(np.isfinite(got))
+        assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)

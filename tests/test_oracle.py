@@ -669,3 +669,39 @@ def test_block_linear_exact_cases():
     # unit scales: the integer product; a power-of-two scale: the same, scaled
     np.testing.assert_array_equal(O.q8_block_linear(x, q, np.ones((8, 3))), exact)
     np.testing.assert_array_equal(O.q8_block_linear(x, q, np.full((8, 3), 2.0 ** -7)), exact * 2.0 ** -7)
+
+
+# ---------------------------------------------------------------- q8_2f
+# zimage.rs ensure_dev: q8_2f = the q8_row bytes + a per-column f16 field;
+# W[o, k] = s[o] q[o, k] col[k].
+
+def test_q8_2f_unit_field_is_q8_row():
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((4, 64))
+    q = rng.integers(-127, 128, (6, 64)).astype(np.int8)
+    s = rng.uniform(0.5, 2, 6)
+    np.testing.assert_array_equal(O.q8_2f_linear(x, q, np.ones(64), s), O.q8_linear(x, q, s))
+
+
+def test_q8_2f_power_of_two_field_scales_columns_exactly():
+    # col[k] = 2^e_k: bf16(q col) = q col exactly, so y = (x * col) q^T s
+    rng = np.random.default_rng(22)
+    x = rng.integers(-16, 17, (5, 64)).astype(np.float64)
+    q = rng.integers(-127, 128, (7, 64)).astype(np.int8)
+    col = 2.0 ** rng.integers(-3, 4, 64)
+    y = O.q8_2f_linear(x, q, col, np.ones(7))
+    np.testing.assert_array_equal(y, (x * col[None, :]) @ q.astype(np.float64).T)
+
+
+def test_q8_2f_matches_brute_force():
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((3, 64))
+    q = rng.integers(-127, 128, (4, 64)).astype(np.int8)
+    col = rng.uniform(0.5, 1.5, 64).astype(np.float16).astype(np.float64)
+    s = rng.uniform(0.5, 2, 4)
+    b = rng.standard_normal(4)
+    y = O.q8_2f_linear(x, q, col, s, b)
+    for t in range(3):
+        for o in range(4):
+            acc = sum(x[t, j] * float(O.round_bf16(float(q[o, j]) * col[j])) for j in range(64))
+            assert abs(y[t, o] - (s[o] * acc + b[o])) <= 1e-12 * (1 + abs(y[t, o]))

@@ -36,7 +36,7 @@ c_i32, c_i64, c_f32, c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctype
 
 class te_q8w(ctypes.Structure):
     _fields_ = [("q", c_p), ("scale", c_p), ("bias", c_p), ("n", c_i32), ("k", c_i32),
-                ("block_scale", c_p)]
+                ("block_scale", c_p), ("col", c_p)]
 
 
 class te_q8_item(ctypes.Structure):
@@ -133,11 +133,12 @@ def _host_i32(a):
 
 # --------------------------------------------------------------------- ops
 
-def q8w(q, s, b=None, block_scale=None) -> te_q8w:
+def q8w(q, s, b=None, block_scale=None, col=None) -> te_q8w:
     """Descriptor of one quantised weight held in device tensors (q int8
     [n, k], s f32 [n] or None, optional b f32 [n]; block_scale: f16 bits
-    [n, k/32] for the 32-element block formats, else None for q8_row)."""
-    return te_q8w(_ptr(q), _ptr(s), _ptr(b), q.shape[0], q.shape[1], _ptr(block_scale))
+    [n, k/32] for the 32-element block formats; col: f32 [k], the q8_2f
+    column field; both None for q8_row)."""
+    return te_q8w(_ptr(q), _ptr(s), _ptr(b), q.shape[0], q.shape[1], _ptr(block_scale), _ptr(col))
 
 
 def q8_0_unpack(packed, n, k, q, block_scale, stream=None):

@@ -45,6 +45,8 @@ te_status check_w(const te_q8w &w, int n, int k, const char *name) {
         return fail(TE_EINVAL, "block: weight %s has a NULL q or scale (NULL scale needs block scales)", name);
     if (reinterpret_cast<uintptr_t>(w.block_scale) & 3)
         return fail(TE_EALIGN, "block: weight %s: block scales must be 4-byte aligned", name);
+    if (w.col && (w.block_scale || !aligned16(w.col)))
+        return fail(TE_EINVAL, "block: weight %s: the column field must be 16-byte aligned, without block scales", name);
     if (w.n != n || w.k != k)
         return fail(TE_ESHAPE, "block: weight %s is [%d, %d], need [%d, %d]", name, w.n, w.k, n, k);
     if (!aligned16(w.q) || (reinterpret_cast<uintptr_t>(w.scale) & 3) ||

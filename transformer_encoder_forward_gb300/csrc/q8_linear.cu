@@ -67,6 +67,8 @@ struct Item {
     const float *bias2;
     const uint16_t *bsc;      // f16 block scales [n, k/32] of the 32-element formats, or NULL
     const uint16_t *bsc2;     // gated mode: the up projection's
+    const float *col;         // q8_2f column field [k], or NULL
+    const float *col2;        // gated mode: the up projection's
     void *y;
     const float *resid;
     long long ldy, ldr;
@@ -130,6 +132,19 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
     const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - magic;
     lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
     hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+}
+
+// As widen4, value e multiplied by its own factor c[e] (the q8_2f column
+// field) and rounded once to bf16.
+__device__ __forceinline__ void widen4_col(uint32_t w, float4 c, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float magic = 8388736.0f;   // 2^23 + 128
+    const float f0 = (__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - magic) * c.x;
+    const float f1 = (__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - magic) * c.y;
+    const float f2 = (__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - magic) * c.z;
+    const float f3 = (__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - magic) * c.w;
+    lo = pack_bf16x2(f0, f1);
+    hi = pack_bf16x2(f2, f3);
 }
 
 // As widen4, each value then multiplied by the block scale d (exact in f32:
@@ -352,12 +367,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // the 32-element block formats: this row's f16 block scales (the
             // item is uniform over the warp: a warp's 32 rows share it)
             const uint16_t *bsr = nullptr;
+            const float *colp = nullptr;              // q8_2f: the column field (all rows)
             bool blk = false;
             {
                 const TileCoord tc = tile_coord<GATED>(p, u, rank);
                 const bool upper = GATED && row >= BM / 2;
                 const int o = tc.o0 + (GATED ? (row & (BM / 2 - 1)) : row);
                 const uint16_t *b = upper ? p.it[tc.zi].bsc2 : p.it[tc.zi].bsc;
+                colp = upper ? p.it[tc.zi].col2 : p.it[tc.zi].col;
                 blk = b != nullptr;
                 if (blk && o < p.it[tc.zi].n) bsr = b + (long long)o * p.kb32;
             }
@@ -374,7 +391,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + h * L::WBOX + row * 64;
                 const int sw = (row >> 1) & 3;
                 uint32_t r[32];
-                if (blk) {
+                if (colp) {
+                    // column field of K = kb*128 + h*64 + 16c + e (zero past k: the
+                    // weight reads zeros there too)
+                    const int k0 = kb * BK + h * BOX;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw) << 4));
+                        float4 cv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            cv[e] = k0 + 16 * c + 4 * e < p.k
+                                        ? __ldg(reinterpret_cast<const float4 *>(colp + k0 + 16 * c + 4 * e))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                        widen4_col(v.x, cv[0], r[8 * c + 0], r[8 * c + 1]);
+                        widen4_col(v.y, cv[1], r[8 * c + 2], r[8 * c + 3]);
+                        widen4_col(v.z, cv[2], r[8 * c + 4], r[8 * c + 5]);
+                        widen4_col(v.w, cv[3], r[8 * c + 6], r[8 * c + 7]);
+                    }
+                } else if (blk) {
                     const float d2[2] = {__half2float(__ushort_as_half((unsigned short)(dd & 0xFFFFu))),
                                          __half2float(__ushort_as_half((unsigned short)(dd >> 16)))};
 #pragma unroll
@@ -712,6 +747,10 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
             return fail(TE_EINVAL, "q8_linear: item %d has a NULL q, y or scale (NULL scale needs block scales)", i);
         if (src.w.block_scale && (reinterpret_cast<uintptr_t>(src.w.block_scale) & 3))
             return fail(TE_EALIGN, "q8_linear: item %d: block scales must be 4-byte aligned", i);
+        if (src.w.col && src.w.block_scale)
+            return fail(TE_EINVAL, "q8_linear: item %d: a column field and block scales together", i);
+        if (src.w.col && !aligned16(src.w.col))
+            return fail(TE_EALIGN, "q8_linear: item %d: the column field must be 16-byte aligned", i);
         if (src.w.k != k) return fail(TE_ESHAPE, "q8_linear: item %d has k=%d, x has %d", i, src.w.k, k);
         if (src.w.n < 32 || src.w.n % 32)
             return fail(TE_ESHAPE, "q8_linear: item %d n=%d (multiple of 32)", i, src.w.n);
@@ -738,6 +777,7 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         d.scale = src.w.scale;
         d.bias = src.w.bias;
         d.bsc = src.w.block_scale;
+        d.col = src.w.col;
         d.y = src.y;
         d.resid = src.residual;
         d.ldy = src.ldy;
@@ -783,6 +823,10 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
         return fail(TE_EINVAL, "q8_gated_linear: NULL q or scale (NULL scale needs block scales)");
     if ((reinterpret_cast<uintptr_t>(wg->block_scale) & 3) || (reinterpret_cast<uintptr_t>(wu->block_scale) & 3))
         return fail(TE_EALIGN, "q8_gated_linear: block scales must be 4-byte aligned");
+    if ((wg->col && wg->block_scale) || (wu->col && wu->block_scale))
+        return fail(TE_EINVAL, "q8_gated_linear: a column field and block scales together");
+    if ((wg->col && !aligned16(wg->col)) || (wu->col && !aligned16(wu->col)))
+        return fail(TE_EALIGN, "q8_gated_linear: the column field must be 16-byte aligned");
     if (wg->k != k || wu->k != k || wg->n != wu->n)
         return fail(TE_ESHAPE, "q8_gated_linear: wg [%d, %d] and wu [%d, %d] must both be [f, %d]", wg->n,
                     wg->k, wu->n, wu->k, k);
@@ -807,6 +851,8 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     d.bias2 = wu->bias;
     d.bsc = wg->block_scale;
     d.bsc2 = wu->block_scale;
+    d.col = wg->col;
+    d.col2 = wu->col;
     d.y = out;
     d.ldy = ldm;
     d.n = f;

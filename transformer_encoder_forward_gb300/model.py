@@ -48,9 +48,10 @@ class LayerWeights:
                 bs = torch.empty(n, k // 32, dtype=torch.int16, device=device)
                 unpack = q8_0_unpack if w["fmt"] == "q8_0" else q4_0_unpack
                 unpack(_dev(w["packed"], device), n, k, q, bs)
-                self.t[key] = (q, _dev(w.get("s"), device), _dev(w["b"], device), bs)
+                self.t[key] = (q, _dev(w.get("s"), device), _dev(w["b"], device), bs, None)
             else:
-                self.t[key] = (_dev(w["q"], device), _dev(w["s"], device), _dev(w["b"], device), None)
+                self.t[key] = (_dev(w["q"], device), _dev(w["s"], device), _dev(w["b"], device), None,
+                               _dev(w.get("col"), device))
         for key in ("norm1_w", "norm1_b", "norm2_w", "norm2_b", "post_attn_w", "post_ffn_w",
                     "q_norm", "k_norm", "mod"):
             self.t[key] = _dev(p.get(key), device, torch.float32)

@@ -66,7 +66,7 @@ class BlockConfig:
     eps: float = 1e-6
     post: float = 1.0
     adaln: bool = False  # DiT adaLN modulation: per block [s_msa | g_msa | s_mlp | g_mlp]
-    codec: str = "q8_row"  # weight format: "q8_row" | "q8_0" | "q4_0"
+    codec: str = "q8_row"  # weight format: "q8_row" | "q8_2f" | "q8_0" | "q4_0"
 
     def window_of(self, layer: int) -> int:
         if self.window == 0:
@@ -103,6 +103,8 @@ CONFIGS = {
 # outside the block).
 CONFIGS["c4m"] = dataclasses.replace(CONFIGS["c4"], name="c4m_dit_block_adaln_d3840", adaln=True)
 CONFIGS["c5m"] = dataclasses.replace(CONFIGS["c5"], name="c5m_dit_stack30_adaln_d3840", adaln=True)
+# The DiT block with q8_2f weights (zimage.rs: q8_row + a per-column field).
+CONFIGS["c4f"] = dataclasses.replace(CONFIGS["c4"], name="c4f_dit_block_q8_2f_d3840", codec="q8_2f")
 # The ViT stack with the 32-element block weight formats of
 # vision_encoder_gpu.rs (Q8_0, Q4_0) in place of q8_row.
 CONFIGS["c3q8"] = dataclasses.replace(CONFIGS["c3"], name="c3q8_vit_stack16_q8_0_d768", codec="q8_0")
@@ -180,6 +182,11 @@ def draw_layer(cfg: BlockConfig, layer: int, seed: int, jitter: bool = True) -> 
     def w(n, k):
         if cfg.codec == "q8_row":
             return draw_q8(rng, n, k, jitter, cfg.bias)
+        if cfg.codec == "q8_2f":
+            out = draw_q8(rng, n, k, jitter, cfg.bias)
+            # the column field: f16 values (as the file stores them), around 1
+            out["col"] = rng.uniform(0.5, 1.5, k).astype(np.float16).astype(np.float32)
+            return out
         out = draw_block_packed(rng, n, k, cfg.codec)
         out["s"] = None
         out["b"] = (rng.standard_normal(n) * 0.02).astype(np.float32) if cfg.bias else None
