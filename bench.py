@@ -80,7 +80,7 @@ def launches_per_forward(cfg):
     n = 1                                                     # input pre-norm
     for i in range(cfg.layers):
         n += 4                                                # q8 GEMMs: qkv, o, gate|up (+gate), down
-        n += 1 if (cfg.qk_norm or cfg.rope) else 0            # q/k norm + RoPE
+        n += 1 if (cfg.qk_norm or cfg.rope or cfg.v_norm) else 0   # q/k (v) norm + RoPE
         n += 2                                                # attention, FFN pre-norm
         n += 1 if (cfg.form == "sandwich" or i + 1 < cfg.layers) else 0   # closing norm
     return n + (1 if cfg.pool else 0)                         # final norm + pool
@@ -239,11 +239,12 @@ def workload_ops(cfg, st, torch):
             lambda s, win=win: te.attn_varlen_fwd(qkv, ldq, 0, qw, qw + kw, st.cu_host, st.cu_dev, H,
                                                   KV, hd, win, cfg.scale, o, qw, stream=s),
             4 * hd * H * pairs, T * ldq * 2 + T * qw * 2, cnt, "tensor")
-    if cfg.qk_norm or cfg.rope:
-        ops["qk_prep"] = (lambda s: te.qk_prep_rope(
-            qkv, ldq, 0, qw, H, KV, hd, L0.t["q_norm"], L0.t["k_norm"], cfg.eps, st.rope_cos,
-            st.rope_sin, st.rope_pos, st.rope_sec, 1.0, T, stream=s), 0, 2 * T * (qw + kw) * 2, nl,
-            "hbm")
+    if cfg.qk_norm or cfg.rope or cfg.v_norm:
+        vw = kw if cfg.v_norm else 0
+        ops["qk_prep"] = (lambda s: te.qkv_prep_rope(
+            qkv, ldq, 0, qw, qw + kw, H, KV, hd, L0.t["q_norm"], L0.t["k_norm"], cfg.v_norm, cfg.eps,
+            st.rope_cos, st.rope_sin, st.rope_pos, st.rope_sec, 1.0, T, stream=s), 0,
+            2 * T * (qw + kw + vw) * 2, nl, "hbm")
     if cfg.adaln:   # with the gate on the branch and the scale on the next norm
         md = L0.t["mod"]
         ops["add_norm"] = (lambda s: te.add_norm_mod(x, tmp, L0.t["post_attn_w"], md[1], 1.0, L0.t["norm2_w"],
@@ -504,7 +505,7 @@ def cpu_sample(key):
     cfg = synth.CONFIGS[key]
     lens = synth.draw_lens(cfg)
     seed = synth.config_seed(key)
-    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1, "c3q8": 1, "c3q4": 1, "c4f": 1}[key]
+    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1, "c3q8": 1, "c3q4": 1, "c4f": 1, "c2v": 6}[key]
     sl = lens[:take]
     if key in ("c4", "c5", "c4m", "c5m", "c4f"):
         sl = np.asarray([min(int(sl[0]), 1056)], dtype=np.int32)

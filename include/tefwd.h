@@ -172,6 +172,23 @@ te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t
                              int32_t window, float scale, void *out, int64_t ldo,
                              te_stream stream);
 
+/* attn_items_fwd: the same attention over two-range items ([ZI] PFa
+ * {img_off, n_img, cap_off, n_cap}: the CFG program's image rows and caption
+ * rows of one item attend as one sequence).  Item i is int32
+ * [off1, len1, off2, len2]: its joint positions 0..len1-1 are the rows
+ * off1.., positions len1..len1+len2-1 the rows off2..; the window applies to
+ * joint positions; each query's output goes to its own row.
+ * items_host / items_dev: the same int32 [nitems, 4] on the host (validated)
+ * and on the device (16-byte aligned).  len1 >= 1, len2 >= 0, and when
+ * len2 > 0, len1 % 32 == 0 (a key tile spanning both ranges is loaded in
+ * 32-row pieces); every range inside rows [0, rows).  Otherwise as
+ * te_attn_varlen_fwd (len2 = 0 for every item gives the same result). */
+te_status te_attn_items_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off,
+                            int32_t v_off, const int32_t *items_host, const int32_t *items_dev,
+                            int32_t nitems, int32_t rows, int32_t nq_heads, int32_t nkv_heads,
+                            int32_t hd, int32_t window, float scale, void *out, int64_t ldo,
+                            te_stream stream);
+
 /* rownorm: y = Norm(pre * x) per row.
  *   RMS: v / sqrt(mean(v^2) + eps) * w            ([EG2] Prog::rms)
  *   LN : (v - mean) / sqrt(var + eps) * w + b      ([VIT] VitGpuOps::layernorm;
@@ -228,6 +245,16 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
                           int32_t table_rows, int32_t sec, float q_mul, int32_t rows,
                           te_stream stream);
 
+/* qkv_prep_rope: qk_prep_rope, and with v_norm != 0 also the v heads (at
+ * v_off + g*hd) RMS-normalised without a weight and without RoPE:
+ * v = v / sqrt(mean(v^2) + eps) ([EG2] Prog::qkv "q/k norm + RoPE, v norm":
+ * one pass over the nq + 2 nkv heads, weights for q and k only). */
+te_status te_qkv_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t v_off,
+                           int32_t nq, int32_t nkv, int32_t hd, const float *qn, const float *kn,
+                           int32_t v_norm, float eps, const float *cos, const float *sin,
+                           const int32_t *pos, int32_t table_rows, int32_t sec, float q_mul,
+                           int32_t rows, te_stream stream);
+
 /* gate_act: m = act(g) * u with g = gu[:, 0:f], u = gu[:, u_off:u_off+f];
  * u_off < 0: ungated, m = act(g).  act: GELU-tanh
  * 0.5 g (1 + tanh(sqrt(2/pi)(g + 0.044715 g^3))) or SiLU g / (1 + e^-g).
@@ -267,6 +294,7 @@ typedef struct {
      * scales this block's input a, which the caller's previous norm made);
      * next_mod_scale = the next block's s_msa, f32 [d], applied to a_out. */
     const float *mod, *next_mod_scale;
+    int32_t v_norm;      /* 1: RMS-normalise the v heads too (te_qkv_prep_rope) */
 } te_block_desc;
 
 /* Workspace bytes te_encoder_block_fwd needs for t packed rows. */

@@ -246,10 +246,14 @@ def rope(x, cos, sin, sec):
     return out
 
 
-def qk_prep(qkv, nq, nkv, hd, q_off, k_off, qn, kn, eps, cos, sin, pos, sec, q_mul):
+def qk_prep(qkv, nq, nkv, hd, q_off, k_off, qn, kn, eps, cos, sin, pos, sec, q_mul,
+            v_off=None):
     """q/k RMSNorm per head with [hd] weights, then RoPE, then q * q_mul;
     the panel is returned rounded to bf16 (egemma2.rs ``Prog::qkv``;
     zimage.rs ``Enc::block`` "qk-norm + RoPE in place", q pre-multiplied).
+    With ``v_off`` the v heads are RMS-normalised too, without a weight and
+    without RoPE (egemma2.rs ``Prog::qkv`` "v norm": the pass covers the
+    nq + 2 nkv heads and takes weights for q and k only).
 
     ``pos`` selects each row's table row (None = the row index).
     """
@@ -268,6 +272,10 @@ def qk_prep(qkv, nq, nkv, hd, q_off, k_off, qn, kn, eps, cos, sin, pos, sec, q_m
             if sec:
                 v = rope(v, c_rows, s_rows, sec)
             out[:, sl] = v * mul
+    if v_off is not None:
+        for h in range(nkv):
+            sl = slice(v_off + h * hd, v_off + (h + 1) * hd)
+            out[:, sl] = rms_norm(out[:, sl], np.ones(hd), eps)
     return round_bf16(out)
 
 
@@ -329,6 +337,21 @@ def attention_varlen(qkv, cu, nq, nkv, hd, q_off, k_off, v_off, window, scale,
             V = qkv[r0:r1, v_off + kvh * hd: v_off + (kvh + 1) * hd]
             P = softmax_probs(Q, K, scale, vis[qi])
             out[r0 + qi, h * hd:(h + 1) * hd] = P @ V
+    return out
+
+
+def attention_items(qkv, items, nq, nkv, hd, q_off, k_off, v_off, window, scale):
+    """Attention over two-range items (zimage.rs ``PFa``: an item's image rows
+    [off1, off1+len1) and caption rows [off2, off2+len2) attend as one
+    sequence in that joint order; the window counts joint positions).  Each
+    item's rows are gathered into one sequence, attended as such, and the
+    outputs scattered back to their own rows; rows in no item stay NaN."""
+    qkv = np.asarray(qkv, dtype=np.float64)
+    out = np.full((qkv.shape[0], nq * hd), np.nan)
+    for off1, len1, off2, len2 in np.asarray(items, dtype=np.int64).reshape(-1, 4):
+        rows = np.r_[np.arange(off1, off1 + len1), np.arange(off2, off2 + len2)].astype(np.int64)
+        o = attention_varlen(qkv[rows], [0, len(rows)], nq, nkv, hd, q_off, k_off, v_off, window, scale)
+        out[rows] = o
     return out
 
 
@@ -423,11 +446,13 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mo
         linear(a, p["wv"]),
     ], axis=1)
     r["qkv_raw"] = qkv = round_bf16(qkv)
-    if cfg.qk_norm or tables["sec"]:
+    v_norm = getattr(cfg, "v_norm", False)
+    if cfg.qk_norm or tables["sec"] or v_norm:
         qkv = qk_prep(qkv, H, KV, hd, 0, qw,
                       p["q_norm"] if cfg.qk_norm else None,
                       p["k_norm"] if cfg.qk_norm else None,
-                      eps, tables["cos"], tables["sin"], tables["pos"], tables["sec"], 1.0)
+                      eps, tables["cos"], tables["sin"], tables["pos"], tables["sec"], 1.0,
+                      v_off=qw + kw if v_norm else None)
     r["qkv"] = qkv
     o = attention_varlen(qkv, cu, H, KV, hd, 0, qw, qw + kw, cfg.window_of(layer),
                          cfg.scale, rows=rows)

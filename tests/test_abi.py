@@ -151,6 +151,22 @@ def test_block_formats_reject_bad_arguments(L):
     assert _call(L, "te_q8_0_unpack", None, 4, 64, FAKE, FAKE, None)[0] == te.TE_EINVAL
 
 
+def test_attention_items_reject_bad_arguments(L):
+    import numpy as np
+    def items(*rows):
+        arr = np.asarray(rows, np.int32).reshape(-1, 4)
+        return arr, arr.ctypes.data_as(ctypes.c_void_p)
+    a, p = items([0, 33, 40, 10])                     # first range not a multiple of 32
+    assert _call(L, "te_attn_items_fwd", FAKE, 384, 0, 128, 256, p, FAKE, 1, 100, 2, 2, 64, 0, 0.125,
+                 FAKE * 2, 128, None)[0] == te.TE_ESHAPE
+    a, p = items([0, 32, 90, 20])                     # second range past the rows
+    assert _call(L, "te_attn_items_fwd", FAKE, 384, 0, 128, 256, p, FAKE, 1, 100, 2, 2, 64, 0, 0.125,
+                 FAKE * 2, 128, None)[0] == te.TE_EINVAL
+    a, p = items([0, 32, 40, 20])                     # items on the device must be 16-byte aligned
+    assert _call(L, "te_attn_items_fwd", FAKE, 384, 0, 128, 256, p, FAKE + 4, 1, 100, 2, 2, 64, 0,
+                 0.125, FAKE * 2, 128, None)[0] == te.TE_EALIGN
+
+
 def test_adaln_row_ops_reject_bad_arguments(L):
     # scale without a next norm, gate without a branch, misaligned vectors
     assert _call(L, "te_add_norm_mod", FAKE, FAKE, FAKE, None, 1.0, None, None, FAKE, te.TE_NORM_RMS,

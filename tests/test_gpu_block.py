@@ -75,6 +75,8 @@ FORMS = {
     # the ViT block with the 32-element block weight formats
     "c3q8_small": ("c3q8", dict(layers=2), (200, 129)),
     "c3q4_small": ("c3q4", dict(layers=2), (200, 129)),
+    # the text block with the v heads normalised too
+    "c2v_small": ("c2v", dict(layers=2, window=40), (100, 1, 300, 37)),
     # the DiT block with q8_2f weights (column field)
     "c4f_small": ("c4f", dict(layers=2, d=512, heads=4, kv_heads=4, ffn=1024), (150, 133)),
 }

@@ -350,6 +350,28 @@ def test_adaln_identity_vectors_are_bit_exact_no_ops():
 
 
 @pytest.mark.parametrize("hd,nq,nkv,rope,qk", [(64, 8, 8, "1d", True), (128, 4, 4, "2d", True),
+                                               (64, 4, 2, None, False), (128, 30, 30, "2d", True)])
+def test_qkv_prep_with_v_norm_matches_oracle(hd, nq, nkv, rope, qk):
+    torch = _torch()
+    rng = np.random.default_rng([hd, nq, nkv, 5])
+    lens = [37, 64, 100]
+    cfg = synth.small_config("c2", hd=hd, rope=rope)
+    tb = synth.rope_tables(cfg, lens)
+    T = sum(lens)
+    W = (nq + 2 * nkv) * hd
+    x, x64 = bf16_input(rng, (T, W), 2.0)
+    qn = (1 + 0.1 * rng.standard_normal(hd)).astype(np.float32) if qk else None
+    kn = (1 + 0.1 * rng.standard_normal(hd)).astype(np.float32) if qk else None
+    dv = lambda a, dt=None: to_dev(a, dt) if a is not None else None
+    te.qkv_prep_rope(x, W, 0, nq * hd, (nq + nkv) * hd, nq, nkv, hd, dv(qn), dv(kn), True, 1e-6,
+                     dv(tb["cos"]), dv(tb["sin"]), dv(tb["pos"], torch.int32), tb["sec"], 0.5, T)
+    te.check()
+    ref = O.qk_prep(x64, nq, nkv, hd, 0, nq * hd, qn, kn, 1e-6, tb["cos"], tb["sin"], tb["pos"],
+                    tb["sec"], 0.5, v_off=(nq + nkv) * hd)
+    assert rel_frob(to_np(x), ref) < 2e-3
+
+
+@pytest.mark.parametrize("hd,nq,nkv,rope,qk", [(64, 8, 8, "1d", True), (128, 4, 4, "2d", True),
                                                (64, 4, 2, "2d", False), (128, 2, 1, None, True)])
 def test_qk_prep_rope_matches_oracle(hd, nq, nkv, rope, qk):
     torch = _torch()
@@ -520,3 +542,66 @@ def test_q8_2f_gemm_matches_oracle(m, k, ns, ydt):
         got = to_np(y)
         assert np.all(np.isfinite(got))
         assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
+
+
+# ------------------------------------------------------- two-range items
+
+def _items_case(rng, hd, nq, nkv, n_img, n_cap, nitems=2):
+    """A CFG-like packing [img0 | img1 | cap0 | cap1]: item i = (img_i, cap_i)."""
+    W = (nq + 2 * nkv) * hd
+    T = nitems * (n_img + n_cap)
+    items = [[i * n_img, n_img, nitems * n_img + i * n_cap, n_cap] for i in range(nitems)]
+    x, x64 = bf16_input(rng, (T, W))
+    return np.asarray(items, np.int32), x, x64, T, W
+
+
+@pytest.mark.parametrize("hd,nq,nkv,n_img,n_cap,window", [
+    (128, 4, 4, 96, 70, 0),      # query / key tiles spanning the two ranges
+    (128, 2, 1, 256, 33, 0),
+    (64, 4, 2, 160, 200, 0),
+    (64, 2, 2, 224, 61, 50),     # windowed over joint positions
+])
+def test_attention_two_range_items_match_oracle(hd, nq, nkv, n_img, n_cap, window):
+    torch = _torch()
+    rng = np.random.default_rng([hd, n_img, n_cap])
+    items, x, x64, T, W = _items_case(rng, hd, nq, nkv, n_img, n_cap)
+    out = torch.full((T, nq * hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    scale = hd ** -0.5
+    te.attn_items_fwd(x, W, 0, nq * hd, (nq + nkv) * hd, items, to_dev(items), T, nq, nkv, hd, window,
+                      scale, out, nq * hd)
+    te.check()
+    ref = O.attention_items(x64, items, nq, nkv, hd, 0, nq * hd, (nq + nkv) * hd, window, scale)
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    assert rel_frob(got, ref) < 3e-3, rel_frob(got, ref)
+
+
+def test_attention_items_equal_varlen_on_gathered_rows_bit_exactly():
+    torch = _torch()
+    rng = np.random.default_rng(43)
+    hd, nq, nkv = 128, 2, 2
+    items, x, x64, T, W = _items_case(rng, hd, nq, nkv, 128 + 32, 77, nitems=2)
+    out = torch.empty(T, nq * hd, dtype=torch.bfloat16, device="cuda")
+    te.attn_items_fwd(x, W, 0, nq * hd, (nq + nkv) * hd, items, to_dev(items), T, nq, nkv, hd, 0,
+                      hd ** -0.5, out, nq * hd)
+    # the same rows gathered in joint order, as two packed sequences
+    rows = np.concatenate([np.r_[o1:o1 + l1, o2:o2 + l2] for o1, l1, o2, l2 in items])
+    xg = x[torch.from_numpy(rows).cuda()].contiguous()
+    lens = [int(l1 + l2) for _, l1, _, l2 in items]
+    cu = synth.cu_seqlens(lens)
+    og = torch.empty_like(out)
+    te.attn_varlen_fwd(xg, W, 0, nq * hd, (nq + nkv) * hd, cu, torch.from_numpy(cu).cuda(), nq, nkv,
+                       hd, 0, hd ** -0.5, og, nq * hd)
+    te.check()
+    assert torch.equal(out[torch.from_numpy(rows).cuda()], og)
+    # single-range items are the packed sequences themselves
+    it1 = np.asarray([[0, 100, 0, 0], [100, 37, 0, 0]], np.int32)
+    o1 = torch.empty(137, nq * hd, dtype=torch.bfloat16, device="cuda")
+    o2 = torch.empty_like(o1)
+    te.attn_items_fwd(x, W, 0, nq * hd, (nq + nkv) * hd, it1, to_dev(it1), T, nq, nkv, hd, 0,
+                      hd ** -0.5, o1, nq * hd)
+    cu2 = synth.cu_seqlens([100, 37])
+    te.attn_varlen_fwd(x[:137], W, 0, nq * hd, (nq + nkv) * hd, cu2, torch.from_numpy(cu2).cuda(), nq,
+                       nkv, hd, 0, hd ** -0.5, o2, nq * hd)
+    te.check()
+    assert torch.equal(o1, o2)

@@ -705,3 +705,52 @@ def test_q8_2f_matches_brute_force():
         for o in range(4):
             acc = sum(x[t, j] * float(O.round_bf16(float(q[o, j]) * col[j])) for j in range(64))
             assert abs(y[t, o] - (s[o] * acc + b[o])) <= 1e-12 * (1 + abs(y[t, o]))
+
+
+# ------------------------------------------------------------------ v norm
+# egemma2.rs Prog::qkv normalises q, k and v heads in one pass with weights
+# for q and k only: v is RMS-normalised without a weight, without RoPE.
+
+def test_v_norm_gives_unit_rms_v_heads_and_leaves_q_k_alone():
+    rng = np.random.default_rng(31)
+    nq, nkv, hd = 4, 2, 64
+    qkv = O.round_bf16(rng.standard_normal((9, (nq + 2 * nkv) * hd)) * 3)
+    qn, kn = 1 + 0.1 * rng.standard_normal(hd), 1 + 0.1 * rng.standard_normal(hd)
+    base = O.qk_prep(qkv, nq, nkv, hd, 0, nq * hd, qn, kn, 1e-6, None, None, None, 0, 1.0)
+    vn = O.qk_prep(qkv, nq, nkv, hd, 0, nq * hd, qn, kn, 1e-6, None, None, None, 0, 1.0,
+                   v_off=(nq + nkv) * hd)
+    qk = slice(0, (nq + nkv) * hd)
+    np.testing.assert_array_equal(vn[:, qk], base[:, qk])
+    v = vn[:, (nq + nkv) * hd:].reshape(9, nkv, hd)
+    rms = np.sqrt(np.mean(v ** 2, axis=2))
+    np.testing.assert_allclose(rms, 1.0, atol=4e-3)           # bf16-rounded unit rows
+    # a constant head c maps to c / sqrt(c^2 + eps) (times the unit weight)
+    const = np.zeros((1, (nq + 2 * nkv) * hd))
+    const[0, (nq + nkv) * hd:] = 0.25
+    out = O.qk_prep(const, nq, nkv, hd, 0, nq * hd, None, None, 1e-6, None, None, None, 0, 1.0,
+                    v_off=(nq + nkv) * hd)
+    np.testing.assert_allclose(out[0, (nq + nkv) * hd:], O.round_bf16(0.25 / np.sqrt(0.0625 + 1e-6)))
+
+
+# -------------------------------------------------------- two-range items
+# zimage.rs PFa {img_off, n_img, cap_off, n_cap}: image and caption rows of
+# one item attend as one sequence.
+
+def test_two_range_items_reduce_to_varlen_and_ignore_range_order_without_window():
+    rng = np.random.default_rng(41)
+    nq, nkv, hd = 2, 1, 64
+    qkv = rng.standard_normal((70, (nq + 2 * nkv) * hd))
+    scale = hd ** -0.5
+    args = (nq, nkv, hd, 0, nq * hd, (nq + nkv) * hd)
+    # len2 = 0: exactly the packed-sequence attention
+    one = O.attention_items(qkv, [[0, 30, 0, 0], [30, 40, 0, 0]], *args, 0, scale)
+    np.testing.assert_array_equal(one, O.attention_varlen(qkv, [0, 30, 70], *args, 0, scale))
+    # an item = its rows attended as one sequence, wherever they lie
+    it = O.attention_items(qkv, [[40, 30, 0, 12]], *args, 0, scale)
+    rows = np.r_[40:70, 0:12]
+    ref = O.attention_varlen(qkv[rows], [0, 42], *args, 0, scale)
+    np.testing.assert_allclose(it[rows], ref, rtol=0, atol=0)
+    assert np.all(np.isnan(it[12:40]))
+    # full attention: swapping the two ranges changes nothing per row
+    sw = O.attention_items(qkv, [[0, 12, 40, 30]], *args, 0, scale)
+    np.testing.assert_allclose(sw[rows], it[rows], rtol=1e-12, atol=1e-12)

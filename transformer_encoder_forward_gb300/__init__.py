@@ -55,7 +55,7 @@ class te_block_desc(ctypes.Structure):
                 ("post_ffn_w", c_p), ("next_norm_w", c_p), ("next_norm_b", c_p),
                 ("q_norm", c_p), ("k_norm", c_p), ("rope_cos", c_p), ("rope_sin", c_p),
                 ("rope_pos", c_p), ("rope_sec", c_i32), ("rope_rows", c_i32),
-                ("mod", c_p), ("next_mod_scale", c_p)]
+                ("mod", c_p), ("next_mod_scale", c_p), ("v_norm", c_i32)]
 
 
 _lib = None
@@ -66,6 +66,8 @@ EXPORTS = {
                                           ctypes.POINTER(te_q8w), c_i32, c_p, c_i64, c_p]),
     "te_attn_varlen_fwd": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_i32, c_p, c_p, c_i32, c_i32,
                                           c_i32, c_i32, c_i32, c_f32, c_p, c_i64, c_p]),
+    "te_attn_items_fwd": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_i32, c_p, c_p, c_i32, c_i32,
+                                         c_i32, c_i32, c_i32, c_i32, c_f32, c_p, c_i64, c_p]),
     "te_rownorm": (ctypes.c_int, [c_p, c_i32, c_i64, c_p, c_p, c_i32, c_f32, c_f32, c_p, c_i32,
                                   c_i64, c_i32, c_i32, c_p]),
     "te_add_norm": (ctypes.c_int, [c_p, c_p, c_p, c_f32, c_p, c_p, c_i32, c_f32, c_p, c_i32, c_i32,
@@ -78,6 +80,9 @@ EXPORTS = {
                                        c_i32, c_i32, c_i32, c_p]),
     "te_qk_prep_rope": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32, c_p, c_p,
                                        c_f32, c_p, c_p, c_p, c_i32, c_i32, c_f32, c_i32, c_p]),
+    "te_qkv_prep_rope": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_p,
+                                        c_p, c_i32, c_f32, c_p, c_p, c_p, c_i32, c_i32, c_f32, c_i32,
+                                        c_p]),
     "te_gate_act": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_i64, c_i32, c_i32, c_p]),
     "te_pool_mean": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_i32, c_p, c_f32, c_p, c_p]),
     "te_encoder_block_workspace": (ctypes.c_size_t, [ctypes.POINTER(te_block_desc), c_i32]),
@@ -188,6 +193,17 @@ def attn_varlen_fwd(qkv, ld, q_off, k_off, v_off, cu_host, cu_dev, nq, nkv, hd, 
                                  _stream(stream)))
 
 
+def attn_items_fwd(qkv, ld, q_off, k_off, v_off, items_host, items_dev, rows, nq, nkv, hd, window,
+                   scale, out, ldo, stream=None):
+    """Attention over two-range items: items int32 [n, 4] = off1, len1, off2, len2
+    (host numpy array and the same on the device)."""
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(items_host, dtype=np.int32).reshape(-1, 4))
+    _ok(lib().te_attn_items_fwd(qkv.data_ptr(), ld, q_off, k_off, v_off, arr.ctypes.data_as(c_p),
+                                items_dev.data_ptr(), arr.shape[0], rows, nq, nkv, hd, window, scale,
+                                out.data_ptr(), ldo, _stream(stream)))
+
+
 def _dt(t) -> int:
     import torch
     return TE_F32 if t.dtype == torch.float32 else TE_BF16
@@ -218,6 +234,15 @@ def add_norm_mod(h, t, w_post, gate, post, w_next, b_next, mod_scale, kind, eps,
                               _ptr(b_next), _ptr(mod_scale), kind, eps, _ptr(a),
                               _dt(a) if a is not None else TE_BF16, h.shape[0], h.shape[1],
                               _stream(stream)))
+
+
+def qkv_prep_rope(qkv, ld, q_off, k_off, v_off, nq, nkv, hd, qn, kn, v_norm, eps, cos, sin, pos,
+                  sec, q_mul, rows, stream=None):
+    """qk_prep_rope plus (v_norm) the unweighted RMS norm of the v heads."""
+    table_rows = cos.shape[0] if cos is not None else 0
+    _ok(lib().te_qkv_prep_rope(qkv.data_ptr(), ld, q_off, k_off, v_off, nq, nkv, hd, _ptr(qn),
+                               _ptr(kn), 1 if v_norm else 0, eps, _ptr(cos), _ptr(sin), _ptr(pos),
+                               table_rows, sec, q_mul, rows, _stream(stream)))
 
 
 def qk_prep_rope(qkv, ld, q_off, k_off, nq, nkv, hd, qn, kn, eps, cos, sin, pos, sec, q_mul,

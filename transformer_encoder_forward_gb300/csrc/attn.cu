@@ -53,8 +53,10 @@ __device__ int g_attn_err;
 
 struct AttnParams {
     CUtensorMap map;           // the bf16 q|k|v panel [T, ld], box 64 x 128
+    CUtensorMap map32;         // the same panel, box 64 x 32 (tiles across two row ranges)
     __nv_bfloat16 *out;
     const int *cu;
+    const int *items;          // two-range items [n][off1, len1, off2, len2], or NULL (cu)
     long long ldo;
     int q_off, k_off, v_off, group, window;
     float scale_log2;
@@ -162,8 +164,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     using L = ALayout<HD>;
     extern __shared__ uint8_t smem_raw[];
     const int seq = blockIdx.z;
-    const int r0 = p.cu[seq];
-    const int len = p.cu[seq + 1] - r0;
+    // the attention unit: one packed sequence (cu), or a two-range item whose
+    // joint positions 0..len1-1 are rows off1.. and len1.. are rows off2..
+    int off1, len1, off2 = 0, len2 = 0;
+    if (p.items) {
+        const int4 it = reinterpret_cast<const int4 *>(p.items)[seq];
+        off1 = it.x; len1 = it.y; off2 = it.z; len2 = it.w;
+    } else {
+        off1 = p.cu[seq];
+        len1 = p.cu[seq + 1] - off1;
+    }
+    const int len = len1 + len2;
+    auto row_of = [&](int j) { return j < len1 ? off1 + j : off2 + (j - len1); };
     const int q0 = blockIdx.x * 2 * BQ;
     if (q0 >= len) return;
     if (*reinterpret_cast<volatile int *>(&g_attn_err) != 0) return;
@@ -222,24 +234,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&p.map);
+            // 128 joint positions from j0 at column col: one box, or four
+            // 32-row boxes when the tile spans the two ranges (len1 % 32 == 0)
+            auto load_tile = [&](uint32_t dst, int col, int j0, uint32_t bar) {
+                if (len2 == 0 || j0 + BQ <= len1 || j0 >= len1) {
+                    tma_load_2d(dst, &p.map, bar, col, row_of(j0));
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        tma_load_2d(dst + r * 32 * 128, &p.map32, bar, col, row_of(j0 + 32 * r));
+                }
+            };
             mbar_arrive_expect_tx(bar_q, ntile * L::TILE);
             for (int w = 0; w < ntile; ++w)
                 for (int c = 0; c < L::NB; ++c)
-                    tma_load_2d(sb + L::Q_OFF + w * L::TILE + c * 16384, &p.map, bar_q,
-                                p.q_off + h * HD + 64 * c, r0 + q0 + w * BQ);
+                    load_tile(sb + L::Q_OFF + w * L::TILE + c * 16384, p.q_off + h * HD + 64 * c,
+                              q0 + w * BQ, bar_q);
             int j = 0;
             for (; j < n; ++j) {
                 const int st = j & 1;
                 if (!mbar_wait(bar_kve + 8 * st, ((j >> 1) & 1) ^ 1)) { ok = false; break; }
-                const int row = r0 + (kt0 + j) * BKV;
+                const int jk = (kt0 + j) * BKV;
                 mbar_arrive_expect_tx(bar_kf + 8 * st, L::TILE);
                 for (int c = 0; c < L::NB; ++c)
-                    tma_load_2d(sb + L::K_OFF + st * L::TILE + c * 16384, &p.map, bar_kf + 8 * st,
-                                p.k_off + g * HD + 64 * c, row);
+                    load_tile(sb + L::K_OFF + st * L::TILE + c * 16384, p.k_off + g * HD + 64 * c, jk,
+                              bar_kf + 8 * st);
                 mbar_arrive_expect_tx(bar_vf + 8 * st, L::TILE);
                 for (int c = 0; c < L::NB; ++c)
-                    tma_load_2d(sb + L::V_OFF + st * L::TILE + c * 16384, &p.map, bar_vf + 8 * st,
-                                p.v_off + g * HD + 64 * c, row);
+                    load_tile(sb + L::V_OFF + st * L::TILE + c * 16384, p.v_off + g * HD + 64 * c, jk,
+                              bar_vf + 8 * st);
             }
             // no copy of ours may still be landing when the CTA exits
             mbar_wait(bar_q, 0, 20000000ull);
@@ -364,7 +387,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *orow = p.out + (long long)(r0 + qi) * p.ldo + h * HD;
+            __nv_bfloat16 *orow = p.out + (long long)(qi < len ? row_of(qi) : 0) * p.ldo + h * HD;
 #pragma unroll
             for (int cc = 0; cc < HD / 32; ++cc) {
                 uint32_t v[32];
@@ -426,16 +449,14 @@ int read_clear_attn_error() {
 
 using namespace tefwd;
 
-extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off,
-                                        int32_t v_off, const int32_t *cu_host,
-                                        const int32_t *cu_dev, int32_t nseq, int32_t nq_heads,
-                                        int32_t nkv_heads, int32_t hd, int32_t window, float scale,
-                                        void *out, int64_t ldo, te_stream stream) {
+static te_status attn_common_checks(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t v_off,
+                                    int32_t nq_heads, int32_t nkv_heads, int32_t hd, int32_t window,
+                                    const void *out, int64_t ldo) {
     if (!qkv || !out) return fail(TE_EINVAL, "attn: NULL qkv or out");
     if (hd != 64 && hd != 128) return fail(TE_ESHAPE, "attn: hd=%d (64 or 128)", hd);
     if (nq_heads < 1 || nkv_heads < 1 || nq_heads % nkv_heads)
         return fail(TE_ESHAPE, "attn: nq_heads=%d nkv_heads=%d (nq %% nkv == 0)", nq_heads, nkv_heads);
-    if (nq_heads > 65535 || nseq > 65535) return fail(TE_ESHAPE, "attn: too many heads or sequences");
+    if (nq_heads > 65535) return fail(TE_ESHAPE, "attn: too many heads");
     if (window < 0) return fail(TE_EINVAL, "attn: window=%d (>= 0)", window);
     if (q_off < 0 || k_off < 0 || v_off < 0 || (int64_t)q_off + (int64_t)nq_heads * hd > ld ||
         (int64_t)k_off + (int64_t)nkv_heads * hd > ld || (int64_t)v_off + (int64_t)nkv_heads * hd > ld)
@@ -444,9 +465,13 @@ extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_o
     if (!aligned16(qkv) || !aligned16(out) || (ld * 2) % 16 || (ldo * 2) % 16 || q_off % 8 ||
         k_off % 8 || v_off % 8)
         return fail(TE_EALIGN, "attn: rows and head offsets must be 16-byte aligned");
-    int32_t total = 0, max_len = 0;
-    te_status st = check_cu(cu_host, cu_dev, nseq, &total, &max_len);
-    if (st != TE_OK) return st;
+    return TE_OK;
+}
+
+static te_status attn_launch(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t v_off,
+                             const int32_t *cu_dev, const int32_t *items_dev, int32_t units, int32_t total,
+                             int32_t max_len, int32_t nq_heads, int32_t nkv_heads, int32_t hd,
+                             int32_t window, float scale, void *out, int64_t ldo, te_stream stream) {
     {
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(qkv);
         const uintptr_t a1 = a0 + (uintptr_t)total * ld * 2;
@@ -456,11 +481,15 @@ extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_o
     }
     AttnParams p;
     memset(&p, 0, sizeof(p));
-    st = make_map_2d(&p.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)ld, (uint64_t)total,
-                     (uint64_t)ld * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    te_status st = make_map_2d(&p.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)ld, (uint64_t)total,
+                               (uint64_t)ld * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != TE_OK) return st;
+    st = make_map_2d(&p.map32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)ld, (uint64_t)total,
+                     (uint64_t)ld * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_OK) return st;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.cu = cu_dev;
+    p.items = items_dev;
     p.ldo = ldo;
     p.q_off = q_off;
     p.k_off = k_off;
@@ -469,6 +498,47 @@ extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_o
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return hd == 64 ? launch<64>(p, max_len, nq_heads, nseq, s)
-                    : launch<128>(p, max_len, nq_heads, nseq, s);
+    return hd == 64 ? launch<64>(p, max_len, nq_heads, units, s)
+                    : launch<128>(p, max_len, nq_heads, units, s);
+}
+
+extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off,
+                                        int32_t v_off, const int32_t *cu_host,
+                                        const int32_t *cu_dev, int32_t nseq, int32_t nq_heads,
+                                        int32_t nkv_heads, int32_t hd, int32_t window, float scale,
+                                        void *out, int64_t ldo, te_stream stream) {
+    te_status st = attn_common_checks(qkv, ld, q_off, k_off, v_off, nq_heads, nkv_heads, hd, window, out, ldo);
+    if (st != TE_OK) return st;
+    if (nseq > 65535) return fail(TE_ESHAPE, "attn: too many sequences");
+    int32_t total = 0, max_len = 0;
+    if ((st = check_cu(cu_host, cu_dev, nseq, &total, &max_len)) != TE_OK) return st;
+    return attn_launch(qkv, ld, q_off, k_off, v_off, cu_dev, nullptr, nseq, total, max_len, nq_heads,
+                       nkv_heads, hd, window, scale, out, ldo, stream);
+}
+
+extern "C" te_status te_attn_items_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off,
+                                       int32_t v_off, const int32_t *items_host, const int32_t *items_dev,
+                                       int32_t nitems, int32_t rows, int32_t nq_heads, int32_t nkv_heads,
+                                       int32_t hd, int32_t window, float scale, void *out, int64_t ldo,
+                                       te_stream stream) {
+    te_status st = attn_common_checks(qkv, ld, q_off, k_off, v_off, nq_heads, nkv_heads, hd, window, out, ldo);
+    if (st != TE_OK) return st;
+    if (!items_host || !items_dev) return fail(TE_EINVAL, "attn_items: NULL items");
+    if (nitems < 1 || nitems > 65535) return fail(TE_ESHAPE, "attn_items: nitems=%d (1..65535)", nitems);
+    if (rows < 1) return fail(TE_ESHAPE, "attn_items: rows=%d", rows);
+    if (reinterpret_cast<uintptr_t>(items_dev) & 15) return fail(TE_EALIGN, "attn_items: items must be 16-byte aligned");
+    int32_t max_len = 0;
+    for (int32_t i = 0; i < nitems; ++i) {
+        const int32_t o1 = items_host[4 * i], l1 = items_host[4 * i + 1];
+        const int32_t o2 = items_host[4 * i + 2], l2 = items_host[4 * i + 3];
+        if (o1 < 0 || l1 < 1 || o2 < 0 || l2 < 0 || (int64_t)o1 + l1 > rows || (int64_t)o2 + l2 > rows)
+            return fail(TE_EINVAL, "attn_items: item %d (%d, %d, %d, %d) runs outside the %d rows", i, o1, l1,
+                        o2, l2, rows);
+        if (l2 > 0 && l1 % 32)
+            return fail(TE_ESHAPE, "attn_items: item %d: the first range's length %d is not a multiple of 32", i, l1);
+        if ((int64_t)l1 + l2 > (1 << 30)) return fail(TE_ESHAPE, "attn_items: item %d too long", i);
+        if (l1 + l2 > max_len) max_len = l1 + l2;
+    }
+    return attn_launch(qkv, ld, q_off, k_off, v_off, nullptr, items_dev, nitems, rows, max_len, nq_heads,
+                       nkv_heads, hd, window, scale, out, ldo, stream);
 }

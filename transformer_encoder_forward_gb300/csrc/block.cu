@@ -137,11 +137,11 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
     it[1] = {d.wk, qkv + qw, ldqkv, TE_BF16, 0, nullptr, 0};
     it[2] = {d.wv, qkv + qw + kw, ldqkv, TE_BF16, 0, nullptr, 0};
     if ((st = te_q8_linear(a, D, t, D, it, 3, stream)) != TE_OK) return st;
-    // 2. q/k norm + RoPE in place
-    if (d.q_norm || d.rope_sec || d.q_mul != 1.f) {
-        if ((st = te_qk_prep_rope(qkv, ldqkv, 0, qw, H, KV, hd, d.q_norm, d.k_norm, d.eps, d.rope_cos,
-                                  d.rope_sin, d.rope_pos, d.rope_rows,
-                                  d.rope_sec, d.q_mul, t, stream)) != TE_OK)
+    // 2. q/k norm + RoPE (and v norm) in place
+    if (d.q_norm || d.rope_sec || d.q_mul != 1.f || d.v_norm) {
+        if ((st = te_qkv_prep_rope(qkv, ldqkv, 0, qw, qw + kw, H, KV, hd, d.q_norm, d.k_norm,
+                                   d.v_norm ? 1 : 0, d.eps, d.rope_cos, d.rope_sin, d.rope_pos,
+                                   d.rope_rows, d.rope_sec, d.q_mul, t, stream)) != TE_OK)
             return st;
     }
     // 3. attention

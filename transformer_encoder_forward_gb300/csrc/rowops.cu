@@ -362,7 +362,7 @@ constexpr int QK_U = 4;
 
 template <int HD>
 __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long long ld, int q_off,
-                                                      int k_off, int nq, int nkv,
+                                                      int k_off, int v_off, int nq, int nkv, int nv,
                                                       const float *__restrict__ qn,
                                                       const float *__restrict__ kn, float eps,
                                                       const float *__restrict__ cosb,
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
     if (row >= rows) return;
     const int hl = lane / LPH;                  // head slot of this lane in a load slot
     const int c0 = (lane % LPH) * 8;            // first channel of this lane within its head
-    const int nh = nq + nkv;
+    const int nh = nq + nkv + nv;               // q heads, k heads, then (v-norm) v heads
     const int hbase = blockIdx.y * (HPI * QK_U);
     float cv[8], sv[8];
     const int half = sec >> 1;
@@ -410,8 +410,9 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
     for (int u = 0; u < QK_U; ++u) {           // every load of the group first
         const int hh = hbase + u * HPI + hl;
         if (hh < nh) {
-            const __nv_bfloat16 *p =
-                qkv + row * ld + (hh < nq ? q_off + hh * HD : k_off + (hh - nq) * HD) + c0;
+            const int col = hh < nq ? q_off + hh * HD
+                                    : (hh < nq + nkv ? k_off + (hh - nq) * HD : v_off + (hh - nq - nkv) * HD);
+            const __nv_bfloat16 *p = qkv + row * ld + col + c0;
             raw[u] = *reinterpret_cast<const uint4 *>(p);
         } else {
             raw[u] = make_uint4(0u, 0u, 0u, 0u);
@@ -422,41 +423,47 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
         const int hh = hbase + u * HPI + hl;
         const bool active = hh < nh;            // lane groups past the last head idle
         const bool isq = hh < nq;
+        const bool isv = hh >= nq + nkv;        // v heads: RMS norm without weight, no RoPE
         float v[8];
         v[0] = bf16_lo(raw[u].x); v[1] = bf16_hi(raw[u].x); v[2] = bf16_lo(raw[u].y); v[3] = bf16_hi(raw[u].y);
         v[4] = bf16_lo(raw[u].z); v[5] = bf16_hi(raw[u].z); v[6] = bf16_lo(raw[u].w); v[7] = bf16_hi(raw[u].w);
         const float *nw = isq ? qn : kn;
-        if (qn) {                               // qn and kn are both given or both NULL
+        if (qn || nv) {                         // uniform: qn and kn are both given or both NULL
             float q = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) q += v[e] * v[e];
 #pragma unroll
             for (int o = 1; o < LPH; o <<= 1) q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
             const float inv = rsqrtf(q / (float)HD + eps);
-            if (active) {
+            if (active && isv) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= inv;
+            } else if (active && qn) {
                 const float4 w0 = *reinterpret_cast<const float4 *>(nw + c0);
                 const float4 w1 = *reinterpret_cast<const float4 *>(nw + c0 + 4);
                 v[0] *= inv * w0.x; v[1] *= inv * w0.y; v[2] *= inv * w0.z; v[3] *= inv * w0.w;
                 v[4] *= inv * w1.x; v[5] *= inv * w1.y; v[6] *= inv * w1.z; v[7] *= inv * w1.w;
             }
         }
-        if (sec) {
+        if (sec) {                              // every lane exchanges; v heads keep theirs
             float o[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float partner = __shfl_xor_sync(0xFFFFFFFFu, v[e], xr);
                 o[e] = first_half ? v[e] * cv[e] - partner * sv[e] : v[e] * cv[e] + partner * sv[e];
             }
+            if (!isv) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = o[e];
+                for (int e = 0; e < 8; ++e) v[e] = o[e];
+            }
         }
         if (active) {
             const float mul = isq ? q_mul : 1.f;
             uint4 w;
             w.x = pack_bf16x2(v[0] * mul, v[1] * mul); w.y = pack_bf16x2(v[2] * mul, v[3] * mul);
             w.z = pack_bf16x2(v[4] * mul, v[5] * mul); w.w = pack_bf16x2(v[6] * mul, v[7] * mul);
-            __nv_bfloat16 *p =
-                qkv + row * ld + (isq ? q_off + hh * HD : k_off + (hh - nq) * HD) + c0;
+            const int col = isq ? q_off + hh * HD : (isv ? v_off + (hh - nq - nkv) * HD : k_off + (hh - nq) * HD);
+            __nv_bfloat16 *p = qkv + row * ld + col + c0;
             *reinterpret_cast<uint4 *>(p) = w;
         }
     }
@@ -691,16 +698,17 @@ te_status te_add_norm(float *h, const float *t, const float *w_post, float post,
                            stream);
 }
 
-te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t nq,
-                          int32_t nkv, int32_t hd, const float *qn, const float *kn, float eps,
-                          const float *cos, const float *sin, const int32_t *pos,
-                          int32_t table_rows, int32_t sec, float q_mul, int32_t rows,
-                          te_stream stream) {
+te_status te_qkv_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t v_off,
+                           int32_t nq, int32_t nkv, int32_t hd, const float *qn, const float *kn,
+                           int32_t v_norm, float eps, const float *cos, const float *sin,
+                           const int32_t *pos, int32_t table_rows, int32_t sec, float q_mul,
+                           int32_t rows, te_stream stream) {
     if (!qkv) return fail(TE_EINVAL, "qk_prep_rope: NULL qkv");
     if (hd != 64 && hd != 128) return fail(TE_ESHAPE, "qk_prep_rope: hd=%d (64 or 128)", hd);
-    if (nq < 0 || nkv < 0 || rows < 0 || q_off < 0 || k_off < 0)
+    if (nq < 0 || nkv < 0 || rows < 0 || q_off < 0 || k_off < 0 || (v_norm && v_off < 0))
         return fail(TE_ESHAPE, "qk_prep_rope: negative size or offset");
-    if ((int64_t)q_off + (int64_t)nq * hd > ld || (int64_t)k_off + (int64_t)nkv * hd > ld)
+    if ((int64_t)q_off + (int64_t)nq * hd > ld || (int64_t)k_off + (int64_t)nkv * hd > ld ||
+        (v_norm && (int64_t)v_off + (int64_t)nkv * hd > ld))
         return fail(TE_ESHAPE, "qk_prep_rope: heads run past the row (ld=%lld)", (long long)ld);
     if (sec != 0 && sec != hd && sec != hd / 2)
         return fail(TE_ESHAPE, "qk_prep_rope: sec=%d (0, hd or hd/2)", sec);
@@ -709,24 +717,34 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
     if (sec && !pos && table_rows < rows)
         return fail(TE_ESHAPE, "qk_prep_rope: table has %d rows, need %d (pos == NULL)", table_rows, rows);
     if (!aligned16(qkv) || (ld * 2) % 16 || (q_off * 2) % 16 || (k_off * 2) % 16 ||
-        (qn && !aligned16(qn)) || (kn && !aligned16(kn)) || (cos && !aligned16(cos)) ||
-        (sin && !aligned16(sin)))
+        (v_norm && (v_off * 2) % 16) || (qn && !aligned16(qn)) || (kn && !aligned16(kn)) ||
+        (cos && !aligned16(cos)) || (sin && !aligned16(sin)))
         return fail(TE_EALIGN, "qk_prep_rope: qkv rows, head offsets and tables must be 16-byte aligned");
     if ((qn == nullptr) != (kn == nullptr))
         return fail(TE_EINVAL, "qk_prep_rope: give both qn and kn or neither");
-    if (rows == 0 || nq + nkv == 0) return TE_OK;
+    const int nv = v_norm ? nkv : 0;
+    if (rows == 0 || nq + nkv + nv == 0) return TE_OK;
     const int heads_per_warp = (32 / (hd / 8)) * QK_U;
     const dim3 grid((unsigned)(((long long)rows + 7) / 8),
-                    (unsigned)((nq + nkv + heads_per_warp - 1) / heads_per_warp));
+                    (unsigned)((nq + nkv + nv + heads_per_warp - 1) / heads_per_warp));
     if (hd == 64)
-        qk_prep_kernel<64><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, nq,
-                                                     nkv, qn, kn, eps, cos, sin, pos, table_rows,
+        qk_prep_kernel<64><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, v_off, nq,
+                                                     nkv, nv, qn, kn, eps, cos, sin, pos, table_rows,
                                                      sec, q_mul, rows);
     else
-        qk_prep_kernel<128><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, nq,
-                                                      nkv, qn, kn, eps, cos, sin, pos, table_rows,
+        qk_prep_kernel<128><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, v_off, nq,
+                                                      nkv, nv, qn, kn, eps, cos, sin, pos, table_rows,
                                                       sec, q_mul, rows);
     return launched("qk_prep_rope launch");
+}
+
+te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t nq,
+                          int32_t nkv, int32_t hd, const float *qn, const float *kn, float eps,
+                          const float *cos, const float *sin, const int32_t *pos,
+                          int32_t table_rows, int32_t sec, float q_mul, int32_t rows,
+                          te_stream stream) {
+    return te_qkv_prep_rope(qkv, ld, q_off, k_off, 0, nq, nkv, hd, qn, kn, 0, eps, cos, sin, pos,
+                            table_rows, sec, q_mul, rows, stream);
 }
 
 te_status te_gate_act(const void *gu, int64_t ld, int32_t u_off, int32_t act, void *m,

@@ -105,6 +105,7 @@ class EncoderStack:
             d.next_norm_w, d.next_norm_b = ptr(nxt.t["norm1_w"]), ptr(nxt.t["norm1_b"])
             d.next_mod_scale = ptr(nxt.s_msa)
         d.mod = ptr(L.t["mod"])
+        d.v_norm = 1 if getattr(cfg, "v_norm", False) else 0
         if cfg.qk_norm:
             d.q_norm, d.k_norm = ptr(L.t["q_norm"]), ptr(L.t["k_norm"])
         if self.rope_sec:

@@ -67,6 +67,7 @@ class BlockConfig:
     post: float = 1.0
     adaln: bool = False  # DiT adaLN modulation: per block [s_msa | g_msa | s_mlp | g_mlp]
     codec: str = "q8_row"  # weight format: "q8_row" | "q8_2f" | "q8_0" | "q4_0"
+    v_norm: bool = False   # RMS-normalise the v heads too (egemma2.rs Prog::qkv "v norm")
 
     def window_of(self, layer: int) -> int:
         if self.window == 0:
@@ -103,6 +104,8 @@ CONFIGS = {
 # outside the block).
 CONFIGS["c4m"] = dataclasses.replace(CONFIGS["c4"], name="c4m_dit_block_adaln_d3840", adaln=True)
 CONFIGS["c5m"] = dataclasses.replace(CONFIGS["c5"], name="c5m_dit_stack30_adaln_d3840", adaln=True)
+# The text stack with the v heads normalised as well.
+CONFIGS["c2v"] = dataclasses.replace(CONFIGS["c2"], name="c2v_text_stack24_vnorm_d512", v_norm=True)
 # The DiT block with q8_2f weights (zimage.rs: q8_row + a per-column field).
 CONFIGS["c4f"] = dataclasses.replace(CONFIGS["c4"], name="c4f_dit_block_q8_2f_d3840", codec="q8_2f")
 # The ViT stack with the 32-element block weight formats of
