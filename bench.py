@@ -60,7 +60,8 @@ def visible_pairs(lens, window):
 def layer_flops(cfg, lens, layer):
     T = int(np.sum(lens))
     d, hd, H, KV, F = cfg.d, cfg.hd, cfg.heads, cfg.kv_heads, cfg.ffn
-    gemm = 2 * T * (d * (H + 2 * KV) * hd + H * hd * d + d * F * (2 if cfg.gated else 1) + F * d)
+    gemm = 2 * T * (d * (H + 2 * KV) * hd + H * hd * d + d * F * (2 if cfg.gated else 1) + F * d
+                    + 3 * d * cfg.ple_dim)
     attn = 4 * hd * H * visible_pairs(lens, cfg.window_of(layer))
     return gemm, attn
 
@@ -83,6 +84,8 @@ def launches_per_forward(cfg):
         n += 1 if (cfg.qk_norm or cfg.rope or cfg.v_norm) else 0   # q/k (v) norm + RoPE
         n += 2                                                # attention, FFN pre-norm
         n += 1 if (cfg.form == "sandwich" or i + 1 < cfg.layers) else 0   # closing norm
+        n += 7 if cfg.ple_dim else 0       # per-layer input: 3 GEMMs, norm, cast, gate, residual
+    n += 1 if cfg.ple_dim else 0                              # the per-layer inputs' bf16 source
     return n + (1 if cfg.pool else 0)                         # final norm + pool
 
 
@@ -166,7 +169,8 @@ def build_stack(key, device, lens=None, x_seed_offset=0):
     layers = [synth.draw_layer(cfg, i, seed, jitter=False) for i in range(cfg.layers)]
     tables = synth.rope_tables(cfg, lens)
     fin = synth.draw_final_norm(cfg, seed) if cfg.pool else None
-    st = EncoderStack(cfg, layers, lens, tables, fin, device=device)
+    ple = synth.draw_ple(cfg, seed) if cfg.ple_dim else None
+    st = EncoderStack(cfg, layers, lens, tables, fin, device=device, ple=ple)
     x0 = synth.draw_x(st.T, cfg.d, seed + x_seed_offset)
     return cfg, lens, st, x0, layers, tables
 
@@ -505,20 +509,23 @@ def cpu_sample(key):
     cfg = synth.CONFIGS[key]
     lens = synth.draw_lens(cfg)
     seed = synth.config_seed(key)
-    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1, "c3q8": 1, "c3q4": 1, "c4f": 1, "c2v": 6}[key]
+    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1, "c3q8": 1, "c3q4": 1, "c4f": 1, "c2v": 6, "c2p": 6}[key]
     sl = lens[:take]
     if key in ("c4", "c5", "c4m", "c5m", "c4f"):
         sl = np.asarray([min(int(sl[0]), 1056)], dtype=np.int32)
     return cfg, sl, seed
 
 
-def oracle_layer(cfg, lens, layer, p, x, tables):
+def oracle_layer(cfg, lens, layer, p, x, tables, seed=0):
     from oracle import encoder as O
     cu = synth.cu_seqlens(lens)
     mod = p.get("mod")
     a = O.round_bf16(O.norm(cfg.norm, x, p["norm1_w"], p["norm1_b"], cfg.eps,
                             mod_scale=None if mod is None else mod[0]))
-    return O.block_forward(cfg, p, x, a, cu, layer, tables, None, mod=mod)
+    ple = None
+    if cfg.ple_dim:
+        ple = dict(synth.draw_ple(cfg, seed), x_in=x)
+    return O.block_forward(cfg, p, x, a, cu, layer, tables, None, mod=mod, ple=ple)
 
 
 def cpu_baseline(cfg_full, key, budget_s=15.0):
@@ -534,7 +541,7 @@ def cpu_baseline(cfg_full, key, budget_s=15.0):
         if li not in ps:
             ps[li] = synth.draw_layer(cfg, li, seed, jitter=False)
         t0 = time.perf_counter()
-        oracle_layer(cfg, sl, li, ps[li], x, tables)
+        oracle_layer(cfg, sl, li, ps[li], x, tables, seed)
         t_used += time.perf_counter() - t0
         g, a = layer_flops(cfg, sl, li)
         flops += g + a
@@ -559,12 +566,12 @@ def run_reference(args):
     x = synth.draw_x(T, cfg.d, seed).astype(np.float64)
     ps = [synth.draw_layer(cfg, i, seed, jitter=False) for i in range(min(2, cfg.layers))]
     for i in range(args.warmup):
-        oracle_layer(cfg, sl, i % len(ps), ps[i % len(ps)], x, tables)
+        oracle_layer(cfg, sl, i % len(ps), ps[i % len(ps)], x, tables, seed)
     times, flops = [], 0.0
     for i in range(args.steps):
         li = i % len(ps)
         t0 = time.perf_counter()
-        oracle_layer(cfg, sl, li, ps[li], x, tables)
+        oracle_layer(cfg, sl, li, ps[li], x, tables, seed)
         times.append(time.perf_counter() - t0)
         g, a = layer_flops(cfg, sl, li)
         flops += g + a

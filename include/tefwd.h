@@ -245,6 +245,12 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
                           int32_t table_rows, int32_t sec, float q_mul, int32_t rows,
                           te_stream stream);
 
+/* cast_bf16: y = bf16(x) (round to nearest even) for x f32 [rows, d] (ldx),
+ * y bf16 [rows, ldy]; d % 8 == 0.  The per-layer input path's GEMM reads the
+ * residual stream this way. */
+te_status te_cast_bf16(const float *x, int64_t ldx, void *y, int64_t ldy, int32_t rows, int32_t d,
+                       te_stream stream);
+
 /* qkv_prep_rope: qk_prep_rope, and with v_norm != 0 also the v heads (at
  * v_off + g*hd) RMS-normalised without a weight and without RoPE:
  * v = v / sqrt(mean(v^2) + eps) ([EG2] Prog::qkv "q/k norm + RoPE, v norm":
@@ -295,6 +301,19 @@ typedef struct {
      * next_mod_scale = the next block's s_msa, f32 [d], applied to a_out. */
     const float *mod, *next_mod_scale;
     int32_t v_norm;      /* 1: RMS-normalise the v heads too (te_qkv_prep_rope) */
+    /* per-layer input path ([EG2] TextGpu::forward "per-layer input", LayerSpec
+     * ple_in / ple_gate / ple_proj / ple_norm, TextSpec ple_scale / ple_norm;
+     * sandwich form only), or ple_dim == 0.  After the FFN residual (then with
+     * post 1 and no next norm):
+     *   pin = RMS(ple_scale * (ple_x . W_in^T)) * ple_norm_w      [t, ple_dim]
+     *   z   = gelu_tanh(bf16(bf16(x) . W_gate^T)) * pin           [t, ple_dim]
+     *   x   = (x + RMS(z . W_proj^T) * ple_post_w) * post;  a = Norm_next(x)
+     * ple_x: bf16 [t, d], the stack's input (the same for every layer). */
+    int32_t ple_dim;
+    float ple_scale;
+    te_q8w ple_in, ple_gate, ple_proj;
+    const float *ple_norm_w, *ple_post_w;
+    const void *ple_x;
 } te_block_desc;
 
 /* Workspace bytes te_encoder_block_fwd needs for t packed rows. */

@@ -404,7 +404,7 @@ def pool_mean(x, cu, w, eps):
 
 
 def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mod=None,
-                  next_mod_scale=None):
+                  next_mod_scale=None, ple=None):
     """One encoder block, step by step; returns every stored intermediate.
 
     cfg: a BlockConfig-like object (d, heads, kv_heads, hd, ffn, gated, act,
@@ -423,6 +423,11 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mo
     the two residual branches with g_msa, g_mlp and scales the FFN input by
     (1 + s_mlp); s_msa scales this block's input ``a`` (made by the caller)
     and ``next_mod_scale`` (the next block's s_msa) the returned ``a_out``.
+    Per-layer input path (egemma2.rs ``TextGpu::forward`` "per-layer input";
+    ``ple`` = {x_in: the stack's input as bf16, norm_w, scale}, sandwich form):
+    after the FFN residual (taken with post 1) pin = rms(scale * x_in W_in^T)
+    ple_norm, z = gelu_tanh(bf16(x) W_gate^T) * pin, and
+    x = (x + rms(z W_proj^T) w_ple) * post.
     ``rows`` restricts the block to sampled query rows: q|k|v is computed for
     every row (all keys are needed), everything after attention only for the
     sampled rows (it is row-local), and the returned post-attention
@@ -478,7 +483,17 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mo
     else:
         f = round_f32(linear(m, p["wd"]))
         r["f"] = f
-        x = round_f32(add_norm_sandwich(x, f, p["post_ffn_w"], cfg.post, eps, gate=g_mlp))
+        if ple is None:
+            x = round_f32(add_norm_sandwich(x, f, p["post_ffn_w"], cfg.post, eps, gate=g_mlp))
+        else:
+            x = round_f32(add_norm_sandwich(x, f, p["post_ffn_w"], 1.0, eps, gate=g_mlp))
+            x_in = ple["x_in"] if rows is None else np.asarray(ple["x_in"])[rows]
+            t1 = round_f32(linear(round_bf16(x_in), p["ple_in"]))
+            pin = round_bf16(rms_norm(t1, ple["norm_w"], eps, pre=ple["scale"]))
+            g = round_bf16(linear(round_bf16(x), p["ple_gate"]))
+            r["ple_z"] = z = round_bf16(gelu_tanh(g) * pin)
+            tp = round_f32(linear(z, p["ple_proj"]))
+            x = round_f32(add_norm_sandwich(x, tp, p["ple_post_w"], cfg.post, eps))
     r["x_out"] = x
     if next_norm is not None:
         r["a_out"] = round_bf16(norm(cfg.norm, x, next_norm[0], next_norm[1], eps,

@@ -224,6 +224,12 @@ def test_block_validation_and_workspace(L):
     mod_unal = _desc(mod=FAKE + 4, **sand_ok)
     assert _call(L, "te_encoder_block_fwd", ctypes.byref(mod_unal), FAKE, FAKE, p, FAKE, 2,
                  FAKE * 256, ws, None)[0] == te.TE_EALIGN
+    plain_ple = _desc(ple_dim=64, ple_norm_w=FAKE, ple_post_w=FAKE, ple_x=FAKE)
+    assert _call(L, "te_encoder_block_fwd", ctypes.byref(plain_ple), FAKE, FAKE, p, FAKE, 2,
+                 FAKE * 256, ws, None)[0] == te.TE_EINVAL
+    odd_ple = _desc(ple_dim=100, **sand_ok)
+    assert _call(L, "te_encoder_block_fwd", ctypes.byref(odd_ple), FAKE, FAKE, p, FAKE, 2,
+                 FAKE * 256, ws, None)[0] == te.TE_ESHAPE
     next_s_only = _desc(mod=FAKE, next_mod_scale=FAKE, **sand_ok)
     assert _call(L, "te_encoder_block_fwd", ctypes.byref(next_s_only), FAKE, FAKE, p, FAKE, 2,
                  FAKE * 256, ws, None)[0] == te.TE_EINVAL

@@ -25,7 +25,10 @@ def _stack(cfg, lens, layers, seed=11, jitter=True):
     ps = [synth.draw_layer(cfg, i, seed, jitter) for i in range(layers)]
     tables = synth.rope_tables(cfg, lens)
     fin = synth.draw_final_norm(cfg, seed) if cfg.pool else None
-    return EncoderStack(cfg, ps, lens, tables, fin), ps, tables
+    ple = synth.draw_ple(cfg, seed) if cfg.ple_dim else None
+    st = EncoderStack(cfg, ps, lens, tables, fin, ple=ple)
+    st.ple_host = ple
+    return st, ps, tables
 
 
 def _next_norm(ps, i):
@@ -47,8 +50,11 @@ def _check_layer(cfg, st, ps, tables, i, x, a, rows=None):
     te.encoder_block_fwd(st.descs[i], x, a, st.cu_host, st.cu_dev, st.workspace)
     te.check()
     mod, next_s = _mods(ps, i)
+    ple = None
+    if st.ple_x is not None:
+        ple = dict(st.ple_host, x_in=to_np(st.ple_x))
     r = O.block_forward(cfg, ps[i], x_in, a_in, st.cu_host, i, tables, _next_norm(ps, i),
-                        rows=rows, mod=mod, next_mod_scale=next_s)
+                        rows=rows, mod=mod, next_mod_scale=next_s, ple=ple)
     sel = slice(None) if rows is None else np.asarray(rows)
     got_x = to_np(x)[sel]
     xin = x_in[sel]
@@ -77,6 +83,8 @@ FORMS = {
     "c3q4_small": ("c3q4", dict(layers=2), (200, 129)),
     # the text block with the v heads normalised too
     "c2v_small": ("c2v", dict(layers=2, window=40), (100, 1, 300, 37)),
+    # the text block with the per-layer input path
+    "c2p_small": ("c2p", dict(layers=2, window=40), (100, 1, 300, 37)),
     # the DiT block with q8_2f weights (column field)
     "c4f_small": ("c4f", dict(layers=2, d=512, heads=4, kv_heads=4, ffn=1024), (150, 133)),
 }
@@ -90,6 +98,8 @@ def test_block_forms_match_oracle(name):
     x = to_dev(synth.draw_x(st.T, cfg.d, 3))
     import torch
     a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    if st.ple_x is not None:
+        te.cast_bf16(x, st.ple_x)        # the per-layer inputs' source, as a forward makes it
     st.input_norm(x, a)
     s0 = ps[0]["mod"][0] if cfg.adaln else None
     a0 = O.round_bf16(O.norm(cfg.norm, to_np(x), ps[0]["norm1_w"], ps[0]["norm1_b"], cfg.eps,

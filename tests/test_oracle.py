@@ -754,3 +754,47 @@ def test_two_range_items_reduce_to_varlen_and_ignore_range_order_without_window(
     # full attention: swapping the two ranges changes nothing per row
     sw = O.attention_items(qkv, [[0, 12, 40, 30]], *args, 0, scale)
     np.testing.assert_allclose(sw[rows], it[rows], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------ per-layer input (PLE)
+# egemma2.rs TextGpu::forward "per-layer input": pin = rms(ple_scale * x W_in^T)
+# ple_norm; z = gelu(h W_gate^T) * pin; H = (H + rms(z W_proj^T) w) * scalar.
+
+def _ple_case(seed=51):
+    cfg = _tiny("sandwich", "rms", True, "gelu_tanh", "1d", True, 0)
+    import dataclasses
+    cfg = dataclasses.replace(cfg, ple_dim=64)
+    p = synth.draw_layer(cfg, 0, seed)
+    cu = synth.cu_seqlens(cfg.lens)
+    x = synth.draw_x(int(cu[-1]), cfg.d, seed + 1)
+    a = O.round_bf16(O.rms_norm(x, p["norm1_w"], cfg.eps))
+    ple = dict(synth.draw_ple(cfg, seed), x_in=O.round_bf16(x))
+    return cfg, p, cu, x, a, ple, synth.rope_tables(cfg, cfg.lens)
+
+
+@pytest.mark.parametrize("zeroed", ["ple_in", "ple_gate", "ple_proj"])
+def test_ple_path_with_a_zero_weight_adds_nothing(zeroed):
+    # any of the three projections at zero makes the branch exactly 0
+    # (pin = 0, or gelu(0) = 0, or rms(0) = 0): the block without the path
+    cfg, p, cu, x, a, ple, tables = _ple_case()
+    p[zeroed] = dict(p[zeroed], s=np.zeros_like(p[zeroed]["s"]))
+    r = O.block_forward(cfg, p, x, a, cu, 0, tables, ple=ple)
+    import dataclasses
+    base = O.block_forward(dataclasses.replace(cfg, ple_dim=0), p, x, a, cu, 0, tables)
+    np.testing.assert_array_equal(r["x_out"], base["x_out"])
+
+
+def test_ple_pin_ignores_the_scale_of_its_source():
+    # rms(c v) = rms(v) up to eps: scaling the per-layer source by a power of
+    # two (exact in bf16) barely moves the result, while the branch itself is
+    # far from zero
+    cfg, p, cu, x, a, ple, tables = _ple_case(53)
+    r1 = O.block_forward(cfg, p, x, a, cu, 0, tables, ple=ple)
+    r2 = O.block_forward(cfg, p, x, a, cu, 0, tables, ple=dict(ple, x_in=ple["x_in"] * 4.0))
+    import dataclasses
+    base = O.block_forward(dataclasses.replace(cfg, ple_dim=0), p, x, a, cu, 0, tables)
+    assert np.max(np.abs(r1["x_out"] - base["x_out"])) > 0.05
+    # equal up to bf16 rounding flips of pin (eps moves it by ~1e-4 relative)
+    d_scaled, d_branch = r2["x_out"] - r1["x_out"], r1["x_out"] - base["x_out"]
+    assert np.linalg.norm(d_scaled) < 0.02 * np.linalg.norm(d_branch)
+    assert np.any(r1["ple_z"])

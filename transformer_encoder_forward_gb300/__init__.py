@@ -55,7 +55,9 @@ class te_block_desc(ctypes.Structure):
                 ("post_ffn_w", c_p), ("next_norm_w", c_p), ("next_norm_b", c_p),
                 ("q_norm", c_p), ("k_norm", c_p), ("rope_cos", c_p), ("rope_sin", c_p),
                 ("rope_pos", c_p), ("rope_sec", c_i32), ("rope_rows", c_i32),
-                ("mod", c_p), ("next_mod_scale", c_p), ("v_norm", c_i32)]
+                ("mod", c_p), ("next_mod_scale", c_p), ("v_norm", c_i32),
+                ("ple_dim", c_i32), ("ple_scale", c_f32), ("ple_in", te_q8w), ("ple_gate", te_q8w),
+                ("ple_proj", te_q8w), ("ple_norm_w", c_p), ("ple_post_w", c_p), ("ple_x", c_p)]
 
 
 _lib = None
@@ -83,6 +85,7 @@ EXPORTS = {
     "te_qkv_prep_rope": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_p,
                                         c_p, c_i32, c_f32, c_p, c_p, c_p, c_i32, c_i32, c_f32, c_i32,
                                         c_p]),
+    "te_cast_bf16": (ctypes.c_int, [c_p, c_i64, c_p, c_i64, c_i32, c_i32, c_p]),
     "te_gate_act": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_i64, c_i32, c_i32, c_p]),
     "te_pool_mean": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_i32, c_p, c_f32, c_p, c_p]),
     "te_encoder_block_workspace": (ctypes.c_size_t, [ctypes.POINTER(te_block_desc), c_i32]),
@@ -202,6 +205,12 @@ def attn_items_fwd(qkv, ld, q_off, k_off, v_off, items_host, items_dev, rows, nq
     _ok(lib().te_attn_items_fwd(qkv.data_ptr(), ld, q_off, k_off, v_off, arr.ctypes.data_as(c_p),
                                 items_dev.data_ptr(), arr.shape[0], rows, nq, nkv, hd, window, scale,
                                 out.data_ptr(), ldo, _stream(stream)))
+
+
+def cast_bf16(x, y, stream=None):
+    """y (bf16) = x (f32), rows of the same width."""
+    _ok(lib().te_cast_bf16(x.data_ptr(), x.stride(0), y.data_ptr(), y.stride(0), x.shape[0], x.shape[1],
+                           _stream(stream)))
 
 
 def _dt(t) -> int:

@@ -15,6 +15,8 @@
 //
 // Workspace layout (each region 256-byte aligned):
 //   qkv bf16 [t, (nq + 2 nkv) hd] | o bf16 [t, nq hd] | tmp f32 [t, d] | m bf16 [t, F]
+//   and with the per-layer input path: pin f32 [t, P] | panel bf16 [t, 2P] |
+//   z bf16 [t, P] | bf16 copy of x [t, d]
 #include "common.cuh"
 
 namespace tefwd {
@@ -23,7 +25,9 @@ namespace {
 inline size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t qkv, o, tmp, m, total;
+    size_t qkv, o, tmp, m;
+    size_t pin, panel, z, hb;   // per-layer input path only
+    size_t total;
 };
 
 WsLayout ws_layout(const te_block_desc &d, int32_t t) {
@@ -36,6 +40,14 @@ WsLayout ws_layout(const te_block_desc &d, int32_t t) {
     L.o = off;   off = up256(off + T * ow * 2);
     L.tmp = off; off = up256(off + T * d.d * 4);
     L.m = off;   off = up256(off + T * (size_t)d.ffn * 2);
+    L.pin = L.panel = L.z = L.hb = 0;
+    if (d.ple_dim > 0) {
+        const size_t np = (size_t)d.ple_dim;
+        L.pin = off;   off = up256(off + T * np * 4);        // f32 x_in . W_in^T
+        L.panel = off; off = up256(off + T * 2 * np * 2);    // bf16 [gate | pin]
+        L.z = off;     off = up256(off + T * np * 2);        // bf16 gelu(gate) * pin
+        L.hb = off;    off = up256(off + T * (size_t)d.d * 2);   // bf16 copy of x
+    }
     L.total = off;
     return L;
 }
@@ -78,6 +90,15 @@ te_status check_desc(const te_block_desc *d) {
         return fail(TE_EINVAL, "block: adaLN modulation needs the sandwich form");
     if (d->next_mod_scale && !d->next_norm_w)
         return fail(TE_EINVAL, "block: next_mod_scale given without next_norm_w");
+    if (d->ple_dim < 0 || (d->ple_dim > 0 && (d->ple_dim % 64 || d->ple_dim > 4096)))
+        return fail(TE_ESHAPE, "block: ple_dim=%d (0, or a multiple of 64 up to 4096)", d->ple_dim);
+    if (d->ple_dim > 0) {
+        if (d->resid_form != TE_RESID_SANDWICH) return fail(TE_EINVAL, "block: the per-layer input path needs the sandwich form");
+        if (!d->ple_norm_w || !d->ple_post_w || !d->ple_x)
+            return fail(TE_EINVAL, "block: the per-layer input path needs ple_norm_w, ple_post_w and ple_x");
+        if (!aligned16(d->ple_norm_w) || !aligned16(d->ple_post_w) || !aligned16(d->ple_x))
+            return fail(TE_EALIGN, "block: per-layer input vectors must be 16-byte aligned");
+    }
     const float *vecs[] = {d->ffn_norm_w, d->ffn_norm_b, d->post_attn_w, d->post_ffn_w,
                            d->next_norm_w, d->next_norm_b, d->q_norm, d->k_norm,
                            d->mod, d->next_mod_scale};
@@ -90,6 +111,10 @@ te_status check_desc(const te_block_desc *d) {
         (st = check_w(d->wg, d->ffn, d->d, "wg")) || (st = check_w(d->wd, d->d, d->ffn, "wd")))
         return st;
     if (d->gated && (st = check_w(d->wu, d->ffn, d->d, "wu"))) return st;
+    if (d->ple_dim > 0 && ((st = check_w(d->ple_in, d->ple_dim, d->d, "ple_in")) ||
+                           (st = check_w(d->ple_gate, d->ple_dim, d->d, "ple_gate")) ||
+                           (st = check_w(d->ple_proj, d->d, d->ple_dim, "ple_proj"))))
+        return st;
     return TE_OK;
 }
 
@@ -179,6 +204,33 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
         if (d.next_norm_w)
             st = te_rownorm(x, TE_F32, D, d.next_norm_w, d.next_norm_b, d.norm_kind, d.eps, 1.f, a,
                             TE_BF16, D, t, D, stream);
+    } else if (d.ple_dim > 0) {
+        // the FFN residual (post 1, no next norm), then the per-layer input path
+        if ((st = te_add_norm_mod(x, tmp, d.post_ffn_w, d.mod ? d.mod + 3 * D : nullptr, 1.f, nullptr,
+                                  nullptr, nullptr, d.norm_kind, d.eps, nullptr, TE_BF16, t, D, stream)) != TE_OK)
+            return st;
+        const int NP = d.ple_dim;
+        float *pin = reinterpret_cast<float *>(ws + L.pin);
+        __nv_bfloat16 *panel = reinterpret_cast<__nv_bfloat16 *>(ws + L.panel);
+        __nv_bfloat16 *z = reinterpret_cast<__nv_bfloat16 *>(ws + L.z);
+        __nv_bfloat16 *hb = reinterpret_cast<__nv_bfloat16 *>(ws + L.hb);
+        // pin = RMS(ple_scale * x_in W_in^T) * ple_norm, into the panel's second half
+        te_q8_item ip = {d.ple_in, pin, NP, TE_F32, 0, nullptr, 0};
+        if ((st = te_q8_linear(d.ple_x, D, t, D, &ip, 1, stream)) != TE_OK) return st;
+        if ((st = te_rownorm(pin, TE_F32, NP, d.ple_norm_w, nullptr, TE_NORM_RMS, d.eps, d.ple_scale,
+                             panel + NP, TE_BF16, 2 * NP, t, NP, stream)) != TE_OK)
+            return st;
+        // gate = bf16(x) W_gate^T into the first half; z = gelu_tanh(gate) * pin
+        if ((st = te_cast_bf16(x, D, hb, D, t, D, stream)) != TE_OK) return st;
+        te_q8_item ig = {d.ple_gate, panel, 2 * NP, TE_BF16, 0, nullptr, 0};
+        if ((st = te_q8_linear(hb, D, t, D, &ig, 1, stream)) != TE_OK) return st;
+        if ((st = te_gate_act(panel, 2 * NP, NP, TE_ACT_GELU_TANH, z, NP, t, NP, stream)) != TE_OK) return st;
+        // x = (x + RMS(z W_proj^T) w_post) * post; a = Norm_next(x)
+        te_q8_item iq = {d.ple_proj, tmp, D, TE_F32, 0, nullptr, 0};
+        if ((st = te_q8_linear(z, NP, t, NP, &iq, 1, stream)) != TE_OK) return st;
+        st = te_add_norm_mod(x, tmp, d.ple_post_w, nullptr, d.post, d.next_norm_w, d.next_norm_b,
+                             d.next_mod_scale, d.norm_kind, d.eps, d.next_norm_w ? a : nullptr, TE_BF16, t,
+                             D, stream);
     } else {
         // adaLN: gate g_mlp on the FFN branch, the next block's s_msa on its input
         st = te_add_norm_mod(x, tmp, d.post_ffn_w, d.mod ? d.mod + 3 * D : nullptr, d.post, d.next_norm_w,

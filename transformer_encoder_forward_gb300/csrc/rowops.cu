@@ -348,6 +348,23 @@ __global__ void __launch_bounds__(256) add_norm_wide_kernel(float *h, const floa
     }
 }
 
+// ---------------------------------------------------------------- cast bf16
+
+// Grid-stride over 8-column chunks: 32 bytes in, 16 bytes out.
+__global__ void __launch_bounds__(256) cast_bf16_kernel(const float *__restrict__ x, long long ldx,
+                                                        __nv_bfloat16 *__restrict__ y, long long ldy,
+                                                        int rows, int chunks) {
+    const long long total = (long long)rows * chunks;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / chunks;
+        const int c = (int)(i - r * chunks) * 8;
+        float v[8];
+        load8(x + r * ldx + c, v);
+        store8(y + r * ldy + c, v);
+    }
+}
+
 // ------------------------------------------------------------- qk prep + RoPE
 
 // One warp per (packed row, group of QK_U * 32 / (HD / 8) heads).  Each lane
@@ -745,6 +762,20 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
                           te_stream stream) {
     return te_qkv_prep_rope(qkv, ld, q_off, k_off, 0, nq, nkv, hd, qn, kn, 0, eps, cos, sin, pos,
                             table_rows, sec, q_mul, rows, stream);
+}
+
+te_status te_cast_bf16(const float *x, int64_t ldx, void *y, int64_t ldy, int32_t rows, int32_t d,
+                       te_stream stream) {
+    if (!x || !y) return fail(TE_EINVAL, "cast_bf16: NULL x or y");
+    if (rows < 0 || d < 8 || d % 8 || ldx < d || ldy < d) return fail(TE_ESHAPE, "cast_bf16: rows=%d d=%d", rows, d);
+    if (!aligned16(x) || !aligned16(y) || ldx % 4 || ldy % 8)
+        return fail(TE_EALIGN, "cast_bf16: rows must be 16-byte aligned");
+    if (rows == 0) return TE_OK;
+    const long long total = (long long)rows * (d / 8);
+    const long long want = (total + 255) / 256;
+    const unsigned blocks = (unsigned)(want < 152 * 16 ? want : 152 * 16);
+    cast_bf16_kernel<<<blocks, 256, 0, stream>>>(x, ldx, (__nv_bfloat16 *)y, ldy, rows, d / 8);
+    return launched("cast_bf16 launch");
 }
 
 te_status te_gate_act(const void *gu, int64_t ld, int32_t u_off, int32_t act, void *m,

@@ -15,8 +15,8 @@ from typing import List, Optional
 import numpy as np
 
 from . import (TE_ACT_GELU_TANH, TE_ACT_SILU, TE_NORM_LN, TE_NORM_RMS, TE_RESID_PLAIN,
-               TE_RESID_SANDWICH, block_workspace, encoder_block_fwd, pool_mean, q4_0_unpack,
-               q8_0_unpack, q8w, rownorm, rownorm_mod, te_block_desc)
+               TE_RESID_SANDWICH, block_workspace, cast_bf16, encoder_block_fwd, pool_mean,
+               q4_0_unpack, q8_0_unpack, q8w, rownorm, rownorm_mod, te_block_desc)
 
 
 def _dev(a, device, dtype=None):
@@ -35,7 +35,7 @@ class LayerWeights:
     def __init__(self, cfg, p: dict, device):
         import torch
         self.t = {}
-        for key in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+        for key in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "ple_in", "ple_gate", "ple_proj"):
             w = p.get(key)
             if w is None:
                 self.t[key] = None
@@ -53,7 +53,7 @@ class LayerWeights:
                 self.t[key] = (_dev(w["q"], device), _dev(w["s"], device), _dev(w["b"], device), None,
                                _dev(w.get("col"), device))
         for key in ("norm1_w", "norm1_b", "norm2_w", "norm2_b", "post_attn_w", "post_ffn_w",
-                    "q_norm", "k_norm", "mod"):
+                    "q_norm", "k_norm", "mod", "ple_post_w"):
             self.t[key] = _dev(p.get(key), device, torch.float32)
         # adaLN: s_msa (row 0 of mod) scales this layer's input norm
         self.s_msa = self.t["mod"][0] if self.t["mod"] is not None else None
@@ -63,7 +63,7 @@ class EncoderStack:
     """A stack of encoder blocks over a packed batch with fixed lengths."""
 
     def __init__(self, cfg, layers: List[dict], lens, tables: dict,
-                 final_norm: Optional[np.ndarray] = None, device="cuda"):
+                 final_norm: Optional[np.ndarray] = None, device="cuda", ple: Optional[dict] = None):
         import torch
         self.cfg = cfg
         self.device = torch.device(device)
@@ -79,6 +79,16 @@ class EncoderStack:
         self.rope_sin = _dev(tables.get("sin"), self.device, torch.float32)
         self.rope_pos = _dev(tables.get("pos"), self.device, torch.int32)
         self.rope_sec = int(tables.get("sec") or 0)
+        # per-layer input path: the stack's input as bf16 (filled by each
+        # forward) and the stack-level norm of pin
+        self.ple_x = self.ple_norm = None
+        self.ple_scale = 0.0
+        if getattr(cfg, "ple_dim", 0):
+            if ple is None:
+                raise ValueError("the per-layer input path needs the stack-level ple weights")
+            self.ple_x = torch.empty(self.T, cfg.d, dtype=torch.bfloat16, device=self.device)
+            self.ple_norm = _dev(ple["norm_w"], self.device, torch.float32)
+            self.ple_scale = float(ple["scale"])
         self.descs = [self._desc(i) for i in range(len(self.layers))]
         ws = max(block_workspace(d, self.T) for d in self.descs)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
@@ -106,6 +116,11 @@ class EncoderStack:
             d.next_mod_scale = ptr(nxt.s_msa)
         d.mod = ptr(L.t["mod"])
         d.v_norm = 1 if getattr(cfg, "v_norm", False) else 0
+        if self.ple_x is not None:
+            d.ple_dim, d.ple_scale = cfg.ple_dim, self.ple_scale
+            d.ple_in, d.ple_gate, d.ple_proj = (q8w(*L.t[k]) for k in ("ple_in", "ple_gate", "ple_proj"))
+            d.ple_norm_w, d.ple_post_w = ptr(self.ple_norm), ptr(L.t["ple_post_w"])
+            d.ple_x = ptr(self.ple_x)
         if cfg.qk_norm:
             d.q_norm, d.k_norm = ptr(L.t["q_norm"]), ptr(L.t["k_norm"])
         if self.rope_sec:
@@ -136,6 +151,8 @@ class EncoderStack:
         """In place on the device: x (f32 [T, d]) goes through every layer;
         a ends as the last block's FFN input; out (f32 [nseq, d]) receives
         the final-normed mean-pool when the stack pools."""
+        if self.ple_x is not None:
+            cast_bf16(x, self.ple_x, stream=stream)      # the per-layer inputs' source
         self.input_norm(x, a, stream)
         n = len(self.layers) if layers is None else layers
         for i in range(n):

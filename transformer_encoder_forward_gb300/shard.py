@@ -33,7 +33,8 @@ def sequence_costs(cfg, lens) -> np.ndarray:
     """Forward flops of each sequence of the batch over all layers of cfg."""
     d, hd, H, KV, F = cfg.d, cfg.hd, cfg.heads, cfg.kv_heads, cfg.ffn
     c_lin = 2 * cfg.layers * (d * (H + 2 * KV) * hd + H * hd * d
-                              + d * F * (2 if cfg.gated else 1) + F * d)
+                              + d * F * (2 if cfg.gated else 1) + F * d
+                              + 3 * d * getattr(cfg, "ple_dim", 0))
     windows = [cfg.window_of(i) for i in range(cfg.layers)]
     out = np.empty(len(lens), dtype=np.float64)
     for s, n in enumerate(lens):

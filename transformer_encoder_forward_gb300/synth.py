@@ -68,6 +68,7 @@ class BlockConfig:
     adaln: bool = False  # DiT adaLN modulation: per block [s_msa | g_msa | s_mlp | g_mlp]
     codec: str = "q8_row"  # weight format: "q8_row" | "q8_2f" | "q8_0" | "q4_0"
     v_norm: bool = False   # RMS-normalise the v heads too (egemma2.rs Prog::qkv "v norm")
+    ple_dim: int = 0       # per-layer input width (egemma2.rs "per-layer input"), 0 = none
 
     def window_of(self, layer: int) -> int:
         if self.window == 0:
@@ -104,6 +105,8 @@ CONFIGS = {
 # outside the block).
 CONFIGS["c4m"] = dataclasses.replace(CONFIGS["c4"], name="c4m_dit_block_adaln_d3840", adaln=True)
 CONFIGS["c5m"] = dataclasses.replace(CONFIGS["c5"], name="c5m_dit_stack30_adaln_d3840", adaln=True)
+# The text stack with the per-layer input path (256 wide).
+CONFIGS["c2p"] = dataclasses.replace(CONFIGS["c2"], name="c2p_text_stack24_ple256_d512", ple_dim=256)
 # The text stack with the v heads normalised as well.
 CONFIGS["c2v"] = dataclasses.replace(CONFIGS["c2"], name="c2v_text_stack24_vnorm_d512", v_norm=True)
 # The DiT block with q8_2f weights (zimage.rs: q8_row + a per-column field).
@@ -214,7 +217,21 @@ def draw_layer(cfg: BlockConfig, layer: int, seed: int, jitter: bool = True) -> 
         p["k_norm"], _ = draw_norm(rng, hd, False)
     if cfg.adaln:
         p["mod"] = draw_mods(rng, d)
+    if cfg.ple_dim:
+        P = cfg.ple_dim
+        p["ple_in"] = draw_q8(rng, P, d, jitter, False)
+        p["ple_gate"] = draw_q8(rng, P, d, jitter, False)
+        p["ple_proj"] = draw_q8(rng, d, P, jitter, False)
+        p["ple_post_w"], _ = draw_norm(rng, d, False)
     return p
+
+
+def draw_ple(cfg: BlockConfig, seed: int) -> dict:
+    """The stack-level part of the per-layer input path: the norm weight of
+    pin ([P]) and its pre-scale."""
+    rng = np.random.default_rng([seed, 15485863])
+    return {"norm_w": (1.0 + 0.1 * rng.standard_normal(cfg.ple_dim)).astype(np.float32),
+            "scale": 0.0625}
 
 
 def draw_mods(rng: np.random.Generator, d: int) -> np.ndarray:
