@@ -40,6 +40,9 @@
 // (about 200 ms): a timeout sets an error word that te_check() reports.
 #include <cuda.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "common.cuh"
 
 namespace tefwd {
@@ -48,6 +51,7 @@ namespace {
 constexpr int BQ = 128;     // queries per tile (= TMEM lanes); two tiles per CTA
 constexpr int BKV = 128;    // keys per tile
 constexpr int NTHREADS = 320;
+constexpr int MAX_WORK = 640;   // work list entries carried in the launch parameters
 
 __device__ int g_attn_err;
 
@@ -57,6 +61,8 @@ struct AttnParams {
     __nv_bfloat16 *out;
     const int *cu;
     const int *items;          // two-range items [n][off1, len1, off2, len2], or NULL (cu)
+    int nwork;                 // > 0: CTA y -> work[y] = (unit << 16) | query block, longest first
+    uint32_t work[MAX_WORK];
     long long ldo;
     int q_off, k_off, v_off, group, window;
     float scale_log2;
@@ -163,7 +169,20 @@ template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
     using L = ALayout<HD>;
     extern __shared__ uint8_t smem_raw[];
-    const int seq = blockIdx.z;
+    // CTA (head, work): the work list orders (unit, 256-query block) by cost,
+    // longest first, so that the long blocks start early and the launch ends
+    // without a tail of one long block; without it, (query block, head, unit)
+    int seq, qblk, h;
+    if (p.nwork) {
+        const uint32_t wv = p.work[blockIdx.y];
+        seq = (int)(wv >> 16);
+        qblk = (int)(wv & 0xFFFFu);
+        h = blockIdx.x;
+    } else {
+        seq = blockIdx.z;
+        qblk = blockIdx.x;
+        h = blockIdx.y;
+    }
     // the attention unit: one packed sequence (cu), or a two-range item whose
     // joint positions 0..len1-1 are rows off1.. and len1.. are rows off2..
     int off1, len1, off2 = 0, len2 = 0;
@@ -176,10 +195,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     }
     const int len = len1 + len2;
     auto row_of = [&](int j) { return j < len1 ? off1 + j : off2 + (j - len1); };
-    const int q0 = blockIdx.x * 2 * BQ;
+    const int q0 = qblk * 2 * BQ;
     if (q0 >= len) return;
     if (*reinterpret_cast<volatile int *>(&g_attn_err) != 0) return;
-    const int h = blockIdx.y;
     const int g = h / p.group;
     const int W = p.window;
     const int ntile = q0 + BQ < len ? 2 : 1;        // tile B exists
@@ -427,7 +445,7 @@ te_status launch(const AttnParams &p, int max_len, int nq, int nseq, cudaStream_
         if (e != cudaSuccess) return cuda_fail(e, "attn: set shared memory size");
         attr_done = true;
     }
-    const dim3 grid((max_len + 2 * BQ - 1) / (2 * BQ), nq, nseq);
+    const dim3 grid = p.nwork ? dim3(nq, p.nwork, 1) : dim3((max_len + 2 * BQ - 1) / (2 * BQ), nq, nseq);
     attn_tc_kernel<HD><<<grid, NTHREADS, smem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TE_OK : cuda_fail(e, "attn launch");
@@ -468,10 +486,33 @@ static te_status attn_common_checks(const void *qkv, int64_t ld, int32_t q_off, 
     return TE_OK;
 }
 
+// The (unit, 256-query block) pairs with queries, longest first: cost =
+// queries of the block x keys it can see.  Empty when there are more than
+// MAX_WORK pairs (the plain grid is used then).
+static int build_work(const int32_t *lens, int32_t units, int32_t window, uint32_t *work) {
+    int n = 0;
+    for (int32_t u = 0; u < units; ++u) n += (lens[u] + 255) / 256;
+    if (n > MAX_WORK || units > 65535) return 0;
+    struct W { long long cost; uint32_t v; };
+    W tmp[MAX_WORK];
+    n = 0;
+    for (int32_t u = 0; u < units; ++u) {
+        for (int b = 0; b * 256 < lens[u]; ++b) {
+            const long long q = lens[u] - b * 256 < 256 ? lens[u] - b * 256 : 256;
+            long long keys = lens[u];
+            if (window > 0 && 2LL * window + 256 < keys) keys = 2LL * window + 256;
+            tmp[n++] = {q * keys, ((uint32_t)u << 16) | (uint32_t)b};
+        }
+    }
+    std::stable_sort(tmp, tmp + n, [](const W &a, const W &b) { return a.cost > b.cost; });
+    for (int i = 0; i < n; ++i) work[i] = tmp[i].v;
+    return n;
+}
+
 static te_status attn_launch(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off, int32_t v_off,
                              const int32_t *cu_dev, const int32_t *items_dev, int32_t units, int32_t total,
-                             int32_t max_len, int32_t nq_heads, int32_t nkv_heads, int32_t hd,
-                             int32_t window, float scale, void *out, int64_t ldo, te_stream stream) {
+                             int32_t max_len, const int32_t *unit_lens, int32_t nq_heads, int32_t nkv_heads,
+                             int32_t hd, int32_t window, float scale, void *out, int64_t ldo, te_stream stream) {
     {
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(qkv);
         const uintptr_t a1 = a0 + (uintptr_t)total * ld * 2;
@@ -497,6 +538,7 @@ static te_status attn_launch(const void *qkv, int64_t ld, int32_t q_off, int32_t
     p.group = nq_heads / nkv_heads;
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.nwork = build_work(unit_lens, units, window, p.work);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return hd == 64 ? launch<64>(p, max_len, nq_heads, units, s)
                     : launch<128>(p, max_len, nq_heads, units, s);
@@ -512,8 +554,10 @@ extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_o
     if (nseq > 65535) return fail(TE_ESHAPE, "attn: too many sequences");
     int32_t total = 0, max_len = 0;
     if ((st = check_cu(cu_host, cu_dev, nseq, &total, &max_len)) != TE_OK) return st;
-    return attn_launch(qkv, ld, q_off, k_off, v_off, cu_dev, nullptr, nseq, total, max_len, nq_heads,
-                       nkv_heads, hd, window, scale, out, ldo, stream);
+    std::vector<int32_t> lens(nseq);
+    for (int32_t i = 0; i < nseq; ++i) lens[i] = cu_host[i + 1] - cu_host[i];
+    return attn_launch(qkv, ld, q_off, k_off, v_off, cu_dev, nullptr, nseq, total, max_len, lens.data(),
+                       nq_heads, nkv_heads, hd, window, scale, out, ldo, stream);
 }
 
 extern "C" te_status te_attn_items_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off,
@@ -528,6 +572,7 @@ extern "C" te_status te_attn_items_fwd(const void *qkv, int64_t ld, int32_t q_of
     if (rows < 1) return fail(TE_ESHAPE, "attn_items: rows=%d", rows);
     if (reinterpret_cast<uintptr_t>(items_dev) & 15) return fail(TE_EALIGN, "attn_items: items must be 16-byte aligned");
     int32_t max_len = 0;
+    std::vector<int32_t> lens(nitems);
     for (int32_t i = 0; i < nitems; ++i) {
         const int32_t o1 = items_host[4 * i], l1 = items_host[4 * i + 1];
         const int32_t o2 = items_host[4 * i + 2], l2 = items_host[4 * i + 3];
@@ -538,7 +583,8 @@ extern "C" te_status te_attn_items_fwd(const void *qkv, int64_t ld, int32_t q_of
             return fail(TE_ESHAPE, "attn_items: item %d: the first range's length %d is not a multiple of 32", i, l1);
         if ((int64_t)l1 + l2 > (1 << 30)) return fail(TE_ESHAPE, "attn_items: item %d too long", i);
         if (l1 + l2 > max_len) max_len = l1 + l2;
+        lens[i] = l1 + l2;
     }
-    return attn_launch(qkv, ld, q_off, k_off, v_off, nullptr, items_dev, nitems, rows, max_len, nq_heads,
-                       nkv_heads, hd, window, scale, out, ldo, stream);
+    return attn_launch(qkv, ld, q_off, k_off, v_off, nullptr, items_dev, nitems, rows, max_len, lens.data(),
+                       nq_heads, nkv_heads, hd, window, scale, out, ldo, stream);
 }
