@@ -104,7 +104,11 @@ struct Layout {
     // epilogue staging: ungated, one 32 x 32 output tile (f32 or bf16) per
     // epilogue warp; gated, one padded 32 x 33 f32 exchange block per warp and
     // a 16 x 32 bf16 output tile per warp.  128-byte aligned (TMA sources).
-    static constexpr int STG_OFF = W_OFF + NST * WBYTES;
+    // q8_2f: each stage's 128 column-field values (f32), for the gate and the
+    // up weight in the gated form
+    static constexpr int COL_OFF = W_OFF + NST * WBYTES;
+    static constexpr int COL_BYTES = 2 * BK * 4;
+    static constexpr int STG_OFF = COL_OFF + NST * COL_BYTES;
     static constexpr int XCHG_BYTES = 4 * 32 * 33 * 4;
     static constexpr int STG_BYTES = XCHG_BYTES + 4 * 1024;
     static_assert(4 * 4096 <= STG_BYTES && XCHG_BYTES % 128 == 0, "staging");
@@ -296,10 +300,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             for (int u = cid; u < nunits && ok; u += ncl) {
                 const TileCoord tc = tile_coord<GATED>(p, u, rank);
                 const void *wmap = &p.tw[tc.zi];
+                const float *cg = p.it[tc.zi].col, *cu2 = GATED ? p.it[tc.zi].col2 : nullptr;
                 for (int kb = 0; kb < nkb; ++kb, ++kbg) {
                     const int s = kbg % NST;
                     if (!mbar_wait(bar_empty + 8 * s, ((kbg / NST) & 1) ^ 1)) { ok = false; break; }
-                    mbar_arrive_expect_tx(bar_full + 8 * s, L::XBYTES + L::WBYTES);
+                    // the column field slice of this stage (the last stage may hold 64)
+                    const uint32_t cbytes = (uint32_t)((p.k - kb * BK < BK ? p.k - kb * BK : BK) * 4);
+                    mbar_arrive_expect_tx(bar_full + 8 * s, L::XBYTES + L::WBYTES + (cg ? cbytes : 0) +
+                                                                (cu2 ? cbytes : 0));
+                    if (cg) bulk_load(sb + L::COL_OFF + s * L::COL_BYTES, cg + kb * BK, cbytes, bar_full + 8 * s);
+                    if (cu2)
+                        bulk_load(sb + L::COL_OFF + s * L::COL_BYTES + BK * 4, cu2 + kb * BK, cbytes,
+                                  bar_full + 8 * s);
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const uint32_t wdst = sb + L::W_OFF + s * L::WBYTES + c * L::WBOX;
@@ -392,9 +404,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 const int sw = (row >> 1) & 3;
                 uint32_t r[32];
                 if (colp) {
-                    // column field of K = kb*128 + h*64 + 16c + e (zero past k: the
-                    // weight reads zeros there too)
+                    // column field of K = kb*128 + h*64 + 16c + e, staged with the
+                    // weight tile (zero past k: the weight reads zeros there too)
                     const int k0 = kb * BK + h * BOX;
+                    const float *cs = reinterpret_cast<const float *>(smem + L::COL_OFF + s * L::COL_BYTES) +
+                                      (GATED && row >= BM / 2 ? BK : 0) + h * BOX;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint4 v = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw) << 4));
@@ -402,7 +416,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             cv[e] = k0 + 16 * c + 4 * e < p.k
-                                        ? __ldg(reinterpret_cast<const float4 *>(colp + k0 + 16 * c + 4 * e))
+                                        ? *reinterpret_cast<const float4 *>(cs + 16 * c + 4 * e)
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                         widen4_col(v.x, cv[0], r[8 * c + 0], r[8 * c + 1]);
                         widen4_col(v.y, cv[1], r[8 * c + 2], r[8 * c + 3]);

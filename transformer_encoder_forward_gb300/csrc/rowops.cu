@@ -367,15 +367,16 @@ __global__ void __launch_bounds__(256) cast_bf16_kernel(const float *__restrict_
 
 // ------------------------------------------------------------- qk prep + RoPE
 
-// One warp per (packed row, group of QK_U * 32 / (HD / 8) heads).  Each lane
+// One warp per (packed row, group of 4 * 32 / (HD / 8) heads).  Each lane
 // owns 8 consecutive channels (one 16-byte load); a head of HD channels spans
 // HD/8 lanes, so the per-head RMS is a reduction over an aligned lane group and
 // the RoPE partner (channel +-sec/2 in the same section) sits in lane
-// (l ^ sec/16) at the same offset.  The warp issues all QK_U loads of its
-// group before any arithmetic, so QK_U 16-byte loads per lane are in flight
-// (a loop of load -> norm -> store per head pair waited a full memory latency
-// per iteration).
-constexpr int QK_U = 4;
+// (l ^ sec/16) at the same offset.  The warp issues all loads of its group
+// before any arithmetic (4 16-byte loads per lane in flight; a loop of
+// load -> norm -> store per head pair waited a full memory latency per
+// iteration; 8 in flight measured slower at 60 heads x 128).
+template <int HD>
+__host__ __device__ constexpr int qk_u() { return 4; }   // 4 loads per lane in flight
 
 template <int HD>
 __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long long ld, int q_off,
@@ -388,6 +389,7 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
                                                       int sec, float q_mul, int rows) {
     constexpr int LPH = HD / 8;                 // lanes per head
     constexpr int HPI = 32 / LPH;               // heads per load slot
+    constexpr int QK_U = qk_u<HD>();
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -741,7 +743,7 @@ te_status te_qkv_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, 
         return fail(TE_EINVAL, "qk_prep_rope: give both qn and kn or neither");
     const int nv = v_norm ? nkv : 0;
     if (rows == 0 || nq + nkv + nv == 0) return TE_OK;
-    const int heads_per_warp = (32 / (hd / 8)) * QK_U;
+    const int heads_per_warp = (32 / (hd / 8)) * (hd == 128 ? qk_u<128>() : qk_u<64>());
     const dim3 grid((unsigned)(((long long)rows + 7) / 8),
                     (unsigned)((nq + nkv + nv + heads_per_warp - 1) / heads_per_warp));
     if (hd == 64)
