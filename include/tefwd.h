@@ -245,6 +245,14 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
                           int32_t table_rows, int32_t sec, float q_mul, int32_t rows,
                           te_stream stream);
 
+/* selftest_wait_timeout: launches one kernel whose mbarrier wait can never
+ * complete, bounded like every pipeline wait of the library but after
+ * limit_us microseconds (1..1e6).  The kernel then records the same error a
+ * stuck pipeline records and returns: the next te_check reports TE_EDEVICE
+ * (and clears it) and the context stays usable.  No fault is involved.  The
+ * pages have no counterpart of this entry point. */
+te_status te_selftest_wait_timeout(int32_t limit_us, te_stream stream);
+
 /* cast_bf16: y = bf16(x) (round to nearest even) for x f32 [rows, d] (ldx),
  * y bf16 [rows, ldy]; d % 8 == 0.  The per-layer input path's GEMM reads the
  * residual stream this way. */

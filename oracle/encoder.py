@@ -27,7 +27,7 @@ projections that feed a norm are f32; normed activations, the q|k|v panel,
 the attention output, the gate|up output and the FFN hidden are bf16
 (round-to-nearest-even).  Everything between two storage points is f64 here.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent or ambiguous:
 RMSNorm multiplies by the stored weight (not 1 + w) with eps inside the root;
 LayerNorm uses the biased variance; a key j is visible to query i iff both
 lie in the same sequence and (window == 0 or |i - j| <= window); q/k norm is

@@ -50,6 +50,10 @@ GEMM_CASES = [
     # a residual other than y (f32 and bf16 y), rows wider than n
     (300, 512, [96, 160], True, "sep", "f32"),
     (777, 256, [256, 512], False, "sep", "bf16"),
+    # resident weights over long runs of token tiles that cross feature pairs
+    (5000, 512, [512, 512, 512], False, False, "bf16"),
+    (5000, 512, [512], True, True, "f32"),
+    (6001, 448, [1536], False, False, "bf16"),
 ]
 
 
@@ -131,7 +135,8 @@ def test_int8_widening_and_indexing_are_bit_exact():
                                             (1000, 512, 2048, "gelu_tanh", True),
                                             (2112, 3840, 10240, "silu", False),
                                             (101, 256, 96, "silu", True),
-                                            (300, 192, 32, "gelu_tanh", False)])
+                                            (300, 192, 32, "gelu_tanh", False),
+                                            (5000, 512, 2048, "gelu_tanh", False)])
 def test_gated_linear_matches_oracle(m, k, f, act, bias):
     # m = act(bf16(g)) * bf16(u): the same storage points as the g|u panel
     # followed by the gate, without the panel

@@ -85,6 +85,7 @@ EXPORTS = {
     "te_qkv_prep_rope": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_p,
                                         c_p, c_i32, c_f32, c_p, c_p, c_p, c_i32, c_i32, c_f32, c_i32,
                                         c_p]),
+    "te_selftest_wait_timeout": (ctypes.c_int, [c_i32, c_p]),
     "te_cast_bf16": (ctypes.c_int, [c_p, c_i64, c_p, c_i64, c_i32, c_i32, c_p]),
     "te_gate_act": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_i64, c_i32, c_i32, c_p]),
     "te_pool_mean": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_i32, c_p, c_f32, c_p, c_p]),
@@ -205,6 +206,11 @@ def attn_items_fwd(qkv, ld, q_off, k_off, v_off, items_host, items_dev, rows, nq
     _ok(lib().te_attn_items_fwd(qkv.data_ptr(), ld, q_off, k_off, v_off, arr.ctypes.data_as(c_p),
                                 items_dev.data_ptr(), arr.shape[0], rows, nq, nkv, hd, window, scale,
                                 out.data_ptr(), ldo, _stream(stream)))
+
+
+def selftest_wait_timeout(limit_us, stream=None):
+    """Launch the bounded-wait self-test (a wait that can only time out)."""
+    _ok(lib().te_selftest_wait_timeout(limit_us, _stream(stream)))
 
 
 def cast_bf16(x, y, stream=None):

@@ -38,6 +38,13 @@
 //     residual is y itself, the in-place x += proj of the plain block).
 // With long K a unit can hold two token tiles: each widened weight stage then
 // feeds both tiles' MMAs (see tokens_per_stage).
+// With short K (every K stage fits the TMEM A stages at once) the weights stay
+// resident: each cluster takes a contiguous run of units, which share their
+// feature tiles except where the run crosses into the next feature pair; the
+// converters widen a feature tile once, and later units of the run only
+// stream activations.  The peer's warp 1 relays each of its landed stages to
+// the leader's full barrier (which then counts two arrivals), so the MMA
+// issuer waits on one barrier per stage.
 // TMEM: 2 accumulators of BN columns + as many A stages of 64 columns as fit
 // in the 512 (2 for BN = 192, 3 for 160, 4 for 128 and 64).  A stage is 8 MMAs deep, so the barrier round trip between
 // stages (about 0.1-0.2 us for the issuing thread) is amortised over 768
@@ -82,6 +89,7 @@ struct Params {
     Item it[MAXZ];
     int z, m, k, ttiles, nunits;
     int kb32;                 // k / 32: the row stride of the block scales
+    int res;                  // resident weights (see q8_gemm_kernel)
 };
 
 __device__ int g_gemm_err;
@@ -119,6 +127,7 @@ struct Layout {
     static constexpr int A_COL = 2 * BN;                // first TMEM column of the A stages
     static constexpr int TMEM_COLS = 512;
     static_assert(NA >= 2 && 2 * BN + NA * 64 <= TMEM_COLS, "TMEM budget");
+    static_assert(NA < NST, "a free A stage proves the ring passed the slot's previous use");
     static_assert(XBOX % 1024 == 0, "swizzled boxes stay 1024-byte aligned");
     static_assert(BYTES + 1024 <= 227 * 1024, "shared memory per CTA");
 };
@@ -260,13 +269,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const int rank = (int)cluster_rank();
     const bool leader = rank == 0;
     const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const bool res = p.res != 0;
     // once any CTA has given up a wait, the rest skip their work (the call
     // has failed; te_check reports it) instead of timing out one by one
     __shared__ int s_skip;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            // resident weights: the leader's full barriers also take the peer's relay
+            mbar_init(bar_full + 8 * s, res && leader ? 2 : 1);
             mbar_init(bar_empty + 8 * s, 1);      // the leader's MMA commit, multicast
         }
         for (int a = 0; a < NA; ++a) {
@@ -291,40 +302,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // the leader's copies of the pair-wide barriers, as cluster addresses
     const uint32_t afull_ldr = mapa_shared(bar_afull, 0);
     const uint32_t accempty_ldr = mapa_shared(bar_accempty, 0);
+    const uint32_t full_ldr = mapa_shared(bar_full, 0);
+    // this cluster's units: a contiguous run with resident weights, else
+    // every ncl-th unit from cid
+    const int ubeg = res ? (int)((long long)cid * nunits / ncl) : cid;
+    const int ucnt = res ? (int)((long long)(cid + 1) * nunits / ncl) - ubeg
+                         : (cid < nunits ? (nunits - 1 - cid) / ncl + 1 : 0);
+    auto unit_at = [&](int i) { return res ? ubeg + i : cid + i * ncl; };
+    // whether unit i of the run widens its weights: always without resident
+    // weights, else at the run's start and where the feature pair changes
+    auto fills = [&](int i) {
+        return !res || i == 0 || unit_at(i) / p.ttiles != unit_at(i - 1) / p.ttiles;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&p.tx);
             int kbg = 0;
-            for (int u = cid; u < nunits && ok; u += ncl) {
+            for (int i = 0; i < ucnt && ok; ++i) {
+                const int u = unit_at(i);
+                const bool fl = fills(i);   // weights (and column field) only when widened
                 const TileCoord tc = tile_coord<GATED>(p, u, rank);
                 const void *wmap = &p.tw[tc.zi];
-                const float *cg = p.it[tc.zi].col, *cu2 = GATED ? p.it[tc.zi].col2 : nullptr;
+                const float *cg = fl ? p.it[tc.zi].col : nullptr;
+                const float *cu2 = GATED && fl ? p.it[tc.zi].col2 : nullptr;
                 for (int kb = 0; kb < nkb; ++kb, ++kbg) {
                     const int s = kbg % NST;
+                    const uint32_t fb = bar_full + 8 * s;
                     if (!mbar_wait(bar_empty + 8 * s, ((kbg / NST) & 1) ^ 1)) { ok = false; break; }
                     // the column field slice of this stage (the last stage may hold 64)
                     const uint32_t cbytes = (uint32_t)((p.k - kb * BK < BK ? p.k - kb * BK : BK) * 4);
-                    mbar_arrive_expect_tx(bar_full + 8 * s, L::XBYTES + L::WBYTES + (cg ? cbytes : 0) +
-                                                                (cu2 ? cbytes : 0));
-                    if (cg) bulk_load(sb + L::COL_OFF + s * L::COL_BYTES, cg + kb * BK, cbytes, bar_full + 8 * s);
-                    if (cu2)
-                        bulk_load(sb + L::COL_OFF + s * L::COL_BYTES + BK * 4, cu2 + kb * BK, cbytes,
-                                  bar_full + 8 * s);
+                    mbar_arrive_expect_tx(fb, L::XBYTES + (fl ? L::WBYTES : 0) + (cg ? cbytes : 0) +
+                                                  (cu2 ? cbytes : 0));
+                    if (cg) bulk_load(sb + L::COL_OFF + s * L::COL_BYTES, cg + kb * BK, cbytes, fb);
+                    if (cu2) bulk_load(sb + L::COL_OFF + s * L::COL_BYTES + BK * 4, cu2 + kb * BK, cbytes, fb);
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const uint32_t wdst = sb + L::W_OFF + s * L::WBYTES + c * L::WBOX;
 #pragma unroll
                         for (int tt = 0; tt < TPA; ++tt)
                             tma_load_2d(sb + L::X_OFF + s * L::XBYTES + tt * L::XTILE + c * L::XBOX, &p.tx,
-                                        bar_full + 8 * s, kb * BK + c * BOX, (tc.t0 * TPA + tt) * BN + rank * HALF);
+                                        fb, kb * BK + c * BOX, (tc.t0 * TPA + tt) * BN + rank * HALF);
+                        if (!fl) continue;
                         if (GATED) {   // rows 0-63: gate, rows 64-127: up, same features
-                            tma_load_2d(wdst, &p.tw[0], bar_full + 8 * s, kb * BK + c * BOX, tc.o0);
-                            tma_load_2d(wdst + (BM / 2) * BOX, &p.tw[1], bar_full + 8 * s,
-                                        kb * BK + c * BOX, tc.o0);
+                            tma_load_2d(wdst, &p.tw[0], fb, kb * BK + c * BOX, tc.o0);
+                            tma_load_2d(wdst + (BM / 2) * BOX, &p.tw[1], fb, kb * BK + c * BOX, tc.o0);
                         } else {
-                            tma_load_2d(wdst, wmap, bar_full + 8 * s, kb * BK + c * BOX, tc.o0);
+                            tma_load_2d(wdst, wmap, fb, kb * BK + c * BOX, tc.o0);
                         }
                     }
                 }
@@ -337,8 +362,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // -------------------------------------- MMA issuer (leader CTA only)
         if (lane == 0 && leader) {
             constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
-            int kbg = 0, lt = 0;
-            for (int u = cid; u < nunits && ok; u += ncl, ++lt) {
+            int kbg = 0, nfill = 0;
+            for (int lt = 0; lt < ucnt && ok; ++lt) {
+                const bool fl = fills(lt);
+                // resident weights: the A stages are released after the last
+                // unit that uses this widening
+                const bool last_use = !res || lt + 1 == ucnt || fills(lt + 1);
                 // TPA == 1: units alternate between the two accumulators;
                 // TPA == 2: a unit's two token tiles use both
                 const int b = TPA == 2 ? 0 : (lt & 1);
@@ -346,10 +375,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 if (!mbar_wait_cluster(bar_accempty + 8 * b, ph ^ 1)) { ok = false; break; }
                 tc_fence_after();
                 for (int kb = 0; kb < nkb; ++kb, ++kbg) {
-                    const int s = kbg % NST, a = kbg % NA;
+                    const int s = kbg % NST, a = res ? kb : kbg % NA;
+                    // resident weights: both CTAs' stages s have landed (our
+                    // copies, and the peer's as relayed by its warp 1)
+                    if (res && !mbar_wait_cluster(bar_full + 8 * s, (kbg / NST) & 1)) {
+                        ok = false;
+                        break;
+                    }
                     // both CTAs' converters have widened stage a, which they
                     // only do once their own TMA stage s has landed
-                    if (!mbar_wait_cluster(bar_afull + 8 * a, (kbg / NA) & 1)) { ok = false; break; }
+                    if (fl && !mbar_wait_cluster(bar_afull + 8 * a, res ? (nfill & 1) : ((kbg / NA) & 1))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t xs = sb + L::X_OFF + s * L::XBYTES;
 #pragma unroll
@@ -360,13 +398,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                         smem_desc_sw128(xs + tt * L::XTILE + (j >> 2) * L::XBOX + (j & 3) * 32),
                                         idesc, (kb | j) != 0);
                     mma_commit_pair(bar_empty + 8 * s, 0x3);
-                    mma_commit_pair(bar_aempty + 8 * a, 0x3);
+                    if (last_use) mma_commit_pair(bar_aempty + 8 * a, 0x3);
                 }
+                if (fl) ++nfill;
                 if (ok) mma_commit_pair(bar_accfull + 8 * b, 0x3);
             }
             // every MMA issued above has completed once this fires
             mma_commit_pair(bar_done, 0x1);
             mbar_wait(bar_done, 0, 20000000ull);
+        } else if (lane == 0 && res) {
+            // the peer's relay: each of its stages has landed
+            int kbg = 0;
+            for (int i = 0; i < ucnt && ok; ++i)
+                for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+                    const int s = kbg % NST;
+                    if (!mbar_wait(bar_full + 8 * s, (kbg / NST) & 1)) { ok = false; break; }
+                    mbar_arrive_cluster_relaxed(full_ldr + 8 * s);
+                }
         }
     } else if (warp < 10) {
         // -------------------------------- widen int8 -> bf16 into TMEM (A)
@@ -374,8 +422,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const int h = (warp - 2) >> 2;                 // which 64 of the 128 K columns (TMA box)
         const int row = 32 * q + lane;                 // weight row within the tile
         const uint32_t tl = (uint32_t)(32 * q) << 16;
-        int kbg = 0;
-        for (int u = cid; u < nunits && ok; u += ncl) {
+        int kbg = 0, nfill = 0;
+        for (int i = 0; i < ucnt && ok; ++i) {
+            if (!fills(i)) { kbg += nkb; continue; }   // resident weights: nothing to widen
+            const int u = unit_at(i);
             // the 32-element block formats: this row's f16 block scales (the
             // item is uniform over the warp: a warp's 32 rows share it)
             const uint16_t *bsr = nullptr;
@@ -391,13 +441,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 if (blk && o < p.it[tc.zi].n) bsr = b + (long long)o * p.kb32;
             }
             for (int kb = 0; kb < nkb; ++kb, ++kbg) {
-                const int s = kbg % NST, a = kbg % NA;
+                const int s = kbg % NST, a = res ? kb : kbg % NA;
                 // blocks 4 kb + 2 h and the next one (issued before the waits)
                 uint32_t dd = 0;
                 const int j0 = kb * 4 + h * 2;
                 if (bsr && j0 < p.kb32) dd = *reinterpret_cast<const uint32_t *>(bsr + j0);
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8 * s, (kbg / NST) & 1) &&
-                                                 mbar_wait(bar_aempty + 8 * a, ((kbg / NA) & 1) ^ 1));
+                const uint32_t apar = res ? (nfill & 1) ^ 1 : ((kbg / NA) & 1) ^ 1;
+                // A stage a free first: then the MMAs of chunk kbg - nkb (resident
+                // weights) or kbg - NA are done, so the ring has passed the
+                // previous use of this chunk's slot and the parity wait on its
+                // full barrier cannot match a phase two behind (the converters
+                // skip the units that widen nothing)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_aempty + 8 * a, apar) &&
+                                                 mbar_wait(bar_full + 8 * s, (kbg / NST) & 1));
                 if (!ok) break;
                 tc_fence_after();
                 const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + h * L::WBOX + row * 64;
@@ -451,6 +507,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster_relaxed(afull_ldr + 8 * a);
             }
+            ++nfill;
         }
     } else {
         // ----------------------------------------------------------- epilogue
@@ -470,7 +527,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const uint32_t ostg = sb + ostg_off;                 // the TMA source (shared address)
         float *ostg_f = reinterpret_cast<float *>(smem + ostg_off);
         __nv_bfloat16 *ostg_h = reinterpret_cast<__nv_bfloat16 *>(smem + ostg_off);
-        for (int u = cid; u < nunits && ok; u += ncl, ++lt) {
+        for (; lt < ucnt && ok; ++lt) {
+            const int u = unit_at(lt);
             const int b = TPA == 2 ? 0 : (lt & 1);
             const uint32_t ph = TPA == 2 ? (lt & 1) : ((lt >> 1) & 1);
             // this tile's row scale and bias before the wait: their load
@@ -653,6 +711,19 @@ int tokens_per_stage(int m, int k, int ftiles) {
     return (double)w2 * 1.65 < (double)w1 ? 2 : 1;
 }
 
+// Token-tile width and whether the weights stay resident (every K stage in
+// the TMEM A stages at once: K <= 256 at BN = 192, K <= 512 at 128 and 64).
+// For 256 < K <= 512 the 128-wide tile with resident weights beats the
+// 192-wide one that re-widens each stage for every token tile.
+int pick_bn(int m, int k, int &res) {
+    int bn = m >= 1024 ? 192 : (m > 64 ? 128 : 64);
+    const int nkb = (k + BK - 1) / BK;
+    if (bn == 192 && nkb > Layout<192, 1>::NA && nkb <= Layout<128, 1>::NA) bn = 128;
+    const int na = bn == 192 ? Layout<192, 1>::NA : (bn == 128 ? Layout<128, 1>::NA : Layout<64, 1>::NA);
+    res = nkb <= na ? 1 : 0;
+    return bn;
+}
+
 template <int BN, bool GATED, int TPA>
 te_status launch(Params &p, int ftiles, cudaStream_t stream) {
     const int smem = Layout<BN, TPA>::BYTES + 1024;
@@ -804,8 +875,8 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         ftiles += d.ntiles;
     }
     if (m == 0) return TE_OK;
-    const int bn = m >= 1024 ? 192 : (m > 64 ? 128 : 64);
-    const int tpa = bn == 192 ? tokens_per_stage(m, k, ftiles) : 1;
+    const int bn = pick_bn(m, k, p.res);
+    const int tpa = bn == 192 && !p.res ? tokens_per_stage(m, k, ftiles) : 1;
     // each CTA of a cluster pair loads half of the token tile (and multicasts it)
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
                                (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -875,8 +946,8 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     d.tile0 = 0;
     d.ntiles = (f + BM / 2 - 1) / (BM / 2);
     if (m == 0) return TE_OK;
-    const int bn = m >= 1024 ? 192 : (m > 64 ? 128 : 64);
-    const int tpa = bn == 192 ? tokens_per_stage(m, k, d.ntiles) : 1;
+    const int bn = pick_bn(m, k, p.res);
+    const int tpa = bn == 192 && !p.res ? tokens_per_stage(m, k, d.ntiles) : 1;
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
                                (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_OK) return st;

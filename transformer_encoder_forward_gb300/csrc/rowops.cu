@@ -348,6 +348,21 @@ __global__ void __launch_bounds__(256) add_norm_wide_kernel(float *h, const floa
     }
 }
 
+// ------------------------------------------------------ bounded-wait check
+
+// Waits on an mbarrier that nothing arrives at, with the bounded wait every
+// pipeline kernel uses, but a short limit; when the wait gives up it records
+// error 1 in the row-op error word, exactly as a stuck pipeline would.
+__global__ void wait_timeout_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, limit_ns)) atomicExch(&g_rowop_err, 1);
+}
+
 // ---------------------------------------------------------------- cast bf16
 
 // Grid-stride over 8-column chunks: 32 bytes in, 16 bytes out.
@@ -378,7 +393,7 @@ __global__ void __launch_bounds__(256) cast_bf16_kernel(const float *__restrict_
 template <int HD>
 __host__ __device__ constexpr int qk_u() { return 4; }   // 4 loads per lane in flight
 
-template <int HD>
+template <int HD, bool VN>
 __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long long ld, int q_off,
                                                       int k_off, int v_off, int nq, int nkv, int nv,
                                                       const float *__restrict__ qn,
@@ -430,7 +445,7 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
         const int hh = hbase + u * HPI + hl;
         if (hh < nh) {
             const int col = hh < nq ? q_off + hh * HD
-                                    : (hh < nq + nkv ? k_off + (hh - nq) * HD : v_off + (hh - nq - nkv) * HD);
+                                    : (!VN || hh < nq + nkv ? k_off + (hh - nq) * HD : v_off + (hh - nq - nkv) * HD);
             const __nv_bfloat16 *p = qkv + row * ld + col + c0;
             raw[u] = *reinterpret_cast<const uint4 *>(p);
         } else {
@@ -442,19 +457,19 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
         const int hh = hbase + u * HPI + hl;
         const bool active = hh < nh;            // lane groups past the last head idle
         const bool isq = hh < nq;
-        const bool isv = hh >= nq + nkv;        // v heads: RMS norm without weight, no RoPE
+        const bool isv = VN && hh >= nq + nkv;  // v heads: RMS norm without weight, no RoPE
         float v[8];
         v[0] = bf16_lo(raw[u].x); v[1] = bf16_hi(raw[u].x); v[2] = bf16_lo(raw[u].y); v[3] = bf16_hi(raw[u].y);
         v[4] = bf16_lo(raw[u].z); v[5] = bf16_hi(raw[u].z); v[6] = bf16_lo(raw[u].w); v[7] = bf16_hi(raw[u].w);
         const float *nw = isq ? qn : kn;
-        if (qn || nv) {                         // uniform: qn and kn are both given or both NULL
+        if (qn || VN) {                         // uniform: qn and kn are both given or both NULL
             float q = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) q += v[e] * v[e];
 #pragma unroll
             for (int o = 1; o < LPH; o <<= 1) q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
             const float inv = rsqrtf(q / (float)HD + eps);
-            if (active && isv) {
+            if (VN && active && isv) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] *= inv;
             } else if (active && qn) {
@@ -471,7 +486,7 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
                 const float partner = __shfl_xor_sync(0xFFFFFFFFu, v[e], xr);
                 o[e] = first_half ? v[e] * cv[e] - partner * sv[e] : v[e] * cv[e] + partner * sv[e];
             }
-            if (!isv) {
+            if (!VN || !isv) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] = o[e];
             }
@@ -481,7 +496,8 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
             uint4 w;
             w.x = pack_bf16x2(v[0] * mul, v[1] * mul); w.y = pack_bf16x2(v[2] * mul, v[3] * mul);
             w.z = pack_bf16x2(v[4] * mul, v[5] * mul); w.w = pack_bf16x2(v[6] * mul, v[7] * mul);
-            const int col = isq ? q_off + hh * HD : (isv ? v_off + (hh - nq - nkv) * HD : k_off + (hh - nq) * HD);
+            const int col = isq ? q_off + hh * HD
+                                : (VN && isv ? v_off + (hh - nq - nkv) * HD : k_off + (hh - nq) * HD);
             __nv_bfloat16 *p = qkv + row * ld + col + c0;
             *reinterpret_cast<uint4 *>(p) = w;
         }
@@ -746,14 +762,15 @@ te_status te_qkv_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, 
     const int heads_per_warp = (32 / (hd / 8)) * (hd == 128 ? qk_u<128>() : qk_u<64>());
     const dim3 grid((unsigned)(((long long)rows + 7) / 8),
                     (unsigned)((nq + nkv + nv + heads_per_warp - 1) / heads_per_warp));
+    auto go = [&](auto kern) {
+        kern<<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, v_off, nq, nkv, nv, qn, kn, eps,
+                                       cos, sin, pos, table_rows, sec, q_mul, rows);
+    };
+    // the v-norm heads in their own instantiation: the q/k pass keeps its code
     if (hd == 64)
-        qk_prep_kernel<64><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, v_off, nq,
-                                                     nkv, nv, qn, kn, eps, cos, sin, pos, table_rows,
-                                                     sec, q_mul, rows);
+        nv ? go(qk_prep_kernel<64, true>) : go(qk_prep_kernel<64, false>);
     else
-        qk_prep_kernel<128><<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, v_off, nq,
-                                                      nkv, nv, qn, kn, eps, cos, sin, pos, table_rows,
-                                                      sec, q_mul, rows);
+        nv ? go(qk_prep_kernel<128, true>) : go(qk_prep_kernel<128, false>);
     return launched("qk_prep_rope launch");
 }
 
@@ -764,6 +781,12 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
                           te_stream stream) {
     return te_qkv_prep_rope(qkv, ld, q_off, k_off, 0, nq, nkv, hd, qn, kn, 0, eps, cos, sin, pos,
                             table_rows, sec, q_mul, rows, stream);
+}
+
+te_status te_selftest_wait_timeout(int32_t limit_us, te_stream stream) {
+    if (limit_us < 1 || limit_us > 1000000) return fail(TE_EINVAL, "selftest: limit_us=%d (1..1000000)", limit_us);
+    wait_timeout_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_us * 1000ull);
+    return launched("selftest launch");
 }
 
 te_status te_cast_bf16(const float *x, int64_t ldx, void *y, int64_t ldy, int32_t rows, int32_t d,
