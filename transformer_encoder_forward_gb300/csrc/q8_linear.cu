@@ -362,7 +362,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // -------------------------------------- MMA issuer (leader CTA only)
         if (lane == 0 && leader) {
             constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
-            int kbg = 0, nfill = 0;
+            // this thread's instruction rate bounds the MMA rate at N <= 192
+            // (one 2-SM MMA every ~45 cycles at best), so the loop keeps its
+            // indices incremental: ring slot s and A stage ar with their phases
+            int nfill = 0, s = 0, ar = 0;
+            uint32_t sph = 0, aph = 0;
             for (int lt = 0; lt < ucnt && ok; ++lt) {
                 const bool fl = fills(lt);
                 // resident weights: the A stages are released after the last
@@ -374,31 +378,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 const uint32_t ph = TPA == 2 ? (lt & 1) : ((lt >> 1) & 1);
                 if (!mbar_wait_cluster(bar_accempty + 8 * b, ph ^ 1)) { ok = false; break; }
                 tc_fence_after();
-                for (int kb = 0; kb < nkb; ++kb, ++kbg) {
-                    const int s = kbg % NST, a = res ? kb : kbg % NA;
+                const uint32_t dcol = tbase + (TPA == 2 ? 0 : b) * BN;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const int a = res ? kb : ar;
                     // resident weights: both CTAs' stages s have landed (our
                     // copies, and the peer's as relayed by its warp 1)
-                    if (res && !mbar_wait_cluster(bar_full + 8 * s, (kbg / NST) & 1)) {
+                    if (res && !mbar_wait_cluster(bar_full + 8 * s, sph)) {
                         ok = false;
                         break;
                     }
                     // both CTAs' converters have widened stage a, which they
                     // only do once their own TMA stage s has landed
-                    if (fl && !mbar_wait_cluster(bar_afull + 8 * a, res ? (nfill & 1) : ((kbg / NA) & 1))) {
+                    if (fl && !mbar_wait_cluster(bar_afull + 8 * a, res ? (nfill & 1) : aph)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t xs = sb + L::X_OFF + s * L::XBYTES;
+                    // descriptors: the stage's base plus constant offsets (the
+                    // start-address field cannot carry: shared memory < 256 KB)
+                    const uint64_t d0 = smem_desc_sw128(sb + L::X_OFF + s * L::XBYTES);
+                    const uint32_t a0 = tbase + L::A_COL + 64 * a;
+                    const uint32_t acc0 = kb != 0;
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)
 #pragma unroll
                         for (int tt = 0; tt < TPA; ++tt)
-                            mma_ts_pair(tbase + (TPA == 2 ? tt : b) * BN, tbase + L::A_COL + 64 * a + 8 * j,
-                                        smem_desc_sw128(xs + tt * L::XTILE + (j >> 2) * L::XBOX + (j & 3) * 32),
-                                        idesc, (kb | j) != 0);
+                            mma_ts_pair(dcol + tt * BN, a0 + 8 * j,
+                                        d0 + (uint64_t)((tt * L::XTILE + (j >> 2) * L::XBOX + (j & 3) * 32) >> 4),
+                                        idesc, j == 0 ? acc0 : 1u);
                     mma_commit_pair(bar_empty + 8 * s, 0x3);
                     if (last_use) mma_commit_pair(bar_aempty + 8 * a, 0x3);
+                    if (++s == NST) { s = 0; sph ^= 1u; }
+                    if (!res && ++ar == NA) { ar = 0; aph ^= 1u; }
                 }
                 if (fl) ++nfill;
                 if (ok) mma_commit_pair(bar_accfull + 8 * b, 0x3);
