@@ -82,6 +82,24 @@ __device__ __forceinline__ float apply_act(float g, int act) {
     return g * hw_rcp(1.f + hw_exp2(t));
 }
 
+// The same activations through the hardware tanh, one special-function op
+// instead of two: 0.5 g (1 + tanh z) for GELU-tanh, 0.5 g (1 + tanh(g/2))
+// for SiLU (g sigma(g) = 0.5 g (1 + tanh(g/2))).  tanh.approx has a relative
+// error near 2^-11, below the bf16 rounding of the result; the GEMM epilogue
+// uses it, where the special-function unit bounds the drain of the gate.
+__device__ __forceinline__ float hw_tanh(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float apply_act_tanh(float g, int act) {
+    const float z = act == TE_ACT_GELU_TANH
+                        ? g * fmaf(0.035677408f, g * g, 0.79788456f)   // sqrt(2/pi) (g + 0.044715 g^3)
+                        : 0.5f * g;
+    const float h = 0.5f * g;
+    return fmaf(h, hw_tanh(z), h);
+}
+
 // Rounds to the nearest bfloat16 (ties to even) and back: the value a bf16
 // store would keep.
 __device__ __forceinline__ float round_bf16(float v) {

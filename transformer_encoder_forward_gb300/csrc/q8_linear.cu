@@ -109,17 +109,14 @@ struct Layout {
     static constexpr int WBYTES = 2 * WBOX;             // int8 weight stage (own 128 rows)
     static constexpr int X_OFF = 0;
     static constexpr int W_OFF = NST * XBYTES;
-    // epilogue staging: ungated, one 32 x 32 output tile (f32 or bf16) per
-    // epilogue warp; gated, one padded 32 x 33 f32 exchange block per warp and
-    // a 16 x 32 bf16 output tile per warp.  128-byte aligned (TMA sources).
-    // q8_2f: each stage's 128 column-field values (f32), for the gate and the
-    // up weight in the gated form
+    // epilogue staging: one 32 x 32 output tile (f32 or bf16; gated, 32 tokens
+    // x 16 features of bf16) per epilogue warp, 128-byte aligned (TMA
+    // sources).  q8_2f: each stage's 128 column-field values (f32), for the
+    // gate and the up weight in the gated form
     static constexpr int COL_OFF = W_OFF + NST * WBYTES;
     static constexpr int COL_BYTES = 2 * BK * 4;
     static constexpr int STG_OFF = COL_OFF + NST * COL_BYTES;
-    static constexpr int XCHG_BYTES = 4 * 32 * 33 * 4;
-    static constexpr int STG_BYTES = XCHG_BYTES + 4 * 1024;
-    static_assert(4 * 4096 <= STG_BYTES && XCHG_BYTES % 128 == 0, "staging");
+    static constexpr int STG_BYTES = 4 * 4096;
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
     // barriers: full, empty [NST]; afull, aempty [NA]; accfull, accempty [2]; done
     static constexpr int NBAR = 2 * NST + 2 * NA + 4 + 1;
@@ -236,12 +233,6 @@ __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncol
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
-}
-
-// Named barrier between the two epilogue warps that hold the gate and the up
-// values of the same features (barrier ids 1 and 2; id 0 is __syncthreads).
-__device__ __forceinline__ void pair_sync(int pair) {
-    asm volatile("bar.sync %0, 64;" ::"r"(pair + 1) : "memory");
 }
 
 template <int BN, bool GATED, int TPA>
@@ -431,7 +422,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // -------------------------------- widen int8 -> bf16 into TMEM (A)
         const int q = warp & 3;                        // TMEM lane quadrant
         const int h = (warp - 2) >> 2;                 // which 64 of the 128 K columns (TMA box)
-        const int row = 32 * q + lane;                 // weight row within the tile
+        const int row = 32 * q + lane;                 // TMEM lane = row of the MMA tile
+        // gated: each lane quadrant holds 16 gate rows (lanes 0-15) and the
+        // same 16 features' up rows (lanes 16-31), so that one epilogue warp
+        // has both halves of its features; srow is the row in the loaded
+        // weight tile (gate rows 0-63, up rows 64-127)
+        const bool upper = GATED && (lane & 16);
+        const int srow = GATED ? (upper ? BM / 2 : 0) + 16 * q + (lane & 15) : row;
+        const int frow = GATED ? 16 * q + (lane & 15) : row;    // feature offset in the tile
         const uint32_t tl = (uint32_t)(32 * q) << 16;
         int kbg = 0, nfill = 0;
         for (int i = 0; i < ucnt && ok; ++i) {
@@ -444,8 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             bool blk = false;
             {
                 const TileCoord tc = tile_coord<GATED>(p, u, rank);
-                const bool upper = GATED && row >= BM / 2;
-                const int o = tc.o0 + (GATED ? (row & (BM / 2 - 1)) : row);
+                const int o = tc.o0 + frow;
                 const uint16_t *b = upper ? p.it[tc.zi].bsc2 : p.it[tc.zi].bsc;
                 colp = upper ? p.it[tc.zi].col2 : p.it[tc.zi].col;
                 blk = b != nullptr;
@@ -467,15 +464,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                                  mbar_wait(bar_full + 8 * s, (kbg / NST) & 1));
                 if (!ok) break;
                 tc_fence_after();
-                const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + h * L::WBOX + row * 64;
-                const int sw = (row >> 1) & 3;
+                const uint8_t *wrow = smem + L::W_OFF + s * L::WBYTES + h * L::WBOX + srow * 64;
+                const int sw = (srow >> 1) & 3;
                 uint32_t r[32];
                 if (colp) {
                     // column field of K = kb*128 + h*64 + 16c + e, staged with the
                     // weight tile (zero past k: the weight reads zeros there too)
                     const int k0 = kb * BK + h * BOX;
                     const float *cs = reinterpret_cast<const float *>(smem + L::COL_OFF + s * L::COL_BYTES) +
-                                      (GATED && row >= BM / 2 ? BK : 0) + h * BOX;
+                                      (upper ? BK : 0) + h * BOX;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint4 v = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw) << 4));
@@ -528,13 +525,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // tensor store - or a TMA reduce-add when the residual is y itself.
         const int q = warp & 3;
         const int row = 32 * q + lane;
+        // gated: lanes 0-15 hold the gate rows and lanes 16-31 the up rows of
+        // the warp's 16 features (the converters' interleaved layout)
+        const bool upper = GATED && (lane & 16);
+        const int frow = GATED ? 16 * q + (lane & 15) : row;
         const uint32_t tl = (uint32_t)(32 * q) << 16;
         int lt = 0;
-        __shared__ int s_pair_ok[2][4];
-        // gated: the exchange blocks of the gate/up warp pairs, then one
-        // 16-token output tile per warp; ungated: one 32-token tile per warp
-        float *xchg = reinterpret_cast<float *>(smem + L::STG_OFF);
-        const uint32_t ostg_off = L::STG_OFF + (GATED ? L::XCHG_BYTES + (warp - 10) * 1024 : (warp - 10) * 4096);
+        // staging: gated, one 32-token x 16-feature bf16 tile per warp;
+        // ungated, one 32 x 32 tile (f32 or bf16) per warp
+        const uint32_t ostg_off = L::STG_OFF + (warp - 10) * 4096;
         const uint32_t ostg = sb + ostg_off;                 // the TMA source (shared address)
         float *ostg_f = reinterpret_cast<float *>(smem + ostg_off);
         __nv_bfloat16 *ostg_h = reinterpret_cast<__nv_bfloat16 *>(smem + ostg_off);
@@ -545,21 +544,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // this tile's row scale and bias before the wait: their load
             // latency overlaps the mainloop
             const TileCoord tc = tile_coord<GATED>(p, u, rank);
-            const bool upper = GATED && row >= BM / 2;
-            const int o = tc.o0 + (GATED ? (row & (BM / 2 - 1)) : row);
+            const int o = tc.o0 + frow;
             const bool ov = o < p.it[tc.zi].n;
             const float *scale = upper ? p.it[tc.zi].scale2 : p.it[tc.zi].scale;
             const float *bias = upper ? p.it[tc.zi].bias2 : p.it[tc.zi].bias;
             const float sc = ov ? (scale ? scale[o] : 1.f) : 0.f;
             const float bi = (ov && bias) ? bias[o] : 0.f;
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_accfull + 8 * b, ph));
-            if (GATED) {
-                // the gate and up warps of a pair meet at named barriers below:
-                // they continue or stop together
-                if (lane == 0) s_pair_ok[lt & 1][q] = ok;
-                pair_sync(q & 1);
-                ok = ok && s_pair_ok[lt & 1][q ^ 2];
-            }
             if (!ok) break;
             tc_fence_after();
             const int act = p.it[tc.zi].act;
@@ -573,39 +564,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const int acol = (TPA == 2 ? tt : b) * BN;     // this token tile's accumulator
             const int t0 = (tc.t0 * TPA + tt) * BN;
             if (GATED) {
-                // warps q and q+2 hold the up and the gate values of the same
-                // 32 features (warp 10 + i holds quadrant (2 + i) & 3: the gate
-                // warps are 12, 13); both stage their bf16-rounded block, then
-                // each writes m = act(g) * u for 16 of the 32 tokens
-                float *stg = xchg + (warp - 10) * 32 * 33;
-                const float *stg_u = xchg + (q & 1) * 32 * 33;
-                const float *stg_g = stg_u + 2 * 32 * 33;
-                const int fo = tc.o0 + 32 * (q & 1);
-                const int jbase = q < 2 ? 0 : 16;
+                // per 32-token block: both halves bf16-rounded after scale and
+                // bias; gate lane l and up lane l + 16 swap half their tokens, so
+                // that lane l writes m = act(g) * u for tokens 0-15 and lane
+                // l + 16 for tokens 16-31 of feature 16 q + l
+                const int fo = tc.o0 + 16 * q;
+                const int jb = upper ? 16 : 0;
                 for (int c = 0; c < BN / 32; ++c) {
-                    if (t0 + 32 * c >= p.m) break;      // uniform over the pair
+                    if (t0 + 32 * c >= p.m) break;      // warp-uniform
                     uint32_t v[32];
                     tmem_ld32(tbase + tl + acol + 32 * c, v);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) stg[j * 33 + lane] = round_bf16(__uint_as_float(v[j]) * sc + bi);
-                    pair_sync(q & 1);
-                    const int tb = t0 + 32 * c + jbase;
-                    if (lane == 0) bulk_wait_read();       // the previous tile has left ostg
-                    __syncwarp();
                     float yv[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        yv[j] = apply_act(stg_g[(jbase + j) * 33 + lane], act) * stg_u[(jbase + j) * 33 + lane];
+                    for (int j = 0; j < 16; ++j) {
+                        const float lo = round_bf16(__uint_as_float(v[j]) * sc + bi);
+                        const float hi = round_bf16(__uint_as_float(v[16 + j]) * sc + bi);
+                        // the gate lane sends its token 16 + j, the up lane its token j
+                        const float got = __shfl_xor_sync(0xFFFFFFFFu, upper ? lo : hi, 16);
+                        // operands selected first: one activation per lane, no branch
+                        const float gv = upper ? got : lo, uv = upper ? hi : got;
+                        yv[j] = apply_act_tanh(gv, act) * uv;
+                    }
+                    if (lane == 0) bulk_wait_read();       // the previous tile has left ostg
+                    __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) ostg_h[j * 32 + lane] = __float2bfloat16_rn(yv[j]);
+                    for (int j = 0; j < 16; ++j) ostg_h[(jb + j) * 16 + (lane & 15)] = __float2bfloat16_rn(yv[j]);
                     fence_async_smem();
                     __syncwarp();
-                    if (lane == 0 && fo < n && tb < p.m) {
-                        tma_store_2d(ymap, ostg, fo, tb);
+                    if (lane == 0 && fo < n) {
+                        tma_store_2d(ymap, ostg, fo, t0 + 32 * c);
                         bulk_commit();
                     }
-                    pair_sync(q & 1);
                 }
             } else {
                 const int fo = tc.o0 + 32 * q;              // first feature of this warp's block
@@ -619,7 +609,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     if (act) {   // the ungated MLP: act(bf16(s*acc + b)), no residual
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            v[j] = __float_as_uint(apply_act(round_bf16(__uint_as_float(v[j]) * sc + bi), act - 1));
+                            v[j] = __float_as_uint(apply_act_tanh(round_bf16(__uint_as_float(v[j]) * sc + bi), act - 1));
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sc + bi);
@@ -968,9 +958,9 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     if ((st = make_map_2d(&p.tw[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, wu->q, (uint64_t)k, (uint64_t)f,
                           (uint64_t)k, BOX, BM / 2, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_OK)
         return st;
-    // each epilogue warp of a gate/up pair stores 16 of the 32 tokens of a block
+    // each epilogue warp stores 16 features x 32 tokens of a block
     if ((st = make_map_2d(&p.ty[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, (uint64_t)f, (uint64_t)m,
-                          (uint64_t)ldm * 2, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_OK)
+                          (uint64_t)ldm * 2, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (bn == 192) return tpa == 2 ? launch<192, true, 2>(p, d.ntiles, s) : launch<192, true, 1>(p, d.ntiles, s);
