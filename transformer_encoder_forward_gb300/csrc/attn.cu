@@ -13,11 +13,12 @@
 // max and sum, q pre-scaled so that the softmax is 2^(s - max)); "cera 0.2.4
 // src/model/vision_encoder_gpu.rs" (VitGpuOps::attention).
 //
-// GB300 design.  One CTA per (256 queries, head, sequence), as two 128-query
-// tiles A and B that share one stream of 128-key K/V tiles:
-//   * warp 9 (one lane) loads both Q tiles once and streams K and V tiles
-//     with TMA (128-byte swizzle, double-buffered);
-//   * warp 8 (one lane) issues the MMAs: S_w = Q_w K^T (tcgen05.mma kind::f16,
+// GB300 design.  At hd = 128 one CTA per (256 queries, head, sequence), as
+// two 128-query tiles A and B that share one stream of 128-key K/V tiles; at
+// hd = 64 one 128-query tile a CTA and two CTAs an SM (TL below):
+//   * the last warp (one lane) loads the Q tiles once and streams K and V
+//     tiles with TMA (128-byte swizzle, double-buffered);
+//   * the warp before it (one lane) issues the MMAs: S_w = Q_w K^T (tcgen05.mma kind::f16,
 //     M=128 N=128, both operands K-major in shared memory) into tile w's TMEM
 //     S buffer, and O_w += P_w V (A = P_w from TMEM, B = V as an MN-major
 //     shared-memory operand) into its TMEM O accumulator, in the order
@@ -48,9 +49,8 @@
 namespace tefwd {
 namespace {
 
-constexpr int BQ = 128;     // queries per tile (= TMEM lanes); two tiles per CTA
+constexpr int BQ = 128;     // queries per tile (= TMEM lanes); TL tiles per CTA
 constexpr int BKV = 128;    // keys per tile
-constexpr int NTHREADS = 320;
 constexpr int MAX_WORK = 640;   // work list entries carried in the launch parameters
 
 __device__ int g_attn_err;
@@ -68,21 +68,27 @@ struct AttnParams {
     float scale_log2;
 };
 
-template <int HD>
+// TL = query tiles per CTA: 2 (tiles A and B take turns at the exp pass,
+// one CTA per SM), or 1 (hd = 64: half the TMEM and 80 KB of shared memory,
+// so that two CTAs share an SM and one's loads and latencies overlap the
+// other's work - the short sequences of a text batch).
+template <int HD, int TL>
 struct ALayout {
     static constexpr int NB = HD / 64;              // 64-column boxes per tile row
     static constexpr int TILE = 128 * HD * 2;       // one 128-row tile
-    static constexpr int Q_OFF = 0;                 // Q[2] (tiles A, B)
-    static constexpr int K_OFF = 2 * TILE;          // K[2]
-    static constexpr int V_OFF = 4 * TILE;          // V[2]
-    static constexpr int BAR_OFF = 6 * TILE;
+    static constexpr int Q_OFF = 0;                 // Q[TL] (tiles A, B)
+    static constexpr int K_OFF = TL * TILE;         // K[2]
+    static constexpr int V_OFF = K_OFF + 2 * TILE;  // V[2]
+    static constexpr int BAR_OFF = V_OFF + 2 * TILE;
+    static constexpr int NTHREADS = 32 * (4 * TL + 2);   // softmax warps, MMA warp, TMA warp
+    static constexpr int MMA_WARP = 4 * TL, TMA_WARP = 4 * TL + 1;
     // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], fin, turn[2]
     static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 2;
     static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
-    static constexpr int S_COL = 0;                 // S_A, S_B: 2 x 128 f32 columns (P aliased)
-    static constexpr int O_COL = 256;               // O_A, O_B: 2 x HD f32 columns
-    static constexpr int COLS = 512;
-    static_assert(O_COL + 2 * HD <= COLS, "TMEM budget");
+    static constexpr int S_COL = 0;                 // S_A, S_B: TL x 128 f32 columns (P aliased)
+    static constexpr int O_COL = TL * 128;          // O_A, O_B: TL x HD f32 columns
+    static constexpr int COLS = TL == 1 ? 256 : 512;
+    static_assert(O_COL + TL * HD <= COLS, "TMEM budget");
 };
 
 // Shared-memory descriptor of an MN-major operand stored as 64-element-wide
@@ -165,9 +171,10 @@ __device__ __forceinline__ float row_exp(uint32_t scol, float c, float nm, int q
     return ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
 }
 
-template <int HD>
-__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
-    using L = ALayout<HD>;
+template <int HD, int TL>
+__global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
+    attn_tc_kernel(const __grid_constant__ AttnParams p) {
+    using L = ALayout<HD, TL>;
     extern __shared__ uint8_t smem_raw[];
     // CTA (head, work): the work list orders (unit, 256-query block) by cost,
     // longest first, so that the long blocks start early and the launch ends
@@ -195,12 +202,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     }
     const int len = len1 + len2;
     auto row_of = [&](int j) { return j < len1 ? off1 + j : off2 + (j - len1); };
-    const int q0 = qblk * 2 * BQ;
+    const int q0 = qblk * TL * BQ;
     if (q0 >= len) return;
     if (*reinterpret_cast<volatile int *>(&g_attn_err) != 0) return;
     const int g = h / p.group;
     const int W = p.window;
-    const int ntile = q0 + BQ < len ? 2 : 1;        // tile B exists
+    const int ntile = TL == 2 && q0 + BQ < len ? 2 : 1;   // tile B exists
 
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -218,7 +225,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
 
     // key tiles the two query tiles need: the union of their windows, clipped
     int klo = 0, khi = len;
-    const int qhi = (q0 + 2 * BQ < len ? q0 + 2 * BQ : len) - 1;
+    const int qhi = (q0 + TL * BQ < len ? q0 + TL * BQ : len) - 1;
     if (W > 0) {
         klo = q0 - W > 0 ? q0 - W : 0;
         khi = qhi + W + 1 < len ? qhi + W + 1 : len;
@@ -241,14 +248,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         mbar_init(bar_fin, 1);
         fence_mbar_init();
     }
-    if (warp == 8) tmem_alloc(smem_u32(tmem_slot), L::COLS);
+    if (warp == L::MMA_WARP) tmem_alloc(smem_u32(tmem_slot), L::COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
     bool ok = true;
 
-    if (warp == 9) {
+    if (warp == L::TMA_WARP) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&p.map);
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 mbar_wait(bar_vf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
             }
         }
-    } else if (warp == 8) {
+    } else if (warp == L::MMA_WARP) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, BKV);
@@ -428,25 +435,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     if (!ok) atomicExch(&g_attn_err, 1);
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == L::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tbase, L::COLS);
     }
 }
 
-template <int HD>
+template <int HD, int TL>
 te_status launch(const AttnParams &p, int max_len, int nq, int nseq, cudaStream_t stream) {
-    using L = ALayout<HD>;
+    using L = ALayout<HD, TL>;
     const int smem = L::BYTES + 1024;
     static bool attr_done = false;
     if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, TL>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_fail(e, "attn: set shared memory size");
         attr_done = true;
     }
-    const dim3 grid = p.nwork ? dim3(nq, p.nwork, 1) : dim3((max_len + 2 * BQ - 1) / (2 * BQ), nq, nseq);
-    attn_tc_kernel<HD><<<grid, NTHREADS, smem, stream>>>(p);
+    const dim3 grid = p.nwork ? dim3(nq, p.nwork, 1) : dim3((max_len + TL * BQ - 1) / (TL * BQ), nq, nseq);
+    attn_tc_kernel<HD, TL><<<grid, L::NTHREADS, smem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TE_OK : cuda_fail(e, "attn launch");
 }
@@ -486,21 +493,21 @@ static te_status attn_common_checks(const void *qkv, int64_t ld, int32_t q_off, 
     return TE_OK;
 }
 
-// The (unit, 256-query block) pairs with queries, longest first: cost =
+// The (unit, qb-query block) pairs with queries, longest first: cost =
 // queries of the block x keys it can see.  Empty when there are more than
 // MAX_WORK pairs (the plain grid is used then).
-static int build_work(const int32_t *lens, int32_t units, int32_t window, uint32_t *work) {
+static int build_work(const int32_t *lens, int32_t units, int32_t window, int qb, uint32_t *work) {
     int n = 0;
-    for (int32_t u = 0; u < units; ++u) n += (lens[u] + 255) / 256;
+    for (int32_t u = 0; u < units; ++u) n += (lens[u] + qb - 1) / qb;
     if (n > MAX_WORK || units > 65535) return 0;
     struct W { long long cost; uint32_t v; };
     W tmp[MAX_WORK];
     n = 0;
     for (int32_t u = 0; u < units; ++u) {
-        for (int b = 0; b * 256 < lens[u]; ++b) {
-            const long long q = lens[u] - b * 256 < 256 ? lens[u] - b * 256 : 256;
+        for (int b = 0; b * qb < lens[u]; ++b) {
+            const long long q = lens[u] - b * qb < qb ? lens[u] - b * qb : qb;
             long long keys = lens[u];
-            if (window > 0 && 2LL * window + 256 < keys) keys = 2LL * window + 256;
+            if (window > 0 && 2LL * window + qb < keys) keys = 2LL * window + qb;
             tmp[n++] = {q * keys, ((uint32_t)u << 16) | (uint32_t)b};
         }
     }
@@ -538,10 +545,13 @@ static te_status attn_launch(const void *qkv, int64_t ld, int32_t q_off, int32_t
     p.group = nq_heads / nkv_heads;
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.nwork = build_work(unit_lens, units, window, p.work);
+    // hd = 64: one 128-query tile a CTA, two CTAs an SM; hd = 128: two tiles
+    // a CTA (two CTAs would not fit an SM's shared memory)
+    const int tl = hd == 64 ? 1 : 2;
+    p.nwork = build_work(unit_lens, units, window, tl * BQ, p.work);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return hd == 64 ? launch<64>(p, max_len, nq_heads, units, s)
-                    : launch<128>(p, max_len, nq_heads, units, s);
+    return hd == 64 ? launch<64, 1>(p, max_len, nq_heads, units, s)
+                    : launch<128, 2>(p, max_len, nq_heads, units, s);
 }
 
 extern "C" te_status te_attn_varlen_fwd(const void *qkv, int64_t ld, int32_t q_off, int32_t k_off,
