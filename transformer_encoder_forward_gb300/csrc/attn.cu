@@ -171,6 +171,52 @@ __device__ __forceinline__ float row_exp(uint32_t scol, float c, float nm, int q
     return ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
 }
 
+// The same two passes over an S row already loaded into registers (v0 =
+// keys 0-63, v1 = keys 64-127): one TMEM load of the row for both.
+template <bool MASK>
+__device__ __forceinline__ float row_max_regs(const uint32_t (&v0)[64], const uint32_t (&v1)[64], int qi,
+                                              int kv0, int len, int W) {
+    float m8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+        const float x0 = __uint_as_float(v0[e]), x1 = __uint_as_float(v1[e]);
+        if (!MASK || key_visible(kv0 + e, qi, len, W)) m8[e & 7] = fmaxf(m8[e & 7], x0);
+        if (!MASK || key_visible(kv0 + 64 + e, qi, len, W)) m8[e & 7] = fmaxf(m8[e & 7], x1);
+    }
+    return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+}
+
+template <bool MASK>
+__device__ __forceinline__ float row_exp_regs(uint32_t scol, const uint32_t (&v0)[64], const uint32_t (&v1)[64],
+                                              float c, float nm, int qi, int kv0, int len, int W) {
+    float r8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r8[i] = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t (&v)[64] = hh ? v1 : v0;
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), c, nm));
+            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c, nm));
+            if (MASK) {
+                const int k = kv0 + 64 * hh + 2 * e;
+                if (!key_visible(k, qi, len, W)) p0 = 0.f;
+                if (!key_visible(k + 1, qi, len, W)) p1 = 0.f;
+            }
+            r8[(2 * e) & 7] += p0;
+            r8[(2 * e + 1) & 7] += p1;
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(scol + 32 * hh, pk);
+    }
+    return ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+}
+
 template <int HD, int TL>
 __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
     attn_tc_kernel(const __grid_constant__ AttnParams p) {
@@ -367,7 +413,13 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             const bool full = kv0 + BKV <= len &&
                               (W == 0 || (tqhi - kv0 <= W && kv0 + BKV - 1 - tq0 <= W));
             // pass 1: the row max of the raw scores
-            float mx = full ? row_max<false>(scol, qi, kv0, len, W) : row_max<true>(scol, qi, kv0, len, W);
+            // the S row once into registers for both passes
+            uint32_t v0[64], v1[64];
+            tmem_ld64(scol, v0);
+            tmem_ld64(scol + 64, v1);
+            tmem_wait_ld();
+            float mx = full ? row_max_regs<false>(v0, v1, qi, kv0, len, W)
+                            : row_max_regs<true>(v0, v1, qi, kv0, len, W);
             mx *= c;                                     // c > 0: the max of the scaled row
             // The exp pass of the two tiles alternates (A(0), B(0), A(1), ...):
             // each tile then has the SM's exp units to itself while the tensor
@@ -396,8 +448,8 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             }
             // pass 2: P as bf16 into the consumed S columns, and its row sum
             const float nm = m_used == -INFINITY ? 0.f : -m_used;
-            const float rs = full ? row_exp<false>(scol, c, nm, qi, kv0, len, W)
-                                  : row_exp<true>(scol, c, nm, qi, kv0, len, W);
+            const float rs = full ? row_exp_regs<false>(scol, v0, v1, c, nm, qi, kv0, len, W)
+                                  : row_exp_regs<true>(scol, v0, v1, c, nm, qi, kv0, len, W);
             l += rs;
             tmem_wait_st();
             tc_fence_before();
