@@ -114,14 +114,17 @@ def test_q8_linear_exact_integer_case_is_bit_exact():
     np.testing.assert_array_equal(to_np(y), exact.astype(np.float64))
 
 
-def test_int8_widening_and_indexing_are_bit_exact():
+@pytest.mark.parametrize("reps", [2, 4])
+def test_int8_widening_and_indexing_are_bit_exact(reps):
     # one-hot activation rows pick single weight columns: y[t, o] = q[o, j_t]
-    # exactly, for every int8 value (including -128) and every row/column
+    # exactly, for every int8 value (including -128) and every row/column;
+    # with 4 repetitions (1027 tokens) the weights are widened into the
+    # shared-memory-resident tile
     torch = _torch()
     k, n = 256, 256
     q_np = (np.arange(n * k, dtype=np.int64).reshape(n, k) * 37 % 256 - 128).astype(np.int8)
-    m = 2 * k + 3
-    cols = np.r_[np.arange(k), np.arange(k)[::-1], [0, 17, 255]]
+    m = reps * k + 3
+    cols = np.r_[np.tile(np.r_[np.arange(k), np.arange(k)[::-1]], reps // 2), [0, 17, 255]]
     xi = np.zeros((m, k), np.float32)
     xi[np.arange(m), cols] = 1.0
     x = torch.from_numpy(xi).to(torch.bfloat16).cuda()
@@ -470,6 +473,8 @@ def _block_weight(rng, n, k, fmt, with_scale, bias):
     (1000, 3840, [("q8_0", False, False, 384)], "bf16"),
     # enough feature tiles for two 192-token tiles per weight stage, ragged tail
     (2200, 3840, [("q4_0", True, False, 3840), ("q8_0", False, False, 3840)], "bf16"),
+    # K <= 512 with enough tokens: widened into the shared-memory-resident tile
+    (2000, 512, [("q4_0", True, True, 512), ("q8_0", False, False, 256)], "bf16"),
 ])
 def test_block_format_gemm_matches_oracle(m, k, specs, ydt):
     torch = _torch()
@@ -491,10 +496,10 @@ def test_block_format_gemm_matches_oracle(m, k, specs, ydt):
         assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
 
 
-def test_block_format_gated_linear_matches_oracle():
+@pytest.mark.parametrize("m,k,f", [(777, 768, 512), (1500, 384, 512)])
+def test_block_format_gated_linear_matches_oracle(m, k, f):
     torch = _torch()
     rng = np.random.default_rng(71)
-    m, k, f = 777, 768, 512
     x, x64 = bf16_input(rng, (m, k))
     dg, rg = _block_weight(rng, f, k, "q8_0", False, False)
     du, ru = _block_weight(rng, f, k, "q4_0", True, False)
@@ -525,7 +530,8 @@ def test_block_format_gemm_unit_scales_is_bit_exact():
 # ------------------------------------------------------------------- q8_2f
 
 @pytest.mark.parametrize("m,k,ns,ydt", [(101, 256, [256], "f32"), (777, 768, [768, 512], "bf16"),
-                                        (2200, 3840, [3840, 3840], "bf16"), (300, 320, [96], "f32")])
+                                        (2200, 3840, [3840, 3840], "bf16"), (300, 320, [96], "f32"),
+                                        (2000, 448, [384, 256], "f32")])
 def test_q8_2f_gemm_matches_oracle(m, k, ns, ydt):
     torch = _torch()
     rng = np.random.default_rng([m, k, 2])
