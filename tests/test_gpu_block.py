@@ -193,3 +193,27 @@ def test_stack_forward_is_deterministic():
         outs.append((x.clone(), out.clone()))
     te.check()
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_forward_host_graph_replay_equals_the_device_forward():
+    # the public host-to-host call runs eagerly once, then replays a captured
+    # graph: every call returns the device forward's result bit for bit
+    import torch
+    cfg = synth.small_config("c2", layers=2, window=40, lens=(100, 300, 37))
+    st, _, _ = _stack(cfg, cfg.lens, 2)
+    x0 = synth.draw_x(st.T, cfg.d, 9)
+    x, a, out = st.buffers()
+    x.copy_(to_dev(x0))
+    st.forward_device(x, a, out)
+    torch.cuda.synchronize()
+    ref = out.cpu()
+    x_host = torch.from_numpy(np.ascontiguousarray(x0)).pin_memory()
+    res = torch.empty(len(cfg.lens), cfg.d, dtype=torch.float32).pin_memory()
+    s = torch.cuda.Stream()
+    for _ in range(3):
+        res.zero_()
+        st.forward_host(x_host, res, stream=s)
+        s.synchronize()
+        te.check()
+        assert torch.equal(res, ref)
+    assert len(st._graphs) == 1

@@ -162,13 +162,40 @@ class EncoderStack:
             pool_mean(x, self.cu_host, self.cu_dev, self.final_norm, self.cfg.eps, out,
                       stream=stream)
 
-    def forward_host(self, x_host, result_host, x=None, a=None, out=None, stream=None):
+    def forward_host(self, x_host, result_host, x=None, a=None, out=None, stream=None, graph=True):
         """End to end from pinned host memory: copies the input rows in, runs
-        the stack and copies the result (the pooled rows, else x) back."""
+        the stack and copies the result (the pooled rows, else x) back, all on
+        `stream` (a torch.cuda.Stream; the current stream when None).
+
+        With graph=True the device part is replayed from a CUDA graph: the
+        first call with a given set of device buffers runs it eagerly (that
+        call's result is a normal forward) and then captures it; later calls
+        replay the capture, which removes the per-layer host work of the C-ABI
+        calls (validation, tensor maps, work lists) from the critical path."""
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
         if x is None:
-            x, a, out = self.buffers()
-        x.copy_(x_host, non_blocking=True)
-        self.forward_device(x, a, out, stream=stream)
+            if getattr(self, "_bufs", None) is None:
+                self._bufs = self.buffers()
+            x, a, out = self._bufs
         src = out if self.cfg.pool else x
-        result_host.copy_(src, non_blocking=True)
+        key = (x.data_ptr(), a.data_ptr(), out.data_ptr() if out is not None else 0, s.cuda_stream)
+        graphs = self.__dict__.setdefault("_graphs", {})
+        with torch.cuda.stream(s):
+            x.copy_(x_host, non_blocking=True)
+            g = graphs.get(key) if graph else None
+            if g is not None:
+                g.replay()
+            else:
+                self.forward_device(x, a, out, stream=s)
+            result_host.copy_(src, non_blocking=True)
+        if graph and g is None:
+            # capture after the eager forward has run (capturing does not execute)
+            cap = torch.cuda.Stream(device=self.device)
+            cap.wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                self.forward_device(x, a, out, stream=cap)
+            s.wait_stream(cap)
+            graphs[key] = g
         return result_host
