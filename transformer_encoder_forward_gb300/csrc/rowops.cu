@@ -382,16 +382,21 @@ __global__ void __launch_bounds__(256) cast_bf16_kernel(const float *__restrict_
 
 // ------------------------------------------------------------- qk prep + RoPE
 
-// One warp per (packed row, group of 4 * 32 / (HD / 8) heads).  Each lane
-// owns 8 consecutive channels (one 16-byte load); a head of HD channels spans
-// HD/8 lanes, so the per-head RMS is a reduction over an aligned lane group and
-// the RoPE partner (channel +-sec/2 in the same section) sits in lane
-// (l ^ sec/16) at the same offset.  The warp issues all loads of its group
-// before any arithmetic (4 16-byte loads per lane in flight; a loop of
-// load -> norm -> store per head pair waited a full memory latency per
+// One warp per (packed row, group of 4 * 32 / (HD / 8) heads).  A head of HD
+// channels spans HD/8 lanes, so the per-head RMS is a reduction over an
+// aligned lane group.  Each lane owns both members of its RoPE pairs: 4
+// channels of the first half of its section and the matching 4 of the second
+// half (two 8-byte loads), so the rotation needs no exchange between lanes
+// (without RoPE the two 4-channel pieces are simply adjacent).  The warp issues
+// all loads of its group before any arithmetic (4 heads per lane in flight; a
+// loop of load -> norm -> store per head pair waited a full memory latency per
 // iteration; 8 in flight measured slower at 60 heads x 128).
 template <int HD>
-__host__ __device__ constexpr int qk_u() { return 4; }   // 4 loads per lane in flight
+__host__ __device__ constexpr int qk_u() { return 4; }   // 4 heads per lane in flight
+
+__device__ __forceinline__ void unpack4(uint2 r, float (&v)[4]) {
+    v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
+}
 
 template <int HD, bool VN>
 __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long long ld, int q_off,
@@ -409,47 +414,38 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     const int hl = lane / LPH;                  // head slot of this lane in a load slot
-    const int c0 = (lane % LPH) * 8;            // first channel of this lane within its head
+    const int j = lane % LPH;                   // lane within its head
+    // this lane's channels: c1..c1+3 and c2..c2+3 (c2 = c1 + half of the section)
+    const int secl = sec ? sec : 8;             // section (8: no RoPE, adjacent pieces)
+    const int half = secl >> 1;
+    const int lps = secl / 8;                   // lanes per section
+    const int sct = j / lps, jj = j - sct * lps;
+    const int c1 = sct * secl + 4 * jj, c2 = c1 + half;
     const int nh = nq + nkv + nv;               // q heads, k heads, then (v-norm) v heads
     const int hbase = blockIdx.y * (HPI * QK_U);
-    float cv[8], sv[8];
-    const int half = sec >> 1;
+    float4 cv = make_float4(0.f, 0.f, 0.f, 0.f), sv = cv;
     if (sec) {
         long long prow = pos ? pos[row] : row;
         if (prow < 0 || prow >= table_rows) {
             atomicExch(&g_rowop_err, 2);
             prow = 0;
         }
-        const float *cr = cosb + prow * (HD / 2);
-        const float *sr = sinb + prow * (HD / 2);
-        const int sct = c0 / sec;
-        const int i = c0 - sct * sec;
-        const int tc = sct * half + (i < half ? i : i - half);   // 8 consecutive table entries
-        const float4 a0 = *reinterpret_cast<const float4 *>(cr + tc);
-        const float4 a1 = *reinterpret_cast<const float4 *>(cr + tc + 4);
-        const float4 b0 = *reinterpret_cast<const float4 *>(sr + tc);
-        const float4 b1 = *reinterpret_cast<const float4 *>(sr + tc + 4);
-        cv[0] = a0.x; cv[1] = a0.y; cv[2] = a0.z; cv[3] = a0.w;
-        cv[4] = a1.x; cv[5] = a1.y; cv[6] = a1.z; cv[7] = a1.w;
-        sv[0] = b0.x; sv[1] = b0.y; sv[2] = b0.z; sv[3] = b0.w;
-        sv[4] = b1.x; sv[5] = b1.y; sv[6] = b1.z; sv[7] = b1.w;
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) cv[e] = sv[e] = 0.f;
+        // pair index of c1 within its section: table column sct*half + 4*jj
+        cv = *reinterpret_cast<const float4 *>(cosb + prow * (HD / 2) + sct * half + 4 * jj);
+        sv = *reinterpret_cast<const float4 *>(sinb + prow * (HD / 2) + sct * half + 4 * jj);
     }
-    const bool first_half = sec ? ((c0 % sec) < half) : true;
-    const int xr = sec ? half / 8 : 0;          // lane distance to the RoPE partner
-    uint4 raw[QK_U];
+    uint2 r1[QK_U], r2[QK_U];
 #pragma unroll
     for (int u = 0; u < QK_U; ++u) {           // every load of the group first
         const int hh = hbase + u * HPI + hl;
         if (hh < nh) {
             const int col = hh < nq ? q_off + hh * HD
                                     : (!VN || hh < nq + nkv ? k_off + (hh - nq) * HD : v_off + (hh - nq - nkv) * HD);
-            const __nv_bfloat16 *p = qkv + row * ld + col + c0;
-            raw[u] = *reinterpret_cast<const uint4 *>(p);
+            const __nv_bfloat16 *p = qkv + row * ld + col;
+            r1[u] = *reinterpret_cast<const uint2 *>(p + c1);
+            r2[u] = *reinterpret_cast<const uint2 *>(p + c2);
         } else {
-            raw[u] = make_uint4(0u, 0u, 0u, 0u);
+            r1[u] = r2[u] = make_uint2(0u, 0u);
         }
     }
 #pragma unroll
@@ -458,48 +454,45 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
         const bool active = hh < nh;            // lane groups past the last head idle
         const bool isq = hh < nq;
         const bool isv = VN && hh >= nq + nkv;  // v heads: RMS norm without weight, no RoPE
-        float v[8];
-        v[0] = bf16_lo(raw[u].x); v[1] = bf16_hi(raw[u].x); v[2] = bf16_lo(raw[u].y); v[3] = bf16_hi(raw[u].y);
-        v[4] = bf16_lo(raw[u].z); v[5] = bf16_hi(raw[u].z); v[6] = bf16_lo(raw[u].w); v[7] = bf16_hi(raw[u].w);
+        float a[4], b[4];
+        unpack4(r1[u], a);
+        unpack4(r2[u], b);
         const float *nw = isq ? qn : kn;
         if (qn || VN) {                         // uniform: qn and kn are both given or both NULL
             float q = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) q += v[e] * v[e];
+            for (int e = 0; e < 4; ++e) q = fmaf(a[e], a[e], fmaf(b[e], b[e], q));
 #pragma unroll
             for (int o = 1; o < LPH; o <<= 1) q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
             const float inv = rsqrtf(q / (float)HD + eps);
             if (VN && active && isv) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= inv;
+                for (int e = 0; e < 4; ++e) { a[e] *= inv; b[e] *= inv; }
             } else if (active && qn) {
-                const float4 w0 = *reinterpret_cast<const float4 *>(nw + c0);
-                const float4 w1 = *reinterpret_cast<const float4 *>(nw + c0 + 4);
-                v[0] *= inv * w0.x; v[1] *= inv * w0.y; v[2] *= inv * w0.z; v[3] *= inv * w0.w;
-                v[4] *= inv * w1.x; v[5] *= inv * w1.y; v[6] *= inv * w1.z; v[7] *= inv * w1.w;
+                const float4 w1 = *reinterpret_cast<const float4 *>(nw + c1);
+                const float4 w2 = *reinterpret_cast<const float4 *>(nw + c2);
+                a[0] *= inv * w1.x; a[1] *= inv * w1.y; a[2] *= inv * w1.z; a[3] *= inv * w1.w;
+                b[0] *= inv * w2.x; b[1] *= inv * w2.y; b[2] *= inv * w2.z; b[3] *= inv * w2.w;
             }
         }
-        if (sec) {                              // every lane exchanges; v heads keep theirs
-            float o[8];
+        if (sec && !(VN && isv)) {              // rotate-half: (a, b) -> (a c - b s, b c + a s)
+            const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float partner = __shfl_xor_sync(0xFFFFFFFFu, v[e], xr);
-                o[e] = first_half ? v[e] * cv[e] - partner * sv[e] : v[e] * cv[e] + partner * sv[e];
-            }
-            if (!VN || !isv) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = o[e];
+            for (int e = 0; e < 4; ++e) {
+                const float x1 = a[e], x2 = b[e];
+                a[e] = fmaf(x1, cc[e], -x2 * ss[e]);
+                b[e] = fmaf(x2, cc[e], x1 * ss[e]);
             }
         }
         if (active) {
             const float mul = isq ? q_mul : 1.f;
-            uint4 w;
-            w.x = pack_bf16x2(v[0] * mul, v[1] * mul); w.y = pack_bf16x2(v[2] * mul, v[3] * mul);
-            w.z = pack_bf16x2(v[4] * mul, v[5] * mul); w.w = pack_bf16x2(v[6] * mul, v[7] * mul);
             const int col = isq ? q_off + hh * HD
                                 : (VN && isv ? v_off + (hh - nq - nkv) * HD : k_off + (hh - nq) * HD);
-            __nv_bfloat16 *p = qkv + row * ld + col + c0;
-            *reinterpret_cast<uint4 *>(p) = w;
+            __nv_bfloat16 *p = qkv + row * ld + col;
+            *reinterpret_cast<uint2 *>(p + c1) = make_uint2(pack_bf16x2(a[0] * mul, a[1] * mul),
+                                                            pack_bf16x2(a[2] * mul, a[3] * mul));
+            *reinterpret_cast<uint2 *>(p + c2) = make_uint2(pack_bf16x2(b[0] * mul, b[1] * mul),
+                                                            pack_bf16x2(b[2] * mul, b[3] * mul));
         }
     }
 }
