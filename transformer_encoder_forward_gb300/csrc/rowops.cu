@@ -388,11 +388,12 @@ __global__ void __launch_bounds__(256) cast_bf16_kernel(const float *__restrict_
 // channels of the first half of its section and the matching 4 of the second
 // half (two 8-byte loads), so the rotation needs no exchange between lanes
 // (without RoPE the two 4-channel pieces are simply adjacent).  The warp issues
-// all loads of its group before any arithmetic (4 heads per lane in flight; a
-// loop of load -> norm -> store per head pair waited a full memory latency per
-// iteration; 8 in flight measured slower at 60 heads x 128).
+// all loads of its group before any arithmetic (4 heads per lane in flight at
+// hd 64, 6 at hd 128 - 60 heads then split into five whole groups; a loop of
+// load -> norm -> store per head pair waited a full memory latency per
+// iteration).
 template <int HD>
-__host__ __device__ constexpr int qk_u() { return 4; }   // 4 heads per lane in flight
+__host__ __device__ constexpr int qk_u() { return HD == 128 ? 6 : 4; }   // heads per lane in flight
 
 __device__ __forceinline__ void unpack4(uint2 r, float (&v)[4]) {
     v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
