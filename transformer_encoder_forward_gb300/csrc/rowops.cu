@@ -62,6 +62,14 @@ __device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
+// The same load with the streaming (evict-first) cache hint: for rows read
+// once, so that they do not push the per-feature vectors out of L1.
+__device__ __forceinline__ void load8_stream(const float *p, float (&v)[8]) {
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
     const uint4 u = *reinterpret_cast<const uint4 *>(p);
     v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
@@ -262,8 +270,14 @@ __global__ void __launch_bounds__(256) add_norm_wide_kernel(float *h, const floa
     for (int i = 0; i < NV; ++i) {
         const int c = (i * 128 + tid) * 8;
         if (active && c < d) {
-            if (tr) load8(tr + c, tv[i]);
-            load8(hr + c, hv[i]);
+            // adaLN form: its gate and scale vectors compete with the rows for L1
+            if (MOD) {
+                if (tr) load8_stream(tr + c, tv[i]);
+                load8_stream(hr + c, hv[i]);
+            } else {
+                if (tr) load8(tr + c, tv[i]);
+                load8(hr + c, hv[i]);
+            }
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) tv[i][e] = hv[i][e] = 0.f;
