@@ -402,18 +402,18 @@ __global__ void __launch_bounds__(256) cast_bf16_kernel(const float *__restrict_
 // channels of the first half of its section and the matching 4 of the second
 // half (two 8-byte loads), so the rotation needs no exchange between lanes
 // (without RoPE the two 4-channel pieces are simply adjacent).  The warp issues
-// all loads of its group before any arithmetic (4 heads per lane in flight at
-// hd 64, 6 at hd 128 - 60 heads then split into five whole groups; a loop of
-// load -> norm -> store per head pair waited a full memory latency per
-// iteration).
-template <int HD>
-__host__ __device__ constexpr int qk_u() { return HD == 128 ? 6 : 4; }   // heads per lane in flight
+// all loads of its group before any arithmetic (4 or 6 heads per lane in
+// flight, chosen so that the heads split into whole groups: 60 heads of 128
+// into five groups of 12; a loop of load -> norm -> store per head pair waited
+// a full memory latency per iteration).
+// heads per lane in flight: 4 or 6, chosen per launch so that the head
+// count splits into whole groups where it can
 
 __device__ __forceinline__ void unpack4(uint2 r, float (&v)[4]) {
     v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
 }
 
-template <int HD, bool VN>
+template <int HD, bool VN, int QK_U>
 __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long long ld, int q_off,
                                                       int k_off, int v_off, int nq, int nkv, int nv,
                                                       const float *__restrict__ qn,
@@ -424,7 +424,6 @@ __global__ void __launch_bounds__(256) qk_prep_kernel(__nv_bfloat16 *qkv, long l
                                                       int sec, float q_mul, int rows) {
     constexpr int LPH = HD / 8;                 // lanes per head
     constexpr int HPI = 32 / LPH;               // heads per load slot
-    constexpr int QK_U = qk_u<HD>();
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -767,18 +766,24 @@ te_status te_qkv_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, 
         return fail(TE_EINVAL, "qk_prep_rope: give both qn and kn or neither");
     const int nv = v_norm ? nkv : 0;
     if (rows == 0 || nq + nkv + nv == 0) return TE_OK;
-    const int heads_per_warp = (32 / (hd / 8)) * (hd == 128 ? qk_u<128>() : qk_u<64>());
-    const dim3 grid((unsigned)(((long long)rows + 7) / 8),
-                    (unsigned)((nq + nkv + nv + heads_per_warp - 1) / heads_per_warp));
+    // 6 heads a lane in flight when that splits the heads into whole groups and
+    // 4 would not (hd 128: 60 heads; v-norm at hd 64: 24), else 4
+    const int nh = nq + nkv + nv, hpi = 32 / (hd / 8);
+    const int qu = (nh % (6 * hpi) == 0 && nh % (4 * hpi) != 0) || (hd == 128 && nh % (4 * hpi) != 0) ? 6 : 4;
+    const int heads_per_warp = hpi * qu;
+    const dim3 grid((unsigned)(((long long)rows + 7) / 8), (unsigned)((nh + heads_per_warp - 1) / heads_per_warp));
     auto go = [&](auto kern) {
         kern<<<grid, 256, 0, stream>>>((__nv_bfloat16 *)qkv, ld, q_off, k_off, v_off, nq, nkv, nv, qn, kn, eps,
                                        cos, sin, pos, table_rows, sec, q_mul, rows);
     };
     // the v-norm heads in their own instantiation: the q/k pass keeps its code
-    if (hd == 64)
-        nv ? go(qk_prep_kernel<64, true>) : go(qk_prep_kernel<64, false>);
-    else
-        nv ? go(qk_prep_kernel<128, true>) : go(qk_prep_kernel<128, false>);
+    if (hd == 64) {
+        if (qu == 6) nv ? go(qk_prep_kernel<64, true, 6>) : go(qk_prep_kernel<64, false, 6>);
+        else nv ? go(qk_prep_kernel<64, true, 4>) : go(qk_prep_kernel<64, false, 4>);
+    } else {
+        if (qu == 6) nv ? go(qk_prep_kernel<128, true, 6>) : go(qk_prep_kernel<128, false, 6>);
+        else nv ? go(qk_prep_kernel<128, true, 4>) : go(qk_prep_kernel<128, false, 4>);
+    }
     return launched("qk_prep_rope launch");
 }
 
