@@ -116,63 +116,9 @@ __device__ __forceinline__ bool key_visible(int k, int qi, int len, int W) {
     return k < len && (W == 0 || (dq <= W && -dq <= W));
 }
 
-// Row max of one 128-key S row held in TMEM (columns scol..scol+127), with
-// keys outside the sequence or the window ignored when MASK: two 64-column
-// loads behind one wait, eight independent partial maxima.
-template <bool MASK>
-__device__ __forceinline__ float row_max(uint32_t scol, int qi, int kv0, int len, int W) {
-    float m8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-    uint32_t v0[64], v1[64];
-    tmem_ld64(scol, v0);
-    tmem_ld64(scol + 64, v1);
-    tmem_wait_ld();
-#pragma unroll
-    for (int e = 0; e < 64; ++e) {
-        const float x0 = __uint_as_float(v0[e]), x1 = __uint_as_float(v1[e]);
-        if (!MASK || key_visible(kv0 + e, qi, len, W)) m8[e & 7] = fmaxf(m8[e & 7], x0);
-        if (!MASK || key_visible(kv0 + 64 + e, qi, len, W)) m8[e & 7] = fmaxf(m8[e & 7], x1);
-    }
-    return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-}
-
-// P = 2^(s*c + nm) over the row as bf16 pairs, written over S columns the row
-// has already consumed (the half h of P lands in columns [32h, 32h+32), which
-// held keys read by the same or an earlier half).  Returns the row sum of P.
-template <bool MASK>
-__device__ __forceinline__ float row_exp(uint32_t scol, float c, float nm, int qi, int kv0, int len,
-                                         int W) {
-    float r8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r8[i] = 0.f;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        uint32_t v[64];
-        tmem_ld64(scol + 64 * hh, v);
-        tmem_wait_ld();
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), c, nm));
-            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c, nm));
-            if (MASK) {
-                const int k = kv0 + 64 * hh + 2 * e;
-                if (!key_visible(k, qi, len, W)) p0 = 0.f;
-                if (!key_visible(k + 1, qi, len, W)) p1 = 0.f;
-            }
-            r8[(2 * e) & 7] += p0;
-            r8[(2 * e + 1) & 7] += p1;
-            pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(scol + 32 * hh, pk);
-    }
-    return ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
-}
-
-// The same two passes over an S row already loaded into registers (v0 =
-// keys 0-63, v1 = keys 64-127): one TMEM load of the row for both.
+// The two passes over one 128-key S row, loaded from TMEM once into registers
+// (v0 = keys 0-63, v1 = keys 64-127).  Row max: keys outside the sequence or
+// the window ignored when MASK, eight independent partial maxima.
 template <bool MASK>
 __device__ __forceinline__ float row_max_regs(const uint32_t (&v0)[64], const uint32_t (&v1)[64], int qi,
                                               int kv0, int len, int W) {
@@ -189,6 +135,9 @@ __device__ __forceinline__ float row_max_regs(const uint32_t (&v0)[64], const ui
                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
 }
 
+// Exp pass: P = 2^(s*c + nm) as bf16 pairs, written over S columns the row
+// has already consumed (half h of P lands in columns [32h, 32h+32)); returns
+// the row sum of P over the f32 values.
 template <bool MASK>
 __device__ __forceinline__ float row_exp_regs(uint32_t scol, const uint32_t (&v0)[64], const uint32_t (&v1)[64],
                                               float c, float nm, int qi, int kv0, int len, int W) {
