@@ -370,7 +370,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 if (!mbar_wait_cluster(bar_accempty + 8 * b, ph ^ 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t dcol = tbase + (TPA == 2 ? 0 : b) * BN;
-                for (int kb = 0; kb < nkb; ++kb) {
+                int kb0 = 0;   // stages issued for both token tiles before the main loop
+                if (TPA == 2) {
+                    // Token tile 0's MMAs for the first widened stages start
+                    // while the epilogue still drains tile 1 (it drains tile 0
+                    // first and releases each accumulator on its own barrier);
+                    // each accumulator keeps its own MMA order.
+                    const int P = nkb < NA ? nkb : NA;
+                    int ss = s, aa = ar;
+                    uint32_t aph2 = aph;
+                    for (int kb = 0; kb < P && ok; ++kb) {
+                        if (!mbar_wait_cluster(bar_afull + 8 * aa, aph2)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t d0 = smem_desc_sw128(sb + L::X_OFF + ss * L::XBYTES);
+                        const uint32_t a0 = tbase + L::A_COL + 64 * aa;
+#pragma unroll
+                        for (int j = 0; j < BK / 16; ++j)
+                            mma_ts_pair(dcol, a0 + 8 * j, d0 + (uint64_t)(((j >> 2) * L::XBOX + (j & 3) * 32) >> 4),
+                                        idesc, j == 0 ? (uint32_t)(kb != 0) : 1u);
+                        if (++ss == NST) ss = 0;
+                        if (++aa == NA) { aa = 0; aph2 ^= 1u; }
+                    }
+                    if (!ok) break;
+                    if (!mbar_wait_cluster(bar_accempty + 8, ph ^ 1)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int kb = 0; kb < P; ++kb) {   // tile 1 for the same stages, then release them
+                        const uint64_t d0 = smem_desc_sw128(sb + L::X_OFF + s * L::XBYTES);
+                        const uint32_t a0 = tbase + L::A_COL + 64 * ar;
+#pragma unroll
+                        for (int j = 0; j < BK / 16; ++j)
+                            mma_ts_pair(dcol + BN, a0 + 8 * j,
+                                        d0 + (uint64_t)((L::XTILE + (j >> 2) * L::XBOX + (j & 3) * 32) >> 4), idesc,
+                                        j == 0 ? (uint32_t)(kb != 0) : 1u);
+                        mma_commit_pair(bar_empty + 8 * s, 0x3);
+                        mma_commit_pair(bar_aempty + 8 * ar, 0x3);
+                        if (++s == NST) { s = 0; sph ^= 1u; }
+                        if (++ar == NA) { ar = 0; aph ^= 1u; }
+                    }
+                    kb0 = P;
+                }
+                for (int kb = kb0; kb < nkb; ++kb) {
                     const int a = res ? kb : ar;
                     // resident weights: both CTAs' stages s have landed (our
                     // copies, and the peer's as relayed by its warp 1)
@@ -656,11 +695,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     }
                 }
             }
+            if (TPA == 2) {
+                // this token tile's accumulator may take the next unit's MMAs
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_relaxed(accempty_ldr + 8 * tt);
             }
-            // this accumulator may take the next tile's MMAs
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster_relaxed(accempty_ldr + 8 * b);
+            }
+            if (TPA == 1) {
+                // this accumulator may take the next tile's MMAs
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_relaxed(accempty_ldr + 8 * b);
+            }
         }
         // the stores must be complete before the CTA's shared memory goes away
         if (lane == 0) bulk_wait_all();
