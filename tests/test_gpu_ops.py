@@ -139,7 +139,10 @@ def test_int8_widening_and_indexing_are_bit_exact(reps):
                                             (2112, 3840, 10240, "silu", False),
                                             (101, 256, 96, "silu", True),
                                             (300, 192, 32, "gelu_tanh", False),
-                                            (5000, 512, 2048, "gelu_tanh", False)])
+                                            (5000, 512, 2048, "gelu_tanh", False),
+                                            # resident weights with 192-token tiles
+                                            (1500, 256, 768, "silu", True),
+                                            (2100, 192, 512, "gelu_tanh", False)])
 def test_gated_linear_matches_oracle(m, k, f, act, bias):
     # m = act(bf16(g)) * bf16(u): the same storage points as the g|u panel
     # followed by the gate, without the panel
@@ -473,8 +476,9 @@ def _block_weight(rng, n, k, fmt, with_scale, bias):
     (1000, 3840, [("q8_0", False, False, 384)], "bf16"),
     # enough feature tiles for two 192-token tiles per weight stage, ragged tail
     (2200, 3840, [("q4_0", True, False, 3840), ("q8_0", False, False, 3840)], "bf16"),
-    # K <= 512 with enough tokens: widened into the shared-memory-resident tile
+    # K <= 512 with enough tokens: resident weights (128- and 192-token tiles)
     (2000, 512, [("q4_0", True, True, 512), ("q8_0", False, False, 256)], "bf16"),
+    (1500, 256, [("q8_0", True, False, 384), ("q4_0", False, True, 256)], "f32"),
 ])
 def test_block_format_gemm_matches_oracle(m, k, specs, ydt):
     torch = _torch()
@@ -496,7 +500,7 @@ def test_block_format_gemm_matches_oracle(m, k, specs, ydt):
         assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
 
 
-@pytest.mark.parametrize("m,k,f", [(777, 768, 512), (1500, 384, 512)])
+@pytest.mark.parametrize("m,k,f", [(777, 768, 512), (1500, 384, 512), (1800, 256, 256)])
 def test_block_format_gated_linear_matches_oracle(m, k, f):
     torch = _torch()
     rng = np.random.default_rng(71)
@@ -531,7 +535,7 @@ def test_block_format_gemm_unit_scales_is_bit_exact():
 
 @pytest.mark.parametrize("m,k,ns,ydt", [(101, 256, [256], "f32"), (777, 768, [768, 512], "bf16"),
                                         (2200, 3840, [3840, 3840], "bf16"), (300, 320, [96], "f32"),
-                                        (2000, 448, [384, 256], "f32")])
+                                        (2000, 448, [384, 256], "f32"), (1500, 192, [256, 512], "bf16")])
 def test_q8_2f_gemm_matches_oracle(m, k, ns, ydt):
     torch = _torch()
     rng = np.random.default_rng([m, k, 2])
