@@ -50,6 +50,8 @@ GEMM_CASES = [
     # a residual other than y (f32 and bf16 y), rows wider than n
     (300, 512, [96, 160], True, "sep", "f32"),
     (777, 256, [256, 512], False, "sep", "bf16"),
+    # long K, 128-token tiles two a unit (the choice that saves a wave here)
+    (2111, 2048, [3840], False, True, "f32"),
     # resident weights over long runs of token tiles that cross feature pairs
     (5000, 512, [512, 512, 512], False, False, "bf16"),
     (5000, 512, [512], True, True, "f32"),
@@ -142,7 +144,9 @@ def test_int8_widening_and_indexing_are_bit_exact(reps):
                                             (5000, 512, 2048, "gelu_tanh", False),
                                             # resident weights with 192-token tiles
                                             (1500, 256, 768, "silu", True),
-                                            (2100, 192, 512, "gelu_tanh", False)])
+                                            (2100, 192, 512, "gelu_tanh", False),
+                                            # long K, 128-token tiles two a unit
+                                            (2300, 2048, 1024, "silu", True)])
 def test_gated_linear_matches_oracle(m, k, f, act, bias):
     # m = act(bf16(g)) * bf16(u): the same storage points as the g|u panel
     # followed by the gate, without the panel

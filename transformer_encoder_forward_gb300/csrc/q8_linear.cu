@@ -37,7 +37,7 @@
 //     layout and leaves with one TMA tensor store (a TMA reduce-add when the
 //     residual is y itself, the in-place x += proj of the plain block).
 // With long K a unit can hold two token tiles: each widened weight stage then
-// feeds both tiles' MMAs (see tokens_per_stage).
+// feeds both tiles' MMAs (see long_k_tile).
 // With short K (every K stage fits the TMEM A stages at once) the weights stay
 // resident: each cluster takes a contiguous run of units, which share their
 // feature tiles except where the run crosses into the next feature pair; the
@@ -46,7 +46,8 @@
 // the leader's full barrier (which then counts two arrivals), so the MMA
 // issuer waits on one barrier per stage.
 // TMEM: 2 accumulators of BN columns + as many A stages of 64 columns as fit
-// in the 512 (2 for BN = 192, 3 for 160, 4 for 128 and 64).  A stage is 8 MMAs deep, so the barrier round trip between
+// in the 512, fewer than the load stages (2 for BN = 192, 3 for 160 and for
+// 128 with two token tiles a unit, 4 for 128 and 64).  A stage is 8 MMAs deep, so the barrier round trip between
 // stages (about 0.1-0.2 us for the issuing thread) is amortised over 768
 // tensor-core cycles.  Every mbarrier wait is bounded (about 200 ms); a timeout sets
 // an error word that te_check() reports, the role stops, and the kernel still
@@ -98,10 +99,12 @@ template <int BN, int TPA>
 struct Layout {
     static constexpr int HALF = BN / 2;                 // token rows each CTA of the pair holds
     // shared-memory load stages (a stage holds TPA token tiles)
-    static constexpr int NST = TPA == 2 ? 3 : (BN >= 160 ? 5 : 6);
+    static constexpr int NST = TPA == 2 ? (BN == 128 ? 4 : 3) : (BN >= 160 ? 5 : 6);
     // TMEM stages of the widened A operand (64 columns each): what the two
-    // BN-column accumulators leave of the 512 columns, at most 4
-    static constexpr int NA = (512 - 2 * BN) / 64 < 4 ? (512 - 2 * BN) / 64 : 4;
+    // BN-column accumulators leave of the 512 columns, at most 4 and fewer
+    // than the load stages
+    static constexpr int NA0 = (512 - 2 * BN) / 64 < 4 ? (512 - 2 * BN) / 64 : 4;
+    static constexpr int NA = NA0 < NST - 1 ? NA0 : NST - 1;
     static constexpr int XBOX = HALF * BOX * 2;         // one 64-wide box of this CTA's activation half
     static constexpr int XTILE = 2 * XBOX;              // this CTA's half of one token tile's stage
     static constexpr int XBYTES = TPA * XTILE;          // ... of all TPA token tiles
@@ -741,22 +744,31 @@ int sm_count() {
     return count[dev];
 }
 
-// Token tiles of 192 per unit (1 or 2).  With 2, each widened weight stage
-// feeds the MMAs of two token tiles, which halves the TMEM stores of the
-// widened operand per flop (those stores contend with the MMAs for TMEM), at
-// the price of an accumulator drain that the next unit's MMAs wait for: it
-// pays off only with long K (measured: 1.10-1.16x at K = 3840 and 10240 with
-// 8448 tokens, 0.8x at K = 512 and 2048).  Among those shapes the choice
-// follows the estimated time of the busiest cluster.
-int tokens_per_stage(int m, int k, int ftiles) {
-    if (k < 3072) return 1;
+// Long K (re-widened weights): the token-tile width and the token tiles per
+// unit.  With two tiles a unit each widened weight stage feeds the MMAs of both,
+// which halves the TMEM stores of the widened operand per flop (those stores
+// contend with the MMAs for TMEM), at the price of an accumulator drain that
+// is only partly overlapped.  The choice minimises the busiest cluster's time:
+// whole waves of units times a unit's relative cost - a 192 x 2 unit takes
+// about 1.65x a 192 x 1 unit (measured at K = 3840 and 10240; it loses at
+// K <= 2048), a 128 x 2 unit about 1.4x (measured 1.33-1.48 at K = 2048 to
+// 10240; at K = 768 the drain outweighs it).  The 128 x 2 unit pays where it
+// saves a whole wave: the DiT out and down projections (2112 tokens: 62.0 ->
+// 57.6 and 151.5 -> 134.3 us), the text stack's down projection.
+struct LongKTile { int bn, tpa; };
+constexpr double COST_128X2 = 1.4;
+LongKTile long_k_tile(int m, int k, int ftiles) {
     const int clusters = sm_count() / 2;
     const long long fpairs = (ftiles + 1) / 2;
-    const long long u1 = fpairs * ((m + 191) / 192), u2 = fpairs * ((m + 383) / 384);
-    const long long w1 = (u1 + clusters - 1) / clusters, w2 = (u2 + clusters - 1) / clusters;
-    // a two-tile unit takes about 1.5-1.7x as long as a one-tile unit
-    // (measured at K = 3840 and 10240)
-    return (double)w2 * 1.65 < (double)w1 ? 2 : 1;
+    auto t = [&](int tokens, double cost) {
+        const long long units = fpairs * ((m + tokens - 1) / tokens);
+        return (double)((units + clusters - 1) / clusters) * cost;
+    };
+    LongKTile best = {192, 1};
+    double tb = t(192, 1.0);
+    if (k >= 3072 && t(384, 1.65) < tb) { best = {192, 2}; tb = t(384, 1.65); }
+    if (k >= 2048 && t(256, COST_128X2) < tb) best = {128, 2};
+    return best;
 }
 
 // Token-tile width and whether the weights stay resident (every K stage in
@@ -923,8 +935,12 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         ftiles += d.ntiles;
     }
     if (m == 0) return TE_OK;
-    const int bn = pick_bn(m, k, p.res);
-    const int tpa = bn == 192 && !p.res ? tokens_per_stage(m, k, ftiles) : 1;
+    int bn = pick_bn(m, k, p.res), tpa = 1;
+    if (bn == 192 && !p.res) {
+        const LongKTile lt = long_k_tile(m, k, ftiles);
+        bn = lt.bn;
+        tpa = lt.tpa;
+    }
     // each CTA of a cluster pair loads half of the token tile (and multicasts it)
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
                                (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -941,7 +957,7 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (bn == 192) return tpa == 2 ? launch<192, false, 2>(p, ftiles, s) : launch<192, false, 1>(p, ftiles, s);
-    if (bn == 128) return launch<128, false, 1>(p, ftiles, s);
+    if (bn == 128) return tpa == 2 ? launch<128, false, 2>(p, ftiles, s) : launch<128, false, 1>(p, ftiles, s);
     return launch<64, false, 1>(p, ftiles, s);
 }
 
@@ -994,8 +1010,12 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     d.tile0 = 0;
     d.ntiles = (f + BM / 2 - 1) / (BM / 2);
     if (m == 0) return TE_OK;
-    const int bn = pick_bn(m, k, p.res);
-    const int tpa = bn == 192 && !p.res ? tokens_per_stage(m, k, d.ntiles) : 1;
+    int bn = pick_bn(m, k, p.res), tpa = 1;
+    if (bn == 192 && !p.res) {
+        const LongKTile lt = long_k_tile(m, k, d.ntiles);
+        bn = lt.bn;
+        tpa = lt.tpa;
+    }
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
                                (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_OK) return st;
@@ -1011,6 +1031,6 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (bn == 192) return tpa == 2 ? launch<192, true, 2>(p, d.ntiles, s) : launch<192, true, 1>(p, d.ntiles, s);
-    if (bn == 128) return launch<128, true, 1>(p, d.ntiles, s);
+    if (bn == 128) return tpa == 2 ? launch<128, true, 2>(p, d.ntiles, s) : launch<128, true, 1>(p, d.ntiles, s);
     return launch<64, true, 1>(p, d.ntiles, s);
 }
