@@ -548,8 +548,6 @@ def cpu_baseline(cfg_full, key, budget_s=15.0):
         flops += g + a
         done += 1
         layer += 1
-        if done >= 2:
-            break
     return {"value": round(flops / t_used / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle",
             "sample": f"{done} layer(s) of {cfg.name} over the first {len(sl)} sequence(s) "
