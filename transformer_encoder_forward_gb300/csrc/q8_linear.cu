@@ -35,9 +35,14 @@
 //     output feature, so the row scale and bias are per-thread constants;
 //     each 32 x 32 block is written into a staging tile in the output's own
 //     layout and leaves with one TMA tensor store (a TMA reduce-add when the
-//     residual is y itself, the in-place x += proj of the plain block).
-// With long K a unit can hold two token tiles: each widened weight stage then
-// feeds both tiles' MMAs (see long_k_tile).
+//     residual is y itself, the in-place x += proj of the plain block).  In
+//     the gated form each lane quadrant holds 16 gate rows and the same
+//     features' up rows, paired by register shuffles.
+// The issuing thread's instruction rate bounds the MMA rate at N <= 192 (one
+// thread issues a 2-SM MMA every ~45 cycles at best), so its loop is kept
+// lean.  With long K a unit can hold two token tiles: each widened weight
+// stage then feeds both tiles' MMAs, each tile's accumulator is released on
+// its own barrier, and the tile width follows the wave count (long_k_tile).
 // With short K (every K stage fits the TMEM A stages at once) the weights stay
 // resident: each cluster takes a contiguous run of units, which share their
 // feature tiles except where the run crosses into the next feature pair; the
@@ -47,11 +52,10 @@
 // issuer waits on one barrier per stage.
 // TMEM: 2 accumulators of BN columns + as many A stages of 64 columns as fit
 // in the 512, fewer than the load stages (2 for BN = 192, 3 for 160 and for
-// 128 with two token tiles a unit, 4 for 128 and 64).  A stage is 8 MMAs deep, so the barrier round trip between
-// stages (about 0.1-0.2 us for the issuing thread) is amortised over 768
-// tensor-core cycles.  Every mbarrier wait is bounded (about 200 ms); a timeout sets
-// an error word that te_check() reports, the role stops, and the kernel still
-// waits for its own copies and MMAs and frees its TMEM.
+// 128 with two token tiles a unit, 4 for 128 and 64).  A stage is 8 MMAs
+// deep per token tile.  Every mbarrier wait is bounded (about 200 ms); a
+// timeout sets an error word that te_check() reports, the role stops, and the
+// kernel still waits for its own copies and MMAs and frees its TMEM.
 #include <cuda.h>
 
 #include <mutex>
