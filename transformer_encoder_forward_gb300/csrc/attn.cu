@@ -111,9 +111,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-__device__ __forceinline__ bool key_visible(int k, int qi, int len, int W) {
-    const int dq = qi - k;
-    return k < len && (W == 0 || (dq <= W && -dq <= W));
+// The keys row qi sees in the block that starts at key kv0, as offsets
+// [lo, hi] from kv0: key k is visible iff k < len and (W == 0 or |qi - k| <=
+// W); empty when hi < lo.  Two compares per key in the masked passes.
+struct KeySpan {
+    int lo, hi;
+    __device__ __forceinline__ bool has(int e) const { return e >= lo && e <= hi; }
+};
+__device__ __forceinline__ KeySpan key_span(int qi, int kv0, int len, int W) {
+    // clamped before any sum, so that no window size overflows
+    const int first = W > 0 && qi > W ? qi - W : 0;
+    const int last = W > 0 && W < len && qi < len - 1 - W ? qi + W : len - 1;
+    return {first - kv0, last - kv0};
 }
 
 // The two passes over one 128-key S row, loaded from TMEM once into registers
@@ -122,14 +131,15 @@ __device__ __forceinline__ bool key_visible(int k, int qi, int len, int W) {
 template <bool MASK>
 __device__ __forceinline__ float row_max_regs(const uint32_t (&v0)[64], const uint32_t (&v1)[64], int qi,
                                               int kv0, int len, int W) {
+    const KeySpan sp = key_span(qi, kv0, len, W);
     float m8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
     for (int e = 0; e < 64; ++e) {
         const float x0 = __uint_as_float(v0[e]), x1 = __uint_as_float(v1[e]);
-        if (!MASK || key_visible(kv0 + e, qi, len, W)) m8[e & 7] = fmaxf(m8[e & 7], x0);
-        if (!MASK || key_visible(kv0 + 64 + e, qi, len, W)) m8[e & 7] = fmaxf(m8[e & 7], x1);
+        if (!MASK || sp.has(e)) m8[e & 7] = fmaxf(m8[e & 7], x0);
+        if (!MASK || sp.has(64 + e)) m8[e & 7] = fmaxf(m8[e & 7], x1);
     }
     return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
@@ -141,6 +151,7 @@ __device__ __forceinline__ float row_max_regs(const uint32_t (&v0)[64], const ui
 template <bool MASK>
 __device__ __forceinline__ float row_exp_regs(uint32_t scol, const uint32_t (&v0)[64], const uint32_t (&v1)[64],
                                               float c, float nm, int qi, int kv0, int len, int W) {
+    const KeySpan sp = key_span(qi, kv0, len, W);
     float r8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) r8[i] = 0.f;
@@ -154,8 +165,8 @@ __device__ __forceinline__ float row_exp_regs(uint32_t scol, const uint32_t (&v0
             float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c, nm));
             if (MASK) {
                 const int k = kv0 + 64 * hh + 2 * e;
-                if (!key_visible(k, qi, len, W)) p0 = 0.f;
-                if (!key_visible(k + 1, qi, len, W)) p1 = 0.f;
+                if (!sp.has(k - kv0)) p0 = 0.f;
+                if (!sp.has(k - kv0 + 1)) p1 = 0.f;
             }
             r8[(2 * e) & 7] += p0;
             r8[(2 * e + 1) & 7] += p1;
