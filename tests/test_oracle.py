@@ -381,9 +381,16 @@ def _tiny(form, norm, gated, act, rope, qk_norm, window=0, bias=False):
                              rope, window, "all", bias, False, (9, 14))
 
 
-def _torch_block(cfg, p, x, cu, tables, next_norm):
+def _torch_block(cfg, p, x, cu, tables, next_norm, ple=None):
     """The same block written with torch's own library ops (linear, layer_norm,
-    scaled_dot_product_attention, gelu/silu, complex rotation for RoPE)."""
+    scaled_dot_product_attention, gelu/silu, complex rotation for RoPE).
+
+    With ``ple`` ({x_in, norm_w, scale}) the per-layer input path follows the
+    FFN residual as egemma2.rs ``TextGpu::forward`` "per-layer input" chains
+    it: mm(x_in, W_in) -> rms with pre-scale and the stack's norm weight ->
+    mm(h, W_gate) -> gelu of that gate times pin -> mm(z, W_proj) -> add_norm
+    with the layer's own post-norm weight and the layer scalar (the FFN's
+    add_norm before it takes scalar 1)."""
     t = lambda a: torch.as_tensor(np.asarray(a, np.float64))
     bf = lambda v: v.to(torch.float32).to(torch.bfloat16).to(torch.float64)
     f32 = lambda v: v.to(torch.float32).to(torch.float64)
@@ -437,15 +444,24 @@ def _torch_block(cfg, p, x, cu, tables, next_norm):
     if cfg.form == "plain":
         x = f32(x + lin(o, p["wo"]))
     else:
-        x = f32(x + F.rms_norm(f32(lin(o, p["wo"])), (cfg.d,), t(p["post_attn_w"]), cfg.eps))
+        x = f32((x + F.rms_norm(f32(lin(o, p["wo"])), (cfg.d,), t(p["post_attn_w"]), cfg.eps)) * cfg.post)
     a2 = bf(nrm(x, p["norm2_w"], p["norm2_b"]))
     g = lin(a2, p["wg"])
     actf = (lambda u: F.gelu(u, approximate="tanh")) if cfg.act == "gelu_tanh" else F.silu
     m = bf(actf(bf(g)) * bf(lin(a2, p["wu"]))) if cfg.gated else bf(actf(bf(g)))
     if cfg.form == "plain":
         x = f32(x + lin(m, p["wd"]))
+    elif ple is None:
+        x = f32((x + F.rms_norm(f32(lin(m, p["wd"])), (cfg.d,), t(p["post_ffn_w"]), cfg.eps)) * cfg.post)
     else:
         x = f32(x + F.rms_norm(f32(lin(m, p["wd"])), (cfg.d,), t(p["post_ffn_w"]), cfg.eps))
+        P = p["ple_in"]["q"].shape[0]
+        src = f32(lin(bf(t(ple["x_in"])), p["ple_in"]))
+        pin = bf(F.rms_norm(ple["scale"] * src, (P,), t(ple["norm_w"]), cfg.eps))
+        gate = bf(lin(bf(x), p["ple_gate"]))
+        z = bf(F.gelu(gate, approximate="tanh") * pin)
+        proj = f32(lin(z, p["ple_proj"]))
+        x = f32((x + F.rms_norm(proj, (cfg.d,), t(p["ple_post_w"]), cfg.eps)) * cfg.post)
     a_out = bf(nrm(x, *next_norm)) if next_norm is not None else None
     return x.numpy(), (a_out.numpy() if a_out is not None else None), a.numpy()
 
@@ -770,6 +786,37 @@ def _ple_case(seed=51):
     a = O.round_bf16(O.rms_norm(x, p["norm1_w"], cfg.eps))
     ple = dict(synth.draw_ple(cfg, seed), x_in=O.round_bf16(x))
     return cfg, p, cu, x, a, ple, synth.rope_tables(cfg, cfg.lens)
+
+
+def test_ple_block_matches_torch_library_composition():
+    # the per-layer input chain against torch's own ops, with a layer scalar
+    # other than 1 (it must follow the PLE residual, not the FFN's), pin as
+    # wide as d so that swapping the two norm weights would still run, and
+    # distinct, non-unit norm weights; a gelu on pin instead of the gate, the
+    # norm weights swapped or the scalar on the FFN residual all fail here
+    import dataclasses
+    cfg = dataclasses.replace(_tiny("sandwich", "rms", True, "gelu_tanh", "1d", True, 0),
+                              ple_dim=32, post=1.5)
+    p = synth.draw_layer(cfg, 0, 61)
+    lens = cfg.lens
+    cu = synth.cu_seqlens(lens)
+    x = synth.draw_x(int(cu[-1]), cfg.d, 62)
+    tables = synth.rope_tables(cfg, lens)
+    ple = dict(synth.draw_ple(cfg, 61), x_in=O.round_bf16(x))
+    ple["norm_w"] = ple["norm_w"] * 2.0 - 0.5            # far from ple_post_w
+    assert np.max(np.abs(ple["norm_w"] - p["ple_post_w"])) > 0.5
+    nxt = synth.draw_norm(np.random.default_rng(3), cfg.d, False)
+    x_ref, a_ref, a_in = _torch_block(cfg, p, x, cu, tables, nxt, ple=ple)
+    r = O.block_forward(cfg, p, x, a_in, cu, 0, tables, next_norm=nxt, ple=ple)
+    np.testing.assert_allclose(r["x_out"], x_ref, rtol=2e-5, atol=2e-5)
+    # a_out is bf16: the two sides may round a value on either side of a tie
+    # (one bf16 step, 2^-7 relative at most), and only rarely
+    diff = np.abs(r["a_out"] - a_ref)
+    assert np.all(diff <= 2.0 ** -7 * np.abs(a_ref) + 1e-30)
+    assert np.mean(diff > 0) < 0.05
+    # the branch is far from negligible, so the comparison sees it
+    base = O.block_forward(dataclasses.replace(cfg, ple_dim=0), p, x, a_in, cu, 0, tables)
+    assert np.linalg.norm(r["x_out"] - base["x_out"]) > 0.1 * np.linalg.norm(r["x_out"])
 
 
 @pytest.mark.parametrize("zeroed", ["ple_in", "ple_gate", "ple_proj"])
