@@ -344,21 +344,30 @@ te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, void *a,
                                const int32_t *cu_host, const int32_t *cu_dev, int32_t nseq,
                                void *workspace, size_t ws_bytes, te_stream stream);
 
+/* Size of the fixed scratch array of te_encoder_block_fwd_static (bytes). */
+#define TE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
 /* te_encoder_block_fwd_static: the same block as te_encoder_block_fwd, with
  * the same arguments and results, for callers that cannot allocate device
  * memory - e.g. an application whose device memory is all handed to its own
  * allocator and which forbids libraries from calling cudaMalloc, or a
  * latency-critical loop where no allocation may happen.  Such a caller has
  * no workspace to pass, so this entry point takes none: its scratch is one
- * fixed array in device memory owned by the library (32 MiB, 256-byte
- * aligned), which every GPU that loads the library holds until the process
- * exits.  Nothing is allocated or freed by a call.
- *   - Limit: te_encoder_block_workspace(desc, t) must be <= 32 MiB (about
- *     1,800 packed rows for a d=512, F=2048 block); larger t returns
- *     TE_EWORKSPACE before anything is launched.
- *   - The first call on each device looks up the array's device address
- *     with that device current; make that first call before any stream
- *     capture.
+ * fixed array in device memory owned by the library
+ * (TE_STATIC_SCRATCH_BYTES = 32 MiB, 256-byte aligned), which every GPU that
+ * loads the library holds until the process exits.  Nothing is allocated or
+ * freed by a call.
+ *   - Limit: te_encoder_block_workspace(desc, t) must be at most
+ *     TE_STATIC_SCRATCH_BYTES, i.e. t up to about TE_STATIC_SCRATCH_BYTES /
+ *     te_encoder_block_workspace(desc, 1) packed rows (a d=512, F=2048 block
+ *     needs 10,240 bytes a row: about 3,270 rows); larger t returns
+ *     TE_EWORKSPACE before anything is launched.  The descriptor is
+ *     validated first (TE_EINVAL / TE_ESHAPE / TE_EALIGN as for
+ *     te_encoder_block_fwd).
+ *   - The first call on each device (and the first after that device's
+ *     context was destroyed and recreated, e.g. by cudaDeviceReset) looks up
+ *     the array's device address with that device current; make that call
+ *     before any stream capture.
  *   - Every call shares the one array, which keeps the last call's contents.
  *     No part of it needs to start at zero (each scratch region is written
  *     before it is read).  Calls that overlap on the GPU - on different

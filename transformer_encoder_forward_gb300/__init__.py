@@ -20,6 +20,8 @@ TE_NORM_RMS, TE_NORM_LN = 0, 1
 TE_ACT_GELU_TANH, TE_ACT_SILU = 0, 1
 TE_RESID_PLAIN, TE_RESID_SANDWICH = 0, 1
 TE_EPI_NONE, TE_EPI_GELU_TANH, TE_EPI_SILU = 0, 1, 2
+# TE_STATIC_SCRATCH_BYTES of tefwd.h: the scratch array of te_encoder_block_fwd_static
+TE_STATIC_SCRATCH_BYTES = 32 << 20
 
 _STATUS = {0: "TE_OK", 1: "TE_EINVAL", 2: "TE_ESHAPE", 3: "TE_EALIGN", 4: "TE_EWORKSPACE",
            5: "TE_ECUDA", 6: "TE_EDEVICE"}

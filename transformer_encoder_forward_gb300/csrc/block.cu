@@ -67,7 +67,11 @@ te_status check_w(const te_q8w &w, int n, int k, const char *name) {
     return TE_OK;
 }
 
-te_status check_desc(const te_block_desc *d) {
+}  // namespace
+
+// Host validation of a block descriptor (shapes, pointers, alignment); also
+// used by te_encoder_block_fwd_static before it sizes its scratch.
+te_status check_block_desc(const te_block_desc *d) {
     if (!d) return fail(TE_EINVAL, "block: NULL descriptor");
     if (d->head_dim != 64 && d->head_dim != 128) return fail(TE_ESHAPE, "block: head_dim=%d", d->head_dim);
     if (d->n_heads < 1 || d->n_kv_heads < 1 || d->n_heads % d->n_kv_heads)
@@ -118,7 +122,6 @@ te_status check_desc(const te_block_desc *d) {
     return TE_OK;
 }
 
-}  // namespace
 }  // namespace tefwd
 
 using namespace tefwd;
@@ -132,7 +135,7 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
                                           const int32_t *cu_host, const int32_t *cu_dev,
                                           int32_t nseq, void *workspace, size_t ws_bytes,
                                           te_stream stream) {
-    te_status st = check_desc(desc);
+    te_status st = check_block_desc(desc);
     if (st != TE_OK) return st;
     const te_block_desc &d = *desc;
     if (!x || !a || !workspace) return fail(TE_EINVAL, "block: NULL x, a or workspace");

@@ -26,6 +26,9 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 te_status check_cu(const int32_t *cu_host, const int32_t *cu_dev, int32_t nseq,
                    int32_t *total, int32_t *max_len);
 
+// Host validation of an encoder block descriptor (block.cu).
+te_status check_block_desc(const te_block_desc *d);
+
 // Encodes a 2-D tiled TMA descriptor (row-major, `inner` elements per row,
 // `outer` rows, `row_bytes` apart) for a box of box_inner x box_outer.
 te_status make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
