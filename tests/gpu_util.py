@@ -1,5 +1,23 @@
-"""Helpers shared by the GPU parity tests (device transfers and error norms)."""
+"""Helpers shared by the GPU parity tests (device transfers, error norms and
+the record of each parity margin, printed at the end of the run)."""
+import json
+from pathlib import Path
+
 import numpy as np
+
+# (test, quantity, measured error, gate): printed by conftest's terminal summary
+MARGINS = []
+
+
+def record_margin(test: str, what: str, err: float, gate: float) -> float:
+    MARGINS.append((test, what, float(err), float(gate)))
+    return err
+
+
+def page_constant(name: str):
+    """A number the pages print (tests/golden/page_constants.json)."""
+    p = Path(__file__).resolve().parent / "golden" / "page_constants.json"
+    return json.loads(p.read_text())[name]
 
 
 def rel_frob(got, ref) -> float:

@@ -1,10 +1,14 @@
 """Per-op parity of the CUDA kernels (called through the C-ABI) against the
 CPU oracle on the same seeded inputs.
 
-Tolerances (relative Frobenius): 1e-3 per GEMM, 3e-3 for attention (bf16 P),
-2e-3 for row ops with bf16 outputs (the oracle rounds at the same storage
-points, so only rare rounding flips differ).  Integer work (int8 widening,
-index/mask computation) is compared bit for bit.
+Tolerances (relative Frobenius): 1e-3 per GEMM with a bf16 output, 3e-3 for
+attention (bf16 P), 2e-3 for row ops with bf16 outputs (the oracle rounds at
+the same storage points, so only rare rounding flips differ).  A GEMM with an
+f32 output reads the same bf16 x and exact int8 weights as the oracle, so only
+the f32 accumulation order differs: its gate is 20x the pages' own error level
+for that comparison (zimage.rs module doc, Measured: zi_q8mm against f64,
+5e-7).  Integer work (int8 widening, index/mask computation) is compared bit
+for bit.
 """
 import numpy as np
 import pytest
@@ -12,9 +16,16 @@ import pytest
 import transformer_encoder_forward_gb300 as te
 from oracle import encoder as O
 from transformer_encoder_forward_gb300 import synth
-from tests.gpu_util import bf16_input, q8_dev, rel_frob, to_dev, to_np
+from tests.gpu_util import bf16_input, page_constant, q8_dev, record_margin, rel_frob, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
+
+# f32-output GEMM gate: 20x the pages' rel. error of the q8 GEMM against f64
+GEMM_F32_TOL = 20 * page_constant("q8_gemm_rel_error_vs_f64")["value"]
+
+
+def _gemm_gate(ydt):
+    return GEMM_F32_TOL if ydt == "f32" else 1e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -91,10 +102,12 @@ def test_q8_linear_matches_oracle(m, k, ns, bias, resid, ydt):
         refs.append(O.round_bf16(ref) if ydt == "bf16" else ref)
     te.q8_linear(x, items)
     te.check()
-    for (y, (_, _, _, keep)), ref in zip(outs, refs):
+    gate = _gemm_gate(ydt)
+    for i, ((y, (_, _, _, keep)), ref) in enumerate(zip(outs, refs)):
         got = to_np(y)
         assert np.all(np.isfinite(got))
-        assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
+        e = record_margin("q8_linear", f"m={m} k={k} item {i} {ydt}", rel_frob(got, ref), gate)
+        assert e < gate, e
         if keep is not None:                   # the row padding of y is untouched
             assert bool(torch.isnan(keep[1][:, y.shape[1]:]).all())
 
@@ -221,7 +234,57 @@ def test_attention_matches_oracle(lens, nq, nkv, hd, window):
     ref = O.attention_varlen(qkv, cu, nq, nkv, hd, 0, nq * hd, (nq + nkv) * hd, window, scale)
     got = to_np(out)
     assert np.all(np.isfinite(got))
-    assert rel_frob(got, O.round_bf16(ref)) < 3e-3, rel_frob(got, ref)
+    e = record_margin("attention", f"lens={lens[:4]} hd={hd} W={window}", rel_frob(got, O.round_bf16(ref)), 3e-3)
+    assert e < 3e-3, e
+
+
+# More (sequence, query block) pairs than the launch parameters carry as a
+# longest-first work list: the launcher falls back to the plain grid
+# (query block, head, sequence).  A text batch of many short sequences.
+MANY_SEQ_CASES = [(700, 64, 1, 1, 0), (700, 64, 2, 2, 37), (660, 128, 2, 1, 0), (660, 128, 2, 2, 21)]
+
+
+@pytest.mark.parametrize("nseq,hd,nq,nkv,window", MANY_SEQ_CASES)
+def test_attention_many_short_sequences_plain_grid(nseq, hd, nq, nkv, window):
+    torch = _torch()
+    rng = np.random.default_rng([nseq, hd, nq, window])
+    lens = rng.integers(1, 201, nseq)
+    lens[:3] = [1, 200, 129]
+    qb = 128 if hd == 64 else 256                     # queries per CTA
+    assert int(np.sum((lens + qb - 1) // qb)) > 640   # beyond the work list
+    cu = synth.cu_seqlens(lens)
+    T = int(cu[-1])
+    W = (nq + 2 * nkv) * hd
+    qkv_t, qkv = bf16_input(rng, (T, W), 1.5)
+    scale = 1.0 / np.sqrt(hd)
+    out = _attn_run(qkv_t, cu, nq, nkv, hd, window, scale).clone()
+    te.check()
+    ref = O.attention_varlen(qkv, cu, nq, nkv, hd, 0, nq * hd, (nq + nkv) * hd, window, scale)
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    e = record_margin("attention plain grid", f"{nseq} seqs hd={hd} W={window}",
+                      rel_frob(got, O.round_bf16(ref)), 3e-3)
+    assert e < 3e-3, e
+    # other sequences and out-of-window keys have no effect, bit for bit:
+    # change every key/value row of the odd sequences and, with a window, the
+    # keys/values past each even sequence's first window + 1 rows
+    pert = qkv_t.clone()
+    keep = np.zeros(T, dtype=bool)       # query rows whose visible keys are unchanged
+    for s in range(nseq):
+        r0, r1 = int(cu[s]), int(cu[s + 1])
+        if s % 2:
+            pert[r0:r1, nq * hd:] = (torch.randn(r1 - r0, 2 * nkv * hd, device="cuda") * 40).to(torch.bfloat16)
+        elif window and r1 - r0 > 2 * window + 2:
+            cut = r0 + window + 1                      # rows from cut on change
+            pert[cut:r1, nq * hd:] = (torch.randn(r1 - cut, 2 * nkv * hd, device="cuda") * 40).to(torch.bfloat16)
+            keep[r0] = True                            # row r0 sees keys r0 .. r0 + window only
+        else:
+            keep[r0:r1] = True
+    out2 = _attn_run(pert, cu, nq, nkv, hd, window, scale)
+    te.check()
+    idx = torch.from_numpy(np.nonzero(keep)[0]).cuda()
+    assert idx.numel() > 0
+    assert torch.equal(out2[idx], out[idx])
 
 
 def test_attention_scale_one_and_length_one_sequences():
@@ -498,10 +561,12 @@ def test_block_format_gemm_matches_oracle(m, k, specs, ydt):
         checks.append((y, O.round_bf16(r) if ydt == "bf16" else r, dev))
     te.q8_linear(x, items)
     te.check()
-    for y, ref, _ in checks:
+    gate = _gemm_gate(ydt)
+    for i, (y, ref, _) in enumerate(checks):
         got = to_np(y)
         assert np.all(np.isfinite(got))
-        assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
+        e = record_margin("block-format GEMM", f"m={m} k={k} item {i} {ydt}", rel_frob(got, ref), gate)
+        assert e < gate, e
 
 
 @pytest.mark.parametrize("m,k,f", [(777, 768, 512), (1500, 384, 512), (1800, 256, 256)])
@@ -557,10 +622,12 @@ def test_q8_2f_gemm_matches_oracle(m, k, ns, ydt):
         checks.append((y, O.round_bf16(r) if ydt == "bf16" else r))
     te.q8_linear(x, items)
     te.check()
-    for y, ref in checks:
+    gate = _gemm_gate(ydt)
+    for i, (y, ref) in enumerate(checks):
         got = to_np(y)
         assert np.all(np.isfinite(got))
-        assert rel_frob(got, ref) < 1e-3, rel_frob(got, ref)
+        e = record_margin("q8_2f GEMM", f"m={m} k={k} item {i} {ydt}", rel_frob(got, ref), gate)
+        assert e < gate, e
 
 
 # ------------------------------------------------------- two-range items
