@@ -7,8 +7,12 @@ is captured once in a CUDA graph and replayed; L2 is flushed (a 512 MiB
 write) before every timed step and each step is timed with CUDA events on the
 launching stream.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2|c3|c4|c5|c1]
-                  [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5|c4|c3|c2|c1|...]
+                  [--impl ours|reference] [--op <one op of the workload>]
+
+The default workload is the largest one that fits one GPU: the 30-block DiT
+stack (d=3840, 30 heads x 128, SwiGLU 10240) over 2 x 4224 tokens (c5).  The
+smaller workloads stay available with --config.
 
 --impl reference times the CPU oracle (the plain f64 numpy restatement of
 the method, test infrastructure) on a bounded sample of the same workload on
@@ -62,7 +66,7 @@ def layer_flops(cfg, lens, layer):
     d, hd, H, KV, F = cfg.d, cfg.hd, cfg.heads, cfg.kv_heads, cfg.ffn
     gemm = 2 * T * (d * (H + 2 * KV) * hd + H * hd * d + d * F * (2 if cfg.gated else 1) + F * d
                     + 3 * d * cfg.ple_dim)
-    attn = 4 * hd * H * visible_pairs(lens, cfg.window_of(layer))
+    attn = 4 * hd * H * visible_pairs(synth.unit_lens(cfg, lens), cfg.window_of(layer))
     return gemm, attn
 
 
@@ -161,25 +165,40 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def build_stack(key, device, lens=None, x_seed_offset=0):
+def draw_layers(cfg, seed, n):
+    """The first n layers' seeded weights.  Each layer has its own generator
+    and numpy fills arrays without the GIL, so the draws run in threads (the
+    30-layer DiT stack holds 5.3 GB of int8 weights)."""
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(n, os.cpu_count() or 1, 16)) as ex:
+        return list(ex.map(lambda i: synth.draw_layer(cfg, i, seed, jitter=False), range(n)))
+
+
+def build_stack(key, device, lens=None, x_seed_offset=0, layers=None):
+    """The workload's stack on `device`; layers=n builds only its first n
+    layers (one op timed alone needs one layer's weights)."""
     from transformer_encoder_forward_gb300.model import EncoderStack
     cfg = synth.CONFIGS[key]
     lens = synth.draw_lens(cfg) if lens is None else np.asarray(lens, dtype=np.int32)
     seed = synth.config_seed(key)
-    layers = [synth.draw_layer(cfg, i, seed, jitter=False) for i in range(cfg.layers)]
+    ps = draw_layers(cfg, seed, cfg.layers if layers is None else layers)
     tables = synth.rope_tables(cfg, lens)
     fin = synth.draw_final_norm(cfg, seed) if cfg.pool else None
     ple = synth.draw_ple(cfg, seed) if cfg.ple_dim else None
-    st = EncoderStack(cfg, layers, lens, tables, fin, device=device, ple=ple)
+    st = EncoderStack(cfg, ps, lens, tables, fin, device=device, ple=ple,
+                      items=synth.attn_items(cfg, lens))
+    del ps   # the device holds the weights now
     x0 = synth.draw_x(st.T, cfg.d, seed + x_seed_offset)
-    return cfg, lens, st, x0, layers, tables
+    return cfg, lens, st, x0, tables
 
 
 def rank_lens(key, world, rank):
     """This rank's share of the packed batch of a `world`-GPU run."""
     from transformer_encoder_forward_gb300 import shard
     cfg = synth.CONFIGS[key]
-    if world == 1:
+    if world == 1 or cfg.cfg_pair:
+        # a CFG pair is one program over its items' interleaved ranges: every
+        # rank runs the whole one-GPU program (weak scaling)
         return synth.draw_lens(cfg)
     allv = shard.global_lens(cfg, world, lambda c, r: synth.draw_lens(c, synth.BASE_SEED + r))
     part = shard.partition(shard.sequence_costs(cfg, allv), world)
@@ -238,11 +257,14 @@ def workload_ops(cfg, st, torch):
     }
     for win in sorted({cfg.window_of(i) for i in range(nl)}):
         cnt = sum(1 for i in range(nl) if cfg.window_of(i) == win)
-        pairs = visible_pairs(st.lens, win)
-        ops[f"attn_w{win}"] = (
-            lambda s, win=win: te.attn_varlen_fwd(qkv, ldq, 0, qw, qw + kw, st.cu_host, st.cu_dev, H,
-                                                  KV, hd, win, cfg.scale, o, qw, stream=s),
-            4 * hd * H * pairs, T * ldq * 2 + T * qw * 2, cnt, "tensor")
+        pairs = visible_pairs(synth.unit_lens(cfg, st.lens), win)
+        if st.items_host is not None:     # two-range items (the CFG pair)
+            fn = lambda s, win=win: te.attn_items_fwd(qkv, ldq, 0, qw, qw + kw, st.items_host, st.items_dev,
+                                                      T, H, KV, hd, win, cfg.scale, o, qw, stream=s)
+        else:
+            fn = lambda s, win=win: te.attn_varlen_fwd(qkv, ldq, 0, qw, qw + kw, st.cu_host, st.cu_dev, H,
+                                                       KV, hd, win, cfg.scale, o, qw, stream=s)
+        ops[f"attn_w{win}"] = (fn, 4 * hd * H * pairs, T * ldq * 2 + T * qw * 2, cnt, "tensor")
     if cfg.qk_norm or cfg.rope or cfg.v_norm:
         vw = kw if cfg.v_norm else 0
         ops["qk_prep"] = (lambda s: te.qkv_prep_rope(
@@ -339,7 +361,7 @@ def run_op(args):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     te.lib()
-    cfg, lens, st, _, _, _ = build_stack(args.config, dev)
+    cfg, lens, st, _, _ = build_stack(args.config, dev, layers=1)
     ops = workload_ops(cfg, st, torch)
     fn, flops, nbytes, count, bound = ops[args.op]
     stream = torch.cuda.current_stream()
@@ -374,7 +396,7 @@ def run_ours(args):
     import transformer_encoder_forward_gb300 as te
     from transformer_encoder_forward_gb300 import shard
     te.lib()
-    cfg, lens, st, x0_np, _, _ = build_stack(args.config, dev, rank_lens(args.config, world, rank),
+    cfg, lens, st, x0_np, _ = build_stack(args.config, dev, rank_lens(args.config, world, rank),
                                              x_seed_offset=rank)
     T = st.T
     gflops, aflops = forward_flops(cfg, lens)
@@ -510,7 +532,15 @@ def cpu_sample(key):
     cfg = synth.CONFIGS[key]
     lens = synth.draw_lens(cfg)
     seed = synth.config_seed(key)
-    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1, "c3q8": 1, "c3q4": 1, "c4f": 1, "c2v": 6, "c2p": 6}[key]
+    take = {"c1": 2, "c2": 6, "c3": 1, "c4": 1, "c5": 1, "c4m": 1, "c5m": 1, "c3q8": 1, "c3q4": 1, "c4f": 1,
+            "c2v": 6, "c2p": 6, "c4c": 1}[key]
+    if cfg.cfg_pair:
+        # the first item's rows (image and caption) attended as one sequence,
+        # which is what an item is
+        import dataclasses
+        cfg = dataclasses.replace(cfg, cfg_pair=False)
+        sl = np.asarray([int(synth.unit_lens(synth.CONFIGS[key], lens)[0])], dtype=np.int32)
+        return cfg, sl, seed
     sl = lens[:take]
     if key in ("c4", "c5", "c4m", "c5m", "c4f"):
         sl = np.asarray([min(int(sl[0]), 1056)], dtype=np.int32)
@@ -598,7 +628,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="c2", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--config", default="c5", choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -322,6 +322,17 @@ typedef struct {
     te_q8w ple_in, ple_gate, ple_proj;
     const float *ple_norm_w, *ple_post_w;
     const void *ple_x;
+    /* two-range attention items ([ZI] module doc "The chain": the CFG pair is
+     * one batch-2 program over rows [img0 | img1 | cap0 | cap1], every
+     * row-local step runs once over all rows and attention runs per item over
+     * its two row ranges; PFa {img_off, n_img, cap_off, n_cap}), or
+     * n_attn_items == 0 (attention per cu_seqlens sequence).  With items the
+     * attention step is te_attn_items_fwd over attn_items_host / _dev (int32
+     * [n_attn_items, 4] = off1, len1, off2, len2; the same table on the host
+     * and, 16-byte aligned, on the device); the items must cover every row of
+     * [0, t) exactly once, and cu_seqlens then only gives t. */
+    const int32_t *attn_items_host, *attn_items_dev;
+    int32_t n_attn_items;
 } te_block_desc;
 
 /* Workspace bytes te_encoder_block_fwd needs for t packed rows. */

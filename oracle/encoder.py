@@ -404,7 +404,7 @@ def pool_mean(x, cu, w, eps):
 
 
 def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mod=None,
-                  next_mod_scale=None, ple=None):
+                  next_mod_scale=None, ple=None, items=None):
     """One encoder block, step by step; returns every stored intermediate.
 
     cfg: a BlockConfig-like object (d, heads, kv_heads, hd, ffn, gated, act,
@@ -428,6 +428,12 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mo
     after the FFN residual (taken with post 1) pin = rms(scale * x_in W_in^T)
     ple_norm, z = gelu_tanh(bf16(x) W_gate^T) * pin, and
     x = (x + rms(z W_proj^T) w_ple) * post.
+    Two-range attention items (zimage.rs module doc "The chain": the CFG pair
+    is one batch-2 program over rows [img0 | img1 | cap0 | cap1], every
+    row-local step runs once over all rows and attention runs per item over
+    its two row ranges; ``PFa``): with ``items`` ([n, 4] = off1, len1, off2,
+    len2) the attention step is ``attention_items`` instead of the
+    per-sequence attention; ``cu`` then only gives the row count.
     ``rows`` restricts the block to sampled query rows: q|k|v is computed for
     every row (all keys are needed), everything after attention only for the
     sampled rows (it is row-local), and the returned post-attention
@@ -459,8 +465,11 @@ def block_forward(cfg, p, x, a, cu, layer, tables, next_norm=None, rows=None, mo
                       eps, tables["cos"], tables["sin"], tables["pos"], tables["sec"], 1.0,
                       v_off=qw + kw if v_norm else None)
     r["qkv"] = qkv
-    o = attention_varlen(qkv, cu, H, KV, hd, 0, qw, qw + kw, cfg.window_of(layer),
-                         cfg.scale, rows=rows)
+    if items is not None:
+        o = attention_items(qkv, items, H, KV, hd, 0, qw, qw + kw, cfg.window_of(layer), cfg.scale)
+    else:
+        o = attention_varlen(qkv, cu, H, KV, hd, 0, qw, qw + kw, cfg.window_of(layer),
+                             cfg.scale, rows=rows)
     if rows is not None:
         rows = np.asarray(rows)
         o, x = o[rows], x[rows]

@@ -14,7 +14,7 @@ import transformer_encoder_forward_gb300 as te
 from oracle import encoder as O
 from transformer_encoder_forward_gb300 import synth
 from transformer_encoder_forward_gb300.model import EncoderStack
-from tests.gpu_util import rel_frob, to_dev, to_np
+from tests.gpu_util import record_margin, rel_frob, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +26,7 @@ def _stack(cfg, lens, layers, seed=11, jitter=True):
     tables = synth.rope_tables(cfg, lens)
     fin = synth.draw_final_norm(cfg, seed) if cfg.pool else None
     ple = synth.draw_ple(cfg, seed) if cfg.ple_dim else None
-    st = EncoderStack(cfg, ps, lens, tables, fin, ple=ple)
+    st = EncoderStack(cfg, ps, lens, tables, fin, ple=ple, items=synth.attn_items(cfg, lens))
     st.ple_host = ple
     return st, ps, tables
 
@@ -42,7 +42,7 @@ def _mods(ps, i):
     return mod, nxt
 
 
-def _check_layer(cfg, st, ps, tables, i, x, a, rows=None):
+def _check_layer(cfg, st, ps, tables, i, x, a, rows=None, tag=None):
     """Runs GPU layer i in place on (x, a) and compares against the oracle on
     the same inputs."""
     import torch
@@ -54,17 +54,18 @@ def _check_layer(cfg, st, ps, tables, i, x, a, rows=None):
     if st.ple_x is not None:
         ple = dict(st.ple_host, x_in=to_np(st.ple_x))
     r = O.block_forward(cfg, ps[i], x_in, a_in, st.cu_host, i, tables, _next_norm(ps, i),
-                        rows=rows, mod=mod, next_mod_scale=next_s, ple=ple)
+                        rows=rows, mod=mod, next_mod_scale=next_s, ple=ple, items=st.items_host)
     sel = slice(None) if rows is None else np.asarray(rows)
     got_x = to_np(x)[sel]
     xin = x_in[sel]
     assert np.all(np.isfinite(got_x))
-    e_x = rel_frob(got_x, r["x_out"])
-    e_d = rel_frob(got_x - xin, r["x_out"] - xin)
+    tag = f"{tag or cfg.name} layer {i}"
+    e_x = record_margin("block", f"{tag} x_out", rel_frob(got_x, r["x_out"]), TOL)
+    e_d = record_margin("block", f"{tag} x_out - x_in", rel_frob(got_x - xin, r["x_out"] - xin), 2 * TOL)
     assert e_x < TOL, (i, e_x)
     assert e_d < 2 * TOL, (i, e_d)
     if r["a_out"] is not None:
-        e_a = rel_frob(to_np(a)[sel], r["a_out"])
+        e_a = record_margin("block", f"{tag} a_out", rel_frob(to_np(a)[sel], r["a_out"]), TOL)
         assert e_a < TOL, (i, e_a)
     return e_x, e_d
 
@@ -87,6 +88,9 @@ FORMS = {
     "c2p_small": ("c2p", dict(layers=2, window=40), (100, 1, 300, 37)),
     # the DiT block with q8_2f weights (column field)
     "c4f_small": ("c4f", dict(layers=2, d=512, heads=4, kv_heads=4, ffn=1024), (150, 133)),
+    # the DiT block as the CFG pair's batch-2 program: rows [img0 | img1 |
+    # cap0 | cap1], attention per two-range item
+    "c4c_small": ("c4c", dict(layers=2, d=512, heads=4, kv_heads=4, ffn=1024), (256, 256, 64, 32)),
 }
 
 
@@ -106,7 +110,7 @@ def test_block_forms_match_oracle(name):
                              mod_scale=s0))
     assert rel_frob(to_np(a), a0) < 2e-3
     for i in range(cfg.layers):
-        _check_layer(cfg, st, ps, tables, i, x, a)
+        _check_layer(cfg, st, ps, tables, i, x, a, tag=name)
 
 
 def test_text_stack_24_layers_teacher_forced_and_pooled():
@@ -165,6 +169,48 @@ def test_dit_block_with_adaln_full_size():
     a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
     st.input_norm(x, a)
     _check_layer(cfg, st, ps, tables, 0, x, a)
+
+
+def test_dit_cfg_pair_block_full_size():
+    import torch
+    cfg = synth.CONFIGS["c4c"]
+    lens = synth.draw_lens(cfg)
+    st, ps, tables = _stack(cfg, lens, 1, jitter=False)
+    assert st.items_host is not None and st.T == 2240
+    x = to_dev(synth.draw_x(st.T, cfg.d, 6))
+    a = torch.empty(st.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    st.input_norm(x, a)
+    _check_layer(cfg, st, ps, tables, 0, x, a)
+
+
+def test_cfg_pair_block_equals_the_block_over_gathered_items_bit_exactly():
+    # every step but attention works per row, and an item's attention equals
+    # the attention of its rows gathered into one sequence: the block over
+    # [img0 | img1 | cap0 | cap1] with items must give, row for row, the same
+    # bits as the block over [img0 | cap0 | img1 | cap1] with one sequence per
+    # item (each row keeping its RoPE angles)
+    import dataclasses
+    import torch
+    cfg = synth.small_config("c4c", layers=2, d=512, heads=4, kv_heads=4, ffn=1024,
+                             lens=(256, 256, 96, 32))
+    lens = cfg.lens
+    st, ps, tables = _stack(cfg, lens, 2)
+    perm = np.r_[0:256, 512:608, 256:512, 608:640]
+    plain = dataclasses.replace(cfg, cfg_pair=False, lens=(352, 288))
+    tab_g = dict(tables, cos=tables["cos"][perm], sin=tables["sin"][perm])
+    st_g = EncoderStack(plain, ps, plain.lens, tab_g)
+    assert st_g.items_host is None
+    x0 = synth.draw_x(st.T, cfg.d, 13)
+    x, a, _ = st.buffers()
+    x.copy_(to_dev(x0))
+    st.forward_device(x, a)
+    xg, ag, _ = st_g.buffers()
+    xg.copy_(to_dev(x0[perm]))
+    st_g.forward_device(xg, ag)
+    te.check()
+    idx = torch.from_numpy(perm).cuda()
+    assert torch.equal(x[idx], xg)
+    assert torch.equal(a[idx], ag)
 
 
 def test_dit_stack_layer_at_4224_tokens_sampled_rows():

@@ -772,6 +772,55 @@ def test_two_range_items_reduce_to_varlen_and_ignore_range_order_without_window(
     np.testing.assert_allclose(sw[rows], it[rows], rtol=1e-12, atol=1e-12)
 
 
+# ------------------------------------------- two-range items inside the block
+# zimage.rs module doc "The chain": the CFG pair is one batch-2 program over
+# rows [img0 | img1 | cap0 | cap1]; row-local steps run once over all rows and
+# attention runs per item over its two row ranges.
+
+def _cfg_pair_case(window=0):
+    import dataclasses
+    cfg = dataclasses.replace(_tiny("sandwich", "rms", True, "silu", "2d", True, window),
+                              lens=(12, 12, 5, 3), cfg_pair=True)
+    p = synth.draw_layer(cfg, 0, 71)
+    lens = cfg.lens
+    cu = synth.cu_seqlens(lens)
+    x = synth.draw_x(int(cu[-1]), cfg.d, 72)
+    a = O.round_bf16(O.rms_norm(x, p["norm1_w"], cfg.eps))
+    return cfg, p, lens, cu, x, a
+
+
+@pytest.mark.parametrize("window", [0, 4])
+def test_cfg_pair_block_equals_the_gathered_items_as_sequences(window):
+    # the block over [img0 | img1 | cap0 | cap1] with items equals, row for
+    # row, the plain block over the rows gathered as [img0 | cap0 | img1 |
+    # cap1] with one sequence per item and each row keeping its RoPE angles
+    import dataclasses
+    cfg, p, lens, cu, x, a = _cfg_pair_case(window)
+    items = synth.attn_items(cfg, lens)
+    assert items.tolist() == [[0, 12, 24, 5], [12, 12, 29, 3]]
+    tables = synth.rope_tables(cfg, lens)
+    r = O.block_forward(cfg, p, x, a, cu, 0, tables, next_norm=(p["norm1_w"], None), items=items)
+    perm = np.r_[0:12, 24:29, 12:24, 29:32]
+    plain = dataclasses.replace(cfg, cfg_pair=False, lens=(17, 15))
+    tab_g = dict(tables, cos=tables["cos"][perm], sin=tables["sin"][perm])
+    g = O.block_forward(plain, p, x[perm], a[perm], synth.cu_seqlens([17, 15]), 0, tab_g,
+                        next_norm=(p["norm1_w"], None))
+    np.testing.assert_array_equal(r["x_out"][perm], g["x_out"])
+    np.testing.assert_array_equal(r["a_out"][perm], g["a_out"])
+    # and it is not the per-range attention: the caption rows see the image
+    sep = O.block_forward(cfg, p, x, a, cu, 0, tables, next_norm=(p["norm1_w"], None))
+    assert not np.allclose(sep["x_out"][24:], r["x_out"][24:])
+
+
+def test_block_with_single_range_items_equals_the_sequence_block():
+    cfg, p, lens, cu, x, a = _cfg_pair_case()
+    tables = synth.rope_tables(cfg, lens)
+    items = np.asarray([[int(cu[i]), int(lens[i]), 0, 0] for i in range(len(lens))], dtype=np.int32)
+    r = O.block_forward(cfg, p, x, a, cu, 0, tables, items=items)
+    q = O.block_forward(cfg, p, x, a, cu, 0, tables)
+    np.testing.assert_array_equal(r["x_out"], q["x_out"])
+
+
 # ------------------------------------------------------ per-layer input (PLE)
 # egemma2.rs TextGpu::forward "per-layer input": pin = rms(ple_scale * x W_in^T)
 # ple_norm; z = gelu(h W_gate^T) * pin; H = (H + rms(z W_proj^T) w) * scalar.

@@ -59,7 +59,8 @@ class te_block_desc(ctypes.Structure):
                 ("rope_pos", c_p), ("rope_sec", c_i32), ("rope_rows", c_i32),
                 ("mod", c_p), ("next_mod_scale", c_p), ("v_norm", c_i32),
                 ("ple_dim", c_i32), ("ple_scale", c_f32), ("ple_in", te_q8w), ("ple_gate", te_q8w),
-                ("ple_proj", te_q8w), ("ple_norm_w", c_p), ("ple_post_w", c_p), ("ple_x", c_p)]
+                ("ple_proj", te_q8w), ("ple_norm_w", c_p), ("ple_post_w", c_p), ("ple_x", c_p),
+                ("attn_items_host", c_p), ("attn_items_dev", c_p), ("n_attn_items", c_i32)]
 
 
 _lib = None

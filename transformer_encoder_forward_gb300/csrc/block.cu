@@ -17,6 +17,8 @@
 //   qkv bf16 [t, (nq + 2 nkv) hd] | o bf16 [t, nq hd] | tmp f32 [t, d] | m bf16 [t, F]
 //   and with the per-layer input path: pin f32 [t, P] | panel bf16 [t, 2P] |
 //   z bf16 [t, P] | bf16 copy of x [t, d]
+#include <vector>
+
 #include "common.cuh"
 
 namespace tefwd {
@@ -122,6 +124,30 @@ te_status check_block_desc(const te_block_desc *d) {
     return TE_OK;
 }
 
+// With two-range attention items every row's attention output comes from
+// exactly one item: the items' ranges must tile [0, t) (the rest of each
+// item's checks is te_attn_items_fwd's).
+te_status check_items_cover(const te_block_desc &d, int32_t t) {
+    if (!d.attn_items_host || !d.attn_items_dev) return fail(TE_EINVAL, "block: NULL attention items");
+    std::vector<uint8_t> seen((size_t)t, 0);
+    for (int32_t i = 0; i < d.n_attn_items; ++i) {
+        const int32_t *it = d.attn_items_host + 4 * i;
+        for (int r = 0; r < 2; ++r) {
+            const int32_t off = it[2 * r], len = it[2 * r + 1];
+            if (off < 0 || len < 0 || (int64_t)off + len > t)
+                return fail(TE_EINVAL, "block: attention item %d range %d (%d, %d) outside the %d rows", i, r,
+                            off, len, t);
+            for (int32_t j = off; j < off + len; ++j) {
+                if (seen[j]) return fail(TE_EINVAL, "block: row %d is in two attention items", j);
+                seen[j] = 1;
+            }
+        }
+    }
+    for (int32_t j = 0; j < t; ++j)
+        if (!seen[j]) return fail(TE_EINVAL, "block: row %d is in no attention item", j);
+    return TE_OK;
+}
+
 }  // namespace tefwd
 
 using namespace tefwd;
@@ -143,6 +169,8 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
     if ((st = check_cu(cu_host, cu_dev, nseq, &t, &max_len)) != TE_OK) return st;
     if (d.rope_sec && !d.rope_pos && d.rope_rows < t)
         return fail(TE_ESHAPE, "block: RoPE table has %d rows for %d packed rows", d.rope_rows, t);
+    if (d.n_attn_items < 0) return fail(TE_EINVAL, "block: n_attn_items=%d", d.n_attn_items);
+    if (d.n_attn_items > 0 && (st = check_items_cover(d, t)) != TE_OK) return st;
     const WsLayout L = ws_layout(d, t);
     if (ws_bytes < L.total)
         return fail(TE_EWORKSPACE, "block: workspace %zu bytes, need %zu", ws_bytes, L.total);
@@ -172,10 +200,14 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
                                    d.rope_rows, d.rope_sec, d.q_mul, t, stream)) != TE_OK)
             return st;
     }
-    // 3. attention
-    if ((st = te_attn_varlen_fwd(qkv, ldqkv, 0, qw, qw + kw, cu_host, cu_dev, nseq, H, KV, hd,
-                                 d.window, d.attn_scale, o, qw, stream)) != TE_OK)
-        return st;
+    // 3. attention: per sequence, or per two-range item
+    if (d.n_attn_items > 0)
+        st = te_attn_items_fwd(qkv, ldqkv, 0, qw, qw + kw, d.attn_items_host, d.attn_items_dev,
+                               d.n_attn_items, t, H, KV, hd, d.window, d.attn_scale, o, qw, stream);
+    else
+        st = te_attn_varlen_fwd(qkv, ldqkv, 0, qw, qw + kw, cu_host, cu_dev, nseq, H, KV, hd,
+                                d.window, d.attn_scale, o, qw, stream);
+    if (st != TE_OK) return st;
     // 4. O projection: plain form adds into x in the epilogue
     te_q8_item io = plain ? te_q8_item{d.wo, x, D, TE_F32, 0, x, D}
                           : te_q8_item{d.wo, tmp, D, TE_F32, 0, nullptr, 0};

@@ -63,7 +63,11 @@ class EncoderStack:
     """A stack of encoder blocks over a packed batch with fixed lengths."""
 
     def __init__(self, cfg, layers: List[dict], lens, tables: dict,
-                 final_norm: Optional[np.ndarray] = None, device="cuda", ple: Optional[dict] = None):
+                 final_norm: Optional[np.ndarray] = None, device="cuda", ple: Optional[dict] = None,
+                 items: Optional[np.ndarray] = None):
+        """items: two-range attention items, int32 [n, 4] = (off1, len1,
+        off2, len2) covering every row once (the CFG pair's batch-2 program,
+        zimage.rs); None: attention per sequence of ``lens``."""
         import torch
         self.cfg = cfg
         self.device = torch.device(device)
@@ -89,6 +93,10 @@ class EncoderStack:
             self.ple_x = torch.empty(self.T, cfg.d, dtype=torch.bfloat16, device=self.device)
             self.ple_norm = _dev(ple["norm_w"], self.device, torch.float32)
             self.ple_scale = float(ple["scale"])
+        self.items_host = self.items_dev = None
+        if items is not None:
+            self.items_host = np.ascontiguousarray(np.asarray(items, dtype=np.int32).reshape(-1, 4))
+            self.items_dev = torch.from_numpy(self.items_host).to(self.device)
         self.descs = [self._desc(i) for i in range(len(self.layers))]
         ws = max(block_workspace(d, self.T) for d in self.descs)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
@@ -121,6 +129,10 @@ class EncoderStack:
             d.ple_in, d.ple_gate, d.ple_proj = (q8w(*L.t[k]) for k in ("ple_in", "ple_gate", "ple_proj"))
             d.ple_norm_w, d.ple_post_w = ptr(self.ple_norm), ptr(L.t["ple_post_w"])
             d.ple_x = ptr(self.ple_x)
+        if self.items_host is not None:
+            d.attn_items_host = self.items_host.ctypes.data
+            d.attn_items_dev = ptr(self.items_dev)
+            d.n_attn_items = self.items_host.shape[0]
         if cfg.qk_norm:
             d.q_norm, d.k_norm = ptr(L.t["q_norm"]), ptr(L.t["k_norm"])
         if self.rope_sec:

@@ -69,6 +69,11 @@ class BlockConfig:
     codec: str = "q8_row"  # weight format: "q8_row" | "q8_2f" | "q8_0" | "q4_0"
     v_norm: bool = False   # RMS-normalise the v heads too (egemma2.rs Prog::qkv "v norm")
     ple_dim: int = 0       # per-layer input width (egemma2.rs "per-layer input"), 0 = none
+    # CFG pair (zimage.rs, module doc "The chain": the CFG pair is one batch-2
+    # program with rows [img0 | img1 | cap0 | cap1]; attention runs per item
+    # over its two row ranges): ``lens`` lists the ranges in row order, the
+    # first half image ranges, the second half the matching caption ranges
+    cfg_pair: bool = False
 
     def window_of(self, layer: int) -> int:
         if self.window == 0:
@@ -115,6 +120,12 @@ CONFIGS["c4f"] = dataclasses.replace(CONFIGS["c4"], name="c4f_dit_block_q8_2f_d3
 # vision_encoder_gpu.rs (Q8_0, Q4_0) in place of q8_row.
 CONFIGS["c3q8"] = dataclasses.replace(CONFIGS["c3"], name="c3q8_vit_stack16_q8_0_d768", codec="q8_0")
 CONFIGS["c3q4"] = dataclasses.replace(CONFIGS["c3"], name="c3q4_vit_stack16_q4_0_d768", codec="q4_0")
+# The DiT block as the CFG batch-2 program: two items, each a 32 x 32 patch
+# image (1024 rows) with its caption (160 rows for the prompt, 32 for the
+# empty prompt; caption lengths padded to multiples of 32 as zimage.rs pads
+# them), rows [img0 | img1 | cap0 | cap1], joint 2-D RoPE positions.
+CONFIGS["c4c"] = dataclasses.replace(CONFIGS["c4"], name="c4c_dit_block_cfg_pair_d3840",
+                                     lens=(1024, 1024, 160, 32), cfg_pair=True)
 
 
 def config_seed(key: str) -> int:
@@ -128,6 +139,41 @@ def draw_lens(cfg: BlockConfig, seed: int = BASE_SEED) -> np.ndarray:
         return np.asarray(cfg.lens, dtype=np.int32)
     rng = np.random.default_rng(seed)
     return rng.integers(cfg.len_lo, cfg.len_hi + 1, cfg.n_seqs).astype(np.int32)
+
+
+def attn_items(cfg: BlockConfig, lens) -> Optional[np.ndarray]:
+    """The two-range attention items of a CFG-pair packing, int32 [n, 4] =
+    (image offset, image rows, caption offset, caption rows) per item, or
+    None when every range of ``lens`` is its own sequence."""
+    if not cfg.cfg_pair:
+        return None
+    lens = np.asarray(lens, dtype=np.int64)
+    n = len(lens) // 2
+    cu = cu_seqlens(lens).astype(np.int64)
+    return np.asarray([[cu[i], lens[i], cu[n + i], lens[n + i]] for i in range(n)], dtype=np.int32)
+
+
+def unit_lens(cfg: BlockConfig, lens) -> np.ndarray:
+    """Lengths of the attention units: the items' joint lengths for a
+    CFG pair, else the sequences themselves."""
+    it = attn_items(cfg, lens)
+    if it is None:
+        return np.asarray(lens, dtype=np.int64)
+    return (it[:, 1].astype(np.int64) + it[:, 3])
+
+
+def joint_positions(cfg: BlockConfig, lens) -> np.ndarray:
+    """Each packed row's position within its attention unit (a CFG item's
+    caption rows follow its image rows)."""
+    it = attn_items(cfg, lens)
+    lens = np.asarray(lens, dtype=np.int64)
+    if it is None:
+        return np.concatenate([np.arange(n) for n in lens]).astype(np.int64)
+    pos = np.empty(int(lens.sum()), dtype=np.int64)
+    for off1, len1, off2, len2 in it.astype(np.int64):
+        pos[off1:off1 + len1] = np.arange(len1)
+        pos[off2:off2 + len2] = len1 + np.arange(len2)
+    return pos
 
 
 def cu_seqlens(lens) -> np.ndarray:
@@ -253,17 +299,17 @@ def rope_tables(cfg: BlockConfig, lens) -> dict:
 
     1-D (text): angle(p, i) = p * 10000^(-2i/hd); positions restart at 0 in
     every sequence, table rows indexed by position.  2-D (DiT/vision): one
-    table row per packed row; (r, c) = divmod(index in sequence, 32); the
+    table row per packed row; (r, c) = divmod(index in sequence, 32) (for a
+    CFG item, the joint index: its caption rows follow its image rows); the
     first hd/4 entries rotate by the column c, the next hd/4 by the row r,
     each with 10000^(-2i/(hd/2)); ``sec = hd/2``.
     """
     if cfg.rope is None:
         return {"cos": None, "sin": None, "pos": None, "sec": 0}
-    lens = np.asarray(lens, dtype=np.int64)
     hd = cfg.hd
-    local = np.concatenate([np.arange(n) for n in lens]).astype(np.int64)
+    local = joint_positions(cfg, lens)
     if cfg.rope == "1d":
-        P = int(lens.max())
+        P = int(local.max()) + 1
         i = np.arange(hd // 2, dtype=np.float64)
         inv = 10000.0 ** (-2.0 * i / hd)
         ang = np.arange(P, dtype=np.float64)[:, None] * inv[None, :]
