@@ -183,7 +183,8 @@ struct TileCoord {
 
 // Work units are (pair of 128-row feature tiles, BN-token tile).  The two CTAs
 // of a cluster take the two feature tiles of one unit: they share the token
-// tile, so each loads half of it and multicasts that half to both.  Feature
+// tile, and each CTA TMA-loads its own half of it into its own shared memory
+// (no load is multicast); the 2-SM MMA reads both halves.  Feature
 // tile major, token tiles fastest: clusters running together share weight
 // tiles, and the activation (re-read once per feature pair) stays in L2.  A
 // feature tile past the last one (odd count) is a phantom: its weights read
@@ -945,7 +946,7 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         bn = lt.bn;
         tpa = lt.tpa;
     }
-    // each CTA of a cluster pair loads half of the token tile (and multicasts it)
+    // each CTA of a cluster pair TMA-loads its own half of the token tile
     te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
                                (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_OK) return st;
