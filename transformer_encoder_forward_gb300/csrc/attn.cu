@@ -263,93 +263,95 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
 
     if (warp == L::TMA_WARP) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&p.map);
-            // 128 joint positions from j0 at column col: one box, or four
-            // 32-row boxes when the tile spans the two ranges (len1 % 32 == 0)
-            auto load_tile = [&](uint32_t dst, int col, int j0, uint32_t bar) {
-                if (len2 == 0 || j0 + BQ <= len1 || j0 >= len1) {
-                    tma_load_2d(dst, &p.map, bar, col, row_of(j0));
-                } else {
+        // (the whole warp in step, one elected lane issues)
+        const uint32_t e = elect_one();
+        if (e) tma_prefetch_desc(&p.map);
+        // 128 joint positions from j0 at column col: one box, or four
+        // 32-row boxes when the tile spans the two ranges (len1 % 32 == 0)
+        auto load_tile = [&](uint32_t dst, int col, int j0, uint32_t bar) {
+            if (len2 == 0 || j0 + BQ <= len1 || j0 >= len1) {
+                tma_load_2d_e(dst, &p.map, bar, col, row_of(j0), e);
+            } else {
 #pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        tma_load_2d(dst + r * 32 * 128, &p.map32, bar, col, row_of(j0 + 32 * r));
-                }
-            };
-            mbar_arrive_expect_tx(bar_q, ntile * L::TILE);
-            for (int w = 0; w < ntile; ++w)
-                for (int c = 0; c < L::NB; ++c)
-                    load_tile(sb + L::Q_OFF + w * L::TILE + c * 16384, p.q_off + h * HD + 64 * c,
-                              q0 + w * BQ, bar_q);
-            int j = 0;
-            for (; j < n; ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(bar_kve + 8 * st, ((j >> 1) & 1) ^ 1)) { ok = false; break; }
-                const int jk = (kt0 + j) * BKV;
-                mbar_arrive_expect_tx(bar_kf + 8 * st, L::TILE);
-                for (int c = 0; c < L::NB; ++c)
-                    load_tile(sb + L::K_OFF + st * L::TILE + c * 16384, p.k_off + g * HD + 64 * c, jk,
-                              bar_kf + 8 * st);
-                mbar_arrive_expect_tx(bar_vf + 8 * st, L::TILE);
-                for (int c = 0; c < L::NB; ++c)
-                    load_tile(sb + L::V_OFF + st * L::TILE + c * 16384, p.v_off + g * HD + 64 * c, jk,
-                              bar_vf + 8 * st);
+                for (int r = 0; r < 4; ++r)
+                    tma_load_2d_e(dst + r * 32 * 128, &p.map32, bar, col, row_of(j0 + 32 * r), e);
             }
-            // no copy of ours may still be landing when the CTA exits
-            mbar_wait(bar_q, 0, 20000000ull);
-            for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) {
-                mbar_wait(bar_kf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
-                mbar_wait(bar_vf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
-            }
+        };
+        mbar_arrive_expect_tx_e(bar_q, ntile * L::TILE, e);
+        for (int w = 0; w < ntile; ++w)
+            for (int c = 0; c < L::NB; ++c)
+                load_tile(sb + L::Q_OFF + w * L::TILE + c * 16384, p.q_off + h * HD + 64 * c, q0 + w * BQ, bar_q);
+        int j = 0;
+        for (; j < n; ++j) {
+            const int st = j & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_kve + 8 * st, ((j >> 1) & 1) ^ 1))) { ok = false; break; }
+            const int jk = (kt0 + j) * BKV;
+            mbar_arrive_expect_tx_e(bar_kf + 8 * st, L::TILE, e);
+            for (int c = 0; c < L::NB; ++c)
+                load_tile(sb + L::K_OFF + st * L::TILE + c * 16384, p.k_off + g * HD + 64 * c, jk, bar_kf + 8 * st);
+            mbar_arrive_expect_tx_e(bar_vf + 8 * st, L::TILE, e);
+            for (int c = 0; c < L::NB; ++c)
+                load_tile(sb + L::V_OFF + st * L::TILE + c * 16384, p.v_off + g * HD + 64 * c, jk, bar_vf + 8 * st);
+        }
+        // no copy of ours may still be landing when the CTA exits
+        mbar_wait(bar_q, 0, 20000000ull);
+        for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) {
+            mbar_wait(bar_kf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
+            mbar_wait(bar_vf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
         }
     } else if (warp == L::MMA_WARP) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(128, BKV);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD) | (1u << 16);   // B MN-major
-            auto issue_s = [&](int w, int j) -> bool {
-                if (!mbar_wait(bar_kf + 8 * (j & 1), (j >> 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t kb = sb + L::K_OFF + (j & 1) * L::TILE;
-                const uint32_t qb = sb + L::Q_OFF + w * L::TILE;
+        // The whole warp runs the issue loop in step (waits, descriptors) and
+        // one elected lane issues: the loop's values stay warp-uniform.
+        const uint32_t e = elect_one();
+        constexpr uint32_t idesc_s = idesc_bf16_f32(128, BKV);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD) | (1u << 16);   // B MN-major
+        // descriptors computed once; an operand is its base plus a constant
+        // (the start-address field cannot carry: shared memory < 256 KB)
+        const uint64_t kd0 = smem_desc_sw128(sb + L::K_OFF), kd1 = smem_desc_sw128(sb + L::K_OFF + L::TILE);
+        const uint64_t vd0 = smem_desc_mn_sw128(sb + L::V_OFF, 16384);
+        const uint64_t vd1 = smem_desc_mn_sw128(sb + L::V_OFF + L::TILE, 16384);
+        auto issue_s = [&](int w, int j) -> bool {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_kf + 8 * (j & 1), (j >> 1) & 1))) return false;
+            tc_fence_after();
+            const uint64_t k0 = (j & 1) ? kd1 : kd0;
+            const uint64_t q0d = smem_desc_sw128(sb + L::Q_OFF + w * L::TILE);
 #pragma unroll
-                for (int k = 0; k < HD / 16; ++k) {
-                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_ss_bf16(tbase + L::S_COL + w * 128, smem_desc_sw128(qb + off),
-                                smem_desc_sw128(kb + off), idesc_s, k > 0);
-                }
-                mma_commit(bar_sf + 8 * w);
-                return true;
-            };
-            auto issue_pv = [&](int w, int j) {
-                const uint32_t vb = sb + L::V_OFF + (j & 1) * L::TILE;
-#pragma unroll
-                for (int s2 = 0; s2 < BKV / 16; ++s2)
-                    mma_ts_bf16(tbase + L::O_COL + w * HD, tbase + L::S_COL + w * 128 + 8 * s2,
-                                smem_desc_mn_sw128(vb + s2 * 2048, 16384), idesc_pv, (j | s2) != 0);
-                mma_commit(bar_pv + 8 * w);
-            };
-            ok = mbar_wait(bar_q, 0);
-            for (int w = 0; w < ntile && ok; ++w) ok = issue_s(w, 0);
-            // Issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the order in
-            // which the alternating exp passes release them.  S_w(j+1)
-            // overwrites the P_w(j) that PV_w(j) reads (a different
-            // accumulator, so not ordered by the tensor pipe): it waits for
-            // PV_w(j) to complete.
-            for (int j = 0; j < n && ok; ++j) {
-                if (!mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1)) { ok = false; break; }
-                for (int w = 0; w < ntile && ok; ++w) {
-                    if (!mbar_wait(bar_pf + 8 * w, j & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(w, j);
-                    // K(j), V(j) are free once both tiles' PV(j) are done
-                    if (w == ntile - 1) mma_commit(bar_kve + 8 * (j & 1));
-                    if (j + 1 < n) ok = mbar_wait(bar_pv + 8 * w, j & 1) && issue_s(w, j + 1);
-                }
+            for (int k = 0; k < HD / 16; ++k) {
+                const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                mma_ss_bf16_e(tbase + L::S_COL + w * 128, q0d + off, k0 + off, idesc_s, k > 0, e);
             }
-            mma_commit(bar_fin);
-            mbar_wait(bar_fin, 0, 20000000ull);
+            mma_commit_e(bar_sf + 8 * w, e);
+            return true;
+        };
+        auto issue_pv = [&](int w, int j) {
+            const uint64_t v0 = (j & 1) ? vd1 : vd0;
+#pragma unroll
+            for (int s2 = 0; s2 < BKV / 16; ++s2)
+                mma_ts_bf16_e(tbase + L::O_COL + w * HD, tbase + L::S_COL + w * 128 + 8 * s2,
+                              v0 + (uint64_t)(128 * s2), idesc_pv, (j | s2) != 0, e);
+            mma_commit_e(bar_pv + 8 * w, e);
+        };
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_q, 0));
+        for (int w = 0; w < ntile && ok; ++w) ok = issue_s(w, 0);
+        // Issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the order in
+        // which the alternating exp passes release them.  S_w(j+1)
+        // overwrites the P_w(j) that PV_w(j) reads (a different
+        // accumulator, so not ordered by the tensor pipe): it waits for
+        // PV_w(j) to complete.
+        for (int j = 0; j < n && ok; ++j) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1))) { ok = false; break; }
+            for (int w = 0; w < ntile && ok; ++w) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_pf + 8 * w, j & 1))) { ok = false; break; }
+                tc_fence_after();
+                issue_pv(w, j);
+                // K(j), V(j) are free once both tiles' PV(j) are done
+                if (w == ntile - 1) mma_commit_e(bar_kve + 8 * (j & 1), e);
+                if (j + 1 < n) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv + 8 * w, j & 1)) && issue_s(w, j + 1);
+            }
         }
+        mma_commit_e(bar_fin, e);
+        __all_sync(0xFFFFFFFFu, mbar_wait(bar_fin, 0, 20000000ull));
     } else if (warp < 4 * ntile) {
         // ---------------------------------------- softmax, one query per thread
         const int w = warp >> 2;                         // query tile of this warpgroup

@@ -219,6 +219,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint3
         : "memory");
 }
 
+// tma_load_2d / mbar_arrive_expect_tx issued by the lane whose `e` is set
+// (the rest of the warp runs the same loop in step).
+__device__ __forceinline__ void tma_load_2d_e(uint32_t dst, const void *map, uint32_t bar, int32_t c0,
+                                              int32_t c1, uint32_t e) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(e)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_e(uint32_t bar, uint32_t bytes, uint32_t e) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %2, 0;\n\t"
+        "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes), "r"(e)
+        : "memory");
+}
+
 // Tensor store of a box from shared memory (plain layout, no swizzle) to
 // global memory at element coordinates (c0 inner, c1 outer); rows past the
 // tensor's extent are not written.  c0 * element size must be a multiple of
@@ -262,6 +282,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                      dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
+}
+
+// bulk_load issued by the lane whose `e` is set.
+__device__ __forceinline__ void bulk_load_e(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                            uint32_t e) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %4, 0;\n\t"
+        "@q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "r"(e)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *map) {
@@ -309,6 +341,50 @@ __device__ __forceinline__ void mma_ss_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// One lane of a converged warp: 1 there, 0 elsewhere (elect.sync).  A warp
+// that runs its issue loop in step and lets only the elected lane issue keeps
+// the loop's values (descriptors, addresses) warp-uniform, so the tensor
+// instructions take them straight from uniform registers.
+__device__ __forceinline__ uint32_t elect_one() {
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xFFFFFFFF;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e;
+}
+
+// mma_ss_bf16 / mma_ts_bf16 / mma_commit issued by the lane whose `e` is set.
+__device__ __forceinline__ void mma_ss_bf16_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate, uint32_t e) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(e)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_bf16_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate, uint32_t e) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(e)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_e(uint32_t bar, uint32_t e) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(e)
         : "memory");
 }
 

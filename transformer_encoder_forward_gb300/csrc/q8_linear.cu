@@ -231,6 +231,26 @@ __device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// The same, issued by the lane whose `e` is set (the warp runs in step).
+__device__ __forceinline__ void mma_commit_pair_e(uint32_t bar, uint16_t mask, uint32_t e) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %2, 0;\n\t"
+        "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(bar), "h"(mask), "r"(e)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_pair_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate, uint32_t e) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(e)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                  "r"(ncols)
@@ -316,54 +336,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&p.tx);
-            int kbg = 0;
-            for (int i = 0; i < ucnt && ok; ++i) {
-                const int u = unit_at(i);
-                const bool fl = fills(i);   // weights (and column field) only when widened
-                const TileCoord tc = tile_coord<GATED>(p, u, rank);
-                const void *wmap = &p.tw[tc.zi];
-                const float *cg = fl ? p.it[tc.zi].col : nullptr;
-                const float *cu2 = GATED && fl ? p.it[tc.zi].col2 : nullptr;
-                for (int kb = 0; kb < nkb; ++kb, ++kbg) {
-                    const int s = kbg % NST;
-                    const uint32_t fb = bar_full + 8 * s;
-                    if (!mbar_wait(bar_empty + 8 * s, ((kbg / NST) & 1) ^ 1)) { ok = false; break; }
-                    // the column field slice of this stage (the last stage may hold 64)
-                    const uint32_t cbytes = (uint32_t)((p.k - kb * BK < BK ? p.k - kb * BK : BK) * 4);
-                    mbar_arrive_expect_tx(fb, L::XBYTES + (fl ? L::WBYTES : 0) + (cg ? cbytes : 0) +
-                                                  (cu2 ? cbytes : 0));
-                    if (cg) bulk_load(sb + L::COL_OFF + s * L::COL_BYTES, cg + kb * BK, cbytes, fb);
-                    if (cu2) bulk_load(sb + L::COL_OFF + s * L::COL_BYTES + BK * 4, cu2 + kb * BK, cbytes, fb);
+        // (the whole warp in step, one elected lane issues: warp-uniform values)
+        const uint32_t e = elect_one();
+        if (e) tma_prefetch_desc(&p.tx);
+        int kbg = 0;
+        for (int i = 0; i < ucnt && ok; ++i) {
+            const int u = unit_at(i);
+            const bool fl = fills(i);   // weights (and column field) only when widened
+            const TileCoord tc = tile_coord<GATED>(p, u, rank);
+            const void *wmap = &p.tw[tc.zi];
+            const float *cg = fl ? p.it[tc.zi].col : nullptr;
+            const float *cu2 = GATED && fl ? p.it[tc.zi].col2 : nullptr;
+            for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+                const int s = kbg % NST;
+                const uint32_t fb = bar_full + 8 * s;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_empty + 8 * s, ((kbg / NST) & 1) ^ 1))) {
+                    ok = false;
+                    break;
+                }
+                // the column field slice of this stage (the last stage may hold 64)
+                const uint32_t cbytes = (uint32_t)((p.k - kb * BK < BK ? p.k - kb * BK : BK) * 4);
+                mbar_arrive_expect_tx_e(fb, L::XBYTES + (fl ? L::WBYTES : 0) + (cg ? cbytes : 0) + (cu2 ? cbytes : 0),
+                                        e);
+                if (cg) bulk_load_e(sb + L::COL_OFF + s * L::COL_BYTES, cg + kb * BK, cbytes, fb, e);
+                if (cu2) bulk_load_e(sb + L::COL_OFF + s * L::COL_BYTES + BK * 4, cu2 + kb * BK, cbytes, fb, e);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const uint32_t wdst = sb + L::W_OFF + s * L::WBYTES + c * L::WBOX;
+                for (int c = 0; c < 2; ++c) {
+                    const uint32_t wdst = sb + L::W_OFF + s * L::WBYTES + c * L::WBOX;
 #pragma unroll
-                        for (int tt = 0; tt < TPA; ++tt)
-                            tma_load_2d(sb + L::X_OFF + s * L::XBYTES + tt * L::XTILE + c * L::XBOX, &p.tx,
-                                        fb, kb * BK + c * BOX, (tc.t0 * TPA + tt) * BN + rank * HALF);
-                        if (!fl) continue;
-                        if (GATED) {   // rows 0-63: gate, rows 64-127: up, same features
-                            tma_load_2d(wdst, &p.tw[0], fb, kb * BK + c * BOX, tc.o0);
-                            tma_load_2d(wdst + (BM / 2) * BOX, &p.tw[1], fb, kb * BK + c * BOX, tc.o0);
-                        } else {
-                            tma_load_2d(wdst, wmap, fb, kb * BK + c * BOX, tc.o0);
-                        }
+                    for (int tt = 0; tt < TPA; ++tt)
+                        tma_load_2d_e(sb + L::X_OFF + s * L::XBYTES + tt * L::XTILE + c * L::XBOX, &p.tx, fb,
+                                      kb * BK + c * BOX, (tc.t0 * TPA + tt) * BN + rank * HALF, e);
+                    if (!fl) continue;
+                    if (GATED) {   // rows 0-63: gate, rows 64-127: up, same features
+                        tma_load_2d_e(wdst, &p.tw[0], fb, kb * BK + c * BOX, tc.o0, e);
+                        tma_load_2d_e(wdst + (BM / 2) * BOX, &p.tw[1], fb, kb * BK + c * BOX, tc.o0, e);
+                    } else {
+                        tma_load_2d_e(wdst, wmap, fb, kb * BK + c * BOX, tc.o0, e);
                     }
                 }
             }
-            // make sure no copy of ours is still landing when the CTA exits
-            for (int j = kbg - NST < 0 ? 0 : kbg - NST; j < kbg; ++j)
-                mbar_wait(bar_full + 8 * (j % NST), (j / NST) & 1, 20000000ull);
         }
+        // make sure no copy of ours is still landing when the CTA exits
+        for (int j = kbg - NST < 0 ? 0 : kbg - NST; j < kbg; ++j)
+            mbar_wait(bar_full + 8 * (j % NST), (j / NST) & 1, 20000000ull);
     } else if (warp == 1) {
         // -------------------------------------- MMA issuer (leader CTA only)
-        if (lane == 0 && leader) {
+        // The whole warp runs the loop in step (waits, indices, descriptors)
+        // and one elected lane issues: the values stay warp-uniform, so the
+        // MMAs take their operands from uniform registers (an issue loop in
+        // one divergent lane cost about 84 cycles an MMA).
+        if (leader) {
+            const uint32_t e = elect_one();
             constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
-            // this thread's instruction rate bounds the MMA rate at N <= 192
-            // (one 2-SM MMA every ~45 cycles at best), so the loop keeps its
-            // indices incremental: ring slot s and A stage ar with their phases
+            // the loop keeps its indices incremental: ring slot s and A stage
+            // ar with their phases
             int nfill = 0, s = 0, ar = 0;
             uint32_t sph = 0, aph = 0;
             for (int lt = 0; lt < ucnt && ok; ++lt) {
@@ -375,7 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 // TPA == 2: a unit's two token tiles use both
                 const int b = TPA == 2 ? 0 : (lt & 1);
                 const uint32_t ph = TPA == 2 ? (lt & 1) : ((lt >> 1) & 1);
-                if (!mbar_wait_cluster(bar_accempty + 8 * b, ph ^ 1)) { ok = false; break; }
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar_accempty + 8 * b, ph ^ 1))) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t dcol = tbase + (TPA == 2 ? 0 : b) * BN;
                 int kb0 = 0;   // stages issued for both token tiles before the main loop
@@ -388,30 +415,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     int ss = s, aa = ar;
                     uint32_t aph2 = aph;
                     for (int kb = 0; kb < P && ok; ++kb) {
-                        if (!mbar_wait_cluster(bar_afull + 8 * aa, aph2)) { ok = false; break; }
+                        if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar_afull + 8 * aa, aph2))) { ok = false; break; }
                         tc_fence_after();
                         const uint64_t d0 = smem_desc_sw128(sb + L::X_OFF + ss * L::XBYTES);
                         const uint32_t a0 = tbase + L::A_COL + 64 * aa;
 #pragma unroll
                         for (int j = 0; j < BK / 16; ++j)
-                            mma_ts_pair(dcol, a0 + 8 * j, d0 + (uint64_t)(((j >> 2) * L::XBOX + (j & 3) * 32) >> 4),
-                                        idesc, j == 0 ? (uint32_t)(kb != 0) : 1u);
+                            mma_ts_pair_e(dcol, a0 + 8 * j, d0 + (uint64_t)(((j >> 2) * L::XBOX + (j & 3) * 32) >> 4),
+                                        idesc, j == 0 ? (uint32_t)(kb != 0) : 1u, e);
                         if (++ss == NST) ss = 0;
                         if (++aa == NA) { aa = 0; aph2 ^= 1u; }
                     }
                     if (!ok) break;
-                    if (!mbar_wait_cluster(bar_accempty + 8, ph ^ 1)) { ok = false; break; }
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar_accempty + 8, ph ^ 1))) { ok = false; break; }
                     tc_fence_after();
                     for (int kb = 0; kb < P; ++kb) {   // tile 1 for the same stages, then release them
                         const uint64_t d0 = smem_desc_sw128(sb + L::X_OFF + s * L::XBYTES);
                         const uint32_t a0 = tbase + L::A_COL + 64 * ar;
 #pragma unroll
                         for (int j = 0; j < BK / 16; ++j)
-                            mma_ts_pair(dcol + BN, a0 + 8 * j,
+                            mma_ts_pair_e(dcol + BN, a0 + 8 * j,
                                         d0 + (uint64_t)((L::XTILE + (j >> 2) * L::XBOX + (j & 3) * 32) >> 4), idesc,
-                                        j == 0 ? (uint32_t)(kb != 0) : 1u);
-                        mma_commit_pair(bar_empty + 8 * s, 0x3);
-                        mma_commit_pair(bar_aempty + 8 * ar, 0x3);
+                                        j == 0 ? (uint32_t)(kb != 0) : 1u, e);
+                        mma_commit_pair_e(bar_empty + 8 * s, 0x3, e);
+                        mma_commit_pair_e(bar_aempty + 8 * ar, 0x3, e);
                         if (++s == NST) { s = 0; sph ^= 1u; }
                         if (++ar == NA) { ar = 0; aph ^= 1u; }
                     }
@@ -421,13 +448,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const int a = res ? kb : ar;
                     // resident weights: both CTAs' stages s have landed (our
                     // copies, and the peer's as relayed by its warp 1)
-                    if (res && !mbar_wait_cluster(bar_full + 8 * s, sph)) {
+                    if (res && !__all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar_full + 8 * s, sph))) {
                         ok = false;
                         break;
                     }
                     // both CTAs' converters have widened stage a, which they
                     // only do once their own TMA stage s has landed
-                    if (fl && !mbar_wait_cluster(bar_afull + 8 * a, res ? (nfill & 1) : aph)) {
+                    if (fl && !__all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar_afull + 8 * a, res ? (nfill & 1) : aph))) {
                         ok = false;
                         break;
                     }
@@ -441,28 +468,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     for (int j = 0; j < BK / 16; ++j)
 #pragma unroll
                         for (int tt = 0; tt < TPA; ++tt)
-                            mma_ts_pair(dcol + tt * BN, a0 + 8 * j,
+                            mma_ts_pair_e(dcol + tt * BN, a0 + 8 * j,
                                         d0 + (uint64_t)((tt * L::XTILE + (j >> 2) * L::XBOX + (j & 3) * 32) >> 4),
-                                        idesc, j == 0 ? acc0 : 1u);
-                    mma_commit_pair(bar_empty + 8 * s, 0x3);
-                    if (last_use) mma_commit_pair(bar_aempty + 8 * a, 0x3);
+                                        idesc, j == 0 ? acc0 : 1u, e);
+                    mma_commit_pair_e(bar_empty + 8 * s, 0x3, e);
+                    if (last_use) mma_commit_pair_e(bar_aempty + 8 * a, 0x3, e);
                     if (++s == NST) { s = 0; sph ^= 1u; }
                     if (!res && ++ar == NA) { ar = 0; aph ^= 1u; }
                 }
                 if (fl) ++nfill;
-                if (ok) mma_commit_pair(bar_accfull + 8 * b, 0x3);
+                if (ok) mma_commit_pair_e(bar_accfull + 8 * b, 0x3, e);
             }
             // every MMA issued above has completed once this fires
-            mma_commit_pair(bar_done, 0x1);
+            mma_commit_pair_e(bar_done, 0x1, e);
             mbar_wait(bar_done, 0, 20000000ull);
-        } else if (lane == 0 && res) {
+        } else if (res) {
             // the peer's relay: each of its stages has landed
+            const uint32_t e = elect_one();
             int kbg = 0;
             for (int i = 0; i < ucnt && ok; ++i)
                 for (int kb = 0; kb < nkb; ++kb, ++kbg) {
                     const int s = kbg % NST;
-                    if (!mbar_wait(bar_full + 8 * s, (kbg / NST) & 1)) { ok = false; break; }
-                    mbar_arrive_cluster_relaxed(full_ldr + 8 * s);
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8 * s, (kbg / NST) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    if (e) mbar_arrive_cluster_relaxed(full_ldr + 8 * s);
                 }
         }
     } else if (warp < 10) {
