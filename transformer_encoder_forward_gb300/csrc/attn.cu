@@ -71,7 +71,10 @@ struct AttnParams {
 // TL = query tiles per CTA: 2 (tiles A and B take turns at the exp pass,
 // one CTA per SM), or 1 (hd = 64: half the TMEM and 80 KB of shared memory,
 // so that two CTAs share an SM and one's loads and latencies overlap the
-// other's work - the short sequences of a text batch).
+// other's work - the short sequences of a text batch).  With one tile, P has
+// TMEM columns of its own (S 128 | P 64 | O 64 = 256), so S(j+1) is issued as
+// soon as the softmax has read S(j) into registers and runs on the tensor
+// core during the softmax of block j.
 template <int HD, int TL>
 struct ALayout {
     static constexpr int NB = HD / 64;              // 64-column boxes per tile row
@@ -82,12 +85,15 @@ struct ALayout {
     static constexpr int BAR_OFF = V_OFF + 2 * TILE;
     static constexpr int NTHREADS = 32 * (4 * TL + 2);   // softmax warps, MMA warp, TMA warp
     static constexpr int MMA_WARP = 4 * TL, TMA_WARP = 4 * TL + 1;
-    // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], fin, turn[2]
-    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 2;
+    // q_full, k_full[2], v_full[2], kv_empty[2] (TL = 1: V only), s_full[2], p_full[2],
+    // pv_done[2], fin, turn[2], k_empty[2] (TL = 1), s_free (TL = 1)
+    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 2 + 2 + 1;
     static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
-    static constexpr int S_COL = 0;                 // S_A, S_B: TL x 128 f32 columns (P aliased)
-    static constexpr int O_COL = TL * 128;          // O_A, O_B: TL x HD f32 columns
+    static constexpr int S_COL = 0;                 // S_A, S_B: TL x 128 f32 columns
+    static constexpr int P_COL = TL == 1 ? 128 : 0; // TL = 1: 64 columns of its own; TL = 2: over S
+    static constexpr int O_COL = TL == 1 ? 192 : TL * 128;   // O_A, O_B: TL x HD f32 columns
     static constexpr int COLS = TL == 1 ? 256 : 512;
+    static_assert(TL == 2 || HD == 64, "one tile a CTA is the hd = 64 form");
     static_assert(O_COL + TL * HD <= COLS, "TMEM budget");
 };
 
@@ -227,6 +233,8 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
     const uint32_t bar_pv = bar_pf + 16;           // [2] per query tile
     const uint32_t bar_fin = bar_pv + 16;
     const uint32_t bar_turn = bar_fin + 8;         // [2] per query tile: its turn at the exp pass
+    const uint32_t bar_ke = bar_turn + 16;         // [2] TL = 1: K(j) read by S(j)
+    const uint32_t bar_sfree = bar_ke + 16;        // TL = 1: the softmax has read S(j)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBAR);
 
     // key tiles the two query tiles need: the union of their windows, clipped
@@ -250,7 +258,9 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             mbar_init(bar_pf + 8 * i, 4);
             mbar_init(bar_pv + 8 * i, 1);
             mbar_init(bar_turn + 8 * i, 4);
+            mbar_init(bar_ke + 8 * i, 1);
         }
+        mbar_init(bar_sfree, 4);
         mbar_init(bar_fin, 1);
         fence_mbar_init();
     }
@@ -281,24 +291,50 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
         for (int w = 0; w < ntile; ++w)
             for (int c = 0; c < L::NB; ++c)
                 load_tile(sb + L::Q_OFF + w * L::TILE + c * 16384, p.q_off + h * HD + 64 * c, q0 + w * BQ, bar_q);
-        int j = 0;
-        for (; j < n; ++j) {
-            const int st = j & 1;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_kve + 8 * st, ((j >> 1) & 1) ^ 1))) { ok = false; break; }
-            const int jk = (kt0 + j) * BKV;
+        // K(i) into ring slot i & 1 once its previous occupant K(i - 2) is
+        // free (TL = 1: read by S(i - 2); TL = 2: K and V free together after
+        // PV(i - 2)); V(i) once PV(i - 2) is done
+        auto load_k = [&](int i) -> bool {
+            const int st = i & 1;
+            const uint32_t fb = TL == 1 ? bar_ke : bar_kve;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, ((i >> 1) & 1) ^ 1))) return false;
             mbar_arrive_expect_tx_e(bar_kf + 8 * st, L::TILE, e);
             for (int c = 0; c < L::NB; ++c)
-                load_tile(sb + L::K_OFF + st * L::TILE + c * 16384, p.k_off + g * HD + 64 * c, jk, bar_kf + 8 * st);
+                load_tile(sb + L::K_OFF + st * L::TILE + c * 16384, p.k_off + g * HD + 64 * c, (kt0 + i) * BKV,
+                          bar_kf + 8 * st);
+            return true;
+        };
+        auto load_v = [&](int i) -> bool {
+            const int st = i & 1;
+            if (TL == 1 && !__all_sync(0xFFFFFFFFu, mbar_wait(bar_kve + 8 * st, ((i >> 1) & 1) ^ 1))) return false;
             mbar_arrive_expect_tx_e(bar_vf + 8 * st, L::TILE, e);
             for (int c = 0; c < L::NB; ++c)
-                load_tile(sb + L::V_OFF + st * L::TILE + c * 16384, p.v_off + g * HD + 64 * c, jk, bar_vf + 8 * st);
+                load_tile(sb + L::V_OFF + st * L::TILE + c * 16384, p.v_off + g * HD + 64 * c, (kt0 + i) * BKV,
+                          bar_vf + 8 * st);
+            return true;
+        };
+        int nk = 0, nv = 0;   // K and V tiles issued
+        if (TL == 1) {
+            // K runs one tile ahead of V: S(j + 1) needs it while PV(j) waits for P(j)
+            if (n > 0 && (ok = load_k(0))) nk = 1;
+            for (; nv < n && ok; ++nv) {
+                if (nk < n) {
+                    if (!(ok = load_k(nk))) break;
+                    ++nk;
+                }
+                if (!(ok = load_v(nv))) break;
+            }
+        } else {
+            for (; nv < n && ok; ++nv) {
+                if (!(ok = load_k(nv))) break;
+                ++nk;
+                ok = load_v(nv);
+            }
         }
         // no copy of ours may still be landing when the CTA exits
         mbar_wait(bar_q, 0, 20000000ull);
-        for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) {
-            mbar_wait(bar_kf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
-            mbar_wait(bar_vf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
-        }
+        for (int i = nk - 2 < 0 ? 0 : nk - 2; i < nk; ++i) mbar_wait(bar_kf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
+        for (int i = nv - 2 < 0 ? 0 : nv - 2; i < nv; ++i) mbar_wait(bar_vf + 8 * (i & 1), (i >> 1) & 1, 20000000ull);
     } else if (warp == L::MMA_WARP) {
         // ------------------------------------------------------- MMA issuer
         // The whole warp runs the issue loop in step (waits, descriptors) and
@@ -322,24 +358,44 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
                 mma_ss_bf16_e(tbase + L::S_COL + w * 128, q0d + off, k0 + off, idesc_s, k > 0, e);
             }
             mma_commit_e(bar_sf + 8 * w, e);
+            if (TL == 1) mma_commit_e(bar_ke + 8 * (j & 1), e);   // K(j) read
             return true;
         };
         auto issue_pv = [&](int w, int j) {
             const uint64_t v0 = (j & 1) ? vd1 : vd0;
 #pragma unroll
             for (int s2 = 0; s2 < BKV / 16; ++s2)
-                mma_ts_bf16_e(tbase + L::O_COL + w * HD, tbase + L::S_COL + w * 128 + 8 * s2,
+                mma_ts_bf16_e(tbase + L::O_COL + w * HD, tbase + L::P_COL + w * 128 + 8 * s2,
                               v0 + (uint64_t)(128 * s2), idesc_pv, (j | s2) != 0, e);
             mma_commit_e(bar_pv + 8 * w, e);
         };
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_q, 0));
         for (int w = 0; w < ntile && ok; ++w) ok = issue_s(w, 0);
-        // Issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the order in
+        if (TL == 1) {
+            // S(j+1) as soon as the softmax has read S(j) (P has columns of
+            // its own), then PV(j) once P(j) is written
+            for (int j = 0; j < n && ok; ++j) {
+                if (j + 1 < n) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_sfree, j & 1))) { ok = false; break; }
+                    tc_fence_after();
+                    if (!(ok = issue_s(0, j + 1))) break;
+                }
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1)) ||
+                    !__all_sync(0xFFFFFFFFu, mbar_wait(bar_pf, j & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_pv(0, j);
+                mma_commit_e(bar_kve + 8 * (j & 1), e);   // V(j) read
+            }
+        }
+        // TL = 2: issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the order in
         // which the alternating exp passes release them.  S_w(j+1)
         // overwrites the P_w(j) that PV_w(j) reads (a different
         // accumulator, so not ordered by the tensor pipe): it waits for
         // PV_w(j) to complete.
-        for (int j = 0; j < n && ok; ++j) {
+        for (int j = 0; j < n && ok && TL == 2; ++j) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1))) { ok = false; break; }
             for (int w = 0; w < ntile && ok; ++w) {
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_pf + 8 * w, j & 1))) { ok = false; break; }
@@ -362,13 +418,15 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
         const int tqhi = (tq0 + BQ < len ? tq0 + BQ : len) - 1;
         const uint32_t tl = (uint32_t)(32 * wq) << 16;
         const uint32_t scol = tbase + tl + L::S_COL + w * 128;
+        const uint32_t pcol = tbase + tl + L::P_COL + w * 128;
         const uint32_t ocol = tbase + tl + L::O_COL + w * HD;
         const float c = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         for (int j = 0; j < n; ++j) {
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_sf + 8 * w, j & 1));
             if (!ok) break;
-            // S_w(j) landed, so PV_w(j-1) is done: P_w and O_w may be touched
+            // TL = 2: S_w(j) landed, so PV_w(j-1) is done: P_w and O_w may be
+            // touched.  TL = 1: see below.
             tc_fence_after();
             // mask: keys past the sequence end or outside the window
             const int kv0 = (kt0 + j) * BKV;
@@ -380,6 +438,12 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             tmem_ld64(scol, v0);
             tmem_ld64(scol + 64, v1);
             tmem_wait_ld();
+            if (TL == 1) {
+                // S(j) is in registers: the tensor core may compute S(j+1)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sfree);
+            }
             float mx = full ? row_max_regs<false>(v0, v1, qi, kv0, len, W)
                             : row_max_regs<true>(v0, v1, qi, kv0, len, W);
             mx *= c;                                     // c > 0: the max of the scaled row
@@ -389,6 +453,12 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             if (ntile == 2 && (w == 1 || j > 0)) {
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_turn + 8 * w, (w == 0 ? j - 1 : j) & 1));
                 if (!ok) break;
+            }
+            if (TL == 1 && j > 0) {
+                // P and O are free once PV(j-1) is done
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv, (j - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
             }
             const bool resc = mx > m_used + 8.f;
             if (__any_sync(0xFFFFFFFFu, resc)) {
@@ -408,10 +478,10 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
                     tmem_wait_st();
                 }
             }
-            // pass 2: P as bf16 into the consumed S columns, and its row sum
+            // pass 2: P as bf16 (TL = 2: into the consumed S columns), and its row sum
             const float nm = m_used == -INFINITY ? 0.f : -m_used;
-            const float rs = full ? row_exp_regs<false>(scol, v0, v1, c, nm, qi, kv0, len, W)
-                                  : row_exp_regs<true>(scol, v0, v1, c, nm, qi, kv0, len, W);
+            const float rs = full ? row_exp_regs<false>(pcol, v0, v1, c, nm, qi, kv0, len, W)
+                                  : row_exp_regs<true>(pcol, v0, v1, c, nm, qi, kv0, len, W);
             l += rs;
             tmem_wait_st();
             tc_fence_before();

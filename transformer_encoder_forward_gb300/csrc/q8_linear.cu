@@ -211,27 +211,11 @@ __device__ __forceinline__ void cluster_sync() {
                      : "memory");
 }
 
-// Arrives on the mbarrier at `bar`'s offset in every CTA of `mask` once the
-// 2-SM MMAs issued so far by this thread are done.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar), "h"(mask)
-        : "memory");
-}
-
-// D(tmem, both CTAs) (+)= A(tmem, both CTAs) * B(smem desc, N split across the pair).
-__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// The same, issued by the lane whose `e` is set (the warp runs in step).
+// tcgen05.commit (cta_group::2, multicast) and the 2-SM MMA, each issued by
+// the lane whose `e` is set (the warp runs in step): the commit arrives on
+// the mbarrier at `bar`'s offset in every CTA of `mask` once the 2-SM MMAs
+// issued so far are done; the MMA computes D(tmem, both CTAs) (+)= A(tmem,
+// both CTAs) * B(smem desc, N split across the pair).
 __device__ __forceinline__ void mma_commit_pair_e(uint32_t bar, uint16_t mask, uint32_t e) {
     asm volatile(
         "{\n\t.reg .pred q;\n\t"
