@@ -63,6 +63,11 @@ GEMM_CASES = [
     (777, 256, [256, 512], False, "sep", "bf16"),
     # long K, 128-token tiles two a unit (the choice that saves a wave here)
     (2111, 2048, [3840], False, True, "f32"),
+    # the DiT out projection at 8448 tokens: whole waves of two-tile units,
+    # then the rows left in a second launch (in-place residual)
+    (8448, 3840, [3840], False, True, "f32"),
+    # a split with a separate residual and a bf16 output
+    (2111, 2048, [3840], True, "sep", "bf16"),
     # resident weights over long runs of token tiles that cross feature pairs
     (5000, 512, [512, 512, 512], False, False, "bf16"),
     (5000, 512, [512], True, True, "f32"),
@@ -129,6 +134,23 @@ def test_q8_linear_exact_integer_case_is_bit_exact():
     np.testing.assert_array_equal(to_np(y), exact.astype(np.float64))
 
 
+def test_q8_linear_split_launch_is_bit_exact_on_integers():
+    # 2111 rows at K = 2048, N = 3840 run as whole waves of two-tile units
+    # and a second launch for the rest: integer x with |x| <= 4 keeps every
+    # partial sum an integer below 2^24, so each row must be exact in both
+    torch = _torch()
+    rng = np.random.default_rng(6)
+    m, k, n = 2111, 2048, 3840
+    xi = rng.integers(-4, 5, (m, k)).astype(np.float32)
+    x = torch.from_numpy(xi).to(torch.bfloat16).cuda()
+    q_np = rng.integers(-127, 128, (n, k), dtype=np.int8)
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    te.q8_linear(x, [{"w": te.q8w(to_dev(q_np), torch.ones(n, device="cuda")), "y": y, "ldy": n}])
+    te.check()
+    exact = xi.astype(np.int64) @ q_np.astype(np.int64).T
+    np.testing.assert_array_equal(to_np(y), exact.astype(np.float64))
+
+
 @pytest.mark.parametrize("reps", [2, 4])
 def test_int8_widening_and_indexing_are_bit_exact(reps):
     # one-hot activation rows pick single weight columns: y[t, o] = q[o, j_t]
@@ -159,7 +181,9 @@ def test_int8_widening_and_indexing_are_bit_exact(reps):
                                             (1500, 256, 768, "silu", True),
                                             (2100, 192, 512, "gelu_tanh", False),
                                             # long K, 128-token tiles two a unit
-                                            (2300, 2048, 1024, "silu", True)])
+                                            (2300, 2048, 1024, "silu", True),
+                                            # whole waves of two-tile units, then a second launch
+                                            (2400, 3072, 3840, "silu", False)])
 def test_gated_linear_matches_oracle(m, k, f, act, bias):
     # m = act(bf16(g)) * bf16(u): the same storage points as the g|u panel
     # followed by the gate, without the panel

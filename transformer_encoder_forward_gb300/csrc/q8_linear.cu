@@ -103,7 +103,7 @@ template <int BN, int TPA>
 struct Layout {
     static constexpr int HALF = BN / 2;                 // token rows each CTA of the pair holds
     // shared-memory load stages (a stage holds TPA token tiles)
-    static constexpr int NST = TPA == 2 ? (BN == 128 ? 4 : 3) : (BN >= 160 ? 5 : 6);
+    static constexpr int NST = TPA == 2 ? (BN == 128 ? 4 : 3) : (BN >= 128 ? 5 : 6);
     // TMEM stages of the widened A operand (64 columns each): what the two
     // BN-column accumulators leave of the 512 columns, at most 4 and fewer
     // than the load stages
@@ -116,14 +116,18 @@ struct Layout {
     static constexpr int WBYTES = 2 * WBOX;             // int8 weight stage (own 128 rows)
     static constexpr int X_OFF = 0;
     static constexpr int W_OFF = NST * XBYTES;
-    // epilogue staging: one 32 x 32 output tile (f32 or bf16; gated, 32 tokens
-    // x 16 features of bf16) per epilogue warp, 128-byte aligned (TMA
-    // sources).  q8_2f: each stage's 128 column-field values (f32), for the
-    // gate and the up weight in the gated form
+    // epilogue staging, per epilogue warp: a ring of 32-token output blocks
+    // (f32 32 x 32: 4 KB; bf16 32 x 32: 2 KB; gated bf16 32 x 16: 1 KB), so
+    // that a block's TMA store can still be reading while the next ones are
+    // written; 8 KB a warp where shared memory allows (the one-tile units of
+    // the short-K GEMMs, whose epilogue sets their pace), else 4 KB; 128-byte
+    // aligned (TMA sources).  q8_2f: each stage's 128 column-field values
+    // (f32), for the gate and the up weight in the gated form
     static constexpr int COL_OFF = W_OFF + NST * WBYTES;
     static constexpr int COL_BYTES = 2 * BK * 4;
     static constexpr int STG_OFF = COL_OFF + NST * COL_BYTES;
-    static constexpr int STG_BYTES = 4 * 4096;
+    static constexpr int STG_WARP = TPA == 1 && BN <= 128 ? 8192 : 4096;
+    static constexpr int STG_BYTES = 4 * STG_WARP;
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
     // barriers: full, empty [NST]; afull, aempty [NA]; accfull, accempty [2]; done
     static constexpr int NBAR = 2 * NST + 2 * NA + 4 + 1;
@@ -595,10 +599,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         int lt = 0;
         // staging: gated, one 32-token x 16-feature bf16 tile per warp;
         // ungated, one 32 x 32 tile (f32 or bf16) per warp
-        const uint32_t ostg_off = L::STG_OFF + (warp - 10) * 4096;
-        const uint32_t ostg = sb + ostg_off;                 // the TMA source (shared address)
-        float *ostg_f = reinterpret_cast<float *>(smem + ostg_off);
-        __nv_bfloat16 *ostg_h = reinterpret_cast<__nv_bfloat16 *>(smem + ostg_off);
+        // this warp's staging (a shared-memory address)
+        const uint32_t stg = sb + L::STG_OFF + (warp - 10) * L::STG_WARP;
+        int slot = 0, slot_bytes = 0;   // next block of the staging ring, its size
+        // the next staging block of `bytes`: waits until the store that last
+        // used it has finished reading it (at most nb - 1 younger stores may
+        // still be reading), then hands out its shared address.  Items of one launch
+        // may differ in block size: a change of size first lets every store
+        // finish reading.
+        auto next_block = [&](int bytes) -> uint32_t {
+            const int nb = L::STG_WARP / bytes;
+            const bool resize = bytes != slot_bytes;
+            if (slot >= nb || resize) slot = 0;
+            slot_bytes = bytes;
+            if (lane == 0) {
+                if (resize) bulk_wait_read_n<0>();
+                else if (nb >= 8) bulk_wait_read_n<7>();
+                else if (nb >= 4) bulk_wait_read_n<3>();
+                else if (nb >= 2) bulk_wait_read_n<1>();
+                else bulk_wait_read_n<0>();
+            }
+            __syncwarp();
+            return stg + (uint32_t)(slot++ * bytes);
+        };
         for (; lt < ucnt && ok; ++lt) {
             const int u = unit_at(lt);
             const int b = TPA == 2 ? 0 : (lt & 1);
@@ -648,14 +671,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         const float gv = upper ? got : lo, uv = upper ? hi : got;
                         yv[j] = apply_act_tanh(gv, act) * uv;
                     }
-                    if (lane == 0) bulk_wait_read();       // the previous tile has left ostg
-                    __syncwarp();
+                    const uint32_t so = next_block(1024);
+                    uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) ostg_h[(jb + j) * 16 + (lane & 15)] = __float2bfloat16_rn(yv[j]);
+                    for (int j = 0; j < 16; ++j) ostg_h[(jb + j) * 16 + (lane & 15)] = __bfloat16_as_ushort(__float2bfloat16_rn(yv[j]));
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0 && fo < n) {
-                        tma_store_2d(ymap, ostg, fo, t0 + 32 * c);
+                        tma_store_2d(ymap, so, fo, t0 + 32 * c);
                         bulk_commit();
                     }
                 }
@@ -676,8 +699,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sc + bi);
                     }
-                    if (lane == 0) bulk_wait_read();       // the previous tile has left ostg
-                    __syncwarp();
+                    // a residual other than y is added in f32 staging
+                    const uint32_t so = next_block(f32out || (rbase && !inplace) ? 4096 : 2048);
+                    float *ostg_f = reinterpret_cast<float *>(smem + (so - sb));
+                    uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
                     if (rbase && !inplace) {
                         // a residual other than y (not used by the block): stage
                         // f32, add the residual rows from global memory, then
@@ -697,7 +722,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                 __syncwarp();
                                 const float y = ostg_f[j * 32 + lane];
                                 __syncwarp();
-                                ostg_h[j * 32 + lane] = __float2bfloat16_rn(y);
+                                ostg_h[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
                             }
                         }
                     } else if (f32out) {
@@ -705,15 +730,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         for (int j = 0; j < 32; ++j) ostg_f[j * 32 + lane] = __uint_as_float(v[j]);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) ostg_h[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                        for (int j = 0; j < 32; ++j) ostg_h[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
                     }
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0 && fo < n) {
                         if (inplace)
-                            tma_reduce_add_2d(ymap, ostg, fo, tb);
+                            tma_reduce_add_2d(ymap, so, fo, tb);
                         else
-                            tma_store_2d(ymap, ostg, fo, tb);
+                            tma_store_2d(ymap, so, fo, tb);
                         bulk_commit();
                     }
                 }
@@ -802,6 +827,71 @@ int pick_bn(int m, int k, int &res) {
     const int na = bn == 192 ? Layout<192, 1>::NA : (bn == 128 ? Layout<128, 1>::NA : Layout<64, 1>::NA);
     res = nkb <= na ? 1 : 0;
     return bn;
+}
+
+// One launch's tile: width, token tiles a unit, resident weights.
+struct TilePlan {
+    int bn, tpa, res;
+};
+TilePlan tile_for(int m, int k, int ftiles) {
+    TilePlan t;
+    t.tpa = 1;
+    t.bn = pick_bn(m, k, t.res);
+    if (t.bn == 192 && !t.res) {
+        const LongKTile lt = long_k_tile(m, k, ftiles);
+        t.bn = lt.bn;
+        t.tpa = lt.tpa;
+    }
+    return t;
+}
+double unit_cost(const TilePlan &t) {
+    return t.tpa == 1 ? 1.0 : (t.bn == 192 ? 1.65 : COST_128X2);
+}
+double plan_time(int m, int ftiles, const TilePlan &t) {
+    const int clusters = sm_count() / 2;
+    const long long units = (long long)((ftiles + 1) / 2) * ((m + t.bn * t.tpa - 1) / (t.bn * t.tpa));
+    return (double)((units + clusters - 1) / clusters) * unit_cost(t);
+}
+
+// The tile of a split's second launch: the fastest by the model among the
+// long-K tiles (a one-tile unit costs about the same at 128 or 192 tokens: the
+// per-stage cost does not depend on the width).
+TilePlan tail_tile(int m, int k, int ftiles) {
+    TilePlan best = tile_for(m, k, ftiles);
+    if (best.res) return best;
+    const TilePlan cands[4] = {{192, 1, 0}, {128, 1, 0}, {192, 2, 0}, {128, 2, 0}};
+    double tb = plan_time(m, ftiles, best);
+    for (const TilePlan &c : cands) {
+        if ((c.tpa == 2 && c.bn == 192 && k < 3072) || (c.tpa == 2 && c.bn == 128 && k < 2048)) continue;
+        const double tc = plan_time(m, ftiles, c);
+        if (tc < tb) { best = c; tb = tc; }
+    }
+    return best;
+}
+
+// Long K with two 192-token tiles a unit: the last wave of units is often
+// only partly filled (the DiT out and down projections at 8448 tokens: 330
+// units on 76 clusters, 4.3 waves).  Splitting the rows into whole waves of
+// the wide unit and one more launch for the rest, on narrower units, finishes
+// sooner when the model says so (a launch costs about a tenth of a unit).
+// Measured: c5 down 1633 -> 1774 and out 1532 -> 1570 TFLOP/s, DiT block
+// q|k|v 1545 -> 1587; splits of 128 x 2 units (DiT block out and down, text
+// stack down) measured slower, so they are not made.
+// Returns the rows of the first launch, or m (no split).
+int split_rows(int m, int k, int ftiles, const TilePlan &t) {
+    if (t.res || t.tpa != 2 || t.bn != 192) return m;
+    const int clusters = sm_count() / 2;
+    const int fpairs = (ftiles + 1) / 2;
+    const int per = t.bn * t.tpa;
+    const long long units = (long long)fpairs * ((m + per - 1) / per);
+    const long long waves = units / clusters;
+    if (waves < 1) return m;
+    const int k1 = (int)(waves * clusters / fpairs);   // token tiles of the whole waves
+    const int m1 = k1 * per;
+    if (k1 < 1 || m1 >= m) return m;
+    const TilePlan t2 = tail_tile(m - m1, k, ftiles);
+    const double split = plan_time(m1, ftiles, t) + plan_time(m - m1, ftiles, t2) + 0.1;
+    return split < plan_time(m, ftiles, t) ? m1 : m;
 }
 
 template <int BN, bool GATED, int TPA>
@@ -955,30 +1045,39 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
         ftiles += d.ntiles;
     }
     if (m == 0) return TE_OK;
-    int bn = pick_bn(m, k, p.res), tpa = 1;
-    if (bn == 192 && !p.res) {
-        const LongKTile lt = long_k_tile(m, k, ftiles);
-        bn = lt.bn;
-        tpa = lt.tpa;
-    }
-    // each CTA of a cluster pair TMA-loads its own half of the token tile
-    te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
-                               (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != TE_OK) return st;
-    for (int i = 0; i < z; ++i) {
-        st = make_map_2d(&p.tw[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, items[i].w.q, (uint64_t)k,
-                         (uint64_t)items[i].w.n, (uint64_t)k, BOX, BM, CU_TENSOR_MAP_SWIZZLE_64B);
-        if (st != TE_OK) return st;
-        const bool f32 = items[i].y_dtype == TE_F32;
-        st = make_map_2d(&p.ty[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                         items[i].y, (uint64_t)items[i].w.n, (uint64_t)m,
-                         (uint64_t)items[i].ldy * (f32 ? 4 : 2), 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (st != TE_OK) return st;
-    }
+    const TilePlan t1 = tile_for(m, k, ftiles);
+    const int m1 = split_rows(m, k, ftiles, t1);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (bn == 192) return tpa == 2 ? launch<192, false, 2>(p, ftiles, s) : launch<192, false, 1>(p, ftiles, s);
-    if (bn == 128) return tpa == 2 ? launch<128, false, 2>(p, ftiles, s) : launch<128, false, 1>(p, ftiles, s);
-    return launch<64, false, 1>(p, ftiles, s);
+    // rows [r0, r0 + mr) with tile t: the maps and item pointers start at row r0
+    auto part = [&](int r0, int mr, const TilePlan &t) -> te_status {
+        Params q = p;
+        q.m = mr;
+        q.res = t.res;
+        const char *xb = static_cast<const char *>(x) + (size_t)r0 * ldx * 2;
+        // each CTA of a cluster pair TMA-loads its own half of the token tile
+        te_status st = make_map_2d(&q.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, (uint64_t)k, (uint64_t)mr,
+                                   (uint64_t)ldx * 2, BOX, t.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != TE_OK) return st;
+        for (int i = 0; i < z; ++i) {
+            const bool f32 = items[i].y_dtype == TE_F32;
+            Item &d = q.it[i];
+            d.y = static_cast<char *>(items[i].y) + (size_t)r0 * items[i].ldy * (f32 ? 4 : 2);
+            if (items[i].residual) d.resid = items[i].residual + (size_t)r0 * items[i].ldr;
+            st = make_map_2d(&q.tw[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, items[i].w.q, (uint64_t)k,
+                             (uint64_t)items[i].w.n, (uint64_t)k, BOX, BM, CU_TENSOR_MAP_SWIZZLE_64B);
+            if (st != TE_OK) return st;
+            st = make_map_2d(&q.ty[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                             d.y, (uint64_t)items[i].w.n, (uint64_t)mr, (uint64_t)items[i].ldy * (f32 ? 4 : 2), 32,
+                             32, CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (st != TE_OK) return st;
+        }
+        if (t.bn == 192) return t.tpa == 2 ? launch<192, false, 2>(q, ftiles, s) : launch<192, false, 1>(q, ftiles, s);
+        if (t.bn == 128) return t.tpa == 2 ? launch<128, false, 2>(q, ftiles, s) : launch<128, false, 1>(q, ftiles, s);
+        return launch<64, false, 1>(q, ftiles, s);
+    };
+    te_status st = part(0, m1, t1);
+    if (st == TE_OK && m1 < m) st = part(m1, m - m1, tail_tile(m - m1, k, ftiles));
+    return st;
 }
 
 extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, int32_t k,
@@ -1030,27 +1129,36 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     d.tile0 = 0;
     d.ntiles = (f + BM / 2 - 1) / (BM / 2);
     if (m == 0) return TE_OK;
-    int bn = pick_bn(m, k, p.res), tpa = 1;
-    if (bn == 192 && !p.res) {
-        const LongKTile lt = long_k_tile(m, k, d.ntiles);
-        bn = lt.bn;
-        tpa = lt.tpa;
-    }
-    te_status st = make_map_2d(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)k, (uint64_t)m,
-                               (uint64_t)ldx * 2, BOX, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != TE_OK) return st;
-    if ((st = make_map_2d(&p.tw[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, wg->q, (uint64_t)k, (uint64_t)f,
-                          (uint64_t)k, BOX, BM / 2, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_OK)
-        return st;
-    if ((st = make_map_2d(&p.tw[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, wu->q, (uint64_t)k, (uint64_t)f,
-                          (uint64_t)k, BOX, BM / 2, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_OK)
-        return st;
-    // each epilogue warp stores 16 features x 32 tokens of a block
-    if ((st = make_map_2d(&p.ty[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, (uint64_t)f, (uint64_t)m,
-                          (uint64_t)ldm * 2, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_OK)
-        return st;
+    const int ftiles = d.ntiles;
+    const TilePlan t1 = tile_for(m, k, ftiles);
+    const int m1 = split_rows(m, k, ftiles, t1);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (bn == 192) return tpa == 2 ? launch<192, true, 2>(p, d.ntiles, s) : launch<192, true, 1>(p, d.ntiles, s);
-    if (bn == 128) return tpa == 2 ? launch<128, true, 2>(p, d.ntiles, s) : launch<128, true, 1>(p, d.ntiles, s);
-    return launch<64, true, 1>(p, d.ntiles, s);
+    // rows [r0, r0 + mr) with tile t (see te_q8_linear)
+    auto part = [&](int r0, int mr, const TilePlan &t) -> te_status {
+        Params q = p;
+        q.m = mr;
+        q.res = t.res;
+        const char *xb = static_cast<const char *>(x) + (size_t)r0 * ldx * 2;
+        char *ob = static_cast<char *>(out) + (size_t)r0 * ldm * 2;
+        q.it[0].y = ob;
+        te_status st = make_map_2d(&q.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, (uint64_t)k, (uint64_t)mr,
+                                   (uint64_t)ldx * 2, BOX, t.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != TE_OK) return st;
+        if ((st = make_map_2d(&q.tw[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, wg->q, (uint64_t)k, (uint64_t)f,
+                              (uint64_t)k, BOX, BM / 2, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_OK)
+            return st;
+        if ((st = make_map_2d(&q.tw[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, wu->q, (uint64_t)k, (uint64_t)f,
+                              (uint64_t)k, BOX, BM / 2, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_OK)
+            return st;
+        // each epilogue warp stores 16 features x 32 tokens of a block
+        if ((st = make_map_2d(&q.ty[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ob, (uint64_t)f, (uint64_t)mr,
+                              (uint64_t)ldm * 2, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_OK)
+            return st;
+        if (t.bn == 192) return t.tpa == 2 ? launch<192, true, 2>(q, ftiles, s) : launch<192, true, 1>(q, ftiles, s);
+        if (t.bn == 128) return t.tpa == 2 ? launch<128, true, 2>(q, ftiles, s) : launch<128, true, 1>(q, ftiles, s);
+        return launch<64, true, 1>(q, ftiles, s);
+    };
+    te_status st = part(0, m1, t1);
+    if (st == TE_OK && m1 < m) st = part(m1, m - m1, tail_tile(m - m1, k, ftiles));
+    return st;
 }
