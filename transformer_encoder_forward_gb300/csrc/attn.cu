@@ -52,6 +52,10 @@ namespace {
 constexpr int BQ = 128;     // queries per tile (= TMEM lanes); TL tiles per CTA
 constexpr int BKV = 128;    // keys per tile
 constexpr int MAX_WORK = 640;   // work list entries carried in the launch parameters
+// the K and V bytes of all heads that the CTA order treats as one group, and
+// the bytes of one group when they do not fit (see the kernel's CTA order)
+constexpr long long KV_ALL_BYTES = 48ll << 20;
+constexpr long long KV_GROUP_BYTES = 24ll << 20;
 
 __device__ int g_attn_err;
 
@@ -61,7 +65,8 @@ struct AttnParams {
     __nv_bfloat16 *out;
     const int *cu;
     const int *items;          // two-range items [n][off1, len1, off2, len2], or NULL (cu)
-    int nwork;                 // > 0: CTA y -> work[y] = (unit << 16) | query block, longest first
+    int nwork;                 // > 0: work[i] = (unit << 16) | query block, longest first
+    int nq, hgroup;            // with a work list: heads, and heads per group of the CTA order
     uint32_t work[MAX_WORK];
     long long ldo;
     int q_off, k_off, v_off, group, window;
@@ -190,13 +195,24 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
     extern __shared__ uint8_t smem_raw[];
     // CTA (head, work): the work list orders (unit, 256-query block) by cost,
     // longest first, so that the long blocks start early and the launch ends
-    // without a tail of one long block; without it, (query block, head, unit)
+    // without a tail of one long block.  The 1-D grid takes the heads in
+    // groups of hgroup: within a group, work items in list order, the group's
+    // heads fastest, so that the CTAs running together read the K and V of a
+    // few heads (in L2) rather than of all.  Without a work list, (query
+    // block, head, unit) is the grid.
     int seq, qblk, h;
     if (p.nwork) {
-        const uint32_t wv = p.work[blockIdx.y];
+        const int b = blockIdx.x;
+        const int per = p.hgroup * p.nwork;
+        const int g = b / per;
+        const int r = b - g * per;
+        const int h0 = g * p.hgroup;
+        const int gn = p.nq - h0 < p.hgroup ? p.nq - h0 : p.hgroup;
+        const int wi = r / gn;
+        const uint32_t wv = p.work[wi];
         seq = (int)(wv >> 16);
         qblk = (int)(wv & 0xFFFFu);
-        h = blockIdx.x;
+        h = h0 + (r - wi * gn);
     } else {
         seq = blockIdx.z;
         qblk = blockIdx.x;
@@ -536,7 +552,7 @@ te_status launch(const AttnParams &p, int max_len, int nq, int nseq, cudaStream_
         if (e != cudaSuccess) return cuda_fail(e, "attn: set shared memory size");
         attr_done = true;
     }
-    const dim3 grid = p.nwork ? dim3(nq, p.nwork, 1) : dim3((max_len + TL * BQ - 1) / (TL * BQ), nq, nseq);
+    const dim3 grid = p.nwork ? dim3(nq * p.nwork, 1, 1) : dim3((max_len + TL * BQ - 1) / (TL * BQ), nq, nseq);
     attn_tc_kernel<HD, TL><<<grid, L::NTHREADS, smem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TE_OK : cuda_fail(e, "attn launch");
@@ -633,6 +649,17 @@ static te_status attn_launch(const void *qkv, int64_t ld, int32_t q_off, int32_t
     // a CTA (two CTAs would not fit an SM's shared memory)
     const int tl = hd == 64 ? 1 : 2;
     p.nwork = build_work(unit_lens, units, window, tl * BQ, p.work);
+    // heads per group: all when every head's K and V fit in KV_ALL_BYTES
+    // together, else the kv heads whose K and V make about KV_GROUP_BYTES
+    p.nq = nq_heads;
+    const long long kv_head = (long long)total * hd * 4;
+    long long hg = nq_heads;
+    if (kv_head * nkv_heads > KV_ALL_BYTES) {
+        hg = KV_GROUP_BYTES / kv_head * p.group;
+        if (hg < p.group) hg = p.group;
+        if (hg > nq_heads) hg = nq_heads;
+    }
+    p.hgroup = (int)hg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return hd == 64 ? launch<64, 1>(p, max_len, nq_heads, units, s)
                     : launch<128, 2>(p, max_len, nq_heads, units, s);

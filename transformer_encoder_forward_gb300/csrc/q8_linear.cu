@@ -35,7 +35,8 @@
 //     output feature, so the row scale and bias are per-thread constants;
 //     each 32 x 32 block is written into a staging tile in the output's own
 //     layout and leaves with one TMA tensor store (a TMA reduce-add when the
-//     residual is y itself, the in-place x += proj of the plain block).  In
+//     residual is y itself, the in-place x += proj of the plain block); the
+//     blocks go out in chunks, one shared-memory fence a chunk.  In
 //     the gated form each lane quadrant holds 16 gate rows and the same
 //     features' up rows, paired by register shuffles.
 // The issuing thread's instruction rate bounds the MMA rate at N <= 192 (one
@@ -59,6 +60,7 @@
 #include <cuda.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -69,6 +71,9 @@ constexpr int BM = 128;       // weight rows (output features) per tile = TMEM l
 constexpr int BK = 128;       // K per pipeline stage (two 64-wide TMA boxes)
 constexpr int BOX = 64;       // K width of one TMA box
 constexpr int MAXZ = 4;
+// activation bytes of one group of token tiles in the unit order: small
+// enough that the group stays in L2 while outputs and weights stream through
+constexpr long long XGROUP_BYTES = 24ll << 20;
 constexpr int NWARPS = 14;    // producer, MMA, 8 converters, 4 epilogue
 constexpr int NTHREADS = NWARPS * 32;
 
@@ -93,6 +98,8 @@ struct Params {
     CUtensorMap ty[MAXZ];     // y_i: [m, n_i] (f32 or bf16), 32-feature boxes
     Item it[MAXZ];
     int z, m, k, ttiles, nunits;
+    int fpairs;               // pairs of 128-row feature tiles
+    int tgroup;               // token tiles per group of the unit order
     int kb32;                 // k / 32: the row stride of the block scales
     int res;                  // resident weights (see q8_gemm_kernel)
 };
@@ -117,11 +124,11 @@ struct Layout {
     static constexpr int X_OFF = 0;
     static constexpr int W_OFF = NST * XBYTES;
     // epilogue staging, per epilogue warp: a ring of 32-token output blocks
-    // (f32 32 x 32: 4 KB; bf16 32 x 32: 2 KB; gated bf16 32 x 16: 1 KB), so
-    // that a block's TMA store can still be reading while the next ones are
-    // written; 8 KB a warp where shared memory allows (the one-tile units of
-    // the short-K GEMMs, whose epilogue sets their pace), else 4 KB; 128-byte
-    // aligned (TMA sources).  q8_2f: each stage's 128 column-field values
+    // (f32 32 x 32: 4 KB; bf16 32 x 32: 2 KB; gated bf16 32 x 16: 1 KB) in two
+    // halves, so that one chunk's TMA stores can still be reading while the
+    // next chunk is written; 8 KB a warp where shared memory allows (the
+    // one-tile units of the short-K GEMMs, whose epilogue sets their pace),
+    // else 4 KB; 128-byte aligned (TMA sources).  q8_2f: each stage's 128 column-field values
     // (f32), for the gate and the up weight in the gated form
     static constexpr int COL_OFF = W_OFF + NST * WBYTES;
     static constexpr int COL_BYTES = 2 * BK * 4;
@@ -188,15 +195,28 @@ struct TileCoord {
 // Work units are (pair of 128-row feature tiles, BN-token tile).  The two CTAs
 // of a cluster take the two feature tiles of one unit: they share the token
 // tile, and each CTA TMA-loads its own half of it into its own shared memory
-// (no load is multicast); the 2-SM MMA reads both halves.  Feature
-// tile major, token tiles fastest: clusters running together share weight
-// tiles, and the activation (re-read once per feature pair) stays in L2.  A
-// feature tile past the last one (odd count) is a phantom: its weights read
-// as zeros and its epilogue stores nothing.
+// (no load is multicast); the 2-SM MMA reads both halves.  Units come in
+// groups of tgroup token tiles; within a group, feature pair major and the
+// group's token tiles fastest: clusters running together share weight tiles,
+// and the group's activation rows (re-read once per feature pair) stay in L2
+// while the weights stream past them once per group.  A feature tile past the
+// last one (odd count) is a phantom: its weights read as zeros and its
+// epilogue stores nothing.
 template <bool GATED>
 __device__ __forceinline__ TileCoord tile_coord(const Params &p, int unit, int rank) {
-    const int fp = unit / p.ttiles;
-    const int tt = unit - fp * p.ttiles;
+    int fp, tt;
+    if (p.tgroup >= p.ttiles) {
+        fp = unit / p.ttiles;
+        tt = unit - fp * p.ttiles;
+    } else {
+        const int per = p.tgroup * p.fpairs;
+        const int g = unit / per;
+        const int r = unit - g * per;
+        const int t0 = g * p.tgroup;
+        const int gn = p.ttiles - t0 < p.tgroup ? p.ttiles - t0 : p.tgroup;
+        fp = r / gn;
+        tt = t0 + (r - fp * gn);
+    }
     const int ft = 2 * fp + rank;
     int zi = 0;
     while (zi + 1 < p.z && ft >= p.it[zi + 1].tile0) ++zi;
@@ -597,31 +617,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const int frow = GATED ? 16 * q + (lane & 15) : row;
         const uint32_t tl = (uint32_t)(32 * q) << 16;
         int lt = 0;
-        // staging: gated, one 32-token x 16-feature bf16 tile per warp;
-        // ungated, one 32 x 32 tile (f32 or bf16) per warp
-        // this warp's staging (a shared-memory address)
+        // this warp's staging (a shared-memory address): a ring of output
+        // blocks (gated 32 tokens x 16 features bf16, 1 KB; else 32 x 32, f32
+        // 4 KB or bf16 2 KB) in two halves.  A token tile's blocks go out in
+        // chunks of half the ring: each chunk is written, made visible to the
+        // async proxy by one fence, and sent by one TMA store a block (one
+        // bulk group a chunk; gated, one a store); the next chunk takes the
+        // other half once the groups before the previous chunk have finished
+        // reading.  One fence a chunk instead of one a block is what keeps the
+        // short-K GEMMs' drain short.
         const uint32_t stg = sb + L::STG_OFF + (warp - 10) * L::STG_WARP;
-        int slot = 0, slot_bytes = 0;   // next block of the staging ring, its size
-        // the next staging block of `bytes`: waits until the store that last
-        // used it has finished reading it (at most nb - 1 younger stores may
-        // still be reading), then hands out its shared address.  Items of one launch
-        // may differ in block size: a change of size first lets every store
-        // finish reading.
-        auto next_block = [&](int bytes) -> uint32_t {
-            const int nb = L::STG_WARP / bytes;
-            const bool resize = bytes != slot_bytes;
-            if (slot >= nb || resize) slot = 0;
-            slot_bytes = bytes;
-            if (lane == 0) {
-                if (resize) bulk_wait_read_n<0>();
-                else if (nb >= 8) bulk_wait_read_n<7>();
-                else if (nb >= 4) bulk_wait_read_n<3>();
-                else if (nb >= 2) bulk_wait_read_n<1>();
-                else bulk_wait_read_n<0>();
-            }
-            __syncwarp();
-            return stg + (uint32_t)(slot++ * bytes);
-        };
+        int half = 0, slot_bytes = 0;   // the next chunk's half, the ring's block size
+        // gated: the ring position (blocks so far), and whether the last
+        // chunk made GBSZ bulk groups
+        int gslot = 0;
+        bool gfull = true;
         for (; lt < ucnt && ok; ++lt) {
             const int u = unit_at(lt);
             const int b = TPA == 2 ? 0 : (lt & 1);
@@ -645,102 +655,168 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const bool f32out = p.it[tc.zi].ydt == TE_F32;
             const float *__restrict__ rbase = p.it[tc.zi].resid;
             const bool inplace = rbase != nullptr && rbase == p.it[tc.zi].y;
-            for (int tt = 0; tt < TPA; ++tt) {
-            const int acol = (TPA == 2 ? tt : b) * BN;     // this token tile's accumulator
-            const int t0 = (tc.t0 * TPA + tt) * BN;
-            if (GATED) {
-                // per 32-token block: both halves bf16-rounded after scale and
-                // bias; gate lane l and up lane l + 16 swap half their tokens, so
-                // that lane l writes m = act(g) * u for tokens 0-15 and lane
-                // l + 16 for tokens 16-31 of feature 16 q + l
-                const int fo = tc.o0 + 16 * q;
-                const int jb = upper ? 16 : 0;
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (t0 + 32 * c >= p.m) break;      // warp-uniform
-                    uint32_t v[32];
-                    tmem_ld32(tbase + tl + acol + 32 * c, v);
-                    tmem_wait_ld();
-                    float yv[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float lo = round_bf16(__uint_as_float(v[j]) * sc + bi);
-                        const float hi = round_bf16(__uint_as_float(v[16 + j]) * sc + bi);
-                        // the gate lane sends its token 16 + j, the up lane its token j
-                        const float got = __shfl_xor_sync(0xFFFFFFFFu, upper ? lo : hi, 16);
-                        // operands selected first: one activation per lane, no branch
-                        const float gv = upper ? got : lo, uv = upper ? hi : got;
-                        yv[j] = apply_act_tanh(gv, act) * uv;
+            // Drains blocks [0, cn) of one token tile (accumulator column acol,
+            // tokens t0..) in chunks; the block size is a compile-time
+            // constant of each output form (BYTES: 1024 gated, 4096 staged
+            // f32, 2048 bf16), so a chunk's blocks unroll.  Items of one launch
+            // may differ in block size: a change of size first lets every
+            // store finish reading.
+            auto drain_tile = [&](auto bytes_c, int acol, int t0, int cn, int fo) {
+                constexpr int BYTES = decltype(bytes_c)::value;
+                constexpr int NB = L::STG_WARP / BYTES;
+                constexpr int BSZ = NB >= 2 ? NB / 2 : 1;       // blocks a chunk
+                for (int c0 = 0; c0 < cn; c0 += BSZ) {
+                    const bool resize = BYTES != slot_bytes;
+                    if (resize) {
+                        half = 0;
+                        slot_bytes = BYTES;
                     }
-                    const uint32_t so = next_block(1024);
-                    uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
+                    if (lane == 0) {
+                        if (resize || NB < 2) bulk_wait_read_n<0>();
+                        else bulk_wait_read_n<1>();
+                    }
+                    __syncwarp();
+                    const uint32_t base = stg + (uint32_t)(half * (NB / 2) * BYTES);
+                    if (NB >= 2) half ^= 1;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) ostg_h[(jb + j) * 16 + (lane & 15)] = __bfloat16_as_ushort(__float2bfloat16_rn(yv[j]));
+                    for (int i = 0; i < BSZ; ++i) {
+                        const int c = c0 + i;
+                        if (c >= cn) break;                         // warp-uniform
+                        const uint32_t so = base + (uint32_t)(i * BYTES);
+                        uint32_t v[32];
+                        tmem_ld32(tbase + tl + acol + 32 * c, v);
+                        tmem_wait_ld();
+                        {
+                            // v[] becomes the output values in place (f32 bits)
+                            if (act) {   // the ungated MLP: act(bf16(s*acc + b)), no residual
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    v[j] = __float_as_uint(
+                                        apply_act_tanh(round_bf16(__uint_as_float(v[j]) * sc + bi), act - 1));
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sc + bi);
+                            }
+                            if constexpr (BYTES == 4096) {
+                                float *ostg_f = reinterpret_cast<float *>(smem + (so - sb));
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) ostg_f[j * 32 + lane] = __uint_as_float(v[j]);
+                                if (rbase && !inplace) {
+                                    // a residual other than y (not used by the
+                                    // block): added to the f32 staging from
+                                    // global memory, then narrowed in place if
+                                    // y is bf16.  Row j's bf16 bytes only cover
+                                    // f32 rows <= j, which were read before.
+                                    __syncwarp();
+                                    const int tb = t0 + 32 * c;
+                                    const float *rr = rbase + (long long)tb * ldr + o;
+                                    const int jn = p.m - tb < 32 ? p.m - tb : 32;
+#pragma unroll 1
+                                    for (int j = 0; j < jn; ++j)
+                                        if (ov) ostg_f[j * 32 + lane] += rr[(long long)j * ldr];
+                                    if (!f32out) {
+                                        uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
+#pragma unroll 1
+                                        for (int j = 0; j < 32; ++j) {
+                                            __syncwarp();
+                                            const float y = ostg_f[j * 32 + lane];
+                                            __syncwarp();
+                                            ostg_h[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+                                        }
+                                    }
+                                }
+                            } else {
+                                uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    ostg_h[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                            }
+                        }
+                    }
+                    // the chunk's writes, visible to the TMA engine, then its stores
                     fence_async_smem();
                     __syncwarp();
-                    if (lane == 0 && fo < n) {
-                        tma_store_2d(ymap, so, fo, t0 + 32 * c);
+                    if (lane == 0) {
+                        for (int i = 0; i < BSZ && c0 + i < cn; ++i) {
+                            const uint32_t so = base + (uint32_t)(i * BYTES);
+                            if (!GATED && inplace)
+                                tma_reduce_add_2d(ymap, so, fo, t0 + 32 * (c0 + i));
+                            else
+                                tma_store_2d(ymap, so, fo, t0 + 32 * (c0 + i));
+                        }
                         bulk_commit();
                     }
                 }
-            } else {
-                const int fo = tc.o0 + 32 * q;              // first feature of this warp's block
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (t0 + 32 * c >= p.m) break;      // warp-uniform
-                    uint32_t v[32];
-                    tmem_ld32(tbase + tl + acol + 32 * c, v);
-                    tmem_wait_ld();
-                    const int tb = t0 + 32 * c;
-                    // v[] becomes the output values in place (f32 bits)
-                    if (act) {   // the ungated MLP: act(bf16(s*acc + b)), no residual
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            v[j] = __float_as_uint(apply_act_tanh(round_bf16(__uint_as_float(v[j]) * sc + bi), act - 1));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sc + bi);
-                    }
-                    // a residual other than y is added in f32 staging
-                    const uint32_t so = next_block(f32out || (rbase && !inplace) ? 4096 : 2048);
-                    float *ostg_f = reinterpret_cast<float *>(smem + (so - sb));
-                    uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
-                    if (rbase && !inplace) {
-                        // a residual other than y (not used by the block): stage
-                        // f32, add the residual rows from global memory, then
-                        // narrow in place if y is bf16.  Row j's bf16 bytes only
-                        // cover f32 rows <= j, which were read before.
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) ostg_f[j * 32 + lane] = __uint_as_float(v[j]);
-                        __syncwarp();
-                        const float *rr = rbase + (long long)tb * ldr + o;
-                        const int jn = p.m - tb < 32 ? p.m - tb : 32;
-#pragma unroll 1
-                        for (int j = 0; j < jn; ++j)
-                            if (ov) ostg_f[j * 32 + lane] += rr[(long long)j * ldr];
-                        if (!f32out) {
-#pragma unroll 1
-                            for (int j = 0; j < 32; ++j) {
-                                __syncwarp();
-                                const float y = ostg_f[j * 32 + lane];
-                                __syncwarp();
-                                ostg_h[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-                            }
+            };
+            for (int tt = 0; tt < TPA; ++tt) {
+            const int acol = (TPA == 2 ? tt : b) * BN;     // this token tile's accumulator
+            const int t0 = (tc.t0 * TPA + tt) * BN;
+            // the token tile's 32-token blocks (the last may be partial; a
+            // second tile past m has none)
+            const int cn = t0 >= p.m ? 0 : ((p.m - t0 + 31) / 32 < BN / 32 ? (p.m - t0 + 31) / 32 : BN / 32);
+            // this warp's first output feature: a warp whose features all lie
+            // past n (a phantom tile) has nothing to drain
+            const int fo = tc.o0 + (GATED ? 16 : 32) * q;
+            if (fo < n) {
+                if constexpr (GATED) {
+                    // 1 KB blocks in chunks of half the ring (the whole token
+                    // tile where the ring holds two), one bulk group a store.
+                    // Before a chunk, all but the previous chunk's GBSZ groups
+                    // have finished reading - after a chunk of fewer stores
+                    // (a ragged last tile), all of them.
+                    constexpr int GNB = L::STG_WARP / 1024;
+                    constexpr int GBSZ = GNB / 2 < BN / 32 ? GNB / 2 : BN / 32;
+                    static_assert(GBSZ == 2 || GBSZ == 4, "a ring of 2 GBSZ blocks indexed by a mask");
+                    const int jb = upper ? 16 : 0;
+                    for (int c0 = 0; c0 < cn; c0 += GBSZ) {
+                        const int ce = c0 + GBSZ < cn ? c0 + GBSZ : cn;
+                        if (lane == 0) {
+                            if (gfull) bulk_wait_read_n<GBSZ>();
+                            else bulk_wait_read_n<0>();
                         }
-                    } else if (f32out) {
+                        __syncwarp();
+                        for (int c = c0; c < ce; ++c) {
+                            uint32_t v[32];
+                            tmem_ld32(tbase + tl + acol + 32 * c, v);
+                            tmem_wait_ld();
+                            // both halves bf16-rounded after scale and bias; gate
+                            // lane l and up lane l + 16 swap half their tokens,
+                            // so that lane l writes m = act(g) * u for tokens
+                            // 0-15 and lane l + 16 for tokens 16-31 of feature
+                            // 16 q + l
+                            float yv[16];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) ostg_f[j * 32 + lane] = __uint_as_float(v[j]);
-                    } else {
+                            for (int j = 0; j < 16; ++j) {
+                                const float lo = round_bf16(__uint_as_float(v[j]) * sc + bi);
+                                const float hi = round_bf16(__uint_as_float(v[16 + j]) * sc + bi);
+                                // the gate lane sends its token 16 + j, the up lane its token j
+                                const float got = __shfl_xor_sync(0xFFFFFFFFu, upper ? lo : hi, 16);
+                                // operands selected first: one activation per lane, no branch
+                                const float gv = upper ? got : lo, uv = upper ? hi : got;
+                                yv[j] = apply_act_tanh(gv, act) * uv;
+                            }
+                            const uint32_t so = stg + (uint32_t)(((gslot + c) & (2 * GBSZ - 1)) * 1024);
+                            uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) ostg_h[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                            for (int j = 0; j < 16; ++j)
+                                ostg_h[(jb + j) * 16 + (lane & 15)] = __bfloat16_as_ushort(__float2bfloat16_rn(yv[j]));
+                        }
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            for (int c = c0; c < ce; ++c) {
+                                tma_store_2d(ymap, stg + (uint32_t)(((gslot + c) & (2 * GBSZ - 1)) * 1024), fo,
+                                             t0 + 32 * c);
+                                bulk_commit();
+                            }
+                        gfull = ce - c0 == GBSZ;
                     }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && fo < n) {
-                        if (inplace)
-                            tma_reduce_add_2d(ymap, so, fo, tb);
-                        else
-                            tma_store_2d(ymap, so, fo, tb);
-                        bulk_commit();
-                    }
+                    // chunk k of the tile used ring blocks gslot + k GBSZ + i
+                    gslot += (cn + GBSZ - 1) / GBSZ * GBSZ;
+                } else if (f32out || (rbase && !inplace)) {   // a residual other than y is added in f32
+                    drain_tile(std::integral_constant<int, 4096>{}, acol, t0, cn, fo);
+                } else {
+                    drain_tile(std::integral_constant<int, 2048>{}, acol, t0, cn, fo);
                 }
             }
             if (TPA == 2) {
@@ -924,7 +1000,13 @@ te_status launch(Params &p, int ftiles, cudaStream_t stream) {
         max_clusters[dev] = n;
     }
     p.ttiles = (p.m + TPA * BN - 1) / (TPA * BN);
-    p.nunits = p.ttiles * ((ftiles + 1) / 2);
+    p.fpairs = (ftiles + 1) / 2;
+    p.nunits = p.ttiles * p.fpairs;
+    // token tiles per group: about XGROUP_BYTES of activation rows (resident
+    // weights: one group, so a cluster's run keeps its feature pair)
+    const long long xtile = (long long)TPA * BN * p.k * 2;
+    const long long tg = p.res ? p.ttiles : XGROUP_BYTES / xtile;
+    p.tgroup = tg < 1 ? 1 : (tg > p.ttiles ? p.ttiles : (int)tg);
     const int clusters = p.nunits < max_clusters[dev] ? p.nunits : max_clusters[dev];
     q8_gemm_kernel<BN, GATED, TPA><<<2 * clusters, NTHREADS, smem, stream>>>(p);
     e = cudaGetLastError();
