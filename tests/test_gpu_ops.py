@@ -233,6 +233,10 @@ ATTN_CASES = [
     ([700, 129], 2, 1, 128, 512),
     ([1056, 1056], 2, 2, 128, 0),
     ([955, 16, 400], 2, 2, 64, 512),
+    # many heads with grouped K/V: more work items (480) than CTAs resident
+    # at once (two an SM), in several waves
+    ([955, 16, 400, 130, 64, 1, 200, 37], 24, 8, 64, 0),
+    ([955, 16, 400, 130, 64, 1, 200, 37], 24, 24, 64, 100),
 ]
 
 
@@ -684,6 +688,25 @@ def test_attention_two_range_items_match_oracle(hd, nq, nkv, n_img, n_cap, windo
     got = to_np(out)
     assert np.all(np.isfinite(got))
     assert rel_frob(got, ref) < 3e-3, rel_frob(got, ref)
+
+
+def test_attention_two_range_items_many_heads():
+    """More work items (8 query blocks x 48 heads = 384) than hd-64 CTAs
+    resident at once, over four two-range items."""
+    torch = _torch()
+    rng = np.random.default_rng(47)
+    hd, nq, nkv = 64, 48, 16
+    items, x, x64, T, W = _items_case(rng, hd, nq, nkv, 160, 96, nitems=4)
+    out = torch.full((T, nq * hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    scale = hd ** -0.5
+    te.attn_items_fwd(x, W, 0, nq * hd, (nq + nkv) * hd, items, to_dev(items), T, nq, nkv, hd, 0, scale, out,
+                      nq * hd)
+    te.check()
+    ref = O.attention_items(x64, items, nq, nkv, hd, 0, nq * hd, (nq + nkv) * hd, 0, scale)
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    e = record_margin("attention", "two-range items, 48 heads", rel_frob(got, ref), 3e-3)
+    assert e < 3e-3, e
 
 
 def test_attention_items_equal_varlen_on_gathered_rows_bit_exactly():
