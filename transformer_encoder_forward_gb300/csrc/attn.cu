@@ -149,8 +149,12 @@ __device__ __forceinline__ float row_max_regs(const uint32_t (&v0)[64], const ui
 #pragma unroll
     for (int e = 0; e < 64; ++e) {
         const float x0 = __uint_as_float(v0[e]), x1 = __uint_as_float(v1[e]);
-        if (!MASK || sp.has(e)) m8[e & 7] = fmaxf(m8[e & 7], x0);
-        if (!MASK || sp.has(64 + e)) m8[e & 7] = fmaxf(m8[e & 7], x1);
+        if (!MASK) {
+            m8[e & 7] = fmax3(m8[e & 7], x0, x1);
+        } else {
+            if (sp.has(e)) m8[e & 7] = fmaxf(m8[e & 7], x0);
+            if (sp.has(64 + e)) m8[e & 7] = fmaxf(m8[e & 7], x1);
+        }
     }
     return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
@@ -163,28 +167,36 @@ template <bool MASK>
 __device__ __forceinline__ float row_exp_regs(uint32_t scol, const uint32_t (&v0)[64], const uint32_t (&v1)[64],
                                               float c, float nm, int qi, int kv0, int len, int W) {
     const KeySpan sp = key_span(qi, kv0, len, W);
-    float r8[8];
+    // the scale, offset and the eight partial sums as f32 pairs: one paired
+    // FMA and one paired add for two keys (partial sum i keeps the keys
+    // with index = i mod 8, as pairs (2i', 2i' + 1))
+    const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(nm, nm);
+    uint64_t r4[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) r8[i] = 0.f;
+    for (int i = 0; i < 4; ++i) r4[i] = f2_pack(0.f, 0.f);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         const uint32_t (&v)[64] = hh ? v1 : v0;
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), c, nm));
-            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c, nm));
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), c2, nm2), a0, a1);
+            float p0 = fast_exp2(a0);
+            float p1 = fast_exp2(a1);
             if (MASK) {
-                const int k = kv0 + 64 * hh + 2 * e;
-                if (!sp.has(k - kv0)) p0 = 0.f;
-                if (!sp.has(k - kv0 + 1)) p1 = 0.f;
+                const int k = 64 * hh + 2 * e;
+                if (!sp.has(k)) p0 = 0.f;
+                if (!sp.has(k + 1)) p1 = 0.f;
             }
-            r8[(2 * e) & 7] += p0;
-            r8[(2 * e + 1) & 7] += p1;
+            r4[e & 3] = f2_add(r4[e & 3], f2_pack(p0, p1));
             pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st32(scol + 32 * hh, pk);
     }
+    float r8[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f2_unpack(r4[i], r8[2 * i], r8[2 * i + 1]);
     return ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
 }
 

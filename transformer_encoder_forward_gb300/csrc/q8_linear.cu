@@ -688,14 +688,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         tmem_wait_ld();
                         {
                             // v[] becomes the output values in place (f32 bits)
+                            // s*acc + b in f32 pairs (two tokens an instruction)
+                            {
+                                const uint64_t sc2 = f2_pack(sc, sc), bi2 = f2_pack(bi, bi);
+#pragma unroll
+                                for (int j = 0; j < 32; j += 2) {
+                                    float a, b2;
+                                    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sc2, bi2),
+                                              a, b2);
+                                    v[j] = __float_as_uint(a);
+                                    v[j + 1] = __float_as_uint(b2);
+                                }
+                            }
                             if (act) {   // the ungated MLP: act(bf16(s*acc + b)), no residual
 #pragma unroll
                                 for (int j = 0; j < 32; ++j)
-                                    v[j] = __float_as_uint(
-                                        apply_act_tanh(round_bf16(__uint_as_float(v[j]) * sc + bi), act - 1));
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sc + bi);
+                                    v[j] = __float_as_uint(apply_act_tanh(round_bf16(__uint_as_float(v[j])), act - 1));
                             }
                             if constexpr (BYTES == 4096) {
                                 float *ostg_f = reinterpret_cast<float *>(smem + (so - sb));
@@ -764,6 +772,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     // Before a chunk, all but the previous chunk's GBSZ groups
                     // have finished reading - after a chunk of fewer stores
                     // (a ragged last tile), all of them.
+                    // one 32-token block: scale and bias, both halves rounded
+                    // to bf16 (one conversion for the pair); gate lane l and up
+                    // lane l + 16 swap half their tokens, so that lane l
+                    // computes m = act(g) * u for tokens 0-15 and lane l + 16
+                    // for tokens 16-31 of feature 16 q + l; the arithmetic in
+                    // f32 pairs (two tokens an instruction, each rounded as
+                    // the scalar form), the tanh one token at a time
+                    auto gated_math = [&](auto act_c, const uint32_t (&v)[32], float (&yv)[16]) {
+                        constexpr int ACT = decltype(act_c)::value;
+                        const uint64_t sc2 = f2_pack(sc, sc), bi2 = f2_pack(bi, bi);
+                        const uint64_t half2 = f2_pack(0.5f, 0.5f);
+                        float gv[16], uv[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            float lo, hi;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[16 + j])), sc2, bi2),
+                                      lo, hi);
+                            const uint32_t b2 = pack_bf16x2(lo, hi);
+                            lo = bf16_lo(b2);
+                            hi = bf16_hi(b2);
+                            // the gate lane sends its token 16 + j, the up lane its token j
+                            const float got = __shfl_xor_sync(0xFFFFFFFFu, upper ? lo : hi, 16);
+                            // operands selected first: one activation per lane, no branch
+                            gv[j] = upper ? got : lo;
+                            uv[j] = upper ? hi : got;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            const uint64_t g2 = f2_pack(gv[j], gv[j + 1]);
+                            // GELU-tanh: z = g (0.79788456 + 0.035677408 g^2); SiLU: z = g / 2
+                            uint64_t z2;
+                            if constexpr (ACT == TE_ACT_GELU_TANH)
+                                z2 = f2_mul(g2, f2_fma(f2_pack(0.035677408f, 0.035677408f), f2_mul(g2, g2),
+                                                       f2_pack(0.79788456f, 0.79788456f)));
+                            else
+                                z2 = f2_mul(half2, g2);
+                            float z0, z1;
+                            f2_unpack(z2, z0, z1);
+                            const uint64_t h2 = f2_mul(half2, g2);
+                            const uint64_t a2 = f2_fma(h2, f2_pack(hw_tanh(z0), hw_tanh(z1)), h2);
+                            f2_unpack(f2_mul(a2, f2_pack(uv[j], uv[j + 1])), yv[j], yv[j + 1]);
+                        }
+                    };
                     constexpr int GNB = L::STG_WARP / 1024;
                     constexpr int GBSZ = GNB / 2 < BN / 32 ? GNB / 2 : BN / 32;
                     static_assert(GBSZ == 2 || GBSZ == 4, "a ring of 2 GBSZ blocks indexed by a mask");
@@ -779,22 +830,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                             uint32_t v[32];
                             tmem_ld32(tbase + tl + acol + 32 * c, v);
                             tmem_wait_ld();
-                            // both halves bf16-rounded after scale and bias; gate
-                            // lane l and up lane l + 16 swap half their tokens,
-                            // so that lane l writes m = act(g) * u for tokens
-                            // 0-15 and lane l + 16 for tokens 16-31 of feature
-                            // 16 q + l
                             float yv[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const float lo = round_bf16(__uint_as_float(v[j]) * sc + bi);
-                                const float hi = round_bf16(__uint_as_float(v[16 + j]) * sc + bi);
-                                // the gate lane sends its token 16 + j, the up lane its token j
-                                const float got = __shfl_xor_sync(0xFFFFFFFFu, upper ? lo : hi, 16);
-                                // operands selected first: one activation per lane, no branch
-                                const float gv = upper ? got : lo, uv = upper ? hi : got;
-                                yv[j] = apply_act_tanh(gv, act) * uv;
-                            }
+                            if (act == TE_ACT_GELU_TANH)
+                                gated_math(std::integral_constant<int, TE_ACT_GELU_TANH>{}, v, yv);
+                            else
+                                gated_math(std::integral_constant<int, TE_ACT_SILU>{}, v, yv);
                             const uint32_t so = stg + (uint32_t)(((gslot + c) & (2 * GBSZ - 1)) * 1024);
                             uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
 #pragma unroll
