@@ -628,10 +628,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // short-K GEMMs' drain short.
         const uint32_t stg = sb + L::STG_OFF + (warp - 10) * L::STG_WARP;
         int half = 0, slot_bytes = 0;   // the next chunk's half, the ring's block size
-        // gated: the ring position (blocks so far), and whether the last
-        // chunk made GBSZ bulk groups
+        // gated: the ring position (blocks so far)
         int gslot = 0;
-        bool gfull = true;
         for (; lt < ucnt && ok; ++lt) {
             const int u = unit_at(lt);
             const int b = TPA == 2 ? 0 : (lt & 1);
@@ -671,8 +669,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         half = 0;
                         slot_bytes = BYTES;
                     }
-                    if (lane == 0) {
-                        if (resize || NB < 2) bulk_wait_read_n<0>();
+                    // lane i stores block i of each chunk, one bulk group a
+                    // chunk (empty when the chunk is short)
+                    if (resize) bulk_wait_read_n<0>();   // every lane: earlier sizes' stores too
+                    else if (lane < BSZ) {
+                        if (NB < 2) bulk_wait_read_n<0>();
                         else bulk_wait_read_n<1>();
                     }
                     __syncwarp();
@@ -744,13 +745,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     // the chunk's writes, visible to the TMA engine, then its stores
                     fence_async_smem();
                     __syncwarp();
-                    if (lane == 0) {
-                        for (int i = 0; i < BSZ && c0 + i < cn; ++i) {
-                            const uint32_t so = base + (uint32_t)(i * BYTES);
+                    if (lane < BSZ) {
+                        if (c0 + lane < cn) {
+                            const uint32_t so = base + (uint32_t)(lane * BYTES);
                             if (!GATED && inplace)
-                                tma_reduce_add_2d(ymap, so, fo, t0 + 32 * (c0 + i));
+                                tma_reduce_add_2d(ymap, so, fo, t0 + 32 * (c0 + lane));
                             else
-                                tma_store_2d(ymap, so, fo, t0 + 32 * (c0 + i));
+                                tma_store_2d(ymap, so, fo, t0 + 32 * (c0 + lane));
                         }
                         bulk_commit();
                     }
@@ -821,10 +822,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const int jb = upper ? 16 : 0;
                     for (int c0 = 0; c0 < cn; c0 += GBSZ) {
                         const int ce = c0 + GBSZ < cn ? c0 + GBSZ : cn;
-                        if (lane == 0) {
-                            if (gfull) bulk_wait_read_n<GBSZ>();
-                            else bulk_wait_read_n<0>();
-                        }
+                        // lane i stores block i of each chunk, one bulk group
+                        // a chunk (empty when the chunk is short): its group
+                        // of the chunk before the previous, which used this
+                        // half of the ring, has finished reading
+                        if (lane < GBSZ) bulk_wait_read_n<1>();
                         __syncwarp();
                         for (int c = c0; c < ce; ++c) {
                             uint32_t v[32];
@@ -843,13 +845,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         }
                         fence_async_smem();
                         __syncwarp();
-                        if (lane == 0)
-                            for (int c = c0; c < ce; ++c) {
+                        if (lane < GBSZ) {
+                            const int c = c0 + lane;
+                            if (c < ce)
                                 tma_store_2d(ymap, stg + (uint32_t)(((gslot + c) & (2 * GBSZ - 1)) * 1024), fo,
                                              t0 + 32 * c);
-                                bulk_commit();
-                            }
-                        gfull = ce - c0 == GBSZ;
+                            bulk_commit();
+                        }
                     }
                     // chunk k of the tile used ring blocks gslot + k GBSZ + i
                     gslot += (cn + GBSZ - 1) / GBSZ * GBSZ;
@@ -874,7 +876,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
         }
         // the stores must be complete before the CTA's shared memory goes away
-        if (lane == 0) bulk_wait_all();
+        // (each storing lane waits for its own bulk groups)
+        bulk_wait_all();
         __syncwarp();
     }
     if (!ok && s_skip == 0) atomicExch(&g_gemm_err, 1);
