@@ -381,6 +381,28 @@ def run_op(args):
     print(json.dumps(out), flush=True)
 
 
+def run_mma_peak(args):
+    """The q8 GEMM's MMA form issued back to back with no loads (te_mma_peak)
+    at each token-tile width: the tensor ceiling its pipeline could reach,
+    one JSON line per width."""
+    import torch
+    import transformer_encoder_forward_gb300 as te
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    pairs = te.sm_count(dev.index) // 2
+    peaks = read_peaks()
+    for bn in (64, 128, 192, 256):
+        stages = 4000
+        for _ in range(args.warmup):
+            te.mma_peak(bn, stages)
+        ms = min(te.mma_peak(bn, stages) for _ in range(max(args.steps, 1)))
+        flops = pairs * stages * 8 * 2 * 256 * bn * 16
+        tf = flops / (ms * 1e-3) / 1e12
+        print(json.dumps({"op": "mma_peak", "n": bn, "m": 256, "k_per_mma": 16, "sm_pairs": pairs,
+                          "ms": round(ms, 4), "tflops": round(tf, 1),
+                          "of_measured_bf16": round(tf / peaks["bf16_tflops"], 4)}), flush=True)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -634,12 +656,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--op", default=None,
                     help="time one op of the workload alone (gemm_qkv, gemm_o, gemm_gu (gate fused), "
-                         "gemm_down, attn_w<window>, qk_prep, add_norm) instead of the forward")
+                         "gemm_down, attn_w<window>, qk_prep, add_norm) instead of the forward; "
+                         "mma_peak: the GEMM's MMA form without loads, its tensor ceiling")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "mma_peak":
+        run_mma_peak(args)
     elif args.op:
         run_op(args)
     else:

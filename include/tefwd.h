@@ -253,6 +253,17 @@ te_status te_qk_prep_rope(void *qkv, int64_t ld, int32_t q_off, int32_t k_off, i
  * pages have no counterpart of this entry point. */
 te_status te_selftest_wait_timeout(int32_t limit_us, te_stream stream);
 
+/* mma_peak: the tensor-core ceiling of the q8 GEMM's own MMA form.  On every
+ * SM pair of the current device, `stages` x 8 back-to-back 2-SM MMAs
+ * (tcgen05 kind::f16, A in TMEM, B in shared memory, M = 256, N = bn,
+ * K = 16, f32 accumulate) with no loads, no waits and no epilogue; *ms
+ * receives the launch's device time (CUDA events on `stream`; the call
+ * waits for it).  Work = (SMs / 2) x stages x 8 x 2 x 256 x bn x 16 flops.
+ * bn in {64, 128, 192, 256}; 1 <= stages <= 2^22.  A measurement aid: the
+ * counterpart of the [ZI] module doc's "Ceiling" item (a pure MMA loop with
+ * no loads). */
+te_status te_mma_peak(int32_t bn, int32_t stages, float *ms, te_stream stream);
+
 /* cast_bf16: y = bf16(x) (round to nearest even) for x f32 [rows, d] (ldx),
  * y bf16 [rows, ldy]; d % 8 == 0.  The per-layer input path's GEMM reads the
  * residual stream this way. */

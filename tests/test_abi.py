@@ -233,3 +233,12 @@ def test_block_validation_and_workspace(L):
     next_s_only = _desc(mod=FAKE, next_mod_scale=FAKE, **sand_ok)
     assert _call(L, "te_encoder_block_fwd", ctypes.byref(next_s_only), FAKE, FAKE, p, FAKE, 2,
                  FAKE * 256, ws, None)[0] == te.TE_EINVAL
+
+
+def test_mma_peak_rejects_bad_arguments(L):
+    ms = ctypes.c_float(0.0)
+    st, msg = _call(L, "te_mma_peak", 100, 10, ctypes.byref(ms), None)
+    assert st == te.TE_EINVAL and "bn=100" in msg
+    st, msg = _call(L, "te_mma_peak", 192, 0, ctypes.byref(ms), None)
+    assert st == te.TE_EINVAL and "stages=0" in msg
+    assert _call(L, "te_mma_peak", 192, 10, None, None)[0] == te.TE_EINVAL

@@ -738,3 +738,16 @@ def test_attention_items_equal_varlen_on_gathered_rows_bit_exactly():
                        nkv, hd, 0, hd ** -0.5, o2, nq * hd)
     te.check()
     assert torch.equal(o1, o2)
+
+
+def test_mma_peak_runs_at_every_width():
+    """The MMA-form ceiling runs on every SM pair and reports a rate within
+    what the tensor cores can do: 8192 dense bf16 flops a cycle an SM, at
+    most 2.6 PFLOP/s at the 2070 MHz top clock of 152 SMs."""
+    pairs = te.sm_count() // 2
+    for bn in (64, 128, 192, 256):
+        ms = te.mma_peak(bn, 200)
+        te.check()
+        tf = pairs * 200 * 8 * 2 * 256 * bn * 16 / (ms * 1e-3) / 1e12
+        assert 50.0 < tf < 2700.0, (bn, ms, tf)
+

@@ -89,6 +89,7 @@ EXPORTS = {
                                         c_p, c_i32, c_f32, c_p, c_p, c_p, c_i32, c_i32, c_f32, c_i32,
                                         c_p]),
     "te_selftest_wait_timeout": (ctypes.c_int, [c_i32, c_p]),
+    "te_mma_peak": (ctypes.c_int, [c_i32, c_i32, c_p, c_p]),
     "te_cast_bf16": (ctypes.c_int, [c_p, c_i64, c_p, c_i64, c_i32, c_i32, c_p]),
     "te_gate_act": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_i64, c_i32, c_i32, c_p]),
     "te_pool_mean": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_i32, c_p, c_f32, c_p, c_p]),
@@ -214,6 +215,19 @@ def attn_items_fwd(qkv, ld, q_off, k_off, v_off, items_host, items_dev, rows, nq
 def selftest_wait_timeout(limit_us, stream=None):
     """Launch the bounded-wait self-test (a wait that can only time out)."""
     _ok(lib().te_selftest_wait_timeout(limit_us, _stream(stream)))
+
+
+def mma_peak(bn, stages, stream=None):
+    """Device ms of `stages` x 8 back-to-back 2-SM MMAs (N = bn) on every SM
+    pair: the q8 GEMM's tensor ceiling without loads (te_mma_peak)."""
+    ms = ctypes.c_float(0.0)
+    _ok(lib().te_mma_peak(bn, stages, ctypes.byref(ms), _stream(stream)))
+    return float(ms.value)
+
+
+def sm_count(device=0):
+    import torch
+    return torch.cuda.get_device_properties(device).multi_processor_count
 
 
 def cast_bf16(x, y, stream=None):

@@ -893,6 +893,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     cluster_sync();
 }
 
+// ---------------------------------------------------------- MMA ceiling
+// The 2-SM MMA of q8_gemm_kernel (kind::f16, A in TMEM, B in shared memory in
+// the activation stage's layout, M = 256, N = BN, K = 16) issued back to back
+// by the converged leader warp, 8 a stage as in the GEMM's main loop, with no
+// loads, no waits and no epilogue: the rate this pipeline reaches when its
+// operands are always ready.  The operands' values do not matter (B zeros, A
+// whatever TMEM holds); only the time is read.
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1) mma_peak_kernel(int stages) {
+    constexpr int XBOX = BN / 2 * BOX * 2;        // one 64-wide box of this CTA's token half
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar_done = sb + 2 * XBOX;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + 2 * XBOX + 8);
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 2 * XBOX / 16; i += blockDim.x)
+        reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) {
+        mbar_init(bar_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    fence_async_smem();        // the zeros, visible to the tensor core
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    if (cluster_rank() == 0 && warp == 0) {
+        const uint32_t e = elect_one();
+        constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+        const uint64_t d0 = smem_desc_sw128(sb);
+        const uint32_t a0 = tbase + 256;          // one A stage after the accumulator (BN <= 256)
+        for (int st = 0; st < stages; ++st) {
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j)
+                mma_ts_pair_e(tbase, a0 + 8 * j, d0 + (uint64_t)(((j >> 2) * XBOX + (j & 3) * 32) >> 4), idesc,
+                              (st | j) != 0, e);
+        }
+        mma_commit_pair_e(bar_done, 0x3, e);
+    }
+    // both CTAs: the leader's MMAs, which write both CTAs' TMEM, are done
+    if (!mbar_wait(bar_done, 0) && threadIdx.x == 0) atomicExch(&g_gemm_err, 1);
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc_pair(tbase, 512);
+    }
+}
+
+int sm_count();
+
+template <int BN>
+te_status mma_peak_launch(int stages, float *ms, cudaStream_t stream) {
+    constexpr int smem = 2 * (BN / 2 * BOX * 2) + 16 + 1024;
+    const int clusters = sm_count() / 2;
+    cudaEvent_t e0, e1;
+    cudaError_t e = cudaEventCreate(&e0);
+    if (e != cudaSuccess) return cuda_fail(e, "mma_peak: event");
+    e = cudaEventCreate(&e1);
+    if (e != cudaSuccess) {
+        cudaEventDestroy(e0);
+        return cuda_fail(e, "mma_peak: event");
+    }
+    e = cudaEventRecord(e0, stream);
+    if (e == cudaSuccess) {
+        mma_peak_kernel<BN><<<2 * clusters, 128, smem, stream>>>(stages);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(e1, stream);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return e == cudaSuccess ? TE_OK : cuda_fail(e, "mma_peak");
+}
+
 // ------------------------------------------------------------------ host side
 
 int sm_count() {
@@ -1286,4 +1365,17 @@ extern "C" te_status te_q8_gated_linear(const void *x, int64_t ldx, int32_t m, i
     te_status st = part(0, m1, t1);
     if (st == TE_OK && m1 < m) st = part(m1, m - m1, tail_tile(m - m1, k, ftiles));
     return st;
+}
+
+extern "C" te_status te_mma_peak(int32_t bn, int32_t stages, float *ms, te_stream stream) {
+    if (!ms) return fail(TE_EINVAL, "mma_peak: NULL ms");
+    if (stages < 1 || stages > (1 << 22)) return fail(TE_EINVAL, "mma_peak: stages=%d (1..4194304)", stages);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (bn) {
+        case 64: return mma_peak_launch<64>(stages, ms, s);
+        case 128: return mma_peak_launch<128>(stages, ms, s);
+        case 192: return mma_peak_launch<192>(stages, ms, s);
+        case 256: return mma_peak_launch<256>(stages, ms, s);
+        default: return fail(TE_EINVAL, "mma_peak: bn=%d (64, 128, 192 or 256)", bn);
+    }
 }
