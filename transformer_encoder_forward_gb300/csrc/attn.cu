@@ -30,11 +30,10 @@
 //     once PV_w(j) has consumed it).  The running max is only moved (and O
 //     rescaled through TMEM) when it grows by more than 2^8, which keeps P in
 //     range and leaves the result unchanged: O and the row sum always share
-//     one max;
-//     The exp passes of the two tiles take turns (A(0), B(0), A(1), ...,
-//     handed over through an mbarrier pair): the exp units of an SM cannot
-//     keep up with the tensor core for both tiles at once, so each tile's exp
-//     pass runs alone while the tensor core works on the other tile;
+//     one max.  The two tiles' softmax passes run concurrently, each
+//     overlapping the other tile's MMAs (taking turns at the exp pass paid
+//     while the pass issued more instructions; with paired arithmetic it
+//     costs more than it gives);
 //   * at the end the same threads divide O by the sum and store their row.
 // Key tiles wholly outside both tiles' windows or the sequence are never
 // loaded; a masked key contributes exactly 0.  Every mbarrier wait is bounded
@@ -73,8 +72,7 @@ struct AttnParams {
     float scale_log2;
 };
 
-// TL = query tiles per CTA: 2 (tiles A and B take turns at the exp pass,
-// one CTA per SM), or 1 (hd = 64: half the TMEM and 80 KB of shared memory,
+// TL = query tiles per CTA: 2 (tiles A and B, one CTA per SM), or 1 (hd = 64: half the TMEM and 80 KB of shared memory,
 // so that two CTAs share an SM and one's loads and latencies overlap the
 // other's work - the short sequences of a text batch).  With one tile, P has
 // TMEM columns of its own (S 128 | P 64 | O 64 = 256), so S(j+1) is issued as
@@ -91,8 +89,8 @@ struct ALayout {
     static constexpr int NTHREADS = 32 * (4 * TL + 2);   // softmax warps, MMA warp, TMA warp
     static constexpr int MMA_WARP = 4 * TL, TMA_WARP = 4 * TL + 1;
     // q_full, k_full[2], v_full[2], kv_empty[2] (TL = 1: V only), s_full[2], p_full[2],
-    // pv_done[2], fin, turn[2], k_empty[2] (TL = 1), s_free (TL = 1)
-    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 2 + 2 + 1;
+    // pv_done[2], fin, k_empty[2] (TL = 1), s_free (TL = 1)
+    static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 2 + 1;
     static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
     static constexpr int S_COL = 0;                 // S_A, S_B: TL x 128 f32 columns
     static constexpr int P_COL = TL == 1 ? 128 : 0; // TL = 1: 64 columns of its own; TL = 2: over S
@@ -260,8 +258,7 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
     const uint32_t bar_pf = bar_sf + 16;           // [2] per query tile
     const uint32_t bar_pv = bar_pf + 16;           // [2] per query tile
     const uint32_t bar_fin = bar_pv + 16;
-    const uint32_t bar_turn = bar_fin + 8;         // [2] per query tile: its turn at the exp pass
-    const uint32_t bar_ke = bar_turn + 16;         // [2] TL = 1: K(j) read by S(j)
+    const uint32_t bar_ke = bar_fin + 8;           // [2] TL = 1: K(j) read by S(j)
     const uint32_t bar_sfree = bar_ke + 16;        // TL = 1: the softmax has read S(j)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBAR);
 
@@ -285,7 +282,6 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             mbar_init(bar_sf + 8 * i, 1);
             mbar_init(bar_pf + 8 * i, 4);
             mbar_init(bar_pv + 8 * i, 1);
-            mbar_init(bar_turn + 8 * i, 4);
             mbar_init(bar_ke + 8 * i, 1);
         }
         mbar_init(bar_sfree, 4);
@@ -418,8 +414,8 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
                 mma_commit_e(bar_kve + 8 * (j & 1), e);   // V(j) read
             }
         }
-        // TL = 2: issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the order in
-        // which the alternating exp passes release them.  S_w(j+1)
+        // TL = 2: issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): S_A(j) lands
+        // first, so tile A's pass usually releases P first.  S_w(j+1)
         // overwrites the P_w(j) that PV_w(j) reads (a different
         // accumulator, so not ordered by the tensor pipe): it waits for
         // PV_w(j) to complete.
@@ -475,13 +471,6 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             float mx = full ? row_max_regs<false>(v0, v1, qi, kv0, len, W)
                             : row_max_regs<true>(v0, v1, qi, kv0, len, W);
             mx *= c;                                     // c > 0: the max of the scaled row
-            // The exp pass of the two tiles alternates (A(0), B(0), A(1), ...):
-            // each tile then has the SM's exp units to itself while the tensor
-            // core runs the other tile's MMAs.
-            if (ntile == 2 && (w == 1 || j > 0)) {
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_turn + 8 * w, (w == 0 ? j - 1 : j) & 1));
-                if (!ok) break;
-            }
             if (TL == 1 && j > 0) {
                 // P and O are free once PV(j-1) is done
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv, (j - 1) & 1));
@@ -514,10 +503,7 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar_pf + 8 * w);
-                if (ntile == 2) mbar_arrive(bar_turn + 8 * (w ^ 1));   // the other tile's turn
-            }
+            if (lane == 0) mbar_arrive(bar_pf + 8 * w);
         }
         // ---- epilogue: O / l, one row per thread
         if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_pv + 8 * w, (n - 1) & 1));
