@@ -757,6 +757,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     }
                 }
             };
+            // f32 outputs where a warp's staging ring holds only one 32-token
+            // block (4 KB): 16-token halves (2 KB; the f32 maps' box is 16
+            // rows there), double-buffered, so that one half's store reads
+            // while the next half is written (a whole block would wait for
+            // its predecessor's store every time)
+            auto drain_f32_halves = [&](int acol, int t0, int cn, int fo) {
+                constexpr int HB = 2048;
+                const uint64_t sc2 = f2_pack(sc, sc), bi2 = f2_pack(bi, bi);
+                auto half_out = [&](const uint32_t (&v)[32], int h, int tb) {
+                    const bool resize = slot_bytes != HB + 1;   // HB + 1: this form's mark
+                    if (resize) {
+                        half = 0;
+                        slot_bytes = HB + 1;
+                        bulk_wait_read_n<0>();                   // every lane: other forms' stores
+                    } else if (lane == 0) {
+                        bulk_wait_read_n<1>();                   // the other half may still be read
+                    }
+                    __syncwarp();
+                    const uint32_t so = stg + (uint32_t)(half * HB);
+                    half ^= 1;
+                    float *ostg = reinterpret_cast<float *>(smem + (so - sb));
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) ostg[j * 32 + lane] = __uint_as_float(v[16 * h + j]);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (inplace)
+                            tma_reduce_add_2d(ymap, so, fo, tb);
+                        else
+                            tma_store_2d(ymap, so, fo, tb);
+                        bulk_commit();
+                    }
+                };
+                for (int c = 0; c < cn; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + tl + acol + 32 * c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        float a, b2;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sc2, bi2), a,
+                                  b2);
+                        v[j] = __float_as_uint(a);
+                        v[j + 1] = __float_as_uint(b2);
+                    }
+                    const int tb = t0 + 32 * c;
+                    half_out(v, 0, tb);
+                    if (tb + 16 < p.m) half_out(v, 1, tb + 16);
+                }
+            };
             for (int tt = 0; tt < TPA; ++tt) {
             const int acol = (TPA == 2 ? tt : b) * BN;     // this token tile's accumulator
             const int t0 = (tc.t0 * TPA + tt) * BN;
@@ -856,7 +906,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     // chunk k of the tile used ring blocks gslot + k GBSZ + i
                     gslot += (cn + GBSZ - 1) / GBSZ * GBSZ;
                 } else if (f32out || (rbase && !inplace)) {   // a residual other than y is added in f32
-                    drain_tile(std::integral_constant<int, 4096>{}, acol, t0, cn, fo);
+                    if (L::STG_WARP == 4096 && !(rbase && !inplace))
+                        drain_f32_halves(acol, t0, cn, fo);
+                    else
+                        drain_tile(std::integral_constant<int, 4096>{}, acol, t0, cn, fo);
                 } else {
                     drain_tile(std::integral_constant<int, 2048>{}, acol, t0, cn, fo);
                 }
@@ -1270,9 +1323,14 @@ extern "C" te_status te_q8_linear(const void *x, int64_t ldx, int32_t m, int32_t
             st = make_map_2d(&q.tw[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, items[i].w.q, (uint64_t)k,
                              (uint64_t)items[i].w.n, (uint64_t)k, BOX, BM, CU_TENSOR_MAP_SWIZZLE_64B);
             if (st != TE_OK) return st;
+            // f32 outputs without a separate residual go out in 16-token halves
+            // where a warp's staging holds one 32-token f32 block (every tile
+            // but the one-tile units at N <= 128): the kernel's own condition
+            const bool halves = f32 && !(t.tpa == 1 && t.bn <= 128) &&
+                                !(items[i].residual && items[i].residual != items[i].y);
             st = make_map_2d(&q.ty[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                              d.y, (uint64_t)items[i].w.n, (uint64_t)mr, (uint64_t)items[i].ldy * (f32 ? 4 : 2), 32,
-                             32, CU_TENSOR_MAP_SWIZZLE_NONE);
+                             halves ? 16 : 32, CU_TENSOR_MAP_SWIZZLE_NONE);
             if (st != TE_OK) return st;
         }
         if (t.bn == 192) return t.tpa == 2 ? launch<192, false, 2>(q, ftiles, s) : launch<192, false, 1>(q, ftiles, s);
