@@ -263,3 +263,31 @@ def test_forward_host_graph_replay_equals_the_device_forward():
         te.check()
         assert torch.equal(res, ref)
     assert len(st._graphs) == 1
+
+
+def test_forward_host_stream_overlapped_copies_give_each_input_its_own_result():
+    # five inputs in sequence through the overlapped path (two buffer sets,
+    # copies on their own streams): each result equals the device forward of
+    # that input bit for bit, for a pooled and an unpooled stack
+    import torch
+    for key, lens in (("c2", (100, 300, 37)), ("c3", (64, 130))):
+        cfg = synth.small_config(key, layers=2, lens=lens)
+        st, _, _ = _stack(cfg, cfg.lens, 2)
+        xs = [synth.draw_x(st.T, cfg.d, 20 + i) for i in range(5)]
+        refs = []
+        for x0 in xs:
+            x, a, out = st.buffers()
+            x.copy_(to_dev(x0))
+            st.forward_device(x, a, out)
+            torch.cuda.synchronize()
+            refs.append((out if cfg.pool else x).cpu())
+        hosts = [torch.from_numpy(np.ascontiguousarray(x0)).pin_memory() for x0 in xs]
+        shape = (len(cfg.lens), cfg.d) if cfg.pool else (st.T, cfg.d)
+        res = [torch.full(shape, float("nan"), dtype=torch.float32).pin_memory() for _ in xs]
+        s = torch.cuda.Stream()
+        start, end = st.forward_host_stream(hosts, res, stream=s)
+        end.synchronize()
+        te.check()
+        for i in range(len(xs)):
+            assert torch.equal(res[i], refs[i]), (key, i)
+        assert start.elapsed_time(end) > 0

@@ -174,6 +174,71 @@ class EncoderStack:
             pool_mean(x, self.cu_host, self.cu_dev, self.final_norm, self.cfg.eps, out,
                       stream=stream)
 
+    def forward_host_stream(self, x_hosts, result_hosts, stream=None, before=None):
+        """End to end for a sequence of inputs, the copies overlapped with the
+        neighbouring forwards: forward i copies x_hosts[i] (pinned) in on a
+        copy stream while forward i-1 computes, and its result (the pooled
+        rows, else x) out to result_hosts[i] (pinned) on another while forward
+        i+1 computes.  Two device buffer sets alternate; the forwards run in
+        order on `stream` (the current stream when None) and share the
+        workspace.  Each set's forward is replayed from a CUDA graph captured
+        by forward_host on its first use (that call runs eagerly).  `before`,
+        if given, is called on the compute stream ahead of each forward (the
+        bench flushes L2 there).  Returns the events (start, end) that
+        bracket the whole sequence; wait on `end` before reading results."""
+        import torch
+        n = len(x_hosts)
+        if n != len(result_hosts):
+            raise ValueError("forward_host_stream: as many result buffers as inputs")
+        comp = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if getattr(self, "_pipe", None) is None:
+            # two buffer sets, two copy streams and their graphs (captured
+            # through forward_host on the compute stream)
+            sets = [self.buffers() for _ in range(2)]
+            cin = torch.cuda.Stream(device=self.device)
+            cout = torch.cuda.Stream(device=self.device)
+            self._pipe = (sets, cin, cout)
+        sets, cin, cout = self._pipe
+        for b in range(2):
+            x, a, out = sets[b]
+            if (x.data_ptr(), a.data_ptr(), out.data_ptr(), comp.cuda_stream) not in self.__dict__.get("_graphs", {}):
+                tmp = torch.empty_like(result_hosts[0], device="cpu").pin_memory()
+                self.forward_host(x_hosts[0], tmp, x, a, out, stream=comp)
+                comp.synchronize()
+        graphs = self._graphs
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+        in_done = [ev(), ev()]
+        comp_done = [ev(), ev()]
+        out_done = [None, None]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(comp)
+        cin.wait_stream(comp)
+        for i in range(n):
+            b = i & 1
+            x, a, out = sets[b]
+            src = out if self.cfg.pool else x
+            # copy in once the result of the forward two back has left x
+            if out_done[b] is not None:
+                cin.wait_event(out_done[b])
+            with torch.cuda.stream(cin):
+                x.copy_(x_hosts[i], non_blocking=True)
+            in_done[b].record(cin)
+            comp.wait_event(in_done[b])
+            with torch.cuda.stream(comp):
+                if before is not None:
+                    before()
+                graphs[(x.data_ptr(), a.data_ptr(), out.data_ptr(), comp.cuda_stream)].replay()
+            comp_done[b].record(comp)
+            cout.wait_event(comp_done[b])
+            with torch.cuda.stream(cout):
+                result_hosts[i].copy_(src, non_blocking=True)
+            out_done[b] = ev()
+            out_done[b].record(cout)
+        comp.wait_stream(cout)
+        end.record(comp)
+        return start, end
+
     def forward_host(self, x_host, result_host, x=None, a=None, out=None, stream=None, graph=True):
         """End to end from pinned host memory: copies the input rows in, runs
         the stack and copies the result (the pooled rows, else x) back, all on
