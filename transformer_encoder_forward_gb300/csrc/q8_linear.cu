@@ -135,7 +135,12 @@ struct Layout {
     static constexpr int STG_OFF = COL_OFF + NST * COL_BYTES;
     static constexpr int STG_WARP = TPA == 1 && BN <= 128 ? 8192 : 4096;
     static constexpr int STG_BYTES = 4 * STG_WARP;
-    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+    // one-tile units at N = 128: 4 KB a warp for four converter warps that
+    // help drain the gated form while the weights are resident
+    static constexpr bool HELP = TPA == 1 && BN == 128;
+    static constexpr int HSTG_OFF = STG_OFF + STG_BYTES;
+    static constexpr int HSTG_BYTES = HELP ? 4 * 4096 : 0;
+    static constexpr int BAR_OFF = HSTG_OFF + HSTG_BYTES;
     // barriers: full, empty [NST]; afull, aempty [NA]; accfull, accempty [2]; done
     static constexpr int NBAR = 2 * NST + 2 * NA + 4 + 1;
     static constexpr int BYTES = BAR_OFF + 8 * NBAR + 16;
@@ -297,6 +302,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const bool leader = rank == 0;
     const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
     const bool res = p.res != 0;
+    // The gated form with resident weights at N = 128 is drained by the four
+    // epilogue warps (blocks 0-1 of each token tile) and by converter warps
+    // 2-5 (blocks 2-3), idle otherwise once the run's weights are widened:
+    // one warp's drain of a unit outlasts the unit's MMAs, and each warp's
+    // drain is bound by its own instruction latencies, so two warps a lane
+    // quadrant halve it.
+    const bool helpers = GATED && L::HELP && res;
     // once any CTA has given up a wait, the rest skip their work (the call
     // has failed; te_check reports it) instead of timing out one by one
     __shared__ int s_skip;
@@ -313,7 +325,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_accfull + 8 * b, 1);
-            mbar_init(bar_accempty + 8 * b, 8);   // every epilogue warp of both CTAs (leader's copy)
+            // every draining warp of both CTAs (leader's copy): the epilogue
+            // warps, and with helpers four converter warps too
+            mbar_init(bar_accempty + 8 * b, helpers ? 16 : 8);
         }
         mbar_init(bar_done, 1);
         fence_mbar_init();
@@ -340,6 +354,92 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // weights, else at the run's start and where the feature pair changes
     auto fills = [&](int i) {
         return !res || i == 0 || unit_at(i) / p.ttiles != unit_at(i - 1) / p.ttiles;
+    };
+    // With helpers: the drain of unit lt's accumulator (one token tile), blocks
+    // [cb, ce), by the calling warp (lane quadrant warp & 3), in chunks of two
+    // blocks through its own 4-block ring at shared address hstg (gslot: the
+    // ring position); lane i stores block i of a chunk and commits its own
+    // bulk group.  The arithmetic is the epilogue's gated form (see there).
+    auto gated_drain = [&](int lt, int cb, int ce, uint32_t hstg, int &gslot) -> bool {
+        const int q = warp & 3;
+        const bool upper = lane & 16;
+        const int frow = 16 * q + (lane & 15);
+        const uint32_t tl = (uint32_t)(32 * q) << 16;
+        const int u = unit_at(lt);
+        const int b = lt & 1;
+        const uint32_t ph = (lt >> 1) & 1;
+        const TileCoord tc = tile_coord<GATED>(p, u, rank);
+        const int o = tc.o0 + frow;
+        const bool ov = o < p.it[tc.zi].n;
+        const float *scale = upper ? p.it[tc.zi].scale2 : p.it[tc.zi].scale;
+        const float *bias = upper ? p.it[tc.zi].bias2 : p.it[tc.zi].bias;
+        const float sc = ov ? (scale ? scale[o] : 1.f) : 0.f;
+        const float bi = (ov && bias) ? bias[o] : 0.f;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_accfull + 8 * b, ph))) return false;
+        tc_fence_after();
+        const int act = p.it[tc.zi].act;
+        const int n = p.it[tc.zi].n;
+        const void *ymap = &p.ty[tc.zi];
+        const int acol = b * BN;
+        const int t0 = tc.t0 * BN;
+        const int cn = t0 >= p.m ? 0 : ((p.m - t0 + 31) / 32 < BN / 32 ? (p.m - t0 + 31) / 32 : BN / 32);
+        const int cend = ce < cn ? ce : cn;
+        const int fo = tc.o0 + 16 * q;
+        const int jb = upper ? 16 : 0;
+        const uint64_t sc2 = f2_pack(sc, sc), bi2 = f2_pack(bi, bi), half2 = f2_pack(0.5f, 0.5f);
+        for (int c0 = cb; c0 < cend && fo < n; c0 += 2) {
+            const int ceb = c0 + 2 < cend ? c0 + 2 : cend;
+            if (lane < 2) bulk_wait_read_n<1>();
+            __syncwarp();
+            for (int c = c0; c < ceb; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tbase + tl + acol + 32 * c, v);
+                tmem_wait_ld();
+                float gv[16], uv[16], yv[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float lo, hi;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[16 + j])), sc2, bi2), lo, hi);
+                    const uint32_t b2 = pack_bf16x2(lo, hi);
+                    lo = bf16_lo(b2);
+                    hi = bf16_hi(b2);
+                    const float got = __shfl_xor_sync(0xFFFFFFFFu, upper ? lo : hi, 16);
+                    gv[j] = upper ? got : lo;
+                    uv[j] = upper ? hi : got;
+                }
+                const bool gelu = act == TE_ACT_GELU_TANH;
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    const uint64_t g2 = f2_pack(gv[j], gv[j + 1]);
+                    const uint64_t z2 = gelu ? f2_mul(g2, f2_fma(f2_pack(0.035677408f, 0.035677408f), f2_mul(g2, g2),
+                                                                 f2_pack(0.79788456f, 0.79788456f)))
+                                             : f2_mul(half2, g2);
+                    float z0, z1;
+                    f2_unpack(z2, z0, z1);
+                    const uint64_t h2 = f2_mul(half2, g2);
+                    const uint64_t a2 = f2_fma(h2, f2_pack(hw_tanh(z0), hw_tanh(z1)), h2);
+                    f2_unpack(f2_mul(a2, f2_pack(uv[j], uv[j + 1])), yv[j], yv[j + 1]);
+                }
+                const uint32_t so = hstg + (uint32_t)(((gslot + c - c0) & 3) * 1024);
+                uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    ostg_h[(jb + j) * 16 + (lane & 15)] = __bfloat16_as_ushort(__float2bfloat16_rn(yv[j]));
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane < 2) {
+                const int c = c0 + lane;
+                if (c < ceb) tma_store_2d(ymap, hstg + (uint32_t)(((gslot + lane) & 3) * 1024), fo, t0 + 32 * c);
+                bulk_commit();
+            }
+            gslot += 2;
+        }
+        // this accumulator may take the next tile's MMAs
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(accempty_ldr + 8 * b);
+        return true;
     };
 
     if (warp == 0) {
@@ -518,8 +618,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const int frow = GATED ? 16 * q + (lane & 15) : row;    // feature offset in the tile
         const uint32_t tl = (uint32_t)(32 * q) << 16;
         int kbg = 0, nfill = 0;
+        const bool helper = helpers && h == 0;         // warps 2-5 also drain (see gated_drain)
+        const uint32_t hstg = sb + L::HSTG_OFF + (uint32_t)((warp - 2) & 3) * 4096u;
+        int hslot = 0;
         for (int i = 0; i < ucnt && ok; ++i) {
-            if (!fills(i)) { kbg += nkb; continue; }   // resident weights: nothing to widen
+            if (!fills(i)) {                            // resident weights: nothing to widen
+                kbg += nkb;
+                if (helper) ok = gated_drain(i, 2, 4, hstg, hslot);
+                continue;
+            }
             const int u = unit_at(i);
             // the 32-element block formats: this row's f16 block scales (the
             // item is uniform over the warp: a warp's 32 rows share it)
@@ -602,6 +709,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 if (lane == 0) mbar_arrive_cluster_relaxed(afull_ldr + 8 * a);
             }
             ++nfill;
+            if (helper && ok) ok = gated_drain(i, 2, 4, hstg, hslot);
+        }
+        if (helper) {
+            // the stores must be complete before the CTA's shared memory goes away
+            bulk_wait_all();
+            __syncwarp();
         }
     } else {
         // ----------------------------------------------------------- epilogue
@@ -630,6 +743,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         int half = 0, slot_bytes = 0;   // the next chunk's half, the ring's block size
         // gated: the ring position (blocks so far)
         int gslot = 0;
+        if (helpers) {
+            // blocks 0-1 of each token tile here, 2-3 by converter warps 2-5
+            int hs = 0;
+            for (; lt < ucnt && ok; ++lt) ok = gated_drain(lt, 0, 2, stg, hs);
+        }
         for (; lt < ucnt && ok; ++lt) {
             const int u = unit_at(lt);
             const int b = TPA == 2 ? 0 : (lt & 1);
