@@ -273,7 +273,21 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
     const int n = (khi + BKV - 1) / BKV - kt0;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
+    // 128 joint positions from j0 at column col: one box, or four 32-row
+    // boxes when the tile spans the two ranges (len1 % 32 == 0); issued by
+    // the lane whose e is set
+    auto load_tile = [&](uint32_t dst, int col, int j0, uint32_t bar, uint32_t e) {
+        if (len2 == 0 || j0 + BQ <= len1 || j0 >= len1) {
+            tma_load_2d_e(dst, &p.map, bar, col, row_of(j0), e);
+        } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                tma_load_2d_e(dst + r * 32 * 128, &p.map32, bar, col, row_of(j0 + 32 * r), e);
+        }
+    };
+    // The TMA warp initialises the barriers and starts the Q load at once:
+    // its latency then overlaps the TMEM allocation and the block's sync.
+    if (warp == L::TMA_WARP && lane == 0) {
         mbar_init(bar_q, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_kf + 8 * i, 1);
@@ -287,6 +301,10 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
         mbar_init(bar_sfree, 4);
         mbar_init(bar_fin, 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(bar_q, ntile * L::TILE);
+        for (int w = 0; w < ntile; ++w)
+            for (int c = 0; c < L::NB; ++c)
+                load_tile(sb + L::Q_OFF + w * L::TILE + c * 16384, p.q_off + h * HD + 64 * c, q0 + w * BQ, bar_q, 1u);
     }
     if (warp == L::MMA_WARP) tmem_alloc(smem_u32(tmem_slot), L::COLS);
     tc_fence_before();
@@ -300,21 +318,6 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
         // (the whole warp in step, one elected lane issues)
         const uint32_t e = elect_one();
         if (e) tma_prefetch_desc(&p.map);
-        // 128 joint positions from j0 at column col: one box, or four
-        // 32-row boxes when the tile spans the two ranges (len1 % 32 == 0)
-        auto load_tile = [&](uint32_t dst, int col, int j0, uint32_t bar) {
-            if (len2 == 0 || j0 + BQ <= len1 || j0 >= len1) {
-                tma_load_2d_e(dst, &p.map, bar, col, row_of(j0), e);
-            } else {
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    tma_load_2d_e(dst + r * 32 * 128, &p.map32, bar, col, row_of(j0 + 32 * r), e);
-            }
-        };
-        mbar_arrive_expect_tx_e(bar_q, ntile * L::TILE, e);
-        for (int w = 0; w < ntile; ++w)
-            for (int c = 0; c < L::NB; ++c)
-                load_tile(sb + L::Q_OFF + w * L::TILE + c * 16384, p.q_off + h * HD + 64 * c, q0 + w * BQ, bar_q);
         // K(i) into ring slot i & 1 once its previous occupant K(i - 2) is
         // free (TL = 1: read by S(i - 2); TL = 2: K and V free together after
         // PV(i - 2)); V(i) once PV(i - 2) is done
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             mbar_arrive_expect_tx_e(bar_kf + 8 * st, L::TILE, e);
             for (int c = 0; c < L::NB; ++c)
                 load_tile(sb + L::K_OFF + st * L::TILE + c * 16384, p.k_off + g * HD + 64 * c, (kt0 + i) * BKV,
-                          bar_kf + 8 * st);
+                          bar_kf + 8 * st, e);
             return true;
         };
         auto load_v = [&](int i) -> bool {
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(ALayout<HD, TL>::NTHREADS, TL == 1 ? 2 : 1)
             mbar_arrive_expect_tx_e(bar_vf + 8 * st, L::TILE, e);
             for (int c = 0; c < L::NB; ++c)
                 load_tile(sb + L::V_OFF + st * L::TILE + c * 16384, p.v_off + g * HD + 64 * c, (kt0 + i) * BKV,
-                          bar_vf + 8 * st);
+                          bar_vf + 8 * st, e);
             return true;
         };
         int nk = 0, nv = 0;   // K and V tiles issued
