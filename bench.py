@@ -208,7 +208,7 @@ def rank_lens(key, world, rank):
 # --------------------------------------------------------------- GPU timing
 
 OP_SOURCE = {"gemm": "q8_linear.cu", "attn": "attn.cu", "qk_prep": "rowops.cu",
-             "add_norm": "rowops.cu"}
+             "add_norm": "rowops.cu", "rownorm": "rowops.cu"}
 
 
 def workload_ops(cfg, st, torch):
@@ -276,11 +276,17 @@ def workload_ops(cfg, st, torch):
         ops["add_norm"] = (lambda s: te.add_norm_mod(x, tmp, L0.t["post_attn_w"], md[1], 1.0, L0.t["norm2_w"],
                                                      None, md[2], te.TE_NORM_RMS, cfg.eps, a, stream=s),
                            0, T * d * (4 * 3 + 2), 2 * nl, "hbm")
-    else:
-        ops["add_norm"] = (lambda s: te.add_norm(x, tmp, L0.t["post_attn_w"] if cfg.form == "sandwich" else None,
-                                                 1.0, L0.t["norm2_w"], L0.t["norm2_b"],
+    elif cfg.form == "sandwich":
+        ops["add_norm"] = (lambda s: te.add_norm(x, tmp, L0.t["post_attn_w"], 1.0, L0.t["norm2_w"], L0.t["norm2_b"],
                                                  te.TE_NORM_LN if cfg.norm == "ln" else te.TE_NORM_RMS, cfg.eps,
                                                  a, stream=s), 0, T * d * (4 * 3 + 2), 2 * nl, "hbm")
+    else:
+        # the plain form adds each projection into x in its GEMM's epilogue;
+        # its row op is the norm of x into the next GEMM's bf16 input (the
+        # FFN norm and the next block's norm, or the stack's input norm)
+        ops["rownorm"] = (lambda s: te.rownorm(x, L0.t["norm2_w"], L0.t["norm2_b"],
+                                               te.TE_NORM_LN if cfg.norm == "ln" else te.TE_NORM_RMS, cfg.eps,
+                                               a, stream=s), 0, T * d * (4 + 2), 2 * nl, "hbm")
     return ops
 
 
@@ -363,6 +369,8 @@ def run_op(args):
     te.lib()
     cfg, lens, st, _, _ = build_stack(args.config, dev, layers=1)
     ops = workload_ops(cfg, st, torch)
+    if args.op not in ops:
+        raise SystemExit(f"--op {args.op}: not an op of {cfg.name}'s forward (ops: {', '.join(sorted(ops))})")
     fn, flops, nbytes, count, bound = ops[args.op]
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -675,7 +683,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--op", default=None,
                     help="time one op of the workload alone (gemm_qkv, gemm_o, gemm_gu (gate fused), "
-                         "gemm_down, attn_w<window>, qk_prep, add_norm) instead of the forward; "
+                         "gemm_down, attn_w<window>, qk_prep, add_norm or rownorm) instead of the forward; "
                          "mma_peak: the GEMM's MMA form without loads, its tensor ceiling")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

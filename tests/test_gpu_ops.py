@@ -381,7 +381,9 @@ def test_rownorm_matches_oracle(d, kind, xdt):
 @pytest.mark.parametrize("d,sandwich,nxt,kind", [(512, True, True, "rms"), (3840, True, False, "rms"),
                                                  (768, False, True, "ln"), (256, False, False, "rms"),
                                                  (3840, True, True, "rms"), (2048, False, True, "ln"),
-                                                 (4096, True, True, "ln"), (1032, True, True, "rms")])
+                                                 (4096, True, True, "ln"), (1032, True, True, "rms"),
+                                                 (1024, True, True, "rms"), (520, False, True, "ln"),
+                                                 (1024, False, False, "ln")])
 def test_add_norm_matches_oracle(d, sandwich, nxt, kind):
     torch = _torch()
     rng = np.random.default_rng([d, int(sandwich), int(nxt)])
@@ -405,7 +407,8 @@ def test_add_norm_matches_oracle(d, sandwich, nxt, kind):
 
 
 @pytest.mark.parametrize("d,sandwich,kind", [(512, True, "rms"), (3840, True, "rms"),
-                                            (768, False, "ln"), (2048, False, "rms")])
+                                            (768, False, "ln"), (2048, False, "rms"),
+                                            (1024, True, "rms")])
 def test_add_norm_with_adaln_gate_and_scale_matches_oracle(d, sandwich, kind):
     torch = _torch()
     rng = np.random.default_rng([d, 77, int(sandwich)])
@@ -436,11 +439,13 @@ def test_add_norm_with_adaln_gate_and_scale_matches_oracle(d, sandwich, kind):
     assert rel_frob(to_np(y), y_ref) < 2e-3
 
 
-def test_adaln_identity_vectors_are_bit_exact_no_ops():
-    # s = 0 and g = 1 must give exactly the unmodulated row ops
+@pytest.mark.parametrize("d", [256, 768, 3840])
+def test_adaln_identity_vectors_are_bit_exact_no_ops(d):
+    # s = 0 and g = 1 must give exactly the unmodulated row ops (one width of
+    # each add_norm layout: a warp, four warps and eight warps a row)
     torch = _torch()
-    rng = np.random.default_rng(91)
-    rows, d = 99, 3840
+    rng = np.random.default_rng([91, d])
+    rows = 99
     h = to_dev(rng.standard_normal((rows, d)).astype(np.float32))
     t = to_dev(rng.standard_normal((rows, d)).astype(np.float32))
     wp, _ = synth.draw_norm(rng, d, False)

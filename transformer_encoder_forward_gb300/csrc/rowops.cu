@@ -235,7 +235,8 @@ __global__ void __launch_bounds__(256) add_norm_kernel(float *h, const float *__
                              MOD ? ms : nullptr, a + (long long)row * d);
 }
 
-// Wide rows (d > 1024): WPR warps per row (8: one row per 256-thread CTA).
+// Wide rows: WPR warps per row (d > 1024: 8, one row per 256-thread CTA;
+// 512 < d <= 1024: 4, two rows a CTA, one 8-column chunk a thread).
 // Each thread holds at most NV 8-column chunks of t and of h, all loaded up
 // front (more bytes in flight per SM than one warp per row allows); the row
 // reductions go through shared memory.  Eight warps a row (2 chunks a thread,
@@ -247,7 +248,8 @@ __device__ __forceinline__ float row4_sum(float x, float (*red)[WPR], int slot, 
     x = warp_sum(x);
     if (lane == 0) red[slot][wr] = x;
     __syncthreads();
-    float s = (red[slot][0] + red[slot][1]) + (red[slot][2] + red[slot][3]);
+    float s = red[slot][0] + red[slot][1];
+    if (WPR >= 4) s += red[slot][2] + red[slot][3];
     if (WPR == 8) s += (red[slot][4] + red[slot][5]) + (red[slot][6] + red[slot][7]);
     __syncthreads();
     return s;
@@ -697,6 +699,30 @@ te_status te_add_norm_mod(float *h, const float *t, const float *w_post, const f
     // the adaLN loads only in their own instantiation: the unmodulated kernel
     // keeps its registers (and occupancy)
     const bool mod = gate || ms;
+    if (d > 512 && d <= 1024) {
+        // four warps a row, one 8-column chunk a thread: at d = 768 this beats
+        // the one-warp-a-row kernel (more loads in flight a row); at d <= 512
+        // the one-warp kernel stays ahead, so narrow rows keep it.  Both
+        // forms take the same kernel, so identity adaLN vectors stay a no-op
+        // to the bit.
+        const dim3 g2((rows + 1) / 2);
+        if (adt == TE_F32) {
+            if (mod)
+                add_norm_wide_kernel<float, 1, true, 4><<<g2, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (float *)a, rows, d);
+            else
+                add_norm_wide_kernel<float, 1, false, 4><<<g2, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (float *)a, rows, d);
+        } else {
+            if (mod)
+                add_norm_wide_kernel<__nv_bfloat16, 1, true, 4><<<g2, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (__nv_bfloat16 *)a, rows, d);
+            else
+                add_norm_wide_kernel<__nv_bfloat16, 1, false, 4><<<g2, 256, 0, stream>>>(
+                    h, t, w_post, gate, post, w_next, b_next, ms, kind, eps, (__nv_bfloat16 *)a, rows, d);
+        }
+        return launched("add_norm launch");
+    }
     if (d > 1024) {
         // eight warps per row (d <= 4096: at most 2 chunks of 8 per thread)
         const dim3 grid2(rows);
