@@ -68,6 +68,9 @@ GEMM_CASES = [
     (8448, 3840, [3840], False, True, "f32"),
     # a split with a separate residual and a bf16 output
     (2111, 2048, [3840], True, "sep", "bf16"),
+    # two 192-token tiles a unit at long K, bf16 out: the second tile partly
+    # drained by converter warps (whole waves, then a second launch)
+    (6000, 3072, [768, 768, 768], True, False, "bf16"),
     # resident weights over long runs of token tiles that cross feature pairs
     (5000, 512, [512, 512, 512], False, False, "bf16"),
     (5000, 512, [512], True, True, "f32"),
@@ -205,19 +208,28 @@ def test_gated_linear_matches_oracle(m, k, f, act, bias):
     assert rel_frob(got, ref) < 2e-3, rel_frob(got, ref)
 
 
-@pytest.mark.parametrize("m,k,n,act", [(4096, 768, 3072, "gelu_tanh"), (77, 256, 96, "silu")])
-def test_q8_linear_epilogue_activation_matches_oracle(m, k, n, act):
+@pytest.mark.parametrize("m,k,n,act,ydt", [(4096, 768, 3072, "gelu_tanh", "bf16"), (77, 256, 96, "silu", "bf16"),
+                                            # f32 out: 16-token halves (192-token tiles), and
+                                            # two tiles a unit at long K
+                                            (4096, 768, 512, "gelu_tanh", "f32"),
+                                            (6000, 3072, 768, "silu", "f32"),
+                                            (6000, 3072, 768, "gelu_tanh", "bf16")])
+def test_q8_linear_epilogue_activation_matches_oracle(m, k, n, act, ydt):
+    # y = act(bf16(s * acc + b)), stored as y's type
     torch = _torch()
     rng = np.random.default_rng([m, n])
     x, x64 = bf16_input(rng, (m, k))
     w = synth.draw_q8(rng, n, k, True, True)
     dw = q8_dev(w)
-    y = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dt = torch.float32 if ydt == "f32" else torch.bfloat16
+    y = torch.full((m, n), float("nan"), dtype=dt, device="cuda")
     te.q8_linear(x, [{"w": te.q8w(*dw), "y": y, "ldy": n,
                       "epilogue": te.TE_EPI_SILU if act == "silu" else te.TE_EPI_GELU_TANH}])
     te.check()
     pre = O.round_bf16(O.q8_linear(x64, w["q"], w["s"], w["b"]))
-    ref = O.round_bf16(O.gate_act(pre, n, False, act))
+    ref = O.gate_act(pre, n, False, act)
+    if ydt == "bf16":
+        ref = O.round_bf16(ref)
     assert rel_frob(to_np(y), ref) < 2e-3
 
 

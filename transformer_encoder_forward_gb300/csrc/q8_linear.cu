@@ -138,8 +138,12 @@ struct Layout {
     // one-tile units at N = 128: 4 KB a warp for four converter warps that
     // help drain the gated form while the weights are resident
     static constexpr bool HELP = TPA == 1 && BN == 128;
+    // two-tile units: converter warps 2-5 drain the later blocks of the
+    // second token tile while the epilogue warps drain the first (one 2 KB
+    // slot a warp: a bf16 block, two gated blocks, or an f32 16-token half)
+    static constexpr bool HELP2 = TPA == 2;
     static constexpr int HSTG_OFF = STG_OFF + STG_BYTES;
-    static constexpr int HSTG_BYTES = HELP ? 4 * 4096 : 0;
+    static constexpr int HSTG_BYTES = HELP ? 4 * 4096 : (HELP2 ? 4 * 2048 : 0);
     static constexpr int BAR_OFF = HSTG_OFF + HSTG_BYTES;
     // barriers: full, empty [NST]; afull, aempty [NA]; accfull, accempty [2]; done
     static constexpr int NBAR = 2 * NST + 2 * NA + 4 + 1;
@@ -326,8 +330,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_accfull + 8 * b, 1);
             // every draining warp of both CTAs (leader's copy): the epilogue
-            // warps, and with helpers four converter warps too
-            mbar_init(bar_accempty + 8 * b, helpers ? 16 : 8);
+            // warps, and four converter warps too with helpers (for a
+            // two-tile unit's second tile, converter warps 2-5)
+            mbar_init(bar_accempty + 8 * b, helpers || (L::HELP2 && b == 1) ? 16 : 8);
         }
         mbar_init(bar_done, 1);
         fence_mbar_init();
@@ -439,6 +444,151 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(accempty_ldr + 8 * b);
+        return true;
+    };
+
+    // Two-tile units: the blocks of the second token tile that the epilogue
+    // warps drain themselves; converter warps 2-5 take the rest (none where a
+    // residual other than y is added from global memory).  The epilogue warps
+    // start at the accumulator's completion while the converters first widen
+    // the next unit's leading stages, so the epilogue keeps one block.
+    auto e_blocks2 = [&](int zi, int cn) -> int {
+        const bool other_resid = p.it[zi].resid != nullptr && p.it[zi].resid != p.it[zi].y;
+        return other_resid || cn < 1 ? cn : 1;
+    };
+    // Two-tile units: the calling converter warp (lane quadrant warp & 3)
+    // drains blocks [e_blocks2, cn) of unit lt's second token tile through
+    // its own 2 KB slot at shared address hstg, with the epilogue's
+    // arithmetic for the item's output form, then releases that accumulator
+    // together with the epilogue warps.  Lane 0 issues the stores, one bulk
+    // group each; hslot counts the gated blocks (two 1 KB slots).
+    auto help2_drain = [&](int lt, uint32_t hstg, int &hslot) -> bool {
+        const int q = warp & 3;
+        const bool upper = GATED && (lane & 16);
+        const int frow = GATED ? 16 * q + (lane & 15) : 32 * q + lane;
+        const uint32_t tl = (uint32_t)(32 * q) << 16;
+        const TileCoord tc = tile_coord<GATED>(p, unit_at(lt), rank);
+        const Item &it = p.it[tc.zi];
+        const int o = tc.o0 + frow;
+        const bool ov = o < it.n;
+        const float *scale = upper ? it.scale2 : it.scale;
+        const float *bias = upper ? it.bias2 : it.bias;
+        const float sc = ov ? (scale ? scale[o] : 1.f) : 0.f;
+        const float bi = (ov && bias) ? bias[o] : 0.f;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_accfull, lt & 1))) return false;
+        tc_fence_after();
+        const int t0 = (tc.t0 * 2 + 1) * BN;
+        const int cn = t0 >= p.m ? 0 : ((p.m - t0 + 31) / 32 < BN / 32 ? (p.m - t0 + 31) / 32 : BN / 32);
+        const int fo = tc.o0 + (GATED ? 16 : 32) * q;
+        const void *ymap = &p.ty[tc.zi];
+        const bool f32out = it.ydt == TE_F32;
+        const bool inplace = it.resid != nullptr && it.resid == it.y;
+        const uint64_t sc2 = f2_pack(sc, sc), bi2 = f2_pack(bi, bi);
+        for (int c = e_blocks2(tc.zi, cn); c < cn && fo < it.n; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + tl + BN + 32 * c, v);
+            tmem_wait_ld();
+            const int tb = t0 + 32 * c;
+            if constexpr (GATED) {
+                // the epilogue's gated form: scale and bias, both halves
+                // rounded to bf16, gate and up lanes swap half their tokens,
+                // m = act(g) * u in f32 pairs
+                const uint64_t half2 = f2_pack(0.5f, 0.5f);
+                float gv[16], uv[16], yv[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float lo, hi;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[16 + j])), sc2, bi2), lo, hi);
+                    const uint32_t b2 = pack_bf16x2(lo, hi);
+                    lo = bf16_lo(b2);
+                    hi = bf16_hi(b2);
+                    const float got = __shfl_xor_sync(0xFFFFFFFFu, upper ? lo : hi, 16);
+                    gv[j] = upper ? got : lo;
+                    uv[j] = upper ? hi : got;
+                }
+                const bool gelu = it.act == TE_ACT_GELU_TANH;
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    const uint64_t g2 = f2_pack(gv[j], gv[j + 1]);
+                    const uint64_t z2 = gelu ? f2_mul(g2, f2_fma(f2_pack(0.035677408f, 0.035677408f), f2_mul(g2, g2),
+                                                                 f2_pack(0.79788456f, 0.79788456f)))
+                                             : f2_mul(half2, g2);
+                    float z0, z1;
+                    f2_unpack(z2, z0, z1);
+                    const uint64_t h2 = f2_mul(half2, g2);
+                    const uint64_t a2 = f2_fma(h2, f2_pack(hw_tanh(z0), hw_tanh(z1)), h2);
+                    f2_unpack(f2_mul(a2, f2_pack(uv[j], uv[j + 1])), yv[j], yv[j + 1]);
+                }
+                // the store two blocks back, which used this slot, has read it
+                if (lane == 0) bulk_wait_read_n<1>();
+                __syncwarp();
+                const uint32_t so = hstg + (uint32_t)((hslot & 1) * 1024);
+                uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (so - sb));
+                const int jb = upper ? 16 : 0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    ostg_h[(jb + j) * 16 + (lane & 15)] = __bfloat16_as_ushort(__float2bfloat16_rn(yv[j]));
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(ymap, so, fo, tb);
+                    bulk_commit();
+                }
+                ++hslot;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    float a, b2;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sc2, bi2), a, b2);
+                    v[j] = __float_as_uint(a);
+                    v[j + 1] = __float_as_uint(b2);
+                }
+                if (it.act) {   // the ungated MLP: act(bf16(s*acc + b))
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __float_as_uint(apply_act_tanh(round_bf16(__uint_as_float(v[j])), it.act - 1));
+                }
+                if (f32out) {
+                    // 16-token halves (the two-tile units' f32 maps have
+                    // 16-row boxes), each after the previous has been read
+                    float *ostg = reinterpret_cast<float *>(smem + (hstg - sb));
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh == 1 && tb + 16 >= p.m) break;       // warp-uniform
+                        if (lane == 0) bulk_wait_read_n<0>();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) ostg[j * 32 + lane] = __uint_as_float(v[16 * hh + j]);
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (inplace)
+                                tma_reduce_add_2d(ymap, hstg, fo, tb + 16 * hh);
+                            else
+                                tma_store_2d(ymap, hstg, fo, tb + 16 * hh);
+                            bulk_commit();
+                        }
+                    }
+                } else {
+                    if (lane == 0) bulk_wait_read_n<0>();
+                    __syncwarp();
+                    uint16_t *ostg_h = reinterpret_cast<uint16_t *>(smem + (hstg - sb));
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        ostg_h[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(ymap, hstg, fo, tb);
+                        bulk_commit();
+                    }
+                }
+            }
+        }
+        // the second tile's accumulator may take the next unit's MMAs
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(accempty_ldr + 8);
         return true;
     };
 
@@ -621,6 +771,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const bool helper = helpers && h == 0;         // warps 2-5 also drain (see gated_drain)
         const uint32_t hstg = sb + L::HSTG_OFF + (uint32_t)((warp - 2) & 3) * 4096u;
         int hslot = 0;
+        // two-tile units: warps 2-5 drain part of each unit's second tile (see help2_drain)
+        const bool helper2 = L::HELP2 && h == 0;
+        const uint32_t hstg2 = sb + L::HSTG_OFF + (uint32_t)((warp - 2) & 3) * 2048u;
         for (int i = 0; i < ucnt && ok; ++i) {
             if (!fills(i)) {                            // resident weights: nothing to widen
                 kbg += nkb;
@@ -642,6 +795,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 if (blk && o < p.it[tc.zi].n) bsr = b + (long long)o * p.kb32;
             }
             for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+                // two-tile units: the previous unit's second tile, once this
+                // unit's leading stages are widened (the first tile's MMAs
+                // take them while its second tile drains); the next stage's
+                // A slot is only released after that drain
+                if (helper2 && i > 0 && kb == (NA < nkb ? NA : nkb)) {
+                    ok = help2_drain(i - 1, hstg2, hslot);
+                    if (!ok) break;
+                }
                 const int s = kbg % NST, a = res ? kb : kbg % NA;
                 // blocks 4 kb + 2 h and the next one (issued before the waits)
                 uint32_t dd = 0;
@@ -710,8 +871,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
             ++nfill;
             if (helper && ok) ok = gated_drain(i, 2, 4, hstg, hslot);
+            if (helper2 && ok && i > 0 && nkb <= NA) ok = help2_drain(i - 1, hstg2, hslot);
         }
-        if (helper) {
+        if (helper2 && ok && ucnt > 0) ok = help2_drain(ucnt - 1, hstg2, hslot);
+        if (helper || helper2) {
             // the stores must be complete before the CTA's shared memory goes away
             bulk_wait_all();
             __syncwarp();
@@ -920,6 +1083,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         v[j] = __float_as_uint(a);
                         v[j + 1] = __float_as_uint(b2);
                     }
+                    if (act) {   // the ungated MLP with an f32 output: act(bf16(s*acc + b))
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = __float_as_uint(apply_act_tanh(round_bf16(__uint_as_float(v[j])), act - 1));
+                    }
                     const int tb = t0 + 32 * c;
                     half_out(v, 0, tb);
                     if (tb + 16 < p.m) half_out(v, 1, tb + 16);
@@ -929,8 +1097,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const int acol = (TPA == 2 ? tt : b) * BN;     // this token tile's accumulator
             const int t0 = (tc.t0 * TPA + tt) * BN;
             // the token tile's 32-token blocks (the last may be partial; a
-            // second tile past m has none)
-            const int cn = t0 >= p.m ? 0 : ((p.m - t0 + 31) / 32 < BN / 32 ? (p.m - t0 + 31) / 32 : BN / 32);
+            // second tile past m has none); of a two-tile unit's second tile
+            // only the first (converter warps 2-5 drain the rest)
+            const int cn0 = t0 >= p.m ? 0 : ((p.m - t0 + 31) / 32 < BN / 32 ? (p.m - t0 + 31) / 32 : BN / 32);
+            const int cn = L::HELP2 && tt == 1 ? e_blocks2(tc.zi, cn0) : cn0;
             // this warp's first output feature: a warp whose features all lie
             // past n (a phantom tile) has nothing to drain
             const int fo = tc.o0 + (GATED ? 16 : 32) * q;
