@@ -138,8 +138,8 @@ struct Layout {
     // one-tile units at N = 128: 4 KB a warp for four converter warps that
     // help drain the gated form while the weights are resident
     static constexpr bool HELP = TPA == 1 && BN == 128;
-    // two-tile units: converter warps 2-5 drain the later blocks of the
-    // second token tile while the epilogue warps drain the first (one 2 KB
+    // two-tile units: converter warps 2-5 drain the second token tile while
+    // the epilogue warps drain the first (one 2 KB
     // slot a warp: a bf16 block, two gated blocks, or an f32 16-token half)
     static constexpr bool HELP2 = TPA == 2;
     static constexpr int HSTG_OFF = STG_OFF + STG_BYTES;
@@ -448,13 +448,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     };
 
     // Two-tile units: the blocks of the second token tile that the epilogue
-    // warps drain themselves; converter warps 2-5 take the rest (none where a
-    // residual other than y is added from global memory).  The epilogue warps
-    // start at the accumulator's completion while the converters first widen
-    // the next unit's leading stages, so the epilogue keeps one block.
+    // warps drain themselves: none (converter warps 2-5 drain that tile while
+    // the epilogue warps drain the first, which the next unit's first MMAs
+    // need), or all where a residual other than y is added from global
+    // memory.  Keeping its first block with the epilogue warps measured the
+    // same.
     auto e_blocks2 = [&](int zi, int cn) -> int {
         const bool other_resid = p.it[zi].resid != nullptr && p.it[zi].resid != p.it[zi].y;
-        return other_resid || cn < 1 ? cn : 1;
+        return other_resid ? cn : 0;
     };
     // Two-tile units: the calling converter warp (lane quadrant warp & 3)
     // drains blocks [e_blocks2, cn) of unit lt's second token tile through
@@ -1097,8 +1098,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const int acol = (TPA == 2 ? tt : b) * BN;     // this token tile's accumulator
             const int t0 = (tc.t0 * TPA + tt) * BN;
             // the token tile's 32-token blocks (the last may be partial; a
-            // second tile past m has none); of a two-tile unit's second tile
-            // only the first (converter warps 2-5 drain the rest)
+            // second tile past m has none); a two-tile unit's second tile is
+            // drained by converter warps 2-5 (see e_blocks2)
             const int cn0 = t0 >= p.m ? 0 : ((p.m - t0 + 31) / 32 < BN / 32 ? (p.m - t0 + 31) / 32 : BN / 32);
             const int cn = L::HELP2 && tt == 1 ? e_blocks2(tc.zi, cn0) : cn0;
             // this warp's first output feature: a warp whose features all lie
