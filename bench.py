@@ -567,6 +567,17 @@ def run_ours(args):
         "wall_s_timed": round(wall, 3),
         "cpu_baseline": cpu,
     }
+    if os.environ.get("TEFWD_PROF"):
+        # the pages' per-op-class switch: one eager forward with the blocks'
+        # step-boundary events, GPU ms a class over the whole stack
+        x.copy_(x0)
+        cls = st.profile_forward(x, a, stream=stream)
+        te.check(stream)
+        line["step_classes_ms"] = {k: round(v, 4) for k, v in cls.items()}
+        if rank == 0:
+            tot = sum(cls.values()) or 1.0
+            for k, v in cls.items():
+                print(f"[TEFWD_PROF] {k:10s} {v:9.3f} ms {100 * v / tot:5.1f} %", file=sys.stderr)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

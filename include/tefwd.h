@@ -344,7 +344,23 @@ typedef struct {
      * [0, t) exactly once, and cu_seqlens then only gives t. */
     const int32_t *attn_items_host, *attn_items_dev;
     int32_t n_attn_items;
+    /* per-step GPU timing (the pages' per-op-class profiling switch: [EG2]
+     * the CMF_EGEMMA2_GPU_PROF recorder, one command buffer per op class;
+     * [VIT] VitProfiler), or NULL.  TE_BLOCK_PROF_EVENTS events that the
+     * caller created (cudaEvent_t with timing, owned by the caller); the
+     * block records event k on its stream at step boundary k:
+     *   0 before the q|k|v projection, 1 after it, 2 after the q/k norm and
+     *   RoPE (right after 1 when the block has none), 3 after attention,
+     *   4 after the O projection, 5 after the residual and FFN pre-norm,
+     *   6 after gate|up, 7 after the down projection, 8 after the closing
+     *   row ops (with the per-layer input path).
+     * The time between events k and k+1 is step class k.  Only event records
+     * are added: nothing synchronises.  Rejected (TE_EINVAL) while the stream
+     * is being captured into a graph, where records give no timing. */
+    void *const *prof_events;
 } te_block_desc;
+
+#define TE_BLOCK_PROF_EVENTS 9
 
 /* Workspace bytes te_encoder_block_fwd needs for t packed rows. */
 size_t te_encoder_block_workspace(const te_block_desc *desc, int32_t t);
@@ -410,6 +426,12 @@ const char *te_last_error(void);
 
 /* Library version string. */
 const char *te_version(void);
+
+/* Struct sizes as this library was compiled: sizes[0] = sizeof(te_q8w),
+ * [1] = sizeof(te_q8_item), [2] = sizeof(te_block_desc), for a binding to
+ * check its own mirror of them.  Writes min(n, 3) entries and returns 3;
+ * sizes may be NULL when n == 0.  Host only. */
+int32_t te_abi_sizes(size_t *sizes, int32_t n);
 
 #ifdef __cplusplus
 }

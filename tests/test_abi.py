@@ -39,6 +39,17 @@ def test_version_and_empty_error(L):
     assert "sm_103a" in te.version()
 
 
+def test_binding_structs_match_the_compiled_abi(L):
+    # the ctypes mirrors of te_q8w, te_q8_item and te_block_desc have the
+    # library's own sizes (a field added on one side only shows here)
+    assert te.abi_sizes() == (ctypes.sizeof(te.te_q8w), ctypes.sizeof(te.te_q8_item),
+                              ctypes.sizeof(te.te_block_desc))
+    assert L.te_abi_sizes(None, 0) == 3
+    src = open(os.path.join(ROOT, "include", "tefwd.h")).read()
+    assert int(re.search(r"#define TE_BLOCK_PROF_EVENTS (\d+)", src).group(1)) == te.TE_BLOCK_PROF_EVENTS
+    assert len(te.EncoderStack.STEP_CLASSES) + 1 == te.TE_BLOCK_PROF_EVENTS
+
+
 FAKE = 0x10000   # never dereferenced: every call below fails validation first
 
 

@@ -291,3 +291,61 @@ def test_forward_host_stream_overlapped_copies_give_each_input_its_own_result():
         for i in range(len(xs)):
             assert torch.equal(res[i], refs[i]), (key, i)
         assert start.elapsed_time(end) > 0
+
+
+def test_profiled_forward_times_every_step_class_and_changes_nothing():
+    # the block's step-boundary events (te_block_desc.prof_events) give each
+    # step class's GPU time; recording them leaves every output bit-identical
+    import torch
+    cfg = synth.small_config("c2", layers=2, window=40, lens=(100, 300, 37))
+    st, _, _ = _stack(cfg, cfg.lens, 2)
+    x0 = to_dev(synth.draw_x(st.T, cfg.d, 9))
+    x, a, out = st.buffers()
+    x.copy_(x0)
+    st.forward_device(x, a)
+    te.check()
+    ref_x, ref_a = x.clone(), a.clone()
+    x.copy_(x0)
+    s = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    ms = st.profile_forward(x, a, stream=s)
+    t1.record(s)
+    te.check()
+    assert torch.equal(x, ref_x) and torch.equal(a, ref_a)
+    assert set(ms) == set(st.STEP_CLASSES)
+    for name in ("gemm_qkv", "qk_prep", "attention", "gemm_o", "norm_ffn", "gemm_gu", "gemm_down"):
+        assert ms[name] > 0, (name, ms)
+    assert all(v >= 0 for v in ms.values())
+    assert sum(ms.values()) <= t0.elapsed_time(t1) * 1.01 + 0.01
+    assert all(d.prof_events is None for d in st.descs)
+
+
+def test_prof_events_are_refused_during_graph_capture():
+    import ctypes
+    import torch
+    cfg = synth.small_config("c2", layers=1, window=0, lens=(64,))
+    st, _, _ = _stack(cfg, cfg.lens, 1)
+    x, a, _ = st.buffers()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(te.TE_BLOCK_PROF_EVENTS)]
+    s = torch.cuda.Stream()
+    for e in evs:
+        e.record(s)
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * te.TE_BLOCK_PROF_EVENTS)(*[e.cuda_event for e in evs])
+    d = st.descs[0]
+    d.prof_events = ctypes.cast(arr, ctypes.c_void_p).value
+    g = torch.cuda.CUDAGraph()
+    err = None
+    try:
+        # the call is refused before it enqueues anything: the capture ends empty
+        with torch.cuda.graph(g, stream=s):
+            try:
+                te.encoder_block_fwd(d, x, a, st.cu_host, st.cu_dev, st.workspace, stream=s)
+            except te.TEError as e:
+                err = e
+    finally:
+        d.prof_events = None
+    assert err is not None and err.status == te.TE_EINVAL and "captured" in str(err)
+    torch.cuda.synchronize()
+    te.check()

@@ -22,6 +22,8 @@ TE_RESID_PLAIN, TE_RESID_SANDWICH = 0, 1
 TE_EPI_NONE, TE_EPI_GELU_TANH, TE_EPI_SILU = 0, 1, 2
 # TE_STATIC_SCRATCH_BYTES of tefwd.h: the scratch array of te_encoder_block_fwd_static
 TE_STATIC_SCRATCH_BYTES = 32 << 20
+# TE_BLOCK_PROF_EVENTS of tefwd.h: the step-boundary events of te_block_desc.prof_events
+TE_BLOCK_PROF_EVENTS = 9
 
 _STATUS = {0: "TE_OK", 1: "TE_EINVAL", 2: "TE_ESHAPE", 3: "TE_EALIGN", 4: "TE_EWORKSPACE",
            5: "TE_ECUDA", 6: "TE_EDEVICE"}
@@ -60,7 +62,8 @@ class te_block_desc(ctypes.Structure):
                 ("mod", c_p), ("next_mod_scale", c_p), ("v_norm", c_i32),
                 ("ple_dim", c_i32), ("ple_scale", c_f32), ("ple_in", te_q8w), ("ple_gate", te_q8w),
                 ("ple_proj", te_q8w), ("ple_norm_w", c_p), ("ple_post_w", c_p), ("ple_x", c_p),
-                ("attn_items_host", c_p), ("attn_items_dev", c_p), ("n_attn_items", c_i32)]
+                ("attn_items_host", c_p), ("attn_items_dev", c_p), ("n_attn_items", c_i32),
+                ("prof_events", c_p)]
 
 
 _lib = None
@@ -101,6 +104,7 @@ EXPORTS = {
     "te_check": (ctypes.c_int, [c_p]),
     "te_last_error": (ctypes.c_char_p, []),
     "te_version": (ctypes.c_char_p, []),
+    "te_abi_sizes": (c_i32, [ctypes.POINTER(ctypes.c_size_t), c_i32]),
 }
 
 
@@ -323,6 +327,13 @@ def check(stream=None):
 
 def version() -> str:
     return lib().te_version().decode()
+
+
+def abi_sizes():
+    """(sizeof te_q8w, te_q8_item, te_block_desc) as the library was compiled."""
+    out = (ctypes.c_size_t * 3)()
+    n = lib().te_abi_sizes(out, 3)
+    return tuple(int(v) for v in out[:n])
 
 
 from .model import EncoderStack, LayerWeights  # noqa: E402,F401

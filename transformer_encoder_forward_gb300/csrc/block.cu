@@ -152,6 +152,12 @@ te_status check_items_cover(const te_block_desc &d, int32_t t) {
 
 using namespace tefwd;
 
+extern "C" int32_t te_abi_sizes(size_t *sizes, int32_t n) {
+    const size_t v[3] = {sizeof(te_q8w), sizeof(te_q8_item), sizeof(te_block_desc)};
+    for (int32_t i = 0; i < n && i < 3 && sizes; ++i) sizes[i] = v[i];
+    return 3;
+}
+
 extern "C" size_t te_encoder_block_workspace(const te_block_desc *desc, int32_t t) {
     if (!desc || t < 0) return 0;
     return ws_layout(*desc, t).total;
@@ -178,6 +184,24 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
         return fail(TE_EALIGN, "block: workspace must be 256-byte aligned");
     if (!aligned16(x) || !aligned16(a)) return fail(TE_EALIGN, "block: x and a must be 16-byte aligned");
 
+    // per-step timing: every event given, and the stream not being captured
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (d.prof_events) {
+        for (int k = 0; k < TE_BLOCK_PROF_EVENTS; ++k)
+            if (!d.prof_events[k]) return fail(TE_EINVAL, "block: prof_events[%d] is NULL", k);
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        const cudaError_t ce = cudaStreamIsCapturing(cs, &cap);
+        if (ce != cudaSuccess) return cuda_fail(ce, "block: cudaStreamIsCapturing");
+        if (cap != cudaStreamCaptureStatusNone)
+            return fail(TE_EINVAL, "block: prof_events while the stream is being captured");
+    }
+    // records step boundary k when timing is on
+    auto mark = [&](int k) -> te_status {
+        if (!d.prof_events) return TE_OK;
+        const cudaError_t e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(d.prof_events[k]), cs);
+        return e == cudaSuccess ? TE_OK : cuda_fail(e, "block: cudaEventRecord");
+    };
+
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int hd = d.head_dim, H = d.n_heads, KV = d.n_kv_heads, D = d.d, F = d.ffn;
     const int qw = H * hd, kw = KV * hd, ldqkv = qw + 2 * kw;
@@ -192,7 +216,9 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
     it[0] = {d.wq, qkv, ldqkv, TE_BF16, TE_EPI_NONE, nullptr, 0};
     it[1] = {d.wk, qkv + qw, ldqkv, TE_BF16, 0, nullptr, 0};
     it[2] = {d.wv, qkv + qw + kw, ldqkv, TE_BF16, 0, nullptr, 0};
-    if ((st = te_q8_linear(a, D, t, D, it, 3, stream)) != TE_OK) return st;
+    if ((st = mark(0)) != TE_OK || (st = te_q8_linear(a, D, t, D, it, 3, stream)) != TE_OK ||
+        (st = mark(1)) != TE_OK)
+        return st;
     // 2. q/k norm + RoPE (and v norm) in place
     if (d.q_norm || d.rope_sec || d.q_mul != 1.f || d.v_norm) {
         if ((st = te_qkv_prep_rope(qkv, ldqkv, 0, qw, qw + kw, H, KV, hd, d.q_norm, d.k_norm,
@@ -200,6 +226,7 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
                                    d.rope_rows, d.rope_sec, d.q_mul, t, stream)) != TE_OK)
             return st;
     }
+    if ((st = mark(2)) != TE_OK) return st;
     // 3. attention: per sequence, or per two-range item
     if (d.n_attn_items > 0)
         st = te_attn_items_fwd(qkv, ldqkv, 0, qw, qw + kw, d.attn_items_host, d.attn_items_dev,
@@ -207,11 +234,11 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
     else
         st = te_attn_varlen_fwd(qkv, ldqkv, 0, qw, qw + kw, cu_host, cu_dev, nseq, H, KV, hd,
                                 d.window, d.attn_scale, o, qw, stream);
-    if (st != TE_OK) return st;
+    if (st != TE_OK || (st = mark(3)) != TE_OK) return st;
     // 4. O projection: plain form adds into x in the epilogue
     te_q8_item io = plain ? te_q8_item{d.wo, x, D, TE_F32, 0, x, D}
                           : te_q8_item{d.wo, tmp, D, TE_F32, 0, nullptr, 0};
-    if ((st = te_q8_linear(o, qw, t, qw, &io, 1, stream)) != TE_OK) return st;
+    if ((st = te_q8_linear(o, qw, t, qw, &io, 1, stream)) != TE_OK || (st = mark(4)) != TE_OK) return st;
     // 5. residual + FFN pre-norm
     if (plain)
         st = te_rownorm(x, TE_F32, D, d.ffn_norm_w, d.ffn_norm_b, d.norm_kind, d.eps, 1.f, a, TE_BF16,
@@ -220,7 +247,7 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
         st = te_add_norm_mod(x, tmp, d.post_attn_w, d.mod ? d.mod + D : nullptr, d.post, d.ffn_norm_w,
                              d.ffn_norm_b, d.mod ? d.mod + 2 * D : nullptr, d.norm_kind, d.eps, a,
                              TE_BF16, t, D, stream);
-    if (st != TE_OK) return st;
+    if (st != TE_OK || (st = mark(5)) != TE_OK) return st;
     // 6-7. gate|up with the gate in the epilogue, or up with the activation
     if (d.gated) {
         st = te_q8_gated_linear(a, D, t, D, &d.wg, &d.wu, d.act, m, F, stream);
@@ -229,11 +256,11 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
                          nullptr, 0};
         st = te_q8_linear(a, D, t, D, &iu, 1, stream);
     }
-    if (st != TE_OK) return st;
+    if (st != TE_OK || (st = mark(6)) != TE_OK) return st;
     // 8. down projection
     te_q8_item id = plain ? te_q8_item{d.wd, x, D, TE_F32, 0, x, D}
                           : te_q8_item{d.wd, tmp, D, TE_F32, 0, nullptr, 0};
-    if ((st = te_q8_linear(m, F, t, F, &id, 1, stream)) != TE_OK) return st;
+    if ((st = te_q8_linear(m, F, t, F, &id, 1, stream)) != TE_OK || (st = mark(7)) != TE_OK) return st;
     // 9. residual + the next block's pre-norm
     if (plain) {
         if (d.next_norm_w)
@@ -272,5 +299,5 @@ extern "C" te_status te_encoder_block_fwd(const te_block_desc *desc, float *x, v
                              d.next_norm_b, d.next_mod_scale, d.norm_kind, d.eps,
                              d.next_norm_w ? a : nullptr, TE_BF16, t, D, stream);
     }
-    return st;
+    return st != TE_OK ? st : mark(8);
 }

@@ -174,6 +174,40 @@ class EncoderStack:
             pool_mean(x, self.cu_host, self.cu_dev, self.final_norm, self.cfg.eps, out,
                       stream=stream)
 
+    # the block's step classes, between its TE_BLOCK_PROF_EVENTS boundaries
+    STEP_CLASSES = ("gemm_qkv", "qk_prep", "attention", "gemm_o", "norm_ffn", "gemm_gu", "gemm_down",
+                    "norm_next")
+
+    def profile_forward(self, x, a, stream=None):
+        """One eager forward_device with the blocks' step-boundary events
+        (te_block_desc.prof_events; the pages' per-op-class GPU timing):
+        GPU ms of each step class, summed over the layers (the input norm and
+        the pool fall outside the classes).  Synchronises the stream."""
+        import ctypes
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        n_ev = len(self.STEP_CLASSES) + 1
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in self.descs]
+        for row in evs:
+            for e in row:
+                e.record(s)          # creates the event
+        keep = []
+        try:
+            for d, row in zip(self.descs, evs):
+                arr = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in row])
+                keep.append(arr)
+                d.prof_events = ctypes.cast(arr, ctypes.c_void_p).value
+            self.forward_device(x, a, stream=s)
+            s.synchronize()
+        finally:
+            for d in self.descs:
+                d.prof_events = None
+        ms = dict.fromkeys(self.STEP_CLASSES, 0.0)
+        for row in evs:
+            for k, name in enumerate(self.STEP_CLASSES):
+                ms[name] += row[k].elapsed_time(row[k + 1])
+        return ms
+
     def forward_host_stream(self, x_hosts, result_hosts, stream=None, before=None):
         """End to end for a sequence of inputs, the copies overlapped with the
         neighbouring forwards: forward i copies x_hosts[i] (pinned) in on a
