@@ -321,6 +321,7 @@ def test_profiled_forward_times_every_step_class_and_changes_nothing():
     assert all(d.prof_events is None for d in st.descs)
 
 
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty:UserWarning")   # the refused call enqueues nothing
 def test_prof_events_are_refused_during_graph_capture():
     import ctypes
     import torch
